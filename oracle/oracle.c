@@ -1,0 +1,306 @@
+/*
+ * oracle.c - plain CPU oracle for the deterministic, batch-invariant
+ * linear-layer GEMM (forward Y = X.W + b, dX = dY.W^T, dW = X^T.dY).
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library.  It shares no code, header, table
+ * or helper with the CUDA library: it decodes its own inputs, runs its own
+ * summation and rounds its own outputs.
+ *
+ * What it computes (Carbon README, "How It Works"): every product is taken
+ * in float64, and products are accumulated with Kahan-Babushka-Neumaier
+ * (KBN) compensation in a fixed order.  The fixed order is the one stated
+ * for this library: the reduction index r runs in 256-wide chunks
+ * [0,256), [256,512), ... summed left to right with KBN, each chunk yields
+ * the single double fl(s + c), and the chunk values are combined left to
+ * right with KBN again.  The forward pass then adds the bias in float64
+ * (one rounded addition) and every pass rounds the float64 value once,
+ * to nearest-even, to the output type (fp32 or bf16).  sgemm-bi's
+ * "Determinism contracts" table describes the same final step as an RNE
+ * downcast.
+ *
+ * Layouts (weights stored [in, out], sgemm-bi "Use"): row-major X[M,K],
+ * W[K,N], b[N], Y[M,N], dY[M,N], dX[M,K], dW[K,N].
+ *   fwd : Y[i,j]  = sum_r X[i,r]  * W[r,j]   (R = K)
+ *   dX  : dX[i,j] = sum_r dY[i,r] * W[j,r]   (R = N)
+ *   dW  : dW[i,j] = sum_r X[r,i]  * dY[r,j]  (R = M)
+ *
+ * Build: -O2 -ffp-contract=off -fno-fast-math.  With contraction off every
+ * `a * b` and `a + b` below is one IEEE-754 binary64 operation rounded to
+ * nearest-even; products of two fp32 (or two bf16) values are exact in
+ * binary64, so the only roundings are the additions the algorithm names.
+ */
+#include <float.h>
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#if !defined(FLT_EVAL_METHOD) || FLT_EVAL_METHOD != 0
+#error "the oracle needs FLT_EVAL_METHOD == 0 (no excess precision)"
+#endif
+
+#define ORACLE_CHUNK 256
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_FWD = 0, ORACLE_DX = 1, ORACLE_DW = 2 };
+
+/* ---- input decoding (exact widening to binary64) ------------------------ */
+
+static double decode(const void *base, int dtype, int64_t idx)
+{
+    float f;
+    if (dtype == ORACLE_F32) {
+        memcpy(&f, (const char *)base + 4 * idx, 4);
+    } else {
+        uint16_t h;
+        uint32_t u;
+        memcpy(&h, (const char *)base + 2 * idx, 2);
+        u = (uint32_t)h << 16;          /* bf16 is the top half of an fp32 */
+        memcpy(&f, &u, 4);
+    }
+    return (double)f;                   /* exact: binary32 is a subset of binary64 */
+}
+
+/* ---- output rounding ----------------------------------------------------- */
+
+/* binary64 -> binary32, nearest-even: C's conversion in the default mode. */
+static uint32_t round_to_f32_bits(double y)
+{
+    float f = (float)y;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return u;
+}
+
+/* binary64 -> bf16, nearest-even, in ONE rounding (never through fp32).
+ * bf16 has 8 significant bits and the exponent range of fp32: normal
+ * exponents -126..127, subnormal quantum 2^-133, largest finite
+ * (2 - 2^-7) * 2^127.  The value is divided by its quantum (a power of two,
+ * so exactly), rounded to an integer with ties to even, and scaled back. */
+static uint16_t round_to_bf16_bits(double y)
+{
+    double a, quantum, n, r;
+    int e, E;
+    uint16_t sign = signbit(y) ? 0x8000u : 0u;
+    float f;
+    uint32_t u;
+
+    if (isnan(y))
+        return 0x7FC0u | sign;
+    a = fabs(y);
+    if (a >= 0x1p128)                   /* already beyond every finite bf16 */
+        return 0x7F80u | sign;
+    if (a == 0.0)
+        return sign;
+    (void)frexp(a, &e);                 /* a = m * 2^e, m in [0.5, 1) */
+    E = e - 1;                          /* floor(log2(a)) */
+    if (E < -126)
+        E = -126;                       /* subnormal range: fixed quantum */
+    quantum = ldexp(1.0, E - 7);
+    n = nearbyint(a / quantum);         /* default mode: ties to even */
+    r = n * quantum;
+    if (r >= 0x1p128)                   /* rounded past the largest finite value */
+        return 0x7F80u | sign;
+    f = (float)r;                       /* exact: r has <= 8 significant bits */
+    memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16) | sign;
+}
+
+/* ---- the summation ------------------------------------------------------- */
+
+/* One step of Neumaier's improved Kahan-Babuska summation, as on the page
+ * the Carbon README links: add x to (sum, comp). */
+static void kbn_step(double *sum, double *comp, double x)
+{
+    double t = *sum + x;
+    if (fabs(*sum) >= fabs(x))
+        *comp += (*sum - t) + x;
+    else
+        *comp += (x - t) + *sum;
+    *sum = t;
+}
+
+/* Fixed-order dot product of a[a0 + r*as] and b[b0 + r*bs], r = 0..R-1.
+ * Returns the float64 value before the bias and the output rounding. */
+static double fixed_order_dot(const void *A, int64_t a0, int64_t as,
+                              const void *B, int64_t b0, int64_t bs,
+                              int64_t R, int dtype)
+{
+    double S = 0.0, C = 0.0;            /* outer KBN over chunk values */
+    int64_t q0;
+    for (q0 = 0; q0 < R; q0 += ORACLE_CHUNK) {
+        int64_t q1 = (R - q0 > ORACLE_CHUNK) ? q0 + ORACLE_CHUNK : R;
+        double s = 0.0, c = 0.0;        /* KBN inside the chunk */
+        int64_t r;
+        for (r = q0; r < q1; ++r) {
+            double p = decode(A, dtype, a0 + r * as) * decode(B, dtype, b0 + r * bs);
+            kbn_step(&s, &c, p);
+        }
+        kbn_step(&S, &C, s + c);        /* chunk value fl(s + c) */
+    }
+    return S + C;
+}
+
+/* ---- one output element --------------------------------------------------- */
+
+typedef struct {
+    int pass, dtype;
+    const void *A, *B, *bias;
+    int64_t M, K, N;
+    void *out;          /* output-typed array, or NULL */
+    double *y64;        /* float64 value before output rounding, or NULL */
+    /* either a dense range [first, last) of row-major output positions ... */
+    int64_t first, last;
+    /* ... or explicit coordinates (when rows != NULL) */
+    const int64_t *rows, *cols;
+    int64_t ncols_out;  /* row length of the output matrix */
+} job_t;
+
+static void one_output(const job_t *jb, int64_t i, int64_t j, int64_t slot)
+{
+    double y;
+    switch (jb->pass) {
+    case ORACLE_FWD:    /* X[i, r] * W[r, j] */
+        y = fixed_order_dot(jb->A, i * jb->K, 1, jb->B, j, jb->N, jb->K, jb->dtype);
+        if (jb->bias)
+            y = y + decode(jb->bias, jb->dtype, j);
+        break;
+    case ORACLE_DX:     /* dY[i, r] * W[j, r] */
+        y = fixed_order_dot(jb->A, i * jb->N, 1, jb->B, j * jb->N, 1, jb->N, jb->dtype);
+        break;
+    default:            /* X[r, i] * dY[r, j] */
+        y = fixed_order_dot(jb->A, i, jb->K, jb->B, j, jb->N, jb->M, jb->dtype);
+        break;
+    }
+    if (jb->y64)
+        jb->y64[slot] = y;
+    if (jb->out) {
+        if (jb->dtype == ORACLE_F32) {
+            uint32_t u = round_to_f32_bits(y);
+            memcpy((char *)jb->out + 4 * slot, &u, 4);
+        } else {
+            uint16_t h = round_to_bf16_bits(y);
+            memcpy((char *)jb->out + 2 * slot, &h, 2);
+        }
+    }
+}
+
+static void *run_job(void *arg)
+{
+    const job_t *jb = (const job_t *)arg;
+    int64_t k;
+    for (k = jb->first; k < jb->last; ++k) {
+        if (jb->rows)
+            one_output(jb, jb->rows[k], jb->cols[k], k);
+        else
+            one_output(jb, k / jb->ncols_out, k % jb->ncols_out, k);
+    }
+    return NULL;
+}
+
+static int launch(job_t proto, int64_t count, int nthreads)
+{
+    pthread_t *tid;
+    job_t *jobs;
+    int t, started = 0;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (count < (int64_t)nthreads)
+        nthreads = count > 0 ? (int)count : 1;
+    tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
+    if (!tid || !jobs) {
+        free(tid);
+        free(jobs);
+        return -2;
+    }
+    for (t = 0; t < nthreads; ++t) {
+        jobs[t] = proto;
+        jobs[t].first = count * t / nthreads;
+        jobs[t].last = count * (t + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        run_job(&jobs[0]);
+    } else {
+        for (t = 0; t < nthreads; ++t) {
+            if (pthread_create(&tid[t], NULL, run_job, &jobs[t]) != 0)
+                break;
+            ++started;
+        }
+        for (t = started; t < nthreads; ++t)   /* could not start: run here */
+            run_job(&jobs[t]);
+        for (t = 0; t < started; ++t)
+            pthread_join(tid[t], NULL);
+    }
+    free(tid);
+    free(jobs);
+    return 0;
+}
+
+static int check(int pass, int dtype, int64_t M, int64_t K, int64_t N)
+{
+    if (pass < ORACLE_FWD || pass > ORACLE_DW)
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+        return -1;
+    if (M < 0 || K < 0 || N < 0)
+        return -1;
+    return 0;
+}
+
+/* ---- exported API ------------------------------------------------------- */
+
+/* Dense pass.  A/B are (X, W) for fwd, (dY, W) for dX, (X, dY) for dW;
+ * bias is used by fwd only (may be NULL).  out (output dtype) and y64
+ * (float64) may each be NULL.  Output shape: fwd [M,N], dX [M,K], dW [K,N]. */
+int oracle_gemm(int pass, int dtype, const void *A, const void *B, const void *bias,
+                int64_t M, int64_t K, int64_t N, void *out, double *y64, int nthreads)
+{
+    job_t jb;
+    int64_t rows, cols;
+    if (check(pass, dtype, M, K, N))
+        return -1;
+    memset(&jb, 0, sizeof jb);
+    jb.pass = pass; jb.dtype = dtype; jb.A = A; jb.B = B;
+    jb.bias = (pass == ORACLE_FWD) ? bias : NULL;
+    jb.M = M; jb.K = K; jb.N = N; jb.out = out; jb.y64 = y64;
+    rows = (pass == ORACLE_DW) ? K : M;
+    cols = (pass == ORACLE_DX) ? K : N;
+    jb.ncols_out = cols;
+    return launch(jb, rows * cols, nthreads);
+}
+
+/* Selected outputs only: out[k], y64[k] for output (rows[k], cols[k]). */
+int oracle_gemm_at(int pass, int dtype, const void *A, const void *B, const void *bias,
+                   int64_t M, int64_t K, int64_t N, const int64_t *rows, const int64_t *cols,
+                   int64_t count, void *out, double *y64, int nthreads)
+{
+    job_t jb;
+    if (check(pass, dtype, M, K, N) || count < 0 || (count > 0 && (!rows || !cols)))
+        return -1;
+    memset(&jb, 0, sizeof jb);
+    jb.pass = pass; jb.dtype = dtype; jb.A = A; jb.B = B;
+    jb.bias = (pass == ORACLE_FWD) ? bias : NULL;
+    jb.M = M; jb.K = K; jb.N = N; jb.out = out; jb.y64 = y64;
+    jb.rows = rows; jb.cols = cols;
+    return launch(jb, count, nthreads);
+}
+
+/* The output rounding on its own, for checking it against exact rounding. */
+void oracle_round(int dtype, const double *y, void *out, int64_t n)
+{
+    int64_t k;
+    for (k = 0; k < n; ++k) {
+        if (dtype == ORACLE_F32) {
+            uint32_t u = round_to_f32_bits(y[k]);
+            memcpy((char *)out + 4 * k, &u, 4);
+        } else {
+            uint16_t h = round_to_bf16_bits(y[k]);
+            memcpy((char *)out + 2 * k, &h, 2);
+        }
+    }
+}
+
+int oracle_chunk_width(void) { return ORACLE_CHUNK; }
