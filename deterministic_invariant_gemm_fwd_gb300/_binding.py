@@ -1,0 +1,174 @@
+"""Thin ctypes binding of the carbon_gemm C ABI (include/carbon_gemm.h).
+
+Argument marshalling only: every step of the GEMMs runs in the library's
+CUDA kernels.  Functions take torch tensors (or raw integer device pointers)
+and the same arguments as the C entry points, and raise ``CarbonError`` on a
+status other than CARBON_OK.  There is no fallback: if the compiled library
+is missing, importing the binding raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libcarbon_gemm.so")
+HEADERS = [os.path.join(os.path.dirname(HERE), "include", h)
+           for h in ("carbon_gemm.h", "carbon_gemm_debug.h")]
+
+F32, BF16 = 0, 1
+TIER_EXACT, TIER_TC = 0, 1
+PASS_FWD, PASS_DX, PASS_DW = 0, 1, 2
+STATUS = {0: "CARBON_OK", 1: "CARBON_ERR_INVALID_ARG", 2: "CARBON_ERR_UNSUPPORTED",
+          3: "CARBON_ERR_MISALIGNED", 4: "CARBON_ERR_CUDA", 5: "CARBON_ERR_TIMEOUT"}
+DTYPES = {"f32": F32, "bf16": BF16}
+TIERS = {"exact": TIER_EXACT, "tc": TIER_TC}
+PASSES = {"fwd": PASS_FWD, "dx": PASS_DX, "dw": PASS_DW}
+
+
+class CarbonError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"carbon_gemm CUDA library not built ({LIB_PATH} missing); run "
+            "`python -m deterministic_invariant_gemm_fwd_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, dp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    sig = {
+        "carbon_gemm_fwd": [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp],
+        "carbon_gemm_dx": [vp, vp, vp, i64, i64, i64, i32, i32, vp],
+        "carbon_gemm_dw": [vp, vp, vp, i64, i64, i64, i32, i32, vp],
+        "carbon_get_device_status": [vp],
+        "carbon_debug_exact_y64": [i32, vp, vp, vp, vp, i64, i64, i64, i32, vp],
+        "carbon_debug_tc_f32": [i32, vp, vp, vp, vp, i64, i64, i64, vp],
+        "carbon_debug_round": [i32, vp, vp, i64, vp],
+        "carbon_debug_timeout_probe": [i64, vp],
+        "carbon_measure_fp64_rate": [ctypes.POINTER(dp), ctypes.POINTER(dp), vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.carbon_status_string.argtypes = [i32]
+    lib.carbon_status_string.restype = ctypes.c_char_p
+    lib.carbon_last_cuda_error.argtypes = []
+    lib.carbon_last_cuda_error.restype = ctypes.c_char_p
+    lib.carbon_abi_version.argtypes = []
+    lib.carbon_abi_version.restype = ctypes.c_int
+    lib.carbon_debug_launch_count.argtypes = []
+    lib.carbon_debug_launch_count.restype = ctypes.c_int64
+    return lib
+
+
+lib = _load()
+
+
+def declared_functions() -> list:
+    """Names of every function declared in include/*.h."""
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(carbon_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        detail = lib.carbon_last_cuda_error().decode() if status == 4 else ""
+        raise CarbonError(status, where, detail)
+
+
+def _code(table, v):
+    return table[v] if isinstance(v, str) else int(v)
+
+
+def carbon_gemm_fwd(Y, X, W, bias, M, K, N, dtype, tier, stream=None) -> None:
+    _check(lib.carbon_gemm_fwd(_ptr(Y), _ptr(X), _ptr(W), _ptr(bias), M, K, N,
+                               _code(DTYPES, dtype), _code(TIERS, tier), _stream(stream)),
+           "carbon_gemm_fwd")
+
+
+def carbon_gemm_dx(dX, dY, W, M, K, N, dtype, tier, stream=None) -> None:
+    _check(lib.carbon_gemm_dx(_ptr(dX), _ptr(dY), _ptr(W), M, K, N,
+                              _code(DTYPES, dtype), _code(TIERS, tier), _stream(stream)),
+           "carbon_gemm_dx")
+
+
+def carbon_gemm_dw(dW, X, dY, M, K, N, dtype, tier, stream=None) -> None:
+    _check(lib.carbon_gemm_dw(_ptr(dW), _ptr(X), _ptr(dY), M, K, N,
+                              _code(DTYPES, dtype), _code(TIERS, tier), _stream(stream)),
+           "carbon_gemm_dw")
+
+
+def carbon_get_device_status(stream=None) -> int:
+    """Synchronises the stream; returns the status code (does not raise)."""
+    return int(lib.carbon_get_device_status(_stream(stream)))
+
+
+def carbon_debug_exact_y64(pass_, y64, A, B, bias, M, K, N, dtype, stream=None) -> None:
+    _check(lib.carbon_debug_exact_y64(_code(PASSES, pass_), _ptr(y64), _ptr(A), _ptr(B),
+                                      _ptr(bias), M, K, N, _code(DTYPES, dtype),
+                                      _stream(stream)), "carbon_debug_exact_y64")
+
+
+def carbon_debug_tc_f32(pass_, acc, A, B, bias, M, K, N, stream=None) -> None:
+    _check(lib.carbon_debug_tc_f32(_code(PASSES, pass_), _ptr(acc), _ptr(A), _ptr(B),
+                                   _ptr(bias), M, K, N, _stream(stream)),
+           "carbon_debug_tc_f32")
+
+
+def carbon_debug_round(dtype, out, inp, n, stream=None) -> None:
+    _check(lib.carbon_debug_round(_code(DTYPES, dtype), _ptr(out), _ptr(inp), n,
+                                  _stream(stream)), "carbon_debug_round")
+
+
+def carbon_debug_timeout_probe(budget_ns: int, stream=None) -> None:
+    _check(lib.carbon_debug_timeout_probe(budget_ns, _stream(stream)),
+           "carbon_debug_timeout_probe")
+
+
+def carbon_measure_fp64_rate(stream=None) -> tuple:
+    """(DFMA lane-ops/s, DADD lane-ops/s) measured on the current device."""
+    a, b = ctypes.c_double(), ctypes.c_double()
+    _check(lib.carbon_measure_fp64_rate(ctypes.byref(a), ctypes.byref(b), _stream(stream)),
+           "carbon_measure_fp64_rate")
+    return a.value, b.value
+
+
+def carbon_status_string(status: int) -> str:
+    return lib.carbon_status_string(status).decode()
+
+
+def carbon_abi_version() -> int:
+    return int(lib.carbon_abi_version())
+
+
+def carbon_debug_launch_count() -> int:
+    return int(lib.carbon_debug_launch_count())

@@ -1,0 +1,64 @@
+// carbon_internal.h - declarations shared by the translation units of the
+// carbon_gemm library (never by its tests' CPU reference).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/carbon_gemm.h"
+#include "../../include/carbon_gemm_debug.h"
+
+namespace carbon {
+
+// Passes of a linear layer, expressed as one generic product
+//   out[i, j] = sum_r A(i, r) * B(r, j),  r = 0 .. R-1
+// with A(i, r) = A[i * a_si + r * a_sr] and B(r, j) = B[r * b_sr + j * b_sj].
+//   fwd: A = X  [M,K] (a_si = K, a_sr = 1), B = W  [K,N] (b_sr = N, b_sj = 1), R = K
+//   dX : A = dY [M,N] (a_si = N, a_sr = 1), B = W  [K,N] (b_sr = 1, b_sj = N), R = N
+//   dW : A = X  [M,K] (a_si = 1, a_sr = K), B = dY [M,N] (b_sr = N, b_sj = 1), R = M
+struct Problem {
+    int pass;                 // CARBON_PASS_*
+    int dtype;                // CARBON_F32 / CARBON_BF16
+    const void *A, *B, *bias; // bias: fwd only, may be null
+    void *out;
+    int64_t M, K, N;          // layer sizes
+    int64_t rows, cols, R;    // output shape and reduction length
+};
+
+inline Problem make_problem(int pass, int dtype, void *out, const void *A, const void *B,
+                            const void *bias, int64_t M, int64_t K, int64_t N) {
+    Problem p;
+    p.pass = pass; p.dtype = dtype; p.A = A; p.B = B;
+    p.bias = (pass == CARBON_PASS_FWD) ? bias : nullptr;
+    p.out = out; p.M = M; p.K = K; p.N = N;
+    p.rows = (pass == CARBON_PASS_DW) ? K : M;
+    p.cols = (pass == CARBON_PASS_DX) ? K : N;
+    p.R = (pass == CARBON_PASS_FWD) ? K : (pass == CARBON_PASS_DX ? N : M);
+    return p;
+}
+
+// Records a CUDA error message for carbon_last_cuda_error(); returns
+// CARBON_ERR_CUDA when err != cudaSuccess, CARBON_OK otherwise.
+carbon_status_t note_cuda(cudaError_t err);
+
+// Counts kernel launches enqueued by the library.
+void count_launch(int n = 1);
+
+// Checks that the current device is a GB300 (compute capability 10.3) and
+// returns its SM count.
+carbon_status_t current_device(int *device, int *sm_count);
+
+// Exact tier (exact_kbn.cu).  out_f64 selects the float64 pre-rounding output.
+carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream);
+carbon_status_t exact_round_launch(int dtype, void *out, const double *in, int64_t n,
+                                   cudaStream_t stream);
+
+// Tensor-core tier (tc_gemm.cu).  out_f32 selects the fp32 pre-rounding output.
+carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream);
+// Reads and clears the tensor-core tier's device status word.
+carbon_status_t tc_take_device_status();
+
+// Measurement helpers (measure.cu).
+carbon_status_t measure_take_device_status();
+
+}  // namespace carbon

@@ -1,0 +1,311 @@
+// exact_kbn.cu - exact tier: float64 products, fixed-order Kahan-Babushka-
+// Neumaier summation, one round-to-nearest-even to the output type.
+//
+// What is computed (Carbon README, "How It Works"; sgemm-bi "Determinism
+// contracts" for the downcast): for every output, the products a_r * b_r are
+// formed in float64 (exact for fp32 and bf16 operands), summed with KBN in
+// 256-wide chunks of the reduction index taken left to right, each chunk
+// contributing fl(s + c), the chunk values combined left to right with KBN,
+// the bias added once in float64 (forward pass), and the float64 value
+// rounded once to fp32 or bf16.
+//
+// How it is computed on GB300.  GB300 issues float64 instructions at two
+// lanes per SM per clock (1/64 of its fp32 rate); everything here is shaped
+// to spend that pipe only on the additions the method names:
+//  * Operands are widened to float64 with integer bit operations while they
+//    are staged into shared memory (a hardware fp32->fp64 conversion would
+//    run on the float64 pipe).
+//  * One KBN step costs four float64 instructions instead of five:
+//      t = fma(x, w, s)           == fl(s + p), since p = x*w is exact
+//      d = fma(a1, a2, -t)        error, first half
+//      e = fma(b1, b2, d)         error, second half
+//      c = c + e
+//    KBN's correction (a - t) + b with a the operand of larger magnitude
+//    is Fast2Sum, whose result is the exact rounding error of s + p whenever
+//    the exponent of a is at least that of b.  Which operand plays a is
+//    chosen from exponent fields on the integer pipe: s is taken as a when
+//    E(s) > E(x) + E(w) (then E(s) >= E(p)); otherwise p is (then
+//    E(p) >= E(x) + E(w) >= E(s)).  Both choices give the exact error, which
+//    is the value the literal |s| >= |p| test produces, so the bits equal the
+//    plain algorithm's.  The choice is applied with predicated selects
+//    (a1, a2) = (s, 1) or (x, w), never with a branch, so a warp whose lanes
+//    disagree issues the four float64 instructions once.
+//  * Every output is owned by one thread (output-stationary), so the
+//    summation order is the documented one by construction, for every M.
+// Zero padding of ragged tiles is exact: adding a +0 product leaves s and c
+// unchanged (s is never -0: it starts at +0 and fl(a + b) is -0 only when
+// both are -0).
+#include "carbon_internal.h"
+
+#include <cuda_bf16.h>
+
+namespace carbon {
+namespace {
+
+constexpr int kChunk = 256;              // documented chunk width
+constexpr int kBK = 32;                  // reduction slice staged per step (divides kChunk)
+constexpr int kTX = 16, kTY = 16;        // thread grid of a CTA
+constexpr int kTM = 2, kTN = 2;          // outputs per thread (rows x cols)
+constexpr int kBM = kTY * kTM;           // CTA output tile rows
+constexpr int kBN = kTX * kTN;           // CTA output tile cols
+constexpr int kThreads = kTX * kTY;
+static_assert(kChunk % kBK == 0, "a staged slice must not straddle chunks");
+
+struct KArgs {
+    const void *A, *B, *bias;
+    void *out;
+    int64_t rows, cols, R;
+    int64_t a_si, a_sr, b_sr, b_sj;
+    int64_t tiles_n;
+};
+
+// Exact widening of an fp32 bit pattern to float64.  Normal numbers are
+// re-biased with integer operations; zeros keep their sign; subnormals,
+// infinities and NaNs (rare) take the hardware conversion, which is exact.
+__device__ __forceinline__ double widen(uint32_t f) {
+    const uint32_t mag = f & 0x7fffffffu;
+    if (mag - 0x00800000u < 0x7f000000u) {            // exponent field 1..254
+        const uint32_t hi = (f & 0x80000000u) | ((mag >> 3) + (896u << 20));
+        return __hiloint2double((int)hi, (int)(f << 29));
+    }
+    if (mag == 0u) return __hiloint2double((int)(f & 0x80000000u), 0);
+    return (double)__uint_as_float(f);
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t load_bits(const void *base, int64_t idx) {
+    if (DT == CARBON_F32) return __ldg(static_cast<const unsigned int *>(base) + idx);
+    return (uint32_t)__ldg(static_cast<const unsigned short *>(base) + idx) << 16;
+}
+
+// One KBN step with an exact product p = x * w.  key = (x_hi & EXP) +
+// (w_hi & EXP): the sum of the operands' shifted exponent fields.
+__device__ __forceinline__ void kbn_product_step(double &s, double &c, double x, double w,
+                                                 uint32_t key) {
+    const double t = __fma_rn(x, w, s);
+    // E(s) > E(x) + E(w)  <=>  es_field + 1022 >= ex_field + ew_field
+    const uint32_t es = ((uint32_t)__double2hiint(s) & 0x7ff00000u) + (1022u << 20);
+    double a1, a2, b1, b2;
+    asm("{\n\t.reg .pred sbig;\n\t"
+        "setp.ge.u32 sbig, %4, %5;\n\t"
+        "selp.f64 %0, %6, %7, sbig;\n\t"
+        "selp.f64 %1, %8, %9, sbig;\n\t"
+        "selp.f64 %2, %7, %6, sbig;\n\t"
+        "selp.f64 %3, %9, %8, sbig;\n\t}"
+        : "=d"(a1), "=d"(a2), "=d"(b1), "=d"(b2)
+        : "r"(es), "r"(key), "d"(s), "d"(x), "d"(1.0), "d"(w));
+    const double d = __fma_rn(a1, a2, -t);   // s - t   or   p - t   (exact)
+    const double e = __fma_rn(b1, b2, d);    // + p     or   + s     (exact)
+    c = __dadd_rn(c, e);
+    s = t;
+}
+
+// One KBN step of the outer sum over chunk values (no product).  The
+// magnitude test is exact: for non-NaN doubles the order of |a| equals the
+// unsigned order of their bit patterns with the sign cleared.
+__device__ __forceinline__ void kbn_value_step(double &S, double &C, double P) {
+    const double t = __dadd_rn(S, P);
+    const unsigned long long aS = (unsigned long long)__double_as_longlong(S) & 0x7fffffffffffffffull;
+    const unsigned long long aP = (unsigned long long)__double_as_longlong(P) & 0x7fffffffffffffffull;
+    const bool sbig = aS >= aP;
+    const double u = sbig ? S : P;
+    const double v = sbig ? P : S;
+    C = __dadd_rn(C, __dadd_rn(__dadd_rn(u, -t), v));
+    S = t;
+}
+
+// float64 -> bf16, round to nearest even, one rounding.
+__device__ __forceinline__ unsigned short round_bf16(double y) {
+    const unsigned long long u = (unsigned long long)__double_as_longlong(y);
+    const unsigned int sign = (unsigned int)(u >> 48) & 0x8000u;
+    const unsigned long long mag = u & 0x7fffffffffffffffull;
+    if (mag > 0x7ff0000000000000ull) return (unsigned short)(sign | 0x7fc0u);  // NaN
+    const int E = (int)(mag >> 52) - 1023;
+    if (E >= 128) return (unsigned short)(sign | 0x7f80u);                    // |y| >= 2^128
+    if (E >= -126) {                                                          // bf16 normal range
+        const unsigned long long lsb = (mag >> 45) & 1ull;
+        const unsigned long long r = (mag + 0x00001fffffffffffull + lsb) >> 45;
+        const int Ed = (int)(r >> 7);                                         // biased, after carry
+        if (Ed - 1023 >= 128) return (unsigned short)(sign | 0x7f80u);
+        return (unsigned short)(sign | ((unsigned int)(Ed - 1023 + 127) << 7) | (unsigned int)(r & 0x7f));
+    }
+    if (E < -134) return (unsigned short)sign;                                // below half the quantum
+    // bf16 subnormal range: n = RNE(|y| / 2^-133), 0 <= n <= 128 (128 = min normal)
+    const unsigned long long sig = (mag & 0x000fffffffffffffull) | 0x0010000000000000ull;
+    const int shift = -81 - E;                                                // 46 .. 53
+    const unsigned long long n = sig >> shift;
+    const unsigned long long rem = sig & ((1ull << shift) - 1ull);
+    const unsigned long long half = 1ull << (shift - 1);
+    const unsigned long long nr = n + ((rem > half || (rem == half && (n & 1ull))) ? 1ull : 0ull);
+    return (unsigned short)(sign | (unsigned int)nr);
+}
+
+template <int DT, int PASS>
+__device__ __forceinline__ void stage_slice(const KArgs &p, double (*As)[kBM + 1],
+                                            double (*Bs)[kBN + 1], int64_t i0, int64_t j0,
+                                            int64_t r0, int64_t rend, int tid) {
+#pragma unroll
+    for (int l = 0; l < (kBK * kBM) / kThreads; ++l) {
+        const int e = tid + kThreads * l;
+        int ii, rr;
+        if (PASS == CARBON_PASS_DW) { ii = e % kBM; rr = e / kBM; }   // i contiguous in memory
+        else                        { rr = e % kBK; ii = e / kBK; }   // r contiguous in memory
+        const int64_t i = i0 + ii, r = r0 + rr;
+        double v = 0.0;
+        if (i < p.rows && r < rend) v = widen(load_bits<DT>(p.A, i * p.a_si + r * p.a_sr));
+        As[rr][ii] = v;
+    }
+#pragma unroll
+    for (int l = 0; l < (kBK * kBN) / kThreads; ++l) {
+        const int e = tid + kThreads * l;
+        int jj, rr;
+        if (PASS == CARBON_PASS_DX) { rr = e % kBK; jj = e / kBK; }   // r contiguous in memory
+        else                        { jj = e % kBN; rr = e / kBN; }   // j contiguous in memory
+        const int64_t j = j0 + jj, r = r0 + rr;
+        double v = 0.0;
+        if (j < p.cols && r < rend) v = widen(load_bits<DT>(p.B, r * p.b_sr + j * p.b_sj));
+        Bs[rr][jj] = v;
+    }
+}
+
+template <int DT, int PASS, bool OUT_F64>
+__global__ void __launch_bounds__(kThreads)
+exact_kbn_kernel(const KArgs p) {
+    __shared__ double As[kBK][kBM + 1];
+    __shared__ double Bs[kBK][kBN + 1];
+    const int tid = threadIdx.x;
+    const int tx = tid % kTX, ty = tid / kTX;
+    const int64_t tile = blockIdx.x;
+    const int64_t i0 = (tile / p.tiles_n) * kBM;
+    const int64_t j0 = (tile % p.tiles_n) * kBN;
+
+    double S[kTM][kTN], C[kTM][kTN];
+#pragma unroll
+    for (int m = 0; m < kTM; ++m)
+#pragma unroll
+        for (int n = 0; n < kTN; ++n) { S[m][n] = 0.0; C[m][n] = 0.0; }
+
+    for (int64_t q0 = 0; q0 < p.R; q0 += kChunk) {
+        const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
+        double s[kTM][kTN], c[kTM][kTN];
+#pragma unroll
+        for (int m = 0; m < kTM; ++m)
+#pragma unroll
+            for (int n = 0; n < kTN; ++n) { s[m][n] = 0.0; c[m][n] = 0.0; }
+
+        for (int64_t r0 = q0; r0 < qend; r0 += kBK) {
+            __syncthreads();
+            stage_slice<DT, PASS>(p, As, Bs, i0, j0, r0, qend, tid);
+            __syncthreads();
+#pragma unroll 4
+            for (int k = 0; k < kBK; ++k) {
+                double a[kTM], b[kTN];
+                uint32_t ak[kTM], bk[kTN];
+#pragma unroll
+                for (int m = 0; m < kTM; ++m) {
+                    a[m] = As[k][ty + kTY * m];
+                    ak[m] = (uint32_t)__double2hiint(a[m]) & 0x7ff00000u;
+                }
+#pragma unroll
+                for (int n = 0; n < kTN; ++n) {
+                    b[n] = Bs[k][tx + kTX * n];
+                    bk[n] = (uint32_t)__double2hiint(b[n]) & 0x7ff00000u;
+                }
+#pragma unroll
+                for (int m = 0; m < kTM; ++m)
+#pragma unroll
+                    for (int n = 0; n < kTN; ++n)
+                        kbn_product_step(s[m][n], c[m][n], a[m], b[n], ak[m] + bk[n]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kTM; ++m)
+#pragma unroll
+            for (int n = 0; n < kTN; ++n)
+                kbn_value_step(S[m][n], C[m][n], __dadd_rn(s[m][n], c[m][n]));
+    }
+
+#pragma unroll
+    for (int m = 0; m < kTM; ++m) {
+        const int64_t i = i0 + ty + kTY * m;
+        if (i >= p.rows) continue;
+#pragma unroll
+        for (int n = 0; n < kTN; ++n) {
+            const int64_t j = j0 + tx + kTX * n;
+            if (j >= p.cols) continue;
+            double y = __dadd_rn(S[m][n], C[m][n]);
+            if (p.bias) y = __dadd_rn(y, widen(load_bits<DT>(p.bias, j)));
+            const int64_t o = i * p.cols + j;
+            if (OUT_F64)
+                static_cast<double *>(p.out)[o] = y;
+            else if (DT == CARBON_F32)
+                static_cast<float *>(p.out)[o] = __double2float_rn(y);
+            else
+                static_cast<unsigned short *>(p.out)[o] = round_bf16(y);
+        }
+    }
+}
+
+__global__ void round_kernel(int dtype, void *out, const double *in, int64_t n) {
+    for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < n;
+         k += (int64_t)gridDim.x * blockDim.x) {
+        const double y = in[k];
+        if (dtype == CARBON_F32) static_cast<float *>(out)[k] = __double2float_rn(y);
+        else static_cast<unsigned short *>(out)[k] = round_bf16(y);
+    }
+}
+
+template <int DT, int PASS, bool OUT_F64>
+cudaError_t launch_one(const KArgs &a, int64_t tiles, cudaStream_t stream) {
+    exact_kbn_kernel<DT, PASS, OUT_F64><<<(unsigned)tiles, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int DT, int PASS>
+cudaError_t launch_pass(const KArgs &a, int64_t tiles, bool out_f64, cudaStream_t stream) {
+    return out_f64 ? launch_one<DT, PASS, true>(a, tiles, stream)
+                   : launch_one<DT, PASS, false>(a, tiles, stream);
+}
+
+template <int DT>
+cudaError_t launch_dtype(int pass, const KArgs &a, int64_t tiles, bool out_f64, cudaStream_t s) {
+    switch (pass) {
+    case CARBON_PASS_FWD: return launch_pass<DT, CARBON_PASS_FWD>(a, tiles, out_f64, s);
+    case CARBON_PASS_DX:  return launch_pass<DT, CARBON_PASS_DX>(a, tiles, out_f64, s);
+    default:              return launch_pass<DT, CARBON_PASS_DW>(a, tiles, out_f64, s);
+    }
+}
+
+}  // namespace
+
+carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream) {
+    if (p.rows == 0 || p.cols == 0) return CARBON_OK;
+    KArgs a;
+    a.A = p.A; a.B = p.B; a.bias = p.bias; a.out = p.out;
+    a.rows = p.rows; a.cols = p.cols; a.R = p.R;
+    switch (p.pass) {
+    case CARBON_PASS_FWD: a.a_si = p.K; a.a_sr = 1; a.b_sr = p.N; a.b_sj = 1; break;
+    case CARBON_PASS_DX:  a.a_si = p.N; a.a_sr = 1; a.b_sr = 1;   a.b_sj = p.N; break;
+    default:              a.a_si = 1;   a.a_sr = p.K; a.b_sr = p.N; a.b_sj = 1; break;
+    }
+    const int64_t tiles_m = (p.rows + kBM - 1) / kBM;
+    a.tiles_n = (p.cols + kBN - 1) / kBN;
+    const int64_t tiles = tiles_m * a.tiles_n;
+    if (tiles > 0x7fffffff) return CARBON_ERR_INVALID_ARG;
+    const cudaError_t err = (p.dtype == CARBON_F32)
+        ? launch_dtype<CARBON_F32>(p.pass, a, tiles, out_f64, stream)
+        : launch_dtype<CARBON_BF16>(p.pass, a, tiles, out_f64, stream);
+    count_launch();
+    return note_cuda(err);
+}
+
+carbon_status_t exact_round_launch(int dtype, void *out, const double *in, int64_t n,
+                                   cudaStream_t stream) {
+    if (n == 0) return CARBON_OK;
+    const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    round_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dtype, out, in, n);
+    count_launch();
+    return note_cuda(cudaGetLastError());
+}
+
+}  // namespace carbon

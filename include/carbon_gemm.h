@@ -1,0 +1,134 @@
+/*
+ * carbon_gemm.h - deterministic, batch-invariant linear-layer GEMM for
+ * NVIDIA GB300 (sm_103a).  Public C ABI.
+ *
+ * The three passes of a linear layer whose weight is stored [in, out]
+ * ("GEMM-natural", sgemm-bi page, "Use"):
+ *
+ *   carbon_gemm_fwd : Y  = X . W + b     X[M,K]  W[K,N]  b[N]  -> Y[M,N]
+ *   carbon_gemm_dx  : dX = dY . W^T      dY[M,N] W[K,N]        -> dX[M,K]
+ *   carbon_gemm_dw  : dW = X^T . dY      X[M,K]  dY[M,N]       -> dW[K,N]
+ *
+ * All matrices are dense, row-major and contiguous (row pitch = number of
+ * columns).  M is the number of tokens (rows of X, dY); K = in-features,
+ * N = out-features.  Every operand and the output have the same dtype.
+ *
+ * Two tiers (tier argument):
+ *
+ * CARBON_TIER_EXACT - every product is formed in float64 (exactly: products
+ *   of two fp32 or two bf16 values fit in binary64), and products are summed
+ *   with Kahan-Babushka-Neumaier compensation in a fixed order (Carbon
+ *   README, "How It Works": tiles, upcast to float64, KBN compensation in a
+ *   fixed order).  The order depends only on the reduction length R (K for
+ *   fwd, N for dX, M for dW): R is cut into 256-wide chunks from index 0; each
+ *   chunk is summed left to right with KBN and contributes the single double
+ *   fl(s + c); the chunk values are combined left to right with KBN again.
+ *   The forward pass adds the bias once in float64.  The float64 value is
+ *   rounded once, to nearest-even, to fp32 or bf16 (the RNE downcast of
+ *   sgemm-bi's "Determinism contracts").  The result is a pure function of
+ *   the inputs' bits: identical on every run, for every M, on every device,
+ *   and identical to a plain CPU implementation of the same steps.
+ *   Accepts CARBON_F32 and CARBON_BF16, any shape, any element alignment.
+ *
+ * CARBON_TIER_TC - bf16 x bf16 products accumulated in fp32 on the tensor
+ *   cores (tcgen05, accumulators in tensor memory), with a K schedule that
+ *   depends only on the shape of the reduction and the output columns, never
+ *   on the batch size of fwd/dX (sgemm-bi, "Determinism contracts", tensor
+ *   core tier: fixed tile families, shape-only dispatch).  fwd adds the bias
+ *   in fp32; the fp32 value is rounded once, to nearest-even, to bf16.
+ *   Bit-identical run to run; fwd and dX rows are bit-identical for every M.
+ *   Accepts CARBON_BF16 only (CARBON_F32 -> CARBON_ERR_UNSUPPORTED).  Base
+ *   pointers must be 16-byte aligned and K and N multiples of 8 (16-byte row
+ *   pitch), else CARBON_ERR_MISALIGNED.
+ *
+ * Conventions
+ *   - Pointers are DEVICE pointers on the current CUDA device; the caller
+ *     owns every buffer.
+ *   - Calls are asynchronous: they validate, enqueue the kernels on `stream`
+ *     and return.  Argument errors are returned synchronously and nothing is
+ *     enqueued.  Errors raised while kernels run are reported by
+ *     carbon_get_device_status().
+ *   - M == 0 or an output dimension of 0: nothing to do, CARBON_OK.
+ *     Reduction length 0: every output is +0 (fwd: the bias, rounded).
+ *   - Negative sizes, sizes whose element counts overflow int64, and NULL
+ *     pointers for operands with a non-zero element count:
+ *     CARBON_ERR_INVALID_ARG.  `bias` may be NULL (no bias).
+ *   - The output must not overlap any input (undefined result otherwise).
+ *   - A current device other than compute capability 10.3 (GB300):
+ *     CARBON_ERR_UNSUPPORTED.  There is no fallback path.
+ *   - Thread-safe.
+ */
+#ifndef CARBON_GEMM_H
+#define CARBON_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream: the same handle as cudaStream_t / CUstream.  NULL is the
+ * legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *carbon_stream_t;
+
+typedef enum {
+    CARBON_F32 = 0,     /* IEEE binary32 */
+    CARBON_BF16 = 1     /* bfloat16 (top 16 bits of binary32) */
+} carbon_dtype_t;
+
+typedef enum {
+    CARBON_TIER_EXACT = 0,  /* float64 products, fixed-order KBN, one RNE */
+    CARBON_TIER_TC = 1      /* bf16 tcgen05 MMA, fp32 accumulate */
+} carbon_tier_t;
+
+typedef enum {
+    CARBON_OK = 0,
+    CARBON_ERR_INVALID_ARG = 1,   /* bad size, pointer, dtype or tier */
+    CARBON_ERR_UNSUPPORTED = 2,   /* device or dtype/tier combination */
+    CARBON_ERR_MISALIGNED = 3,    /* TC tier: pointer/pitch not 16-byte aligned */
+    CARBON_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    CARBON_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up */
+} carbon_status_t;
+
+/* Forward pass Y[M,N] = X[M,K] . W[K,N] + bias[N].
+ * Reduction over K.  bias may be NULL. */
+carbon_status_t carbon_gemm_fwd(void *Y, const void *X, const void *W, const void *bias,
+                                int64_t M, int64_t K, int64_t N,
+                                carbon_dtype_t dtype, carbon_tier_t tier,
+                                carbon_stream_t stream);
+
+/* Input gradient dX[M,K] = dY[M,N] . W[K,N]^T.  Reduction over N. */
+carbon_status_t carbon_gemm_dx(void *dX, const void *dY, const void *W,
+                               int64_t M, int64_t K, int64_t N,
+                               carbon_dtype_t dtype, carbon_tier_t tier,
+                               carbon_stream_t stream);
+
+/* Weight gradient dW[K,N] = X[M,K]^T . dY[M,N].  Reduction over M (tokens). */
+carbon_status_t carbon_gemm_dw(void *dW, const void *X, const void *dY,
+                               int64_t M, int64_t K, int64_t N,
+                               carbon_dtype_t dtype, carbon_tier_t tier,
+                               carbon_stream_t stream);
+
+/* Synchronises `stream`, then reports (and clears) the device status word
+ * that kernels set when a bounded wait gives up (CARBON_ERR_TIMEOUT), or
+ * CARBON_ERR_CUDA if the stream reports an error. */
+carbon_status_t carbon_get_device_status(carbon_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *carbon_status_string(carbon_status_t status);
+
+/* Message of the last CUDA error seen by this thread inside the library
+ * ("" if none). */
+const char *carbon_last_cuda_error(void);
+
+/* ABI version of this header: (major << 16) | minor. */
+int carbon_abi_version(void);
+
+#define CARBON_ABI_VERSION ((1 << 16) | 0)
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CARBON_GEMM_H */

@@ -1,0 +1,65 @@
+/*
+ * carbon_gemm_debug.h - inspection and measurement entry points of the
+ * carbon_gemm library.  Not needed to use the GEMMs; used by the parity
+ * tests and the benchmark.  Same conventions as carbon_gemm.h (device
+ * pointers, asynchronous on `stream` unless stated, status codes).
+ */
+#ifndef CARBON_GEMM_DEBUG_H
+#define CARBON_GEMM_DEBUG_H
+
+#include "carbon_gemm.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { CARBON_PASS_FWD = 0, CARBON_PASS_DX = 1, CARBON_PASS_DW = 2 } carbon_pass_t;
+
+/* Exact tier, float64 value before the output rounding.
+ * Runs the same kernel arithmetic as carbon_gemm_{fwd,dx,dw} with
+ * CARBON_TIER_EXACT (fixed-order KBN of the float64 products, plus the bias
+ * for fwd) and stores the float64 result, so it can be compared bit for bit
+ * with a CPU implementation before rounding.
+ * pass: CARBON_PASS_*; A, B = (X, W) fwd, (dY, W) dX, (X, dY) dW; bias is
+ * used by fwd only (NULL allowed).  y64: float64 [rows x cols] with the
+ * output shape of the pass. */
+carbon_status_t carbon_debug_exact_y64(carbon_pass_t pass, double *y64,
+                                       const void *A, const void *B, const void *bias,
+                                       int64_t M, int64_t K, int64_t N,
+                                       carbon_dtype_t dtype, carbon_stream_t stream);
+
+/* Tensor-core tier, fp32 value before the bf16 rounding (accumulator plus
+ * bias for fwd), same kernel and K schedule as the CARBON_TIER_TC entry
+ * points.  acc: fp32 [rows x cols] with the output shape of the pass. */
+carbon_status_t carbon_debug_tc_f32(carbon_pass_t pass, float *acc,
+                                    const void *A, const void *B, const void *bias,
+                                    int64_t M, int64_t K, int64_t N,
+                                    carbon_stream_t stream);
+
+/* The exact tier's device-side output rounding applied to n float64 values
+ * (out: fp32 or bf16 elements), to check it against round-to-nearest-even. */
+carbon_status_t carbon_debug_round(carbon_dtype_t dtype, void *out, const double *in,
+                                   int64_t n, carbon_stream_t stream);
+
+/* Launches one block whose single thread waits on an mbarrier that nothing
+ * arrives on, with a budget of `budget_ns` nanoseconds; the wait gives up,
+ * sets the device status word and the kernel returns.  A following
+ * carbon_get_device_status() must report CARBON_ERR_TIMEOUT.  Exercises the
+ * timeout path that every bounded wait in the library shares. */
+carbon_status_t carbon_debug_timeout_probe(int64_t budget_ns, carbon_stream_t stream);
+
+/* FP64 issue-rate microbenchmark on the current device (blocking).
+ * Runs streams of independent DFMA and of independent DADD instructions
+ * on every SM and reports instructions per second (lane operations: one
+ * DFMA counts 1).  Used as the FP64 roofline denominator. */
+carbon_status_t carbon_measure_fp64_rate(double *dfma_per_s, double *dadd_per_s,
+                                         carbon_stream_t stream);
+
+/* Number of kernel launches the library has enqueued in this process. */
+int64_t carbon_debug_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CARBON_GEMM_DEBUG_H */
