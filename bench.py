@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Benchmark: deterministic GEMM throughput on GPT-2-124M linear shapes.
+
+One step = the whole hot path over one synthetic batch: for each GPT-2 layer
+shape (K, N) in {(768,2304), (768,768), (768,3072), (3072,768)} at
+M = 8192 tokens in bf16, the forward pass Y = X.W + b, dX = dY.W^T and
+dW = X^T.dY, on the exact tier (float64 products, fixed-order KBN) and on the
+tensor-core tier (tcgen05, fp32 accumulate).  Throughput counts 2*M*K*N
+useful flops per GEMM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--tiers exact,tc]
+
+Prints one JSON line (rank 0).  Inputs are seeded and synthetic (the pages'
+GPT-2 fine-tune needs weights and data that are not available).  L2 is
+flushed (a 256 MiB write) between timed steps, outside the timed events.
+Under torchrun every rank runs its own replica of the workload (weak
+scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("deterministic GEMM GFLOP/s (fwd+dX+dW, GPT-2 shapes) and % of FP64 / "
+          "bf16-TC peak")
+LAYERS = ((768, 2304), (768, 768), (768, 3072), (3072, 768))
+TOKENS = 8192
+SEED = 42
+PASSES = ("fwd", "dx", "dw")
+# float64 instructions one KBN step of the exact tier issues (DFMA for the
+# running sum, two for Fast2Sum's exact error, one DADD for the compensation)
+FP64_OPS_PER_MAC = 4
+
+
+def _r(x, n=4):
+    return None if x is None else float(f"{x:.{n}g}")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------- workload
+
+def pass_dims(pass_, M, K, N):
+    """(rows, cols, R) of the pass's output and reduction."""
+    return {"fwd": (M, N, K), "dx": (M, K, N), "dw": (K, N, M)}[pass_]
+
+
+def step_flops(M=TOKENS, layers=LAYERS):
+    return sum(2.0 * M * K * N for (K, N) in layers) * len(PASSES)
+
+
+def make_host_layers(seed, M=TOKENS, layers=LAYERS):
+    from deterministic_invariant_gemm_fwd_gb300 import inputs
+    return inputs.gpt2(seed, M=M, layers=layers)
+
+
+class Workload:
+    """Device-resident operands and outputs of one step."""
+
+    def __init__(self, host_layers, device, tiers):
+        import torch
+        self.torch = torch
+        self.layers = []
+        self.tiers = tiers
+        for L in host_layers:
+            d = {k: torch.from_numpy(L[k].view(np.int16)).to(device).view(torch.bfloat16)
+                 for k in ("X", "W", "b", "dY")}
+            M, K, N = L["M"], L["K"], L["N"]
+            d.update(M=M, K=K, N=N)
+            for t in tiers:
+                d[f"Y_{t}"] = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+                d[f"dX_{t}"] = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+                d[f"dW_{t}"] = torch.empty((K, N), dtype=torch.bfloat16, device=device)
+            self.layers.append(d)
+
+    def launch(self, tier, stream, events=None):
+        """Enqueue the 12 GEMMs of one tier; optional per-launch events."""
+        import deterministic_invariant_gemm_fwd_gb300 as cg
+        s = stream.cuda_stream
+        for d in self.layers:
+            M, K, N = d["M"], d["K"], d["N"]
+            calls = (
+                lambda: cg.carbon_gemm_fwd(d[f"Y_{tier}"], d["X"], d["W"], d["b"], M, K, N, "bf16", tier, s),
+                lambda: cg.carbon_gemm_dx(d[f"dX_{tier}"], d["dY"], d["W"], M, K, N, "bf16", tier, s),
+                lambda: cg.carbon_gemm_dw(d[f"dW_{tier}"], d["X"], d["dY"], M, K, N, "bf16", tier, s),
+            )
+            for p, call in zip(PASSES, calls):
+                if events is not None:
+                    e0 = self.torch.cuda.Event(enable_timing=True)
+                    e1 = self.torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    call()
+                    e1.record(stream)
+                    events.append((tier, p, M, K, N, e0, e1))
+                else:
+                    call()
+
+
+def tc_available():
+    import torch
+    import deterministic_invariant_gemm_fwd_gb300 as cg
+    X = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    try:
+        cg.linear_fwd(X, W, None, tier="tc")
+        torch.cuda.synchronize()
+        return True
+    except cg.CarbonError as e:
+        if e.status == 2:
+            return False
+        raise
+
+
+# ------------------------------------------------------------------- clocks
+
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clocks_setting"}
+
+
+class ClockSampler:
+    def __init__(self, index):
+        self.proc = None
+        self.index = index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for line in self.out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 4:
+                continue
+            try:
+                s, m = float(parts[0]), float(parts[1])
+                bitsv = int(parts[3], 16)
+            except ValueError:
+                continue
+            if bitsv & 0x1:          # idle samples between launches
+                continue
+            sm.append(s)
+            mx.append(m)
+            for b, name in REASON_BITS.items():
+                if bitsv & b:
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU baseline
+
+def oracle_sample(host_layers, target_s, threads=None):
+    """Time the oracle on a random sample of outputs of every exact-tier GEMM
+    of the step.  Returns (useful GFLOP/s, seconds, sampled MACs, threads)."""
+    import oracle
+    from deterministic_invariant_gemm_fwd_gb300 import inputs
+    threads = threads or oracle.default_threads()
+
+    def run(per_gemm):
+        macs, t0 = 0, time.perf_counter()
+        for li, L in enumerate(host_layers):
+            M, K, N = L["M"], L["K"], L["N"]
+            for p, (A, B, bias) in zip(PASSES, ((L["X"], L["W"], L["b"]),
+                                               (L["dY"], L["W"], None),
+                                               (L["X"], L["dY"], None))):
+                rows, cols, R = pass_dims(p, M, K, N)
+                ri, ci = inputs.sample_indices(li * 7 + len(p), rows, cols, per_gemm, corners=False)
+                oracle.gemm_at(p, "bf16", A, B, bias, M, K, N, ri, ci, threads=threads)
+                macs += per_gemm * R
+        return macs, time.perf_counter() - t0
+
+    per = 64
+    macs, dt = run(per)
+    while dt < target_s / 4 and per < 1 << 22:
+        per = int(per * min(8.0, max(2.0, target_s / max(dt, 1e-3))))
+        macs, dt = run(per)
+    return 2.0 * macs / dt / 1e9, dt, macs, threads, per
+
+
+# -------------------------------------------------------------------- main
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reference_arm(args, world, rank):
+    """The reference arm: the CPU oracle, timed as it stands, on a bounded
+    sample of the same workload in every step."""
+    if world > 1 and rank != 0:
+        return
+    host = make_host_layers(SEED)
+    per_step = max(1.0, 90.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, dt, macs, threads, per = oracle_sample(host, per_step)
+        if i >= args.warmup:
+            vals.append((v, dt))
+    value = statistics.median(v for v, _ in vals)
+    ms = statistics.median(dt for _, dt in vals) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": _r(value), "unit": "GFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": _r(ms), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "gpt2-124m linear layers bf16 M=8192, exact fixed-order KBN "
+                               "(CPU oracle on a sample of outputs of every GEMM)",
+                   "sample": f"{per} outputs of each of the 12 GEMMs per step"},
+        "cpu_baseline": {"value": _r(value), "unit": "GFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": f"{per} outputs x 12 GEMMs, {macs} MACs"},
+        "e2e": {"value": _r(value), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tiers", default="auto")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+
+    import torch
+    import deterministic_invariant_gemm_fwd_gb300 as cg
+
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+
+    tiers = ["exact", "tc"] if args.tiers == "auto" else args.tiers.split(",")
+    if "tc" in tiers and not tc_available():
+        tiers = [t for t in tiers if t != "tc"]
+    host = make_host_layers(SEED + rank)
+    wl = Workload(host, device, tiers)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if pg is not None:
+            pg.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for t in tiers:
+                wl.launch(t, stream)
+        stream.synchronize()
+        assert cg.carbon_get_device_status(stream.cuda_stream) == 0
+
+        barrier()
+        launches0 = cg.carbon_debug_launch_count()
+        step_events, kernel_events = [], []
+        with ClockSampler(local) as clocks:
+            for _ in range(args.steps):
+                flush.fill_(1)                                  # L2 flush, outside the events
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for t in tiers:
+                    wl.launch(t, stream, kernel_events)
+                e1.record(stream)
+                step_events.append((e0, e1))
+            stream.synchronize()
+        barrier()
+        launches = cg.carbon_debug_launch_count() - launches0
+        assert cg.carbon_get_device_status(stream.cuda_stream) == 0
+
+    step_ms = sum(a.elapsed_time(b) for a, b in step_events) / args.steps
+    if pg is not None:
+        t = torch.tensor([step_ms], device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        step_ms = float(t.item())
+    flops = step_flops() * len(tiers)
+    value = flops * world / (step_ms * 1e-3) / 1e9
+
+    tier_info, rooflines = {}, {}
+    pk, pk_kind = peaks()
+    fp64_rate = None
+    for t in tiers:
+        ev = [e for e in kernel_events if e[0] == t]
+        ms = sum(e0.elapsed_time(e1) for *_, e0, e1 in ev)
+        fl = sum(2.0 * M * K * N for (_, _, M, K, N, _, _) in ev)
+        per_gemm = {}
+        for (_, p, M, K, N, e0, e1) in ev:
+            per_gemm.setdefault(f"{p}_{K}x{N}", []).append(e0.elapsed_time(e1))
+        tier_info[t] = {"ms_per_step": _r(ms / args.steps), "gflops": _r(fl / (ms * 1e-3) / 1e9),
+                        "launches_per_step": len(ev) // args.steps,
+                        "ms_per_gemm": {k: _r(sum(v) / len(v)) for k, v in per_gemm.items()}}
+        if t == "exact":
+            if fp64_rate is None:
+                fp64_rate, _ = cg.carbon_measure_fp64_rate(stream.cuda_stream)
+            achieved = FP64_OPS_PER_MAC * (fl / 2.0) / (ms * 1e-3) / 1e12
+            peak = fp64_rate / 1e12
+            rooflines["exact"] = {
+                "bound": "alu", "unit": "TFLOP/s", "achieved": _r(achieved), "peak": _r(peak),
+                "frac": _r(achieved / peak), "traffic": None,
+                "kernel": "exact_kbn_kernel",
+                "note": ("float64 lane operations: 4 per KBN step; peak = DFMA lane rate "
+                         "measured live by carbon_measure_fp64_rate (of measured)"),
+                "useful_gflops": tier_info[t]["gflops"],
+                "survey_5op_utilisation": _r(5 * (fl / 2.0) / (ms * 1e-3) / fp64_rate)}
+        else:
+            achieved = fl / (ms * 1e-3) / 1e12
+            peak = float(pk["bf16_tflops"])
+            rooflines["tc"] = {"bound": "tensor", "unit": "TFLOP/s", "achieved": _r(achieved),
+                               "peak": _r(peak), "frac": _r(achieved / peak), "traffic": None,
+                               "kernel": "tc_gemm_kernel", "peak_kind": f"bf16 burst, of {pk_kind}"}
+
+    # end to end through the public API: pinned host inputs -> device -> host
+    e2e = None
+    if not args.no_e2e:
+        pinned_in = [{k: torch.from_numpy(L[k].view(np.int16)).pin_memory() for k in ("X", "W", "b", "dY")}
+                     for L in host]
+        pinned_out = []
+        for L in host:
+            M, K, N = L["M"], L["K"], L["N"]
+            pinned_out.append({f"{n}_{t}": torch.empty(shape, dtype=torch.int16).pin_memory()
+                               for t in tiers for n, shape in (("Y", (M, N)), ("dX", (M, K)), ("dW", (K, N)))})
+        h2d = sum(v.numel() * 2 for d in pinned_in for v in d.values())
+        d2h = sum(v.numel() * 2 for d in pinned_out for v in d.values())
+        with torch.cuda.stream(stream):
+            barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                for d, pi in zip(wl.layers, pinned_in):
+                    for k in ("X", "W", "b", "dY"):
+                        d[k].view(torch.int16).copy_(pi[k], non_blocking=True)
+                for t in tiers:
+                    wl.launch(t, stream)
+                for d, po in zip(wl.layers, pinned_out):
+                    for t in tiers:
+                        for n in ("Y", "dX", "dW"):
+                            po[f"{n}_{t}"].copy_(d[f"{n}_{t}"].view(torch.int16), non_blocking=True)
+            e1.record(stream)
+            stream.synchronize()
+            e2e_ms = e0.elapsed_time(e1) / args.steps
+        if pg is not None:
+            t_ = torch.tensor([e2e_ms], device=device)
+            pg.all_reduce(t_, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t_.item())
+        e2e = {"value": _r(flops * world / (e2e_ms * 1e-3) / 1e9), "unit": "GFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": _r(e2e_ms)}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        v, dt, macs, threads, per = oracle_sample(host, args.cpu_seconds)
+        cpu = {"value": _r(v), "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{per} outputs of each of the 12 exact-tier GEMMs "
+                         f"({macs} MACs, {dt:.1f} s)"}
+
+    if rank == 0:
+        dom = "exact" if "exact" in rooflines else "tc"
+        line = {
+            "metric": METRIC, "value": _r(value), "unit": "GFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": _r(step_ms),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64" if tiers == ["exact"] else "f64+f32acc",
+            "data": "synthetic",
+            "config": {"workload": "gpt2-124m linear layers, bf16, M=8192 tokens, "
+                                   "(K,N) in {(768,2304),(768,768),(768,3072),(3072,768)}, "
+                                   "fwd+dX+dW, tiers " + "+".join(tiers),
+                       "tiers": tiers, "l2": "flushed between steps (256 MiB write)",
+                       "parallelism": f"replicas x{world}", "seed": SEED},
+            "tiers": tier_info,
+            "roofline": rooflines[dom],
+            "rooflines": rooflines,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,80 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+function its headers declare, and rejects bad arguments before touching the
+device."""
+import ctypes
+
+import pytest
+
+from deterministic_invariant_gemm_fwd_gb300 import _binding as b
+
+INVALID, UNSUPPORTED, MISALIGNED = 1, 2, 3
+
+
+def test_every_declared_symbol_is_exported():
+    names = b.declared_functions()
+    for must in ("carbon_gemm_fwd", "carbon_gemm_dx", "carbon_gemm_dw",
+                 "carbon_get_device_status", "carbon_status_string",
+                 "carbon_abi_version"):
+        assert must in names
+    raw = ctypes.CDLL(b.LIB_PATH)
+    for name in names:
+        assert hasattr(raw, name), name
+
+
+def test_abi_version_and_status_names():
+    assert b.carbon_abi_version() >> 16 == 1
+    for code, name in b.STATUS.items():
+        assert b.carbon_status_string(code) == name
+
+
+FAKE = 0x1000   # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("fn", ["fwd", "dx", "dw"])
+def test_negative_sizes_rejected(fn):
+    for M, K, N in ((-1, 2, 3), (2, -1, 3), (2, 3, -1)):
+        if fn == "fwd":
+            st = b.lib.carbon_gemm_fwd(FAKE, FAKE, FAKE, None, M, K, N, 0, 0, None)
+        elif fn == "dx":
+            st = b.lib.carbon_gemm_dx(FAKE, FAKE, FAKE, M, K, N, 0, 0, None)
+        else:
+            st = b.lib.carbon_gemm_dw(FAKE, FAKE, FAKE, M, K, N, 0, 0, None)
+        assert st == INVALID
+
+
+def test_overflowing_sizes_rejected():
+    big = 1 << 40
+    assert b.lib.carbon_gemm_fwd(FAKE, FAKE, FAKE, None, big, big, 4, 0, 0, None) == INVALID
+    assert b.lib.carbon_gemm_dw(FAKE, FAKE, FAKE, 4, big, 1 << 30, 0, 0, None) == INVALID
+
+
+def test_bad_dtype_and_tier_rejected():
+    assert b.lib.carbon_gemm_fwd(FAKE, FAKE, FAKE, None, 2, 3, 4, 7, 0, None) == INVALID
+    assert b.lib.carbon_gemm_fwd(FAKE, FAKE, FAKE, None, 2, 3, 4, 0, 9, None) == INVALID
+    assert b.lib.carbon_debug_exact_y64(5, FAKE, FAKE, FAKE, None, 2, 3, 4, 0, None) == INVALID
+
+
+def test_tc_tier_rejects_f32():
+    assert b.lib.carbon_gemm_fwd(FAKE, FAKE, FAKE, None, 2, 8, 8, 0, 1, None) == UNSUPPORTED
+
+
+def test_null_pointers_rejected():
+    assert b.lib.carbon_gemm_fwd(None, FAKE, FAKE, None, 2, 3, 4, 0, 0, None) == INVALID
+    assert b.lib.carbon_gemm_fwd(FAKE, None, FAKE, None, 2, 3, 4, 0, 0, None) == INVALID
+    assert b.lib.carbon_gemm_dx(FAKE, FAKE, None, 2, 3, 4, 0, 0, None) == INVALID
+    assert b.lib.carbon_gemm_dw(FAKE, None, FAKE, 2, 3, 4, 1, 0, None) == INVALID
+
+
+def test_empty_outputs_are_a_no_op():
+    # no output elements: OK without touching the device or any pointer
+    assert b.lib.carbon_gemm_fwd(None, None, None, None, 0, 3, 4, 0, 0, None) == 0
+    assert b.lib.carbon_gemm_fwd(None, None, None, None, 5, 3, 0, 1, 0, None) == 0
+    assert b.lib.carbon_gemm_dx(None, None, None, 5, 0, 4, 0, 0, None) == 0
+    assert b.lib.carbon_gemm_dw(None, None, None, 5, 0, 4, 0, 0, None) == 0
+
+
+def test_debug_round_validation():
+    assert b.lib.carbon_debug_round(3, FAKE, FAKE, 4, None) == INVALID
+    assert b.lib.carbon_debug_round(0, None, FAKE, 4, None) == INVALID
+    assert b.lib.carbon_debug_round(0, None, None, 0, None) == 0
+    assert b.lib.carbon_debug_timeout_probe(0, None) == INVALID
