@@ -40,7 +40,7 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"carbon_gemm CUDA library not built ({LIB_PATH} missing); run "
-            "`python -m deterministic_invariant_gemm_fwd_gb300.build`")
+            "`python deterministic_invariant_gemm_fwd_gb300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i64, i32, dp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
     sig = {

@@ -5,7 +5,8 @@ linked statically, so the library needs only the NVIDIA driver at run time;
 the driver's tensor-map encoder is looked up through the runtime's
 driver-entry-point query, so there is no link-time dependency on libcuda.
 
-Usage: ``python -m deterministic_invariant_gemm_fwd_gb300.build [--force]``.
+Usage: ``python deterministic_invariant_gemm_fwd_gb300/build.py [--force]`` (run as a
+file: importing the package itself loads the library).
 """
 from __future__ import annotations
 
