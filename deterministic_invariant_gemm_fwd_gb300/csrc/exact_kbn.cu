@@ -124,7 +124,7 @@ __device__ __forceinline__ unsigned short round_bf16(double y) {
     if (E >= 128) return (unsigned short)(sign | 0x7f80u);                    // |y| >= 2^128
     if (E >= -126) {                                                          // bf16 normal range
         const unsigned long long lsb = (mag >> 45) & 1ull;
-        const unsigned long long r = (mag + 0x00001fffffffffffull + lsb) >> 45;
+        const unsigned long long r = (mag + 0x00000fffffffffffull + lsb) >> 45;
         const int Ed = (int)(r >> 7);                                         // biased, after carry
         if (Ed - 1023 >= 128) return (unsigned short)(sign | 0x7f80u);
         return (unsigned short)(sign | ((unsigned int)(Ed - 1023 + 127) << 7) | (unsigned int)(r & 0x7f));
