@@ -1,12 +1,481 @@
-// tc_gemm.cu - tensor-core tier (placeholder until the tcgen05 kernel lands).
+// tc_gemm.cu - tensor-core tier: bf16 x bf16 -> fp32 on tcgen05, accumulator
+// in tensor memory, operands staged by TMA, fixed K schedule.
+//
+// What is computed (sgemm-bi page, "Determinism contracts", tensor-core
+// tier: fp32-accumulated bf16 products, bit-identical across runs, forward
+// batch-invariant across M, shape-only dispatch): out = A.B (+ bias, fwd) in
+// fp32, rounded once to bf16 (RNE).
+//
+// Determinism and batch invariance by construction:
+//  * the output tile is always 128 rows x BN columns; BN depends on the
+//    output column count only; rows past M are zero-filled by TMA and their
+//    results dropped, so row i's instruction sequence is the same for every M;
+//  * each tile's reduction runs its k-blocks of 64 in ascending order, four
+//    K=16 MMAs per block in ascending order, into one TMEM accumulator;
+//    nothing is split across CTAs and no atomics are used;
+//  * tile-to-CTA scheduling depends on M, the arithmetic of a row does not.
+//
+// Kernel structure (one CTA per SM, persistent over output tiles):
+//  warp 0     TMA producer: fills a ring of shared-memory stages (A 128x64 and
+//             B BNx64 bf16 tiles, 128-byte swizzle), mbarrier transaction counts
+//  warp 1     MMA issuer: allocates TMEM (two accumulators of BN columns),
+//             issues tcgen05.mma per stage, commits stage release and tile
+//             completion to mbarriers
+//  warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter of the
+//             accumulator, bias, bf16 rounding, global stores; while they
+//             drain one accumulator the MMA warp fills the other.
+// Every mbarrier wait is bounded (device_sync.cuh); a wait that gives up
+// records CARBON_ERR_TIMEOUT, raises a CTA-wide abort flag so the other roles
+// leave their loops, and the TMEM allocation is still released.
 #include "carbon_internal.h"
+#include "device_sync.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
 
 namespace carbon {
 namespace {
+
 __device__ unsigned int g_tc_status = 0;
+
+constexpr int kBM = 128;          // tile rows (= MMA M, = TMEM lanes)
+constexpr int kBK = 64;           // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int kUMMA_K = 16;       // K of one tcgen05.mma kind::f16
+constexpr int kStages = 4;
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kEpiWarps = 4;
+constexpr uint32_t kABytes = kBM * kBK * 2;           // 16 KiB
+constexpr uint32_t kMNBlockBytes = 64 * kBK * 2;      // one 64-wide MN block of an MN-major tile
+
+enum Major { K_MAJOR = 0, MN_MAJOR = 1 };
+
+struct TcArgs {
+    void *out;
+    const void *bias;         // bf16 [cols] or null (fwd only)
+    int64_t rows, cols, R;
+    int tiles_m, tiles_n, num_kb;
+};
+
+template <int BN>
+struct Smem {
+    static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kBarOffset = kStages * kStageBytes;
+    // full[S], empty[S], tfull[2], tempty[2], then tmem base slot and abort flag
+    static constexpr uint32_t kBytes = kBarOffset + (2 * kStages + 4) * 8 + 16;
+    static constexpr uint32_t kDynamic = kBytes + 1024;   // room to align the base to 1 KiB
+};
+
+// ---- PTX wrappers -----------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"(map), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
 }
 
-carbon_status_t tc_launch(const Problem &, bool, cudaStream_t) { return CARBON_ERR_UNSUPPORTED; }
+__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(slot_smem), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                 ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+        ::"r"(bar) : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit: thread t of the warp receives lane
+// (base lane + t), columns col .. col+31.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format:
+// start>>4 @0, LBO>>4 @16, SBO>>4 @32, version 1 @46, layout 2 @61).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B,
+// majorness of A and B, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t instr_desc(int bn, int a_major, int b_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_major << 15) |
+           ((uint32_t)b_major << 16) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+// Descriptor of the K=16 slice `k` (0..3) of a 64-deep k-block tile whose
+// MN extent is `mn` (rows of a K-major tile, or 64-wide blocks of an MN-major one).
+template <int MAJOR>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t tile_base, int k) {
+    if (MAJOR == K_MAJOR)   // rows of 128 B; 8-row atoms 1024 B apart; K slice = +32 B
+        return smem_desc(tile_base + (uint32_t)k * (kUMMA_K * 2), 16, 1024);
+    // MN-major: rows are k (128 B = 64 MN elements); 8-k groups 1024 B apart (SBO);
+    // 64-wide MN blocks kMNBlockBytes apart (LBO); K slice = 16 rows = +2048 B
+    return smem_desc(tile_base + (uint32_t)k * (kUMMA_K * 128), kMNBlockBytes, 1024);
+}
+
+__device__ __forceinline__ bool aborted(volatile uint32_t *flag) { return *flag != 0; }
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile uint32_t *flag) {
+    if (mbar_wait(bar, parity)) return true;
+    *flag = 1u;
+    atomicExch(&g_tc_status, (unsigned)CARBON_ERR_TIMEOUT);
+    return false;
+}
+
+template <int BN, int A_MAJOR, int B_MAJOR, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+               const TcArgs p) {
+    using L = Smem<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
+    const uint32_t full0 = smem_addr(bars);
+    const uint32_t empty0 = full0 + 8 * kStages;
+    const uint32_t tfull0 = empty0 + 8 * kStages;
+    const uint32_t tempty0 = tfull0 + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 4);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    constexpr uint32_t kTmemCols = 2 * BN;                 // 256 or 512: powers of two
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, kEpiWarps);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+        prefetch_map(&map_a);
+        prefetch_map(&map_b);
+    }
+    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_tiles = p.tiles_m * p.tiles_n;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+                const int m0 = (t / p.tiles_n) * kBM, n0 = (t % p.tiles_n) * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    const uint32_t fb = full0 + 8 * s, eb = empty0 + 8 * s;
+                    if (!wait_or_abort(eb, ph ^ 1u, abort_flag)) break;
+                    mbar_arrive_expect_tx(fb, L::kStageBytes);
+                    const uint32_t sa = sbase + s * L::kStageBytes, sb = sa + kABytes;
+                    const int k0 = kb * kBK;
+                    if (A_MAJOR == K_MAJOR) {
+                        tma_load_2d(sa, &map_a, fb, k0, m0);
+                    } else {
+                        tma_load_2d(sa, &map_a, fb, m0, k0);
+                        tma_load_2d(sa + kMNBlockBytes, &map_a, fb, m0 + 64, k0);
+                    }
+                    if (B_MAJOR == K_MAJOR) {
+                        tma_load_2d(sb, &map_b, fb, k0, n0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(sb + j * kMNBlockBytes, &map_b, fb, n0 + 64 * j, k0);
+                    }
+                    if (++s == kStages) { s = 0; ph ^= 1u; }
+                }
+            }
+            // let every load this thread issued land before the CTA can exit
+            for (int i = 0; i < kStages; ++i) {
+                if (--s < 0) { s = kStages - 1; ph ^= 1u; }
+                // a stage armed in this pass completes with parity ph; unarmed ones
+                // were completed earlier, so this wait returns at once either way
+                if (!mbar_wait(full0 + 8 * s, ph, kWaitBudgetNs)) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc = instr_desc(BN, A_MAJOR, B_MAJOR);
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+                if (!wait_or_abort(tempty0 + 8 * acc, aph ^ 1u, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+                bool ok = true;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_or_abort(full0 + 8 * s, ph, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + s * L::kStageBytes, sb = sa + kABytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUMMA_K; ++k)
+                        mma_bf16(d, operand_desc<A_MAJOR>(sa, k), operand_desc<B_MAJOR>(sb, k),
+                                 idesc, (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(empty0 + 8 * s);          // stage free once these MMAs finish
+                    if (++s == kStages) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(tfull0 + 8 * acc);            // accumulator ready
+                if (++acc == 2) { acc = 0; aph ^= 1u; }
+            }
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int quarter = warp % 4;                    // TMEM lanes 32*quarter .. +31
+        const int row_in_tile = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
+            const int64_t row = (int64_t)(t / p.tiles_n) * kBM + row_in_tile;
+            const int64_t n0 = (int64_t)(t % p.tiles_n) * BN;
+            if (!wait_or_abort(tfull0 + 8 * acc, aph, abort_flag)) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c), v);
+                if (row < p.rows) {
+                    const int64_t col0 = n0 + c;
+                    float f[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+                    if (p.bias) {
+                        const __nv_bfloat16 *bp = static_cast<const __nv_bfloat16 *>(p.bias);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + i < p.cols) f[i] = __fadd_rn(f[i], __bfloat162float(bp[col0 + i]));
+                    }
+                    if (OUT_F32) {
+                        float *o = static_cast<float *>(p.out) + row * p.cols + col0;
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            if (col0 + 4 * g < p.cols)
+                                *reinterpret_cast<float4 *>(o + 4 * g) =
+                                    make_float4(f[4 * g], f[4 * g + 1], f[4 * g + 2], f[4 * g + 3]);
+                    } else {
+                        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + row * p.cols + col0;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            if (col0 + 8 * g >= p.cols) continue;   // cols is a multiple of 8
+                            uint4 w;
+                            __nv_bfloat162 h;
+                            h = __floats2bfloat162_rn(f[8 * g + 0], f[8 * g + 1]); w.x = *reinterpret_cast<uint32_t *>(&h);
+                            h = __floats2bfloat162_rn(f[8 * g + 2], f[8 * g + 3]); w.y = *reinterpret_cast<uint32_t *>(&h);
+                            h = __floats2bfloat162_rn(f[8 * g + 4], f[8 * g + 5]); w.z = *reinterpret_cast<uint32_t *>(&h);
+                            h = __floats2bfloat162_rn(f[8 * g + 6], f[8 * g + 7]); w.w = *reinterpret_cast<uint32_t *>(&h);
+                            *reinterpret_cast<uint4 *>(o + 8 * g) = w;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            if (++acc == 2) { acc = 0; aph ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// Fills an output whose reduction is empty: bias (fwd) or +0.
+template <bool OUT_F32>
+__global__ void tc_fill_kernel(void *out, const void *bias, int64_t rows, int64_t cols) {
+    const int64_t n = rows * cols;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = bias ? __bfloat162float(static_cast<const __nv_bfloat16 *>(bias)[i % cols]) : 0.0f;
+        if (OUT_F32) static_cast<float *>(out)[i] = v;
+        else static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
+    }
+}
+
+// ---- host side ----------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t get_encoder() {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            g_encode_err = cudaErrorNotSupported;
+        if (g_encode_err == cudaSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode_err;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix with a
+// {64, box_outer} box and 128-byte swizzle; out-of-range elements read as 0.
+bool encode_map(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int box_outer) {
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_outer};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int AM, int BM_, bool F32>
+cudaError_t launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
+                          int grid, cudaStream_t stream) {
+    auto kern = tc_gemm_kernel<BN, AM, BM_, F32>;
+    const int smem = (int)Smem<BN>::kDynamic;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, kThreads, smem, stream>>>(ma, mb, a);
+    return cudaGetLastError();
+}
+
+template <int BN, bool F32>
+cudaError_t launch_pass(int pass, const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
+                        int grid, cudaStream_t s) {
+    switch (pass) {
+    case CARBON_PASS_FWD: return launch_kernel<BN, K_MAJOR, MN_MAJOR, F32>(ma, mb, a, grid, s);
+    case CARBON_PASS_DX:  return launch_kernel<BN, K_MAJOR, K_MAJOR, F32>(ma, mb, a, grid, s);
+    default:              return launch_kernel<BN, MN_MAJOR, MN_MAJOR, F32>(ma, mb, a, grid, s);
+    }
+}
+
+// Output-tile width from the output column count only (never from M).
+int choose_bn(int64_t cols) { return cols <= 128 ? 128 : 256; }
+
+}  // namespace
+
+carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
+    if (p.rows == 0 || p.cols == 0) return CARBON_OK;
+    // 16-byte aligned bases and row pitches (K and N multiples of 8 bf16)
+    if ((p.K % 8) != 0 || (p.N % 8) != 0) return CARBON_ERR_MISALIGNED;
+    auto mis = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0; };
+    if (mis(p.A) || mis(p.B) || mis(p.out) || (p.bias && (reinterpret_cast<uintptr_t>(p.bias) & 1u)))
+        return CARBON_ERR_MISALIGNED;
+    int dev = 0, sms = 0;
+    carbon_status_t st = current_device(&dev, &sms);
+    if (st != CARBON_OK) return st;
+
+    if (p.R == 0) {
+        const int64_t n = p.rows * p.cols;
+        const int blocks = (int)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535);
+        if (out_f32) tc_fill_kernel<true><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
+        else tc_fill_kernel<false><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
+        count_launch();
+        return note_cuda(cudaGetLastError());
+    }
+    if (p.rows > (int64_t)0x7fffffff || p.cols > (int64_t)0x7fffffff || p.R > (int64_t)0x7fffffff)
+        return CARBON_ERR_INVALID_ARG;
+
+    cudaError_t err = get_encoder();
+    if (err != cudaSuccess) return note_cuda(err);
+
+    const int bn = choose_bn(p.cols);
+    CUtensorMap ma, mb;
+    bool ok;
+    switch (p.pass) {
+    case CARBON_PASS_FWD:   // A = X [M, K] K-major; B = W [K, N] N-contiguous (MN-major)
+        ok = encode_map(&ma, p.A, p.K, p.M, kBM) && encode_map(&mb, p.B, p.N, p.K, 64);
+        break;
+    case CARBON_PASS_DX:    // A = dY [M, N] K-major; B = W [K, N]: rows = out cols, K-major
+        ok = encode_map(&ma, p.A, p.N, p.M, kBM) && encode_map(&mb, p.B, p.N, p.K, bn);
+        break;
+    default:                // A = X [M, K] and B = dY [M, N], both MN-major
+        ok = encode_map(&ma, p.A, p.K, p.M, 64) && encode_map(&mb, p.B, p.N, p.M, 64);
+        break;
+    }
+    if (!ok) return CARBON_ERR_MISALIGNED;
+
+    TcArgs a;
+    a.out = p.out; a.bias = p.bias;
+    a.rows = p.rows; a.cols = p.cols; a.R = p.R;
+    a.tiles_m = (int)((p.rows + kBM - 1) / kBM);
+    a.tiles_n = (int)((p.cols + bn - 1) / bn);
+    a.num_kb = (int)((p.R + kBK - 1) / kBK);
+    const int64_t tiles = (int64_t)a.tiles_m * a.tiles_n;
+    if (tiles > (int64_t)0x7fffffff) return CARBON_ERR_INVALID_ARG;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+
+    if (bn == 128)
+        err = out_f32 ? launch_pass<128, true>(p.pass, ma, mb, a, grid, stream)
+                      : launch_pass<128, false>(p.pass, ma, mb, a, grid, stream);
+    else
+        err = out_f32 ? launch_pass<256, true>(p.pass, ma, mb, a, grid, stream)
+                      : launch_pass<256, false>(p.pass, ma, mb, a, grid, stream);
+    count_launch();
+    return note_cuda(err);
+}
 
 carbon_status_t tc_take_device_status() {
     unsigned int v = 0, zero = 0;
