@@ -74,11 +74,12 @@ def make_host_layers(seed, M=TOKENS, layers=LAYERS):
 class Workload:
     """Device-resident operands and outputs of one step."""
 
-    def __init__(self, host_layers, device, tiers):
+    def __init__(self, host_layers, device, tiers, only=None):
         import torch
         self.torch = torch
         self.layers = []
         self.tiers = tiers
+        self.only = only          # optional set of "tier:pass:KxN" to run alone
         for L in host_layers:
             d = {k: torch.from_numpy(L[k].view(np.int16)).to(device).view(torch.bfloat16)
                  for k in ("X", "W", "b", "dY")}
@@ -102,6 +103,8 @@ class Workload:
                 lambda: cg.carbon_gemm_dw(d[f"dW_{tier}"], d["X"], d["dY"], M, K, N, "bf16", tier, s),
             )
             for p, call in zip(PASSES, calls):
+                if self.only is not None and f"{tier}:{p}:{K}x{N}" not in self.only:
+                    continue
                 if events is not None:
                     e0 = self.torch.cuda.Event(enable_timing=True)
                     e1 = self.torch.cuda.Event(enable_timing=True)
@@ -265,6 +268,9 @@ def main():
     ap.add_argument("--tiers", default="auto")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gemm", default=None,
+                    help="profiling aid: comma list of tier:pass:KxN to run alone "
+                         "(e.g. tc:fwd:768x2304); the JSON line then covers only those")
     args = ap.parse_args()
     world, rank, local = dist_env()
 
@@ -289,7 +295,8 @@ def main():
     if "tc" in tiers and not tc_available():
         tiers = [t for t in tiers if t != "tc"]
     host = make_host_layers(SEED + rank)
-    wl = Workload(host, device, tiers)
+    only = set(args.gemm.split(",")) if args.gemm else None
+    wl = Workload(host, device, tiers, only)
     stream = torch.cuda.Stream(device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
@@ -328,7 +335,7 @@ def main():
         t = torch.tensor([step_ms], device=device)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         step_ms = float(t.item())
-    flops = step_flops() * len(tiers)
+    flops = sum(2.0 * M * K * N for (t, p, M, K, N, _, _) in kernel_events) / args.steps
     value = flops * world / (step_ms * 1e-3) / 1e9
 
     tier_info, rooflines = {}, {}
@@ -336,6 +343,8 @@ def main():
     fp64_rate = None
     for t in tiers:
         ev = [e for e in kernel_events if e[0] == t]
+        if not ev:
+            continue
         ms = sum(e0.elapsed_time(e1) for *_, e0, e1 in ev)
         fl = sum(2.0 * M * K * N for (_, _, M, K, N, _, _) in ev)
         per_gemm = {}
@@ -410,6 +419,10 @@ def main():
 
     if rank == 0:
         dom = "exact" if "exact" in rooflines else "tc"
+        if only is not None:
+            line_note = {"gemm_filter": sorted(only)}
+        else:
+            line_note = {}
         line = {
             "metric": METRIC, "value": _r(value), "unit": "GFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": _r(step_ms),
@@ -428,6 +441,7 @@ def main():
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clocks.summary(),
+            **line_note,
         }
         print(json.dumps(line), flush=True)
     if pg is not None:
