@@ -11,19 +11,30 @@
 //    output column count only; rows past M are zero-filled by TMA and their
 //    results dropped, so row i's instruction sequence is the same for every M;
 //  * each tile's reduction runs its k-blocks of 64 in ascending order, four
-//    K=16 MMAs per block in ascending order, into one TMEM accumulator;
-//    nothing is split across CTAs and no atomics are used;
+//    K=16 MMAs per block in ascending order, into one TMEM accumulator; the
+//    forward and dX reductions are never split; no atomics are used;
 //  * tile-to-CTA scheduling depends on M, the arithmetic of a row does not.
 //
-// Kernel structure (one CTA per SM, persistent over output tiles):
-//  warp 0     TMA producer: fills a ring of shared-memory stages (A 128x64 and
-//             B BNx64 bf16 tiles, 128-byte swizzle), mbarrier transaction counts
-//  warp 1     MMA issuer: allocates TMEM (two accumulators of BN columns),
-//             issues tcgen05.mma per stage, commits stage release and tile
-//             completion to mbarriers
-//  warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter of the
-//             accumulator, bias, bf16 rounding, global stores; while they
-//             drain one accumulator the MMA warp fills the other.
+// Kernels.
+//  tc_gemm_kernel (fwd, dX, and dW when its tile count fills the GPU): one CTA
+//  per SM, persistent over output tiles.
+//   warp 0     TMA producer: fills a ring of shared-memory stages (A 128x64,
+//              B BNx64 bf16, 128-byte swizzle), mbarrier transaction counts
+//   warp 1     MMA issuer: allocates TMEM (two accumulators of BN columns),
+//              issues tcgen05.mma per stage, commits stage release and tile
+//              completion to mbarriers
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter of the
+//              accumulator, bias from a shared-memory copy, one RNE rounding to
+//              bf16, 32x32 sub-tiles written to swizzled shared memory and
+//              stored by TMA; while they drain one accumulator the MMA warp
+//              fills the other.
+//  tc_dw_split_kernel (dW with few output tiles): the token (reduction) range
+//  is cut into s contiguous pieces of whole k-blocks, s depending only on the
+//  output tile count; the s CTAs of a thread-block cluster each reduce one
+//  piece of the same tile, park their fp32 partial in shared memory, and the
+//  partials are added in piece order (0, 1, ..., s-1) through distributed
+//  shared memory; each CTA rounds and stores 128/s rows.  No atomics, so the
+//  result is the same on every run.
 // Every mbarrier wait is bounded (device_sync.cuh); a wait that gives up
 // records CARBON_ERR_TIMEOUT, raises a CTA-wide abort flag so the other roles
 // leave their loops, and the TMEM allocation is still released.
@@ -57,16 +68,25 @@ struct TcArgs {
     const void *bias;         // bf16 [cols] or null (fwd only)
     int64_t rows, cols, R;
     int tiles_m, tiles_n, num_kb;
+    int splits, kb_per_split; // dW cluster split (tc_dw_split_kernel only)
 };
 
 template <int BN>
 struct Smem {
     static constexpr uint32_t kBBytes = BN * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kBarOffset = kStages * kStageBytes;
+    static constexpr uint32_t kPipeBytes = kStages * kStageBytes;
+    // epilogue staging: per epilogue warp two 32x32 bf16 sub-tiles (2 KiB each)
+    static constexpr uint32_t kStagingOffset = kPipeBytes;
+    static constexpr uint32_t kStagingBytes = kEpiWarps * 2 * 2048;
+    static constexpr uint32_t kBiasOffset = kStagingOffset + kStagingBytes;
+    static constexpr uint32_t kBarOffset = kBiasOffset + kEpiWarps * BN * 4;   // per-warp bias copy
     // full[S], empty[S], tfull[2], tempty[2], then tmem base slot and abort flag
     static constexpr uint32_t kBytes = kBarOffset + (2 * kStages + 4) * 8 + 16;
     static constexpr uint32_t kDynamic = kBytes + 1024;   // room to align the base to 1 KiB
+    // split kernel: fp32 partial tile [128][BN + 4] placed over the pipeline ring
+    static constexpr uint32_t kPartialPitch = BN + 4;
+    static_assert(kBM * kPartialPitch * 4 <= kPipeBytes, "partial tile must fit the ring");
 };
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -174,170 +194,389 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     return false;
 }
 
+// ---- more PTX wrappers: TMA store, bulk groups, proxies, clusters -----------
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(map), "r"(src), "r"(c0), "r"(c1) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most one committed bulk group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Make generic-proxy shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    float4 v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);     // RNE, one rounding each
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// ---- the roles shared by both kernels -----------------------------------------
+
+struct Bars {
+    uint32_t full0, empty0, tfull0, tempty0;
+    __device__ uint32_t full(int s) const { return full0 + 8u * s; }
+    __device__ uint32_t empty(int s) const { return empty0 + 8u * s; }
+    __device__ uint32_t tfull(int b) const { return tfull0 + 8u * b; }
+    __device__ uint32_t tempty(int b) const { return tempty0 + 8u * b; }
+};
+
+// Producer: k-blocks [kb0, kb1) of the tile at (m0, n0) into the ring.
+template <int BN, int A_MAJOR, int B_MAJOR>
+__device__ __forceinline__ bool produce_tile(const CUtensorMap *ma, const CUtensorMap *mb,
+                                             uint32_t sbase, const Bars &bar, int m0, int n0,
+                                             int kb0, int kb1, int &s, uint32_t &ph,
+                                             volatile uint32_t *abort_flag) {
+    using L = Smem<BN>;
+    for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_or_abort(bar.empty(s), ph ^ 1u, abort_flag)) return false;
+        mbar_arrive_expect_tx(bar.full(s), L::kStageBytes);
+        const uint32_t sa = sbase + s * L::kStageBytes, sb = sa + kABytes;
+        const int k0 = kb * kBK;
+        if (A_MAJOR == K_MAJOR) {
+            tma_load_2d(sa, ma, bar.full(s), k0, m0);
+        } else {
+            tma_load_2d(sa, ma, bar.full(s), m0, k0);
+            tma_load_2d(sa + kMNBlockBytes, ma, bar.full(s), m0 + 64, k0);
+        }
+        if (B_MAJOR == K_MAJOR) {
+            tma_load_2d(sb, mb, bar.full(s), k0, n0);
+        } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(sb + j * kMNBlockBytes, mb, bar.full(s), n0 + 64 * j, k0);
+        }
+        if (++s == kStages) { s = 0; ph ^= 1u; }
+    }
+    return true;
+}
+
+// Lets every load the producer issued land before the CTA may exit: a stage
+// armed in the last pass completes with parity ph; stages not armed in it
+// completed earlier, so their wait returns at once.
+__device__ __forceinline__ void drain_producer(const Bars &bar, int s, uint32_t ph) {
+    for (int i = 0; i < kStages; ++i) {
+        if (--s < 0) { s = kStages - 1; ph ^= 1u; }
+        if (!mbar_wait(bar.full(s), ph)) break;
+    }
+}
+
+// MMA issuer: nkb k-blocks from the ring into the accumulator at TMEM column d.
+template <int BN, int A_MAJOR, int B_MAJOR>
+__device__ __forceinline__ bool mma_tile(uint32_t d, uint32_t sbase, const Bars &bar, int nkb,
+                                         int &s, uint32_t &ph, volatile uint32_t *abort_flag) {
+    using L = Smem<BN>;
+    constexpr uint32_t idesc = instr_desc(BN, A_MAJOR, B_MAJOR);
+    for (int kb = 0; kb < nkb; ++kb) {
+        if (!wait_or_abort(bar.full(s), ph, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t sa = sbase + s * L::kStageBytes, sb = sa + kABytes;
+#pragma unroll
+        for (int k = 0; k < kBK / kUMMA_K; ++k)
+            mma_bf16(d, operand_desc<A_MAJOR>(sa, k), operand_desc<B_MAJOR>(sb, k), idesc,
+                     (kb | k) != 0 ? 1u : 0u);
+        mma_commit(bar.empty(s));                  // stage free once these MMAs finish
+        if (++s == kStages) { s = 0; ph ^= 1u; }
+    }
+    return true;
+}
+
+// Sets up barriers and TMEM; returns the TMEM base column address.
+template <int BN>
+__device__ __forceinline__ uint32_t setup_cta(uint8_t *smem, const Bars &bar,
+                                              const CUtensorMap *ma, const CUtensorMap *mb,
+                                              uint32_t *tmem_slot, volatile uint32_t *abort_flag,
+                                              uint32_t tmem_cols) {
+    const int warp = threadIdx.x / 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar.full(s), 1);
+            mbar_init(bar.empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar.tfull(b), 1);
+            mbar_init(bar.tempty(b), kEpiWarps);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+        prefetch_map(ma);
+        prefetch_map(mb);
+    }
+    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    return *tmem_slot;
+}
+
+// ---- persistent kernel (fwd, dX, dW without split) ----------------------------
+
 template <int BN, int A_MAJOR, int B_MAJOR, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-               const TcArgs p) {
+               const __grid_constant__ CUtensorMap map_out, const TcArgs p) {
     using L = Smem<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(smem);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOffset);
-    const uint32_t full0 = smem_addr(bars);
-    const uint32_t empty0 = full0 + 8 * kStages;
-    const uint32_t tfull0 = empty0 + 8 * kStages;
-    const uint32_t tempty0 = tfull0 + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * kStages + 4);
+    Bars bar;
+    bar.full0 = sbase + L::kBarOffset;
+    bar.empty0 = bar.full0 + 8 * kStages;
+    bar.tfull0 = bar.empty0 + 8 * kStages;
+    bar.tempty0 = bar.tfull0 + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + (2 * kStages + 4) * 8);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr uint32_t kTmemCols = 2 * BN;                 // 256 or 512: powers of two
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, kEpiWarps);
-        }
-        *abort_flag = 0u;
-        fence_mbar_init();
-        prefetch_map(&map_a);
-        prefetch_map(&map_b);
-    }
-    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t tmem_base = setup_cta<BN>(smem, bar, &map_a, &map_b, tmem_slot, abort_flag, kTmemCols);
     const int num_tiles = p.tiles_m * p.tiles_n;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
-                const int m0 = (t / p.tiles_n) * kBM, n0 = (t % p.tiles_n) * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    const uint32_t fb = full0 + 8 * s, eb = empty0 + 8 * s;
-                    if (!wait_or_abort(eb, ph ^ 1u, abort_flag)) break;
-                    mbar_arrive_expect_tx(fb, L::kStageBytes);
-                    const uint32_t sa = sbase + s * L::kStageBytes, sb = sa + kABytes;
-                    const int k0 = kb * kBK;
-                    if (A_MAJOR == K_MAJOR) {
-                        tma_load_2d(sa, &map_a, fb, k0, m0);
-                    } else {
-                        tma_load_2d(sa, &map_a, fb, m0, k0);
-                        tma_load_2d(sa + kMNBlockBytes, &map_a, fb, m0 + 64, k0);
-                    }
-                    if (B_MAJOR == K_MAJOR) {
-                        tma_load_2d(sb, &map_b, fb, k0, n0);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(sb + j * kMNBlockBytes, &map_b, fb, n0 + 64 * j, k0);
-                    }
-                    if (++s == kStages) { s = 0; ph ^= 1u; }
-                }
-            }
-            // let every load this thread issued land before the CTA can exit
-            for (int i = 0; i < kStages; ++i) {
-                if (--s < 0) { s = kStages - 1; ph ^= 1u; }
-                // a stage armed in this pass completes with parity ph; unarmed ones
-                // were completed earlier, so this wait returns at once either way
-                if (!mbar_wait(full0 + 8 * s, ph, kWaitBudgetNs)) break;
-            }
+            for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x)
+                if (!produce_tile<BN, A_MAJOR, B_MAJOR>(&map_a, &map_b, sbase, bar,
+                                                        (t / p.tiles_n) * kBM, (t % p.tiles_n) * BN,
+                                                        0, p.num_kb, s, ph, abort_flag))
+                    break;
+            drain_producer(bar, s, ph);
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA
         if (lane == 0) {
-            constexpr uint32_t idesc = instr_desc(BN, A_MAJOR, B_MAJOR);
             int s = 0, acc = 0;
             uint32_t ph = 0, aph = 0;
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
-                if (!wait_or_abort(tempty0 + 8 * acc, aph ^ 1u, abort_flag)) break;
+                if (!wait_or_abort(bar.tempty(acc), aph ^ 1u, abort_flag)) break;
                 tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-                bool ok = true;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_or_abort(full0 + 8 * s, ph, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sa = sbase + s * L::kStageBytes, sb = sa + kABytes;
-#pragma unroll
-                    for (int k = 0; k < kBK / kUMMA_K; ++k)
-                        mma_bf16(d, operand_desc<A_MAJOR>(sa, k), operand_desc<B_MAJOR>(sb, k),
-                                 idesc, (kb | k) != 0 ? 1u : 0u);
-                    mma_commit(empty0 + 8 * s);          // stage free once these MMAs finish
-                    if (++s == kStages) { s = 0; ph ^= 1u; }
-                }
-                if (!ok) break;
-                mma_commit(tfull0 + 8 * acc);            // accumulator ready
+                if (!mma_tile<BN, A_MAJOR, B_MAJOR>(tmem_base + (uint32_t)(acc * BN), sbase, bar,
+                                                    p.num_kb, s, ph, abort_flag))
+                    break;
+                mma_commit(bar.tfull(acc));            // accumulator ready
                 if (++acc == 2) { acc = 0; aph ^= 1u; }
             }
         }
     } else {
-        // ----------------------------------------------------------- epilogue
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;                         // 0..3
         const int quarter = warp % 4;                    // TMEM lanes 32*quarter .. +31
-        const int row_in_tile = quarter * 32 + lane;
-        int acc = 0;
+        const uint32_t stg = sbase + L::kStagingOffset + ew * 4096;
+        float *bias_s = reinterpret_cast<float *>(smem + L::kBiasOffset) + ew * BN;
+        const __nv_bfloat16 *bias = static_cast<const __nv_bfloat16 *>(p.bias);
+        int acc = 0, nstores = 0;
         uint32_t aph = 0;
         for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
-            const int64_t row = (int64_t)(t / p.tiles_n) * kBM + row_in_tile;
-            const int64_t n0 = (int64_t)(t % p.tiles_n) * BN;
-            if (!wait_or_abort(tfull0 + 8 * acc, aph, abort_flag)) break;
+            const int m0 = (t / p.tiles_n) * kBM;
+            const int n0 = (t % p.tiles_n) * BN;
+            if (bias) {                                   // this warp's copy of the tile's bias
+                __syncwarp();                             // the previous tile's reads are done
+                for (int i = lane; i < BN; i += 32)
+                    bias_s[i] = (n0 + i < p.cols) ? __bfloat162float(bias[n0 + i]) : 0.0f;
+                __syncwarp();
+            }
+            if (!wait_or_abort(bar.tfull(acc), aph, abort_flag)) break;
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
+                if (n0 + c >= p.cols) break;             // whole chunk past the last column
                 uint32_t v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c), v);
-                if (row < p.rows) {
-                    const int64_t col0 = n0 + c;
-                    float f[32];
+                float f[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-                    if (p.bias) {
-                        const __nv_bfloat16 *bp = static_cast<const __nv_bfloat16 *>(p.bias);
+                for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+                if (bias) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (col0 + i < p.cols) f[i] = __fadd_rn(f[i], __bfloat162float(bp[col0 + i]));
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 b4 = *reinterpret_cast<const float4 *>(bias_s + c + i);
+                        f[i] = __fadd_rn(f[i], b4.x);
+                        f[i + 1] = __fadd_rn(f[i + 1], b4.y);
+                        f[i + 2] = __fadd_rn(f[i + 2], b4.z);
+                        f[i + 3] = __fadd_rn(f[i + 3], b4.w);
                     }
-                    if (OUT_F32) {
-                        float *o = static_cast<float *>(p.out) + row * p.cols + col0;
+                }
+                if (OUT_F32) {                           // inspection path: direct fp32 stores
+                    const int64_t row = (int64_t)m0 + quarter * 32 + lane;
+                    if (row < p.rows) {
+                        float *o = static_cast<float *>(p.out) + row * p.cols + n0 + c;
 #pragma unroll
                         for (int g = 0; g < 8; ++g)
-                            if (col0 + 4 * g < p.cols)
+                            if (n0 + c + 4 * g < p.cols)
                                 *reinterpret_cast<float4 *>(o + 4 * g) =
                                     make_float4(f[4 * g], f[4 * g + 1], f[4 * g + 2], f[4 * g + 3]);
-                    } else {
-                        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + row * p.cols + col0;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            if (col0 + 8 * g >= p.cols) continue;   // cols is a multiple of 8
-                            uint4 w;
-                            __nv_bfloat162 h;
-                            h = __floats2bfloat162_rn(f[8 * g + 0], f[8 * g + 1]); w.x = *reinterpret_cast<uint32_t *>(&h);
-                            h = __floats2bfloat162_rn(f[8 * g + 2], f[8 * g + 3]); w.y = *reinterpret_cast<uint32_t *>(&h);
-                            h = __floats2bfloat162_rn(f[8 * g + 4], f[8 * g + 5]); w.z = *reinterpret_cast<uint32_t *>(&h);
-                            h = __floats2bfloat162_rn(f[8 * g + 6], f[8 * g + 7]); w.w = *reinterpret_cast<uint32_t *>(&h);
-                            *reinterpret_cast<uint4 *>(o + 8 * g) = w;
-                        }
                     }
+                } else {
+                    // 32 rows x 64 bytes, 16-byte pieces swizzled as TMA's 64-byte mode
+                    // expects (piece index ^= (row >> 1) & 3): conflict-free v4 stores.
+                    const uint32_t buf = stg + (uint32_t)(nstores & 1) * 2048u;
+                    if (nstores >= 2 && lane == 0) bulk_wait_read_1();
+                    __syncwarp();
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint4 w;
+                        w.x = pack_bf16x2(f[8 * g + 0], f[8 * g + 1]);
+                        w.y = pack_bf16x2(f[8 * g + 2], f[8 * g + 3]);
+                        w.z = pack_bf16x2(f[8 * g + 4], f[8 * g + 5]);
+                        w.w = pack_bf16x2(f[8 * g + 6], f[8 * g + 7]);
+                        st_shared_v4(buf + lane * 64 + 16 * (g ^ ((lane >> 1) & 3)), w);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&map_out, buf, n0 + c, m0 + quarter * 32);   // clipped at rows/cols
+                        bulk_commit();
+                    }
+                    ++nstores;
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            if (lane == 0) mbar_arrive(bar.tempty(acc));
             if (++acc == 2) { acc = 0; aph ^= 1u; }
         }
+        if (!OUT_F32 && lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
     __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---- dW with few tiles: token range split over a cluster --------------------
+
+template <int BN, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const TcArgs p) {
+    using L = Smem<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    Bars bar;
+    bar.full0 = sbase + L::kBarOffset;
+    bar.empty0 = bar.full0 + 8 * kStages;
+    bar.tfull0 = bar.empty0 + 8 * kStages;
+    bar.tempty0 = bar.tfull0 + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + (2 * kStages + 4) * 8);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+    constexpr uint32_t kTmemCols = BN;                     // one accumulator: 128 or 256 columns
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t tmem_base = setup_cta<BN>(smem, bar, &map_a, &map_b, tmem_slot, abort_flag, kTmemCols);
+
+    const int piece = (int)cluster_rank();                 // == blockIdx.x
+    const int t = blockIdx.y;
+    const int m0 = (t / p.tiles_n) * kBM, n0 = (t % p.tiles_n) * BN;
+    const int kb0 = piece * p.kb_per_split;
+    const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+    const int nkb = kb1 > kb0 ? kb1 - kb0 : 0;
+    float *part = reinterpret_cast<float *>(smem);          // [128][BN + 4] over the ring
+
+    if (warp == 0) {
+        if (lane == 0 && nkb > 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            produce_tile<BN, MN_MAJOR, MN_MAJOR>(&map_a, &map_b, sbase, bar, m0, n0, kb0, kb1, s, ph,
+                                                 abort_flag);
+            drain_producer(bar, s, ph);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && nkb > 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            if (mma_tile<BN, MN_MAJOR, MN_MAJOR>(tmem_base, sbase, bar, nkb, s, ph, abort_flag))
+                mma_commit(bar.tfull(0));
+        }
+    } else {
+        const int quarter = warp % 4;
+        const int row = quarter * 32 + lane;
+        bool have = nkb > 0;
+        if (have) {
+            have = wait_or_abort(bar.tfull(0), 0, abort_flag);
+            tc_fence_after();
+        }
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+            uint32_t v[32];
+            if (have) tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
+            float *dst = part + row * L::kPartialPitch + c;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4 *>(dst + i) =
+                    have ? make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                       __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();                                    // every partial is parked
+
+    // piece r rounds and stores rows [r*128/s, (r+1)*128/s) of the tile,
+    // adding the partials in piece order 0, 1, ..., s-1
+    const int rows_per = kBM / p.splits;
+    const int r0 = piece * rows_per;
+    const int nvec = rows_per * (BN / 4);
+    const uint32_t part_addr = smem_addr(part);
+    for (int idx = threadIdx.x; idx < nvec; idx += kThreads) {
+        const int rr = r0 + idx / (BN / 4);
+        const int cc = (idx % (BN / 4)) * 4;
+        const int64_t grow = (int64_t)m0 + rr, gcol = (int64_t)n0 + cc;
+        if (grow >= p.rows || gcol >= p.cols) continue;
+        const uint32_t off = part_addr + (uint32_t)(rr * L::kPartialPitch + cc) * 4u;
+        float4 a = ld_cluster_f4(off, 0);
+        for (int q = 1; q < p.splits; ++q) {
+            const float4 b = ld_cluster_f4(off, (uint32_t)q);
+            a.x = __fadd_rn(a.x, b.x);
+            a.y = __fadd_rn(a.y, b.y);
+            a.z = __fadd_rn(a.z, b.z);
+            a.w = __fadd_rn(a.w, b.w);
+        }
+        if (OUT_F32) {
+            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + grow * p.cols + gcol) = a;
+        } else {
+            uint2 w;
+            w.x = pack_bf16x2(a.x, a.y);
+            w.y = pack_bf16x2(a.z, a.w);
+            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) + grow * p.cols + gcol) = w;
+        }
+    }
+    cluster_sync_all();                                    // peers are done reading this CTA
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
@@ -377,42 +616,84 @@ cudaError_t get_encoder() {
 }
 
 // 2-D bf16 tensor map over a row-major [outer, inner] matrix with a
-// {64, box_outer} box and 128-byte swizzle; out-of-range elements read as 0.
-bool encode_map(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int box_outer) {
+// {box_inner, box_outer} box; out-of-range elements read as 0 and are not
+// written by stores.
+bool encode_map(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int box_inner,
+                int box_outer, CUtensorMapSwizzle swizzle) {
     cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
     cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)box_outer};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
     cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
-                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
+bool encode_operand(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int box_outer) {
+    return encode_map(map, base, inner, outer, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <typename Kern>
+cudaError_t prepare(Kern kern, int smem) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
 template <int BN, int AM, int BM_, bool F32>
-cudaError_t launch_kernel(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
-                          int grid, cudaStream_t stream) {
+cudaError_t launch_persistent(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mo,
+                              const TcArgs &a, int grid, cudaStream_t stream) {
     auto kern = tc_gemm_kernel<BN, AM, BM_, F32>;
     const int smem = (int)Smem<BN>::kDynamic;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t err = prepare(kern, smem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, smem, stream>>>(ma, mb, a);
+    kern<<<grid, kThreads, smem, stream>>>(ma, mb, mo, a);
     return cudaGetLastError();
 }
 
 template <int BN, bool F32>
-cudaError_t launch_pass(int pass, const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
-                        int grid, cudaStream_t s) {
+cudaError_t launch_persistent_pass(int pass, const CUtensorMap &ma, const CUtensorMap &mb,
+                                   const CUtensorMap &mo, const TcArgs &a, int grid, cudaStream_t s) {
     switch (pass) {
-    case CARBON_PASS_FWD: return launch_kernel<BN, K_MAJOR, MN_MAJOR, F32>(ma, mb, a, grid, s);
-    case CARBON_PASS_DX:  return launch_kernel<BN, K_MAJOR, K_MAJOR, F32>(ma, mb, a, grid, s);
-    default:              return launch_kernel<BN, MN_MAJOR, MN_MAJOR, F32>(ma, mb, a, grid, s);
+    case CARBON_PASS_FWD: return launch_persistent<BN, K_MAJOR, MN_MAJOR, F32>(ma, mb, mo, a, grid, s);
+    case CARBON_PASS_DX:  return launch_persistent<BN, K_MAJOR, K_MAJOR, F32>(ma, mb, mo, a, grid, s);
+    default:              return launch_persistent<BN, MN_MAJOR, MN_MAJOR, F32>(ma, mb, mo, a, grid, s);
     }
+}
+
+template <int BN, bool F32>
+cudaError_t launch_split(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
+                         cudaStream_t stream) {
+    auto kern = tc_dw_split_kernel<BN, F32>;
+    const int smem = (int)Smem<BN>::kDynamic;
+    cudaError_t err = prepare(kern, smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.splits, (unsigned)(a.tiles_m * a.tiles_n), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, a);
 }
 
 // Output-tile width from the output column count only (never from M).
 int choose_bn(int64_t cols) { return cols <= 128 ? 128 : 256; }
+
+// dW split count from the output tile count only: the largest s in
+// {1, 2, 4, 8} with tiles * s <= 152 (GB300's SM count, fixed here so the
+// bits do not depend on the device a run lands on).
+int choose_splits(int64_t tiles) {
+    int s = 1;
+    while (s < 8 && tiles * (2 * s) <= 152) s *= 2;
+    return s;
+}
 
 }  // namespace
 
@@ -442,20 +723,23 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
     if (err != cudaSuccess) return note_cuda(err);
 
     const int bn = choose_bn(p.cols);
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mo;
     bool ok;
     switch (p.pass) {
     case CARBON_PASS_FWD:   // A = X [M, K] K-major; B = W [K, N] N-contiguous (MN-major)
-        ok = encode_map(&ma, p.A, p.K, p.M, kBM) && encode_map(&mb, p.B, p.N, p.K, 64);
+        ok = encode_operand(&ma, p.A, p.K, p.M, kBM) && encode_operand(&mb, p.B, p.N, p.K, 64);
         break;
     case CARBON_PASS_DX:    // A = dY [M, N] K-major; B = W [K, N]: rows = out cols, K-major
-        ok = encode_map(&ma, p.A, p.N, p.M, kBM) && encode_map(&mb, p.B, p.N, p.K, bn);
+        ok = encode_operand(&ma, p.A, p.N, p.M, kBM) && encode_operand(&mb, p.B, p.N, p.K, bn);
         break;
     default:                // A = X [M, K] and B = dY [M, N], both MN-major
-        ok = encode_map(&ma, p.A, p.K, p.M, 64) && encode_map(&mb, p.B, p.N, p.M, 64);
+        ok = encode_operand(&ma, p.A, p.K, p.M, 64) && encode_operand(&mb, p.B, p.N, p.M, 64);
         break;
     }
+    // output [rows, cols] bf16, 32x32 boxes, 64-byte swizzle (epilogue staging layout)
+    ok = ok && (out_f32 || encode_map(&mo, p.out, p.cols, p.rows, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B));
     if (!ok) return CARBON_ERR_MISALIGNED;
+    if (out_f32) mo = ma;                                // unused by the fp32 inspection path
 
     TcArgs a;
     a.out = p.out; a.bias = p.bias;
@@ -463,16 +747,32 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
     a.tiles_m = (int)((p.rows + kBM - 1) / kBM);
     a.tiles_n = (int)((p.cols + bn - 1) / bn);
     a.num_kb = (int)((p.R + kBK - 1) / kBK);
+    a.splits = 1;
+    a.kb_per_split = a.num_kb;
     const int64_t tiles = (int64_t)a.tiles_m * a.tiles_n;
-    if (tiles > (int64_t)0x7fffffff) return CARBON_ERR_INVALID_ARG;
-    const int grid = (int)(tiles < sms ? tiles : sms);
+    if (tiles > 65535) {
+        if (tiles > (int64_t)0x7fffffff) return CARBON_ERR_INVALID_ARG;
+    }
 
-    if (bn == 128)
-        err = out_f32 ? launch_pass<128, true>(p.pass, ma, mb, a, grid, stream)
-                      : launch_pass<128, false>(p.pass, ma, mb, a, grid, stream);
-    else
-        err = out_f32 ? launch_pass<256, true>(p.pass, ma, mb, a, grid, stream)
-                      : launch_pass<256, false>(p.pass, ma, mb, a, grid, stream);
+    if (p.pass == CARBON_PASS_DW) {
+        a.splits = choose_splits(tiles);
+        if (a.splits > a.num_kb) a.splits = 1;
+        a.kb_per_split = (a.num_kb + a.splits - 1) / a.splits;
+    }
+    if (a.splits > 1) {
+        if (bn == 128)
+            err = out_f32 ? launch_split<128, true>(ma, mb, a, stream) : launch_split<128, false>(ma, mb, a, stream);
+        else
+            err = out_f32 ? launch_split<256, true>(ma, mb, a, stream) : launch_split<256, false>(ma, mb, a, stream);
+    } else {
+        const int grid = (int)(tiles < sms ? tiles : sms);
+        if (bn == 128)
+            err = out_f32 ? launch_persistent_pass<128, true>(p.pass, ma, mb, mo, a, grid, stream)
+                          : launch_persistent_pass<128, false>(p.pass, ma, mb, mo, a, grid, stream);
+        else
+            err = out_f32 ? launch_persistent_pass<256, true>(p.pass, ma, mb, mo, a, grid, stream)
+                          : launch_persistent_pass<256, false>(p.pass, ma, mb, mo, a, grid, stream);
+    }
     count_launch();
     return note_cuda(err);
 }

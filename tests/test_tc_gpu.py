@@ -99,6 +99,22 @@ def test_small_integer_inputs_accumulate_exactly():
         assert np.array_equal(acc, exact), f"{pass_}: {np.count_nonzero(acc != exact)} wrong"
 
 
+@pytest.mark.parametrize("M,K,N", [(2048, 256, 256), (4000, 384, 200), (1100, 128, 1024)])
+def test_dw_token_split_accumulates_exactly(M, K, N):
+    """dW shapes with few output tiles take the cluster split of the token
+    range; with small-integer operands every partial and their in-order sum
+    are exact, so the result must equal the exact product."""
+    rng = np.random.default_rng(M)
+    X = inputs.f32_to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    dY = inputs.f32_to_bf16_bits(rng.integers(-4, 5, size=(M, N)).astype(np.float32))
+    acc = run_tc("dw", X, dY, None, M, K, N, f32=True).cpu().numpy().astype(np.float64)
+    exact = f64(X).T @ f64(dY)
+    assert np.array_equal(acc, exact), f"{np.count_nonzero(acc != exact)} wrong"
+    out = host_bits(run_tc("dw", X, dY, None, M, K, N))
+    again = host_bits(run_tc("dw", X, dY, None, M, K, N))
+    assert np.array_equal(out, again)
+
+
 @pytest.mark.parametrize("M,K,N", [(128, 64, 128), (7, 768, 768), (513, 256, 2304),
                                    (300, 3072, 136), (64, 1000, 264)])
 def test_tolerance_all_passes(M, K, N):
