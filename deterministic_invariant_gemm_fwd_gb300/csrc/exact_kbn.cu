@@ -30,6 +30,20 @@
 //    plain algorithm's.  The choice is applied with predicated selects
 //    (a1, a2) = (s, 1) or (x, w), never with a branch, so a warp whose lanes
 //    disagree issues the four float64 instructions once.
+//  * Most KBN steps on bf16 data do not round at all: a bf16 x bf16 product
+//    has at most 16 significant bits, so s + p is usually representable and
+//    the correction term is exactly 0.  The kernel first runs each 32-deep
+//    slice of the reduction issuing only t = fma(x, w, s) per step, together
+//    with an integer proof that the step was exact: s is always an integer
+//    multiple of 2^L, where L is the lowest set-bit exponent over the chunk's
+//    products so far (true for the sums of the plain algorithm too: rounding
+//    to a coarser grid keeps multiples of 2^L), and the product is a multiple
+//    of 2^(L(x) + L(w)); if both are multiples of ulp(t), then s + p = t
+//    exactly, the correction is 0 and c is unchanged -- the same bits the
+//    full step produces.  If any lane of the warp cannot prove every step of
+//    the slice, the warp restores its state at the slice start and runs the
+//    slice with the full four-instruction step.  Either way the bits are the
+//    plain algorithm's.
 //  * Every output is owned by one thread (output-stationary), so the
 //    summation order is the documented one by construction, for every M.
 // Zero padding of ragged tiles is exact: adding a +0 product leaves s and c
@@ -70,6 +84,39 @@ __device__ __forceinline__ double widen(uint32_t f) {
     }
     if (mag == 0u) return __hiloint2double((int)(f & 0x80000000u), 0);
     return (double)__uint_as_float(f);
+}
+
+// Grain keys for the exactness proof, kept shifted left by 20 so they compare
+// directly with a double's exponent field (hi word & 0x7ff00000).
+// For a nonzero finite operand v, L(v) is the exponent of its lowest set bit.
+// A-side key: (L(x) + 1075) << 20; B-side key: L(w) << 20.  Their sum G is
+// the biased exponent field of 2^(L(x) + L(w) + 52): the step is exact when
+// the result's exponent field is <= min(G) over the chunk so far.
+// Zeros get keys that never lower the minimum; non-finite operands get keys
+// that always fail the proof (the full step then handles them).
+constexpr int kGrainZeroA = 0x58000000;
+constexpr int kGrainZeroB = 0x20000000;
+constexpr int kGrainBad = -0x40000000;
+
+__device__ __forceinline__ int lsb_exponent(double v) {
+    const unsigned long long u = (unsigned long long)__double_as_longlong(v);
+    const int f = (int)((u >> 52) & 0x7ffull);
+    const unsigned long long mant = u & 0x000fffffffffffffull;
+    return mant ? (f - 1023 - 52 + __ffsll((long long)mant) - 1) : (f - 1023);
+}
+
+__device__ __forceinline__ int grain_key_a(double v) {
+    const uint32_t f = ((uint32_t)__double2hiint(v) >> 20) & 0x7ffu;
+    if (f == 0x7ffu) return kGrainBad;
+    if (v == 0.0) return kGrainZeroA;
+    return (lsb_exponent(v) + 1075) << 20;
+}
+
+__device__ __forceinline__ int grain_key_b(double v) {
+    const uint32_t f = ((uint32_t)__double2hiint(v) >> 20) & 0x7ffu;
+    if (f == 0x7ffu) return kGrainBad;
+    if (v == 0.0) return kGrainZeroB;
+    return lsb_exponent(v) << 20;
 }
 
 template <int DT>
@@ -142,7 +189,8 @@ __device__ __forceinline__ unsigned short round_bf16(double y) {
 
 template <int DT, int PASS>
 __device__ __forceinline__ void stage_slice(const KArgs &p, double (*As)[kBM + 1],
-                                            double (*Bs)[kBN + 1], int64_t i0, int64_t j0,
+                                            double (*Bs)[kBN + 1], int (*Ag)[kBM + 1],
+                                            int (*Bg)[kBN + 1], int64_t i0, int64_t j0,
                                             int64_t r0, int64_t rend, int tid) {
 #pragma unroll
     for (int l = 0; l < (kBK * kBM) / kThreads; ++l) {
@@ -154,6 +202,7 @@ __device__ __forceinline__ void stage_slice(const KArgs &p, double (*As)[kBM + 1
         double v = 0.0;
         if (i < p.rows && r < rend) v = widen(load_bits<DT>(p.A, i * p.a_si + r * p.a_sr));
         As[rr][ii] = v;
+        Ag[rr][ii] = grain_key_a(v);
     }
 #pragma unroll
     for (int l = 0; l < (kBK * kBN) / kThreads; ++l) {
@@ -165,6 +214,7 @@ __device__ __forceinline__ void stage_slice(const KArgs &p, double (*As)[kBM + 1
         double v = 0.0;
         if (j < p.cols && r < rend) v = widen(load_bits<DT>(p.B, r * p.b_sr + j * p.b_sj));
         Bs[rr][jj] = v;
+        Bg[rr][jj] = grain_key_b(v);
     }
 }
 
@@ -173,6 +223,8 @@ __global__ void __launch_bounds__(kThreads)
 exact_kbn_kernel(const KArgs p) {
     __shared__ double As[kBK][kBM + 1];
     __shared__ double Bs[kBK][kBN + 1];
+    __shared__ int Ag[kBK][kBM + 1];
+    __shared__ int Bg[kBK][kBN + 1];
     const int tid = threadIdx.x;
     const int tx = tid % kTX, ty = tid / kTX;
     const int64_t tile = blockIdx.x;
@@ -188,34 +240,80 @@ exact_kbn_kernel(const KArgs p) {
     for (int64_t q0 = 0; q0 < p.R; q0 += kChunk) {
         const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
         double s[kTM][kTN], c[kTM][kTN];
+        int g[kTM][kTN];                     // min grain key over the chunk so far
 #pragma unroll
         for (int m = 0; m < kTM; ++m)
 #pragma unroll
-            for (int n = 0; n < kTN; ++n) { s[m][n] = 0.0; c[m][n] = 0.0; }
+            for (int n = 0; n < kTN; ++n) { s[m][n] = 0.0; c[m][n] = 0.0; g[m][n] = 0x7fffffff; }
+        bool try_fast = true;                // warp-uniform
 
         for (int64_t r0 = q0; r0 < qend; r0 += kBK) {
             __syncthreads();
-            stage_slice<DT, PASS>(p, As, Bs, i0, j0, r0, qend, tid);
+            stage_slice<DT, PASS>(p, As, Bs, Ag, Bg, i0, j0, r0, qend, tid);
             __syncthreads();
-#pragma unroll 4
-            for (int k = 0; k < kBK; ++k) {
-                double a[kTM], b[kTN];
-                uint32_t ak[kTM], bk[kTN];
-#pragma unroll
-                for (int m = 0; m < kTM; ++m) {
-                    a[m] = As[k][ty + kTY * m];
-                    ak[m] = (uint32_t)__double2hiint(a[m]) & 0x7ff00000u;
-                }
-#pragma unroll
-                for (int n = 0; n < kTN; ++n) {
-                    b[n] = Bs[k][tx + kTX * n];
-                    bk[n] = (uint32_t)__double2hiint(b[n]) & 0x7ff00000u;
-                }
+
+            bool slow = !try_fast;
+            if (try_fast) {
+                // fast attempt: one DFMA per step plus the integer exactness proof
+                double s0[kTM][kTN];
+                int g0[kTM][kTN];
 #pragma unroll
                 for (int m = 0; m < kTM; ++m)
 #pragma unroll
-                    for (int n = 0; n < kTN; ++n)
-                        kbn_product_step(s[m][n], c[m][n], a[m], b[n], ak[m] + bk[n]);
+                    for (int n = 0; n < kTN; ++n) { s0[m][n] = s[m][n]; g0[m][n] = g[m][n]; }
+                int bad = 0;
+#pragma unroll 4
+                for (int k = 0; k < kBK; ++k) {
+                    double a[kTM], b[kTN];
+                    int ga[kTM], gb[kTN];
+#pragma unroll
+                    for (int m = 0; m < kTM; ++m) { a[m] = As[k][ty + kTY * m]; ga[m] = Ag[k][ty + kTY * m]; }
+#pragma unroll
+                    for (int n = 0; n < kTN; ++n) { b[n] = Bs[k][tx + kTX * n]; gb[n] = Bg[k][tx + kTX * n]; }
+#pragma unroll
+                    for (int m = 0; m < kTM; ++m)
+#pragma unroll
+                        for (int n = 0; n < kTN; ++n) {
+                            s[m][n] = __fma_rn(a[m], b[n], s[m][n]);
+                            g[m][n] = min(g[m][n], ga[m] + gb[n]);
+                            bad |= (__double2hiint(s[m][n]) & 0x7ff00000) > g[m][n];
+                        }
+                }
+                if (__any_sync(0xffffffffu, bad)) {
+#pragma unroll
+                    for (int m = 0; m < kTM; ++m)
+#pragma unroll
+                        for (int n = 0; n < kTN; ++n) { s[m][n] = s0[m][n]; g[m][n] = g0[m][n]; }
+                    slow = true;
+                    try_fast = false;        // rest of this chunk: straight to the full step
+                }
+            }
+            if (slow) {
+#pragma unroll 4
+                for (int k = 0; k < kBK; ++k) {
+                    double a[kTM], b[kTN];
+                    uint32_t ak[kTM], bk[kTN];
+                    int ga[kTM], gb[kTN];
+#pragma unroll
+                    for (int m = 0; m < kTM; ++m) {
+                        a[m] = As[k][ty + kTY * m];
+                        ak[m] = (uint32_t)__double2hiint(a[m]) & 0x7ff00000u;
+                        ga[m] = Ag[k][ty + kTY * m];
+                    }
+#pragma unroll
+                    for (int n = 0; n < kTN; ++n) {
+                        b[n] = Bs[k][tx + kTX * n];
+                        bk[n] = (uint32_t)__double2hiint(b[n]) & 0x7ff00000u;
+                        gb[n] = Bg[k][tx + kTX * n];
+                    }
+#pragma unroll
+                    for (int m = 0; m < kTM; ++m)
+#pragma unroll
+                        for (int n = 0; n < kTN; ++n) {
+                            kbn_product_step(s[m][n], c[m][n], a[m], b[n], ak[m] + bk[n]);
+                            g[m][n] = min(g[m][n], ga[m] + gb[n]);
+                        }
+                }
             }
         }
 #pragma unroll

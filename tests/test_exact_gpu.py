@@ -241,3 +241,40 @@ def test_fp64_rate_microbenchmark_is_sane():
     # GB300: a few lanes per SM per clock; nominal 1.25 TFLOP/s = 0.6e12 DFMA/s
     assert 1e11 < dfma < 5e12
     assert 1e11 < dadd < 5e12
+
+
+# ------------------------------------------- fast path / full step boundary
+
+def _adversarial(kind, rng, shape):
+    """Operands that make some KBN steps round and others not (the kernel
+    proves exactness per 32-deep slice and falls back to the full step)."""
+    if kind == "wide":        # bf16 values spread over 2^-60 .. 2^60
+        v = np.ldexp(1.0, rng.integers(-60, 61, shape)) * (1 + rng.integers(0, 128, shape) / 128.0)
+        return v * rng.choice([-1.0, 1.0], shape)
+    if kind == "rare_tiny":   # normal data with rare tiny entries
+        v = rng.standard_normal(shape)
+        flat = v.reshape(-1)
+        flat[rng.integers(0, flat.size, max(1, flat.size // 500))] *= 2.0 ** -45
+        return v
+    if kind == "growing":     # magnitudes growing along the reduction
+        v = rng.standard_normal(shape)
+        return v * np.ldexp(1.0, (np.arange(v.size) % 97 // 6).reshape(shape))
+    if kind == "integers":    # small integers: every step exact
+        return rng.integers(-8, 9, shape).astype(np.float64)
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("kind", ["wide", "rare_tiny", "growing", "integers"])
+def test_exactness_proof_boundaries(kind, dtype):
+    rng = np.random.default_rng(hash(kind) % 1000 + (dtype == "f32"))
+    M, K, N = 70, 600, 45
+    enc = (lambda a: a.astype(np.float32)) if dtype == "f32" else \
+        (lambda a: inputs.f32_to_bf16_bits(a.astype(np.float32)))
+    X = enc(_adversarial(kind, rng, (M, K)))
+    W = enc(_adversarial(kind, rng, (K, N)) * 0.02)
+    dY = enc(_adversarial(kind, rng, (M, N)) * 1e-3)
+    b = enc(rng.standard_normal(N) * 0.02)
+    check_dense("fwd", dtype, X, W, b, M, K, N)
+    check_dense("dx", dtype, dY, W, None, M, K, N)
+    check_dense("dw", dtype, X, dY, None, M, K, N)
