@@ -38,9 +38,11 @@ LAYERS = ((768, 2304), (768, 768), (768, 3072), (3072, 768))
 TOKENS = 8192
 SEED = 42
 PASSES = ("fwd", "dx", "dw")
-# float64 instructions one KBN step of the exact tier issues (DFMA for the
-# running sum, two for Fast2Sum's exact error, one DADD for the compensation)
-FP64_OPS_PER_MAC = 4
+# Floor of float64 instructions per multiply-add on the exact tier: every KBN
+# step needs at least the rounded addition t = fl(s + x*w) (one DFMA, the
+# product folded in).  The full step costs 4; the kernel issues 1 wherever it
+# can prove the step does not round (then the correction is exactly 0).
+FP64_OPS_PER_MAC = 1
 
 
 def _r(x, n=4):
@@ -435,8 +437,9 @@ def main():
                 "bound": "alu", "unit": "TFLOP/s", "achieved": _r(achieved), "peak": _r(peak),
                 "frac": _r(achieved / peak), "traffic": None,
                 "kernel": "exact_kbn_kernel",
-                "note": ("float64 lane operations: 4 per KBN step; peak = DFMA lane rate "
-                         "measured live by carbon_measure_fp64_rate (of measured)"),
+                "note": ("useful multiply-adds x 1 float64 lane-op (the DFMA every KBN step "
+                         "needs) per second; peak = DFMA lane rate measured live by "
+                         "carbon_measure_fp64_rate (of measured)"),
                 "useful_gflops": tier_info[t]["gflops"],
                 "survey_5op_utilisation": _r(5 * (fl_all / 2.0) / (ms * 1e-3) / fp64_rate)}
         else:
