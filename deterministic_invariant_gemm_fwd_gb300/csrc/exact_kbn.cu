@@ -105,17 +105,22 @@ __device__ __forceinline__ int lsb_exponent(double v) {
     return mant ? (f - 1023 - 52 + __ffsll((long long)mant) - 1) : (f - 1023);
 }
 
+// Zero test on the bit pattern: a float64 compare would run on the FP64 pipe.
+__device__ __forceinline__ bool is_zero_bits(double v) {
+    return (((uint32_t)__double2hiint(v) & 0x7fffffffu) | (uint32_t)__double2loint(v)) == 0u;
+}
+
 __device__ __forceinline__ int grain_key_a(double v) {
     const uint32_t f = ((uint32_t)__double2hiint(v) >> 20) & 0x7ffu;
     if (f == 0x7ffu) return kGrainBad;
-    if (v == 0.0) return kGrainZeroA;
+    if (is_zero_bits(v)) return kGrainZeroA;
     return (lsb_exponent(v) + 1075) << 20;
 }
 
 __device__ __forceinline__ int grain_key_b(double v) {
     const uint32_t f = ((uint32_t)__double2hiint(v) >> 20) & 0x7ffu;
     if (f == 0x7ffu) return kGrainBad;
-    if (v == 0.0) return kGrainZeroB;
+    if (is_zero_bits(v)) return kGrainZeroB;
     return lsb_exponent(v) << 20;
 }
 
