@@ -91,7 +91,9 @@ carbon_status_t run(const Problem &p, int tier, int debug_out, carbon_stream_t s
     st = current_device(nullptr, nullptr);
     if (st != CARBON_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (tier == CARBON_TIER_EXACT) return exact_launch(p, debug_out != 0, s);
+    if (tier == CARBON_TIER_EXACT)
+        return p.dtype == CARBON_BF16 ? exact_int_launch(p, debug_out != 0, s)
+                                      : exact_launch(p, debug_out != 0, s);
     return tc_launch(p, debug_out != 0, s);
 }
 

@@ -50,6 +50,8 @@ carbon_status_t current_device(int *device, int *sm_count);
 
 // Exact tier (exact_kbn.cu).  out_f64 selects the float64 pre-rounding output.
 carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream);
+// bf16 exact tier on the integer pipes (exact_int.cu); same bits.
+carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t stream);
 carbon_status_t exact_round_launch(int dtype, void *out, const double *in, int64_t n,
                                    cudaStream_t stream);
 
