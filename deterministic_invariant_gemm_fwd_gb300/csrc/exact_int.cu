@@ -29,6 +29,13 @@
 // The outer sum over chunk values uses one DADD per chunk when an integer proof
 // shows the addition is exact (both addends are multiples of ulp of the
 // result, by the same grain argument as exact_kbn.cu), else the full KBN step.
+//
+// Structure.  int_prep_kernel converts each operand once into the int32
+// operands of every (line, chunk) and that group's base and width (a
+// stream-ordered workspace of 4 bytes per operand element, allocated and
+// freed on the caller's stream); exact_int_kernel then streams 32-deep int32
+// slices with cp.async (double-buffered) into IMAD.WIDE accumulators, one
+// 64x64 output tile per CTA, 4x4 outputs per thread.
 #include "carbon_internal.h"
 #include "exact_common.cuh"
 
@@ -36,7 +43,6 @@ namespace carbon {
 namespace {
 
 constexpr int kChunk = 256;
-constexpr int kHalf = 128;                 // reduction rows staged at a time
 constexpr int kTile = 64;                  // CTA output tile: 64 x 64
 constexpr int kThreads = 256;              // 16 x 16 threads, 4 x 4 outputs each
 constexpr int kPitch = kTile + 4;          // int32 row pitch of the staged tiles
@@ -180,135 +186,199 @@ __device__ __forceinline__ void gather_stats(const unsigned short *base, int64_t
     }
 }
 
-// Integer operands of one staged half: T[r - r0][l] = m * 2^(e - base(l)),
-// or 0 for lines too wide for int32 (those outputs never use the integer sum).
+// ---- pre-pass: int32 operands and (base, width) per (line, chunk) ------------
+
+// T[r * Lp + line] = m * 2^(e - base(line, chunk of r)) for lines whose width
+// fits int32, else 0 (those outputs never use the integer sum).  Rows past R,
+// up to the padded length Rp, and lines past nlines are 0.
 template <bool LINE_CONTIG>
-__device__ __forceinline__ void stage_ints(const unsigned short *base, int64_t line_stride,
-                                           int64_t r_stride, int64_t line0, int64_t nlines,
-                                           int64_t r0, int64_t rend, const int *lbase,
-                                           const int *lwidth, int (*T)[kPitch], int tid) {
-#pragma unroll 4
-    for (int l8 = 0; l8 < (kHalf * kTile) / kThreads; ++l8) {
-        const int e = tid + kThreads * l8;
-        int l, rr;
-        if (LINE_CONTIG) { l = e % kTile; rr = e / kTile; }
-        else             { rr = e % kHalf; l = e / kHalf; }
-        const int64_t line = line0 + l, r = r0 + rr;
+__global__ void __launch_bounds__(kThreads)
+int_prep_kernel(const unsigned short *src, int64_t line_stride, int64_t r_stride, int64_t nlines,
+                int64_t R, int64_t Rp, int64_t Lp, int *T, int2 *stats) {
+    __shared__ LineStats st;
+    __shared__ int lbase[kTile], lwidth[kTile];
+    __shared__ unsigned short raw[kTile][kChunk + 2];     // transpose buffer (reduction-contiguous sources)
+    const int tid = threadIdx.x;
+    const int64_t line0 = (int64_t)blockIdx.x * kTile;
+    const int64_t q0 = (int64_t)blockIdx.y * kChunk;
+    const int64_t qend = (R - q0 > kChunk) ? q0 + kChunk : R;
+    const int64_t rtop = (Rp - q0 > kChunk) ? q0 + kChunk : Rp;
+
+    if (tid < kTile) { st.emin[tid] = 1 << 20; st.emax[tid] = -(1 << 20); st.bad[tid] = 0; }
+    __syncthreads();
+    gather_stats<LINE_CONTIG>(src, line_stride, r_stride, line0, nlines, q0, qend, st, tid);
+    __syncthreads();
+    if (tid < kTile) {
+        const int lo = st.emin[tid], hi = st.emax[tid];
+        const int base = (lo > hi) ? 0 : lo;                    // all-zero line: base 0
+        const int width = st.bad[tid] ? kWidthBad : ((lo > hi) ? 0 : hi + 8 - lo);
+        lbase[tid] = base;
+        lwidth[tid] = width;
+        stats[(int64_t)blockIdx.y * Lp + line0 + tid] = make_int2(base, width);
+    }
+    if (!LINE_CONTIG) {
+        // coalesced read along the reduction into shared memory
+        for (int e = tid; e < kTile * kChunk; e += kThreads) {
+            const int l = e / kChunk, rr = e % kChunk;
+            const int64_t line = line0 + l, r = q0 + rr;
+            raw[l][rr] = (line < nlines && r < qend) ? src[line * line_stride + r * r_stride] : 0;
+        }
+    }
+    __syncthreads();
+    const int rows_here = (int)(rtop - q0);
+    for (int e = tid; e < kTile * rows_here; e += kThreads) {
+        const int l = e % kTile, rr = e / kTile;
+        const int64_t line = line0 + l, r = q0 + rr;
         int v = 0;
-        if (line < nlines && r < rend && lwidth[l] <= 31) {
+        if (line < nlines && r < qend && lwidth[l] <= 31) {
+            const uint32_t h = LINE_CONTIG ? (uint32_t)src[line * line_stride + r * r_stride]
+                                           : (uint32_t)raw[l][rr];
             int m, ex;
             bool b;
-            decode(ld_bits(base, line * line_stride + r * r_stride), m, ex, b);
+            decode(h, m, ex, b);
             if (m != 0) v = m * (1 << (ex - lbase[l]));          // shift <= 23: |v| < 2^31
         }
-        T[rr][l] = v;
+        T[r * Lp + line] = v;
     }
 }
 
+// ---- main kernel --------------------------------------------------------------
+
+constexpr int kSlice = 32;                   // reduction rows per cp.async stage
+constexpr int kSlicesPerChunk = kChunk / kSlice;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 ::"r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+struct MainSmem {
+    int X[2][kSlice][kPitch];
+    int W[2][kSlice][kPitch];
+    double C[16][kThreads];                  // KBN compensation of the outer sum, per output
+    int G[16][kThreads];                     // outer grain per output
+    int rb[2][kTile], rw[2][kTile], cb[2][kTile], cw[2][kTile];   // per-chunk stats, by chunk parity
+};
+
 template <int PASS, bool OUT_F64>
 __global__ void __launch_bounds__(kThreads, 2)
-exact_int_kernel(const IArgs p) {
-    __shared__ __align__(16) int Xs[kHalf][kPitch];
-    __shared__ __align__(16) int Ws[kHalf][kPitch];
-    __shared__ LineStats rs, cs;
-    __shared__ int rbase[kTile], rwidth[kTile], cbase[kTile], cwidth[kTile];
-
+exact_int_kernel(const IArgs p, const int *__restrict__ TA, const int *__restrict__ TB,
+                 const int2 *__restrict__ SA, const int2 *__restrict__ SB, int64_t LpA,
+                 int64_t LpB, int64_t Rp) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    MainSmem &sm = *reinterpret_cast<MainSmem *>(smem_raw);
     const int tid = threadIdx.x;
     const int tx = tid % 16, ty = tid / 16;
     const int64_t i0 = (blockIdx.x / p.tiles_n) * kTile;
     const int64_t j0 = (blockIdx.x % p.tiles_n) * kTile;
-    // A lines (rows i) are contiguous in memory for dW; B lines (cols j) for fwd and dW
-    constexpr bool A_CONTIG = (PASS == CARBON_PASS_DW);
-    constexpr bool B_CONTIG = (PASS != CARBON_PASS_DX);
 
-    double S[4][4], C[4][4];
-    int G[4][4];                               // outer grain: min over chunks of (base + 1075) << 20
+    double S[4][4];
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int n = 0; n < 4; ++n) { S[m][n] = 0.0; C[m][n] = 0.0; G[m][n] = 0x7fffffff; }
-
-    for (int64_t q0 = 0; q0 < p.R; q0 += kChunk) {
-        const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
-
-        // ---- per-line statistics of this chunk
-        __syncthreads();
-        if (tid < kTile) {
-            rs.emin[tid] = 1 << 20; rs.emax[tid] = -(1 << 20); rs.bad[tid] = 0;
-            cs.emin[tid] = 1 << 20; cs.emax[tid] = -(1 << 20); cs.bad[tid] = 0;
+        for (int n = 0; n < 4; ++n) {
+            S[m][n] = 0.0;
+            sm.C[4 * m + n][tid] = 0.0;
+            sm.G[4 * m + n][tid] = 0x7fffffff;
         }
-        __syncthreads();
-        gather_stats<A_CONTIG>(p.A, p.a_si, p.a_sr, i0, p.rows, q0, qend, rs, tid);
-        gather_stats<B_CONTIG>(p.B, p.b_sj, p.b_sr, j0, p.cols, q0, qend, cs, tid);
-        __syncthreads();
-        if (tid < kTile) {
-            const int lo = rs.emin[tid], hi = rs.emax[tid];
-            rbase[tid] = (lo > hi) ? 0 : lo;                          // all-zero line: base 0
-            rwidth[tid] = rs.bad[tid] ? kWidthBad : ((lo > hi) ? 0 : hi + 8 - lo);
-        } else if (tid < 2 * kTile) {
-            const int l = tid - kTile;
-            const int lo = cs.emin[l], hi = cs.emax[l];
-            cbase[l] = (lo > hi) ? 0 : lo;
-            cwidth[l] = cs.bad[l] ? kWidthBad : ((lo > hi) ? 0 : hi + 8 - lo);
-        }
+    unsigned long long acc[4][4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[m][n] = 0ull;
 
-        // ---- integer dot products over the chunk, two staged halves
-        unsigned long long acc[4][4];
+    const int nslices = (int)(Rp / kSlice);
+    // each slice: 32 rows x 64 ints of each operand = 2 x 512 16-byte pieces
+    auto issue = [&](int g) {
+        const int buf = g & 1;
+        const int64_t r0 = (int64_t)g * kSlice;
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int n = 0; n < 4; ++n) acc[m][n] = 0ull;
-        for (int64_t r0 = q0; r0 < qend; r0 += kHalf) {
-            const int64_t rend = (qend - r0 > kHalf) ? r0 + kHalf : qend;
-            __syncthreads();
-            stage_ints<A_CONTIG>(p.A, p.a_si, p.a_sr, i0, p.rows, r0, rend, rbase, rwidth, Xs, tid);
-            stage_ints<B_CONTIG>(p.B, p.b_sj, p.b_sr, j0, p.cols, r0, rend, cbase, cwidth, Ws, tid);
-            __syncthreads();
-            const int kn = (int)(rend - r0);
-#pragma unroll 4
-            for (int k = 0; k < kn; ++k) {
-                const int4 a4 = *reinterpret_cast<const int4 *>(&Xs[k][4 * ty]);
-                const int4 b4 = *reinterpret_cast<const int4 *>(&Ws[k][4 * tx]);
-                const int a[4] = {a4.x, a4.y, a4.z, a4.w};
-                const int b[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-#pragma unroll
-                    for (int n = 0; n < 4; ++n)
-                        acc[m][n] += (unsigned long long)((long long)a[m] * (long long)b[n]);
+        for (int h = 0; h < 2; ++h) {
+            const int e = tid + kThreads * h;                   // 0..511
+            const int rr = e / 16, c4 = (e % 16) * 4;
+            cp_async16(&sm.X[buf][rr][c4], TA + (r0 + rr) * LpA + i0 + c4);
+            cp_async16(&sm.W[buf][rr][c4], TB + (r0 + rr) * LpB + j0 + c4);
+        }
+        cp_async_commit();
+    };
+
+    if (nslices > 0) issue(0);
+    for (int g = 0; g < nslices; ++g) {
+        const int q = g / kSlicesPerChunk;
+        if (g % kSlicesPerChunk == 0 && tid < 2 * kTile) {     // this chunk's line stats
+            const int l = tid % kTile;
+            if (tid < kTile) {
+                const int2 v = SA[(int64_t)q * LpA + i0 + l];
+                sm.rb[q & 1][l] = v.x; sm.rw[q & 1][l] = v.y;
+            } else {
+                const int2 v = SB[(int64_t)q * LpB + j0 + l];
+                sm.cb[q & 1][l] = v.x; sm.cw[q & 1][l] = v.y;
             }
         }
+        if (g + 1 < nslices) { issue(g + 1); cp_async_wait<1>(); }
+        else cp_async_wait<0>();
+        __syncthreads();
+        const int buf = g & 1;
+#pragma unroll 8
+        for (int k = 0; k < kSlice; ++k) {
+            const int4 a4 = *reinterpret_cast<const int4 *>(&sm.X[buf][k][4 * ty]);
+            const int4 b4 = *reinterpret_cast<const int4 *>(&sm.W[buf][k][4 * tx]);
+            const int a[4] = {a4.x, a4.y, a4.z, a4.w};
+            const int b[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int n = 0; n < 4; ++n)
+                    acc[m][n] += (unsigned long long)((long long)a[m] * (long long)b[n]);
+        }
+        __syncthreads();                                       // buffer may be refilled
 
-        // ---- chunk values and the outer KBN step, one output at a time
+        const bool chunk_end = (g % kSlicesPerChunk == kSlicesPerChunk - 1) || (g == nslices - 1);
+        if (!chunk_end) continue;
+        const int64_t q0 = (int64_t)q * kChunk;
+        const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
+        const int par = q & 1;
 #pragma unroll
         for (int m = 0; m < 4; ++m)
 #pragma unroll
             for (int n = 0; n < 4; ++n) {
                 const int li = 4 * ty + m, lj = 4 * tx + n;
-                const int wx = rwidth[li], ww = cwidth[lj];
-                const int b = rbase[li] + cbase[lj];
+                const int wx = sm.rw[par][li], ww = sm.cw[par][lj];
+                const int bx = sm.rb[par][li], bw = sm.cb[par][lj];
+                const int b = bx + bw;
                 const int64_t i = i0 + li, j = j0 + lj;
                 double P;
                 if (wx <= 31 && ww <= 31 && wx + ww <= 45) {
                     P = scaled_int_to_double((long long)acc[m][n], b);
                 } else if (i < p.rows && j < p.cols) {
                     if (wx <= 31 && ww <= 31 && wx + ww <= 54 &&
-                        chunk_exact_precise(p, i, j, q0, qend, rbase[li], cbase[lj]))
+                        chunk_exact_precise(p, i, j, q0, qend, bx, bw))
                         P = scaled_int_to_double((long long)acc[m][n], b);
                     else
                         P = chunk_kbn_global(p, i, j, q0, qend);
                 } else {
-                    P = 0.0;                                           // padding output
+                    P = 0.0;                                   // padding output
                 }
-                // P is a multiple of 2^b; S of 2^(min b so far).  If both are
-                // multiples of ulp(S + P), the addition is exact and C is unchanged.
-                const int g = (wx == kWidthBad || ww == kWidthBad) ? kGrainBad
-                              : (wx == 0 || ww == 0) ? kGrainZero : (b + 1075) << 20;
-                G[m][n] = min(G[m][n], g);
+                acc[m][n] = 0ull;
+                // P is a multiple of 2^b and S of 2^(min b so far): if both are
+                // multiples of ulp(S + P), the addition is exact and C unchanged.
+                const int o = 4 * m + n;
+                const int gq = (wx == kWidthBad || ww == kWidthBad) ? kGrainBad
+                               : (wx == 0 || ww == 0) ? kGrainZero : (b + 1075) << 20;
+                const int G = min(sm.G[o][tid], gq);
+                sm.G[o][tid] = G;
                 const double t = __dadd_rn(S[m][n], P);
-                const bool inexact = (__double2hiint(t) & 0x7ff00000) > G[m][n];
-                if (!__any_sync(0xffffffffu, inexact)) S[m][n] = t;
-                else kbn_value_step(S[m][n], C[m][n], P);
+                const bool inexact = (__double2hiint(t) & 0x7ff00000) > G;
+                if (!__any_sync(0xffffffffu, inexact)) {
+                    S[m][n] = t;
+                } else {
+                    double c = sm.C[o][tid];
+                    kbn_value_step(S[m][n], c, P);
+                    sm.C[o][tid] = c;
+                }
             }
     }
 
@@ -321,7 +391,7 @@ exact_int_kernel(const IArgs p) {
         for (int n = 0; n < 4; ++n) {
             const int64_t j = j0 + 4 * tx + n;
             if (j >= p.cols) continue;
-            double y = __dadd_rn(S[m][n], C[m][n]);
+            double y = __dadd_rn(S[m][n], sm.C[4 * m + n][tid]);
             if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
             const int64_t o = i * p.cols + j;
             if (OUT_F64) static_cast<double *>(p.out)[o] = y;
@@ -330,11 +400,24 @@ exact_int_kernel(const IArgs p) {
     }
 }
 
-template <int PASS>
-cudaError_t launch_int_pass(const IArgs &a, int64_t tiles, bool out_f64, cudaStream_t s) {
-    if (out_f64) exact_int_kernel<PASS, true><<<(unsigned)tiles, kThreads, 0, s>>>(a);
-    else exact_int_kernel<PASS, false><<<(unsigned)tiles, kThreads, 0, s>>>(a);
+template <int PASS, bool F64>
+cudaError_t launch_main(const IArgs &a, int64_t tiles, const int *TA, const int *TB,
+                        const int2 *SA, const int2 *SB, int64_t LpA, int64_t LpB, int64_t Rp,
+                        cudaStream_t s) {
+    auto kern = exact_int_kernel<PASS, F64>;
+    const int smem = (int)sizeof(MainSmem);
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kern<<<(unsigned)tiles, kThreads, smem, s>>>(a, TA, TB, SA, SB, LpA, LpB, Rp);
     return cudaGetLastError();
+}
+
+template <int PASS>
+cudaError_t launch_main_pass(bool f64, const IArgs &a, int64_t tiles, const int *TA, const int *TB,
+                             const int2 *SA, const int2 *SB, int64_t LpA, int64_t LpB, int64_t Rp,
+                             cudaStream_t s) {
+    return f64 ? launch_main<PASS, true>(a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, s)
+               : launch_main<PASS, false>(a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, s);
 }
 
 }  // namespace
@@ -353,15 +436,51 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
     default:              a.a_si = 1;   a.a_sr = p.K; a.b_sr = p.N; a.b_sj = 1; break;
     }
     a.tiles_n = (p.cols + kTile - 1) / kTile;
-    const int64_t tiles = ((p.rows + kTile - 1) / kTile) * a.tiles_n;
+    const int64_t tiles_m = (p.rows + kTile - 1) / kTile;
+    const int64_t tiles = tiles_m * a.tiles_n;
     if (tiles > 0x7fffffff) return CARBON_ERR_INVALID_ARG;
-    cudaError_t err;
-    switch (p.pass) {
-    case CARBON_PASS_FWD: err = launch_int_pass<CARBON_PASS_FWD>(a, tiles, out_f64, stream); break;
-    case CARBON_PASS_DX:  err = launch_int_pass<CARBON_PASS_DX>(a, tiles, out_f64, stream); break;
-    default:              err = launch_int_pass<CARBON_PASS_DW>(a, tiles, out_f64, stream); break;
+    const int64_t LpA = tiles_m * kTile, LpB = a.tiles_n * kTile;
+    const int64_t Rp = ((p.R + 63) / 64) * 64;
+    const int64_t nchunks = (p.R + kChunk - 1) / kChunk;
+    if (nchunks > 65535) return CARBON_ERR_INVALID_ARG;
+
+    // workspace: int32 operands [Rp][Lp] of A and B, then (base, width) per
+    // (chunk, line); stream-ordered, released at the end of this call
+    const size_t tA = (size_t)Rp * LpA, tB = (size_t)Rp * LpB;
+    const size_t bytes = 4 * (tA + tB) + 8 * (size_t)nchunks * (LpA + LpB);
+    char *ws = nullptr;
+    cudaError_t err = cudaSuccess;
+    if (bytes > 0) {
+        err = cudaMallocAsync(reinterpret_cast<void **>(&ws), bytes, stream);
+        if (err != cudaSuccess) return note_cuda(err);
     }
-    count_launch();
+    int *TA = reinterpret_cast<int *>(ws);
+    int *TB = TA + tA;
+    int2 *SA = reinterpret_cast<int2 *>(TB + tB);
+    int2 *SB = SA + (size_t)nchunks * LpA;
+
+    const bool a_contig = (p.pass == CARBON_PASS_DW), b_contig = (p.pass != CARBON_PASS_DX);
+    if (nchunks > 0) {
+        const dim3 ga((unsigned)tiles_m, (unsigned)nchunks), gb((unsigned)a.tiles_n, (unsigned)nchunks);
+        if (a_contig) int_prep_kernel<true><<<ga, kThreads, 0, stream>>>(a.A, a.a_si, a.a_sr, p.rows, p.R, Rp, LpA, TA, SA);
+        else int_prep_kernel<false><<<ga, kThreads, 0, stream>>>(a.A, a.a_si, a.a_sr, p.rows, p.R, Rp, LpA, TA, SA);
+        if (b_contig) int_prep_kernel<true><<<gb, kThreads, 0, stream>>>(a.B, a.b_sj, a.b_sr, p.cols, p.R, Rp, LpB, TB, SB);
+        else int_prep_kernel<false><<<gb, kThreads, 0, stream>>>(a.B, a.b_sj, a.b_sr, p.cols, p.R, Rp, LpB, TB, SB);
+        count_launch(2);
+        err = cudaGetLastError();
+    }
+    if (err == cudaSuccess) {
+        switch (p.pass) {
+        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(out_f64, a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, stream); break;
+        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(out_f64, a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, stream); break;
+        default:              err = launch_main_pass<CARBON_PASS_DW>(out_f64, a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, stream); break;
+        }
+        count_launch();
+    }
+    if (ws) {
+        const cudaError_t ferr = cudaFreeAsync(ws, stream);
+        if (err == cudaSuccess) err = ferr;
+    }
     return note_cuda(err);
 }
 

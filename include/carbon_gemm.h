@@ -44,6 +44,14 @@
  * Conventions
  *   - Pointers are DEVICE pointers on the current CUDA device; the caller
  *     owns every buffer.
+ *   - Workspace: with CARBON_BF16 the exact tier converts its operands once
+ *     into scaled int32 form in a workspace of about 4 bytes per operand
+ *     element (plus 8 bytes per 256 reduction indices per output row and
+ *     column), taken from the device's stream-ordered memory pool with
+ *     cudaMallocAsync on `stream` and released with cudaFreeAsync on `stream`
+ *     before the call returns.  If the pool cannot supply it the call returns
+ *     CARBON_ERR_CUDA and enqueues nothing.  The fp32 exact tier and the TC
+ *     tier use no workspace.
  *   - Calls are asynchronous: they validate, enqueue the kernels on `stream`
  *     and return.  Argument errors are returned synchronously and nothing is
  *     enqueued.  Errors raised while kernels run are reported by
