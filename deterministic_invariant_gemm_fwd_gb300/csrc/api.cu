@@ -156,8 +156,10 @@ carbon_status_t carbon_get_device_status(carbon_stream_t stream) {
         cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
     const carbon_status_t tc = carbon::tc_take_device_status();
     const carbon_status_t ms = carbon::measure_take_device_status();
+    const carbon_status_t ex = carbon::exact_take_device_status();
     if (st != CARBON_OK) return st;
     if (tc != CARBON_OK) return tc;
+    if (ex != CARBON_OK) return ex;
     return ms;
 }
 

@@ -2,6 +2,7 @@
 // carbon_gemm library (never by its tests' CPU reference).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -54,6 +55,16 @@ carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream
 carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t stream);
 carbon_status_t exact_round_launch(int dtype, void *out, const double *in, int64_t n,
                                    cudaStream_t stream);
+
+// 2-D tiled TMA tensor map over a row-major [outer, inner] matrix (row pitch
+// row_bytes); out-of-range elements read as zero.  cudaErrorInvalidValue if
+// the driver rejects the description.
+cudaError_t encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                                 uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+// Reads and clears the exact tier's device status word (exact_int.cu).
+carbon_status_t exact_take_device_status();
 
 // Tensor-core tier (tc_gemm.cu).  out_f32 selects the fp32 pre-rounding output.
 carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream);

@@ -33,14 +33,23 @@
 // Structure.  int_prep_kernel converts each operand once into the int32
 // operands of every (line, chunk) and that group's base and width (a
 // stream-ordered workspace of 4 bytes per operand element, allocated and
-// freed on the caller's stream); exact_int_kernel then streams 32-deep int32
-// slices with cp.async (double-buffered) into IMAD.WIDE accumulators, one
-// 64x64 output tile per CTA, 4x4 outputs per thread.
+// freed on the caller's stream).  exact_int_kernel computes one 64x64 output
+// tile per CTA: a producer warp streams 64-deep int32 tiles of both operands
+// by TMA into a 4-stage shared-memory ring (mbarrier transaction counts);
+// eight consumer warps, 4x4 outputs per thread, run the IMAD.WIDE loop and
+// release each stage through an mbarrier, with no CTA-wide barrier in the
+// loop.  Every wait is bounded; a wait that gives up records
+// CARBON_ERR_TIMEOUT and the CTA winds down.
 #include "carbon_internal.h"
+#include "device_sync.cuh"
 #include "exact_common.cuh"
+
+#include <cstring>
 
 namespace carbon {
 namespace {
+
+__device__ unsigned int g_exact_status = 0;
 
 constexpr int kChunk = 256;
 constexpr int kTile = 64;                  // CTA output tile: 64 x 64
@@ -244,88 +253,93 @@ int_prep_kernel(const unsigned short *src, int64_t line_stride, int64_t r_stride
 
 // ---- main kernel --------------------------------------------------------------
 
-constexpr int kSlice = 32;                   // reduction rows per cp.async stage
-constexpr int kSlicesPerChunk = kChunk / kSlice;
+constexpr int kStageK = 64;                          // reduction rows per ring stage
+constexpr int kStages = 4;
+constexpr int kStagesPerChunk = kChunk / kStageK;
+constexpr int kConsumerWarps = 8;
+constexpr int kMainThreads = (kConsumerWarps + 1) * 32;
+constexpr uint32_t kTileBytes = kStageK * kTile * 4; // 16 KiB per operand per stage
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                 ::"r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-struct MainSmem {
-    int X[2][kSlice][kPitch];
-    int W[2][kSlice][kPitch];
-    double C[16][kThreads];                  // KBN compensation of the outer sum, per output
-    int G[16][kThreads];                     // outer grain per output
-    int rb[2][kTile], rw[2][kTile], cb[2][kTile], cw[2][kTile];   // per-chunk stats, by chunk parity
+struct __align__(1024) MainSmem {
+    int X[kStages][kStageK][kTile];
+    int W[kStages][kStageK][kTile];
+    uint64_t full[kStages], empty[kStages];
+    uint32_t abort;
 };
 
 template <int PASS, bool OUT_F64>
-__global__ void __launch_bounds__(kThreads, 2)
-exact_int_kernel(const IArgs p, const int *__restrict__ TA, const int *__restrict__ TB,
-                 const int2 *__restrict__ SA, const int2 *__restrict__ SB, int64_t LpA,
-                 int64_t LpB, int64_t Rp) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    MainSmem &sm = *reinterpret_cast<MainSmem *>(smem_raw);
+__global__ void __launch_bounds__(kMainThreads, 1)
+exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                 const IArgs p, const int2 *__restrict__ SA, const int2 *__restrict__ SB,
+                 int64_t LpA, int64_t LpB, int64_t Rp) {
+    extern __shared__ uint8_t smem_raw[];
+    MainSmem &sm = *reinterpret_cast<MainSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x;
-    const int tx = tid % 16, ty = tid / 16;
+    const int warp = tid / 32, lane = tid % 32;
     const int64_t i0 = (blockIdx.x / p.tiles_n) * kTile;
     const int64_t j0 = (blockIdx.x % p.tiles_n) * kTile;
+    const int nstages = (int)(Rp / kStageK);
+    volatile uint32_t *abort_flag = &sm.abort;
 
-    double S[4][4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m)
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-            S[m][n] = 0.0;
-            sm.C[4 * m + n][tid] = 0.0;
-            sm.G[4 * m + n][tid] = 0x7fffffff;
+    if (tid == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(smem_addr(&sm.full[st]), 1);
+            mbar_init(smem_addr(&sm.empty[st]), kConsumerWarps);
         }
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_map(&map_a);
+            prefetch_map(&map_b);
+            int issued = 0;
+            for (int g = 0; g < nstages && !*abort_flag; ++g) {
+                const int st = g % kStages;
+                const uint32_t use = (uint32_t)(g / kStages);
+                if (!mbar_wait(smem_addr(&sm.empty[st]), (use & 1u) ^ 1u)) {
+                    *abort_flag = 1u;
+                    atomicExch(&g_exact_status, (unsigned)CARBON_ERR_TIMEOUT);
+                    break;
+                }
+                const uint32_t fb = smem_addr(&sm.full[st]);
+                mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+                tma_load_2d(smem_addr(&sm.X[st][0][0]), &map_a, fb, (int)i0, g * kStageK);
+                tma_load_2d(smem_addr(&sm.W[st][0][0]), &map_b, fb, (int)j0, g * kStageK);
+                issued = g + 1;
+            }
+            // every issued load lands before the CTA may exit
+            for (int g = (issued > kStages ? issued - kStages : 0); g < issued; ++g)
+                if (!mbar_wait(smem_addr(&sm.full[g % kStages]), (uint32_t)(g / kStages) & 1u)) break;
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int tx = tid % 16, ty = tid / 16;               // 16 x 16 consumer threads
+    double S[4][4], C[4][4];
+    int G[4][4];
     unsigned long long acc[4][4];
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int n = 0; n < 4; ++n) acc[m][n] = 0ull;
+        for (int n = 0; n < 4; ++n) { S[m][n] = 0.0; C[m][n] = 0.0; G[m][n] = 0x7fffffff; acc[m][n] = 0ull; }
 
-    const int nslices = (int)(Rp / kSlice);
-    // each slice: 32 rows x 64 ints of each operand = 2 x 512 16-byte pieces
-    auto issue = [&](int g) {
-        const int buf = g & 1;
-        const int64_t r0 = (int64_t)g * kSlice;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int e = tid + kThreads * h;                   // 0..511
-            const int rr = e / 16, c4 = (e % 16) * 4;
-            cp_async16(&sm.X[buf][rr][c4], TA + (r0 + rr) * LpA + i0 + c4);
-            cp_async16(&sm.W[buf][rr][c4], TB + (r0 + rr) * LpB + j0 + c4);
+    for (int g = 0; g < nstages; ++g) {
+        const int st = g % kStages;
+        if (!mbar_wait(smem_addr(&sm.full[st]), (uint32_t)(g / kStages) & 1u)) {
+            *abort_flag = 1u;
+            atomicExch(&g_exact_status, (unsigned)CARBON_ERR_TIMEOUT);
+            break;
         }
-        cp_async_commit();
-    };
-
-    if (nslices > 0) issue(0);
-    for (int g = 0; g < nslices; ++g) {
-        const int q = g / kSlicesPerChunk;
-        if (g % kSlicesPerChunk == 0 && tid < 2 * kTile) {     // this chunk's line stats
-            const int l = tid % kTile;
-            if (tid < kTile) {
-                const int2 v = SA[(int64_t)q * LpA + i0 + l];
-                sm.rb[q & 1][l] = v.x; sm.rw[q & 1][l] = v.y;
-            } else {
-                const int2 v = SB[(int64_t)q * LpB + j0 + l];
-                sm.cb[q & 1][l] = v.x; sm.cw[q & 1][l] = v.y;
-            }
-        }
-        if (g + 1 < nslices) { issue(g + 1); cp_async_wait<1>(); }
-        else cp_async_wait<0>();
-        __syncthreads();
-        const int buf = g & 1;
 #pragma unroll 8
-        for (int k = 0; k < kSlice; ++k) {
-            const int4 a4 = *reinterpret_cast<const int4 *>(&sm.X[buf][k][4 * ty]);
-            const int4 b4 = *reinterpret_cast<const int4 *>(&sm.W[buf][k][4 * tx]);
+        for (int k = 0; k < kStageK; ++k) {
+            const int4 a4 = *reinterpret_cast<const int4 *>(&sm.X[st][k][4 * ty]);
+            const int4 b4 = *reinterpret_cast<const int4 *>(&sm.W[st][k][4 * tx]);
             const int a[4] = {a4.x, a4.y, a4.z, a4.w};
             const int b[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
@@ -334,28 +348,39 @@ exact_int_kernel(const IArgs p, const int *__restrict__ TA, const int *__restric
                 for (int n = 0; n < 4; ++n)
                     acc[m][n] += (unsigned long long)((long long)a[m] * (long long)b[n]);
         }
-        __syncthreads();                                       // buffer may be refilled
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[st]));
 
-        const bool chunk_end = (g % kSlicesPerChunk == kSlicesPerChunk - 1) || (g == nslices - 1);
+        const bool chunk_end = ((g + 1) % kStagesPerChunk == 0) || (g == nstages - 1);
         if (!chunk_end) continue;
+        // ---- chunk values and the outer KBN step
+        const int q = g / kStagesPerChunk;
         const int64_t q0 = (int64_t)q * kChunk;
         const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
-        const int par = q & 1;
+        int rbx[4], rwx[4], cbw[4], cww[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int2 v = __ldg(&SA[(int64_t)q * LpA + i0 + 4 * ty + m]);
+            rbx[m] = v.x; rwx[m] = v.y;
+        }
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const int2 v = __ldg(&SB[(int64_t)q * LpB + j0 + 4 * tx + n]);
+            cbw[n] = v.x; cww[n] = v.y;
+        }
 #pragma unroll
         for (int m = 0; m < 4; ++m)
 #pragma unroll
             for (int n = 0; n < 4; ++n) {
-                const int li = 4 * ty + m, lj = 4 * tx + n;
-                const int wx = sm.rw[par][li], ww = sm.cw[par][lj];
-                const int bx = sm.rb[par][li], bw = sm.cb[par][lj];
-                const int b = bx + bw;
-                const int64_t i = i0 + li, j = j0 + lj;
+                const int wx = rwx[m], ww = cww[n];
+                const int b = rbx[m] + cbw[n];
+                const int64_t i = i0 + 4 * ty + m, j = j0 + 4 * tx + n;
                 double P;
                 if (wx <= 31 && ww <= 31 && wx + ww <= 45) {
                     P = scaled_int_to_double((long long)acc[m][n], b);
                 } else if (i < p.rows && j < p.cols) {
                     if (wx <= 31 && ww <= 31 && wx + ww <= 54 &&
-                        chunk_exact_precise(p, i, j, q0, qend, bx, bw))
+                        chunk_exact_precise(p, i, j, q0, qend, rbx[m], cbw[n]))
                         P = scaled_int_to_double((long long)acc[m][n], b);
                     else
                         P = chunk_kbn_global(p, i, j, q0, qend);
@@ -365,20 +390,13 @@ exact_int_kernel(const IArgs p, const int *__restrict__ TA, const int *__restric
                 acc[m][n] = 0ull;
                 // P is a multiple of 2^b and S of 2^(min b so far): if both are
                 // multiples of ulp(S + P), the addition is exact and C unchanged.
-                const int o = 4 * m + n;
                 const int gq = (wx == kWidthBad || ww == kWidthBad) ? kGrainBad
                                : (wx == 0 || ww == 0) ? kGrainZero : (b + 1075) << 20;
-                const int G = min(sm.G[o][tid], gq);
-                sm.G[o][tid] = G;
+                G[m][n] = min(G[m][n], gq);
                 const double t = __dadd_rn(S[m][n], P);
-                const bool inexact = (__double2hiint(t) & 0x7ff00000) > G;
-                if (!__any_sync(0xffffffffu, inexact)) {
-                    S[m][n] = t;
-                } else {
-                    double c = sm.C[o][tid];
-                    kbn_value_step(S[m][n], c, P);
-                    sm.C[o][tid] = c;
-                }
+                const bool inexact = (__double2hiint(t) & 0x7ff00000) > G[m][n];
+                if (!__any_sync(0xffffffffu, inexact)) S[m][n] = t;
+                else kbn_value_step(S[m][n], C[m][n], P);
             }
     }
 
@@ -391,7 +409,7 @@ exact_int_kernel(const IArgs p, const int *__restrict__ TA, const int *__restric
         for (int n = 0; n < 4; ++n) {
             const int64_t j = j0 + 4 * tx + n;
             if (j >= p.cols) continue;
-            double y = __dadd_rn(S[m][n], sm.C[4 * m + n][tid]);
+            double y = __dadd_rn(S[m][n], C[m][n]);
             if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
             const int64_t o = i * p.cols + j;
             if (OUT_F64) static_cast<double *>(p.out)[o] = y;
@@ -401,23 +419,23 @@ exact_int_kernel(const IArgs p, const int *__restrict__ TA, const int *__restric
 }
 
 template <int PASS, bool F64>
-cudaError_t launch_main(const IArgs &a, int64_t tiles, const int *TA, const int *TB,
+cudaError_t launch_main(const CUtensorMap &ma, const CUtensorMap &mb, const IArgs &a, int64_t tiles,
                         const int2 *SA, const int2 *SB, int64_t LpA, int64_t LpB, int64_t Rp,
                         cudaStream_t s) {
     auto kern = exact_int_kernel<PASS, F64>;
-    const int smem = (int)sizeof(MainSmem);
+    const int smem = (int)sizeof(MainSmem) + 1024;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    kern<<<(unsigned)tiles, kThreads, smem, s>>>(a, TA, TB, SA, SB, LpA, LpB, Rp);
+    kern<<<(unsigned)tiles, kMainThreads, smem, s>>>(ma, mb, a, SA, SB, LpA, LpB, Rp);
     return cudaGetLastError();
 }
 
 template <int PASS>
-cudaError_t launch_main_pass(bool f64, const IArgs &a, int64_t tiles, const int *TA, const int *TB,
-                             const int2 *SA, const int2 *SB, int64_t LpA, int64_t LpB, int64_t Rp,
-                             cudaStream_t s) {
-    return f64 ? launch_main<PASS, true>(a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, s)
-               : launch_main<PASS, false>(a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, s);
+cudaError_t launch_main_pass(bool f64, const CUtensorMap &ma, const CUtensorMap &mb, const IArgs &a,
+                             int64_t tiles, const int2 *SA, const int2 *SB, int64_t LpA,
+                             int64_t LpB, int64_t Rp, cudaStream_t s) {
+    return f64 ? launch_main<PASS, true>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s)
+               : launch_main<PASS, false>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s);
 }
 
 }  // namespace
@@ -469,11 +487,24 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
         count_launch(2);
         err = cudaGetLastError();
     }
+    // int32 tiles: 64 lines x 64 reduction rows per TMA box, no swizzle
+    CUtensorMap ma, mb;
+    if (err == cudaSuccess && nchunks > 0) {
+        err = encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_INT32, TA, (uint64_t)LpA, (uint64_t)Rp,
+                                   (uint64_t)LpA * 4, kTile, kStageK, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (err == cudaSuccess)
+            err = encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_INT32, TB, (uint64_t)LpB,
+                                       (uint64_t)Rp, (uint64_t)LpB * 4, kTile, kStageK,
+                                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+        std::memset(&ma, 0, sizeof ma);
+        std::memset(&mb, 0, sizeof mb);
+    }
     if (err == cudaSuccess) {
         switch (p.pass) {
-        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(out_f64, a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, stream); break;
-        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(out_f64, a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, stream); break;
-        default:              err = launch_main_pass<CARBON_PASS_DW>(out_f64, a, tiles, TA, TB, SA, SB, LpA, LpB, Rp, stream); break;
+        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, stream); break;
+        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, stream); break;
+        default:              err = launch_main_pass<CARBON_PASS_DW>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, stream); break;
         }
         count_launch();
     }
@@ -482,6 +513,13 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
         if (err == cudaSuccess) err = ferr;
     }
     return note_cuda(err);
+}
+
+carbon_status_t exact_take_device_status() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_exact_status, sizeof v) != cudaSuccess) return CARBON_OK;
+    if (v != 0) cudaMemcpyToSymbol(g_exact_status, &zero, sizeof zero);
+    return (carbon_status_t)v;
 }
 
 }  // namespace carbon

@@ -91,19 +91,6 @@ struct Smem {
 
 // ---- PTX wrappers -----------------------------------------------------------
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];"
-        ::"r"(dst), "l"(map), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -597,38 +584,14 @@ __global__ void tc_fill_kernel(void *out, const void *bias, int64_t rows, int64_
 
 // ---- host side ----------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-cudaError_t g_encode_err = cudaSuccess;
-
-cudaError_t get_encoder() {
-    std::call_once(g_encode_once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void *fn = nullptr;
-        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                        cudaEnableDefault, &q);
-        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
-            g_encode_err = cudaErrorNotSupported;
-        if (g_encode_err == cudaSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    return g_encode_err;
-}
-
 // 2-D bf16 tensor map over a row-major [outer, inner] matrix with a
 // {box_inner, box_outer} box; out-of-range elements read as 0 and are not
 // written by stores.
 bool encode_map(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int box_inner,
                 int box_outer, CUtensorMapSwizzle swizzle) {
-    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-    cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
-    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
-    cuuint32_t estr[2] = {1u, 1u};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
-                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, (uint64_t)inner,
+                                (uint64_t)outer, (uint64_t)inner * 2, (uint32_t)box_inner,
+                                (uint32_t)box_outer, swizzle) == cudaSuccess;
 }
 
 bool encode_operand(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int box_outer) {
@@ -719,8 +682,7 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
     if (p.rows > (int64_t)0x7fffffff || p.cols > (int64_t)0x7fffffff || p.R > (int64_t)0x7fffffff)
         return CARBON_ERR_INVALID_ARG;
 
-    cudaError_t err = get_encoder();
-    if (err != cudaSuccess) return note_cuda(err);
+    cudaError_t err = cudaSuccess;
 
     const int bn = choose_bn(p.cols);
     CUtensorMap ma, mb, mo;
@@ -775,6 +737,42 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
     }
     count_launch();
     return note_cuda(err);
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t get_encoder() {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            g_encode_err = cudaErrorNotSupported;
+        if (g_encode_err == cudaSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode_err;
+}
+
+}  // namespace
+
+cudaError_t encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                                 uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    const cudaError_t err = get_encoder();
+    if (err != cudaSuccess) return err;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 carbon_status_t tc_take_device_status() {
