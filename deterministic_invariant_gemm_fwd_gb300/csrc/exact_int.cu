@@ -77,6 +77,12 @@ __device__ __forceinline__ void decode(uint32_t h, int &m, int &e, bool &bad) {
     bad = (e8 == 0xff);
 }
 
+// acc += a * b, 32 x 32 -> 64-bit signed multiply-add in one instruction
+// (two's-complement wrap; callers only use sums they have bounded).
+__device__ __forceinline__ void mad_wide(long long &acc, int a, int b) {
+    asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc) : "r"(a), "r"(b));
+}
+
 __device__ __forceinline__ uint32_t ld_bits(const unsigned short *base, int64_t idx) {
     return (uint32_t)__ldg(base + idx);
 }
@@ -108,16 +114,23 @@ __device__ __noinline__ double chunk_kbn_global(const IArgs &p, int64_t i, int64
     return __dadd_rn(s, c);
 }
 
-// Precise exactness check of one (row, column, chunk) on the integer pipes:
-// with X, W the integer operands at bases bx, bw, every partial sum is
-// representable if sum |X W| < 2^(53 + t), t the smallest number of trailing
-// zero bits of a nonzero product X*W.  Needs wx, ww <= 31 and wx + ww <= 54
-// (so sum |X W| < 2^62 cannot overflow).
-__device__ __noinline__ bool chunk_exact_precise(const IArgs &p, int64_t i, int64_t j, int64_t q0,
-                                                 int64_t qend, int bx, int bw) {
+// Precise exactness check of one (row, column, chunk) on the integer pipes,
+// run by the whole warp for the output owned by lane `owner` (every lane takes
+// every 32nd reduction index, then the warp reduces): with X, W the integer
+// operands at bases bx, bw, every partial sum is representable if
+// sum |X W| < 2^(53 + t), t the smallest number of trailing zero bits of a
+// nonzero product.  Requires wx, ww <= 31 and wx + ww <= 54 for the owner
+// (so sum |X W| < 2^62).  Returns the verdict to every lane.
+__device__ __forceinline__ bool warp_exact_precise(const IArgs &p, int owner, int64_t i, int64_t j,
+                                                   int64_t q0, int64_t qend, int bx, int bw) {
+    const int lane = threadIdx.x % 32;
+    i = __shfl_sync(0xffffffffu, i, owner);
+    j = __shfl_sync(0xffffffffu, j, owner);
+    bx = __shfl_sync(0xffffffffu, bx, owner);
+    bw = __shfl_sync(0xffffffffu, bw, owner);
     unsigned long long abs_sum = 0;
     int tz = 1 << 20;
-    for (int64_t r = q0; r < qend; ++r) {
+    for (int64_t r = q0 + lane; r < qend; r += 32) {
         int mx, ex, mw, ew;
         bool bad_x, bad_w;
         decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bad_x);
@@ -129,6 +142,9 @@ __device__ __noinline__ bool chunk_exact_precise(const IArgs &p, int64_t i, int6
         abs_sum += (unsigned long long)(prod < 0 ? -prod : prod);
         tz = min(tz, __ffsll(prod) - 1);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) abs_sum += __shfl_xor_sync(0xffffffffu, abs_sum, off);
+    tz = __reduce_min_sync(0xffffffffu, tz);
     if (abs_sum == 0) return true;
     return tz + 53 >= 64 || abs_sum < (1ull << (tz + 53));
 }
@@ -323,11 +339,11 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     const int tx = tid % 16, ty = tid / 16;               // 16 x 16 consumer threads
     double S[4][4], C[4][4];
     int G[4][4];
-    unsigned long long acc[4][4];
+    long long acc[4][4];
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int n = 0; n < 4; ++n) { S[m][n] = 0.0; C[m][n] = 0.0; G[m][n] = 0x7fffffff; acc[m][n] = 0ull; }
+        for (int n = 0; n < 4; ++n) { S[m][n] = 0.0; C[m][n] = 0.0; G[m][n] = 0x7fffffff; acc[m][n] = 0ll; }
 
     for (int g = 0; g < nstages; ++g) {
         const int st = g % kStages;
@@ -346,7 +362,7 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             for (int m = 0; m < 4; ++m)
 #pragma unroll
                 for (int n = 0; n < 4; ++n)
-                    acc[m][n] += (unsigned long long)((long long)a[m] * (long long)b[n]);
+                    mad_wide(acc[m][n], a[m], b[n]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.empty[st]));
@@ -375,19 +391,22 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 const int wx = rwx[m], ww = cww[n];
                 const int b = rbx[m] + cbw[n];
                 const int64_t i = i0 + 4 * ty + m, j = j0 + 4 * tx + n;
-                double P;
-                if (wx <= 31 && ww <= 31 && wx + ww <= 45) {
-                    P = scaled_int_to_double((long long)acc[m][n], b);
-                } else if (i < p.rows && j < p.cols) {
-                    if (wx <= 31 && ww <= 31 && wx + ww <= 54 &&
-                        chunk_exact_precise(p, i, j, q0, qend, rbx[m], cbw[n]))
-                        P = scaled_int_to_double((long long)acc[m][n], b);
-                    else
-                        P = chunk_kbn_global(p, i, j, q0, qend);
-                } else {
-                    P = 0.0;                                   // padding output
+                const bool real = (i < p.rows && j < p.cols);
+                // 0: integer sum proven by the widths; 1: needs the precise check;
+                // 2: needs the float64 KBN step
+                int how = (wx <= 31 && ww <= 31 && wx + ww <= 45) || !real ? 0
+                          : (wx <= 31 && ww <= 31 && wx + ww <= 54) ? 1 : 2;
+                unsigned pending = __ballot_sync(0xffffffffu, how == 1);
+                while (pending) {                             // the warp checks each one together
+                    const int owner = __ffs(pending) - 1;
+                    pending &= pending - 1;
+                    const bool ok = warp_exact_precise(p, owner, i, j, q0, qend, rbx[m], cbw[n]);
+                    if (lane == owner) how = ok ? 0 : 2;
                 }
-                acc[m][n] = 0ull;
+                double P;
+                if (how == 0) P = real ? scaled_int_to_double(acc[m][n], b) : 0.0;
+                else P = chunk_kbn_global(p, i, j, q0, qend);
+                acc[m][n] = 0ll;
                 // P is a multiple of 2^b and S of 2^(min b so far): if both are
                 // multiples of ulp(S + P), the addition is exact and C unchanged.
                 const int gq = (wx == kWidthBad || ww == kWidthBad) ? kGrainBad
