@@ -16,6 +16,7 @@ from ._binding import (CarbonError, carbon_abi_version, carbon_debug_exact_y64, 
                        carbon_debug_tc_f32, carbon_debug_timeout_probe,
                        carbon_gemm_dw, carbon_gemm_dx, carbon_gemm_fwd,
                        carbon_get_device_status, carbon_measure_fp64_rate,
+                       carbon_measure_int_mac_rate,
                        carbon_status_string)
 
 

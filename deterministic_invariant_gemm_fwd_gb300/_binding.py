@@ -53,6 +53,7 @@ def _load() -> ctypes.CDLL:
         "carbon_debug_round": [i32, vp, vp, i64, vp],
         "carbon_debug_timeout_probe": [i64, vp],
         "carbon_measure_fp64_rate": [ctypes.POINTER(dp), ctypes.POINTER(dp), vp],
+        "carbon_measure_int_mac_rate": [ctypes.POINTER(dp), vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -160,6 +161,14 @@ def carbon_measure_fp64_rate(stream=None) -> tuple:
     _check(lib.carbon_measure_fp64_rate(ctypes.byref(a), ctypes.byref(b), _stream(stream)),
            "carbon_measure_fp64_rate")
     return a.value, b.value
+
+
+def carbon_measure_int_mac_rate(stream=None) -> float:
+    """32x32->64-bit integer multiply-adds per second on the current device."""
+    a = ctypes.c_double()
+    _check(lib.carbon_measure_int_mac_rate(ctypes.byref(a), _stream(stream)),
+           "carbon_measure_int_mac_rate")
+    return a.value
 
 
 def carbon_status_string(status: int) -> str:

@@ -26,6 +26,34 @@ __global__ void fp64_rate_kernel(double *sink, int iters, double a, double b) {
     sink[blockIdx.x * (int64_t)blockDim.x + threadIdx.x] = s;
 }
 
+// Independent 32x32->64-bit integer multiply-add chains (one mad.wide.s32
+// each), operands refreshed from a 4x4 outer product like a GEMM micro-tile.
+__global__ void int_mac_rate_kernel(long long *sink, int iters, int seed) {
+    long long acc[4][4];
+    int a[4], b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { a[i] = seed * 7 + i + (int)threadIdx.x; b[i] = seed * 3 - i; }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = i * 4 + j;
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc[i][j]) : "r"(a[i]), "r"(b[j]));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { a[i] ^= it; b[i] += 3; }
+    }
+    long long s = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s ^= acc[i][j];
+    sink[blockIdx.x * (int64_t)blockDim.x + threadIdx.x] = s;
+}
+
 __global__ void timeout_probe_kernel(int64_t budget_ns) {
     __shared__ __align__(8) uint64_t bar;
     if (threadIdx.x != 0) return;
@@ -92,5 +120,37 @@ extern "C" carbon_status_t carbon_measure_fp64_rate(double *dfma_per_s, double *
     if (err != cudaSuccess) return carbon::note_cuda(err);
     if (dfma_per_s) *dfma_per_s = best[0];
     if (dadd_per_s) *dadd_per_s = best[1];
+    return CARBON_OK;
+}
+
+extern "C" carbon_status_t carbon_measure_int_mac_rate(double *macs_per_s, carbon_stream_t stream) {
+    int sms = 0;
+    carbon_status_t st = carbon::current_device(nullptr, &sms);
+    if (st != CARBON_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int threads = 256, blocks = sms * 8, iters = 4000;
+    long long *sink = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t err = cudaMalloc(&sink, sizeof(long long) * (size_t)threads * blocks);
+    if (err == cudaSuccess) err = cudaEventCreate(&e0);
+    if (err == cudaSuccess) err = cudaEventCreate(&e1);
+    double best = 0.0;
+    for (int rep = 0; rep < 4 && err == cudaSuccess; ++rep) {       // rep 0 warms up
+        cudaEventRecord(e0, s);
+        carbon::int_mac_rate_kernel<<<blocks, threads, 0, s>>>(sink, iters, rep + 1);
+        carbon::count_launch();
+        cudaEventRecord(e1, s);
+        err = cudaEventSynchronize(e1);
+        if (err == cudaSuccess) err = cudaGetLastError();
+        float ms = 0.f;
+        if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, e0, e1);
+        const double macs = (double)threads * blocks * iters * 16;
+        if (rep > 0 && ms > 0.f && macs / (ms * 1e-3) > best) best = macs / (ms * 1e-3);
+    }
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    if (sink) cudaFree(sink);
+    if (err != cudaSuccess) return carbon::note_cuda(err);
+    if (macs_per_s) *macs_per_s = best;
     return CARBON_OK;
 }

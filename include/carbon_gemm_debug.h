@@ -55,6 +55,12 @@ carbon_status_t carbon_debug_timeout_probe(int64_t budget_ns, carbon_stream_t st
 carbon_status_t carbon_measure_fp64_rate(double *dfma_per_s, double *dadd_per_s,
                                          carbon_stream_t stream);
 
+/* Integer multiply-add rate microbenchmark on the current device (blocking):
+ * independent 32x32->64-bit mad.wide.s32 chains on every SM, reported as
+ * multiply-adds per second.  The roofline denominator of the bf16 exact
+ * tier, whose inner loop is one such multiply-add per product. */
+carbon_status_t carbon_measure_int_mac_rate(double *macs_per_s, carbon_stream_t stream);
+
 /* Number of kernel launches the library has enqueued in this process. */
 int64_t carbon_debug_launch_count(void);
 

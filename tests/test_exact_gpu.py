@@ -278,3 +278,31 @@ def test_exactness_proof_boundaries(kind, dtype):
     check_dense("fwd", dtype, X, W, b, M, K, N)
     check_dense("dx", dtype, dY, W, None, M, K, N)
     check_dense("dw", dtype, X, dY, None, M, K, N)
+
+
+def test_int_mac_rate_microbenchmark_is_sane():
+    rate = cg.carbon_measure_int_mac_rate()
+    # GB300: tens of 32x32->64 multiply-adds per SM per clock over 152 SMs
+    assert 1e12 < rate < 1e14
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dx", "dw"])
+def test_bf16_outlier_rows_and_columns(pass_):
+    """bf16 operands with a few huge-range rows/columns: the integer path must
+    route those (row, column, chunk) groups through the precise check or the
+    float64 step, and every other group through the integer sum, with the
+    oracle's bits everywhere."""
+    rng = np.random.default_rng(31)
+    M, K, N = 130, 700, 70
+    L = inputs.linear_layer(rng, M, K, N, "bf16", 1e-3)
+    for key, axis in (("X", 0), ("W", 1), ("dY", 0)):
+        a = inputs.bf16_bits_to_f32(L[key]).copy()
+        idx = rng.integers(0, a.shape[axis], 3)
+        if axis == 0:
+            a[idx, rng.integers(0, a.shape[1], 3)] *= np.float32(2.0 ** -40)
+            a[idx[:1], :5] *= np.float32(2.0 ** 30)
+        else:
+            a[rng.integers(0, a.shape[0], 3), idx] *= np.float32(2.0 ** -40)
+        L[key] = inputs.f32_to_bf16_bits(a)
+    A, B, bias = layer_operands(L, pass_)
+    check_dense(pass_, "bf16", A, B, bias, M, K, N)
