@@ -21,7 +21,8 @@ F32, BF16 = 0, 1
 TIER_EXACT, TIER_TC = 0, 1
 PASS_FWD, PASS_DX, PASS_DW = 0, 1, 2
 STATUS = {0: "CARBON_OK", 1: "CARBON_ERR_INVALID_ARG", 2: "CARBON_ERR_UNSUPPORTED",
-          3: "CARBON_ERR_MISALIGNED", 4: "CARBON_ERR_CUDA", 5: "CARBON_ERR_TIMEOUT"}
+          3: "CARBON_ERR_MISALIGNED", 4: "CARBON_ERR_CUDA", 5: "CARBON_ERR_TIMEOUT",
+          6: "CARBON_ERR_SCRATCH_LIMIT"}
 DTYPES = {"f32": F32, "bf16": BF16}
 TIERS = {"exact": TIER_EXACT, "tc": TIER_TC}
 PASSES = {"fwd": PASS_FWD, "dx": PASS_DX, "dw": PASS_DW}
@@ -48,6 +49,7 @@ def _load() -> ctypes.CDLL:
         "carbon_gemm_dx": [vp, vp, vp, i64, i64, i64, i32, i32, vp],
         "carbon_gemm_dw": [vp, vp, vp, i64, i64, i64, i32, i32, vp],
         "carbon_get_device_status": [vp],
+        "carbon_gemm_exact_bf16_noalloc": [i32, vp, vp, vp, vp, i64, i64, i64, vp],
         "carbon_debug_exact_y64": [i32, vp, vp, vp, vp, i64, i64, i64, i32, vp],
         "carbon_debug_tc_f32": [i32, vp, vp, vp, vp, i64, i64, i64, vp],
         "carbon_debug_round": [i32, vp, vp, i64, vp],
@@ -126,6 +128,14 @@ def carbon_gemm_dw(dW, X, dY, M, K, N, dtype, tier, stream=None) -> None:
     _check(lib.carbon_gemm_dw(_ptr(dW), _ptr(X), _ptr(dY), M, K, N,
                               _code(DTYPES, dtype), _code(TIERS, tier), _stream(stream)),
            "carbon_gemm_dw")
+
+
+def carbon_gemm_exact_bf16_noalloc(pass_, out, A, B, bias, M, K, N, stream=None) -> None:
+    """Exact-tier bf16 GEMM that allocates no device memory (fixed 64 MiB
+    library workspace); same bits as carbon_gemm_fwd/dx/dw with the exact tier."""
+    _check(lib.carbon_gemm_exact_bf16_noalloc(_code(PASSES, pass_), _ptr(out), _ptr(A), _ptr(B),
+                                              _ptr(bias), M, K, N, _stream(stream)),
+           "carbon_gemm_exact_bf16_noalloc")
 
 
 def carbon_get_device_status(stream=None) -> int:

@@ -171,6 +171,7 @@ const char *carbon_status_string(carbon_status_t status) {
     case CARBON_ERR_MISALIGNED: return "CARBON_ERR_MISALIGNED";
     case CARBON_ERR_CUDA: return "CARBON_ERR_CUDA";
     case CARBON_ERR_TIMEOUT: return "CARBON_ERR_TIMEOUT";
+    case CARBON_ERR_SCRATCH_LIMIT: return "CARBON_ERR_SCRATCH_LIMIT";
     }
     return "CARBON_ERR_UNKNOWN";
 }

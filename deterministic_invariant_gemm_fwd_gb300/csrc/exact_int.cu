@@ -45,6 +45,7 @@
 #include "exact_common.cuh"
 
 #include <cstring>
+#include <mutex>
 
 namespace carbon {
 namespace {
@@ -54,7 +55,6 @@ __device__ unsigned int g_exact_status = 0;
 constexpr int kChunk = 256;
 constexpr int kTile = 64;                  // CTA output tile: 64 x 64
 constexpr int kThreads = 256;              // 16 x 16 threads, 4 x 4 outputs each
-constexpr int kPitch = kTile + 4;          // int32 row pitch of the staged tiles
 constexpr int kWidthBad = 99;              // width of a row/column holding inf/NaN
 constexpr int kGrainBad = -0x40000000;
 constexpr int kGrainZero = 0x70000000;
@@ -542,3 +542,134 @@ carbon_status_t exact_take_device_status() {
 }
 
 }  // namespace carbon
+
+// ---- bf16 exact tier without any device allocation ----------------------------
+//
+// Some callers cannot allocate device memory while they run: code inside a
+// framework whose allocator owns every byte of the GPU, code on a path that
+// must never block on or fail in an allocator (a latency-critical serving
+// loop, a watchdog), or a process where the stream-ordered pool is
+// unavailable.  For them carbon_gemm_exact_bf16_noalloc runs the same two
+// kernels as the bf16 exact tier above, with the workspace taken from a
+// fixed array in device memory that the library reserves when it is loaded.
+
+namespace carbon {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;   // 64 MiB per device
+
+// Fixed workspace of the no-allocation entry point.  Every GPU that loads
+// this library holds it until the process exits.  Host code must not use the
+// symbol as an address (it is a host-side stand-in); the device address comes
+// from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[128];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the first call on each device does this; it is not a stream
+// operation, but make that first call before any stream capture).
+cudaError_t noalloc_scratch(void **ptr) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace carbon
+
+extern "C" carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, void *out,
+                                                          const void *A, const void *B,
+                                                          const void *bias, int64_t M, int64_t K,
+                                                          int64_t N, carbon_stream_t stream) {
+    using namespace carbon;
+    if (pass < CARBON_PASS_FWD || pass > CARBON_PASS_DW) return CARBON_ERR_INVALID_ARG;
+    if (M < 0 || K < 0 || N < 0) return CARBON_ERR_INVALID_ARG;
+    int64_t mk, kn, mn;
+    if (__builtin_mul_overflow(M, K, &mk) || __builtin_mul_overflow(K, N, &kn) ||
+        __builtin_mul_overflow(M, N, &mn))
+        return CARBON_ERR_INVALID_ARG;
+    const Problem p = make_problem(pass, CARBON_BF16, out, A, B, bias, M, K, N);
+    const int64_t a_elems = (pass == CARBON_PASS_DX) ? mn : mk;
+    const int64_t b_elems = (pass == CARBON_PASS_DW) ? mn : kn;
+    const int64_t out_elems = p.rows * p.cols;
+    if (out_elems == 0) return CARBON_OK;
+    if (out == nullptr || (a_elems > 0 && A == nullptr) || (b_elems > 0 && B == nullptr))
+        return CARBON_ERR_INVALID_ARG;
+
+    // the same workspace layout as exact_int_launch, checked against the array
+    const int64_t tiles_m = (p.rows + kTile - 1) / kTile, tiles_n = (p.cols + kTile - 1) / kTile;
+    const int64_t LpA = tiles_m * kTile, LpB = tiles_n * kTile;
+    const int64_t Rp = ((p.R + 63) / 64) * 64;
+    const int64_t nchunks = (p.R + kChunk - 1) / kChunk;
+    if (tiles_m * tiles_n > 0x7fffffff || nchunks > 65535) return CARBON_ERR_INVALID_ARG;
+    const double need = 4.0 * (double)Rp * (double)(LpA + LpB) + 8.0 * (double)nchunks * (double)(LpA + LpB);
+    if (need > (double)kNoAllocScratchBytes) return CARBON_ERR_SCRATCH_LIMIT;
+
+    carbon_status_t st = current_device(nullptr, nullptr);
+    if (st != CARBON_OK) return st;
+    void *scratch = nullptr;
+    cudaError_t err = noalloc_scratch(&scratch);
+    if (err != cudaSuccess) return note_cuda(err);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    IArgs a;
+    a.A = static_cast<const unsigned short *>(p.A);
+    a.B = static_cast<const unsigned short *>(p.B);
+    a.bias = static_cast<const unsigned short *>(p.bias);
+    a.out = p.out;
+    a.rows = p.rows; a.cols = p.cols; a.R = p.R;
+    switch (p.pass) {
+    case CARBON_PASS_FWD: a.a_si = p.K; a.a_sr = 1; a.b_sr = p.N; a.b_sj = 1; break;
+    case CARBON_PASS_DX:  a.a_si = p.N; a.a_sr = 1; a.b_sr = 1;   a.b_sj = p.N; break;
+    default:              a.a_si = 1;   a.a_sr = p.K; a.b_sr = p.N; a.b_sj = 1; break;
+    }
+    a.tiles_n = tiles_n;
+    const size_t tA = (size_t)Rp * LpA, tB = (size_t)Rp * LpB;
+    int *TA = static_cast<int *>(scratch);
+    int *TB = TA + tA;
+    int2 *SA = reinterpret_cast<int2 *>(TB + tB);
+    int2 *SB = SA + (size_t)nchunks * LpA;
+
+    // Nothing in the array has to start at zero: the pre-pass writes every
+    // operand word and statistic the main kernel reads, in this same call.
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof ma);
+    std::memset(&mb, 0, sizeof mb);
+    if (nchunks > 0) {
+        const dim3 ga((unsigned)tiles_m, (unsigned)nchunks), gb((unsigned)tiles_n, (unsigned)nchunks);
+        if (p.pass == CARBON_PASS_DW) int_prep_kernel<true><<<ga, kThreads, 0, s>>>(a.A, a.a_si, a.a_sr, p.rows, p.R, Rp, LpA, TA, SA);
+        else int_prep_kernel<false><<<ga, kThreads, 0, s>>>(a.A, a.a_si, a.a_sr, p.rows, p.R, Rp, LpA, TA, SA);
+        if (p.pass != CARBON_PASS_DX) int_prep_kernel<true><<<gb, kThreads, 0, s>>>(a.B, a.b_sj, a.b_sr, p.cols, p.R, Rp, LpB, TB, SB);
+        else int_prep_kernel<false><<<gb, kThreads, 0, s>>>(a.B, a.b_sj, a.b_sr, p.cols, p.R, Rp, LpB, TB, SB);
+        count_launch(2);
+        err = cudaGetLastError();
+        if (err == cudaSuccess)
+            err = encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_INT32, TA, (uint64_t)LpA, (uint64_t)Rp,
+                                       (uint64_t)LpA * 4, kTile, kStageK, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (err == cudaSuccess)
+            err = encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_INT32, TB, (uint64_t)LpB, (uint64_t)Rp,
+                                       (uint64_t)LpB * 4, kTile, kStageK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (err == cudaSuccess) {
+        const int64_t tiles = tiles_m * tiles_n;
+        switch (p.pass) {
+        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s); break;
+        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s); break;
+        default:              err = launch_main_pass<CARBON_PASS_DW>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s); break;
+        }
+        count_launch();
+    }
+    return note_cuda(err);
+}

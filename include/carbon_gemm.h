@@ -80,6 +80,8 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *carbon_stream_t;
 
+typedef enum { CARBON_PASS_FWD = 0, CARBON_PASS_DX = 1, CARBON_PASS_DW = 2 } carbon_pass_t;
+
 typedef enum {
     CARBON_F32 = 0,     /* IEEE binary32 */
     CARBON_BF16 = 1     /* bfloat16 (top 16 bits of binary32) */
@@ -96,7 +98,8 @@ typedef enum {
     CARBON_ERR_UNSUPPORTED = 2,   /* device or dtype/tier combination */
     CARBON_ERR_MISALIGNED = 3,    /* TC tier: pointer/pitch not 16-byte aligned */
     CARBON_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
-    CARBON_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up */
+    CARBON_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up */
+    CARBON_ERR_SCRATCH_LIMIT = 6  /* needs more than the fixed no-allocation workspace */
 } carbon_status_t;
 
 /* Forward pass Y[M,N] = X[M,K] . W[K,N] + bias[N].
@@ -117,6 +120,37 @@ carbon_status_t carbon_gemm_dw(void *dW, const void *X, const void *dY,
                                int64_t M, int64_t K, int64_t N,
                                carbon_dtype_t dtype, carbon_tier_t tier,
                                carbon_stream_t stream);
+
+/* Exact tier, bf16, without any device allocation.  (No counterpart in the
+ * source pages: this entry point exists for callers, not for the method.)
+ *
+ * Same result, bit for bit, as carbon_gemm_fwd / _dx / _dw with CARBON_BF16
+ * and CARBON_TIER_EXACT, for callers that cannot allocate device memory while
+ * they run -- code inside a framework whose allocator owns all of the GPU's
+ * memory, latency-critical loops that must never block on or fail in an
+ * allocator, or processes where the stream-ordered pool is unavailable.  The
+ * workspace the bf16 exact tier needs comes instead from a fixed 64 MiB array
+ * in device memory that the library reserves on every GPU that loads it,
+ * until the process exits.  No cudaMalloc, cudaMallocAsync, cudaFree or other
+ * allocating call is made.
+ *
+ * pass: CARBON_PASS_FWD (A = X, B = W, bias allowed), CARBON_PASS_DX
+ * (A = dY, B = W), CARBON_PASS_DW (A = X, B = dY); out, A, B, bias, M, K, N
+ * as in the per-pass entry points; all bf16, device pointers, caller-owned.
+ * Limit: 4*Rp*(Lr + Lc) + 8*ceil(R/256)*(Lr + Lc) bytes must fit 64 MiB, where
+ * R is the reduction length (K, N or M for fwd, dX, dW), Rp = R rounded up to
+ * a multiple of 64, and Lr, Lc the output's row and column counts rounded up
+ * to multiples of 64 (e.g. fwd with M = 8192, K = 768, N = 2304 needs 32.5 MB);
+ * larger problems return CARBON_ERR_SCRATCH_LIMIT and enqueue nothing.
+ * The first call on each device looks the array's device address up (not a
+ * stream operation); make that first call before any stream capture.  All
+ * calls share the array and it keeps the last call's contents; nothing in it
+ * needs to start at zero.  Calls whose kernels may overlap on the GPU (other
+ * streams, other host threads) race on the array: order them on one stream. */
+carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, void *out, const void *A,
+                                               const void *B, const void *bias,
+                                               int64_t M, int64_t K, int64_t N,
+                                               carbon_stream_t stream);
 
 /* Synchronises `stream`, then reports (and clears) the device status word
  * that kernels set when a bounded wait gives up (CARBON_ERR_TIMEOUT), or

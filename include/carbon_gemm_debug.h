@@ -13,8 +13,6 @@
 extern "C" {
 #endif
 
-typedef enum { CARBON_PASS_FWD = 0, CARBON_PASS_DX = 1, CARBON_PASS_DW = 2 } carbon_pass_t;
-
 /* Exact tier, float64 value before the output rounding.
  * Runs the same kernel arithmetic as carbon_gemm_{fwd,dx,dw} with
  * CARBON_TIER_EXACT (fixed-order KBN of the float64 products, plus the bias
