@@ -269,22 +269,23 @@ int_prep_kernel(const unsigned short *src, int64_t line_stride, int64_t r_stride
 
 // ---- main kernel --------------------------------------------------------------
 
-constexpr int kStageK = 64;                          // reduction rows per ring stage
+constexpr int kStageK = 32;                          // reduction rows per ring stage
 constexpr int kStages = 4;
 constexpr int kStagesPerChunk = kChunk / kStageK;
 constexpr int kConsumerWarps = 8;
 constexpr int kMainThreads = (kConsumerWarps + 1) * 32;
-constexpr uint32_t kTileBytes = kStageK * kTile * 4; // 16 KiB per operand per stage
+constexpr uint32_t kTileBytes = kStageK * kTile * 4; // 8 KiB per operand per stage
 
 struct __align__(1024) MainSmem {
     int X[kStages][kStageK][kTile];
     int W[kStages][kStageK][kTile];
+    double C[16][kConsumerWarps * 32];               // outer KBN compensation, per output
     uint64_t full[kStages], empty[kStages];
     uint32_t abort;
 };
 
 template <int PASS, bool OUT_F64>
-__global__ void __launch_bounds__(kMainThreads, 1)
+__global__ void __launch_bounds__(kMainThreads, 2)
 exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                  const IArgs p, const int2 *__restrict__ SA, const int2 *__restrict__ SB,
                  int64_t LpA, int64_t LpB, int64_t Rp) {
@@ -337,13 +338,21 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
 
     // ---------------------------------------------------------------- consumers
     const int tx = tid % 16, ty = tid / 16;               // 16 x 16 consumer threads
-    double S[4][4], C[4][4];
-    int G[4][4];
+    double S[4][4];
     long long acc[4][4];
 #pragma unroll
     for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int n = 0; n < 4; ++n) { S[m][n] = 0.0; C[m][n] = 0.0; G[m][n] = 0x7fffffff; acc[m][n] = 0ll; }
+        for (int n = 0; n < 4; ++n) { S[m][n] = 0.0; acc[m][n] = 0ll; sm.C[4 * m + n][tid] = 0.0; }
+    // Outer grain: the running sum S is a multiple of 2^(min over chunks of
+    // rb + cb); (min rb) + (min cb) over the chunks with nonzero products is a
+    // lower bound of that, kept per line (rows of this thread, columns of this
+    // thread).  A line that held inf/NaN makes every later outer step take the
+    // full KBN step.
+    int rbmin[4], cbmin[4];
+    bool rbad[4], cbad[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) { rbmin[m] = 1 << 20; cbmin[m] = 1 << 20; rbad[m] = false; cbad[m] = false; }
 
     for (int g = 0; g < nstages; ++g) {
         const int st = g % kStages;
@@ -378,11 +387,15 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         for (int m = 0; m < 4; ++m) {
             const int2 v = __ldg(&SA[(int64_t)q * LpA + i0 + 4 * ty + m]);
             rbx[m] = v.x; rwx[m] = v.y;
+            if (v.y == kWidthBad) rbad[m] = true;
+            else if (v.y > 0) rbmin[m] = min(rbmin[m], v.x);
         }
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
             const int2 v = __ldg(&SB[(int64_t)q * LpB + j0 + 4 * tx + n]);
             cbw[n] = v.x; cww[n] = v.y;
+            if (v.y == kWidthBad) cbad[n] = true;
+            else if (v.y > 0) cbmin[n] = min(cbmin[n], v.x);
         }
 #pragma unroll
         for (int m = 0; m < 4; ++m)
@@ -407,15 +420,20 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 if (how == 0) P = real ? scaled_int_to_double(acc[m][n], b) : 0.0;
                 else P = chunk_kbn_global(p, i, j, q0, qend);
                 acc[m][n] = 0ll;
-                // P is a multiple of 2^b and S of 2^(min b so far): if both are
-                // multiples of ulp(S + P), the addition is exact and C unchanged.
-                const int gq = (wx == kWidthBad || ww == kWidthBad) ? kGrainBad
-                               : (wx == 0 || ww == 0) ? kGrainZero : (b + 1075) << 20;
-                G[m][n] = min(G[m][n], gq);
+                // P and S are multiples of 2^(rbmin + cbmin): if that is at least
+                // ulp(S + P), the addition is exact and C is unchanged.
+                const int G = (rbad[m] || cbad[n]) ? kGrainBad
+                              : (rbmin[m] + cbmin[n] > (1 << 19)) ? kGrainZero
+                              : (rbmin[m] + cbmin[n] + 1075) << 20;
                 const double t = __dadd_rn(S[m][n], P);
-                const bool inexact = (__double2hiint(t) & 0x7ff00000) > G[m][n];
-                if (!__any_sync(0xffffffffu, inexact)) S[m][n] = t;
-                else kbn_value_step(S[m][n], C[m][n], P);
+                const bool inexact = (__double2hiint(t) & 0x7ff00000) > G;
+                if (!__any_sync(0xffffffffu, inexact)) {
+                    S[m][n] = t;
+                } else {
+                    double c = sm.C[4 * m + n][tid];
+                    kbn_value_step(S[m][n], c, P);
+                    sm.C[4 * m + n][tid] = c;
+                }
             }
     }
 
@@ -428,7 +446,7 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         for (int n = 0; n < 4; ++n) {
             const int64_t j = j0 + 4 * tx + n;
             if (j >= p.cols) continue;
-            double y = __dadd_rn(S[m][n], C[m][n]);
+            double y = __dadd_rn(S[m][n], sm.C[4 * m + n][tid]);
             if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
             const int64_t o = i * p.cols + j;
             if (OUT_F64) static_cast<double *>(p.out)[o] = y;
@@ -442,7 +460,7 @@ cudaError_t launch_main(const CUtensorMap &ma, const CUtensorMap &mb, const IArg
                         const int2 *SA, const int2 *SB, int64_t LpA, int64_t LpB, int64_t Rp,
                         cudaStream_t s) {
     auto kern = exact_int_kernel<PASS, F64>;
-    const int smem = (int)sizeof(MainSmem) + 1024;
+    const int smem = (int)sizeof(MainSmem) + 1024;     // two CTAs per SM fit
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     kern<<<(unsigned)tiles, kMainThreads, smem, s>>>(ma, mb, a, SA, SB, LpA, LpB, Rp);
