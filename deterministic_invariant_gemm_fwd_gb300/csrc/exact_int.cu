@@ -114,41 +114,6 @@ __device__ __noinline__ double chunk_kbn_global(const IArgs &p, int64_t i, int64
     return __dadd_rn(s, c);
 }
 
-// Precise exactness check of one (row, column, chunk) on the integer pipes,
-// run by the whole warp for the output owned by lane `owner` (every lane takes
-// every 32nd reduction index, then the warp reduces): with X, W the integer
-// operands at bases bx, bw, every partial sum is representable if
-// sum |X W| < 2^(53 + t), t the smallest number of trailing zero bits of a
-// nonzero product.  Requires wx, ww <= 31 and wx + ww <= 54 for the owner
-// (so sum |X W| < 2^62).  Returns the verdict to every lane.
-__device__ __forceinline__ bool warp_exact_precise(const IArgs &p, int owner, int64_t i, int64_t j,
-                                                   int64_t q0, int64_t qend, int bx, int bw) {
-    const int lane = threadIdx.x % 32;
-    i = __shfl_sync(0xffffffffu, i, owner);
-    j = __shfl_sync(0xffffffffu, j, owner);
-    bx = __shfl_sync(0xffffffffu, bx, owner);
-    bw = __shfl_sync(0xffffffffu, bw, owner);
-    unsigned long long abs_sum = 0;
-    int tz = 1 << 20;
-    for (int64_t r = q0 + lane; r < qend; r += 32) {
-        int mx, ex, mw, ew;
-        bool bad_x, bad_w;
-        decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bad_x);
-        decode(ld_bits(p.B, r * p.b_sr + j * p.b_sj), mw, ew, bad_w);
-        if (mx == 0 || mw == 0) continue;
-        const long long X = (long long)mx * (1ll << (ex - bx));      // |X| < 2^31
-        const long long W = (long long)mw * (1ll << (ew - bw));
-        const long long prod = X * W;
-        abs_sum += (unsigned long long)(prod < 0 ? -prod : prod);
-        tz = min(tz, __ffsll(prod) - 1);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) abs_sum += __shfl_xor_sync(0xffffffffu, abs_sum, off);
-    tz = __reduce_min_sync(0xffffffffu, tz);
-    if (abs_sum == 0) return true;
-    return tz + 53 >= 64 || abs_sum < (1ull << (tz + 53));
-}
-
 // Per-chunk row/column statistics.  For the A tile the "lines" are rows i, for
 // the B tile columns j.  Every line gets the minimum exponent of its nonzero
 // significand units (base), the maximum, and a flag for inf/NaN.
@@ -211,17 +176,23 @@ __device__ __forceinline__ void gather_stats(const unsigned short *base, int64_t
     }
 }
 
-// ---- pre-pass: int32 operands and (base, width) per (line, chunk) ------------
+// ---- pre-pass: int32 operands and per-(line, chunk) statistics --------------
+
+// Bits needed for an unsigned value (0 for 0): v < 2^bits.
+__device__ __forceinline__ int bit_count(unsigned long long v) { return 64 - __clzll((long long)v); }
 
 // T[r * Lp + line] = m * 2^(e - base(line, chunk of r)) for lines whose width
 // fits int32, else 0 (those outputs never use the integer sum).  Rows past R,
-// up to the padded length Rp, and lines past nlines are 0.
+// up to the padded length Rp, and lines past nlines are 0.  stats[chunk * Lp +
+// line] = (base, width, bits of sum |T|, bits of max |T|) over the chunk.
 template <bool LINE_CONTIG>
 __global__ void __launch_bounds__(kThreads)
 int_prep_kernel(const unsigned short *src, int64_t line_stride, int64_t r_stride, int64_t nlines,
-                int64_t R, int64_t Rp, int64_t Lp, int *T, int2 *stats) {
+                int64_t R, int64_t Rp, int64_t Lp, int *T, int4 *stats) {
     __shared__ LineStats st;
     __shared__ int lbase[kTile], lwidth[kTile];
+    __shared__ unsigned long long lsum[kTile];
+    __shared__ unsigned int lmax[kTile];
     __shared__ unsigned short raw[kTile][kChunk + 2];     // transpose buffer (reduction-contiguous sources)
     const int tid = threadIdx.x;
     const int64_t line0 = (int64_t)blockIdx.x * kTile;
@@ -229,17 +200,17 @@ int_prep_kernel(const unsigned short *src, int64_t line_stride, int64_t r_stride
     const int64_t qend = (R - q0 > kChunk) ? q0 + kChunk : R;
     const int64_t rtop = (Rp - q0 > kChunk) ? q0 + kChunk : Rp;
 
-    if (tid < kTile) { st.emin[tid] = 1 << 20; st.emax[tid] = -(1 << 20); st.bad[tid] = 0; }
+    if (tid < kTile) {
+        st.emin[tid] = 1 << 20; st.emax[tid] = -(1 << 20); st.bad[tid] = 0;
+        lsum[tid] = 0ull; lmax[tid] = 0u;
+    }
     __syncthreads();
     gather_stats<LINE_CONTIG>(src, line_stride, r_stride, line0, nlines, q0, qend, st, tid);
     __syncthreads();
     if (tid < kTile) {
         const int lo = st.emin[tid], hi = st.emax[tid];
-        const int base = (lo > hi) ? 0 : lo;                    // all-zero line: base 0
-        const int width = st.bad[tid] ? kWidthBad : ((lo > hi) ? 0 : hi + 8 - lo);
-        lbase[tid] = base;
-        lwidth[tid] = width;
-        stats[(int64_t)blockIdx.y * Lp + line0 + tid] = make_int2(base, width);
+        lbase[tid] = (lo > hi) ? 0 : lo;                        // all-zero line: base 0
+        lwidth[tid] = st.bad[tid] ? kWidthBad : ((lo > hi) ? 0 : hi + 8 - lo);
     }
     if (!LINE_CONTIG) {
         // coalesced read along the reduction into shared memory
@@ -251,6 +222,9 @@ int_prep_kernel(const unsigned short *src, int64_t line_stride, int64_t r_stride
     }
     __syncthreads();
     const int rows_here = (int)(rtop - q0);
+    // every thread keeps one line (kThreads is a multiple of kTile)
+    unsigned long long my_sum = 0ull;
+    unsigned int my_max = 0u;
     for (int e = tid; e < kTile * rows_here; e += kThreads) {
         const int l = e % kTile, rr = e / kTile;
         const int64_t line = line0 + l, r = q0 + rr;
@@ -264,7 +238,16 @@ int_prep_kernel(const unsigned short *src, int64_t line_stride, int64_t r_stride
             if (m != 0) v = m * (1 << (ex - lbase[l]));          // shift <= 23: |v| < 2^31
         }
         T[r * Lp + line] = v;
+        const unsigned int av = (unsigned int)(v < 0 ? -v : v);
+        my_sum += av;
+        my_max = max(my_max, av);
     }
+    atomicAdd(&lsum[tid % kTile], my_sum);
+    atomicMax(&lmax[tid % kTile], my_max);
+    __syncthreads();
+    if (tid < kTile)
+        stats[(int64_t)blockIdx.y * Lp + line0 + tid] =
+            make_int4(lbase[tid], lwidth[tid], bit_count(lsum[tid]), bit_count(lmax[tid]));
 }
 
 // ---- main kernel --------------------------------------------------------------
@@ -287,8 +270,8 @@ struct __align__(1024) MainSmem {
 template <int PASS, bool OUT_F64>
 __global__ void __launch_bounds__(kMainThreads, 2)
 exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                 const IArgs p, const int2 *__restrict__ SA, const int2 *__restrict__ SB,
-                 int64_t LpA, int64_t LpB, int64_t Rp) {
+                 const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
+                 int64_t LpA, int64_t LpB, int64_t Rp, unsigned char *__restrict__ deferred_flags) {
     extern __shared__ uint8_t smem_raw[];
     MainSmem &sm = *reinterpret_cast<MainSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -353,6 +336,8 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     bool rbad[4], cbad[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) { rbmin[m] = 1 << 20; cbmin[m] = 1 << 20; rbad[m] = false; cbad[m] = false; }
+    // outputs with a chunk the bounds cannot prove: left to the fix-up pass
+    unsigned int deferred = 0u;
 
     for (int g = 0; g < nstages; ++g) {
         const int st = g % kStages;
@@ -380,20 +365,18 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         if (!chunk_end) continue;
         // ---- chunk values and the outer KBN step
         const int q = g / kStagesPerChunk;
-        const int64_t q0 = (int64_t)q * kChunk;
-        const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
-        int rbx[4], rwx[4], cbw[4], cww[4];
+        int rbx[4], rwx[4], rsx[4], rmx[4], cbw[4], cww[4], csw[4], cmw[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const int2 v = __ldg(&SA[(int64_t)q * LpA + i0 + 4 * ty + m]);
-            rbx[m] = v.x; rwx[m] = v.y;
+            const int4 v = __ldg(&SA[(int64_t)q * LpA + i0 + 4 * ty + m]);
+            rbx[m] = v.x; rwx[m] = v.y; rsx[m] = v.z; rmx[m] = v.w;
             if (v.y == kWidthBad) rbad[m] = true;
             else if (v.y > 0) rbmin[m] = min(rbmin[m], v.x);
         }
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-            const int2 v = __ldg(&SB[(int64_t)q * LpB + j0 + 4 * tx + n]);
-            cbw[n] = v.x; cww[n] = v.y;
+            const int4 v = __ldg(&SB[(int64_t)q * LpB + j0 + 4 * tx + n]);
+            cbw[n] = v.x; cww[n] = v.y; csw[n] = v.z; cmw[n] = v.w;
             if (v.y == kWidthBad) cbad[n] = true;
             else if (v.y > 0) cbmin[n] = min(cbmin[n], v.x);
         }
@@ -401,25 +384,17 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         for (int m = 0; m < 4; ++m)
 #pragma unroll
             for (int n = 0; n < 4; ++n) {
+                const int o = 4 * m + n;
                 const int wx = rwx[m], ww = cww[n];
-                const int b = rbx[m] + cbw[n];
-                const int64_t i = i0 + 4 * ty + m, j = j0 + 4 * tx + n;
-                const bool real = (i < p.rows && j < p.cols);
-                // 0: integer sum proven by the widths; 1: needs the precise check;
-                // 2: needs the float64 KBN step
-                int how = (wx <= 31 && ww <= 31 && wx + ww <= 45) || !real ? 0
-                          : (wx <= 31 && ww <= 31 && wx + ww <= 54) ? 1 : 2;
-                unsigned pending = __ballot_sync(0xffffffffu, how == 1);
-                while (pending) {                             // the warp checks each one together
-                    const int owner = __ffs(pending) - 1;
-                    pending &= pending - 1;
-                    const bool ok = warp_exact_precise(p, owner, i, j, q0, qend, rbx[m], cbw[n]);
-                    if (lane == owner) how = ok ? 0 : 2;
-                }
-                double P;
-                if (how == 0) P = real ? scaled_int_to_double(acc[m][n], b) : 0.0;
-                else P = chunk_kbn_global(p, i, j, q0, qend);
+                // every partial sum below 2^53 (in units of 2^(bx + bw)) if
+                // sum_k |X W| < 256 * 2^(wx + ww) <= 2^53, or if
+                // sum_k |X W| <= (sum |X|) (max |W|) or (max |X|) (sum |W|) < 2^53
+                const bool proven = wx <= 31 && ww <= 31 &&
+                                    (wx + ww <= 45 || min(rsx[m] + cmw[n], rmx[m] + csw[n]) <= 53);
+                if (!proven) deferred |= 1u << o;
+                const double P = scaled_int_to_double(acc[m][n], rbx[m] + cbw[n]);
                 acc[m][n] = 0ll;
+                if (deferred & (1u << o)) continue;               // recomputed by the fix-up pass
                 // P and S are multiples of 2^(rbmin + cbmin): if that is at least
                 // ulp(S + P), the addition is exact and C is unchanged.
                 const int G = (rbad[m] || cbad[n]) ? kGrainBad
@@ -427,12 +402,12 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                               : (rbmin[m] + cbmin[n] + 1075) << 20;
                 const double t = __dadd_rn(S[m][n], P);
                 const bool inexact = (__double2hiint(t) & 0x7ff00000) > G;
-                if (!__any_sync(0xffffffffu, inexact)) {
+                if (!inexact) {
                     S[m][n] = t;
                 } else {
-                    double c = sm.C[4 * m + n][tid];
+                    double c = sm.C[o][tid];
                     kbn_value_step(S[m][n], c, P);
-                    sm.C[4 * m + n][tid] = c;
+                    sm.C[o][tid] = c;
                 }
             }
     }
@@ -446,33 +421,92 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         for (int n = 0; n < 4; ++n) {
             const int64_t j = j0 + 4 * tx + n;
             if (j >= p.cols) continue;
+            const int64_t o = i * p.cols + j;
+            const bool later = (deferred >> (4 * m + n)) & 1u;
+            deferred_flags[o] = later ? 1 : 0;
+            if (later) continue;
             double y = __dadd_rn(S[m][n], sm.C[4 * m + n][tid]);
             if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
-            const int64_t o = i * p.cols + j;
             if (OUT_F64) static_cast<double *>(p.out)[o] = y;
             else static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
         }
     }
 }
 
+// ---- fix-up pass: outputs with a chunk the main kernel's bounds left open ------
+//
+// One thread per flagged output recomputes it from the bf16 operands, chunk by
+// chunk: the exact int64 chunk sum when the precise check proves every partial
+// sum representable (sum |X W| < 2^(53 + t), t the fewest trailing zero bits of
+// a product), else the float64 KBN step over the chunk; chunk values are
+// combined with the full KBN step.  All literal-algorithm bits.
+template <bool OUT_F64>
+__global__ void __launch_bounds__(256)
+exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
+                   int64_t LpA, int64_t LpB, const unsigned char *__restrict__ deferred_flags) {
+    const int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (o >= p.rows * p.cols || deferred_flags[o] == 0) return;
+    const int64_t i = o / p.cols, j = o % p.cols;
+    double S = 0.0, C = 0.0;
+    for (int64_t q0 = 0, q = 0; q0 < p.R; q0 += kChunk, ++q) {
+        const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
+        const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
+        double P;
+        bool done = false;
+        if (sa.y <= 31 && sb.y <= 31 && sa.y + sb.y <= 54) {      // |sum| < 2^62: int64 is exact
+            long long I = 0;
+            unsigned long long abs_sum = 0;
+            int tz = 1 << 20;
+            for (int64_t r = q0; r < qend; ++r) {
+                int mx, ex, mw, ew;
+                bool bx_, bw_;
+                decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bx_);
+                decode(ld_bits(p.B, r * p.b_sr + j * p.b_sj), mw, ew, bw_);
+                if (mx == 0 || mw == 0) continue;
+                const long long X = (long long)mx * (1ll << (ex - sa.x));   // |X| < 2^31
+                const long long W = (long long)mw * (1ll << (ew - sb.x));
+                const long long prod = X * W;
+                I += prod;
+                abs_sum += (unsigned long long)(prod < 0 ? -prod : prod);
+                tz = min(tz, __ffsll(prod) - 1);
+            }
+            if (abs_sum == 0 || tz + 53 >= 64 || abs_sum < (1ull << (tz + 53))) {
+                P = scaled_int_to_double(I, sa.x + sb.x);
+                done = true;
+            }
+        }
+        if (!done) P = chunk_kbn_global(p, i, j, q0, qend);
+        kbn_value_step(S, C, P);
+    }
+    double y = __dadd_rn(S, C);
+    if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
+    if (OUT_F64) static_cast<double *>(p.out)[o] = y;
+    else static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
+}
+
 template <int PASS, bool F64>
 cudaError_t launch_main(const CUtensorMap &ma, const CUtensorMap &mb, const IArgs &a, int64_t tiles,
-                        const int2 *SA, const int2 *SB, int64_t LpA, int64_t LpB, int64_t Rp,
-                        cudaStream_t s) {
+                        const int4 *SA, const int4 *SB, int64_t LpA, int64_t LpB, int64_t Rp,
+                        unsigned char *flags, cudaStream_t s) {
     auto kern = exact_int_kernel<PASS, F64>;
     const int smem = (int)sizeof(MainSmem) + 1024;     // two CTAs per SM fit
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    kern<<<(unsigned)tiles, kMainThreads, smem, s>>>(ma, mb, a, SA, SB, LpA, LpB, Rp);
+    kern<<<(unsigned)tiles, kMainThreads, smem, s>>>(ma, mb, a, SA, SB, LpA, LpB, Rp, flags);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const int64_t n = a.rows * a.cols;
+    exact_fixup_kernel<F64><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, SA, SB, LpA, LpB, flags);
+    count_launch();
     return cudaGetLastError();
 }
 
 template <int PASS>
 cudaError_t launch_main_pass(bool f64, const CUtensorMap &ma, const CUtensorMap &mb, const IArgs &a,
-                             int64_t tiles, const int2 *SA, const int2 *SB, int64_t LpA,
-                             int64_t LpB, int64_t Rp, cudaStream_t s) {
-    return f64 ? launch_main<PASS, true>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s)
-               : launch_main<PASS, false>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s);
+                             int64_t tiles, const int4 *SA, const int4 *SB, int64_t LpA,
+                             int64_t LpB, int64_t Rp, unsigned char *flags, cudaStream_t s) {
+    return f64 ? launch_main<PASS, true>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s)
+               : launch_main<PASS, false>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s);
 }
 
 }  // namespace
@@ -499,10 +533,12 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
     const int64_t nchunks = (p.R + kChunk - 1) / kChunk;
     if (nchunks > 65535) return CARBON_ERR_INVALID_ARG;
 
-    // workspace: int32 operands [Rp][Lp] of A and B, then (base, width) per
-    // (chunk, line); stream-ordered, released at the end of this call
+    // workspace: int32 operands [Rp][Lp] of A and B, the statistics of every
+    // (chunk, line), one deferral flag per output; stream-ordered, released at
+    // the end of this call
     const size_t tA = (size_t)Rp * LpA, tB = (size_t)Rp * LpB;
-    const size_t bytes = 4 * (tA + tB) + 8 * (size_t)nchunks * (LpA + LpB);
+    const size_t bytes = 4 * (tA + tB) + 16 * (size_t)nchunks * (LpA + LpB) +
+                         (size_t)p.rows * (size_t)p.cols;
     char *ws = nullptr;
     cudaError_t err = cudaSuccess;
     if (bytes > 0) {
@@ -511,8 +547,9 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
     }
     int *TA = reinterpret_cast<int *>(ws);
     int *TB = TA + tA;
-    int2 *SA = reinterpret_cast<int2 *>(TB + tB);
-    int2 *SB = SA + (size_t)nchunks * LpA;
+    int4 *SA = reinterpret_cast<int4 *>(TB + tB);
+    int4 *SB = SA + (size_t)nchunks * LpA;
+    unsigned char *flags = reinterpret_cast<unsigned char *>(SB + (size_t)nchunks * LpB);
 
     const bool a_contig = (p.pass == CARBON_PASS_DW), b_contig = (p.pass != CARBON_PASS_DX);
     if (nchunks > 0) {
@@ -539,9 +576,9 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
     }
     if (err == cudaSuccess) {
         switch (p.pass) {
-        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, stream); break;
-        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, stream); break;
-        default:              err = launch_main_pass<CARBON_PASS_DW>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, stream); break;
+        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, stream); break;
+        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, stream); break;
+        default:              err = launch_main_pass<CARBON_PASS_DW>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, stream); break;
         }
         count_launch();
     }
@@ -632,7 +669,8 @@ extern "C" carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, vo
     const int64_t Rp = ((p.R + 63) / 64) * 64;
     const int64_t nchunks = (p.R + kChunk - 1) / kChunk;
     if (tiles_m * tiles_n > 0x7fffffff || nchunks > 65535) return CARBON_ERR_INVALID_ARG;
-    const double need = 4.0 * (double)Rp * (double)(LpA + LpB) + 8.0 * (double)nchunks * (double)(LpA + LpB);
+    const double need = 4.0 * (double)Rp * (double)(LpA + LpB) +
+                        16.0 * (double)nchunks * (double)(LpA + LpB) + (double)out_elems;
     if (need > (double)kNoAllocScratchBytes) return CARBON_ERR_SCRATCH_LIMIT;
 
     carbon_status_t st = current_device(nullptr, nullptr);
@@ -657,11 +695,13 @@ extern "C" carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, vo
     const size_t tA = (size_t)Rp * LpA, tB = (size_t)Rp * LpB;
     int *TA = static_cast<int *>(scratch);
     int *TB = TA + tA;
-    int2 *SA = reinterpret_cast<int2 *>(TB + tB);
-    int2 *SB = SA + (size_t)nchunks * LpA;
+    int4 *SA = reinterpret_cast<int4 *>(TB + tB);
+    int4 *SB = SA + (size_t)nchunks * LpA;
+    unsigned char *flags = reinterpret_cast<unsigned char *>(SB + (size_t)nchunks * LpB);
 
     // Nothing in the array has to start at zero: the pre-pass writes every
-    // operand word and statistic the main kernel reads, in this same call.
+    // operand word and statistic, and the main kernel every deferral flag,
+    // before they are read in this same call.
     CUtensorMap ma, mb;
     std::memset(&ma, 0, sizeof ma);
     std::memset(&mb, 0, sizeof mb);
@@ -683,9 +723,9 @@ extern "C" carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, vo
     if (err == cudaSuccess) {
         const int64_t tiles = tiles_m * tiles_n;
         switch (p.pass) {
-        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s); break;
-        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s); break;
-        default:              err = launch_main_pass<CARBON_PASS_DW>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, s); break;
+        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s); break;
+        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s); break;
+        default:              err = launch_main_pass<CARBON_PASS_DW>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s); break;
         }
         count_launch();
     }

@@ -46,8 +46,9 @@
  *     owns every buffer.
  *   - Workspace: with CARBON_BF16 the exact tier converts its operands once
  *     into scaled int32 form in a workspace of about 4 bytes per operand
- *     element (plus 8 bytes per 256 reduction indices per output row and
- *     column), taken from the device's stream-ordered memory pool with
+ *     element (plus 16 bytes per 256 reduction indices per output row and
+ *     column, and 1 byte per output), taken from the device's stream-ordered
+ *     memory pool with
  *     cudaMallocAsync on `stream` and released with cudaFreeAsync on `stream`
  *     before the call returns.  If the pool cannot supply it the call returns
  *     CARBON_ERR_CUDA and enqueues nothing.  The fp32 exact tier and the TC
@@ -137,10 +138,11 @@ carbon_status_t carbon_gemm_dw(void *dW, const void *X, const void *dY,
  * pass: CARBON_PASS_FWD (A = X, B = W, bias allowed), CARBON_PASS_DX
  * (A = dY, B = W), CARBON_PASS_DW (A = X, B = dY); out, A, B, bias, M, K, N
  * as in the per-pass entry points; all bf16, device pointers, caller-owned.
- * Limit: 4*Rp*(Lr + Lc) + 8*ceil(R/256)*(Lr + Lc) bytes must fit 64 MiB, where
- * R is the reduction length (K, N or M for fwd, dX, dW), Rp = R rounded up to
- * a multiple of 64, and Lr, Lc the output's row and column counts rounded up
- * to multiples of 64 (e.g. fwd with M = 8192, K = 768, N = 2304 needs 32.5 MB);
+ * Limit: 4*Rp*(Lr + Lc) + 16*ceil(R/256)*(Lr + Lc) + rows*cols bytes must fit
+ * 64 MiB, where R is the reduction length (K, N or M for fwd, dX, dW), Rp = R
+ * rounded up to a multiple of 64, Lr, Lc the output's row and column counts
+ * rounded up to multiples of 64, and rows*cols the output's size (e.g. fwd
+ * with M = 8192, K = 768, N = 2304 needs 51.6 MB);
  * larger problems return CARBON_ERR_SCRATCH_LIMIT and enqueue nothing.
  * The first call on each device looks the array's device address up (not a
  * stream operation); make that first call before any stream capture.  All
