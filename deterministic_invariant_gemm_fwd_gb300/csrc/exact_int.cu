@@ -114,6 +114,48 @@ __device__ __noinline__ double chunk_kbn_global(const IArgs &p, int64_t i, int64
     return __dadd_rn(s, c);
 }
 
+// Precise exactness check of one (row, column, chunk), run by the whole warp
+// for the output owned by lane `owner`: every lane loads its eight reduction
+// indices up front (one memory latency), then the warp reduces sum |X W| and
+// the fewest trailing zero bits t of a nonzero product; every partial sum is
+// representable if sum |X W| < 2^(53 + t).  Requires wx, ww <= 31 and
+// wx + ww <= 54 for the owner, so sum |X W| < 2^62.  Verdict to every lane.
+__device__ __forceinline__ bool warp_exact_precise(const IArgs &p, int owner, int64_t i, int64_t j,
+                                                   int64_t q0, int64_t qend, int bx, int bw) {
+    const int lane = threadIdx.x % 32;
+    i = __shfl_sync(0xffffffffu, i, owner);
+    j = __shfl_sync(0xffffffffu, j, owner);
+    bx = __shfl_sync(0xffffffffu, bx, owner);
+    bw = __shfl_sync(0xffffffffu, bw, owner);
+    uint32_t hx[kChunk / 32], hw[kChunk / 32];
+#pragma unroll
+    for (int t = 0; t < kChunk / 32; ++t) {
+        const int64_t r = q0 + lane + 32 * t;
+        hx[t] = r < qend ? ld_bits(p.A, i * p.a_si + r * p.a_sr) : 0u;
+        hw[t] = r < qend ? ld_bits(p.B, r * p.b_sr + j * p.b_sj) : 0u;
+    }
+    unsigned long long abs_sum = 0;
+    int tz = 1 << 20;
+#pragma unroll
+    for (int t = 0; t < kChunk / 32; ++t) {
+        int mx, ex, mw, ew;
+        bool bad_x, bad_w;
+        decode(hx[t], mx, ex, bad_x);
+        decode(hw[t], mw, ew, bad_w);
+        if (mx == 0 || mw == 0) continue;
+        const long long X = (long long)mx * (1ll << (ex - bx));      // |X| < 2^31
+        const long long W = (long long)mw * (1ll << (ew - bw));
+        const long long prod = X * W;
+        abs_sum += (unsigned long long)(prod < 0 ? -prod : prod);
+        tz = min(tz, __ffsll(prod) - 1);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) abs_sum += __shfl_xor_sync(0xffffffffu, abs_sum, off);
+    tz = __reduce_min_sync(0xffffffffu, tz);
+    if (abs_sum == 0) return true;
+    return tz + 53 >= 64 || abs_sum < (1ull << (tz + 53));
+}
+
 // Per-chunk row/column statistics.  For the A tile the "lines" are rows i, for
 // the B tile columns j.  Every line gets the minimum exponent of its nonzero
 // significand units (base), the maximum, and a flag for inf/NaN.
@@ -268,7 +310,7 @@ struct __align__(1024) MainSmem {
 };
 
 template <int PASS, bool OUT_F64>
-__global__ void __launch_bounds__(kMainThreads, 2)
+__global__ void __launch_bounds__(kMainThreads, 1)
 exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                  const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
                  int64_t LpA, int64_t LpB, int64_t Rp, unsigned char *__restrict__ deferred_flags) {
@@ -386,11 +428,23 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             for (int n = 0; n < 4; ++n) {
                 const int o = 4 * m + n;
                 const int wx = rwx[m], ww = cww[n];
+                const int64_t i = i0 + 4 * ty + m, j = j0 + 4 * tx + n;
                 // every partial sum below 2^53 (in units of 2^(bx + bw)) if
                 // sum_k |X W| < 256 * 2^(wx + ww) <= 2^53, or if
                 // sum_k |X W| <= (sum |X|) (max |W|) or (max |X|) (sum |W|) < 2^53
-                const bool proven = wx <= 31 && ww <= 31 &&
-                                    (wx + ww <= 45 || min(rsx[m] + cmw[n], rmx[m] + csw[n]) <= 53);
+                const bool fits = wx <= 31 && ww <= 31;
+                bool proven = fits && (wx + ww <= 45 || min(rsx[m] + cmw[n], rmx[m] + csw[n]) <= 53);
+                if (i >= p.rows || j >= p.cols) proven = true;        // padding output
+                const bool checkable = !proven && fits && wx + ww <= 54;
+                unsigned pending = __ballot_sync(0xffffffffu, checkable);
+                while (pending) {                                      // the warp checks together
+                    const int owner = __ffs(pending) - 1;
+                    pending &= pending - 1;
+                    const int64_t q0 = (int64_t)q * kChunk;
+                    const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
+                    const bool ok = warp_exact_precise(p, owner, i, j, q0, qend, rbx[m], cbw[n]);
+                    if (lane == owner) proven = ok;
+                }
                 if (!proven) deferred |= 1u << o;
                 const double P = scaled_int_to_double(acc[m][n], rbx[m] + cbw[n]);
                 acc[m][n] = 0ll;
@@ -433,55 +487,81 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     }
 }
 
-// ---- fix-up pass: outputs with a chunk the main kernel's bounds left open ------
+// ---- fix-up pass: outputs with a chunk the main kernel could not prove ---------
 //
-// One thread per flagged output recomputes it from the bf16 operands, chunk by
-// chunk: the exact int64 chunk sum when the precise check proves every partial
-// sum representable (sum |X W| < 2^(53 + t), t the fewest trailing zero bits of
-// a product), else the float64 KBN step over the chunk; chunk values are
-// combined with the full KBN step.  All literal-algorithm bits.
+// One warp per flagged output recomputes it from the bf16 operands: the lanes
+// take the chunks in turn, each chunk summed exactly in int64 when the precise
+// check proves every partial sum representable (sum |X W| < 2^(53 + t), t the
+// fewest trailing zero bits of a product), else with the float64 KBN step;
+// lane 0 then combines the chunk values in order with the full KBN step, adds
+// the bias and rounds.  Literal-algorithm bits throughout.
+constexpr int kFixWarps = 8;
+constexpr int kFixChunks = 64;                       // chunk values buffered per warp
+
 template <bool OUT_F64>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kFixWarps * 32)
 exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
                    int64_t LpA, int64_t LpB, const unsigned char *__restrict__ deferred_flags) {
-    const int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (o >= p.rows * p.cols || deferred_flags[o] == 0) return;
-    const int64_t i = o / p.cols, j = o % p.cols;
-    double S = 0.0, C = 0.0;
-    for (int64_t q0 = 0, q = 0; q0 < p.R; q0 += kChunk, ++q) {
-        const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
-        const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
-        double P;
-        bool done = false;
-        if (sa.y <= 31 && sb.y <= 31 && sa.y + sb.y <= 54) {      // |sum| < 2^62: int64 is exact
-            long long I = 0;
-            unsigned long long abs_sum = 0;
-            int tz = 1 << 20;
-            for (int64_t r = q0; r < qend; ++r) {
-                int mx, ex, mw, ew;
-                bool bx_, bw_;
-                decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bx_);
-                decode(ld_bits(p.B, r * p.b_sr + j * p.b_sj), mw, ew, bw_);
-                if (mx == 0 || mw == 0) continue;
-                const long long X = (long long)mx * (1ll << (ex - sa.x));   // |X| < 2^31
-                const long long W = (long long)mw * (1ll << (ew - sb.x));
-                const long long prod = X * W;
-                I += prod;
-                abs_sum += (unsigned long long)(prod < 0 ? -prod : prod);
-                tz = min(tz, __ffsll(prod) - 1);
+    __shared__ double vals[kFixWarps][kFixChunks];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t n = p.rows * p.cols;
+    const int64_t base = (blockIdx.x * (int64_t)kFixWarps + warp) * 32;
+    const int64_t mine = base + lane;
+    unsigned pending = __ballot_sync(0xffffffffu, mine < n && deferred_flags[mine] != 0);
+    const int64_t nchunks = (p.R + kChunk - 1) / kChunk;
+    while (pending) {
+        const int who = __ffs(pending) - 1;
+        pending &= pending - 1;
+        const int64_t o = base + who;
+        const int64_t i = o / p.cols, j = o % p.cols;
+        double S = 0.0, C = 0.0;
+        for (int64_t c0 = 0; c0 < nchunks; c0 += kFixChunks) {
+            const int64_t cn = (nchunks - c0 < kFixChunks) ? nchunks - c0 : kFixChunks;
+            for (int64_t c = lane; c < cn; c += 32) {
+                const int64_t q = c0 + c;
+                const int64_t q0 = q * kChunk;
+                const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
+                const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
+                double P = 0.0;
+                bool done = false;
+                if (sa.y <= 31 && sb.y <= 31 && sa.y + sb.y <= 54) {  // |sum| < 2^62: int64 exact
+                    long long I = 0;
+                    unsigned long long abs_sum = 0;
+                    int tz = 1 << 20;
+#pragma unroll 8
+                    for (int64_t r = q0; r < qend; ++r) {
+                        int mx, ex, mw, ew;
+                        bool bx_, bw_;
+                        decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bx_);
+                        decode(ld_bits(p.B, r * p.b_sr + j * p.b_sj), mw, ew, bw_);
+                        if (mx == 0 || mw == 0) continue;
+                        const long long X = (long long)mx * (1ll << (ex - sa.x));   // |X| < 2^31
+                        const long long W = (long long)mw * (1ll << (ew - sb.x));
+                        const long long prod = X * W;
+                        I += prod;
+                        abs_sum += (unsigned long long)(prod < 0 ? -prod : prod);
+                        tz = min(tz, __ffsll(prod) - 1);
+                    }
+                    if (abs_sum == 0 || tz + 53 >= 64 || abs_sum < (1ull << (tz + 53))) {
+                        P = scaled_int_to_double(I, sa.x + sb.x);
+                        done = true;
+                    }
+                }
+                if (!done) P = chunk_kbn_global(p, i, j, q0, qend);
+                vals[warp][c] = P;
             }
-            if (abs_sum == 0 || tz + 53 >= 64 || abs_sum < (1ull << (tz + 53))) {
-                P = scaled_int_to_double(I, sa.x + sb.x);
-                done = true;
-            }
+            __syncwarp();
+            if (lane == 0)
+                for (int64_t c = 0; c < cn; ++c) kbn_value_step(S, C, vals[warp][c]);
+            __syncwarp();
         }
-        if (!done) P = chunk_kbn_global(p, i, j, q0, qend);
-        kbn_value_step(S, C, P);
+        if (lane == 0) {
+            double y = __dadd_rn(S, C);
+            if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
+            if (OUT_F64) static_cast<double *>(p.out)[o] = y;
+            else static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
+        }
     }
-    double y = __dadd_rn(S, C);
-    if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
-    if (OUT_F64) static_cast<double *>(p.out)[o] = y;
-    else static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
 }
 
 template <int PASS, bool F64>
@@ -496,7 +576,9 @@ cudaError_t launch_main(const CUtensorMap &ma, const CUtensorMap &mb, const IArg
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     const int64_t n = a.rows * a.cols;
-    exact_fixup_kernel<F64><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, SA, SB, LpA, LpB, flags);
+    const int64_t per_block = (int64_t)kFixWarps * 32;
+    exact_fixup_kernel<F64><<<(unsigned)((n + per_block - 1) / per_block), kFixWarps * 32, 0, s>>>(
+        a, SA, SB, LpA, LpB, flags);
     count_launch();
     return cudaGetLastError();
 }
