@@ -489,71 +489,93 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
 
 // ---- fix-up pass: outputs with a chunk the main kernel could not prove ---------
 //
-// One warp per flagged output recomputes it from the bf16 operands: the lanes
-// take the chunks in turn, each chunk summed exactly in int64 when the precise
-// check proves every partial sum representable (sum |X W| < 2^(53 + t), t the
-// fewest trailing zero bits of a product), else with the float64 KBN step;
-// lane 0 then combines the chunk values in order with the full KBN step, adds
-// the bias and rounds.  Literal-algorithm bits throughout.
+// One warp per flagged output recomputes it from the bf16 operands, chunk by
+// chunk in order.  The 32 lanes load a chunk's 256 operand pairs at once and
+// reduce the exact int64 sum, sum |X W| and the fewest trailing zero bits t of
+// a product; if every partial sum is provably representable (sum |X W| <
+// 2^(53 + t)) the chunk value is the exact sum, else lane 0 runs the float64
+// KBN step over the chunk from shared memory.  Lane 0 combines the chunk
+// values with the full KBN step, adds the bias and rounds.  Literal-algorithm
+// bits throughout.
 constexpr int kFixWarps = 8;
-constexpr int kFixChunks = 64;                       // chunk values buffered per warp
 
 template <bool OUT_F64>
 __global__ void __launch_bounds__(kFixWarps * 32)
 exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
                    int64_t LpA, int64_t LpB, const unsigned char *__restrict__ deferred_flags) {
-    __shared__ double vals[kFixWarps][kFixChunks];
+    __shared__ double xs[kFixWarps][kChunk], ws[kFixWarps][kChunk];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t n = p.rows * p.cols;
     const int64_t base = (blockIdx.x * (int64_t)kFixWarps + warp) * 32;
     const int64_t mine = base + lane;
     unsigned pending = __ballot_sync(0xffffffffu, mine < n && deferred_flags[mine] != 0);
-    const int64_t nchunks = (p.R + kChunk - 1) / kChunk;
     while (pending) {
         const int who = __ffs(pending) - 1;
         pending &= pending - 1;
         const int64_t o = base + who;
         const int64_t i = o / p.cols, j = o % p.cols;
         double S = 0.0, C = 0.0;
-        for (int64_t c0 = 0; c0 < nchunks; c0 += kFixChunks) {
-            const int64_t cn = (nchunks - c0 < kFixChunks) ? nchunks - c0 : kFixChunks;
-            for (int64_t c = lane; c < cn; c += 32) {
-                const int64_t q = c0 + c;
-                const int64_t q0 = q * kChunk;
-                const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
-                const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
-                double P = 0.0;
-                bool done = false;
-                if (sa.y <= 31 && sb.y <= 31 && sa.y + sb.y <= 54) {  // |sum| < 2^62: int64 exact
-                    long long I = 0;
-                    unsigned long long abs_sum = 0;
-                    int tz = 1 << 20;
-#pragma unroll 8
-                    for (int64_t r = q0; r < qend; ++r) {
-                        int mx, ex, mw, ew;
-                        bool bx_, bw_;
-                        decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bx_);
-                        decode(ld_bits(p.B, r * p.b_sr + j * p.b_sj), mw, ew, bw_);
-                        if (mx == 0 || mw == 0) continue;
-                        const long long X = (long long)mx * (1ll << (ex - sa.x));   // |X| < 2^31
-                        const long long W = (long long)mw * (1ll << (ew - sb.x));
-                        const long long prod = X * W;
-                        I += prod;
-                        abs_sum += (unsigned long long)(prod < 0 ? -prod : prod);
-                        tz = min(tz, __ffsll(prod) - 1);
-                    }
-                    if (abs_sum == 0 || tz + 53 >= 64 || abs_sum < (1ull << (tz + 53))) {
-                        P = scaled_int_to_double(I, sa.x + sb.x);
-                        done = true;
+        for (int64_t q0 = 0, q = 0; q0 < p.R; q0 += kChunk, ++q) {
+            const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
+            const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
+            uint32_t hx[kChunk / 32], hw[kChunk / 32];
+#pragma unroll
+            for (int t = 0; t < kChunk / 32; ++t) {
+                const int64_t r = q0 + lane + 32 * t;
+                hx[t] = r < qend ? ld_bits(p.A, i * p.a_si + r * p.a_sr) : 0u;
+                hw[t] = r < qend ? ld_bits(p.B, r * p.b_sr + j * p.b_sj) : 0u;
+            }
+            bool exact = false;
+            long long I = 0;
+            if (sa.y <= 31 && sb.y <= 31 && sa.y + sb.y <= 54) {     // |sum| < 2^62: int64 exact
+                unsigned long long abs_sum = 0;
+                int tz = 1 << 20;
+#pragma unroll
+                for (int t = 0; t < kChunk / 32; ++t) {
+                    int mx, ex, mw, ew;
+                    bool bx_, bw_;
+                    decode(hx[t], mx, ex, bx_);
+                    decode(hw[t], mw, ew, bw_);
+                    if (mx == 0 || mw == 0) continue;
+                    const long long X = (long long)mx * (1ll << (ex - sa.x));   // |X| < 2^31
+                    const long long W = (long long)mw * (1ll << (ew - sb.x));
+                    const long long prod = X * W;
+                    I += prod;
+                    abs_sum += (unsigned long long)(prod < 0 ? -prod : prod);
+                    tz = min(tz, __ffsll(prod) - 1);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    I += __shfl_xor_sync(0xffffffffu, I, off);
+                    abs_sum += __shfl_xor_sync(0xffffffffu, abs_sum, off);
+                }
+                tz = __reduce_min_sync(0xffffffffu, tz);
+                exact = abs_sum == 0 || tz + 53 >= 64 || abs_sum < (1ull << (tz + 53));
+            }
+            double P;
+            if (exact) {
+                P = scaled_int_to_double(I, sa.x + sb.x);
+            } else {
+#pragma unroll
+                for (int t = 0; t < kChunk / 32; ++t) {
+                    xs[warp][lane + 32 * t] = widen_bf16(hx[t]);
+                    ws[warp][lane + 32 * t] = widen_bf16(hw[t]);
+                }
+                __syncwarp();
+                double s_ = 0.0, c_ = 0.0;
+                if (lane == 0) {
+                    const int len = (int)(qend - q0);
+                    for (int k = 0; k < len; ++k) {
+                        const double x = xs[warp][k], w = ws[warp][k];
+                        kbn_product_step(s_, c_, x, w,
+                                         ((uint32_t)__double2hiint(x) & 0x7ff00000u) +
+                                         ((uint32_t)__double2hiint(w) & 0x7ff00000u));
                     }
                 }
-                if (!done) P = chunk_kbn_global(p, i, j, q0, qend);
-                vals[warp][c] = P;
+                __syncwarp();
+                P = __dadd_rn(s_, c_);
             }
-            __syncwarp();
-            if (lane == 0)
-                for (int64_t c = 0; c < cn; ++c) kbn_value_step(S, C, vals[warp][c]);
-            __syncwarp();
+            if (lane == 0) kbn_value_step(S, C, P);
         }
         if (lane == 0) {
             double y = __dadd_rn(S, C);
