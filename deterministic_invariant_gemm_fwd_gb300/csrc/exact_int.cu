@@ -100,20 +100,6 @@ __device__ __forceinline__ double scaled_int_to_double(long long I, int b) {
 
 __device__ __forceinline__ double widen_bf16(uint32_t h) { return widen(h << 16); }
 
-// Chunk value by the float64 KBN step, operands read from global memory.
-__device__ __noinline__ double chunk_kbn_global(const IArgs &p, int64_t i, int64_t j, int64_t q0,
-                                                int64_t qend) {
-    double s = 0.0, c = 0.0;
-    for (int64_t r = q0; r < qend; ++r) {
-        const double x = widen_bf16(ld_bits(p.A, i * p.a_si + r * p.a_sr));
-        const double w = widen_bf16(ld_bits(p.B, r * p.b_sr + j * p.b_sj));
-        kbn_product_step(s, c, x, w,
-                         ((uint32_t)__double2hiint(x) & 0x7ff00000u) +
-                         ((uint32_t)__double2hiint(w) & 0x7ff00000u));
-    }
-    return __dadd_rn(s, c);
-}
-
 // Precise exactness check of one (row, column, chunk), run by the whole warp
 // for the output owned by lane `owner`: every lane loads its eight reduction
 // indices up front (one memory latency), then the warp reduces sum |X W| and
@@ -506,13 +492,16 @@ exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__res
     __shared__ double xs[kFixWarps][kChunk], ws[kFixWarps][kChunk];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t n = p.rows * p.cols;
-    const int64_t base = (blockIdx.x * (int64_t)kFixWarps + warp) * 32;
-    const int64_t mine = base + lane;
+    // outputs interleaved across warps: deferred outputs cluster (whole rows or
+    // columns with an outlier), so neighbours go to different warps
+    const int64_t gw = blockIdx.x * (int64_t)kFixWarps + warp;
+    const int64_t nwarps = (int64_t)gridDim.x * kFixWarps;
+    const int64_t mine = gw + (int64_t)lane * nwarps;
     unsigned pending = __ballot_sync(0xffffffffu, mine < n && deferred_flags[mine] != 0);
     while (pending) {
         const int who = __ffs(pending) - 1;
         pending &= pending - 1;
-        const int64_t o = base + who;
+        const int64_t o = gw + (int64_t)who * nwarps;
         const int64_t i = o / p.cols, j = o % p.cols;
         double S = 0.0, C = 0.0;
         for (int64_t q0 = 0, q = 0; q0 < p.R; q0 += kChunk, ++q) {
