@@ -299,7 +299,8 @@ template <int PASS, bool OUT_F64>
 __global__ void __launch_bounds__(kMainThreads, 1)
 exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                  const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
-                 int64_t LpA, int64_t LpB, int64_t Rp, unsigned char *__restrict__ deferred_flags) {
+                 int64_t LpA, int64_t LpB, int64_t Rp, unsigned int *__restrict__ work_count,
+                 unsigned int *__restrict__ work_list) {
     extern __shared__ uint8_t smem_raw[];
     MainSmem &sm = *reinterpret_cast<MainSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -462,9 +463,10 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             const int64_t j = j0 + 4 * tx + n;
             if (j >= p.cols) continue;
             const int64_t o = i * p.cols + j;
-            const bool later = (deferred >> (4 * m + n)) & 1u;
-            deferred_flags[o] = later ? 1 : 0;
-            if (later) continue;
+            if ((deferred >> (4 * m + n)) & 1u) {                // for the fix-up pass
+                work_list[atomicAdd(work_count, 1u)] = (unsigned int)o;
+                continue;
+            }
             double y = __dadd_rn(S[m][n], sm.C[4 * m + n][tid]);
             if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
             if (OUT_F64) static_cast<double *>(p.out)[o] = y;
@@ -475,7 +477,7 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
 
 // ---- fix-up pass: outputs with a chunk the main kernel could not prove ---------
 //
-// One warp per flagged output recomputes it from the bf16 operands, chunk by
+// One warp per deferred output recomputes it from the bf16 operands, chunk by
 // chunk in order.  The 32 lanes load a chunk's 256 operand pairs at once and
 // reduce the exact int64 sum, sum |X W| and the fewest trailing zero bits t of
 // a product; if every partial sum is provably representable (sum |X W| <
@@ -484,24 +486,22 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
 // values with the full KBN step, adds the bias and rounds.  Literal-algorithm
 // bits throughout.
 constexpr int kFixWarps = 8;
+constexpr int kFixBlocks = 608;                      // 4 per SM of a GB300
 
 template <bool OUT_F64>
 __global__ void __launch_bounds__(kFixWarps * 32)
 exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
-                   int64_t LpA, int64_t LpB, const unsigned char *__restrict__ deferred_flags) {
+                   int64_t LpA, int64_t LpB, const unsigned int *__restrict__ work_count,
+                   const unsigned int *__restrict__ work_list) {
     __shared__ double xs[kFixWarps][kChunk], ws[kFixWarps][kChunk];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int64_t n = p.rows * p.cols;
-    // outputs interleaved across warps: deferred outputs cluster (whole rows or
-    // columns with an outlier), so neighbours go to different warps
+    // the main kernel appended the deferred outputs in no particular order;
+    // each warp takes every nwarps-th entry, one output at a time
     const int64_t gw = blockIdx.x * (int64_t)kFixWarps + warp;
     const int64_t nwarps = (int64_t)gridDim.x * kFixWarps;
-    const int64_t mine = gw + (int64_t)lane * nwarps;
-    unsigned pending = __ballot_sync(0xffffffffu, mine < n && deferred_flags[mine] != 0);
-    while (pending) {
-        const int who = __ffs(pending) - 1;
-        pending &= pending - 1;
-        const int64_t o = gw + (int64_t)who * nwarps;
+    const int64_t count = *work_count;
+    for (int64_t item = gw; item < count; item += nwarps) {
+        const int64_t o = work_list[item];
         const int64_t i = o / p.cols, j = o % p.cols;
         double S = 0.0, C = 0.0;
         for (int64_t q0 = 0, q = 0; q0 < p.R; q0 += kChunk, ++q) {
@@ -578,18 +578,18 @@ exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__res
 template <int PASS, bool F64>
 cudaError_t launch_main(const CUtensorMap &ma, const CUtensorMap &mb, const IArgs &a, int64_t tiles,
                         const int4 *SA, const int4 *SB, int64_t LpA, int64_t LpB, int64_t Rp,
-                        unsigned char *flags, cudaStream_t s) {
-    auto kern = exact_int_kernel<PASS, F64>;
-    const int smem = (int)sizeof(MainSmem) + 1024;     // two CTAs per SM fit
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                        unsigned int *work, cudaStream_t s) {
+    // work[0] = number of deferred outputs, work[1..] = their indices
+    cudaError_t err = cudaMemsetAsync(work, 0, sizeof(unsigned int), s);
     if (err != cudaSuccess) return err;
-    kern<<<(unsigned)tiles, kMainThreads, smem, s>>>(ma, mb, a, SA, SB, LpA, LpB, Rp, flags);
+    auto kern = exact_int_kernel<PASS, F64>;
+    const int smem = (int)sizeof(MainSmem) + 1024;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kern<<<(unsigned)tiles, kMainThreads, smem, s>>>(ma, mb, a, SA, SB, LpA, LpB, Rp, work, work + 1);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const int64_t n = a.rows * a.cols;
-    const int64_t per_block = (int64_t)kFixWarps * 32;
-    exact_fixup_kernel<F64><<<(unsigned)((n + per_block - 1) / per_block), kFixWarps * 32, 0, s>>>(
-        a, SA, SB, LpA, LpB, flags);
+    exact_fixup_kernel<F64><<<kFixBlocks, kFixWarps * 32, 0, s>>>(a, SA, SB, LpA, LpB, work, work + 1);
     count_launch();
     return cudaGetLastError();
 }
@@ -597,15 +597,18 @@ cudaError_t launch_main(const CUtensorMap &ma, const CUtensorMap &mb, const IArg
 template <int PASS>
 cudaError_t launch_main_pass(bool f64, const CUtensorMap &ma, const CUtensorMap &mb, const IArgs &a,
                              int64_t tiles, const int4 *SA, const int4 *SB, int64_t LpA,
-                             int64_t LpB, int64_t Rp, unsigned char *flags, cudaStream_t s) {
-    return f64 ? launch_main<PASS, true>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s)
-               : launch_main<PASS, false>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s);
+                             int64_t LpB, int64_t Rp, unsigned int *work, cudaStream_t s) {
+    return f64 ? launch_main<PASS, true>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, work, s)
+               : launch_main<PASS, false>(ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, work, s);
 }
 
 }  // namespace
 
 carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t stream) {
     if (p.rows == 0 || p.cols == 0) return CARBON_OK;
+    // the deferral list holds 32-bit output indices; larger outputs run the
+    // float64 kernel, which computes the same bits
+    if (p.rows * p.cols >= ((int64_t)1 << 32)) return exact_launch(p, out_f64, stream);
     IArgs a;
     a.A = static_cast<const unsigned short *>(p.A);
     a.B = static_cast<const unsigned short *>(p.B);
@@ -631,7 +634,7 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
     // the end of this call
     const size_t tA = (size_t)Rp * LpA, tB = (size_t)Rp * LpB;
     const size_t bytes = 4 * (tA + tB) + 16 * (size_t)nchunks * (LpA + LpB) +
-                         (size_t)p.rows * (size_t)p.cols;
+                         4 * ((size_t)p.rows * (size_t)p.cols + 1);
     char *ws = nullptr;
     cudaError_t err = cudaSuccess;
     if (bytes > 0) {
@@ -642,7 +645,7 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
     int *TB = TA + tA;
     int4 *SA = reinterpret_cast<int4 *>(TB + tB);
     int4 *SB = SA + (size_t)nchunks * LpA;
-    unsigned char *flags = reinterpret_cast<unsigned char *>(SB + (size_t)nchunks * LpB);
+    unsigned int *work = reinterpret_cast<unsigned int *>(SB + (size_t)nchunks * LpB);
 
     const bool a_contig = (p.pass == CARBON_PASS_DW), b_contig = (p.pass != CARBON_PASS_DX);
     if (nchunks > 0) {
@@ -669,9 +672,9 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
     }
     if (err == cudaSuccess) {
         switch (p.pass) {
-        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, stream); break;
-        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, stream); break;
-        default:              err = launch_main_pass<CARBON_PASS_DW>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, stream); break;
+        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, work, stream); break;
+        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, work, stream); break;
+        default:              err = launch_main_pass<CARBON_PASS_DW>(out_f64, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, work, stream); break;
         }
         count_launch();
     }
@@ -762,8 +765,9 @@ extern "C" carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, vo
     const int64_t Rp = ((p.R + 63) / 64) * 64;
     const int64_t nchunks = (p.R + kChunk - 1) / kChunk;
     if (tiles_m * tiles_n > 0x7fffffff || nchunks > 65535) return CARBON_ERR_INVALID_ARG;
+    if (out_elems >= ((int64_t)1 << 32)) return CARBON_ERR_SCRATCH_LIMIT;
     const double need = 4.0 * (double)Rp * (double)(LpA + LpB) +
-                        16.0 * (double)nchunks * (double)(LpA + LpB) + (double)out_elems;
+                        16.0 * (double)nchunks * (double)(LpA + LpB) + 4.0 * ((double)out_elems + 1.0);
     if (need > (double)kNoAllocScratchBytes) return CARBON_ERR_SCRATCH_LIMIT;
 
     carbon_status_t st = current_device(nullptr, nullptr);
@@ -790,11 +794,12 @@ extern "C" carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, vo
     int *TB = TA + tA;
     int4 *SA = reinterpret_cast<int4 *>(TB + tB);
     int4 *SB = SA + (size_t)nchunks * LpA;
-    unsigned char *flags = reinterpret_cast<unsigned char *>(SB + (size_t)nchunks * LpB);
+    unsigned int *work = reinterpret_cast<unsigned int *>(SB + (size_t)nchunks * LpB);
 
-    // Nothing in the array has to start at zero: the pre-pass writes every
-    // operand word and statistic, and the main kernel every deferral flag,
-    // before they are read in this same call.
+    // Only the deferral counter has to start at zero; it is cleared on the
+    // stream before the main kernel.  The pre-pass writes every operand word
+    // and statistic, and the main kernel every list entry it counts, before
+    // they are read in this same call.
     CUtensorMap ma, mb;
     std::memset(&ma, 0, sizeof ma);
     std::memset(&mb, 0, sizeof mb);
@@ -816,9 +821,9 @@ extern "C" carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, vo
     if (err == cudaSuccess) {
         const int64_t tiles = tiles_m * tiles_n;
         switch (p.pass) {
-        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s); break;
-        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s); break;
-        default:              err = launch_main_pass<CARBON_PASS_DW>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, flags, s); break;
+        case CARBON_PASS_FWD: err = launch_main_pass<CARBON_PASS_FWD>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, work, s); break;
+        case CARBON_PASS_DX:  err = launch_main_pass<CARBON_PASS_DX>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, work, s); break;
+        default:              err = launch_main_pass<CARBON_PASS_DW>(false, ma, mb, a, tiles, SA, SB, LpA, LpB, Rp, work, s); break;
         }
         count_launch();
     }

@@ -47,7 +47,7 @@
  *   - Workspace: with CARBON_BF16 the exact tier converts its operands once
  *     into scaled int32 form in a workspace of about 4 bytes per operand
  *     element (plus 16 bytes per 256 reduction indices per output row and
- *     column, and 1 byte per output), taken from the device's stream-ordered
+ *     column, and 4 bytes per output), taken from the device's stream-ordered
  *     memory pool with
  *     cudaMallocAsync on `stream` and released with cudaFreeAsync on `stream`
  *     before the call returns.  If the pool cannot supply it the call returns
@@ -138,16 +138,16 @@ carbon_status_t carbon_gemm_dw(void *dW, const void *X, const void *dY,
  * pass: CARBON_PASS_FWD (A = X, B = W, bias allowed), CARBON_PASS_DX
  * (A = dY, B = W), CARBON_PASS_DW (A = X, B = dY); out, A, B, bias, M, K, N
  * as in the per-pass entry points; all bf16, device pointers, caller-owned.
- * Limit: 4*Rp*(Lr + Lc) + 16*ceil(R/256)*(Lr + Lc) + rows*cols bytes must fit
- * 64 MiB, where R is the reduction length (K, N or M for fwd, dX, dW), Rp = R
- * rounded up to a multiple of 64, Lr, Lc the output's row and column counts
- * rounded up to multiples of 64, and rows*cols the output's size (e.g. fwd
- * with M = 8192, K = 768, N = 2304 needs 51.6 MB);
+ * Limit: 4*Rp*(Lr + Lc) + 16*ceil(R/256)*(Lr + Lc) + 4*(rows*cols + 1) bytes
+ * must fit 64 MiB, where R is the reduction length (K, N or M for fwd, dX,
+ * dW), Rp = R rounded up to a multiple of 64, Lr, Lc the output's row and
+ * column counts rounded up to multiples of 64, and rows*cols the output's size
+ * (e.g. fwd with M = 8192, K = 768, N = 768 needs 52.8 MB);
  * larger problems return CARBON_ERR_SCRATCH_LIMIT and enqueue nothing.
  * The first call on each device looks the array's device address up (not a
  * stream operation); make that first call before any stream capture.  All
- * calls share the array and it keeps the last call's contents; nothing in it
- * needs to start at zero.  Calls whose kernels may overlap on the GPU (other
+ * calls share the array and it keeps the last call's contents; the one word
+ * that must start at zero is cleared on `stream` by each call.  Calls whose kernels may overlap on the GPU (other
  * streams, other host threads) race on the array: order them on one stream. */
 carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, void *out, const void *A,
                                                const void *B, const void *bias,
