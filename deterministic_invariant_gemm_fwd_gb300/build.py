@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libcarbon_gemm.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "exact_kbn.cu", "exact_int.cu", "tc_gemm.cu", "measure.cu"]
+SOURCES = ["api.cu", "exact_kbn.cu", "exact_int.cu", "exact_tc.cu", "tc_gemm.cu", "measure.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -47,7 +47,7 @@ def _compile(src: str, nvcc: str) -> tuple[str, str]:
     cmd = [nvcc, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
     # the exact tier's float64 arithmetic is written with explicit *_rn
     # intrinsics; forbid any contraction the compiler might add on top
-    if src in ("exact_kbn.cu", "exact_int.cu"):
+    if src in ("exact_kbn.cu", "exact_int.cu", "exact_tc.cu"):
         cmd.insert(1, "-fmad=false")
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

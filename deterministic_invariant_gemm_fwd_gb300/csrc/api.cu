@@ -92,7 +92,7 @@ carbon_status_t run(const Problem &p, int tier, int debug_out, carbon_stream_t s
     if (st != CARBON_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tier == CARBON_TIER_EXACT)
-        return p.dtype == CARBON_BF16 ? exact_int_launch(p, debug_out != 0, s)
+        return p.dtype == CARBON_BF16 ? exact_tc_launch(p, debug_out != 0, s)
                                       : exact_launch(p, debug_out != 0, s);
     return tc_launch(p, debug_out != 0, s);
 }
@@ -157,9 +157,11 @@ carbon_status_t carbon_get_device_status(carbon_stream_t stream) {
     const carbon_status_t tc = carbon::tc_take_device_status();
     const carbon_status_t ms = carbon::measure_take_device_status();
     const carbon_status_t ex = carbon::exact_take_device_status();
+    const carbon_status_t et = carbon::exact_tc_take_device_status();
     if (st != CARBON_OK) return st;
     if (tc != CARBON_OK) return tc;
     if (ex != CARBON_OK) return ex;
+    if (et != CARBON_OK) return et;
     return ms;
 }
 

@@ -53,6 +53,8 @@ carbon_status_t current_device(int *device, int *sm_count);
 carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream);
 // bf16 exact tier on the integer pipes (exact_int.cu); same bits.
 carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t stream);
+// bf16 exact tier on the tensor cores (exact_tc.cu); same bits.
+carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t stream);
 carbon_status_t exact_round_launch(int dtype, void *out, const double *in, int64_t n,
                                    cudaStream_t stream);
 
@@ -63,8 +65,10 @@ cudaError_t encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, co
                                  uint64_t inner, uint64_t outer, uint64_t row_bytes,
                                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
-// Reads and clears the exact tier's device status word (exact_int.cu).
+// Read and clear the exact tier's device status words (exact_int.cu,
+// exact_tc.cu).
 carbon_status_t exact_take_device_status();
+carbon_status_t exact_tc_take_device_status();
 
 // Tensor-core tier (tc_gemm.cu).  out_f32 selects the fp32 pre-rounding output.
 carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream);

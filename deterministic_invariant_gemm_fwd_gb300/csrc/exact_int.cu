@@ -43,6 +43,7 @@
 #include "carbon_internal.h"
 #include "device_sync.cuh"
 #include "exact_common.cuh"
+#include "exact_bf16.cuh"
 
 #include <cstring>
 #include <mutex>
@@ -52,53 +53,16 @@ namespace {
 
 __device__ unsigned int g_exact_status = 0;
 
-constexpr int kChunk = 256;
 constexpr int kTile = 64;                  // CTA output tile: 64 x 64
 constexpr int kThreads = 256;              // 16 x 16 threads, 4 x 4 outputs each
-constexpr int kWidthBad = 99;              // width of a row/column holding inf/NaN
 constexpr int kGrainBad = -0x40000000;
 constexpr int kGrainZero = 0x70000000;
-
-struct IArgs {
-    const unsigned short *A, *B, *bias;
-    void *out;
-    int64_t rows, cols, R;
-    int64_t a_si, a_sr, b_sr, b_sj;
-    int64_t tiles_n;
-};
-
-// bf16 bits -> value = m * 2^e with m a signed integer, |m| < 2^8 (subnormals
-// share the scale of the smallest normal binade).  Flags inf/NaN.
-__device__ __forceinline__ void decode(uint32_t h, int &m, int &e, bool &bad) {
-    const int e8 = (int)((h >> 7) & 0xffu);
-    const int mag = (e8 ? 128 : 0) | (int)(h & 0x7fu);
-    m = (h & 0x8000u) ? -mag : mag;
-    e = (e8 ? e8 : 1) - 134;
-    bad = (e8 == 0xff);
-}
 
 // acc += a * b, 32 x 32 -> 64-bit signed multiply-add in one instruction
 // (two's-complement wrap; callers only use sums they have bounded).
 __device__ __forceinline__ void mad_wide(long long &acc, int a, int b) {
     asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc) : "r"(a), "r"(b));
 }
-
-__device__ __forceinline__ uint32_t ld_bits(const unsigned short *base, int64_t idx) {
-    return (uint32_t)__ldg(base + idx);
-}
-
-// Exact float64 of an integer with at most 53 significant bits, times 2^b.
-__device__ __forceinline__ double scaled_int_to_double(long long I, int b) {
-    if (I == 0) return 0.0;
-    const unsigned long long sign = (unsigned long long)I & 0x8000000000000000ull;
-    const unsigned long long mag = sign ? (unsigned long long)(-I) : (unsigned long long)I;
-    const int lz = __clzll((long long)mag);
-    const int exp2 = 63 - lz + b;                          // value in [2^exp2, 2^(exp2+1))
-    const unsigned long long frac = ((mag << lz) << 1) >> 12;  // 52 stored bits (exact: <= 53 significant)
-    return __longlong_as_double((long long)(sign | ((unsigned long long)(exp2 + 1023) << 52) | frac));
-}
-
-__device__ __forceinline__ double widen_bf16(uint32_t h) { return widen(h << 16); }
 
 // Precise exactness check of one (row, column, chunk), run by the whole warp
 // for the output owned by lane `owner`: every lane loads its eight reduction
@@ -205,9 +169,6 @@ __device__ __forceinline__ void gather_stats(const unsigned short *base, int64_t
 }
 
 // ---- pre-pass: int32 operands and per-(line, chunk) statistics --------------
-
-// Bits needed for an unsigned value (0 for 0): v < 2^bits.
-__device__ __forceinline__ int bit_count(unsigned long long v) { return 64 - __clzll((long long)v); }
 
 // T[r * Lp + line] = m * 2^(e - base(line, chunk of r)) for lines whose width
 // fits int32, else 0 (those outputs never use the integer sum).  Rows past R,
@@ -475,105 +436,6 @@ exact_int_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     }
 }
 
-// ---- fix-up pass: outputs with a chunk the main kernel could not prove ---------
-//
-// One warp per deferred output recomputes it from the bf16 operands, chunk by
-// chunk in order.  The 32 lanes load a chunk's 256 operand pairs at once and
-// reduce the exact int64 sum, sum |X W| and the fewest trailing zero bits t of
-// a product; if every partial sum is provably representable (sum |X W| <
-// 2^(53 + t)) the chunk value is the exact sum, else lane 0 runs the float64
-// KBN step over the chunk from shared memory.  Lane 0 combines the chunk
-// values with the full KBN step, adds the bias and rounds.  Literal-algorithm
-// bits throughout.
-constexpr int kFixWarps = 8;
-constexpr int kFixBlocks = 608;                      // 4 per SM of a GB300
-
-template <bool OUT_F64>
-__global__ void __launch_bounds__(kFixWarps * 32)
-exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
-                   int64_t LpA, int64_t LpB, const unsigned int *__restrict__ work_count,
-                   const unsigned int *__restrict__ work_list) {
-    __shared__ double xs[kFixWarps][kChunk], ws[kFixWarps][kChunk];
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // the main kernel appended the deferred outputs in no particular order;
-    // each warp takes every nwarps-th entry, one output at a time
-    const int64_t gw = blockIdx.x * (int64_t)kFixWarps + warp;
-    const int64_t nwarps = (int64_t)gridDim.x * kFixWarps;
-    const int64_t count = *work_count;
-    for (int64_t item = gw; item < count; item += nwarps) {
-        const int64_t o = work_list[item];
-        const int64_t i = o / p.cols, j = o % p.cols;
-        double S = 0.0, C = 0.0;
-        for (int64_t q0 = 0, q = 0; q0 < p.R; q0 += kChunk, ++q) {
-            const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
-            const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
-            uint32_t hx[kChunk / 32], hw[kChunk / 32];
-#pragma unroll
-            for (int t = 0; t < kChunk / 32; ++t) {
-                const int64_t r = q0 + lane + 32 * t;
-                hx[t] = r < qend ? ld_bits(p.A, i * p.a_si + r * p.a_sr) : 0u;
-                hw[t] = r < qend ? ld_bits(p.B, r * p.b_sr + j * p.b_sj) : 0u;
-            }
-            bool exact = false;
-            long long I = 0;
-            if (sa.y <= 31 && sb.y <= 31 && sa.y + sb.y <= 54) {     // |sum| < 2^62: int64 exact
-                unsigned long long abs_sum = 0;
-                int tz = 1 << 20;
-#pragma unroll
-                for (int t = 0; t < kChunk / 32; ++t) {
-                    int mx, ex, mw, ew;
-                    bool bx_, bw_;
-                    decode(hx[t], mx, ex, bx_);
-                    decode(hw[t], mw, ew, bw_);
-                    if (mx == 0 || mw == 0) continue;
-                    const long long X = (long long)mx * (1ll << (ex - sa.x));   // |X| < 2^31
-                    const long long W = (long long)mw * (1ll << (ew - sb.x));
-                    const long long prod = X * W;
-                    I += prod;
-                    abs_sum += (unsigned long long)(prod < 0 ? -prod : prod);
-                    tz = min(tz, __ffsll(prod) - 1);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    I += __shfl_xor_sync(0xffffffffu, I, off);
-                    abs_sum += __shfl_xor_sync(0xffffffffu, abs_sum, off);
-                }
-                tz = __reduce_min_sync(0xffffffffu, tz);
-                exact = abs_sum == 0 || tz + 53 >= 64 || abs_sum < (1ull << (tz + 53));
-            }
-            double P;
-            if (exact) {
-                P = scaled_int_to_double(I, sa.x + sb.x);
-            } else {
-#pragma unroll
-                for (int t = 0; t < kChunk / 32; ++t) {
-                    xs[warp][lane + 32 * t] = widen_bf16(hx[t]);
-                    ws[warp][lane + 32 * t] = widen_bf16(hw[t]);
-                }
-                __syncwarp();
-                double s_ = 0.0, c_ = 0.0;
-                if (lane == 0) {
-                    const int len = (int)(qend - q0);
-                    for (int k = 0; k < len; ++k) {
-                        const double x = xs[warp][k], w = ws[warp][k];
-                        kbn_product_step(s_, c_, x, w,
-                                         ((uint32_t)__double2hiint(x) & 0x7ff00000u) +
-                                         ((uint32_t)__double2hiint(w) & 0x7ff00000u));
-                    }
-                }
-                __syncwarp();
-                P = __dadd_rn(s_, c_);
-            }
-            if (lane == 0) kbn_value_step(S, C, P);
-        }
-        if (lane == 0) {
-            double y = __dadd_rn(S, C);
-            if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
-            if (OUT_F64) static_cast<double *>(p.out)[o] = y;
-            else static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
-        }
-    }
-}
 
 template <int PASS, bool F64>
 cudaError_t launch_main(const CUtensorMap &ma, const CUtensorMap &mb, const IArgs &a, int64_t tiles,

@@ -1,0 +1,724 @@
+// exact_tc.cu - exact tier for bf16 operands on the tensor cores.
+//
+// Same result as exact_kbn.cu and exact_int.cu, bit for bit: the fixed-order
+// KBN sum of the float64 products (256-wide chunks left to right, chunk values
+// fl(s + c) combined left to right with KBN), bias in float64, one RNE
+// rounding (Carbon README, "How It Works"; sgemm-bi "Determinism contracts"
+// for the downcast).
+//
+// Why integer sums give the literal algorithm's bits.  Over one chunk, row i
+// of A is X[k] * 2^bx(i) and column j of B is W[k] * 2^bw(j) with integers
+// |X| < 2^wx, |W| < 2^ww (the statistics of exact_bf16.cuh).  In the chunk's
+// KBN loop every product, partial sum and correction is a multiple of
+// 2^(bx + bw).  Each step's rounding error is recovered exactly (the larger
+// magnitude goes first, as in Fast2Sum), and the errors also add up exactly:
+// each is at most half an ulp of a partial sum below 2^(wx + ww + 8) grain
+// units, so 256 of them stay below 2^(wx + ww - 37) grain units, which is
+// representable while wx + ww < 90.  Then s + c equals the exact chunk sum and
+// the chunk value fl(s + c) is the exact sum I * 2^(bx + bw) rounded once to
+// float64.  The outer KBN over the chunk values behaves the same way (at most
+// 65535 chunk values, each a multiple of the output grain), so the result
+// before the bias is the exact sum of the chunk values rounded once.
+//
+// Chunk sums on the tensor cores.  I is computed exactly:
+//  * every X is written in balanced base-256 digits, X = sum_a d_a 256^a with
+//    |d_a| <= 128 (digits 0..n-2 in [-128, 127], the top digit the remainder),
+//    likewise W = sum_b e_b 256^b; a digit is an integer of at most 8
+//    significant bits, so it is exact in bf16;
+//  * for one digit pair (a, b) the 256 products d_a e_b are integers of
+//    magnitude <= 2^14, their sum is at most 2^22 in magnitude, and the
+//    tensor core accumulates it in an fp32 accumulator that starts at
+//    1.5 * 2^23: every partial sum stays in [2^23, 2^24], where fp32 spacing
+//    is 1, so the accumulation is exact for any order of addition, and the
+//    accumulator's bit pattern minus that of 1.5 * 2^23 is the pair sum;
+//  * I = sum_{a,b} 256^(a+b) (pair sum), assembled modulo 2^64 with integer
+//    multiply-adds; it is exact when the statistics bound |I| below 2^62.
+// A line of width w <= 31 needs ceil((w + 1) / 8) digits; a tile uses the most
+// any of its rows needs (A side, 1..4 planes per chunk) and always 4 planes on
+// the B side.  One tcgen05.mma of M = 128, N = 256, K = 16 multiplies one A
+// digit plane of 128 rows with all four B digit planes of 64 columns at once,
+// so one "k-group" (the four K=16 slices of each of four 64-deep blocks)
+// yields the pair sums of four digit pairs for a 128 x 64 output tile.
+//
+// Outer sum.  The chunk values (I rounded to 53 significant bits when it is
+// larger) are added exactly in the integer grain 2^(Gx(i) + Gw(j)), the
+// smallest bases of row i and column j over all chunks: T += I << shift.  At
+// the end T * 2^grain is rounded once to float64, the bias added in float64,
+// and the result rounded once to bf16.  Outputs with a line wider than 31 bits
+// (or inf/NaN), a chunk sum that may reach 2^62, or a running sum that would
+// leave 2^62 go to the fix-up kernel of exact_bf16.cuh, which recomputes them
+// from the operands.
+//
+// Structure.
+//  digit_prep_kernel: one block per (group of lines, chunk): statistics and
+//    digit planes [plane][line][R padded to 256] (bf16, reduction index
+//    contiguous), the A side's plane count per (row tile, chunk).
+//  exact_tc_kernel: persistent, one CTA per SM, 128 x 64 output tiles.
+//   warp 0     TMA producer: per chunk the four B planes of each 64-deep block
+//              (4 x 32 KiB, resident for the chunk), and a 3-stage ring of A
+//              plane blocks (16 KiB each), mbarrier transaction counts
+//   warp 1     MMA issuer: two accumulators of 256 TMEM columns used in turn,
+//              one per k-group
+//   warps 2-3  idle (they complete warpgroup 0 for the register split)
+//   warps 4-11 epilogue: warp w reads lanes 32 (w % 4) .. +31 and 32 of the 64
+//              output columns; adds the pair sums into per-output int64 chunk
+//              sums, writes 1.5 * 2^23 back into the accumulator, releases it;
+//              at each chunk end proves the chunk, updates the outer sum; at the
+//              tile end adds the bias, rounds and stores.  Each thread keeps
+//              32 outputs' chunk and outer sums in registers, which is why
+//              warpgroup 0 hands its registers to the epilogue (setmaxnreg).
+// Every wait is bounded (device_sync.cuh); a wait that gives up records
+// CARBON_ERR_TIMEOUT and raises a CTA-wide abort flag, and the CTA still waits
+// for its copies and MMAs in flight and frees its tensor memory.
+#include "carbon_internal.h"
+#include "device_sync.cuh"
+#include "exact_bf16.cuh"
+#include "tcgen05.cuh"
+
+#include <cstring>
+
+namespace carbon {
+namespace {
+
+__device__ unsigned int g_exact_tc_status = 0;
+
+constexpr int kRowTile = 128;                         // output rows per tile = MMA M = TMEM lanes
+constexpr int kColTile = 64;                          // output columns per tile
+constexpr int kPlanes = 4;                            // base-256 digits of a line of width <= 31
+constexpr int kMmaN = kColTile * kPlanes;             // 256
+constexpr int kKBlock = 64;                           // reduction indices per 128-byte swizzle row
+constexpr int kKBlocks = kChunk / kKBlock;            // 4
+constexpr int kUmmaK = 16;
+constexpr int kAStages = 3;
+constexpr int kEpiWarps = 8;
+constexpr int kTcxThreads = 384;                      // warpgroup 0: TMA + MMA; 1-2: epilogue
+// Register split (setmaxnreg): the block is launched at kLaunchRegs per
+// thread; warpgroup 0 gives registers back, warpgroups 1-2 take them:
+// 128 * kRegsLow + 256 * kRegsHigh must not exceed 384 * kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 224;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kTcxThreads * kLaunchRegs, "register split");
+constexpr uint32_t kMagicBits = 0x4B400000u;          // fp32 bits of 1.5 * 2^23
+constexpr uint32_t kABytes = kRowTile * kKBlock * 2;  // 16 KiB
+constexpr uint32_t kBPlaneBytes = kColTile * kKBlock * 2;   // 8 KiB
+constexpr uint32_t kBBytes = kPlanes * kBPlaneBytes;        // 32 KiB
+constexpr uint32_t kTmemCols = 2 * kMmaN;             // 512
+constexpr int kGrainNone = 0x40000000;                // grain of a line with no nonzero chunk
+
+struct __align__(1024) TcxSmem {
+    uint8_t B[kKBlocks][kBBytes];                     // 128 KiB: the chunk's B planes
+    uint8_t A[kAStages][kABytes];                     // 48 KiB: A plane blocks
+    int colG[kEpiWarps][32];                          // grain of each warp's columns
+    uint32_t pk[kEpiWarps][32];                       // packed column words of the current chunk
+    uint64_t afull[kAStages], aempty[kAStages], bfull[kKBlocks], bempty[kKBlocks];
+    uint64_t tfull[2], tempty[2], mdone;
+    uint32_t tmem_slot, abort;
+};
+
+struct TcxArgs {
+    const unsigned short *bias;                       // bf16 [cols] or null
+    void *out;
+    int64_t rows, cols, LpA, LpB;
+    int tiles_m, tiles_n, nchunks;
+    const int4 *SA, *SB;                              // statistics [chunk][Lp]
+    const unsigned char *cntA;                        // A planes per (row tile, chunk)
+    unsigned int *work_count, *work_list;             // deferred outputs
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile uint32_t *flag) {
+    if (mbar_wait(bar, parity)) return true;
+    *flag = 1u;
+    atomicExch(&g_exact_tc_status, (unsigned)CARBON_ERR_TIMEOUT);
+    return false;
+}
+
+// ---- pre-pass: statistics and digit planes ------------------------------------
+
+// Balanced base-256 digits of X in np planes: digits 0 .. np-2 in [-128, 127],
+// digit np-1 the remainder (|remainder| <= 128 when |X| < 2^(8 np - 1)).
+__device__ __forceinline__ void split_digits(int X, int np, int (&d)[kPlanes]) {
+    int x = X;
+#pragma unroll
+    for (int a = 0; a < kPlanes; ++a) {
+        if (a < np - 1) {
+            const int u = x & 0xff, carry = u >> 7;
+            d[a] = u - (carry << 8);
+            x = (x >> 8) + carry;
+        } else if (a == np - 1) {
+            d[a] = x;
+            x = 0;
+        } else {
+            d[a] = 0;
+        }
+    }
+}
+
+// bf16 bits of an integer of magnitude <= 256 (exact).
+__device__ __forceinline__ uint32_t small_int_bf16(int d) {
+    return __float_as_uint((float)d) >> 16;
+}
+
+// Digits a line of this width needs (0: all zero, or not representable).
+__device__ __forceinline__ int digits_for_width(int w) {
+    return (w > 0 && w <= 31) ? (w + 8) / 8 : 0;
+}
+
+constexpr int kPrepThreads = 256;
+constexpr int kRawPitch = kChunk + 8;                 // bf16 per staged line (16-byte rows)
+
+// One block: G lines (G = 128 for A, 64 for B) x one chunk.  The source
+// element (line, r) is src[line * ls + r * rs]; RCONTIG says rs == 1.
+// Writes stats[chunk * Lp + line], digit planes planes[(a * Lp + line) * Rp +
+// r] for a < np (np = 4 if all_planes, else the most any line of the block
+// needs), and cnt[group * nchunks + chunk] = np when cnt is not null.
+template <bool RCONTIG, int G>
+__global__ void __launch_bounds__(kPrepThreads)
+digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs, int64_t nlines,
+                  int64_t R, int64_t Lp, int64_t Rp, int all_planes,
+                  unsigned short *__restrict__ planes, int4 *__restrict__ stats,
+                  unsigned char *__restrict__ cnt, int nchunks) {
+    extern __shared__ __align__(16) unsigned short raw[];   // [G][kRawPitch]
+    __shared__ int lbase[G], lwidth[G];
+    __shared__ int nmax;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int64_t line0 = (int64_t)blockIdx.x * G;
+    const int q = blockIdx.y;
+    const int64_t q0 = (int64_t)q * kChunk;
+    if (tid == 0) nmax = 0;
+
+    // stage the block's operands, coalesced along whichever index is contiguous
+    for (int e = tid; e < G * kChunk; e += kPrepThreads) {
+        const int l = RCONTIG ? e / kChunk : e % G;
+        const int r = RCONTIG ? e % kChunk : e / G;
+        const int64_t line = line0 + l, rr = q0 + r;
+        raw[l * kRawPitch + r] = (line < nlines && rr < R) ? src[line * ls + rr * rs] : (unsigned short)0;
+    }
+    __syncthreads();
+
+    // per-line statistics: warp w takes lines w, w + 8, ...
+    int wmax = 0;
+    for (int l = warp; l < G; l += kPrepThreads / 32) {
+        int lo = 1 << 20, hi = -(1 << 20), bad = 0;
+        int m[kChunk / 32], ex[kChunk / 32];
+#pragma unroll
+        for (int t = 0; t < kChunk / 32; ++t) {
+            bool b;
+            decode(raw[l * kRawPitch + lane + 32 * t], m[t], ex[t], b);
+            if (m[t] != 0) { lo = min(lo, ex[t]); hi = max(hi, ex[t]); }
+            bad |= (int)b;
+        }
+        lo = __reduce_min_sync(0xffffffffu, lo);
+        hi = __reduce_max_sync(0xffffffffu, hi);
+        bad = (int)__reduce_or_sync(0xffffffffu, (unsigned)bad);
+        const int base = (lo > hi) ? 0 : lo;
+        const int width = bad ? kWidthBad : ((lo > hi) ? 0 : hi + 8 - lo);
+        unsigned long long sum = 0ull;
+        unsigned int mx = 0u;
+        if (width > 0 && width <= 31) {
+#pragma unroll
+            for (int t = 0; t < kChunk / 32; ++t) {
+                if (m[t] != 0) {
+                    const unsigned int a = (unsigned int)abs(m[t]) << (ex[t] - base);   // < 2^31
+                    sum += a;
+                    mx = max(mx, a);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if (lane == 0) {
+            lbase[l] = base;
+            lwidth[l] = width;
+            stats[(int64_t)q * Lp + line0 + l] = make_int4(base, width, bit_count(sum), bit_count(mx));
+        }
+        wmax = max(wmax, digits_for_width(width));
+    }
+    if (lane == 0) atomicMax(&nmax, wmax);
+    __syncthreads();
+    const int np = all_planes ? kPlanes : nmax;
+    if (cnt != nullptr && tid == 0) cnt[(int64_t)blockIdx.x * nchunks + q] = (unsigned char)np;
+
+    // digit planes: item (line, 8 consecutive r) -> np 16-byte stores
+    for (int item = tid; item < G * (kChunk / 8); item += kPrepThreads) {
+        const int l = item / (kChunk / 8), g = item % (kChunk / 8);
+        const uint4 h = *reinterpret_cast<const uint4 *>(&raw[l * kRawPitch + 8 * g]);
+        const uint32_t hv[8] = {h.x & 0xffffu, h.x >> 16, h.y & 0xffffu, h.y >> 16,
+                                h.z & 0xffffu, h.z >> 16, h.w & 0xffffu, h.w >> 16};
+        const int base = lbase[l], width = lwidth[l];
+        const bool use = width > 0 && width <= 31;
+        uint32_t packed[kPlanes][4];
+#pragma unroll
+        for (int a = 0; a < kPlanes; ++a)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) packed[a][w] = 0u;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            int mm, ee;
+            bool b;
+            decode(hv[e], mm, ee, b);
+            const int X = (use && mm != 0) ? mm * (1 << (ee - base)) : 0;   // |X| < 2^31
+            int d[kPlanes];
+            split_digits(X, np, d);
+#pragma unroll
+            for (int a = 0; a < kPlanes; ++a)
+                packed[a][e / 2] |= small_int_bf16(d[a]) << (16 * (e & 1));
+        }
+        const int64_t off = (line0 + l) * Rp + q0 + 8 * g;
+#pragma unroll
+        for (int a = 0; a < kPlanes; ++a)
+            if (a < np)
+                *reinterpret_cast<uint4 *>(planes + (int64_t)a * Lp * Rp + off) =
+                    make_uint4(packed[a][0], packed[a][1], packed[a][2], packed[a][3]);
+    }
+}
+
+// ---- main kernel ----------------------------------------------------------------
+
+// I += v * mul (mul = 256^c, c <= 3), 32 x 32 -> 64-bit.
+__device__ __forceinline__ void acc_lo(unsigned long long &I, uint32_t v, uint32_t mul) {
+    asm("mad.wide.u32 %0, %1, %2, %0;" : "+l"(I) : "r"(v), "r"(mul));
+}
+// I += v * mul * 2^32 modulo 2^64 (mul = 256^(c - 4), c >= 4).
+__device__ __forceinline__ void acc_hi(unsigned long long &I, uint32_t v, uint32_t mul) {
+    asm("{\n\t.reg .u32 lo, hi;\n\t"
+        "mov.b64 {lo, hi}, %0;\n\t"
+        "mad.lo.u32 hi, %1, %2, hi;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "+l"(I) : "r"(v), "r"(mul));
+}
+
+// Lets every A block and B plane the producer loaded land before the CTA may
+// exit.  Stage s_next is the next A stage to be armed (parity ph_next);
+// walking back, each stage's last arming completed a phase of known parity.
+// B buffer kb was armed barm[kb] times; its last arming completes phase
+// barm[kb] - 1.
+__device__ __forceinline__ void drain_loads(TcxSmem &sm, int s_next, uint32_t ph_next,
+                                            const uint32_t (&barm)[kKBlocks]) {
+    int s = s_next;
+    uint32_t ph = ph_next;
+    for (int i = 0; i < kAStages; ++i) {
+        if (--s < 0) { s = kAStages - 1; ph ^= 1u; }
+        if (!mbar_wait(smem_addr(&sm.afull[s]), ph)) break;
+    }
+    for (int kb = 0; kb < kKBlocks; ++kb)
+        if (barm[kb] > 0 && !mbar_wait(smem_addr(&sm.bfull[kb]), (barm[kb] - 1u) & 1u)) break;
+}
+
+// I rounded to 53 significant bits, ties to even (|I| >= 2^53, |I| < 2^63).
+__device__ __forceinline__ long long round_to_53_bits(long long I) {
+    const bool neg = I < 0;
+    const unsigned long long mag = neg ? 0ull - (unsigned long long)I : (unsigned long long)I;
+    const int sh = 11 - __clzll((long long)mag);           // 1 .. 10 low bits to drop
+    const unsigned long long rem = mag & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
+    unsigned long long m = mag >> sh;
+    m += (rem > half || (rem == half && (m & 1ull))) ? 1ull : 0ull;
+    const unsigned long long r = m << sh;
+    return neg ? -(long long)r : (long long)r;
+}
+
+template <bool OUT_F64>
+__global__ void __launch_bounds__(kTcxThreads, 1)
+exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const TcxArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    TcxSmem &sm = *reinterpret_cast<TcxSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    volatile uint32_t *abort_flag = &sm.abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(smem_addr(&sm.afull[s]), 1);
+            mbar_init(smem_addr(&sm.aempty[s]), 1);
+        }
+        for (int kb = 0; kb < kKBlocks; ++kb) {
+            mbar_init(smem_addr(&sm.bfull[kb]), 1);
+            mbar_init(smem_addr(&sm.bempty[kb]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&sm.tfull[b]), 1);
+            mbar_init(smem_addr(&sm.tempty[b]), kEpiWarps);
+        }
+        mbar_init(smem_addr(&sm.mdone), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        if (p.nchunks > 0) {                                // maps are blank for an empty reduction
+            prefetch_map(&map_a);
+            prefetch_map(&map_b);
+        }
+    }
+    if (warp == 1) tmem_alloc(smem_addr(&sm.tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_slot;
+    const int ntiles = p.tiles_m * p.tiles_n;
+    const int nchunks = p.nchunks;
+
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+      if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, bu = 0;
+            uint32_t barm[kKBlocks] = {0u, 0u, 0u, 0u};
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < ntiles && !*abort_flag; t += gridDim.x) {
+                const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+                const int i0 = tm * kRowTile, j0 = tn * kColTile;
+                for (int q = 0; ok && q < nchunks; ++q) {
+                    const int nx = p.cntA[(int64_t)tm * nchunks + q];
+                    if (nx == 0) continue;
+                    for (int k = 0; ok && k < nx; ++k)
+                        for (int kb = 0; kb < kKBlocks; ++kb) {
+                            const int x = q * kChunk + kb * kKBlock;
+                            if (k == 0) {
+                                if (!(ok = wait_or_abort(smem_addr(&sm.bempty[kb]), (bu & 1u) ^ 1u, abort_flag))) break;
+                                const uint32_t fb = smem_addr(&sm.bfull[kb]);
+                                mbar_arrive_expect_tx(fb, kBBytes);
+                                ++barm[kb];
+                                for (int b = 0; b < kPlanes; ++b)
+                                    tma_load_2d(smem_addr(&sm.B[kb][b * kBPlaneBytes]), &map_b, fb, x,
+                                                (int)(b * p.LpB + j0));
+                            }
+                            if (!(ok = wait_or_abort(smem_addr(&sm.aempty[s]), ph ^ 1u, abort_flag))) break;
+                            const uint32_t fa = smem_addr(&sm.afull[s]);
+                            mbar_arrive_expect_tx(fa, kABytes);
+                            tma_load_2d(smem_addr(&sm.A[s][0]), &map_a, fa, x, (int)(k * p.LpA + i0));
+                            if (++s == kAStages) { s = 0; ph ^= 1u; }
+                        }
+                    ++bu;
+                }
+            }
+            drain_loads(sm, s, ph, barm);
+        }
+      } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                       ((uint32_t)(kMmaN >> 3) << 17) | ((uint32_t)(kRowTile >> 4) << 24);
+            int s = 0, acc = 0;
+            uint32_t ph = 0, bu = 0, aph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < ntiles && !*abort_flag; t += gridDim.x) {
+                const int tm = t % p.tiles_m;
+                for (int q = 0; ok && q < nchunks; ++q) {
+                    const int nx = p.cntA[(int64_t)tm * nchunks + q];
+                    if (nx == 0) continue;
+                    for (int k = 0; ok && k < nx; ++k) {
+                        if (!(ok = wait_or_abort(smem_addr(&sm.tempty[acc]), aph, abort_flag))) break;
+                        tc_fence_after();
+                        const uint32_t d = tmem + (uint32_t)(acc * kMmaN);
+                        for (int kb = 0; kb < kKBlocks; ++kb) {
+                            if (k == 0 && !(ok = wait_or_abort(smem_addr(&sm.bfull[kb]), bu & 1u, abort_flag))) break;
+                            if (!(ok = wait_or_abort(smem_addr(&sm.afull[s]), ph, abort_flag))) break;
+                            tc_fence_after();
+                            const uint32_t sa = smem_addr(&sm.A[s][0]), sb = smem_addr(&sm.B[kb][0]);
+#pragma unroll
+                            for (int kk = 0; kk < kKBlock / kUmmaK; ++kk)
+                                mma_bf16(d, smem_desc(sa + kk * (kUmmaK * 2), 16, 1024),
+                                         smem_desc(sb + kk * (kUmmaK * 2), 16, 1024), idesc, 1u);
+                            mma_commit(smem_addr(&sm.aempty[s]));
+                            if (k == nx - 1) mma_commit(smem_addr(&sm.bempty[kb]));
+                            if (++s == kAStages) { s = 0; ph ^= 1u; }
+                        }
+                        if (!ok) break;
+                        mma_commit(smem_addr(&sm.tfull[acc]));          // k-group done
+                        if (++acc == 2) { acc = 0; aph ^= 1u; }
+                    }
+                    ++bu;
+                }
+            }
+            // every MMA issued so far has finished before the CTA frees TMEM
+            mma_commit(smem_addr(&sm.mdone));
+            mbar_wait(smem_addr(&sm.mdone), 0);
+        }
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 4;                             // 0..7
+        const int quarter = warp % 4;                        // TMEM lanes 32 quarter .. +31
+        const int half = ew / 4;                             // output columns 32 half .. +31
+        const int rl = quarter * 32 + lane;                  // row within the tile
+        const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * 32);
+        // both accumulators start at 1.5 * 2^23
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int pl = 0; pl < kPlanes; ++pl)
+                tmem_fill32(tlane + (uint32_t)(b * kMmaN + pl * kColTile), kMagicBits);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(smem_addr(&sm.tempty[0]));
+            mbar_arrive(smem_addr(&sm.tempty[1]));
+        }
+        int acc = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < ntiles && !*abort_flag; t += gridDim.x) {
+            const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+            const int64_t i = (int64_t)tm * kRowTile + rl;
+            const int64_t jw = (int64_t)tn * kColTile + half * 32;   // this warp's first column
+            // grains: smallest base over the chunks where the line is nonzero
+            int Gx = kGrainNone, Gw = kGrainNone;
+            for (int q = 0; q < nchunks; ++q) {
+                const int4 r4 = __ldg(&p.SA[(int64_t)q * p.LpA + i]);
+                const int4 c4 = __ldg(&p.SB[(int64_t)q * p.LpB + jw + lane]);
+                if (r4.y > 0 && r4.y <= 31) Gx = min(Gx, r4.x);
+                if (c4.y > 0 && c4.y <= 31) Gw = min(Gw, c4.x);
+            }
+            __syncwarp();
+            sm.colG[ew][lane] = Gw;
+            __syncwarp();
+            unsigned long long I[32], T[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) { I[c] = 0ull; T[c] = 0ull; }
+            uint32_t defer = 0u;
+
+            for (int q = 0; ok && q < nchunks; ++q) {
+                const int nx = p.cntA[(int64_t)tm * nchunks + q];
+                for (int k = 0; k < nx; ++k) {
+                    if (!(ok = wait_or_abort(smem_addr(&sm.tfull[acc]), aph, abort_flag))) break;
+                    tc_fence_after();
+                    const uint32_t ta = tlane + (uint32_t)(acc * kMmaN);
+#pragma unroll
+                    for (int pl = 0; pl < kPlanes; ++pl) {
+                        const int c = k + pl;                // weight 256^c
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t v[16];
+                            tmem_ld16(ta + (uint32_t)(pl * kColTile + 16 * h), v);
+                            if (c <= 3) {
+                                const uint32_t mul = 1u << (8 * c);
+#pragma unroll
+                                for (int jj = 0; jj < 16; ++jj) acc_lo(I[16 * h + jj], v[jj], mul);
+                            } else {
+                                const uint32_t mul = 1u << (8 * (c - 4));
+#pragma unroll
+                                for (int jj = 0; jj < 16; ++jj) acc_hi(I[16 * h + jj], v[jj], mul);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int pl = 0; pl < kPlanes; ++pl)
+                        tmem_fill32(ta + (uint32_t)(pl * kColTile), kMagicBits);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&sm.tempty[acc]));
+                    if (++acc == 2) { acc = 0; aph ^= 1u; }
+                }
+                if (!ok) break;
+                // ---- chunk end: the outer step
+                const int4 rs = __ldg(&p.SA[(int64_t)q * p.LpA + i]);
+                const int4 cl = __ldg(&p.SB[(int64_t)q * p.LpB + jw + lane]);
+                __syncwarp();                                // last chunk's words are read
+                // this lane's column in one word: bits 0-7 shift to the column grain
+                // (255 when larger), 8-14 width, 15-20 bits of sum |W|, 21-26 of max |W|
+                const int shc = (cl.y > 0 && cl.y <= 31) ? min(cl.x - Gw, 255) : 0;
+                sm.pk[ew][lane] = (uint32_t)shc | ((uint32_t)min(cl.y, 127) << 8) |
+                                  ((uint32_t)cl.z << 15) | ((uint32_t)cl.w << 21);
+                __syncwarp();
+                // the accumulators held 1.5 * 2^23 for each of the nx * 4 pairs
+                unsigned long long wsum = 0ull;
+                for (int k = 0; k < nx; ++k) wsum |= 1ull << (8 * k);
+                const unsigned long long corr = (unsigned long long)kMagicBits * (wsum * 0x01010101ull);
+                const int bx = rs.x, wx = rs.y, lsx = rs.z, lmx = rs.w;
+                const int shr = (wx > 0 && wx <= 31) ? bx - Gx : 0;
+                // T += (chunk value in units of the output grain), exactly.  The
+                // chunk value is the exact chunk sum rounded once to float64
+                // (KBN recovers every rounding error of its loop exactly while
+                // wx + ww < 90), i.e. I itself when |I| < 2^53.
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const uint32_t bit = 1u << jj;
+                    long long Ij = (long long)(I[jj] - corr);
+                    I[jj] = 0ull;
+                    const uint32_t w = sm.pk[ew][jj];
+                    const int ww = (int)((w >> 8) & 0x7fu);
+                    const int bnd = min(min(lsx + (int)((w >> 21) & 0x3fu), lmx + (int)((w >> 15) & 0x3fu)),
+                                        wx + ww + 8);                       // |I| < 2^bnd
+                    // I is exact modulo 2^64 and below 2^62 in magnitude
+                    const bool fits = wx <= 31 && ww <= 31 && bnd <= 62;
+                    if (bnd > 53 && (unsigned long long)(Ij + (1ll << 53)) >= (1ull << 54))
+                        Ij = round_to_53_bits(Ij);                          // |result| <= 2^bnd
+                    const int sh = shr + (int)(w & 0xffu);
+                    const long long Tn = (long long)T[jj] + (Ij << (sh & 63));
+                    // no bit of I << sh lost, and the running sum stays below 2^62
+                    const bool ok_add = bnd + sh <= 61 &&
+                                        (unsigned long long)(Tn + (1ll << 62)) < (1ull << 63);
+                    // a zero line (wx or ww 0) adds +0, which changes nothing
+                    const bool live = fits && !(defer & bit) && wx != 0 && ww != 0;
+                    T[jj] = (live && ok_add) ? (unsigned long long)Tn : T[jj];
+                    defer |= (fits && (live ? ok_add : true)) ? 0u : bit;
+                }
+            }
+            if (!ok) break;
+
+            // ---- bias, one rounding, store
+            if (i < p.rows) {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int64_t j = jw + jj;
+                    if (j >= p.cols) break;
+                    const int64_t o = i * p.cols + j;
+                    const uint32_t bit = 1u << jj;
+                    if (defer & bit) {                          // for the fix-up pass
+                        p.work_list[atomicAdd(p.work_count, 1u)] = (unsigned int)o;
+                        continue;
+                    }
+                    // KBN over the chunk values is exact in the same way: the sum
+                    // is the exact total rounded once to float64
+                    double y = round_int_to_double((long long)T[jj], Gx + sm.colG[ew][jj]);
+                    if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
+                    if (OUT_F64) static_cast<double *>(p.out)[o] = y;
+                    else static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
+                }
+            }
+            __syncwarp();                                      // colG / col reads done
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool F64>
+cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const TcxArgs &a, int grid,
+                           const IArgs &ia, const int4 *SA, const int4 *SB, int64_t LpA, int64_t LpB,
+                           unsigned int *work, cudaStream_t s) {
+    auto kern = exact_tc_kernel<F64>;
+    const int smem = (int)sizeof(TcxSmem) + 1024;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, kTcxThreads, smem, s>>>(ma, mb, a);
+    count_launch();
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    exact_fixup_kernel<F64><<<kFixBlocks, kFixWarps * 32, 0, s>>>(ia, SA, SB, LpA, LpB, work, work + 1);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <bool RCONTIG, int G>
+cudaError_t launch_prep(const unsigned short *src, int64_t ls, int64_t rs, int64_t nlines, int64_t R,
+                        int64_t Lp, int64_t Rp, int all_planes, unsigned short *planes, int4 *stats,
+                        unsigned char *cnt, int nchunks, cudaStream_t s) {
+    auto kern = digit_prep_kernel<RCONTIG, G>;
+    const int smem = G * kRawPitch * 2;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    const dim3 grid((unsigned)(Lp / G), (unsigned)nchunks);
+    kern<<<grid, kPrepThreads, smem, s>>>(src, ls, rs, nlines, R, Lp, Rp, all_planes, planes, stats,
+                                          cnt, nchunks);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t stream) {
+    if (p.rows == 0 || p.cols == 0) return CARBON_OK;
+    // deferred outputs are listed by 32-bit index; larger outputs take the
+    // float64 kernel, which computes the same bits
+    if (p.rows * p.cols >= ((int64_t)1 << 32)) return exact_launch(p, out_f64, stream);
+    int dev = 0, sms = 0;
+    carbon_status_t st = current_device(&dev, &sms);
+    if (st != CARBON_OK) return st;
+
+    IArgs ia;
+    ia.A = static_cast<const unsigned short *>(p.A);
+    ia.B = static_cast<const unsigned short *>(p.B);
+    ia.bias = static_cast<const unsigned short *>(p.bias);
+    ia.out = p.out;
+    ia.rows = p.rows; ia.cols = p.cols; ia.R = p.R;
+    switch (p.pass) {
+    case CARBON_PASS_FWD: ia.a_si = p.K; ia.a_sr = 1; ia.b_sr = p.N; ia.b_sj = 1; break;
+    case CARBON_PASS_DX:  ia.a_si = p.N; ia.a_sr = 1; ia.b_sr = 1;   ia.b_sj = p.N; break;
+    default:              ia.a_si = 1;   ia.a_sr = p.K; ia.b_sr = p.N; ia.b_sj = 1; break;
+    }
+    const int64_t tiles_m = (p.rows + kRowTile - 1) / kRowTile;
+    const int64_t tiles_n = (p.cols + kColTile - 1) / kColTile;
+    ia.tiles_n = tiles_n;
+    const int64_t LpA = tiles_m * kRowTile, LpB = tiles_n * kColTile;
+    const int64_t nchunks = (p.R + kChunk - 1) / kChunk;
+    const int64_t Rp = nchunks * kChunk;
+    if (tiles_m * tiles_n > 0x7fffffff || nchunks > 65535 || 4 * LpA > 0x7fffffff ||
+        4 * LpB > 0x7fffffff || Rp > 0x7fffffff)
+        return CARBON_ERR_INVALID_ARG;
+
+    // workspace (stream-ordered, released at the end of this call): digit
+    // planes of A and B, statistics, A plane counts, the deferral counter and list
+    const size_t pA = (size_t)kPlanes * LpA * Rp, pB = (size_t)kPlanes * LpB * Rp;
+    const size_t sA = (size_t)nchunks * LpA, sB = (size_t)nchunks * LpB;
+    const size_t cntBytes = (((size_t)tiles_m * nchunks) + 15) & ~(size_t)15;
+    const size_t bytes = 2 * (pA + pB) + 16 * (sA + sB) + cntBytes +
+                         4 * ((size_t)p.rows * (size_t)p.cols + 1);
+    char *ws = nullptr;
+    cudaError_t err = cudaMallocAsync(reinterpret_cast<void **>(&ws), bytes, stream);
+    if (err != cudaSuccess) return note_cuda(err);
+    unsigned short *PA = reinterpret_cast<unsigned short *>(ws);
+    unsigned short *PB = PA + pA;
+    int4 *SA = reinterpret_cast<int4 *>(PB + pB);
+    int4 *SB = SA + sA;
+    unsigned char *cntA = reinterpret_cast<unsigned char *>(SB + sB);
+    unsigned int *work = reinterpret_cast<unsigned int *>(cntA + cntBytes);
+
+    err = cudaMemsetAsync(work, 0, sizeof(unsigned int), stream);
+    const bool a_rc = (p.pass != CARBON_PASS_DW), b_rc = (p.pass == CARBON_PASS_DX);
+    if (err == cudaSuccess && nchunks > 0)
+        err = a_rc ? launch_prep<true, kRowTile>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, 0, PA, SA, cntA, (int)nchunks, stream)
+                   : launch_prep<false, kRowTile>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, 0, PA, SA, cntA, (int)nchunks, stream);
+    if (err == cudaSuccess && nchunks > 0)
+        err = b_rc ? launch_prep<true, kColTile>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, 1, PB, SB, nullptr, (int)nchunks, stream)
+                   : launch_prep<false, kColTile>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, 1, PB, SB, nullptr, (int)nchunks, stream);
+    // planes as 2-D [4 Lp][Rp] bf16 maps, 64-deep boxes, 128-byte swizzle
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof ma);
+    std::memset(&mb, 0, sizeof mb);
+    if (err == cudaSuccess && nchunks > 0) {
+        err = encode_tensor_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, PA, (uint64_t)Rp,
+                                   (uint64_t)(kPlanes * LpA), (uint64_t)Rp * 2, kKBlock, kRowTile,
+                                   CU_TENSOR_MAP_SWIZZLE_128B);
+        if (err == cudaSuccess)
+            err = encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, PB, (uint64_t)Rp,
+                                       (uint64_t)(kPlanes * LpB), (uint64_t)Rp * 2, kKBlock, kColTile,
+                                       CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (err == cudaSuccess) {
+        TcxArgs a;
+        a.bias = ia.bias;
+        a.out = p.out;
+        a.rows = p.rows; a.cols = p.cols; a.LpA = LpA; a.LpB = LpB;
+        a.tiles_m = (int)tiles_m; a.tiles_n = (int)tiles_n; a.nchunks = (int)nchunks;
+        a.SA = SA; a.SB = SB; a.cntA = cntA;
+        a.work_count = work; a.work_list = work + 1;
+        const int64_t tiles = tiles_m * tiles_n;
+        const int grid = (int)(tiles < sms ? tiles : sms);
+        err = out_f64 ? launch_tc_main<true>(ma, mb, a, grid, ia, SA, SB, LpA, LpB, work, stream)
+                      : launch_tc_main<false>(ma, mb, a, grid, ia, SA, SB, LpA, LpB, work, stream);
+    }
+    const cudaError_t ferr = cudaFreeAsync(ws, stream);
+    if (err == cudaSuccess) err = ferr;
+    return note_cuda(err);
+}
+
+carbon_status_t exact_tc_take_device_status() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_exact_tc_status, sizeof v) != cudaSuccess) return CARBON_OK;
+    if (v != 0) cudaMemcpyToSymbol(g_exact_tc_status, &zero, sizeof zero);
+    return (carbon_status_t)v;
+}
+
+}  // namespace carbon
