@@ -54,12 +54,12 @@
 //    digit planes [plane][line][R padded to 256] (bf16, reduction index
 //    contiguous), the A side's plane count per (row tile, chunk).
 //  exact_tc_kernel: persistent, one CTA per SM, 128 x 64 output tiles.
-//   warp 0     TMA producer: per chunk the four B planes of each 64-deep block
-//              (4 x 32 KiB, resident for the chunk), and a 3-stage ring of A
-//              plane blocks (16 KiB each), mbarrier transaction counts
+//   warps 0, 2 TMA producers of A: a 5-stage ring of A plane blocks (16 KiB
+//              each), alternate loads (one thread's copies complete in turn)
+//   warp 3     TMA producer of B: per chunk the four B planes of each 64-deep
+//              block (4 x 32 KiB, resident for the chunk)
 //   warp 1     MMA issuer: two accumulators of 256 TMEM columns used in turn,
 //              one per k-group
-//   warps 2-3  idle (they complete warpgroup 0 for the register split)
 //   warps 4-11 epilogue: warp w reads lanes 32 (w % 4) .. +31 and 32 of the 64
 //              output columns; adds the pair sums into per-output int64 chunk
 //              sums, writes 1.5 * 2^23 back into the accumulator, releases it;
@@ -89,7 +89,7 @@ constexpr int kMmaN = kColTile * kPlanes;             // 256
 constexpr int kKBlock = 64;                           // reduction indices per 128-byte swizzle row
 constexpr int kKBlocks = kChunk / kKBlock;            // 4
 constexpr int kUmmaK = 16;
-constexpr int kAStages = 3;
+constexpr int kAStages = 5;
 constexpr int kEpiWarps = 8;
 constexpr int kTcxThreads = 384;                      // warpgroup 0: TMA + MMA; 1-2: epilogue
 // Register split (setmaxnreg): the block is launched at kLaunchRegs per
@@ -104,12 +104,12 @@ constexpr uint32_t kABytes = kRowTile * kKBlock * 2;  // 16 KiB
 constexpr uint32_t kBPlaneBytes = kColTile * kKBlock * 2;   // 8 KiB
 constexpr uint32_t kBBytes = kPlanes * kBPlaneBytes;        // 32 KiB
 constexpr uint32_t kTmemCols = 2 * kMmaN;             // 512
-constexpr int kGrainNone = 0x40000000;                // grain of a line with no nonzero chunk
+constexpr int kGrainNone = 0x40404040;                // grain of a line with no nonzero chunk (byte fill)
+constexpr long long kDeferredSum = (long long)0x8000000000000000ull;   // Tout of a deferred output
 
 struct __align__(1024) TcxSmem {
     uint8_t B[kKBlocks][kBBytes];                     // 128 KiB: the chunk's B planes
-    uint8_t A[kAStages][kABytes];                     // 48 KiB: A plane blocks
-    int colG[kEpiWarps][32];                          // grain of each warp's columns
+    uint8_t A[kAStages][kABytes];                     // 80 KiB: A plane blocks
     uint32_t pk[kEpiWarps][32];                       // packed column words of the current chunk
     uint64_t afull[kAStages], aempty[kAStages], bfull[kKBlocks], bempty[kKBlocks];
     uint64_t tfull[2], tempty[2], mdone;
@@ -122,8 +122,11 @@ struct TcxArgs {
     int64_t rows, cols, LpA, LpB;
     int tiles_m, tiles_n, nchunks;
     const int4 *SA, *SB;                              // statistics [chunk][Lp]
+    const int *GA, *GB;                               // line grains (smallest base) [Lp]
     const unsigned char *cntA;                        // A planes per (row tile, chunk)
     unsigned int *work_count, *work_list;             // deferred outputs
+    long long *Tout;                                  // exact sums in the output grain [rows][cols]
+    int vec_t;                                        // Tout rows start 16-byte aligned
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -170,15 +173,17 @@ constexpr int kRawPitch = kChunk + 8;                 // bf16 per staged line (1
 
 // One block: G lines (G = 128 for A, 64 for B) x one chunk.  The source
 // element (line, r) is src[line * ls + r * rs]; RCONTIG says rs == 1.
-// Writes stats[chunk * Lp + line], digit planes planes[(a * Lp + line) * Rp +
-// r] for a < np (np = 4 if all_planes, else the most any line of the block
-// needs), and cnt[group * nchunks + chunk] = np when cnt is not null.
+// Writes stats[chunk * Lp + line], digit planes tile by tile: plane a of line
+// line0 + l at row 4 line0 + a G + l of the [4 Lp][Rp] array, for a < np (np = 4 if all_planes, else the most any line of the block
+// needs), cnt[group * nchunks + chunk] = np when cnt is not null, and lowers
+// grain[line] (preset to kGrainNone) to the line's smallest base over the
+// chunks where it is nonzero and representable.
 template <bool RCONTIG, int G>
 __global__ void __launch_bounds__(kPrepThreads)
 digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs, int64_t nlines,
                   int64_t R, int64_t Lp, int64_t Rp, int all_planes,
                   unsigned short *__restrict__ planes, int4 *__restrict__ stats,
-                  unsigned char *__restrict__ cnt, int nchunks) {
+                  int *__restrict__ grain, unsigned char *__restrict__ cnt, int nchunks) {
     extern __shared__ __align__(16) unsigned short raw[];   // [G][kRawPitch]
     __shared__ int lbase[G], lwidth[G];
     __shared__ int nmax;
@@ -233,6 +238,7 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
             lbase[l] = base;
             lwidth[l] = width;
             stats[(int64_t)q * Lp + line0 + l] = make_int4(base, width, bit_count(sum), bit_count(mx));
+            if (width > 0 && width <= 31) atomicMin(&grain[line0 + l], base);
         }
         wmax = max(wmax, digits_for_width(width));
     }
@@ -266,11 +272,10 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
             for (int a = 0; a < kPlanes; ++a)
                 packed[a][e / 2] |= small_int_bf16(d[a]) << (16 * (e & 1));
         }
-        const int64_t off = (line0 + l) * Rp + q0 + 8 * g;
 #pragma unroll
         for (int a = 0; a < kPlanes; ++a)
             if (a < np)
-                *reinterpret_cast<uint4 *>(planes + (int64_t)a * Lp * Rp + off) =
+                *reinterpret_cast<uint4 *>(planes + (kPlanes * line0 + a * G + l) * Rp + q0 + 8 * g) =
                     make_uint4(packed[a][0], packed[a][1], packed[a][2], packed[a][3]);
     }
 }
@@ -290,24 +295,55 @@ __device__ __forceinline__ void acc_hi(unsigned long long &I, uint32_t v, uint32
         : "+l"(I) : "r"(v), "r"(mul));
 }
 
-// Lets every A block and B plane the producer loaded land before the CTA may
-// exit.  Stage s_next is the next A stage to be armed (parity ph_next);
-// walking back, each stage's last arming completed a phase of known parity.
-// B buffer kb was armed barm[kb] times; its last arming completes phase
-// barm[kb] - 1.
-__device__ __forceinline__ void drain_loads(TcxSmem &sm, int s_next, uint32_t ph_next,
-                                            const uint32_t (&barm)[kKBlocks]) {
-    int s = s_next;
-    uint32_t ph = ph_next;
-    for (int i = 0; i < kAStages; ++i) {
-        if (--s < 0) { s = kAStages - 1; ph ^= 1u; }
-        if (!mbar_wait(smem_addr(&sm.afull[s]), ph)) break;
-    }
-    for (int kb = 0; kb < kKBlocks; ++kb)
-        if (barm[kb] > 0 && !mbar_wait(smem_addr(&sm.bfull[kb]), (barm[kb] - 1u) & 1u)) break;
+// Sum over the nx * 4 digit pairs of a chunk of the accumulators' starting
+// value times the pair's weight: kMagicBits * sum_{a < nx, b < 4} 256^(a+b),
+// modulo 2^64.
+__device__ __forceinline__ unsigned long long magic_sum(int nx) {
+    unsigned long long wa = 0ull;
+    for (int a = 0; a < nx; ++a) wa |= 1ull << (8 * a);
+    return (unsigned long long)kMagicBits * (wa * 0x01010101ull);
 }
 
-// I rounded to 53 significant bits, ties to even (|I| >= 2^53, |I| < 2^63).
+// bf16 bits of RN_bf16(RN_float64(V * 2^s)) (both nearest-even), |V| < 2^63,
+// computed on the integer: false when the result leaves the bf16 normal
+// range (the caller then rounds through float64).
+__device__ __forceinline__ bool round_int_to_bf16(long long V, int s, uint32_t &bits) {
+    if (V == 0) { bits = 0u; return true; }
+    const uint32_t sign = V < 0 ? 0x8000u : 0u;
+    unsigned long long mag = V < 0 ? 0ull - (unsigned long long)V : (unsigned long long)V;
+    int nb = 64 - __clzll((long long)mag);
+    if (nb > 53) {                                          // the float64 rounding
+        const int sh = nb - 53;
+        const unsigned long long rem = mag & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
+        unsigned long long m = mag >> sh;
+        m += (rem > half || (rem == half && (m & 1ull))) ? 1ull : 0ull;
+        mag = m << sh;
+        nb = 64 - __clzll((long long)mag);
+    }
+    uint32_t m8;
+    if (nb > 8) {                                           // the bf16 rounding
+        const int sh = nb - 8;
+        const unsigned long long rem = mag & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
+        m8 = (uint32_t)(mag >> sh);
+        m8 += (rem > half || (rem == half && (m8 & 1u))) ? 1u : 0u;
+        if (m8 == 256u) { m8 = 128u; ++nb; }
+    } else {
+        m8 = (uint32_t)mag << (8 - nb);
+    }
+    const int E = nb - 1 + s;                               // value in [2^E, 2^(E+1))
+    if (E < -126 || E > 127) return false;
+    bits = sign | ((uint32_t)(E + 127) << 7) | (m8 & 0x7fu);
+    return true;
+}
+
+// Output bits the long way: float64 value, bias in float64, one rounding.
+__device__ __noinline__ uint32_t out_bits_f64(long long T, int G, const unsigned short *bias, int64_t j) {
+    double y = round_int_to_double(T, G);
+    if (bias != nullptr) y = __dadd_rn(y, widen_bf16(ld_bits(bias, j)));
+    return exact_round_bf16(y);
+}
+
+// I rounded to 53 significant bits, ties to even (|I| > 2^53 - 1, |I| < 2^63).
 __device__ __forceinline__ long long round_to_53_bits(long long I) {
     const bool neg = I < 0;
     const unsigned long long mag = neg ? 0ull - (unsigned long long)I : (unsigned long long)I;
@@ -360,41 +396,62 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-      if (warp == 0) {
-        // ------------------------------------------------------------ producer
+      if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ A producers
+        // The A loads of the CTA, numbered g = 0, 1, ... in the order the MMA
+        // consumes them, go to stage g % kAStages; warp 0 issues the even g,
+        // warp 2 the odd ones (one thread's copies complete one after another,
+        // so two threads double the rate).
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0, bu = 0;
-            uint32_t barm[kKBlocks] = {0u, 0u, 0u, 0u};
+            const uint32_t mine = warp == 0 ? 0u : 1u;
+            uint32_t g = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < ntiles && !*abort_flag; t += gridDim.x) {
+                const int tm = t % p.tiles_m;
+                for (int q = 0; ok && q < nchunks; ++q) {
+                    const int nx = p.cntA[(int64_t)tm * nchunks + q];
+                    for (int k = 0; ok && k < nx; ++k)
+                        for (int kb = 0; kb < kKBlocks; ++kb, ++g) {
+                            if ((g & 1u) != mine) continue;
+                            const uint32_t st = g % kAStages, use = g / kAStages;
+                            if (!(ok = wait_or_abort(smem_addr(&sm.aempty[st]), (use & 1u) ^ 1u, abort_flag))) break;
+                            const uint32_t fa = smem_addr(&sm.afull[st]);
+                            mbar_arrive_expect_tx(fa, kABytes);
+                            tma_load_2d(smem_addr(&sm.A[st][0]), &map_a, fa, q * kChunk + kb * kKBlock,
+                                        tm * kPlanes * kRowTile + k * kRowTile);
+                        }
+                }
+            }
+            // the last use of each stage lands before the CTA may exit (an
+            // earlier use was consumed, hence landed, before the stage was reused)
+            for (uint32_t st = 0; st < (uint32_t)kAStages && st < g; ++st) {
+                const uint32_t last = st + ((g - 1u - st) / kAStages) * kAStages;
+                if ((last & 1u) == mine && !mbar_wait(smem_addr(&sm.afull[st]), (last / kAStages) & 1u)) break;
+            }
+        }
+      } else if (warp == 3) {
+        // ------------------------------------------------------------ B producer
+        // per chunk the four planes of each 64-deep block, 256 rows in one box
+        if (lane == 0) {
+            uint32_t bu = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < ntiles && !*abort_flag; t += gridDim.x) {
                 const int tm = t % p.tiles_m, tn = t / p.tiles_m;
-                const int i0 = tm * kRowTile, j0 = tn * kColTile;
                 for (int q = 0; ok && q < nchunks; ++q) {
-                    const int nx = p.cntA[(int64_t)tm * nchunks + q];
-                    if (nx == 0) continue;
-                    for (int k = 0; ok && k < nx; ++k)
-                        for (int kb = 0; kb < kKBlocks; ++kb) {
-                            const int x = q * kChunk + kb * kKBlock;
-                            if (k == 0) {
-                                if (!(ok = wait_or_abort(smem_addr(&sm.bempty[kb]), (bu & 1u) ^ 1u, abort_flag))) break;
-                                const uint32_t fb = smem_addr(&sm.bfull[kb]);
-                                mbar_arrive_expect_tx(fb, kBBytes);
-                                ++barm[kb];
-                                for (int b = 0; b < kPlanes; ++b)
-                                    tma_load_2d(smem_addr(&sm.B[kb][b * kBPlaneBytes]), &map_b, fb, x,
-                                                (int)(b * p.LpB + j0));
-                            }
-                            if (!(ok = wait_or_abort(smem_addr(&sm.aempty[s]), ph ^ 1u, abort_flag))) break;
-                            const uint32_t fa = smem_addr(&sm.afull[s]);
-                            mbar_arrive_expect_tx(fa, kABytes);
-                            tma_load_2d(smem_addr(&sm.A[s][0]), &map_a, fa, x, (int)(k * p.LpA + i0));
-                            if (++s == kAStages) { s = 0; ph ^= 1u; }
-                        }
-                    ++bu;
+                    if (p.cntA[(int64_t)tm * nchunks + q] == 0) continue;
+                    for (int kb = 0; kb < kKBlocks; ++kb) {
+                        if (!(ok = wait_or_abort(smem_addr(&sm.bempty[kb]), (bu & 1u) ^ 1u, abort_flag))) break;
+                        const uint32_t fb = smem_addr(&sm.bfull[kb]);
+                        mbar_arrive_expect_tx(fb, kBBytes);
+                        tma_load_2d(smem_addr(&sm.B[kb][0]), &map_b, fb, q * kChunk + kb * kKBlock,
+                                    tn * kPlanes * kColTile);
+                    }
+                    if (ok) ++bu;
                 }
             }
-            drain_loads(sm, s, ph, barm);
+            if (bu > 0)
+                for (int kb = 0; kb < kKBlocks; ++kb)
+                    if (!mbar_wait(smem_addr(&sm.bfull[kb]), (bu - 1u) & 1u)) break;
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -466,44 +523,53 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             const int tm = t % p.tiles_m, tn = t / p.tiles_m;
             const int64_t i = (int64_t)tm * kRowTile + rl;
             const int64_t jw = (int64_t)tn * kColTile + half * 32;   // this warp's first column
-            // grains: smallest base over the chunks where the line is nonzero
-            int Gx = kGrainNone, Gw = kGrainNone;
-            for (int q = 0; q < nchunks; ++q) {
-                const int4 r4 = __ldg(&p.SA[(int64_t)q * p.LpA + i]);
-                const int4 c4 = __ldg(&p.SB[(int64_t)q * p.LpB + jw + lane]);
-                if (r4.y > 0 && r4.y <= 31) Gx = min(Gx, r4.x);
-                if (c4.y > 0 && c4.y <= 31) Gw = min(Gw, c4.x);
-            }
+            const unsigned char *cnt = p.cntA + (int64_t)tm * nchunks;
+            const int Gx = __ldg(&p.GA[i]);                   // output grain: 2^(Gx + Gw)
+            const int Gwl = __ldg(&p.GB[jw + lane]);
+            __syncwarp();                                    // last tile's reads are done
             __syncwarp();
-            sm.colG[ew][lane] = Gw;
-            __syncwarp();
+            // I starts at minus the accumulators' starting values summed over
+            // the chunk's pairs, so that after the k-groups it is the chunk sum
+            int nx = nchunks > 0 ? cnt[0] : 0;
             unsigned long long I[32], T[32];
+            {
+                const unsigned long long c0 = 0ull - magic_sum(nx);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) { I[c] = 0ull; T[c] = 0ull; }
+                for (int c = 0; c < 32; ++c) { I[c] = c0; T[c] = 0ull; }
+            }
             uint32_t defer = 0u;
+            int4 rs = make_int4(0, 0, 0, 0), cl = rs;        // this chunk's statistics, loaded ahead
+            if (nchunks > 0) {
+                rs = __ldg(&p.SA[i]);
+                cl = __ldg(&p.SB[jw + lane]);
+            }
 
             for (int q = 0; ok && q < nchunks; ++q) {
-                const int nx = p.cntA[(int64_t)tm * nchunks + q];
                 for (int k = 0; k < nx; ++k) {
                     if (!(ok = wait_or_abort(smem_addr(&sm.tfull[acc]), aph, abort_flag))) break;
                     tc_fence_after();
                     const uint32_t ta = tlane + (uint32_t)(acc * kMmaN);
+                    // 8 loads of 16 columns (4 planes x 2 halves), each issued
+                    // before the previous one's values are added in
+                    uint32_t va[16], vb[16];
+                    tmem_ld16_issue(ta, va);
 #pragma unroll
-                    for (int pl = 0; pl < kPlanes; ++pl) {
+                    for (int idx = 0; idx < 2 * kPlanes; ++idx) {
+                        const int pl = idx >> 1, h = idx & 1;
+                        uint32_t(&cur)[16] = (idx & 1) ? vb : va;
+                        uint32_t(&nxt)[16] = (idx & 1) ? va : vb;
+                        tmem_wait_ld16(cur);
+                        if (idx + 1 < 2 * kPlanes)
+                            tmem_ld16_issue(ta + (uint32_t)(((idx + 1) >> 1) * kColTile + 16 * ((idx + 1) & 1)), nxt);
                         const int c = k + pl;                // weight 256^c
+                        if (c <= 3) {
+                            const uint32_t mul = 1u << (8 * c);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            uint32_t v[16];
-                            tmem_ld16(ta + (uint32_t)(pl * kColTile + 16 * h), v);
-                            if (c <= 3) {
-                                const uint32_t mul = 1u << (8 * c);
+                            for (int jj = 0; jj < 16; ++jj) acc_lo(I[16 * h + jj], cur[jj], mul);
+                        } else {
+                            const uint32_t mul = 1u << (8 * (c - 4));
 #pragma unroll
-                                for (int jj = 0; jj < 16; ++jj) acc_lo(I[16 * h + jj], v[jj], mul);
-                            } else {
-                                const uint32_t mul = 1u << (8 * (c - 4));
-#pragma unroll
-                                for (int jj = 0; jj < 16; ++jj) acc_hi(I[16 * h + jj], v[jj], mul);
-                            }
+                            for (int jj = 0; jj < 16; ++jj) acc_hi(I[16 * h + jj], cur[jj], mul);
                         }
                     }
 #pragma unroll
@@ -516,73 +582,105 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     if (++acc == 2) { acc = 0; aph ^= 1u; }
                 }
                 if (!ok) break;
-                // ---- chunk end: the outer step
-                const int4 rs = __ldg(&p.SA[(int64_t)q * p.LpA + i]);
-                const int4 cl = __ldg(&p.SB[(int64_t)q * p.LpB + jw + lane]);
+                // ---- chunk end: T += (chunk value in units of the output grain)
+                const int bx = rs.x, wx = rs.y, lsx = rs.z, lmx = rs.w;
+                const int shr = (wx > 0 && wx <= 31) ? bx - Gx : 0;
+                const int shc = (cl.y > 0 && cl.y <= 31) ? min(cl.x - Gwl, 255) : 0;
+                // bounds over the warp's 32 x 32 outputs (its rows and columns are
+                // the lanes' rows and columns)
+                const int wxm = (int)__reduce_max_sync(0xffffffffu, (unsigned)wx);
+                const int wwm = (int)__reduce_max_sync(0xffffffffu, (unsigned)cl.y);
+                const int bndm = min(min((int)__reduce_max_sync(0xffffffffu, (unsigned)lsx) +
+                                             (int)__reduce_max_sync(0xffffffffu, (unsigned)cl.w),
+                                         (int)__reduce_max_sync(0xffffffffu, (unsigned)lmx) +
+                                             (int)__reduce_max_sync(0xffffffffu, (unsigned)cl.z)),
+                                     wxm + wwm + 8);         // every |I| < 2^bndm
                 __syncwarp();                                // last chunk's words are read
                 // this lane's column in one word: bits 0-7 shift to the column grain
                 // (255 when larger), 8-14 width, 15-20 bits of sum |W|, 21-26 of max |W|
-                const int shc = (cl.y > 0 && cl.y <= 31) ? min(cl.x - Gw, 255) : 0;
                 sm.pk[ew][lane] = (uint32_t)shc | ((uint32_t)min(cl.y, 127) << 8) |
                                   ((uint32_t)cl.z << 15) | ((uint32_t)cl.w << 21);
                 __syncwarp();
-                // the accumulators held 1.5 * 2^23 for each of the nx * 4 pairs
-                unsigned long long wsum = 0ull;
-                for (int k = 0; k < nx; ++k) wsum |= 1ull << (8 * k);
-                const unsigned long long corr = (unsigned long long)kMagicBits * (wsum * 0x01010101ull);
-                const int bx = rs.x, wx = rs.y, lsx = rs.z, lmx = rs.w;
-                const int shr = (wx > 0 && wx <= 31) ? bx - Gx : 0;
-                // T += (chunk value in units of the output grain), exactly.  The
-                // chunk value is the exact chunk sum rounded once to float64
-                // (KBN recovers every rounding error of its loop exactly while
-                // wx + ww < 90), i.e. I itself when |I| < 2^53.
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const uint32_t bit = 1u << jj;
-                    long long Ij = (long long)(I[jj] - corr);
-                    I[jj] = 0ull;
-                    const uint32_t w = sm.pk[ew][jj];
-                    const int ww = (int)((w >> 8) & 0x7fu);
-                    const int bnd = min(min(lsx + (int)((w >> 21) & 0x3fu), lmx + (int)((w >> 15) & 0x3fu)),
-                                        wx + ww + 8);                       // |I| < 2^bnd
-                    // I is exact modulo 2^64 and below 2^62 in magnitude
-                    const bool fits = wx <= 31 && ww <= 31 && bnd <= 62;
-                    if (bnd > 53 && (unsigned long long)(Ij + (1ll << 53)) >= (1ull << 54))
-                        Ij = round_to_53_bits(Ij);                          // |result| <= 2^bnd
-                    const int sh = shr + (int)(w & 0xffu);
-                    const long long Tn = (long long)T[jj] + (Ij << (sh & 63));
-                    // no bit of I << sh lost, and the running sum stays below 2^62
-                    const bool ok_add = bnd + sh <= 61 &&
-                                        (unsigned long long)(Tn + (1ll << 62)) < (1ull << 63);
-                    // a zero line (wx or ww 0) adds +0, which changes nothing
-                    const bool live = fits && !(defer & bit) && wx != 0 && ww != 0;
-                    T[jj] = (live && ok_add) ? (unsigned long long)Tn : T[jj];
-                    defer |= (fits && (live ? ok_add : true)) ? 0u : bit;
+                if (q + 1 < nchunks) {                       // next chunk's statistics
+                    rs = __ldg(&p.SA[(int64_t)(q + 1) * p.LpA + i]);
+                    cl = __ldg(&p.SB[(int64_t)(q + 1) * p.LpB + jw + lane]);
                 }
+                // I is exact (modulo 2^64, and below 2^62) when every line fits
+                const bool exact_i = wxm <= 31 && wwm <= 31 && bndm <= 62;
+                uint32_t redo = exact_i ? 0u : 0xffffffffu;  // outputs for the per-output path
+                if (exact_i) {
+                    // T += I << sh wherever |I| <= 2^53 (the chunk value needs no
+                    // rounding), the shift loses no bit and T stays below 2^62;
+                    // zero lines have I = 0, so their shift does not matter
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const long long Ij = (long long)I[jj];
+                        const int sh = shr + (int)(sm.pk[ew][jj] & 0xffu);
+                        const int ib = 64 - __clzll(Ij ^ (Ij >> 63));     // |I| <= 2^ib
+                        const long long Tn = (long long)T[jj] + (Ij << (sh & 63));
+                        const bool ok = ib <= 53 && ib + sh <= 61 &&
+                                        (unsigned long long)(Tn + (1ll << 62)) < (1ull << 63);
+                        T[jj] = ok ? (unsigned long long)Tn : T[jj];
+                        redo |= ok ? 0u : (1u << jj);
+                    }
+                }
+                if (redo != 0u) {
+                    // per output: the chunk value is the exact chunk sum rounded
+                    // once to float64 (KBN recovers every rounding error of its
+                    // loop exactly while wx + ww < 90), i.e. I itself when |I| < 2^53
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const uint32_t bit = 1u << jj;
+                        if (!(redo & bit)) continue;
+                        long long Ij = (long long)I[jj];
+                        const uint32_t w = sm.pk[ew][jj];
+                        const int ww = (int)((w >> 8) & 0x7fu);
+                        const int bnd = min(min(lsx + (int)((w >> 21) & 0x3fu), lmx + (int)((w >> 15) & 0x3fu)),
+                                            wx + ww + 8);                   // |I| < 2^bnd
+                        const bool fits = wx <= 31 && ww <= 31 && bnd <= 62;
+                        if (bnd > 53 && (unsigned long long)(Ij + (1ll << 53)) >= (1ull << 54))
+                            Ij = round_to_53_bits(Ij);                      // |result| <= 2^bnd
+                        const int sh = shr + (int)(w & 0xffu);
+                        const long long Tn = (long long)T[jj] + (Ij << (sh & 63));
+                        // no bit of I << sh lost, and the running sum stays below 2^62
+                        const bool ok_add = bnd + sh <= 61 &&
+                                            (unsigned long long)(Tn + (1ll << 62)) < (1ull << 63);
+                        // a zero line (wx or ww 0) adds +0, which changes nothing
+                        const bool live = fits && !(defer & bit) && wx != 0 && ww != 0;
+                        T[jj] = (live && ok_add) ? (unsigned long long)Tn : T[jj];
+                        defer |= (fits && (live ? ok_add : true)) ? 0u : bit;
+                    }
+                }
+                nx = (q + 1 < nchunks) ? cnt[q + 1] : 0;
+                const unsigned long long c0 = 0ull - magic_sum(nx);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) I[c] = c0;
             }
             if (!ok) break;
 
-            // ---- bias, one rounding, store
+            // ---- the exact sums go to the finalize kernel (deferred outputs: a
+            // sentinel no sum reaches, |T| < 2^62)
             if (i < p.rows) {
+                long long *trow = p.Tout + i * p.cols + jw;
+                if (p.vec_t && jw + 32 <= p.cols) {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int64_t j = jw + jj;
-                    if (j >= p.cols) break;
-                    const int64_t o = i * p.cols + j;
-                    const uint32_t bit = 1u << jj;
-                    if (defer & bit) {                          // for the fix-up pass
-                        p.work_list[atomicAdd(p.work_count, 1u)] = (unsigned int)o;
-                        continue;
+                    for (int c = 0; c < 16; ++c) {
+                        const long long a0 = ((defer >> (2 * c)) & 1u) ? kDeferredSum : (long long)T[2 * c];
+                        const long long a1 = ((defer >> (2 * c + 1)) & 1u) ? kDeferredSum : (long long)T[2 * c + 1];
+                        *reinterpret_cast<longlong2 *>(trow + 2 * c) = make_longlong2(a0, a1);
                     }
-                    // KBN over the chunk values is exact in the same way: the sum
-                    // is the exact total rounded once to float64
-                    double y = round_int_to_double((long long)T[jj], Gx + sm.colG[ew][jj]);
-                    if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
-                    if (OUT_F64) static_cast<double *>(p.out)[o] = y;
-                    else static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        if (jw + jj < p.cols) trow[jj] = ((defer >> jj) & 1u) ? kDeferredSum : (long long)T[jj];
                 }
             }
-            __syncwarp();                                      // colG / col reads done
+            // outputs for the fix-up pass
+            for (uint32_t dm = defer; dm != 0u; dm &= dm - 1u) {
+                const int jj = __ffs((int)dm) - 1;
+                if (i < p.rows && jw + jj < p.cols)
+                    p.work_list[atomicAdd(p.work_count, 1u)] = (unsigned int)(i * p.cols + jw + jj);
+            }
         }
     }
 
@@ -591,6 +689,72 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- finalize: bias and the two roundings ------------------------------------
+//
+// KBN over the chunk values is exact in the same way as inside a chunk: the
+// value before the bias is the exact total T * 2^G rounded once to float64.
+// That rounding is done on the integer, the bias (m * 2^e) joins it exactly,
+// and the sum is rounded once more, to float64 and then to bf16 (both nearest
+// even), all on integers; values outside those fast ranges take the float64
+// route.  One thread per 8 consecutive outputs of a row.
+template <bool OUT_F64>
+__global__ void __launch_bounds__(256)
+exact_finalize_kernel(const long long *__restrict__ Tout, const int *__restrict__ GA,
+                      const int *__restrict__ GB, const unsigned short *__restrict__ bias, void *out,
+                      int64_t rows, int64_t cols, int vec_out) {
+    const int64_t gpr = (cols + 7) / 8;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < rows * gpr;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = g / gpr, j0 = (g % gpr) * 8;
+        const int gx = __ldg(&GA[i]);
+        uint32_t packed[4] = {0u, 0u, 0u, 0u};
+        uint32_t skip = 0u;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int64_t j = j0 + e;
+            if (j >= cols) { skip |= 1u << e; continue; }
+            const long long T = __ldg(&Tout[i * cols + j]);
+            if (T == kDeferredSum) { skip |= 1u << e; continue; }
+            const int G = gx + __ldg(&GB[j]);
+            if (OUT_F64) {
+                double y = round_int_to_double(T, G);
+                if (bias != nullptr) y = __dadd_rn(y, widen_bf16(ld_bits(bias, j)));
+                static_cast<double *>(out)[i * cols + j] = y;
+                continue;
+            }
+            int bm = 0, be = 0;
+            bool bad = false;
+            if (bias != nullptr) decode(ld_bits(bias, j), bm, be, bad);
+            long long Tv = T;
+            int gs = G;
+            bool fused = !bad;
+            if (fused && bm != 0) {
+                if ((unsigned long long)(Tv ^ (Tv >> 63)) >> 53) Tv = round_to_53_bits(Tv);
+                if (be >= G && be - G <= 54) {
+                    Tv += (long long)bm << (be - G);
+                } else if (be < G && G - be <= 9 && (unsigned long long)(Tv + (1ll << 53)) < (1ull << 54)) {
+                    Tv = (Tv << (G - be)) + bm;
+                    gs = be;
+                } else {
+                    fused = false;
+                }
+            }
+            uint32_t bits = 0u;
+            if (!(fused && round_int_to_bf16(Tv, gs, bits))) bits = out_bits_f64(T, G, bias, j);
+            packed[e / 2] |= bits << (16 * (e & 1));
+        }
+        if (OUT_F64) continue;
+        unsigned short *orow = static_cast<unsigned short *>(out) + i * cols + j0;
+        if (skip == 0u && vec_out) {
+            *reinterpret_cast<uint4 *>(orow) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (!((skip >> e) & 1u)) orow[e] = (unsigned short)(packed[e / 2] >> (16 * (e & 1)));
+        }
     }
 }
 
@@ -606,6 +770,16 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
     count_launch();
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    {
+        const int64_t groups = a.rows * ((a.cols + 7) / 8);
+        const int64_t want = (groups + 255) / 256;
+        const int blocks = (int)(want < 8 * 152 ? (want > 0 ? want : 1) : 8 * 152);
+        const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0 && (a.cols % 8) == 0) ? 1 : 0;
+        exact_finalize_kernel<F64><<<blocks, 256, 0, s>>>(a.Tout, a.GA, a.GB, a.bias, a.out, a.rows, a.cols, vec_out);
+        count_launch();
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
     exact_fixup_kernel<F64><<<kFixBlocks, kFixWarps * 32, 0, s>>>(ia, SA, SB, LpA, LpB, work, work + 1);
     count_launch();
     return cudaGetLastError();
@@ -614,14 +788,14 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
 template <bool RCONTIG, int G>
 cudaError_t launch_prep(const unsigned short *src, int64_t ls, int64_t rs, int64_t nlines, int64_t R,
                         int64_t Lp, int64_t Rp, int all_planes, unsigned short *planes, int4 *stats,
-                        unsigned char *cnt, int nchunks, cudaStream_t s) {
+                        int *grain, unsigned char *cnt, int nchunks, cudaStream_t s) {
     auto kern = digit_prep_kernel<RCONTIG, G>;
     const int smem = G * kRawPitch * 2;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     const dim3 grid((unsigned)(Lp / G), (unsigned)nchunks);
     kern<<<grid, kPrepThreads, smem, s>>>(src, ls, rs, nlines, R, Lp, Rp, all_planes, planes, stats,
-                                          cnt, nchunks);
+                                          grain, cnt, nchunks);
     count_launch();
     return cudaGetLastError();
 }
@@ -663,27 +837,37 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     const size_t pA = (size_t)kPlanes * LpA * Rp, pB = (size_t)kPlanes * LpB * Rp;
     const size_t sA = (size_t)nchunks * LpA, sB = (size_t)nchunks * LpB;
     const size_t cntBytes = (((size_t)tiles_m * nchunks) + 15) & ~(size_t)15;
-    const size_t bytes = 2 * (pA + pB) + 16 * (sA + sB) + cntBytes +
-                         4 * ((size_t)p.rows * (size_t)p.cols + 1);
+    const size_t outs = (size_t)p.rows * (size_t)p.cols;
+    const size_t tBytes = (8 * outs + 255) & ~(size_t)255;   // keeps the planes 256-byte aligned
+    const size_t bytes = tBytes + 2 * (pA + pB) + 16 * (sA + sB) + 4 * (size_t)(LpA + LpB) +
+                         cntBytes + 4 * (outs + 1);
     char *ws = nullptr;
     cudaError_t err = cudaMallocAsync(reinterpret_cast<void **>(&ws), bytes, stream);
     if (err != cudaSuccess) return note_cuda(err);
-    unsigned short *PA = reinterpret_cast<unsigned short *>(ws);
+    long long *Tout = reinterpret_cast<long long *>(ws);
+    unsigned short *PA = reinterpret_cast<unsigned short *>(ws + tBytes);
     unsigned short *PB = PA + pA;
     int4 *SA = reinterpret_cast<int4 *>(PB + pB);
     int4 *SB = SA + sA;
-    unsigned char *cntA = reinterpret_cast<unsigned char *>(SB + sB);
+    int *GA = reinterpret_cast<int *>(SB + sB);
+    int *GB = GA + LpA;
+    unsigned char *cntA = reinterpret_cast<unsigned char *>(GB + LpB);
     unsigned int *work = reinterpret_cast<unsigned int *>(cntA + cntBytes);
 
+    // the deferral counter starts at 0, the line grains at kGrainNone
     err = cudaMemsetAsync(work, 0, sizeof(unsigned int), stream);
+    if (err == cudaSuccess)
+        err = cudaMemsetAsync(GA, kGrainNone & 0xff, 4 * (size_t)(LpA + LpB), stream);
     const bool a_rc = (p.pass != CARBON_PASS_DW), b_rc = (p.pass == CARBON_PASS_DX);
     if (err == cudaSuccess && nchunks > 0)
-        err = a_rc ? launch_prep<true, kRowTile>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, 0, PA, SA, cntA, (int)nchunks, stream)
-                   : launch_prep<false, kRowTile>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, 0, PA, SA, cntA, (int)nchunks, stream);
+        err = a_rc ? launch_prep<true, kRowTile>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, 0, PA, SA, GA, cntA, (int)nchunks, stream)
+                   : launch_prep<false, kRowTile>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, 0, PA, SA, GA, cntA, (int)nchunks, stream);
     if (err == cudaSuccess && nchunks > 0)
-        err = b_rc ? launch_prep<true, kColTile>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, 1, PB, SB, nullptr, (int)nchunks, stream)
-                   : launch_prep<false, kColTile>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, 1, PB, SB, nullptr, (int)nchunks, stream);
-    // planes as 2-D [4 Lp][Rp] bf16 maps, 64-deep boxes, 128-byte swizzle
+        err = b_rc ? launch_prep<true, kColTile>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, 1, PB, SB, GB, nullptr, (int)nchunks, stream)
+                   : launch_prep<false, kColTile>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, 1, PB, SB, GB, nullptr, (int)nchunks, stream);
+    // planes as 2-D [4 Lp][Rp] bf16 maps, 64-deep boxes, 128-byte swizzle:
+    // one A plane of a row tile (128 rows), all four B planes of a column tile
+    // (256 rows) per box
     CUtensorMap ma, mb;
     std::memset(&ma, 0, sizeof ma);
     std::memset(&mb, 0, sizeof mb);
@@ -693,8 +877,8 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
                                    CU_TENSOR_MAP_SWIZZLE_128B);
         if (err == cudaSuccess)
             err = encode_tensor_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, PB, (uint64_t)Rp,
-                                       (uint64_t)(kPlanes * LpB), (uint64_t)Rp * 2, kKBlock, kColTile,
-                                       CU_TENSOR_MAP_SWIZZLE_128B);
+                                       (uint64_t)(kPlanes * LpB), (uint64_t)Rp * 2, kKBlock,
+                                       kPlanes * kColTile, CU_TENSOR_MAP_SWIZZLE_128B);
     }
     if (err == cudaSuccess) {
         TcxArgs a;
@@ -702,8 +886,10 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         a.out = p.out;
         a.rows = p.rows; a.cols = p.cols; a.LpA = LpA; a.LpB = LpB;
         a.tiles_m = (int)tiles_m; a.tiles_n = (int)tiles_n; a.nchunks = (int)nchunks;
-        a.SA = SA; a.SB = SB; a.cntA = cntA;
+        a.SA = SA; a.SB = SB; a.GA = GA; a.GB = GB; a.cntA = cntA;
         a.work_count = work; a.work_list = work + 1;
+        a.Tout = Tout;
+        a.vec_t = (p.cols % 2) == 0 ? 1 : 0;
         const int64_t tiles = tiles_m * tiles_n;
         const int grid = (int)(tiles < sms ? tiles : sms);
         err = out_f64 ? launch_tc_main<true>(ma, mb, a, grid, ia, SA, SB, LpA, LpB, work, stream)
