@@ -100,17 +100,18 @@ __device__ __forceinline__ double round_i128_to_double(__int128 I, int b) {
 // Bits needed for an unsigned value (0 for 0): v < 2^bits.
 __device__ __forceinline__ int bit_count(unsigned long long v) { return 64 - __clzll((long long)v); }
 
-// ---- fix-up pass: outputs with a chunk the main kernel could not prove ---------
+// ---- fix-up pass: outputs the fast kernels left undone ----------------------
 //
-// One warp per deferred output recomputes it from the bf16 operands, chunk by
-// chunk in order.  The 32 lanes load a chunk's 256 operand pairs at once and
-// reduce the exact chunk sum in 128-bit integers; the chunk value is that sum
-// rounded once to float64 (see the argument in the loop).  Chunks with inf or
-// NaN operands, or of extreme width, run the float64 KBN loop on lane 0 from
-// shared memory.  Lane 0 combines the chunk values with the full KBN step,
-// adds the bias and rounds.  Literal-algorithm bits throughout.
+// One block per listed output recomputes it from the bf16 operands.  Its eight
+// warps take eight chunks at a time: the 32 lanes of a warp load the chunk's
+// 256 operand pairs at once and reduce the exact chunk sum in 128-bit
+// integers; the chunk value is that sum rounded once to float64 (see the
+// argument in the loop).  Chunks with inf or NaN operands, or of extreme
+// width, run the float64 KBN loop on the warp's lane 0 from shared memory.
+// Thread 0 then combines the chunk values in order with the full KBN step, and
+// finally adds the bias and rounds.  Literal-algorithm bits throughout.
 constexpr int kFixWarps = 8;
-constexpr int kFixBlocks = 608;                      // 4 per SM of a GB300
+constexpr int kFixBlocks = 1024;
 
 template <bool OUT_F64>
 __global__ void __launch_bounds__(kFixWarps * 32)
@@ -118,78 +119,82 @@ exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__res
                    int64_t LpA, int64_t LpB, const unsigned int *__restrict__ work_count,
                    const unsigned int *__restrict__ work_list) {
     __shared__ double xs[kFixWarps][kChunk], ws[kFixWarps][kChunk];
+    __shared__ double Pq[kFixWarps];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // the main kernel appended the deferred outputs in no particular order;
-    // each warp takes every nwarps-th entry, one output at a time
-    const int64_t gw = blockIdx.x * (int64_t)kFixWarps + warp;
-    const int64_t nwarps = (int64_t)gridDim.x * kFixWarps;
     const int64_t count = *work_count;
-    for (int64_t item = gw; item < count; item += nwarps) {
+    const int64_t nq = (p.R + kChunk - 1) / kChunk;
+    for (int64_t item = blockIdx.x; item < count; item += gridDim.x) {
         const int64_t o = work_list[item];
         const int64_t i = o / p.cols, j = o % p.cols;
-        double S = 0.0, C = 0.0;
-        for (int64_t q0 = 0, q = 0; q0 < p.R; q0 += kChunk, ++q) {
-            const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
-            const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
-            uint32_t hx[kChunk / 32], hw[kChunk / 32];
-#pragma unroll
-            for (int t = 0; t < kChunk / 32; ++t) {
-                const int64_t r = q0 + lane + 32 * t;
-                hx[t] = r < qend ? ld_bits(p.A, i * p.a_si + r * p.a_sr) : 0u;
-                hw[t] = r < qend ? ld_bits(p.B, r * p.b_sr + j * p.b_sj) : 0u;
-            }
-            // KBN over a chunk captures every rounding error exactly and,
-            // while wx + ww < 90, also sums them exactly (each error is a
-            // multiple of 2^(bx + bw) below 2^(wx + ww - 45) of it), so the
-            // chunk value fl(s + c) is the exact chunk sum rounded once to
-            // float64; the exact sum is an integer dot product in 128 bits
-            const bool exact = sa.y <= 62 && sb.y <= 62 && sa.y + sb.y < 90;   // no inf/NaN either
-            __int128 I = 0;
-            if (exact) {
+        double S = 0.0, C = 0.0;                        // thread 0's outer KBN state
+        for (int64_t qb = 0; qb < nq; qb += kFixWarps) {
+            const int64_t q = qb + warp;
+            if (q < nq) {
+                const int64_t q0 = q * kChunk;
+                const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
+                const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
+                uint32_t hx[kChunk / 32], hw[kChunk / 32];
 #pragma unroll
                 for (int t = 0; t < kChunk / 32; ++t) {
-                    int mx, ex, mw, ew;
-                    bool bx_, bw_;
-                    decode(hx[t], mx, ex, bx_);
-                    decode(hw[t], mw, ew, bw_);
-                    if (mx == 0 || mw == 0) continue;
-                    const long long X = (long long)mx * (1ll << (ex - sa.x));   // |X| < 2^62
-                    const long long W = (long long)mw * (1ll << (ew - sb.x));
-                    I += (__int128)X * W;                                     // |X W| < 2^90
+                    const int64_t r = q0 + lane + 32 * t;
+                    hx[t] = r < qend ? ld_bits(p.A, i * p.a_si + r * p.a_sr) : 0u;
+                    hw[t] = r < qend ? ld_bits(p.B, r * p.b_sr + j * p.b_sj) : 0u;
                 }
+                // KBN over a chunk captures every rounding error exactly and,
+                // while wx + ww < 90, also sums them exactly (each error is a
+                // multiple of 2^(bx + bw) below 2^(wx + ww - 45) of it), so the
+                // chunk value fl(s + c) is the exact chunk sum rounded once to
+                // float64; the exact sum is an integer dot product in 128 bits
+                const bool exact = sa.y <= 62 && sb.y <= 62 && sa.y + sb.y < 90;   // no inf/NaN either
+                double P;
+                if (exact) {
+                    __int128 I = 0;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const long long lo = __shfl_xor_sync(0xffffffffu, (long long)(unsigned long long)I, off);
-                    const long long hi = __shfl_xor_sync(0xffffffffu, (long long)(I >> 64), off);
-                    I += ((__int128)hi << 64) | (__int128)(unsigned long long)lo;
-                }
-            }
-            double P;
-            if (exact) {
-                P = round_i128_to_double(I, sa.x + sb.x);
-            } else {                                   // inf/NaN or extreme widths: literal loop
-#pragma unroll
-                for (int t = 0; t < kChunk / 32; ++t) {
-                    xs[warp][lane + 32 * t] = widen_bf16(hx[t]);
-                    ws[warp][lane + 32 * t] = widen_bf16(hw[t]);
-                }
-                __syncwarp();
-                double s_ = 0.0, c_ = 0.0;
-                if (lane == 0) {
-                    const int len = (int)(qend - q0);
-                    for (int k = 0; k < len; ++k) {
-                        const double x = xs[warp][k], w = ws[warp][k];
-                        kbn_product_step(s_, c_, x, w,
-                                         ((uint32_t)__double2hiint(x) & 0x7ff00000u) +
-                                         ((uint32_t)__double2hiint(w) & 0x7ff00000u));
+                    for (int t = 0; t < kChunk / 32; ++t) {
+                        int mx, ex, mw, ew;
+                        bool bx_, bw_;
+                        decode(hx[t], mx, ex, bx_);
+                        decode(hw[t], mw, ew, bw_);
+                        if (mx == 0 || mw == 0) continue;
+                        const long long X = (long long)mx * (1ll << (ex - sa.x));   // |X| < 2^62
+                        const long long W = (long long)mw * (1ll << (ew - sb.x));
+                        I += (__int128)X * W;                                     // |X W| < 2^90
                     }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const long long lo = __shfl_xor_sync(0xffffffffu, (long long)(unsigned long long)I, off);
+                        const long long hi = __shfl_xor_sync(0xffffffffu, (long long)(I >> 64), off);
+                        I += ((__int128)hi << 64) | (__int128)(unsigned long long)lo;
+                    }
+                    P = round_i128_to_double(I, sa.x + sb.x);
+                } else {                                   // inf/NaN or extreme widths: literal loop
+#pragma unroll
+                    for (int t = 0; t < kChunk / 32; ++t) {
+                        xs[warp][lane + 32 * t] = widen_bf16(hx[t]);
+                        ws[warp][lane + 32 * t] = widen_bf16(hw[t]);
+                    }
+                    __syncwarp();
+                    double s_ = 0.0, c_ = 0.0;
+                    if (lane == 0) {
+                        const int len = (int)(qend - q0);
+                        for (int k = 0; k < len; ++k) {
+                            const double x = xs[warp][k], w = ws[warp][k];
+                            kbn_product_step(s_, c_, x, w,
+                                             ((uint32_t)__double2hiint(x) & 0x7ff00000u) +
+                                             ((uint32_t)__double2hiint(w) & 0x7ff00000u));
+                        }
+                    }
+                    __syncwarp();
+                    P = __dadd_rn(s_, c_);
                 }
-                __syncwarp();
-                P = __dadd_rn(s_, c_);
+                if (lane == 0) Pq[warp] = P;
             }
-            if (lane == 0) kbn_value_step(S, C, P);
+            __syncthreads();
+            if (threadIdx.x == 0)
+                for (int w = 0; w < kFixWarps && qb + w < nq; ++w) kbn_value_step(S, C, Pq[w]);
+            __syncthreads();
         }
-        if (lane == 0) {
+        if (threadIdx.x == 0) {
             double y = __dadd_rn(S, C);
             if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
             if (OUT_F64) static_cast<double *>(p.out)[o] = y;

@@ -50,9 +50,9 @@
 // from the operands.
 //
 // Structure.
-//  digit_prep_kernel: one block per (group of lines, chunk): statistics and
-//    digit planes [plane][line][R padded to 256] (bf16, reduction index
-//    contiguous), the A side's plane count per (row tile, chunk).
+//  digit_prep_kernel: one warp per (line, chunk): statistics and digit planes
+//    (bf16, reduction index contiguous, the four planes of a tile's lines
+//    together), the A side's plane count per (row tile, chunk).
 //  exact_tc_kernel: persistent, one CTA per SM, 128 x 64 output tiles.
 //   warps 0, 2 TMA producers of A: a 5-stage ring of A plane blocks (16 KiB
 //              each), alternate loads (one thread's copies complete in turn)
@@ -75,6 +75,7 @@
 #include "exact_bf16.cuh"
 #include "tcgen05.cuh"
 
+#include <algorithm>
 #include <cstring>
 
 namespace carbon {
@@ -121,11 +122,15 @@ struct TcxArgs {
     void *out;
     int64_t rows, cols, LpA, LpB;
     int tiles_m, tiles_n, nchunks;
+    int splits, cps;                                  // chunk range split into pieces of cps chunks
     const int4 *SA, *SB;                              // statistics [chunk][Lp]
     const int *GA, *GB;                               // line grains (smallest base) [Lp]
-    const unsigned char *cntA;                        // A planes per (row tile, chunk)
+    const int *cntA;                                  // A planes per (row tile, chunk)
     unsigned int *work_count, *work_list;             // deferred outputs
-    long long *Tout;                                  // exact sums in the output grain [rows][cols]
+    long long *Tout;                                  // exact sums in the output grain [piece][rows][cols]
+    unsigned int *chunk_count;                        // (output, chunk) pairs for the chunk repair
+    uint2 *chunk_list;
+    unsigned int chunk_cap;
     int vec_t;                                        // Tout rows start 16-byte aligned
 };
 
@@ -169,49 +174,59 @@ __device__ __forceinline__ int digits_for_width(int w) {
 }
 
 constexpr int kPrepThreads = 256;
+constexpr int kPrepLines = 32;                        // lines per block (4 per warp)
 constexpr int kRawPitch = kChunk + 8;                 // bf16 per staged line (16-byte rows)
 
-// One block: G lines (G = 128 for A, 64 for B) x one chunk.  The source
-// element (line, r) is src[line * ls + r * rs]; RCONTIG says rs == 1.
-// Writes stats[chunk * Lp + line], digit planes tile by tile: plane a of line
-// line0 + l at row 4 line0 + a G + l of the [4 Lp][Rp] array, for a < np (np = 4 if all_planes, else the most any line of the block
-// needs), cnt[group * nchunks + chunk] = np when cnt is not null, and lowers
-// grain[line] (preset to kGrainNone) to the line's smallest base over the
-// chunks where it is nonzero and representable.
-template <bool RCONTIG, int G>
+// One block: 32 lines x one chunk; one warp per line at a time, lane t taking
+// the reduction indices 8t .. 8t+7.  The source element (line, r) is
+// src[line * ls + r * rs]; RCONTIG says rs == 1 (lines are read directly),
+// otherwise the block's lines are staged in shared memory first (coalesced
+// along the lines).  Writes stats[chunk * Lp + line]; the line's digits in its
+// own count n of planes (the top one the remainder) and zeros in the planes
+// above, tile by tile: plane a of line L at row (L / tg) 4 tg + a tg + L % tg
+// of the [4 Lp][Rp] array (tg = tile lines); raises cnt[(L / tg) * nchunks +
+// chunk] to n when cnt is not null; and lowers grain[L] (preset to
+// kGrainNone) to the line's smallest base over the chunks where it is nonzero
+// and finite with width <= 62 (the chunk repair adds the wider chunks in it).
+template <bool RCONTIG>
 __global__ void __launch_bounds__(kPrepThreads)
 digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs, int64_t nlines,
-                  int64_t R, int64_t Lp, int64_t Rp, int all_planes,
-                  unsigned short *__restrict__ planes, int4 *__restrict__ stats,
-                  int *__restrict__ grain, unsigned char *__restrict__ cnt, int nchunks) {
-    extern __shared__ __align__(16) unsigned short raw[];   // [G][kRawPitch]
-    __shared__ int lbase[G], lwidth[G];
-    __shared__ int nmax;
+                  int64_t R, int64_t Lp, int64_t Rp, int tg, unsigned short *__restrict__ planes,
+                  int4 *__restrict__ stats, int *__restrict__ grain, int *__restrict__ cnt,
+                  int nchunks) {
+    __shared__ __align__(16) unsigned short raw[RCONTIG ? 1 : kPrepLines * kRawPitch];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int64_t line0 = (int64_t)blockIdx.x * G;
+    const int64_t line0 = (int64_t)blockIdx.x * kPrepLines;
     const int q = blockIdx.y;
     const int64_t q0 = (int64_t)q * kChunk;
-    if (tid == 0) nmax = 0;
-
-    // stage the block's operands, coalesced along whichever index is contiguous
-    for (int e = tid; e < G * kChunk; e += kPrepThreads) {
-        const int l = RCONTIG ? e / kChunk : e % G;
-        const int r = RCONTIG ? e % kChunk : e / G;
-        const int64_t line = line0 + l, rr = q0 + r;
-        raw[l * kRawPitch + r] = (line < nlines && rr < R) ? src[line * ls + rr * rs] : (unsigned short)0;
+    if (!RCONTIG) {
+        for (int e = tid; e < kPrepLines * kChunk; e += kPrepThreads) {
+            const int l = e % kPrepLines, r = e / kPrepLines;
+            const int64_t line = line0 + l, rr = q0 + r;
+            raw[l * kRawPitch + r] = (line < nlines && rr < R) ? src[line * ls + rr * rs] : (unsigned short)0;
+        }
+        __syncthreads();
     }
-    __syncthreads();
-
-    // per-line statistics: warp w takes lines w, w + 8, ...
-    int wmax = 0;
-    for (int l = warp; l < G; l += kPrepThreads / 32) {
-        int lo = 1 << 20, hi = -(1 << 20), bad = 0;
-        int m[kChunk / 32], ex[kChunk / 32];
+    for (int l = warp; l < kPrepLines; l += kPrepThreads / 32) {
+        const int64_t L = line0 + l;
+        uint32_t h[8];
+        if (RCONTIG) {
 #pragma unroll
-        for (int t = 0; t < kChunk / 32; ++t) {
+            for (int e = 0; e < 8; ++e) {
+                const int64_t rr = q0 + 8 * lane + e;
+                h[e] = (L < nlines && rr < R) ? (uint32_t)__ldg(src + L * ls + rr) : 0u;
+            }
+        } else {
+            const uint4 v = *reinterpret_cast<const uint4 *>(&raw[l * kRawPitch + 8 * lane]);
+            h[0] = v.x & 0xffffu; h[1] = v.x >> 16; h[2] = v.y & 0xffffu; h[3] = v.y >> 16;
+            h[4] = v.z & 0xffffu; h[5] = v.z >> 16; h[6] = v.w & 0xffffu; h[7] = v.w >> 16;
+        }
+        int m[8], ex[8], lo = 1 << 20, hi = -(1 << 20), bad = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
             bool b;
-            decode(raw[l * kRawPitch + lane + 32 * t], m[t], ex[t], b);
-            if (m[t] != 0) { lo = min(lo, ex[t]); hi = max(hi, ex[t]); }
+            decode(h[e], m[e], ex[e], b);
+            if (m[e] != 0) { lo = min(lo, ex[e]); hi = max(hi, ex[e]); }
             bad |= (int)b;
         }
         lo = __reduce_min_sync(0xffffffffu, lo);
@@ -219,42 +234,28 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
         bad = (int)__reduce_or_sync(0xffffffffu, (unsigned)bad);
         const int base = (lo > hi) ? 0 : lo;
         const int width = bad ? kWidthBad : ((lo > hi) ? 0 : hi + 8 - lo);
+        const bool use = width > 0 && width <= 31;
+        const int n = digits_for_width(width);
+        int X[8];
         unsigned long long sum = 0ull;
         unsigned int mx = 0u;
-        if (width > 0 && width <= 31) {
 #pragma unroll
-            for (int t = 0; t < kChunk / 32; ++t) {
-                if (m[t] != 0) {
-                    const unsigned int a = (unsigned int)abs(m[t]) << (ex[t] - base);   // < 2^31
-                    sum += a;
-                    mx = max(mx, a);
-                }
-            }
+        for (int e = 0; e < 8; ++e) {
+            X[e] = (use && m[e] != 0) ? m[e] * (1 << (ex[e] - base)) : 0;     // |X| < 2^31
+            const unsigned int a = (unsigned int)abs(X[e]);
+            sum += a;
+            mx = max(mx, a);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
         mx = __reduce_max_sync(0xffffffffu, mx);
         if (lane == 0) {
-            lbase[l] = base;
-            lwidth[l] = width;
-            stats[(int64_t)q * Lp + line0 + l] = make_int4(base, width, bit_count(sum), bit_count(mx));
-            if (width > 0 && width <= 31) atomicMin(&grain[line0 + l], base);
+            stats[(int64_t)q * Lp + L] = make_int4(base, width, bit_count(sum), bit_count(mx));
+            // the grain also covers finite lines too wide for the digits,
+            // whose chunks the chunk repair adds in the same grain
+            if (width > 0 && width <= 62) atomicMin(&grain[L], base);
+            if (use && cnt != nullptr) atomicMax(&cnt[(L / tg) * nchunks + q], n);
         }
-        wmax = max(wmax, digits_for_width(width));
-    }
-    if (lane == 0) atomicMax(&nmax, wmax);
-    __syncthreads();
-    const int np = all_planes ? kPlanes : nmax;
-    if (cnt != nullptr && tid == 0) cnt[(int64_t)blockIdx.x * nchunks + q] = (unsigned char)np;
-
-    // digit planes: item (line, 8 consecutive r) -> np 16-byte stores
-    for (int item = tid; item < G * (kChunk / 8); item += kPrepThreads) {
-        const int l = item / (kChunk / 8), g = item % (kChunk / 8);
-        const uint4 h = *reinterpret_cast<const uint4 *>(&raw[l * kRawPitch + 8 * g]);
-        const uint32_t hv[8] = {h.x & 0xffffu, h.x >> 16, h.y & 0xffffu, h.y >> 16,
-                                h.z & 0xffffu, h.z >> 16, h.w & 0xffffu, h.w >> 16};
-        const int base = lbase[l], width = lwidth[l];
-        const bool use = width > 0 && width <= 31;
         uint32_t packed[kPlanes][4];
 #pragma unroll
         for (int a = 0; a < kPlanes; ++a)
@@ -262,21 +263,16 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
             for (int w = 0; w < 4; ++w) packed[a][w] = 0u;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            int mm, ee;
-            bool b;
-            decode(hv[e], mm, ee, b);
-            const int X = (use && mm != 0) ? mm * (1 << (ee - base)) : 0;   // |X| < 2^31
             int d[kPlanes];
-            split_digits(X, np, d);
+            split_digits(X[e], n, d);
 #pragma unroll
-            for (int a = 0; a < kPlanes; ++a)
-                packed[a][e / 2] |= small_int_bf16(d[a]) << (16 * (e & 1));
+            for (int a = 0; a < kPlanes; ++a) packed[a][e / 2] |= small_int_bf16(d[a]) << (16 * (e & 1));
         }
+        const int64_t row = (L / tg) * kPlanes * tg + L % tg;
 #pragma unroll
         for (int a = 0; a < kPlanes; ++a)
-            if (a < np)
-                *reinterpret_cast<uint4 *>(planes + (kPlanes * line0 + a * G + l) * Rp + q0 + 8 * g) =
-                    make_uint4(packed[a][0], packed[a][1], packed[a][2], packed[a][3]);
+            *reinterpret_cast<uint4 *>(planes + (row + (int64_t)a * tg) * Rp + q0 + 8 * lane) =
+                make_uint4(packed[a][0], packed[a][1], packed[a][2], packed[a][3]);
     }
 }
 
@@ -391,7 +387,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_slot;
-    const int ntiles = p.tiles_m * p.tiles_n;
+    const int nunits = p.tiles_m * p.tiles_n * p.splits;   // (tile, chunk piece) work units
     const int nchunks = p.nchunks;
 
     if (warp < 4) {
@@ -406,9 +402,11 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             const uint32_t mine = warp == 0 ? 0u : 1u;
             uint32_t g = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles && !*abort_flag; t += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
+                const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
+                const int qhi = min(nchunks, qlo + p.cps);
                 const int tm = t % p.tiles_m;
-                for (int q = 0; ok && q < nchunks; ++q) {
+                for (int q = qlo; ok && q < qhi; ++q) {
                     const int nx = p.cntA[(int64_t)tm * nchunks + q];
                     for (int k = 0; ok && k < nx; ++k)
                         for (int kb = 0; kb < kKBlocks; ++kb, ++g) {
@@ -435,9 +433,11 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         if (lane == 0) {
             uint32_t bu = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles && !*abort_flag; t += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
+                const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
+                const int qhi = min(nchunks, qlo + p.cps);
                 const int tm = t % p.tiles_m, tn = t / p.tiles_m;
-                for (int q = 0; ok && q < nchunks; ++q) {
+                for (int q = qlo; ok && q < qhi; ++q) {
                     if (p.cntA[(int64_t)tm * nchunks + q] == 0) continue;
                     for (int kb = 0; kb < kKBlocks; ++kb) {
                         if (!(ok = wait_or_abort(smem_addr(&sm.bempty[kb]), (bu & 1u) ^ 1u, abort_flag))) break;
@@ -461,9 +461,11 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             int s = 0, acc = 0;
             uint32_t ph = 0, bu = 0, aph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < ntiles && !*abort_flag; t += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
+                const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
+                const int qhi = min(nchunks, qlo + p.cps);
                 const int tm = t % p.tiles_m;
-                for (int q = 0; ok && q < nchunks; ++q) {
+                for (int q = qlo; ok && q < qhi; ++q) {
                     const int nx = p.cntA[(int64_t)tm * nchunks + q];
                     if (nx == 0) continue;
                     for (int k = 0; ok && k < nx; ++k) {
@@ -519,18 +521,20 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         int acc = 0;
         uint32_t aph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < ntiles && !*abort_flag; t += gridDim.x) {
+        for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
+            const int t = u / p.splits, piece = u % p.splits, qlo = piece * p.cps;
+            const int qhi = min(nchunks, qlo + p.cps);
             const int tm = t % p.tiles_m, tn = t / p.tiles_m;
             const int64_t i = (int64_t)tm * kRowTile + rl;
             const int64_t jw = (int64_t)tn * kColTile + half * 32;   // this warp's first column
-            const unsigned char *cnt = p.cntA + (int64_t)tm * nchunks;
+            const int *cnt = p.cntA + (int64_t)tm * nchunks;
             const int Gx = __ldg(&p.GA[i]);                   // output grain: 2^(Gx + Gw)
             const int Gwl = __ldg(&p.GB[jw + lane]);
             __syncwarp();                                    // last tile's reads are done
             __syncwarp();
             // I starts at minus the accumulators' starting values summed over
             // the chunk's pairs, so that after the k-groups it is the chunk sum
-            int nx = nchunks > 0 ? cnt[0] : 0;
+            int nx = qlo < qhi ? cnt[qlo] : 0;
             unsigned long long I[32], T[32];
             {
                 const unsigned long long c0 = 0ull - magic_sum(nx);
@@ -539,12 +543,12 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             }
             uint32_t defer = 0u;
             int4 rs = make_int4(0, 0, 0, 0), cl = rs;        // this chunk's statistics, loaded ahead
-            if (nchunks > 0) {
-                rs = __ldg(&p.SA[i]);
-                cl = __ldg(&p.SB[jw + lane]);
+            if (qlo < qhi) {
+                rs = __ldg(&p.SA[(int64_t)qlo * p.LpA + i]);
+                cl = __ldg(&p.SB[(int64_t)qlo * p.LpB + jw + lane]);
             }
 
-            for (int q = 0; ok && q < nchunks; ++q) {
+            for (int q = qlo; ok && q < qhi; ++q) {
                 for (int k = 0; k < nx; ++k) {
                     if (!(ok = wait_or_abort(smem_addr(&sm.tfull[acc]), aph, abort_flag))) break;
                     tc_fence_after();
@@ -601,7 +605,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 sm.pk[ew][lane] = (uint32_t)shc | ((uint32_t)min(cl.y, 127) << 8) |
                                   ((uint32_t)cl.z << 15) | ((uint32_t)cl.w << 21);
                 __syncwarp();
-                if (q + 1 < nchunks) {                       // next chunk's statistics
+                if (q + 1 < qhi) {                           // next chunk's statistics
                     rs = __ldg(&p.SA[(int64_t)(q + 1) * p.LpA + i]);
                     cl = __ldg(&p.SB[(int64_t)(q + 1) * p.LpB + jw + lane]);
                 }
@@ -648,20 +652,31 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         // a zero line (wx or ww 0) adds +0, which changes nothing
                         const bool live = fits && !(defer & bit) && wx != 0 && ww != 0;
                         T[jj] = (live && ok_add) ? (unsigned long long)Tn : T[jj];
-                        defer |= (fits && (live ? ok_add : true)) ? 0u : bit;
+                        bool bad = !(fits && (live ? ok_add : true));
+                        // a finite line too wide for the digits: only this chunk is
+                        // recomputed (and added to T) by the chunk repair kernel
+                        if (!fits && !(defer & bit) && wx > 0 && ww > 0 && wx <= 62 && ww <= 62 &&
+                            wx + ww < 90 && i < p.rows && jw + jj < p.cols) {
+                            const unsigned int e = atomicAdd(p.chunk_count, 1u);
+                            if (e < p.chunk_cap) {
+                                p.chunk_list[e] = make_uint2((unsigned int)(i * p.cols + jw + jj), (unsigned int)q);
+                                bad = false;
+                            }
+                        }
+                        defer |= bad ? bit : 0u;
                     }
                 }
-                nx = (q + 1 < nchunks) ? cnt[q + 1] : 0;
+                nx = (q + 1 < qhi) ? cnt[q + 1] : 0;
                 const unsigned long long c0 = 0ull - magic_sum(nx);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) I[c] = c0;
             }
             if (!ok) break;
 
-            // ---- the exact sums go to the finalize kernel (deferred outputs: a
-            // sentinel no sum reaches, |T| < 2^62)
+            // ---- this piece's exact partial sums go to the finalize kernel
+            // (deferred outputs: a sentinel no sum reaches, |T| < 2^62)
             if (i < p.rows) {
-                long long *trow = p.Tout + i * p.cols + jw;
+                long long *trow = p.Tout + (int64_t)piece * p.rows * p.cols + i * p.cols + jw;
                 if (p.vec_t && jw + 32 <= p.cols) {
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
@@ -692,6 +707,86 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     }
 }
 
+// ---- chunk repair: single chunks with a line too wide for the digits ----------
+//
+// One warp per listed (output, chunk): the lanes load the chunk's 256 operand
+// pairs, reduce the exact chunk sum I in 128-bit integers, and lane 0 rounds
+// it once to 53 significant bits (the chunk value, as the KBN argument shows)
+// and adds it, shifted to the output grain, into the output's piece sum with
+// an integer atomic (exact, so the order of the additions does not matter).
+// A value that does not fit, or an addition that overflows, lists the output
+// for the full fix-up instead.
+__device__ __forceinline__ __int128 round_i128_to_53_bits(__int128 I) {
+    const bool neg = I < 0;
+    const unsigned __int128 mag = neg ? (unsigned __int128)0 - (unsigned __int128)I : (unsigned __int128)I;
+    const unsigned long long hi = (unsigned long long)(mag >> 64), lo = (unsigned long long)mag;
+    const int nb = hi ? 128 - __clzll((long long)hi) : 64 - __clzll((long long)lo);
+    if (nb <= 53) return I;
+    const int sh = nb - 53;
+    const unsigned __int128 rem = mag & (((unsigned __int128)1 << sh) - 1), half = (unsigned __int128)1 << (sh - 1);
+    unsigned __int128 m = mag >> sh;
+    m += (rem > half || (rem == half && (m & 1))) ? 1 : 0;
+    const __int128 r = (__int128)(m << sh);
+    return neg ? -r : r;
+}
+
+__global__ void __launch_bounds__(256)
+exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
+                          int64_t LpA, int64_t LpB, const int *__restrict__ GA,
+                          const int *__restrict__ GB, const unsigned int *__restrict__ chunk_count,
+                          const uint2 *__restrict__ chunk_list, unsigned int chunk_cap,
+                          long long *Tout, int cps, unsigned int *work_count, unsigned int *work_list) {
+    const int lane = threadIdx.x % 32;
+    const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32;
+    const int64_t nw = (int64_t)gridDim.x * blockDim.x / 32;
+    const int64_t count = min(*chunk_count, chunk_cap);
+    for (int64_t e = gw; e < count; e += nw) {
+        const uint2 en = chunk_list[e];
+        const int64_t o = en.x, q = en.y;
+        const int64_t i = o / p.cols, j = o % p.cols;
+        const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
+        const int64_t q0 = q * kChunk, qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
+        __int128 I = 0;
+#pragma unroll
+        for (int t = 0; t < kChunk / 32; ++t) {
+            const int64_t r = q0 + lane + 32 * t;
+            if (r >= qend) continue;
+            int mx, ex, mw, ew;
+            bool bx_, bw_;
+            decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bx_);
+            decode(ld_bits(p.B, r * p.b_sr + j * p.b_sj), mw, ew, bw_);
+            if (mx == 0 || mw == 0) continue;
+            const long long X = (long long)mx * (1ll << (ex - sa.x));           // |X| < 2^62
+            const long long W = (long long)mw * (1ll << (ew - sb.x));
+            I += (__int128)X * W;                                             // |X W| < 2^90
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const long long lo = __shfl_xor_sync(0xffffffffu, (long long)(unsigned long long)I, off);
+            const long long hi = __shfl_xor_sync(0xffffffffu, (long long)(I >> 64), off);
+            I += ((__int128)hi << 64) | (__int128)(unsigned long long)lo;
+        }
+        if (lane != 0) continue;
+        const __int128 J = round_i128_to_53_bits(I);
+        const int sh = (sa.x - __ldg(&GA[i])) + (sb.x - __ldg(&GB[j]));
+        bool ok = sh >= 0 && sh < 62;
+        __int128 v = 0;
+        if (ok) {
+            v = J << sh;
+            ok = (v >> sh) == J && v >= -((__int128)1 << 61) && v < ((__int128)1 << 61);
+        }
+        if (ok) {
+            long long *slot = Tout + (q / cps) * p.rows * p.cols + o;
+            const long long add = (long long)v;
+            const long long old = (long long)atomicAdd(reinterpret_cast<unsigned long long *>(slot),
+                                                       (unsigned long long)add);
+            const long long sum = (long long)((unsigned long long)old + (unsigned long long)add);
+            ok = !((old >= 0) == (add >= 0) && (sum >= 0) != (old >= 0));
+        }
+        if (!ok) work_list[atomicAdd(work_count, 1u)] = (unsigned int)o;
+    }
+}
+
 // ---- finalize: bias and the two roundings ------------------------------------
 //
 // KBN over the chunk values is exact in the same way as inside a chunk: the
@@ -699,13 +794,15 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 // That rounding is done on the integer, the bias (m * 2^e) joins it exactly,
 // and the sum is rounded once more, to float64 and then to bf16 (both nearest
 // even), all on integers; values outside those fast ranges take the float64
-// route.  One thread per 8 consecutive outputs of a row.
+// route.  The chunk range of an output may have been split into pieces whose
+// partial sums T add exactly.  One thread per 8 consecutive outputs of a row.
 template <bool OUT_F64>
 __global__ void __launch_bounds__(256)
-exact_finalize_kernel(const long long *__restrict__ Tout, const int *__restrict__ GA,
+exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int *__restrict__ GA,
                       const int *__restrict__ GB, const unsigned short *__restrict__ bias, void *out,
                       int64_t rows, int64_t cols, int vec_out) {
     const int64_t gpr = (cols + 7) / 8;
+    const int64_t plane = rows * cols;
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < rows * gpr;
          g += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i = g / gpr, j0 = (g % gpr) * 8;
@@ -716,15 +813,25 @@ exact_finalize_kernel(const long long *__restrict__ Tout, const int *__restrict_
         for (int e = 0; e < 8; ++e) {
             const int64_t j = j0 + e;
             if (j >= cols) { skip |= 1u << e; continue; }
-            const long long T = __ldg(&Tout[i * cols + j]);
-            if (T == kDeferredSum) { skip |= 1u << e; continue; }
+            // the pieces' partial sums add exactly (128 bits)
+            __int128 acc = 0;
+            bool deferred = false;
+            for (int k = 0; k < pieces; ++k) {
+                const long long t = __ldg(&Tout[k * plane + i * cols + j]);
+                if (t == kDeferredSum) { deferred = true; break; }
+                acc += t;
+            }
+            if (deferred) { skip |= 1u << e; continue; }
             const int G = gx + __ldg(&GB[j]);
-            if (OUT_F64) {
-                double y = round_int_to_double(T, G);
+            const bool small = acc >= -((__int128)1 << 62) && acc < ((__int128)1 << 62);
+            if (OUT_F64 || !small) {
+                double y = small ? round_int_to_double((long long)acc, G) : round_i128_to_double(acc, G);
                 if (bias != nullptr) y = __dadd_rn(y, widen_bf16(ld_bits(bias, j)));
-                static_cast<double *>(out)[i * cols + j] = y;
+                if (OUT_F64) static_cast<double *>(out)[i * cols + j] = y;
+                else packed[e / 2] |= (uint32_t)exact_round_bf16(y) << (16 * (e & 1));
                 continue;
             }
+            const long long T = (long long)acc;
             int bm = 0, be = 0;
             bool bad = false;
             if (bias != nullptr) decode(ld_bits(bias, j), bm, be, bad);
@@ -770,12 +877,19 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
     count_launch();
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    exact_chunk_repair_kernel<<<kFixBlocks, 256, 0, s>>>(ia, SA, SB, LpA, LpB, a.GA, a.GB, a.chunk_count,
+                                                          a.chunk_list, a.chunk_cap, a.Tout, a.cps,
+                                                          work, work + 1);
+    count_launch();
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
     {
         const int64_t groups = a.rows * ((a.cols + 7) / 8);
         const int64_t want = (groups + 255) / 256;
         const int blocks = (int)(want < 8 * 152 ? (want > 0 ? want : 1) : 8 * 152);
         const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0 && (a.cols % 8) == 0) ? 1 : 0;
-        exact_finalize_kernel<F64><<<blocks, 256, 0, s>>>(a.Tout, a.GA, a.GB, a.bias, a.out, a.rows, a.cols, vec_out);
+        exact_finalize_kernel<F64><<<blocks, 256, 0, s>>>(a.Tout, a.splits, a.GA, a.GB, a.bias, a.out,
+                                                           a.rows, a.cols, vec_out);
         count_launch();
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
@@ -785,17 +899,28 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
     return cudaGetLastError();
 }
 
-template <bool RCONTIG, int G>
+// Pieces the chunk range of each output tile is cut into: only when the
+// output tiles are few (under two waves), the count (<= 8, <= chunks) that
+// minimises waves x chunks per piece, the smaller on ties.  The result does
+// not depend on it: the pieces' integer sums add exactly.
+int choose_pieces(int64_t tiles, int64_t nchunks, int sms) {
+    if (tiles >= 2 * (int64_t)sms || nchunks <= 1) return 1;
+    int best = 1;
+    int64_t best_cost = ((tiles + sms - 1) / sms) * nchunks;
+    for (int s = 2; s <= 8 && s <= nchunks; ++s) {
+        const int64_t cost = ((tiles * s + sms - 1) / sms) * ((nchunks + s - 1) / s);
+        if (cost < best_cost) { best = s; best_cost = cost; }
+    }
+    return best;
+}
+
+template <bool RCONTIG>
 cudaError_t launch_prep(const unsigned short *src, int64_t ls, int64_t rs, int64_t nlines, int64_t R,
-                        int64_t Lp, int64_t Rp, int all_planes, unsigned short *planes, int4 *stats,
-                        int *grain, unsigned char *cnt, int nchunks, cudaStream_t s) {
-    auto kern = digit_prep_kernel<RCONTIG, G>;
-    const int smem = G * kRawPitch * 2;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    const dim3 grid((unsigned)(Lp / G), (unsigned)nchunks);
-    kern<<<grid, kPrepThreads, smem, s>>>(src, ls, rs, nlines, R, Lp, Rp, all_planes, planes, stats,
-                                          grain, cnt, nchunks);
+                        int64_t Lp, int64_t Rp, int tg, unsigned short *planes, int4 *stats,
+                        int *grain, int *cnt, int nchunks, cudaStream_t s) {
+    const dim3 grid((unsigned)(Lp / kPrepLines), (unsigned)nchunks);
+    digit_prep_kernel<RCONTIG><<<grid, kPrepThreads, 0, s>>>(src, ls, rs, nlines, R, Lp, Rp, tg, planes,
+                                                             stats, grain, cnt, nchunks);
     count_launch();
     return cudaGetLastError();
 }
@@ -836,11 +961,16 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     // planes of A and B, statistics, A plane counts, the deferral counter and list
     const size_t pA = (size_t)kPlanes * LpA * Rp, pB = (size_t)kPlanes * LpB * Rp;
     const size_t sA = (size_t)nchunks * LpA, sB = (size_t)nchunks * LpB;
-    const size_t cntBytes = (((size_t)tiles_m * nchunks) + 15) & ~(size_t)15;
+    const size_t cntBytes = ((4 * (size_t)tiles_m * nchunks) + 15) & ~(size_t)15;
+    const int pieces = choose_pieces(tiles_m * tiles_n, nchunks, sms);
     const size_t outs = (size_t)p.rows * (size_t)p.cols;
-    const size_t tBytes = (8 * outs + 255) & ~(size_t)255;   // keeps the planes 256-byte aligned
+    const size_t tBytes = (8 * outs * pieces + 255) & ~(size_t)255;   // keeps the planes aligned
+    // chunk repair list (capacity capped; an output that does not get a slot is
+    // listed for the full fix-up instead); each piece and each repaired chunk
+    // may list an output for the fix-up
+    const size_t ccap = std::min<size_t>(outs * (size_t)nchunks, (size_t)1 << 22);
     const size_t bytes = tBytes + 2 * (pA + pB) + 16 * (sA + sB) + 4 * (size_t)(LpA + LpB) +
-                         cntBytes + 4 * (outs + 1);
+                         cntBytes + 8 * ccap + 16 + 4 * (outs * pieces + ccap + 1);
     char *ws = nullptr;
     cudaError_t err = cudaMallocAsync(reinterpret_cast<void **>(&ws), bytes, stream);
     if (err != cudaSuccess) return note_cuda(err);
@@ -851,20 +981,25 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     int4 *SB = SA + sA;
     int *GA = reinterpret_cast<int *>(SB + sB);
     int *GB = GA + LpA;
-    unsigned char *cntA = reinterpret_cast<unsigned char *>(GB + LpB);
-    unsigned int *work = reinterpret_cast<unsigned int *>(cntA + cntBytes);
+    int *cntA = GB + LpB;
+    uint2 *clist = reinterpret_cast<uint2 *>(reinterpret_cast<char *>(cntA) + cntBytes);
+    unsigned int *ccount = reinterpret_cast<unsigned int *>(clist + ccap);
+    unsigned int *work = ccount + 4;
 
-    // the deferral counter starts at 0, the line grains at kGrainNone
+    // the deferral counter and the plane counts start at 0, the line grains
+    // at kGrainNone
     err = cudaMemsetAsync(work, 0, sizeof(unsigned int), stream);
     if (err == cudaSuccess)
         err = cudaMemsetAsync(GA, kGrainNone & 0xff, 4 * (size_t)(LpA + LpB), stream);
+    if (err == cudaSuccess) err = cudaMemsetAsync(cntA, 0, cntBytes, stream);
+    if (err == cudaSuccess) err = cudaMemsetAsync(ccount, 0, sizeof(unsigned int), stream);
     const bool a_rc = (p.pass != CARBON_PASS_DW), b_rc = (p.pass == CARBON_PASS_DX);
     if (err == cudaSuccess && nchunks > 0)
-        err = a_rc ? launch_prep<true, kRowTile>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, 0, PA, SA, GA, cntA, (int)nchunks, stream)
-                   : launch_prep<false, kRowTile>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, 0, PA, SA, GA, cntA, (int)nchunks, stream);
+        err = a_rc ? launch_prep<true>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, stream)
+                   : launch_prep<false>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, stream);
     if (err == cudaSuccess && nchunks > 0)
-        err = b_rc ? launch_prep<true, kColTile>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, 1, PB, SB, GB, nullptr, (int)nchunks, stream)
-                   : launch_prep<false, kColTile>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, 1, PB, SB, GB, nullptr, (int)nchunks, stream);
+        err = b_rc ? launch_prep<true>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, nullptr, (int)nchunks, stream)
+                   : launch_prep<false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, nullptr, (int)nchunks, stream);
     // planes as 2-D [4 Lp][Rp] bf16 maps, 64-deep boxes, 128-byte swizzle:
     // one A plane of a row tile (128 rows), all four B planes of a column tile
     // (256 rows) per box
@@ -886,12 +1021,17 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         a.out = p.out;
         a.rows = p.rows; a.cols = p.cols; a.LpA = LpA; a.LpB = LpB;
         a.tiles_m = (int)tiles_m; a.tiles_n = (int)tiles_n; a.nchunks = (int)nchunks;
+        a.splits = pieces;
+        a.cps = (int)((nchunks + pieces - 1) / pieces);
         a.SA = SA; a.SB = SB; a.GA = GA; a.GB = GB; a.cntA = cntA;
         a.work_count = work; a.work_list = work + 1;
         a.Tout = Tout;
+        a.chunk_count = ccount;
+        a.chunk_list = clist;
+        a.chunk_cap = (unsigned int)ccap;
         a.vec_t = (p.cols % 2) == 0 ? 1 : 0;
-        const int64_t tiles = tiles_m * tiles_n;
-        const int grid = (int)(tiles < sms ? tiles : sms);
+        const int64_t units = tiles_m * tiles_n * pieces;
+        const int grid = (int)(units < sms ? units : sms);
         err = out_f64 ? launch_tc_main<true>(ma, mb, a, grid, ia, SA, SB, LpA, LpB, work, stream)
                       : launch_tc_main<false>(ma, mb, a, grid, ia, SA, SB, LpA, LpB, work, stream);
     }
