@@ -69,6 +69,12 @@ def _load() -> ctypes.CDLL:
     lib.carbon_abi_version.restype = ctypes.c_int
     lib.carbon_debug_launch_count.argtypes = []
     lib.carbon_debug_launch_count.restype = ctypes.c_int64
+    lib.carbon_debug_kernel_timing.argtypes = [ctypes.c_int]
+    lib.carbon_debug_kernel_timing.restype = None
+    lib.carbon_debug_kernel_time.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                             ctypes.POINTER(ctypes.c_int64),
+                                             ctypes.POINTER(ctypes.c_int64)]
+    lib.carbon_debug_kernel_time.restype = ctypes.c_int
     return lib
 
 
@@ -191,3 +197,16 @@ def carbon_abi_version() -> int:
 
 def carbon_debug_launch_count() -> int:
     return int(lib.carbon_debug_launch_count())
+
+
+def carbon_debug_kernel_timing(enable: bool) -> None:
+    """Start (and clear) or stop event timing of the exact tier's tensor-core kernel."""
+    lib.carbon_debug_kernel_timing(1 if enable else 0)
+
+
+def carbon_debug_kernel_time():
+    """(milliseconds, launches, k-groups) recorded since timing was enabled."""
+    ms, n, kg = ctypes.c_double(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib.carbon_debug_kernel_time(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(kg)),
+           "carbon_debug_kernel_time")
+    return ms.value, int(n.value), int(kg.value)

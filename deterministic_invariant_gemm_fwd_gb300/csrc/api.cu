@@ -184,4 +184,10 @@ int carbon_abi_version(void) { return CARBON_ABI_VERSION; }
 
 int64_t carbon_debug_launch_count(void) { return carbon::g_launches.load(); }
 
+void carbon_debug_kernel_timing(int enable) { carbon::exact_tc_timing(enable); }
+
+carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t *kgroups) {
+    return carbon::exact_tc_time(ms, launches, kgroups);
+}
+
 }  // extern "C"

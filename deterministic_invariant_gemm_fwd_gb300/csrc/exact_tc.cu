@@ -76,12 +76,21 @@
 #include "tcgen05.cuh"
 
 #include <algorithm>
+#include <mutex>
+#include <utility>
+#include <vector>
 #include <cstring>
 
 namespace carbon {
 namespace {
 
 __device__ unsigned int g_exact_tc_status = 0;
+__device__ unsigned long long g_exact_tc_kgroups = 0;   // k-groups issued (measurement)
+
+// Optional CUDA-event timing of the main kernel (carbon_debug_kernel_timing).
+std::mutex g_timing_mu;
+bool g_timing_on = false;
+std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_timing_events;
 
 constexpr int kRowTile = 128;                         // output rows per tile = MMA M = TMEM lanes
 constexpr int kColTile = 64;                          // output columns per tile
@@ -460,6 +469,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                                        ((uint32_t)(kMmaN >> 3) << 17) | ((uint32_t)(kRowTile >> 4) << 24);
             int s = 0, acc = 0;
             uint32_t ph = 0, bu = 0, aph = 0;
+            unsigned long long kgroups = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
@@ -487,6 +497,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         }
                         if (!ok) break;
                         mma_commit(smem_addr(&sm.tfull[acc]));          // k-group done
+                        ++kgroups;
                         if (++acc == 2) { acc = 0; aph ^= 1u; }
                     }
                     ++bu;
@@ -495,6 +506,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             // every MMA issued so far has finished before the CTA frees TMEM
             mma_commit(smem_addr(&sm.mdone));
             mbar_wait(smem_addr(&sm.mdone), 0);
+            atomicAdd(&g_exact_tc_kgroups, kgroups);
         }
       }
     } else {
@@ -873,8 +885,21 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
     const int smem = (int)sizeof(TcxSmem) + 1024;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
+    cudaEvent_t t0 = nullptr, t1 = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_timing_mu);
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (g_timing_on && cudaStreamIsCapturing(s, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone &&
+            cudaEventCreate(&t0) == cudaSuccess && cudaEventCreate(&t1) == cudaSuccess) {
+            g_timing_events.emplace_back(t0, t1);
+        } else {
+            t0 = t1 = nullptr;
+        }
+    }
+    if (t0) cudaEventRecord(t0, s);
     kern<<<grid, kTcxThreads, smem, s>>>(ma, mb, a);
     count_launch();
+    if (t1) cudaEventRecord(t1, s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     exact_chunk_repair_kernel<<<kFixBlocks, 256, 0, s>>>(ia, SA, SB, LpA, LpB, a.GA, a.GB, a.chunk_count,
@@ -1038,6 +1063,38 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     const cudaError_t ferr = cudaFreeAsync(ws, stream);
     if (err == cudaSuccess) err = ferr;
     return note_cuda(err);
+}
+
+void exact_tc_timing(int enable) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    if (enable) {
+        for (auto &e : g_timing_events) { cudaEventDestroy(e.first); cudaEventDestroy(e.second); }
+        g_timing_events.clear();
+        const unsigned long long zero = 0;
+        cudaMemcpyToSymbol(g_exact_tc_kgroups, &zero, sizeof zero);
+    }
+    g_timing_on = enable != 0;
+}
+
+carbon_status_t exact_tc_time(double *ms, int64_t *launches, int64_t *kgroups) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    double total = 0.0;
+    for (auto &e : g_timing_events) {
+        cudaError_t err = cudaEventSynchronize(e.second);
+        float t = 0.0f;
+        if (err == cudaSuccess) err = cudaEventElapsedTime(&t, e.first, e.second);
+        if (err != cudaSuccess) return note_cuda(err);
+        total += t;
+    }
+    if (ms) *ms = total;
+    if (launches) *launches = (int64_t)g_timing_events.size();
+    if (kgroups) {
+        unsigned long long v = 0;
+        const cudaError_t err = cudaMemcpyFromSymbol(&v, g_exact_tc_kgroups, sizeof v);
+        if (err != cudaSuccess) return note_cuda(err);
+        *kgroups = (int64_t)v;
+    }
+    return CARBON_OK;
 }
 
 carbon_status_t exact_tc_take_device_status() {

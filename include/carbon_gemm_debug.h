@@ -55,9 +55,23 @@ carbon_status_t carbon_measure_fp64_rate(double *dfma_per_s, double *dadd_per_s,
 
 /* Integer multiply-add rate microbenchmark on the current device (blocking):
  * independent 32x32->64-bit mad.wide.s32 chains on every SM, reported as
- * multiply-adds per second.  The roofline denominator of the bf16 exact
- * tier, whose inner loop is one such multiply-add per product. */
+ * multiply-adds per second.  The roofline denominator of the integer-pipe
+ * bf16 kernel (the no-allocation entry point's path). */
 carbon_status_t carbon_measure_int_mac_rate(double *macs_per_s, carbon_stream_t stream);
+
+/* Timing of the bf16 exact tier's tensor-core kernel.  enable != 0 starts
+ * recording a CUDA event pair on the caller's stream around every launch of
+ * that kernel (outside CUDA-graph capture only) and clears the previous
+ * record; enable == 0 stops recording.  The kernel also counts the
+ * "k-groups" it issues: one k-group is 16 tcgen05.mma instructions of
+ * M = 128, N = 256, K = 16 (one A digit plane against four B digit planes of
+ * one 256-deep chunk), 2 * 128 * 256 * 256 flops. */
+void carbon_debug_kernel_timing(int enable);
+
+/* Sum of the recorded launches' durations in milliseconds (blocking: waits
+ * for the recorded events), their number, and the k-groups issued since the
+ * last carbon_debug_kernel_timing(1).  Any pointer may be NULL. */
+carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t *kgroups);
 
 /* Number of kernel launches the library has enqueued in this process. */
 int64_t carbon_debug_launch_count(void);
