@@ -75,6 +75,9 @@ def _load() -> ctypes.CDLL:
                                              ctypes.POINTER(ctypes.c_int64),
                                              ctypes.POINTER(ctypes.c_int64)]
     lib.carbon_debug_kernel_time.restype = ctypes.c_int
+    lib.carbon_debug_exact_path_counts.argtypes = [ctypes.POINTER(ctypes.c_int64),
+                                                   ctypes.POINTER(ctypes.c_int64)]
+    lib.carbon_debug_exact_path_counts.restype = ctypes.c_int
     return lib
 
 
@@ -210,3 +213,11 @@ def carbon_debug_kernel_time():
     _check(lib.carbon_debug_kernel_time(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(kg)),
            "carbon_debug_kernel_time")
     return ms.value, int(n.value), int(kg.value)
+
+
+def carbon_debug_exact_path_counts():
+    """(chunk repairs, whole-output fix-ups) recorded since timing was enabled."""
+    r, f = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib.carbon_debug_exact_path_counts(ctypes.byref(r), ctypes.byref(f)),
+           "carbon_debug_exact_path_counts")
+    return int(r.value), int(f.value)

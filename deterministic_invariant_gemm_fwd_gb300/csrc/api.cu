@@ -190,4 +190,8 @@ carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t 
     return carbon::exact_tc_time(ms, launches, kgroups);
 }
 
+carbon_status_t carbon_debug_exact_path_counts(int64_t *chunk_repairs, int64_t *fixups) {
+    return carbon::exact_tc_path_counts(chunk_repairs, fixups);
+}
+
 }  // extern "C"

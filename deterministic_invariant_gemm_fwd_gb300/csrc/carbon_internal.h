@@ -72,6 +72,7 @@ carbon_status_t exact_tc_take_device_status();
 // Kernel timing of the bf16 exact tier's tensor-core kernel (exact_tc.cu).
 void exact_tc_timing(int enable);
 carbon_status_t exact_tc_time(double *ms, int64_t *launches, int64_t *kgroups);
+carbon_status_t exact_tc_path_counts(int64_t *repairs, int64_t *fixups);
 
 // Tensor-core tier (tc_gemm.cu).  out_f32 selects the fp32 pre-rounding output.
 carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream);

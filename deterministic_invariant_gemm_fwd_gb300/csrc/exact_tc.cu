@@ -86,6 +86,8 @@ namespace {
 
 __device__ unsigned int g_exact_tc_status = 0;
 __device__ unsigned long long g_exact_tc_kgroups = 0;   // k-groups issued (measurement)
+__device__ unsigned long long g_exact_tc_repairs = 0;   // chunk repairs and fix-ups (measurement)
+__device__ unsigned long long g_exact_tc_fixups = 0;
 
 // Optional CUDA-event timing of the main kernel (carbon_debug_kernel_timing).
 std::mutex g_timing_mu;
@@ -799,6 +801,14 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
     }
 }
 
+// Adds one call's chunk-repair and fix-up list lengths to the measurement
+// counters (launched only while kernel timing is on).
+__global__ void exact_count_kernel(const unsigned int *chunk_count, unsigned int chunk_cap,
+                                   const unsigned int *work_count) {
+    atomicAdd(&g_exact_tc_repairs, (unsigned long long)min(*chunk_count, chunk_cap));
+    atomicAdd(&g_exact_tc_fixups, (unsigned long long)*work_count);
+}
+
 // ---- finalize: bias and the two roundings ------------------------------------
 //
 // KBN over the chunk values is exact in the same way as inside a chunk: the
@@ -908,6 +918,10 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
     count_launch();
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    if (t0) {
+        exact_count_kernel<<<1, 1, 0, s>>>(a.chunk_count, a.chunk_cap, work);
+        count_launch();
+    }
     {
         const int64_t groups = a.rows * ((a.cols + 7) / 8);
         const int64_t want = (groups + 255) / 256;
@@ -1072,6 +1086,8 @@ void exact_tc_timing(int enable) {
         g_timing_events.clear();
         const unsigned long long zero = 0;
         cudaMemcpyToSymbol(g_exact_tc_kgroups, &zero, sizeof zero);
+        cudaMemcpyToSymbol(g_exact_tc_repairs, &zero, sizeof zero);
+        cudaMemcpyToSymbol(g_exact_tc_fixups, &zero, sizeof zero);
     }
     g_timing_on = enable != 0;
 }
@@ -1094,6 +1110,18 @@ carbon_status_t exact_tc_time(double *ms, int64_t *launches, int64_t *kgroups) {
         if (err != cudaSuccess) return note_cuda(err);
         *kgroups = (int64_t)v;
     }
+    return CARBON_OK;
+}
+
+carbon_status_t exact_tc_path_counts(int64_t *repairs, int64_t *fixups) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    unsigned long long r = 0, f = 0;
+    cudaError_t err = cudaDeviceSynchronize();
+    if (err == cudaSuccess) err = cudaMemcpyFromSymbol(&r, g_exact_tc_repairs, sizeof r);
+    if (err == cudaSuccess) err = cudaMemcpyFromSymbol(&f, g_exact_tc_fixups, sizeof f);
+    if (err != cudaSuccess) return note_cuda(err);
+    if (repairs) *repairs = (int64_t)r;
+    if (fixups) *fixups = (int64_t)f;
     return CARBON_OK;
 }
 

@@ -73,6 +73,14 @@ void carbon_debug_kernel_timing(int enable);
  * last carbon_debug_kernel_timing(1).  Any pointer may be NULL. */
 carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t *kgroups);
 
+/* While kernel timing is on, the bf16 exact tier also counts, per call, the
+ * (output, chunk) pairs it recomputes in the chunk repair (a line of that
+ * chunk too wide for the digit planes) and the outputs it recomputes whole
+ * in the fix-up (inf/NaN operands, extreme widths, or integer sums that would
+ * leave the int64 range).  Returns the totals since timing was enabled
+ * (blocking: synchronizes the device).  Any pointer may be NULL. */
+carbon_status_t carbon_debug_exact_path_counts(int64_t *chunk_repairs, int64_t *fixups);
+
 /* Number of kernel launches the library has enqueued in this process. */
 int64_t carbon_debug_launch_count(void);
 

@@ -1,0 +1,188 @@
+"""The bf16 exact tier's tensor-core kernel, path by path, against the oracle.
+
+The kernel computes the literal algorithm's bits (Carbon README, "How It
+Works": float64 products, 256-wide chunks summed with KBN left to right, the
+chunk values combined with KBN) from exact integer chunk sums.  Each test
+below builds operands that drive one of its paths and checks the float64
+value before rounding and the rounded output bit for bit against the CPU
+oracle; where the library's path counters can show that the path ran, the
+test asserts that too:
+
+* rounded chunk values: KBN steps inside a chunk round, the chunk value is the
+  exact chunk sum rounded once to float64;
+* chunk repair: a line of a chunk is wider than the 31 bits the digit planes
+  carry, so that (output, chunk) is summed separately and added in;
+* whole-output fix-up: the integer outer sum would leave the int64 range, or
+  a line holds inf/NaN or is wider than 62 bits;
+* split chunk ranges: few output tiles, the chunk range is cut into pieces
+  whose integer sums add exactly;
+* bias alignment: a bias far finer or far coarser than the output grain.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from deterministic_invariant_gemm_fwd_gb300 import inputs
+from tests.gpu_util import bits, dev, host_bits
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import deterministic_invariant_gemm_fwd_gb300 as cg  # noqa: E402
+
+
+def run(pass_, A, B, bias, M, K, N, f64):
+    shape = oracle.out_shape(pass_, M, K, N)
+    tA, tB = dev(A), dev(B)
+    tb = dev(bias) if bias is not None else None
+    if f64:
+        out = torch.empty(shape, dtype=torch.float64, device="cuda")
+        cg.carbon_debug_exact_y64(pass_, out, tA, tB, tb, M, K, N, "bf16")
+    else:
+        out = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        {"fwd": lambda: cg.carbon_gemm_fwd(out, tA, tB, tb, M, K, N, "bf16", "exact"),
+         "dx": lambda: cg.carbon_gemm_dx(out, tA, tB, M, K, N, "bf16", "exact"),
+         "dw": lambda: cg.carbon_gemm_dw(out, tA, tB, M, K, N, "bf16", "exact")}[pass_]()
+    torch.cuda.synchronize()
+    assert cg.carbon_get_device_status() == 0
+    return host_bits(out)
+
+
+def check(pass_, A, B, bias, M, K, N):
+    """Bit-exact against the oracle; returns (chunk repairs, fix-ups) of the
+    bf16 output call."""
+    ref, ref64 = oracle.gemm(pass_, "bf16", A, B, bias, M, K, N)
+    got64 = run(pass_, A, B, bias, M, K, N, True)
+    cg.carbon_debug_kernel_timing(True)
+    try:
+        got = run(pass_, A, B, bias, M, K, N, False)
+        counts = cg.carbon_debug_exact_path_counts()
+    finally:
+        cg.carbon_debug_kernel_timing(False)
+    assert np.array_equal(got64, bits(ref64)), \
+        f"{pass_} {M}x{K}x{N}: {np.count_nonzero(got64 != bits(ref64))} float64 mismatches"
+    assert np.array_equal(got, bits(ref)), \
+        f"{pass_} {M}x{K}x{N}: {np.count_nonzero(got != bits(ref))} output mismatches"
+    return counts
+
+
+def bf16(a):
+    return inputs.f32_to_bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+def spread(rng, shape, lo, hi, sign=True):
+    """bf16 values m * 2^e, e uniform in [lo, hi], random 8-bit significands."""
+    v = np.ldexp(1.0 + rng.integers(0, 128, shape) / 128.0, rng.integers(lo, hi + 1, shape))
+    if sign:
+        v = v * rng.choice([-1.0, 1.0], shape)
+    return v
+
+
+def test_rounded_chunk_values():
+    """Same-sign operands of width ~30: chunk sums far above 2^53 units of the
+    chunk grain, so KBN's partial sums round; the chunk value must be the exact
+    sum rounded once."""
+    rng = np.random.default_rng(11)
+    M, K, N = 140, 600, 70
+    X = bf16(spread(rng, (M, K), -11, 11, sign=False))
+    W = bf16(spread(rng, (K, N), -11, 11, sign=False))
+    b = bf16(rng.standard_normal(N))
+    check("fwd", X, W, b, M, K, N)
+
+
+def test_chunk_repair_wide_lines():
+    """A few rows and columns hold one tiny entry each (width ~45 bits in that
+    chunk): only those (output, chunk) pairs leave the tensor cores."""
+    rng = np.random.default_rng(12)
+    M, K, N = 200, 520, 100
+    L = inputs.linear_layer(rng, M, K, N, "bf16", 1e-3)
+    X = inputs.bf16_bits_to_f32(L["X"]).copy()
+    W = inputs.bf16_bits_to_f32(L["W"]).copy()
+    X[[3, 77, 150], [10, 300, 511]] = np.float32(2.0 ** -40)
+    W[[5, 260], [7, 64]] = np.float32(-(2.0 ** -50))
+    X, W = bf16(X), bf16(W)
+    repairs, fixups = check("fwd", X, W, L["b"], M, K, N)
+    assert repairs > 0
+    repairs, fixups = check("dw", X, L["dY"], None, M, K, N)
+    assert repairs > 0
+
+
+def test_fixup_outer_sum_out_of_range():
+    """Row 0's first chunk holds tiny entries and its second huge ones: in the
+    output grain the running sum needs far more than 62 bits, so those outputs
+    are recomputed whole."""
+    rng = np.random.default_rng(13)
+    M, K, N = 130, 512, 65
+    X = rng.standard_normal((M, K))
+    X[0, :256] = np.ldexp(1.0, -90) * (1 + rng.integers(0, 128, 256) / 128.0)
+    X[0, 256:] = np.ldexp(1.0, 60) * (1 + rng.integers(0, 128, 256) / 128.0)
+    W = rng.standard_normal((K, N)) * 0.02
+    repairs, fixups = check("fwd", bf16(X), bf16(W), bf16(rng.standard_normal(N) * 0.02), M, K, N)
+    assert fixups > 0
+
+
+def test_fixup_non_finite_and_extreme_widths():
+    """inf in one row, entries 2^-120 and 2^120 in another (width > 62): whole
+    fix-up with the literal float64 loop for those chunks."""
+    rng = np.random.default_rng(14)
+    M, K, N = 66, 300, 33
+    X = rng.standard_normal((M, K))
+    X[5, 17] = np.inf
+    X[9, 3] = 2.0 ** -120
+    X[9, 200] = 2.0 ** 120
+    W = rng.standard_normal((K, N)) * 0.02
+    ref, ref64 = oracle.gemm("fwd", "bf16", bf16(X), bf16(W), None, M, K, N)
+    got64 = run("fwd", bf16(X), bf16(W), None, M, K, N, True)
+    got = run("fwd", bf16(X), bf16(W), None, M, K, N, False)
+    finite = np.isfinite(ref64)
+    assert np.array_equal(got64[finite], bits(ref64)[finite])
+    assert np.array_equal(np.isnan(got64.view(np.float64)), np.isnan(ref64))
+    assert np.array_equal(got[finite], bits(ref)[finite])
+
+
+@pytest.mark.parametrize("M", [4096, 4000])
+def test_split_chunk_ranges_dw(M):
+    """dW with one row tile and two column tiles over 16 chunks of tokens: the
+    chunk range is cut into pieces whose integer sums must add to the
+    one-piece result."""
+    rng = np.random.default_rng(M)
+    K, N = 128, 100
+    L = inputs.linear_layer(rng, M, K, N, "bf16", 1e-4)
+    check("dw", L["X"], L["dY"], None, M, K, N)
+
+
+def test_bias_far_from_the_grain():
+    """Bias entries far finer than the output grain (2^-110) and far coarser
+    (2^50): the bias is added through float64 there."""
+    rng = np.random.default_rng(15)
+    M, K, N = 130, 300, 66
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((K, N)) * 0.02
+    b = rng.standard_normal(N) * 0.02
+    b[:10] = np.ldexp(1.0, -110) * (1 + rng.integers(0, 128, 10) / 128.0)
+    b[10:20] = np.ldexp(1.0, 50) * (1 + rng.integers(0, 128, 10) / 128.0)
+    b[20] = 0.0
+    b[21] = -0.0
+    check("fwd", bf16(X), bf16(W), bf16(b), M, K, N)
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dx", "dw"])
+def test_gpt2_shape_tail_and_zero_lines(pass_):
+    """A GPT-2-like layer with ragged sizes, zero rows and zero columns, and
+    whole zero chunks."""
+    rng = np.random.default_rng(16)
+    M, K, N = 300, 700, 190
+    L = inputs.linear_layer(rng, M, K, N, "bf16", 1e-4)
+    X = inputs.bf16_bits_to_f32(L["X"]).copy()
+    X[7, :] = 0.0
+    X[:, 256:512] = 0.0
+    W = inputs.bf16_bits_to_f32(L["W"]).copy()
+    W[:, 3] = 0.0
+    dY = inputs.bf16_bits_to_f32(L["dY"]).copy()
+    dY[:, 11] = -0.0
+    ops = {"fwd": (bf16(X), bf16(W), L["b"]), "dx": (bf16(dY), bf16(W), None),
+           "dw": (bf16(X), bf16(dY), None)}[pass_]
+    check(pass_, *ops, M, K, N)
