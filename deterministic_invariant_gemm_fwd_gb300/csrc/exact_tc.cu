@@ -138,11 +138,10 @@ struct TcxArgs {
     const int *GA, *GB;                               // line grains (smallest base) [Lp]
     const int *cntA;                                  // A planes per (row tile, chunk)
     unsigned int *work_count, *work_list;             // deferred outputs
-    long long *Tout;                                  // exact sums in the output grain [piece][rows][cols]
+    long long *Tout;                                  // exact sums in the output grain [piece][cols][rows]
     unsigned int *chunk_count;                        // (output, chunk) pairs for the chunk repair
     uint2 *chunk_list;
     unsigned int chunk_cap;
-    int vec_t;                                        // Tout rows start 16-byte aligned
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -608,6 +607,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 // the lanes' rows and columns)
                 const int wxm = (int)__reduce_max_sync(0xffffffffu, (unsigned)wx);
                 const int wwm = (int)__reduce_max_sync(0xffffffffu, (unsigned)cl.y);
+                const int shcm = (int)__reduce_max_sync(0xffffffffu, (unsigned)shc);
                 const int bndm = min(min((int)__reduce_max_sync(0xffffffffu, (unsigned)lsx) +
                                              (int)__reduce_max_sync(0xffffffffu, (unsigned)cl.w),
                                          (int)__reduce_max_sync(0xffffffffu, (unsigned)lmx) +
@@ -623,24 +623,35 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     rs = __ldg(&p.SA[(int64_t)(q + 1) * p.LpA + i]);
                     cl = __ldg(&p.SB[(int64_t)(q + 1) * p.LpB + jw + lane]);
                 }
-                // I is exact (modulo 2^64, and below 2^62) when every line fits
-                const bool exact_i = wxm <= 31 && wwm <= 31 && bndm <= 62;
-                uint32_t redo = exact_i ? 0u : 0xffffffffu;  // outputs for the per-output path
-                if (exact_i) {
-                    // T += I << sh wherever |I| <= 2^53 (the chunk value needs no
-                    // rounding), the shift loses no bit and T stays below 2^62;
-                    // zero lines have I = 0, so their shift does not matter
+                // I is exact (modulo 2^64, and below 2^62) when every line fits.
+                // Then all 32 outputs take T += I << sh at once while the checks
+                // gather: the shifts lose no bit (and are below 64), no chunk
+                // value rounds (|I| < 2^53) and T stays below 2^62 (the sum of
+                // |T| < 2^62 and a lossless shift cannot wrap past that test).
+                // A row that fails takes its additions back (exact, modulo 2^64)
+                // and each of its outputs goes the long way.
+                uint32_t redo = 0xffffffffu;                 // outputs for the per-output path
+                bool added = false;                          // T holds this chunk's additions
+                if (wxm <= 31 && wwm <= 31 && bndm <= 62) {
+                    uint32_t lost = 0u, shs = 0u, ah = 0u, th = 0u;
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
+                        const uint32_t sh = (uint32_t)shr + (sm.pk[ew][jj] & 0xffu);
                         const long long Ij = (long long)I[jj];
-                        const int sh = shr + (int)(sm.pk[ew][jj] & 0xffu);
-                        const int ib = 64 - __clzll(Ij ^ (Ij >> 63));     // |I| <= 2^ib
-                        const long long Tn = (long long)T[jj] + (Ij << (sh & 63));
-                        const bool ok = ib <= 53 && ib + sh <= 61 &&
-                                        (unsigned long long)(Tn + (1ll << 62)) < (1ull << 63);
-                        T[jj] = ok ? (unsigned long long)Tn : T[jj];
-                        redo |= ok ? 0u : (1u << jj);
+                        const long long v = Ij << (sh & 63u);
+                        const long long back = (v >> (sh & 63u)) ^ Ij;
+                        lost |= (uint32_t)back | (uint32_t)(back >> 32);
+                        shs |= sh;
+                        const uint32_t ih = (uint32_t)(Ij >> 32);
+                        ah |= ih ^ (uint32_t)((int)ih >> 31);
+                        T[jj] += (unsigned long long)v;
+                        const uint32_t t = (uint32_t)(T[jj] >> 32);
+                        th |= t ^ (uint32_t)((int)t >> 31);
                     }
+                    // a row that fails redoes its outputs one by one (its additions
+                    // are still in T; each output keeps or takes back its own)
+                    added = !(lost == 0u && shs < 64u && ah < (1u << 21) && th < (1u << 30));
+                    redo = added ? 0xffffffffu : 0u;
                 }
                 if (redo != 0u) {
                     // per output: the chunk value is the exact chunk sum rounded
@@ -650,6 +661,17 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     for (int jj = 0; jj < 32; ++jj) {
                         const uint32_t bit = 1u << jj;
                         if (!(redo & bit)) continue;
+                        if (added) {
+                            // this output's own checks: keep the addition when they pass
+                            const uint32_t sh = (uint32_t)shr + (sm.pk[ew][jj] & 0xffu);
+                            const long long I0 = (long long)I[jj];
+                            const long long v = I0 << (sh & 63u);
+                            const int ih = (int)(I0 >> 32), t = (int)(T[jj] >> 32);
+                            if ((v >> (sh & 63u)) == I0 && sh < 64u && (uint32_t)(ih + (1 << 21)) < (1u << 22) &&
+                                (uint32_t)(t + (1 << 30)) < (1u << 31))
+                                continue;
+                            T[jj] -= (unsigned long long)v;
+                        }
                         long long Ij = (long long)I[jj];
                         const uint32_t w = sm.pk[ew][jj];
                         const int ww = (int)((w >> 8) & 0x7fu);
@@ -660,8 +682,9 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                             Ij = round_to_53_bits(Ij);                      // |result| <= 2^bnd
                         const int sh = shr + (int)(w & 0xffu);
                         const long long Tn = (long long)T[jj] + (Ij << (sh & 63));
+                        const int ib = 64 - __clzll(Ij ^ (Ij >> 63));          // |Ij| <= 2^ib
                         // no bit of I << sh lost, and the running sum stays below 2^62
-                        const bool ok_add = bnd + sh <= 61 &&
+                        const bool ok_add = ib + sh <= 61 &&
                                             (unsigned long long)(Tn + (1ll << 62)) < (1ull << 63);
                         // a zero line (wx or ww 0) adds +0, which changes nothing
                         const bool live = fits && !(defer & bit) && wx != 0 && ww != 0;
@@ -678,6 +701,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                             }
                         }
                         defer |= bad ? bit : 0u;
+                        T[jj] = bad ? 0ull : T[jj];
                     }
                 }
                 nx = (q + 1 < qhi) ? cnt[q + 1] : 0;
@@ -688,21 +712,14 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             if (!ok) break;
 
             // ---- this piece's exact partial sums go to the finalize kernel
-            // (deferred outputs: a sentinel no sum reaches, |T| < 2^62)
+            // (deferred outputs: a sentinel no sum reaches, |T| < 2^62), stored
+            // column-major so that a warp's 32 rows make one contiguous store
             if (i < p.rows) {
-                long long *trow = p.Tout + (int64_t)piece * p.rows * p.cols + i * p.cols + jw;
-                if (p.vec_t && jw + 32 <= p.cols) {
+                long long *tcol = p.Tout + (int64_t)piece * p.rows * p.cols + jw * p.rows + i;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const long long a0 = ((defer >> (2 * c)) & 1u) ? kDeferredSum : (long long)T[2 * c];
-                        const long long a1 = ((defer >> (2 * c + 1)) & 1u) ? kDeferredSum : (long long)T[2 * c + 1];
-                        *reinterpret_cast<longlong2 *>(trow + 2 * c) = make_longlong2(a0, a1);
-                    }
-                } else {
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj)
-                        if (jw + jj < p.cols) trow[jj] = ((defer >> jj) & 1u) ? kDeferredSum : (long long)T[jj];
-                }
+                for (int jj = 0; jj < 32; ++jj)
+                    if (jw + jj < p.cols)
+                        tcol[(int64_t)jj * p.rows] = ((defer >> jj) & 1u) ? kDeferredSum : (long long)T[jj];
             }
             // outputs for the fix-up pass
             for (uint32_t dm = defer; dm != 0u; dm &= dm - 1u) {
@@ -790,7 +807,7 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
             ok = (v >> sh) == J && v >= -((__int128)1 << 61) && v < ((__int128)1 << 61);
         }
         if (ok) {
-            long long *slot = Tout + (q / cps) * p.rows * p.cols + o;
+            long long *slot = Tout + (q / cps) * p.rows * p.cols + j * p.rows + i;
             const long long add = (long long)v;
             const long long old = (long long)atomicAdd(reinterpret_cast<unsigned long long *>(slot),
                                                        (unsigned long long)add);
@@ -817,7 +834,8 @@ __global__ void exact_count_kernel(const unsigned int *chunk_count, unsigned int
 // and the sum is rounded once more, to float64 and then to bf16 (both nearest
 // even), all on integers; values outside those fast ranges take the float64
 // route.  The chunk range of an output may have been split into pieces whose
-// partial sums T add exactly.  One thread per 8 consecutive outputs of a row.
+// partial sums T add exactly.  One thread per 8 consecutive outputs of a row,
+// consecutive threads on consecutive rows (T is stored column-major).
 template <bool OUT_F64>
 __global__ void __launch_bounds__(256)
 exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int *__restrict__ GA,
@@ -827,7 +845,7 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
     const int64_t plane = rows * cols;
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < rows * gpr;
          g += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = g / gpr, j0 = (g % gpr) * 8;
+        const int64_t i = g % rows, j0 = (g / rows) * 8;
         const int gx = __ldg(&GA[i]);
         uint32_t packed[4] = {0u, 0u, 0u, 0u};
         uint32_t skip = 0u;
@@ -839,7 +857,7 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             __int128 acc = 0;
             bool deferred = false;
             for (int k = 0; k < pieces; ++k) {
-                const long long t = __ldg(&Tout[k * plane + i * cols + j]);
+                const long long t = __ldg(&Tout[k * plane + j * rows + i]);
                 if (t == kDeferredSum) { deferred = true; break; }
                 acc += t;
             }
@@ -1068,7 +1086,6 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         a.chunk_count = ccount;
         a.chunk_list = clist;
         a.chunk_cap = (unsigned int)ccap;
-        a.vec_t = (p.cols % 2) == 0 ? 1 : 0;
         const int64_t units = tiles_m * tiles_n * pieces;
         const int grid = (int)(units < sms ? units : sms);
         err = out_f64 ? launch_tc_main<true>(ma, mb, a, grid, ia, SA, SB, LpA, LpB, work, stream)
