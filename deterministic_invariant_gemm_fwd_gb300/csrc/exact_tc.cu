@@ -31,8 +31,11 @@
 //    1.5 * 2^23: every partial sum stays in [2^23, 2^24], where fp32 spacing
 //    is 1, so the accumulation is exact for any order of addition, and the
 //    accumulator's bit pattern minus that of 1.5 * 2^23 is the pair sum;
-//  * I = sum_{a,b} 256^(a+b) (pair sum), assembled modulo 2^64 with integer
-//    multiply-adds; it is exact when the statistics bound |I| below 2^62.
+//  * I = sum_{a,b} 256^(a+b) (pair sum), assembled modulo 2^64: the sums of
+//    B digits 2p and 2p + 1 combine exactly in 32 bits (|s + 256 s'| < 2^31,
+//    the starting values taken out by one constant), then one 64-bit
+//    multiply-add per combined pair; I is exact when the statistics bound
+//    |I| below 2^62.
 // A line of width w <= 31 needs ceil((w + 1) / 8) digits; a tile uses the most
 // any of its rows needs (A side, 1..4 planes per chunk) and always 4 planes on
 // the B side.  One tcgen05.mma of M = 128, N = 256, K = 16 multiplies one A
@@ -301,14 +304,15 @@ __device__ __forceinline__ void acc_hi(unsigned long long &I, uint32_t v, uint32
         : "+l"(I) : "r"(v), "r"(mul));
 }
 
-// Sum over the nx * 4 digit pairs of a chunk of the accumulators' starting
-// value times the pair's weight: kMagicBits * sum_{a < nx, b < 4} 256^(a+b),
-// modulo 2^64.
-__device__ __forceinline__ unsigned long long magic_sum(int nx) {
-    unsigned long long wa = 0ull;
-    for (int a = 0; a < nx; ++a) wa |= 1ull << (8 * a);
-    return (unsigned long long)kMagicBits * (wa * 0x01010101ull);
+// I += P * mul, P a signed 32-bit value, mul = 256^c (c <= 3), 32 x 32 -> 64-bit.
+__device__ __forceinline__ void acc_pair_lo(unsigned long long &I, uint32_t P, uint32_t mul) {
+    asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(I) : "r"(P), "r"(mul));
 }
+
+// Two accumulators a, b of planes 2 pp and 2 pp + 1 (bits = 1.5 * 2^23 + u,
+// |u| <= 2^22): (bits_b << 8) + bits_a + kPairFix = u_a + 256 u_b modulo 2^32,
+// which fits a signed 32-bit value.
+constexpr uint32_t kPairFix = 0u - 257u * kMagicBits;
 
 // bf16 bits of RN_bf16(RN_float64(V * 2^s)) (both nearest-even), |V| < 2^63,
 // computed on the integer: false when the result leaves the bf16 normal
@@ -545,14 +549,13 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             const int Gwl = __ldg(&p.GB[jw + lane]);
             __syncwarp();                                    // last tile's reads are done
             __syncwarp();
-            // I starts at minus the accumulators' starting values summed over
-            // the chunk's pairs, so that after the k-groups it is the chunk sum
+            // I, the chunk sum, starts at 0 (each plane pair's starting values
+            // are taken out as it is added); T, the exact sum, too
             int nx = qlo < qhi ? cnt[qlo] : 0;
             unsigned long long I[32], T[32];
             {
-                const unsigned long long c0 = 0ull - magic_sum(nx);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) { I[c] = c0; T[c] = 0ull; }
+                for (int c = 0; c < 32; ++c) { I[c] = 0ull; T[c] = 0ull; }
             }
             uint32_t defer = 0u;
             int4 rs = make_int4(0, 0, 0, 0), cl = rs;        // this chunk's statistics, loaded ahead
@@ -566,27 +569,35 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     if (!(ok = wait_or_abort(smem_addr(&sm.tfull[acc]), aph, abort_flag))) break;
                     tc_fence_after();
                     const uint32_t ta = tlane + (uint32_t)(acc * kMmaN);
-                    // 8 loads of 16 columns (4 planes x 2 halves), each issued
-                    // before the previous one's values are added in
+                    // 8 units: planes (2 pp, 2 pp + 1) of 8 columns (group g), two
+                    // 8-column loads each, issued before the previous unit's values
+                    // are added in.  The two planes' sums combine exactly in 32 bits
+                    // (|u_a + 256 u_b| < 2^31), on the integer ALUs, before one
+                    // 64-bit multiply-add per pair.
                     uint32_t va[16], vb[16];
-                    tmem_ld16_issue(ta, va);
+                    tmem_ld8x2_issue(ta, ta + (uint32_t)kColTile, va);
 #pragma unroll
-                    for (int idx = 0; idx < 2 * kPlanes; ++idx) {
-                        const int pl = idx >> 1, h = idx & 1;
-                        uint32_t(&cur)[16] = (idx & 1) ? vb : va;
-                        uint32_t(&nxt)[16] = (idx & 1) ? va : vb;
+                    for (int un = 0; un < 8; ++un) {
+                        const int pp = un & 1, g = un >> 1;
+                        uint32_t(&cur)[16] = (un & 1) ? vb : va;
+                        uint32_t(&nxt)[16] = (un & 1) ? va : vb;
                         tmem_wait_ld16(cur);
-                        if (idx + 1 < 2 * kPlanes)
-                            tmem_ld16_issue(ta + (uint32_t)(((idx + 1) >> 1) * kColTile + 16 * ((idx + 1) & 1)), nxt);
-                        const int c = k + pl;                // weight 256^c
+                        if (un + 1 < 8) {
+                            const int pn = (un + 1) & 1, gn = (un + 1) >> 1;
+                            const uint32_t an = ta + (uint32_t)(2 * pn * kColTile + 8 * gn);
+                            tmem_ld8x2_issue(an, an + (uint32_t)kColTile, nxt);
+                        }
+                        const int c = k + 2 * pp;            // weight 256^c of plane 2 pp
                         if (c <= 3) {
                             const uint32_t mul = 1u << (8 * c);
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) acc_lo(I[16 * h + jj], cur[jj], mul);
+                            for (int jj = 0; jj < 8; ++jj)
+                                acc_pair_lo(I[8 * g + jj], (cur[8 + jj] << 8) + cur[jj] + kPairFix, mul);
                         } else {
                             const uint32_t mul = 1u << (8 * (c - 4));
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) acc_hi(I[16 * h + jj], cur[jj], mul);
+                            for (int jj = 0; jj < 8; ++jj)
+                                acc_hi(I[8 * g + jj], (cur[8 + jj] << 8) + cur[jj] + kPairFix, mul);
                         }
                     }
 #pragma unroll
@@ -705,9 +716,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     }
                 }
                 nx = (q + 1 < qhi) ? cnt[q + 1] : 0;
-                const unsigned long long c0 = 0ull - magic_sum(nx);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) I[c] = c0;
+                for (int c = 0; c < 32; ++c) I[c] = 0ull;
             }
             if (!ok) break;
 

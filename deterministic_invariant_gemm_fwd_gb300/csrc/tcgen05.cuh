@@ -85,6 +85,19 @@ __device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&v)[16
         : "r"(taddr));
 }
 
+// Two 32 lanes x 8 columns loads into one array, without the wait: v[0..7]
+// from columns at taddr_a, v[8..15] from columns at taddr_b.
+__device__ __forceinline__ void tmem_ld8x2_issue(uint32_t taddr_a, uint32_t taddr_b, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+        : "r"(taddr_a));
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr_b));
+}
+
 // Waits for this thread's tensor-memory loads; v is tied to the wait so
 // that no read of it moves above it.
 __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&v)[16]) {
