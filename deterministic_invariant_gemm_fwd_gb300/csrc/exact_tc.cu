@@ -62,12 +62,14 @@
 //   warp 3     TMA producer of B: per chunk the four B planes of each 64-deep
 //              block (4 x 32 KiB, resident for the chunk)
 //   warp 1     MMA issuer: two accumulators of 256 TMEM columns used in turn,
-//              one per k-group
+//              one per k-group, each k-group opened by one K = 16 MMA of two
+//              constant shared-memory tiles that sets the accumulator to
+//              1.5 * 2^23 (so the epilogue never writes tensor memory)
 //   warps 4-11 epilogue: warp w reads lanes 32 (w % 4) .. +31 and 32 of the 64
 //              output columns; adds the pair sums into per-output int64 chunk
-//              sums, writes 1.5 * 2^23 back into the accumulator, releases it;
-//              at each chunk end proves the chunk, updates the outer sum; at the
-//              tile end adds the bias, rounds and stores.  Each thread keeps
+//              sums and releases the accumulator; at each chunk end checks the
+//              chunk and adds it to the outer sum; at the tile end stores the
+//              exact partial sums for the finalize kernel.  Each thread keeps
 //              32 outputs' chunk and outer sums in registers, which is why
 //              warpgroup 0 hands its registers to the epilogue (setmaxnreg).
 // Every wait is bounded (device_sync.cuh); a wait that gives up records
@@ -122,9 +124,19 @@ constexpr uint32_t kTmemCols = 2 * kMmaN;             // 512
 constexpr int kGrainNone = 0x40404040;                // grain of a line with no nonzero chunk (byte fill)
 constexpr long long kDeferredSum = (long long)0x8000000000000000ull;   // Tout of a deferred output
 
+// Start tiles: every 16-byte piece holds one bf16 value x and seven zeros, so
+// one K = 16 MMA of the A tile (x = 1) with the B tile (x = 1.5 * 2^22) writes
+// 2 * 1.5 * 2^22 = 1.5 * 2^23 to every accumulator element, whatever the order
+// in which the tensor core walks the pieces.
+constexpr uint32_t kStartABytes = kRowTile * kUmmaK * 2;   // 4 KiB
+constexpr uint32_t kStartBBytes = kMmaN * kUmmaK * 2;      // 8 KiB
+constexpr uint32_t kStartABits = 0x3F80u;                 // bf16 1.0
+constexpr uint32_t kStartBBits = 0x4AC0u;                 // bf16 1.5 * 2^22
+
 struct __align__(1024) TcxSmem {
     uint8_t B[kKBlocks][kBBytes];                     // 128 KiB: the chunk's B planes
     uint8_t A[kAStages][kABytes];                     // 80 KiB: A plane blocks
+    uint8_t SA0[kStartABytes], SB0[kStartBBytes];     // 12 KiB: the accumulators' start tiles
     uint32_t pk[kEpiWarps][32];                       // packed column words of the current chunk
     uint64_t afull[kAStages], aempty[kAStages], bfull[kKBlocks], bempty[kKBlocks];
     uint64_t tfull[2], tempty[2], mdone;
@@ -396,6 +408,12 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             prefetch_map(&map_b);
         }
     }
+    for (uint32_t o = threadIdx.x * 16u; o < kStartABytes + kStartBBytes; o += kTcxThreads * 16u) {
+        const uint32_t x = o < kStartABytes ? kStartABits : kStartBBits;
+        uint8_t *dst = o < kStartABytes ? &sm.SA0[o] : &sm.SB0[o - kStartABytes];
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(x, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
     if (warp == 1) tmem_alloc(smem_addr(&sm.tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -472,6 +490,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         if (lane == 0) {
             constexpr uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                        ((uint32_t)(kMmaN >> 3) << 17) | ((uint32_t)(kRowTile >> 4) << 24);
+            const uint64_t sdesc_a0 = smem_desc_noswizzle(smem_addr(&sm.SA0[0]), 128, 256);
+            const uint64_t sdesc_b0 = smem_desc_noswizzle(smem_addr(&sm.SB0[0]), 128, 256);
             int s = 0, acc = 0;
             uint32_t ph = 0, bu = 0, aph = 0;
             unsigned long long kgroups = 0;
@@ -487,6 +507,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         if (!(ok = wait_or_abort(smem_addr(&sm.tempty[acc]), aph, abort_flag))) break;
                         tc_fence_after();
                         const uint32_t d = tmem + (uint32_t)(acc * kMmaN);
+                        mma_bf16(d, sdesc_a0, sdesc_b0, idesc, 0u);    // every element 1.5 * 2^23
                         for (int kb = 0; kb < kKBlocks; ++kb) {
                             if (k == 0 && !(ok = wait_or_abort(smem_addr(&sm.bfull[kb]), bu & 1u, abort_flag))) break;
                             if (!(ok = wait_or_abort(smem_addr(&sm.afull[s]), ph, abort_flag))) break;
@@ -522,15 +543,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         const int half = ew / 4;                             // output columns 32 half .. +31
         const int rl = quarter * 32 + lane;                  // row within the tile
         const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * 32);
-        // both accumulators start at 1.5 * 2^23
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-#pragma unroll
-            for (int pl = 0; pl < kPlanes; ++pl)
-                tmem_fill32(tlane + (uint32_t)(b * kMmaN + pl * kColTile), kMagicBits);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
+        // both accumulators are free (each k-group's first MMA sets them to
+        // 1.5 * 2^23)
         if (lane == 0) {
             mbar_arrive(smem_addr(&sm.tempty[0]));
             mbar_arrive(smem_addr(&sm.tempty[1]));
@@ -600,10 +614,6 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                                 acc_hi(I[8 * g + jj], (cur[8 + jj] << 8) + cur[jj] + kPairFix, mul);
                         }
                     }
-#pragma unroll
-                    for (int pl = 0; pl < kPlanes; ++pl)
-                        tmem_fill32(ta + (uint32_t)(pl * kColTile), kMagicBits);
-                    tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_addr(&sm.tempty[acc]));

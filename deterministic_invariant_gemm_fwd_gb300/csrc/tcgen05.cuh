@@ -120,6 +120,22 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
+// Shared-memory matrix descriptor without swizzle (core matrices of 8 rows x
+// 16 bytes; lbo between core matrices along K, sbo along M/N).
+__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    return d;
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the
+// tensor cores (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 32 lanes x 32 columns of 32-bit from registers: thread t of the warp writes
 // lane (base lane + t), columns col .. col+31, every column the value v.
 __device__ __forceinline__ void tmem_fill32(uint32_t taddr, uint32_t v) {
