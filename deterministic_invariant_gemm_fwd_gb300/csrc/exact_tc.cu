@@ -861,12 +861,25 @@ __global__ void __launch_bounds__(256)
 exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int *__restrict__ GA,
                       const int *__restrict__ GB, const unsigned short *__restrict__ bias, void *out,
                       int64_t rows, int64_t cols, int vec_out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // a row per thread
+    if (i >= rows) return;
     const int64_t gpr = (cols + 7) / 8;
     const int64_t plane = rows * cols;
-    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < rows * gpr;
-         g += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = g % rows, j0 = (g / rows) * 8;
-        const int gx = __ldg(&GA[i]);
+    const int gx = __ldg(&GA[i]);
+    for (int64_t jg = blockIdx.y; jg < gpr; jg += gridDim.y) {   // 8 columns per step
+        const int64_t j0 = jg * 8;
+        // every load first: the partial sums (a warp reads 32 consecutive
+        // rows of one column), the column grains and the bias
+        long long t0[8];
+        int gw[8];
+        uint32_t hb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const bool in = j0 + e < cols;
+            t0[e] = in ? __ldg(&Tout[(j0 + e) * rows + i]) : 0ll;
+            gw[e] = in ? __ldg(&GB[j0 + e]) : 0;
+            hb[e] = (in && bias != nullptr) ? ld_bits(bias, j0 + e) : 0u;
+        }
         uint32_t packed[4] = {0u, 0u, 0u, 0u};
         uint32_t skip = 0u;
 #pragma unroll
@@ -874,19 +887,19 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             const int64_t j = j0 + e;
             if (j >= cols) { skip |= 1u << e; continue; }
             // the pieces' partial sums add exactly (128 bits)
-            __int128 acc = 0;
-            bool deferred = false;
-            for (int k = 0; k < pieces; ++k) {
+            bool deferred = t0[e] == kDeferredSum;
+            __int128 acc = t0[e];
+            for (int k = 1; k < pieces && !deferred; ++k) {
                 const long long t = __ldg(&Tout[k * plane + j * rows + i]);
-                if (t == kDeferredSum) { deferred = true; break; }
+                deferred = t == kDeferredSum;
                 acc += t;
             }
             if (deferred) { skip |= 1u << e; continue; }
-            const int G = gx + __ldg(&GB[j]);
+            const int G = gx + gw[e];
             const bool small = acc >= -((__int128)1 << 62) && acc < ((__int128)1 << 62);
             if (OUT_F64 || !small) {
                 double y = small ? round_int_to_double((long long)acc, G) : round_i128_to_double(acc, G);
-                if (bias != nullptr) y = __dadd_rn(y, widen_bf16(ld_bits(bias, j)));
+                if (bias != nullptr) y = __dadd_rn(y, widen_bf16(hb[e]));
                 if (OUT_F64) static_cast<double *>(out)[i * cols + j] = y;
                 else packed[e / 2] |= (uint32_t)exact_round_bf16(y) << (16 * (e & 1));
                 continue;
@@ -894,7 +907,7 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             const long long T = (long long)acc;
             int bm = 0, be = 0;
             bool bad = false;
-            if (bias != nullptr) decode(ld_bits(bias, j), bm, be, bad);
+            if (bias != nullptr) decode(hb[e], bm, be, bad);
             long long Tv = T;
             int gs = G;
             bool fused = !bad;
@@ -961,12 +974,11 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
         count_launch();
     }
     {
-        const int64_t groups = a.rows * ((a.cols + 7) / 8);
-        const int64_t want = (groups + 255) / 256;
-        const int blocks = (int)(want < 8 * 152 ? (want > 0 ? want : 1) : 8 * 152);
+        const int64_t gpr = (a.cols + 7) / 8;
+        const dim3 grid((unsigned)((a.rows + 255) / 256), (unsigned)(gpr < 65535 ? gpr : 65535));
         const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0 && (a.cols % 8) == 0) ? 1 : 0;
-        exact_finalize_kernel<F64><<<blocks, 256, 0, s>>>(a.Tout, a.splits, a.GA, a.GB, a.bias, a.out,
-                                                           a.rows, a.cols, vec_out);
+        exact_finalize_kernel<F64><<<grid, 256, 0, s>>>(a.Tout, a.splits, a.GA, a.GB, a.bias, a.out,
+                                                         a.rows, a.cols, vec_out);
         count_launch();
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
