@@ -882,6 +882,37 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
         }
         uint32_t packed[4] = {0u, 0u, 0u, 0u};
         uint32_t skip = 0u;
+        if (!OUT_F64 && pieces == 1) {
+            // one piece: 64-bit sums; the common case (the bias joins the sum
+            // exactly, the two roundings on the integer) stays straight-line,
+            // the rest takes the float64 route of out_bits_f64
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const long long T = t0[e];
+                if (j0 + e >= cols || T == kDeferredSum) { skip |= 1u << e; continue; }
+                const int G = gx + gw[e];
+                int bm = 0, be = 0;
+                bool bad = false;
+                decode(hb[e], bm, be, bad);
+                const bool t53 = (unsigned long long)(T + (1ll << 53)) < (1ull << 54);   // |T| < 2^53
+                long long Tv = T;
+                int gs = G;
+                bool fused = !bad;
+                if (bm != 0) {
+                    if (be >= G && be - G <= 54) {
+                        Tv = (t53 ? T : round_to_53_bits(T)) + ((long long)bm << (be - G));
+                    } else if (be < G && G - be <= 9 && t53) {
+                        Tv = (T << (G - be)) + bm;
+                        gs = be;
+                    } else {
+                        fused = false;
+                    }
+                }
+                uint32_t bits = 0u;
+                if (!(fused && round_int_to_bf16(Tv, gs, bits))) bits = out_bits_f64(T, G, bias, j0 + e);
+                packed[e / 2] |= bits << (16 * (e & 1));
+            }
+        } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int64_t j = j0 + e;
@@ -925,6 +956,7 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             uint32_t bits = 0u;
             if (!(fused && round_int_to_bf16(Tv, gs, bits))) bits = out_bits_f64(T, G, bias, j);
             packed[e / 2] |= bits << (16 * (e & 1));
+        }
         }
         if (OUT_F64) continue;
         unsigned short *orow = static_cast<unsigned short *>(out) + i * cols + j0;
