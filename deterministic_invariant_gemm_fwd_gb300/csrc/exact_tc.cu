@@ -21,8 +21,9 @@
 // before the bias is the exact sum of the chunk values rounded once.
 //
 // Chunk sums on the tensor cores.  I is computed exactly:
-//  * every X is written in balanced base-256 digits, X = sum_a d_a 256^a with
-//    |d_a| <= 128 (digits 0..n-2 in [-128, 127], the top digit the remainder),
+//  * every X is written in base-256 digits, X = sum_a d_a 256^a with
+//    |d_a| <= 128: X = m * 2^s (|m| < 2^8) has two, lo = v mod 256 in
+//    [-128, 127] at a = s / 8 and (v - lo) / 256 at a + 1, v = m * 2^(s % 8);
 //    likewise W = sum_b e_b 256^b; a digit is an integer of at most 8
 //    significant bits, so it is exact in bf16;
 //  * for one digit pair (a, b) the 256 products d_a e_b are integers of
@@ -169,25 +170,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 
 // ---- pre-pass: statistics and digit planes ------------------------------------
 
-// Balanced base-256 digits of X in np planes: digits 0 .. np-2 in [-128, 127],
-// digit np-1 the remainder (|remainder| <= 128 when |X| < 2^(8 np - 1)).
-__device__ __forceinline__ void split_digits(int X, int np, int (&d)[kPlanes]) {
-    int x = X;
-#pragma unroll
-    for (int a = 0; a < kPlanes; ++a) {
-        if (a < np - 1) {
-            const int u = x & 0xff, carry = u >> 7;
-            d[a] = u - (carry << 8);
-            x = (x >> 8) + carry;
-        } else if (a == np - 1) {
-            d[a] = x;
-            x = 0;
-        } else {
-            d[a] = 0;
-        }
-    }
-}
-
 // bf16 bits of an integer of magnitude <= 256 (exact).
 __device__ __forceinline__ uint32_t small_int_bf16(int d) {
     return __float_as_uint((float)d) >> 16;
@@ -206,7 +188,8 @@ constexpr int kRawPitch = kChunk + 8;                 // bf16 per staged line (1
 // the reduction indices 8t .. 8t+7.  The source element (line, r) is
 // src[line * ls + r * rs]; RCONTIG says rs == 1 (lines are read directly),
 // otherwise the block's lines are staged in shared memory first (coalesced
-// along the lines).  Writes stats[chunk * Lp + line]; the line's digits in its
+// along the lines).  vec says 16-byte loads are aligned: 8 reduction indices
+// of a line (RCONTIG), or 8 lines at one reduction index (ls == 1).  Writes stats[chunk * Lp + line]; the line's digits in its
 // own count n of planes (the top one the remainder) and zeros in the planes
 // above, tile by tile: plane a of line L at row (L / tg) 4 tg + a tg + L % tg
 // of the [4 Lp][Rp] array (tg = tile lines); raises cnt[(L / tg) * nchunks +
@@ -218,17 +201,29 @@ __global__ void __launch_bounds__(kPrepThreads)
 digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs, int64_t nlines,
                   int64_t R, int64_t Lp, int64_t Rp, int tg, unsigned short *__restrict__ planes,
                   int4 *__restrict__ stats, int *__restrict__ grain, int *__restrict__ cnt,
-                  int nchunks) {
+                  int nchunks, int vec) {
     __shared__ __align__(16) unsigned short raw[RCONTIG ? 1 : kPrepLines * kRawPitch];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int64_t line0 = (int64_t)blockIdx.x * kPrepLines;
     const int q = blockIdx.y;
     const int64_t q0 = (int64_t)q * kChunk;
     if (!RCONTIG) {
-        for (int e = tid; e < kPrepLines * kChunk; e += kPrepThreads) {
-            const int l = e % kPrepLines, r = e / kPrepLines;
-            const int64_t line = line0 + l, rr = q0 + r;
-            raw[l * kRawPitch + r] = (line < nlines && rr < R) ? src[line * ls + rr * rs] : (unsigned short)0;
+        if (vec && line0 + kPrepLines <= nlines && q0 + kChunk <= R) {
+            // 8 lines at one reduction index per 16-byte load
+            for (int e = tid; e < kPrepLines / 8 * kChunk; e += kPrepThreads) {
+                const int lg = e % (kPrepLines / 8), r = e / (kPrepLines / 8);
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + (line0 + 8 * lg) + (q0 + r) * rs));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    raw[(8 * lg + t) * kRawPitch + r] = (unsigned short)(w[t / 2] >> (16 * (t & 1)));
+            }
+        } else {
+            for (int e = tid; e < kPrepLines * kChunk; e += kPrepThreads) {
+                const int l = e % kPrepLines, r = e / kPrepLines;
+                const int64_t line = line0 + l, rr = q0 + r;
+                raw[l * kRawPitch + r] = (line < nlines && rr < R) ? src[line * ls + rr * rs] : (unsigned short)0;
+            }
         }
         __syncthreads();
     }
@@ -236,10 +231,17 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
         const int64_t L = line0 + l;
         uint32_t h[8];
         if (RCONTIG) {
+            const int64_t r0 = q0 + 8 * lane;
+            if (vec && L < nlines && r0 + 8 <= R) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + L * ls + r0));
+                h[0] = v.x & 0xffffu; h[1] = v.x >> 16; h[2] = v.y & 0xffffu; h[3] = v.y >> 16;
+                h[4] = v.z & 0xffffu; h[5] = v.z >> 16; h[6] = v.w & 0xffffu; h[7] = v.w >> 16;
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int64_t rr = q0 + 8 * lane + e;
-                h[e] = (L < nlines && rr < R) ? (uint32_t)__ldg(src + L * ls + rr) : 0u;
+                for (int e = 0; e < 8; ++e) {
+                    const int64_t rr = r0 + e;
+                    h[e] = (L < nlines && rr < R) ? (uint32_t)__ldg(src + L * ls + rr) : 0u;
+                }
             }
         } else {
             const uint4 v = *reinterpret_cast<const uint4 *>(&raw[l * kRawPitch + 8 * lane]);
@@ -281,6 +283,10 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
             if (width > 0 && width <= 62) atomicMin(&grain[L], base);
             if (use && cnt != nullptr) atomicMax(&cnt[(L / tg) * nchunks + q], n);
         }
+        // X = v * 256^a with v = m << (s % 8), a = s / 8 (s = e - base): two
+        // balanced digits, lo = v mod 256 in [-128, 127] at plane a and
+        // hi = (v - lo) / 256 (|hi| <= 128) at plane a + 1; hi is 0 when a is
+        // the line's top plane (then |v| < 2^(width % 8) <= 128)
         uint32_t packed[kPlanes][4];
 #pragma unroll
         for (int a = 0; a < kPlanes; ++a)
@@ -288,10 +294,14 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
             for (int w = 0; w < 4; ++w) packed[a][w] = 0u;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            int d[kPlanes];
-            split_digits(X[e], n, d);
+            const int sh = ex[e] - base;
+            const int v = (use && m[e] != 0) ? m[e] * (1 << (sh & 7)) : 0;    // |v| < 2^15
+            const int a = sh >> 3;
+            const int lo = ((v + 128) & 255) - 128;
+            const uint32_t blo = small_int_bf16(lo), bhi = small_int_bf16((v - lo) >> 8);
 #pragma unroll
-            for (int a = 0; a < kPlanes; ++a) packed[a][e / 2] |= small_int_bf16(d[a]) << (16 * (e & 1));
+            for (int p = 0; p < kPlanes; ++p)
+                packed[p][e / 2] |= (p == a ? blo : (p == a + 1 ? bhi : 0u)) << (16 * (e & 1));
         }
         const int64_t row = (L / tg) * kPlanes * tg + L % tg;
 #pragma unroll
@@ -303,10 +313,6 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
 
 // ---- main kernel ----------------------------------------------------------------
 
-// I += v * mul (mul = 256^c, c <= 3), 32 x 32 -> 64-bit.
-__device__ __forceinline__ void acc_lo(unsigned long long &I, uint32_t v, uint32_t mul) {
-    asm("mad.wide.u32 %0, %1, %2, %0;" : "+l"(I) : "r"(v), "r"(mul));
-}
 // I += v * mul * 2^32 modulo 2^64 (mul = 256^(c - 4), c >= 4).
 __device__ __forceinline__ void acc_hi(unsigned long long &I, uint32_t v, uint32_t mul) {
     asm("{\n\t.reg .u32 lo, hi;\n\t"
@@ -1040,8 +1046,10 @@ cudaError_t launch_prep(const unsigned short *src, int64_t ls, int64_t rs, int64
                         int64_t Lp, int64_t Rp, int tg, unsigned short *planes, int4 *stats,
                         int *grain, int *cnt, int nchunks, cudaStream_t s) {
     const dim3 grid((unsigned)(Lp / kPrepLines), (unsigned)nchunks);
+    const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+    const int vec = RCONTIG ? (aligned && ls % 8 == 0) : (aligned && ls == 1 && rs % 8 == 0);
     digit_prep_kernel<RCONTIG><<<grid, kPrepThreads, 0, s>>>(src, ls, rs, nlines, R, Lp, Rp, tg, planes,
-                                                             stats, grain, cnt, nchunks);
+                                                             stats, grain, cnt, nchunks, vec);
     count_launch();
     return cudaGetLastError();
 }
