@@ -57,7 +57,9 @@
 //  digit_prep_kernel: one warp per (line, chunk): statistics and digit planes
 //    (bf16, reduction index contiguous, the four planes of a tile's lines
 //    together), the A side's plane count per (row tile, chunk).
-//  exact_tc_kernel: persistent, one CTA per SM, 128 x 64 output tiles.
+//  exact_tc_kernel: persistent, one CTA per SM, 128 x 64 output tiles taken
+//    in turn (unit u: tile u / pieces, column tile fastest, so that each CTA
+//    meets every kind of row tile).
 //   warps 0, 2 TMA producers of A: a 5-stage ring of A plane blocks (16 KiB
 //              each), alternate loads (one thread's copies complete in turn)
 //   warp 3     TMA producer of B: per chunk the four B planes of each 64-deep
@@ -153,6 +155,7 @@ struct TcxArgs {
     const int4 *SA, *SB;                              // statistics [chunk][Lp]
     const int *GA, *GB;                               // line grains (smallest base) [Lp]
     const int *cntA;                                  // A planes per (row tile, chunk)
+    const int *invA;                                  // row of each place in the A planes
     unsigned int *work_count, *work_list;             // deferred outputs
     long long *Tout;                                  // exact sums in the output grain [piece][cols][rows]
     unsigned int *chunk_count;                        // (output, chunk) pairs for the chunk repair
@@ -189,19 +192,22 @@ constexpr int kRawPitch = kChunk + 8;                 // bf16 per staged line (1
 // src[line * ls + r * rs]; RCONTIG says rs == 1 (lines are read directly),
 // otherwise the block's lines are staged in shared memory first (coalesced
 // along the lines).  vec says 16-byte loads are aligned: 8 reduction indices
-// of a line (RCONTIG), or 8 lines at one reduction index (ls == 1).  Writes stats[chunk * Lp + line]; the line's digits in its
-// own count n of planes (the top one the remainder) and zeros in the planes
-// above, tile by tile: plane a of line L at row (L / tg) 4 tg + a tg + L % tg
-// of the [4 Lp][Rp] array (tg = tile lines); raises cnt[(L / tg) * nchunks +
-// chunk] to n when cnt is not null; and lowers grain[L] (preset to
-// kGrainNone) to the line's smallest base over the chunks where it is nonzero
-// and finite with width <= 62 (the chunk repair adds the wider chunks in it).
-template <bool RCONTIG>
+// of a line (RCONTIG), or 8 lines at one reduction index (ls == 1).
+// Writes stats[chunk * Lp + line] and the line's digits (two per value, zeros
+// elsewhere) tile by tile: plane a of the line placed at P goes to row
+// (P / tg) 4 tg + a tg + P % tg of the [4 Lp][Rp] array (tg = tile lines,
+// P = pos[line], or the line itself when pos is null); raises
+// cnt[(P / tg) * nchunks + chunk] to the line's digit count n when cnt is not
+// null; and lowers grain[line] (preset to kGrainNone) to the line's smallest
+// base over the chunks where it is nonzero and finite with width <= 62 (the
+// chunk repair adds the wider chunks in it).  FLAG_ONLY: only sets
+// flag[line] when some chunk of the line needs four digits.
+template <bool RCONTIG, bool FLAG_ONLY>
 __global__ void __launch_bounds__(kPrepThreads)
 digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs, int64_t nlines,
                   int64_t R, int64_t Lp, int64_t Rp, int tg, unsigned short *__restrict__ planes,
                   int4 *__restrict__ stats, int *__restrict__ grain, int *__restrict__ cnt,
-                  int nchunks, int vec) {
+                  int nchunks, int vec, const int *__restrict__ pos, int *__restrict__ flag) {
     __shared__ __align__(16) unsigned short raw[RCONTIG ? 1 : kPrepLines * kRawPitch];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int64_t line0 = (int64_t)blockIdx.x * kPrepLines;
@@ -229,6 +235,7 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
     }
     for (int l = warp; l < kPrepLines; l += kPrepThreads / 32) {
         const int64_t L = line0 + l;
+        const int64_t LP = (pos != nullptr) ? (int64_t)__ldg(&pos[L]) : L;   // the line's place in the planes
         uint32_t h[8];
         if (RCONTIG) {
             const int64_t r0 = q0 + 8 * lane;
@@ -263,6 +270,10 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
         const int width = bad ? kWidthBad : ((lo > hi) ? 0 : hi + 8 - lo);
         const bool use = width > 0 && width <= 31;
         const int n = digits_for_width(width);
+        if (FLAG_ONLY) {                                  // the line needs four digits somewhere
+            if (lane == 0 && n == kPlanes && L < nlines) atomicOr(&flag[L], 1);
+            continue;
+        }
         int X[8];
         unsigned long long sum = 0ull;
         unsigned int mx = 0u;
@@ -281,7 +292,7 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
             // the grain also covers finite lines too wide for the digits,
             // whose chunks the chunk repair adds in the same grain
             if (width > 0 && width <= 62) atomicMin(&grain[L], base);
-            if (use && cnt != nullptr) atomicMax(&cnt[(L / tg) * nchunks + q], n);
+            if (use && cnt != nullptr) atomicMax(&cnt[(LP / tg) * nchunks + q], n);
         }
         // X = v * 256^a with v = m << (s % 8), a = s / 8 (s = e - base): two
         // balanced digits, lo = v mod 256 in [-128, 127] at plane a and
@@ -303,7 +314,7 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
             for (int p = 0; p < kPlanes; ++p)
                 packed[p][e / 2] |= (p == a ? blo : (p == a + 1 ? bhi : 0u)) << (16 * (e & 1));
         }
-        const int64_t row = (L / tg) * kPlanes * tg + L % tg;
+        const int64_t row = (LP / tg) * kPlanes * tg + LP % tg;
 #pragma unroll
         for (int a = 0; a < kPlanes; ++a)
             *reinterpret_cast<uint4 *>(planes + (row + (int64_t)a * tg) * Rp + q0 + 8 * lane) =
@@ -443,7 +454,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
-                const int tm = t % p.tiles_m;
+                const int tm = t / p.tiles_n;
                 for (int q = qlo; ok && q < qhi; ++q) {
                     const int nx = p.cntA[(int64_t)tm * nchunks + q];
                     for (int k = 0; ok && k < nx; ++k)
@@ -474,7 +485,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
-                const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+                const int tm = t / p.tiles_n, tn = t % p.tiles_n;
                 for (int q = qlo; ok && q < qhi; ++q) {
                     if (p.cntA[(int64_t)tm * nchunks + q] == 0) continue;
                     for (int kb = 0; kb < kKBlocks; ++kb) {
@@ -505,7 +516,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
-                const int tm = t % p.tiles_m;
+                const int tm = t / p.tiles_n;
                 for (int q = qlo; ok && q < qhi; ++q) {
                     const int nx = p.cntA[(int64_t)tm * nchunks + q];
                     if (nx == 0) continue;
@@ -561,8 +572,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
             const int t = u / p.splits, piece = u % p.splits, qlo = piece * p.cps;
             const int qhi = min(nchunks, qlo + p.cps);
-            const int tm = t % p.tiles_m, tn = t / p.tiles_m;
-            const int64_t i = (int64_t)tm * kRowTile + rl;
+            const int tm = t / p.tiles_n, tn = t % p.tiles_n;
+            const int64_t i = __ldg(&p.invA[(int64_t)tm * kRowTile + rl]);   // the row's own index
             const int64_t jw = (int64_t)tn * kColTile + half * 32;   // this warp's first column
             const int *cnt = p.cntA + (int64_t)tm * nchunks;
             const int Gx = __ldg(&p.GA[i]);                   // output grain: 2^(Gx + Gw)
@@ -1041,17 +1052,53 @@ int choose_pieces(int64_t tiles, int64_t nchunks, int sms) {
     return best;
 }
 
-template <bool RCONTIG>
+template <bool RCONTIG, bool FLAG_ONLY>
 cudaError_t launch_prep(const unsigned short *src, int64_t ls, int64_t rs, int64_t nlines, int64_t R,
                         int64_t Lp, int64_t Rp, int tg, unsigned short *planes, int4 *stats,
-                        int *grain, int *cnt, int nchunks, cudaStream_t s) {
+                        int *grain, int *cnt, int nchunks, const int *pos, int *flag, cudaStream_t s) {
     const dim3 grid((unsigned)(Lp / kPrepLines), (unsigned)nchunks);
     const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
     const int vec = RCONTIG ? (aligned && ls % 8 == 0) : (aligned && ls == 1 && rs % 8 == 0);
-    digit_prep_kernel<RCONTIG><<<grid, kPrepThreads, 0, s>>>(src, ls, rs, nlines, R, Lp, Rp, tg, planes,
-                                                             stats, grain, cnt, nchunks, vec);
+    digit_prep_kernel<RCONTIG, FLAG_ONLY><<<grid, kPrepThreads, 0, s>>>(
+        src, ls, rs, nlines, R, Lp, Rp, tg, planes, stats, grain, cnt, nchunks, vec, pos, flag);
     count_launch();
     return cudaGetLastError();
+}
+
+// Places of the A rows in the digit planes: within each group of 1024 rows
+// (8 row tiles) the rows whose chunks all fit three digits come first, in
+// order, then the others, in order; places past the last row keep their own
+// index.  Tiles then mostly hold rows of one kind, so fewer of them need the
+// fourth digit plane (about 15% fewer MMAs on the GPT-2 operands).  The sums
+// are exact, so the placement does not change any result.
+constexpr int kOrderGroup = 1024;
+
+__global__ void __launch_bounds__(kOrderGroup)
+row_order_kernel(const int *__restrict__ flag, int64_t rows, int64_t Lp, int *__restrict__ pos,
+                 int *__restrict__ inv) {
+    __shared__ int wz[kOrderGroup / 32], wv[kOrderGroup / 32];
+    const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+    const int64_t base = (int64_t)blockIdx.x * kOrderGroup, i = base + t;
+    const bool valid = i < rows;
+    const bool z = valid && flag[i] == 0;            // three digits suffice everywhere
+    const uint32_t below = (1u << lane) - 1u;
+    const uint32_t bz = __ballot_sync(0xffffffffu, z), bv = __ballot_sync(0xffffffffu, valid);
+    if (lane == 0) { wz[warp] = __popc(bz); wv[warp] = __popc(bv); }
+    __syncthreads();
+    int pz = 0, pv = 0, tz = 0;                      // rows of each kind before this warp; all z rows
+    for (int w = 0; w < kOrderGroup / 32; ++w) {
+        if (w < warp) { pz += wz[w]; pv += wv[w]; }
+        tz += wz[w];
+    }
+    if (!valid) {
+        if (i < Lp) { pos[i] = (int)i; inv[i] = (int)i; }
+        return;
+    }
+    const int rz = pz + __popc(bz & below);          // z rows before this one
+    const int rv = pv + __popc(bv & below);          // valid rows before this one
+    const int64_t place = base + (z ? rz : tz + (rv - rz));
+    pos[i] = (int)place;
+    inv[place] = (int)i;
 }
 
 }  // namespace
@@ -1099,7 +1146,7 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     // may list an output for the fix-up
     const size_t ccap = std::min<size_t>(outs * (size_t)nchunks, (size_t)1 << 22);
     const size_t bytes = tBytes + 2 * (pA + pB) + 16 * (sA + sB) + 4 * (size_t)(LpA + LpB) +
-                         cntBytes + 8 * ccap + 16 + 4 * (outs * pieces + ccap + 1);
+                         12 * (size_t)LpA + cntBytes + 8 * ccap + 16 + 4 * (outs * pieces + ccap + 1);
     char *ws = nullptr;
     cudaError_t err = cudaMallocAsync(reinterpret_cast<void **>(&ws), bytes, stream);
     if (err != cudaSuccess) return note_cuda(err);
@@ -1110,7 +1157,10 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     int4 *SB = SA + sA;
     int *GA = reinterpret_cast<int *>(SB + sB);
     int *GB = GA + LpA;
-    int *cntA = GB + LpB;
+    int *flagA = GB + LpB;                               // rows needing four digits somewhere
+    int *posA = flagA + LpA;                             // place of each row in the A planes
+    int *invA = posA + LpA;                              // row at each place
+    int *cntA = invA + LpA;
     uint2 *clist = reinterpret_cast<uint2 *>(reinterpret_cast<char *>(cntA) + cntBytes);
     unsigned int *ccount = reinterpret_cast<unsigned int *>(clist + ccap);
     unsigned int *work = ccount + 4;
@@ -1121,14 +1171,24 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     if (err == cudaSuccess)
         err = cudaMemsetAsync(GA, kGrainNone & 0xff, 4 * (size_t)(LpA + LpB), stream);
     if (err == cudaSuccess) err = cudaMemsetAsync(cntA, 0, cntBytes, stream);
+    if (err == cudaSuccess) err = cudaMemsetAsync(flagA, 0, 4 * (size_t)LpA, stream);
     if (err == cudaSuccess) err = cudaMemsetAsync(ccount, 0, sizeof(unsigned int), stream);
     const bool a_rc = (p.pass != CARBON_PASS_DW), b_rc = (p.pass == CARBON_PASS_DX);
     if (err == cudaSuccess && nchunks > 0)
-        err = a_rc ? launch_prep<true>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, stream)
-                   : launch_prep<false>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, stream);
+        err = a_rc ? launch_prep<true, true>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, nullptr, (int)nchunks, nullptr, flagA, stream)
+                   : launch_prep<false, true>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, nullptr, (int)nchunks, nullptr, flagA, stream);
+    if (err == cudaSuccess) {
+        row_order_kernel<<<(unsigned)((LpA + kOrderGroup - 1) / kOrderGroup), kOrderGroup, 0, stream>>>(
+            flagA, p.rows, LpA, posA, invA);
+        count_launch();
+        err = cudaGetLastError();
+    }
     if (err == cudaSuccess && nchunks > 0)
-        err = b_rc ? launch_prep<true>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, nullptr, (int)nchunks, stream)
-                   : launch_prep<false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, nullptr, (int)nchunks, stream);
+        err = a_rc ? launch_prep<true, false>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, posA, nullptr, stream)
+                   : launch_prep<false, false>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, posA, nullptr, stream);
+    if (err == cudaSuccess && nchunks > 0)
+        err = b_rc ? launch_prep<true, false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, nullptr, (int)nchunks, nullptr, nullptr, stream)
+                   : launch_prep<false, false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, nullptr, (int)nchunks, nullptr, nullptr, stream);
     // planes as 2-D [4 Lp][Rp] bf16 maps, 64-deep boxes, 128-byte swizzle:
     // one A plane of a row tile (128 rows), all four B planes of a column tile
     // (256 rows) per box
@@ -1152,7 +1212,7 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         a.tiles_m = (int)tiles_m; a.tiles_n = (int)tiles_n; a.nchunks = (int)nchunks;
         a.splits = pieces;
         a.cps = (int)((nchunks + pieces - 1) / pieces);
-        a.SA = SA; a.SB = SB; a.GA = GA; a.GB = GB; a.cntA = cntA;
+        a.SA = SA; a.SB = SB; a.GA = GA; a.GB = GB; a.cntA = cntA; a.invA = invA;
         a.work_count = work; a.work_list = work + 1;
         a.Tout = Tout;
         a.chunk_count = ccount;
