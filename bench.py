@@ -435,8 +435,9 @@ def main():
                 fp64_rate, _ = cg.carbon_measure_fp64_rate(stream.cuda_stream)
             mac_rate = (fl_all / 2.0) / (ms * 1e-3)
             # the dominant kernel runs bf16 digit-plane MMAs on the tensor cores:
-            # one k-group = 16 tcgen05.mma of 128 x 256 x 16 = 2*128*256*256 flops
-            kg_flops = main_kg * 2.0 * 128 * 256 * 256
+            # one plane product = an A plane of 128 rows times a B plane of 64
+            # columns over a 256-deep chunk = 2*128*64*256 flops
+            kg_flops = main_kg * 2.0 * 128 * 64 * 256
             peak = float(pk["bf16_tflops"])
             achieved = kg_flops / (main_ms * 1e-3) / 1e12 if main_ms > 0 else 0.0
             rooflines["exact"] = {
@@ -444,7 +445,7 @@ def main():
                 "frac": _r(achieved / peak), "traffic": None, "kernel": "exact_tc_kernel",
                 "peak_kind": f"bf16 burst, of {pk_kind}",
                 "note": ("algorithmic work = the digit-pair MMAs the kernel issues (counted live: "
-                         f"{main_kg} k-groups of 2*128*256*256 flops in {main_n} launches), "
+                         f"{main_kg} plane products of 2*128*64*256 flops in {main_n} launches), "
                          "over the kernel's own CUDA-event time"),
                 "kernel_ms_per_step": _r(main_ms / args.steps),
                 "kernel_share_of_tier": _r(main_ms / ms) if ms > 0 else None,

@@ -208,7 +208,7 @@ def carbon_debug_kernel_timing(enable: bool) -> None:
 
 
 def carbon_debug_kernel_time():
-    """(milliseconds, launches, k-groups) recorded since timing was enabled."""
+    """(milliseconds, launches, plane products) recorded since timing was enabled."""
     ms, n, kg = ctypes.c_double(), ctypes.c_int64(), ctypes.c_int64()
     _check(lib.carbon_debug_kernel_time(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(kg)),
            "carbon_debug_kernel_time")

@@ -186,8 +186,8 @@ int64_t carbon_debug_launch_count(void) { return carbon::g_launches.load(); }
 
 void carbon_debug_kernel_timing(int enable) { carbon::exact_tc_timing(enable); }
 
-carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t *kgroups) {
-    return carbon::exact_tc_time(ms, launches, kgroups);
+carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t *plane_products) {
+    return carbon::exact_tc_time(ms, launches, plane_products);
 }
 
 carbon_status_t carbon_debug_exact_path_counts(int64_t *chunk_repairs, int64_t *fixups) {

@@ -5,10 +5,12 @@
 //
 // Statistics.  For a line (a row i of A or a column j of B) and a chunk of 256
 // reduction indices, the bf16 values are m * 2^e with |m| < 2^8; the line's
-// base is the smallest exponent e of a nonzero value and its integers are
-// X = m * 2^(e - base).  stats[chunk * Lp + line] = (base, width, bits of
-// sum |X|, bits of max |X|) with |X| < 2^width; width 0 for an all-zero line,
-// kWidthBad for a line holding inf or NaN.
+// base is an exponent of which every value is an integer multiple (the
+// integer-pipe kernel takes the smallest e of a nonzero value, the
+// tensor-core kernel the smallest e + tz, tz the trailing zero bits of m) and
+// its integers are X = m * 2^(e - base) (line_int).  stats[chunk * Lp + line] =
+// (base, width, bits of sum |X|, bits of max |X|) with |X| < 2^width; width 0
+// for an all-zero line, kWidthBad for a line holding inf or NaN.
 #pragma once
 
 #include "carbon_internal.h"
@@ -36,6 +38,14 @@ __device__ __forceinline__ void decode(uint32_t h, int &m, int &e, bool &bad) {
     m = (h & 0x8000u) ? -mag : mag;
     e = (e8 ? e8 : 1) - 134;
     bad = (e8 == 0xff);
+}
+
+// The integer X = m * 2^(e - base) of a value on its line's grid.  A line's
+// base may lie above e when m has trailing zero bits (m * 2^e is still a
+// multiple of 2^base), then the shift is a right shift that drops only zeros.
+__device__ __forceinline__ long long line_int(int m, int e, int base) {
+    const int d = e - base;
+    return d >= 0 ? (long long)m * (1ll << d) : (long long)(m >> -d);
 }
 
 __device__ __forceinline__ uint32_t ld_bits(const unsigned short *base, int64_t idx) {
@@ -156,8 +166,8 @@ exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__res
                         decode(hx[t], mx, ex, bx_);
                         decode(hw[t], mw, ew, bw_);
                         if (mx == 0 || mw == 0) continue;
-                        const long long X = (long long)mx * (1ll << (ex - sa.x));   // |X| < 2^62
-                        const long long W = (long long)mw * (1ll << (ew - sb.x));
+                        const long long X = line_int(mx, ex, sa.x);   // |X| < 2^62
+                        const long long W = line_int(mw, ew, sb.x);
                         I += (__int128)X * W;                                     // |X W| < 2^90
                     }
 #pragma unroll

@@ -37,12 +37,16 @@
 //    the starting values taken out by one constant), then one 64-bit
 //    multiply-add per combined pair; I is exact when the statistics bound
 //    |I| below 2^62.
-// A line of width w <= 31 needs ceil((w + 1) / 8) digits; a tile uses the most
-// any of its rows needs (A side, 1..4 planes per chunk) and always 4 planes on
-// the B side.  One tcgen05.mma of M = 128, N = 256, K = 16 multiplies one A
-// digit plane of 128 rows with all four B digit planes of 64 columns at once,
-// so one "k-group" (the four K=16 slices of each of four 64-deep blocks)
-// yields the pair sums of four digit pairs for a 128 x 64 output tile.
+// A line of width w <= 31 needs ceil((w + 1) / 8) digits (trailing zero bits
+// of the significands are moved into the exponents first, so the base is as
+// high as the values allow); a tile uses the most any of its lines needs in
+// the chunk, nx (1..4) A planes and nb (1..4) B planes.  One tcgen05.mma of
+// M = 128, N = 64 nb, K = 16 multiplies one A digit plane of 128 rows with the
+// nb B digit planes of 64 columns at once, so one "k-group" (the four K=16
+// slices of each of four 64-deep blocks) yields the pair sums of nb digit
+// pairs for a 128 x 64 output tile.  Rows that need four digits in some chunk
+// are placed after the others within groups of 1024 rows, so that most row
+// tiles get by with three.
 //
 // Outer sum.  The chunk values (I rounded to 53 significant bits when it is
 // larger) are added exactly in the integer grain 2^(Gx(i) + Gw(j)), the
@@ -56,7 +60,7 @@
 // Structure.
 //  digit_prep_kernel: one warp per (line, chunk): statistics and digit planes
 //    (bf16, reduction index contiguous, the four planes of a tile's lines
-//    together), the A side's plane count per (row tile, chunk).
+//    together), the plane count per (tile, chunk) of each side.
 //  exact_tc_kernel: persistent, one CTA per SM, 128 x 64 output tiles taken
 //    in turn (unit u: tile u / pieces, column tile fastest, so that each CTA
 //    meets every kind of row tile).
@@ -65,9 +69,10 @@
 //   warp 3     TMA producer of B: per chunk the four B planes of each 64-deep
 //              block (4 x 32 KiB, resident for the chunk)
 //   warp 1     MMA issuer: two accumulators of 256 TMEM columns used in turn,
-//              one per k-group, each k-group opened by one K = 16 MMA of two
-//              constant shared-memory tiles that sets the accumulator to
-//              1.5 * 2^23 (so the epilogue never writes tensor memory)
+//              one per k-group, each k-group opened by one K = 16, N = 256 MMA
+//              of two constant shared-memory tiles that sets the accumulator
+//              to 1.5 * 2^23 (so the epilogue never writes tensor memory, and
+//              the columns of B planes a chunk does not need read as 0)
 //   warps 4-11 epilogue: warp w reads lanes 32 (w % 4) .. +31 and 32 of the 64
 //              output columns; adds the pair sums into per-output int64 chunk
 //              sums and releases the accumulator; at each chunk end checks the
@@ -93,7 +98,7 @@ namespace carbon {
 namespace {
 
 __device__ unsigned int g_exact_tc_status = 0;
-__device__ unsigned long long g_exact_tc_kgroups = 0;   // k-groups issued (measurement)
+__device__ unsigned long long g_exact_tc_kgroups = 0;   // plane products issued (measurement)
 __device__ unsigned long long g_exact_tc_repairs = 0;   // chunk repairs and fix-ups (measurement)
 __device__ unsigned long long g_exact_tc_fixups = 0;
 
@@ -146,6 +151,8 @@ struct __align__(1024) TcxSmem {
     uint32_t tmem_slot, abort;
 };
 
+static_assert(sizeof(TcxSmem) + 1024 <= 232448, "shared memory per block");
+
 struct TcxArgs {
     const unsigned short *bias;                       // bf16 [cols] or null
     void *out;
@@ -156,6 +163,7 @@ struct TcxArgs {
     const int *GA, *GB;                               // line grains (smallest base) [Lp]
     const int *cntA;                                  // A planes per (row tile, chunk)
     const int *invA;                                  // row of each place in the A planes
+    const int *cntB;                                  // B planes per (column tile, chunk)
     unsigned int *work_count, *work_list;             // deferred outputs
     long long *Tout;                                  // exact sums in the output grain [piece][cols][rows]
     unsigned int *chunk_count;                        // (output, chunk) pairs for the chunk repair
@@ -255,19 +263,29 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
             h[0] = v.x & 0xffffu; h[1] = v.x >> 16; h[2] = v.y & 0xffffu; h[3] = v.y >> 16;
             h[4] = v.z & 0xffffu; h[5] = v.z >> 16; h[6] = v.w & 0xffffu; h[7] = v.w >> 16;
         }
+        // values m * 2^e with the trailing zero bits of m moved into e, so the
+        // base (the smallest such e) is as high as the values allow; the
+        // width bound keeps the unstripped exponent (|m| < 2^8 there)
         int m[8], ex[8], lo = 1 << 20, hi = -(1 << 20), bad = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             bool b;
             decode(h[e], m[e], ex[e], b);
-            if (m[e] != 0) { lo = min(lo, ex[e]); hi = max(hi, ex[e]); }
+            if (m[e] != 0) {
+                hi = max(hi, ex[e]);
+                const int tz = __ffs(m[e]) - 1;
+                m[e] >>= tz;                                  // exact: m is a multiple of 2^tz
+                ex[e] += tz;
+                lo = min(lo, ex[e]);
+            }
             bad |= (int)b;
         }
         lo = __reduce_min_sync(0xffffffffu, lo);
         hi = __reduce_max_sync(0xffffffffu, hi);
         bad = (int)__reduce_or_sync(0xffffffffu, (unsigned)bad);
-        const int base = (lo > hi) ? 0 : lo;
-        const int width = bad ? kWidthBad : ((lo > hi) ? 0 : hi + 8 - lo);
+        const bool zero = hi == -(1 << 20);                   // no nonzero value
+        const int base = zero ? 0 : lo;
+        const int width = bad ? kWidthBad : (zero ? 0 : hi + 8 - lo);
         const bool use = width > 0 && width <= 31;
         const int n = digits_for_width(width);
         if (FLAG_ONLY) {                                  // the line needs four digits somewhere
@@ -505,8 +523,12 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                                       ((uint32_t)(kMmaN >> 3) << 17) | ((uint32_t)(kRowTile >> 4) << 24);
+            // instruction descriptor: fp32 accumulate, bf16 A and B, both
+            // K-major, M = 128; N = 256 for the start MMA, 64 per B plane the
+            // column tile needs in the chunk for the others (the columns past
+            // them keep the start value, a pair sum of 0)
+            constexpr uint32_t idesc0 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kRowTile >> 4) << 24);
+            constexpr uint32_t idesc = idesc0 | ((uint32_t)(kMmaN >> 3) << 17);
             const uint64_t sdesc_a0 = smem_desc_noswizzle(smem_addr(&sm.SA0[0]), 128, 256);
             const uint64_t sdesc_b0 = smem_desc_noswizzle(smem_addr(&sm.SB0[0]), 128, 256);
             int s = 0, acc = 0;
@@ -516,10 +538,12 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
-                const int tm = t / p.tiles_n;
+                const int tm = t / p.tiles_n, tn = t % p.tiles_n;
                 for (int q = qlo; ok && q < qhi; ++q) {
                     const int nx = p.cntA[(int64_t)tm * nchunks + q];
                     if (nx == 0) continue;
+                    const int nb = max(1, p.cntB[(int64_t)tn * nchunks + q]);
+                    const uint32_t idesc_q = idesc0 | ((uint32_t)(kColTile * nb >> 3) << 17);
                     for (int k = 0; ok && k < nx; ++k) {
                         if (!(ok = wait_or_abort(smem_addr(&sm.tempty[acc]), aph, abort_flag))) break;
                         tc_fence_after();
@@ -533,14 +557,14 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
 #pragma unroll
                             for (int kk = 0; kk < kKBlock / kUmmaK; ++kk)
                                 mma_bf16(d, smem_desc(sa + kk * (kUmmaK * 2), 16, 1024),
-                                         smem_desc(sb + kk * (kUmmaK * 2), 16, 1024), idesc, 1u);
+                                         smem_desc(sb + kk * (kUmmaK * 2), 16, 1024), idesc_q, 1u);
                             mma_commit(smem_addr(&sm.aempty[s]));
                             if (k == nx - 1) mma_commit(smem_addr(&sm.bempty[kb]));
                             if (++s == kAStages) { s = 0; ph ^= 1u; }
                         }
                         if (!ok) break;
                         mma_commit(smem_addr(&sm.tfull[acc]));          // k-group done
-                        ++kgroups;
+                        kgroups += (unsigned long long)nb;              // A plane x nb B planes
                         if (++acc == 2) { acc = 0; aph ^= 1u; }
                     }
                     ++bu;
@@ -579,7 +603,6 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             const int Gx = __ldg(&p.GA[i]);                   // output grain: 2^(Gx + Gw)
             const int Gwl = __ldg(&p.GB[jw + lane]);
             __syncwarp();                                    // last tile's reads are done
-            __syncwarp();
             // I, the chunk sum, starts at 0 (each plane pair's starting values
             // are taken out as it is added); T, the exact sum, too
             int nx = qlo < qhi ? cnt[qlo] : 0;
@@ -596,14 +619,16 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             }
 
             for (int q = qlo; ok && q < qhi; ++q) {
+                const int nx_next = (q + 1 < qhi) ? cnt[q + 1] : 0;   // loaded a chunk ahead
                 for (int k = 0; k < nx; ++k) {
                     if (!(ok = wait_or_abort(smem_addr(&sm.tfull[acc]), aph, abort_flag))) break;
                     tc_fence_after();
                     const uint32_t ta = tlane + (uint32_t)(acc * kMmaN);
                     // 8 units: planes (2 pp, 2 pp + 1) of 8 columns (group g), two
                     // 8-column loads each, issued before the previous unit's values
-                    // are added in.  The two planes' sums combine exactly in 32 bits
-                    // (|u_a + 256 u_b| < 2^31), on the integer ALUs, before one
+                    // are added in (planes past the chunk's nb hold the start value,
+                    // a pair sum of 0).  The two planes' sums combine exactly in 32
+                    // bits (|u_a + 256 u_b| < 2^31), on the integer ALUs, before one
                     // 64-bit multiply-add per pair.
                     uint32_t va[16], vb[16];
                     tmem_ld8x2_issue(ta, ta + (uint32_t)kColTile, va);
@@ -742,7 +767,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         T[jj] = bad ? 0ull : T[jj];
                     }
                 }
-                nx = (q + 1 < qhi) ? cnt[q + 1] : 0;
+                nx = nx_next;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) I[c] = 0ull;
             }
@@ -824,8 +849,8 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
             decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bx_);
             decode(ld_bits(p.B, r * p.b_sr + j * p.b_sj), mw, ew, bw_);
             if (mx == 0 || mw == 0) continue;
-            const long long X = (long long)mx * (1ll << (ex - sa.x));           // |X| < 2^62
-            const long long W = (long long)mw * (1ll << (ew - sb.x));
+            const long long X = line_int(mx, ex, sa.x);                       // |X| < 2^62
+            const long long W = line_int(mw, ew, sb.x);
             I += (__int128)X * W;                                             // |X W| < 2^90
         }
 #pragma unroll
@@ -1137,7 +1162,7 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     // planes of A and B, statistics, A plane counts, the deferral counter and list
     const size_t pA = (size_t)kPlanes * LpA * Rp, pB = (size_t)kPlanes * LpB * Rp;
     const size_t sA = (size_t)nchunks * LpA, sB = (size_t)nchunks * LpB;
-    const size_t cntBytes = ((4 * (size_t)tiles_m * nchunks) + 15) & ~(size_t)15;
+    const size_t cntBytes = ((4 * (size_t)(tiles_m + tiles_n) * nchunks) + 15) & ~(size_t)15;
     const int pieces = choose_pieces(tiles_m * tiles_n, nchunks, sms);
     const size_t outs = (size_t)p.rows * (size_t)p.cols;
     const size_t tBytes = (8 * outs * pieces + 255) & ~(size_t)255;   // keeps the planes aligned
@@ -1160,7 +1185,8 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     int *flagA = GB + LpB;                               // rows needing four digits somewhere
     int *posA = flagA + LpA;                             // place of each row in the A planes
     int *invA = posA + LpA;                              // row at each place
-    int *cntA = invA + LpA;
+    int *cntA = invA + LpA;                              // planes per (row tile, chunk)
+    int *cntB = cntA + tiles_m * nchunks;                // planes per (column tile, chunk)
     uint2 *clist = reinterpret_cast<uint2 *>(reinterpret_cast<char *>(cntA) + cntBytes);
     unsigned int *ccount = reinterpret_cast<unsigned int *>(clist + ccap);
     unsigned int *work = ccount + 4;
@@ -1187,8 +1213,8 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         err = a_rc ? launch_prep<true, false>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, posA, nullptr, stream)
                    : launch_prep<false, false>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, posA, nullptr, stream);
     if (err == cudaSuccess && nchunks > 0)
-        err = b_rc ? launch_prep<true, false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, nullptr, (int)nchunks, nullptr, nullptr, stream)
-                   : launch_prep<false, false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, nullptr, (int)nchunks, nullptr, nullptr, stream);
+        err = b_rc ? launch_prep<true, false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, cntB, (int)nchunks, nullptr, nullptr, stream)
+                   : launch_prep<false, false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, cntB, (int)nchunks, nullptr, nullptr, stream);
     // planes as 2-D [4 Lp][Rp] bf16 maps, 64-deep boxes, 128-byte swizzle:
     // one A plane of a row tile (128 rows), all four B planes of a column tile
     // (256 rows) per box
@@ -1213,6 +1239,7 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         a.splits = pieces;
         a.cps = (int)((nchunks + pieces - 1) / pieces);
         a.SA = SA; a.SB = SB; a.GA = GA; a.GB = GB; a.cntA = cntA; a.invA = invA;
+        a.cntB = cntB;
         a.work_count = work; a.work_list = work + 1;
         a.Tout = Tout;
         a.chunk_count = ccount;

@@ -62,16 +62,18 @@ carbon_status_t carbon_measure_int_mac_rate(double *macs_per_s, carbon_stream_t 
 /* Timing of the bf16 exact tier's tensor-core kernel.  enable != 0 starts
  * recording a CUDA event pair on the caller's stream around every launch of
  * that kernel (outside CUDA-graph capture only) and clears the previous
- * record; enable == 0 stops recording.  The kernel also counts the
- * "k-groups" it issues: one k-group is 16 tcgen05.mma instructions of
- * M = 128, N = 256, K = 16 (one A digit plane against four B digit planes of
- * one 256-deep chunk), 2 * 128 * 256 * 256 flops. */
+ * record; enable == 0 stops recording.  The kernel also counts the digit
+ * plane products it issues: one unit is one A digit plane of 128 rows times
+ * one B digit plane of 64 columns over a 256-deep chunk (the share of one
+ * plane in 16 tcgen05.mma instructions of M = 128, K = 16 and N = 64 per B
+ * plane), 2 * 128 * 64 * 256 flops.  The accumulators' start MMAs are not
+ * counted. */
 void carbon_debug_kernel_timing(int enable);
 
 /* Sum of the recorded launches' durations in milliseconds (blocking: waits
- * for the recorded events), their number, and the k-groups issued since the
- * last carbon_debug_kernel_timing(1).  Any pointer may be NULL. */
-carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t *kgroups);
+ * for the recorded events), their number, and the plane products issued
+ * since the last carbon_debug_kernel_timing(1).  Any pointer may be NULL. */
+carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t *plane_products);
 
 /* While kernel timing is on, the bf16 exact tier also counts, per call, the
  * (output, chunk) pairs it recomputes in the chunk repair (a line of that

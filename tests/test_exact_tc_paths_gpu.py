@@ -186,3 +186,55 @@ def test_gpt2_shape_tail_and_zero_lines(pass_):
     ops = {"fwd": (bf16(X), bf16(W), L["b"]), "dx": (bf16(dY), bf16(W), None),
            "dw": (bf16(X), bf16(dY), None)}[pass_]
     check(pass_, *ops, M, K, N)
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dx", "dw"])
+def test_plane_counts_per_tile_and_trailing_zeros(pass_):
+    """Operand lines of every digit count: the B side's lines (columns of W,
+    rows of W for dX, columns of dY for dW) come in groups of 64, each group
+    of a different width, so the column tiles of one chunk need 1, 2, 3 and 4
+    digit planes (the tensor-core kernel then runs MMAs of
+    N = 64, 128, 192 and 256); the A side mixes the same spans by row.  Half
+    of the values have significands with trailing zero bits (a line's base
+    sits above its smallest exponent), and one chunk of every B line is all
+    zero, or holds a single power of two."""
+    rng = np.random.default_rng(31)
+    M, K, N = 260, 580, 264            # 3 chunks (the last one short), ragged tiles
+
+    def lines(n, length, seed_off):
+        r = np.random.default_rng(100 + seed_off)
+        v = np.empty((n, length))
+        for li in range(n):
+            kind = (li // 64) % 4                # line width about 6, 12, 20, 28 bits
+            e0 = int(r.integers(-20, 4))
+            if kind == 0:                        # integers below 2^6 times 2^e0: one digit
+                v[li] = np.ldexp(r.integers(-63, 64, length).astype(np.float64), e0)
+            else:                                # 8 + 8 (kind - 1) + 3 bits: kind + 1 digits
+                v[li] = spread(r, length, e0 - (8 * kind - 5), e0)
+            coarse = (r.random(length) < 0.5) & (v[li] != 0)   # 4-bit significands
+            a = np.abs(v[li, coarse])
+            ex = np.floor(np.log2(a)).astype(np.int64)
+            v[li, coarse] = np.sign(v[li, coarse]) * np.ldexp(np.round(np.ldexp(a, 3 - ex)), ex - 3)
+            q = int(r.integers(0, (length + 255) // 256))
+            lo, hi = 256 * q, min(length, 256 * q + 256)
+            if li % 3 == 0:
+                v[li, lo:hi] = 0.0
+            elif li % 3 == 1:
+                v[li, lo:hi] = 0.0
+                v[li, lo + int(r.integers(0, hi - lo))] = np.ldexp(1.0, int(r.integers(-30, 10)))
+        return v
+
+    if pass_ == "fwd":
+        X = bf16(lines(M, K, 0))
+        W = bf16(lines(N, K, 1).T)
+        b = bf16(rng.standard_normal(N))
+        check("fwd", X, W, b, M, K, N)
+    elif pass_ == "dx":
+        dY = bf16(lines(M, N, 2))
+        W = bf16(lines(K, N, 3))           # rows of W are the B lines of dX
+        check("dx", dY, W, None, M, K, N)
+    else:
+        Mt, Kd, Nd = 600, 200, 264         # dW: reduction over 600 tokens
+        X = bf16(lines(Kd, Mt, 4).T)
+        dY = bf16(lines(Nd, Mt, 5).T)
+        check("dw", X, dY, None, Mt, Kd, Nd)
