@@ -629,28 +629,49 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     // are added in (planes past the chunk's nb hold the start value,
                     // a pair sum of 0).  The two planes' sums combine exactly in 32
                     // bits (|u_a + 256 u_b| < 2^31), on the integer ALUs, before one
-                    // 64-bit multiply-add per pair.
+                    // 64-bit multiply-add per pair.  Planes (0, 1) of every group
+                    // first (weight 256^k, k <= 3), then planes (2, 3) (weight
+                    // 256^(k+2)), whose two forms are chosen once per k-group.
                     uint32_t va[16], vb[16];
                     tmem_ld8x2_issue(ta, ta + (uint32_t)kColTile, va);
+                    const uint32_t mul0 = 1u << (8 * k);
 #pragma unroll
-                    for (int un = 0; un < 8; ++un) {
-                        const int pp = un & 1, g = un >> 1;
-                        uint32_t(&cur)[16] = (un & 1) ? vb : va;
-                        uint32_t(&nxt)[16] = (un & 1) ? va : vb;
+                    for (int g = 0; g < 4; ++g) {
+                        uint32_t(&cur)[16] = (g & 1) ? vb : va;
+                        uint32_t(&nxt)[16] = (g & 1) ? va : vb;
                         tmem_wait_ld16(cur);
-                        if (un + 1 < 8) {
-                            const int pn = (un + 1) & 1, gn = (un + 1) >> 1;
-                            const uint32_t an = ta + (uint32_t)(2 * pn * kColTile + 8 * gn);
-                            tmem_ld8x2_issue(an, an + (uint32_t)kColTile, nxt);
-                        }
-                        const int c = k + 2 * pp;            // weight 256^c of plane 2 pp
-                        if (c <= 3) {
-                            const uint32_t mul = 1u << (8 * c);
+                        const uint32_t an = g < 3 ? ta + (uint32_t)(8 * (g + 1)) : ta + (uint32_t)(2 * kColTile);
+                        tmem_ld8x2_issue(an, an + (uint32_t)kColTile, nxt);
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj)
+                            acc_pair_lo(I[8 * g + jj], (cur[8 + jj] << 8) + cur[jj] + kPairFix, mul0);
+                    }
+                    if (k <= 1) {
+                        const uint32_t mul = 1u << (8 * (k + 2));
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            uint32_t(&cur)[16] = (g & 1) ? vb : va;
+                            uint32_t(&nxt)[16] = (g & 1) ? va : vb;
+                            tmem_wait_ld16(cur);
+                            if (g < 3) {
+                                const uint32_t an = ta + (uint32_t)(2 * kColTile + 8 * (g + 1));
+                                tmem_ld8x2_issue(an, an + (uint32_t)kColTile, nxt);
+                            }
 #pragma unroll
                             for (int jj = 0; jj < 8; ++jj)
                                 acc_pair_lo(I[8 * g + jj], (cur[8 + jj] << 8) + cur[jj] + kPairFix, mul);
-                        } else {
-                            const uint32_t mul = 1u << (8 * (c - 4));
+                        }
+                    } else {
+                        const uint32_t mul = 1u << (8 * (k - 2));
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            uint32_t(&cur)[16] = (g & 1) ? vb : va;
+                            uint32_t(&nxt)[16] = (g & 1) ? va : vb;
+                            tmem_wait_ld16(cur);
+                            if (g < 3) {
+                                const uint32_t an = ta + (uint32_t)(2 * kColTile + 8 * (g + 1));
+                                tmem_ld8x2_issue(an, an + (uint32_t)kColTile, nxt);
+                            }
 #pragma unroll
                             for (int jj = 0; jj < 8; ++jj)
                                 acc_hi(I[8 * g + jj], (cur[8 + jj] << 8) + cur[jj] + kPairFix, mul);
