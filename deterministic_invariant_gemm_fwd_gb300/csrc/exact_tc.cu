@@ -117,6 +117,8 @@ constexpr int kUmmaK = 16;
 constexpr int kAStages = 5;
 constexpr int kEpiWarps = 8;
 constexpr int kTcxThreads = 384;                      // warpgroup 0: TMA + MMA; 1-2: epilogue
+constexpr int kUnitSlots = 4;                         // work units handed from the B producer to the others
+constexpr int kUnitReaders = 2 + 1 + kEpiWarps;       // A producers, MMA issuer, epilogue warps
 // Register split (setmaxnreg): the block is launched at kLaunchRegs per
 // thread; warpgroup 0 gives registers back, warpgroups 1-2 take them:
 // 128 * kRegsLow + 256 * kRegsHigh must not exceed 384 * kLaunchRegs.
@@ -148,6 +150,8 @@ struct __align__(1024) TcxSmem {
     uint32_t pk[kEpiWarps][32];                       // packed column words of the current chunk
     uint64_t afull[kAStages], aempty[kAStages], bfull[kKBlocks], bempty[kKBlocks];
     uint64_t tfull[2], tempty[2], mdone;
+    uint64_t ufull[kUnitSlots], uempty[kUnitSlots];
+    int unit_q[kUnitSlots];                           // work unit in each slot (-1: no more)
     uint32_t tmem_slot, abort;
 };
 
@@ -169,6 +173,7 @@ struct TcxArgs {
     unsigned int *chunk_count;                        // (output, chunk) pairs for the chunk repair
     uint2 *chunk_list;
     unsigned int chunk_cap;
+    unsigned int *unit_counter;                       // next work unit (starts at 0)
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -177,6 +182,33 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     *flag = 1u;
     atomicExch(&g_exact_tc_status, (unsigned)CARBON_ERR_TIMEOUT);
     return false;
+}
+
+// Work units are handed out at run time: the B producer takes the next one
+// from the launch's counter when it is ready for it and posts it in slot
+// n % kUnitSlots (-1 once all are taken); the other roles read the slots in
+// the same order, so every role of a CTA works through the same units.  A
+// reader frees its slot as soon as it has read it.
+__device__ __forceinline__ bool fetch_unit(TcxSmem &sm, uint32_t n, unsigned int *counter, int nunits,
+                                           volatile uint32_t *flag, int &u) {
+    const uint32_t slot = n % kUnitSlots, use = n / kUnitSlots;
+    if (!wait_or_abort(smem_addr(&sm.uempty[slot]), (use & 1u) ^ 1u, flag)) return false;
+    const unsigned int v = atomicAdd(counter, 1u);
+    u = v < (unsigned int)nunits ? (int)v : -1;
+    sm.unit_q[slot] = u;
+    mbar_arrive(smem_addr(&sm.ufull[slot]));              // release: the slot's value is visible
+    return true;
+}
+
+__device__ __forceinline__ bool read_unit(TcxSmem &sm, uint32_t n, volatile uint32_t *flag, int &u) {
+    const uint32_t slot = n % kUnitSlots, use = n / kUnitSlots;
+    if (!wait_or_abort(smem_addr(&sm.ufull[slot]), use & 1u, flag)) return false;
+    u = *reinterpret_cast<volatile int *>(&sm.unit_q[slot]);
+    return true;
+}
+
+__device__ __forceinline__ void free_unit_slot(TcxSmem &sm, uint32_t n) {
+    mbar_arrive(smem_addr(&sm.uempty[n % kUnitSlots]));
 }
 
 // ---- pre-pass: statistics and digit planes ------------------------------------
@@ -400,6 +432,19 @@ __device__ __noinline__ uint32_t out_bits_f64(long long T, int G, const unsigned
     return exact_round_bf16(y);
 }
 
+// v * 2^sh as a 64-bit two's complement pattern (the shift of the bits, which
+// signed arithmetic leaves undefined for negative v or a result out of range;
+// the callers check the range themselves).
+__device__ __forceinline__ long long shl64(long long v, uint32_t sh) {
+    return (long long)((unsigned long long)v << (sh & 63u));
+}
+
+// -2^k <= v < 2^k for a signed 64-bit v (0 < k < 63), tested in unsigned
+// arithmetic so that no addition can overflow.
+__device__ __forceinline__ bool below_pow2(long long v, int k) {
+    return (unsigned long long)v + (1ull << k) < (2ull << k);
+}
+
 // I rounded to 53 significant bits, ties to even (|I| > 2^53 - 1, |I| < 2^63).
 __device__ __forceinline__ long long round_to_53_bits(long long I) {
     const bool neg = I < 0;
@@ -436,6 +481,10 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             mbar_init(smem_addr(&sm.tempty[b]), kEpiWarps);
         }
         mbar_init(smem_addr(&sm.mdone), 1);
+        for (int u = 0; u < kUnitSlots; ++u) {
+            mbar_init(smem_addr(&sm.ufull[u]), 1);
+            mbar_init(smem_addr(&sm.uempty[u]), kUnitReaders);
+        }
         *abort_flag = 0u;
         fence_mbar_init();
         if (p.nchunks > 0) {                                // maps are blank for an empty reduction
@@ -467,9 +516,13 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         // so two threads double the rate).
         if (lane == 0) {
             const uint32_t mine = warp == 0 ? 0u : 1u;
-            uint32_t g = 0;
+            uint32_t g = 0, n = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
+            while (ok) {
+                int u;
+                if (!(ok = read_unit(sm, n, abort_flag, u))) break;
+                free_unit_slot(sm, n++);
+                if (u < 0 || *abort_flag) break;
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
                 const int tm = t / p.tiles_n;
@@ -498,9 +551,12 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         // ------------------------------------------------------------ B producer
         // per chunk the four planes of each 64-deep block, 256 rows in one box
         if (lane == 0) {
-            uint32_t bu = 0;
+            uint32_t bu = 0, n = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
+            while (ok) {
+                int u;
+                if (!(ok = fetch_unit(sm, n++, p.unit_counter, nunits, abort_flag, u))) break;
+                if (u < 0 || *abort_flag) break;
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
                 const int tm = t / p.tiles_n, tn = t % p.tiles_n;
@@ -534,8 +590,13 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             int s = 0, acc = 0;
             uint32_t ph = 0, bu = 0, aph = 0;
             unsigned long long kgroups = 0;
+            uint32_t n = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
+            while (ok) {
+                int u;
+                if (!(ok = read_unit(sm, n, abort_flag, u))) break;
+                free_unit_slot(sm, n++);
+                if (u < 0 || *abort_flag) break;
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
                 const int tm = t / p.tiles_n, tn = t % p.tiles_n;
@@ -591,9 +652,22 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             mbar_arrive(smem_addr(&sm.tempty[1]));
         }
         int acc = 0;
-        uint32_t aph = 0;
+        uint32_t aph = 0, n = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < nunits && !*abort_flag; u += gridDim.x) {
+        while (ok) {
+            // lane 0 reads the unit and the warp follows its view, so that the
+            // warp never splits here
+            int u = -1, got = 0;
+            if (lane == 0) {
+                got = read_unit(sm, n, abort_flag, u) ? 1 : 0;
+                if (got) free_unit_slot(sm, n);
+                got |= (got && u >= 0 && !*abort_flag) ? 2 : 0;
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            ++n;
+            if (!(ok = (got & 1) != 0)) break;
+            if (!(got & 2)) break;
             const int t = u / p.splits, piece = u % p.splits, qlo = piece * p.cps;
             const int qhi = min(nchunks, qlo + p.cps);
             const int tm = t / p.tiles_n, tn = t % p.tiles_n;
@@ -722,7 +796,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     for (int jj = 0; jj < 32; ++jj) {
                         const uint32_t sh = (uint32_t)shr + (sm.pk[ew][jj] & 0xffu);
                         const long long Ij = (long long)I[jj];
-                        const long long v = Ij << (sh & 63u);
+                        const long long v = shl64(Ij, sh);
                         const long long back = (v >> (sh & 63u)) ^ Ij;
                         lost |= (uint32_t)back | (uint32_t)(back >> 32);
                         shs |= sh;
@@ -749,10 +823,11 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                             // this output's own checks: keep the addition when they pass
                             const uint32_t sh = (uint32_t)shr + (sm.pk[ew][jj] & 0xffu);
                             const long long I0 = (long long)I[jj];
-                            const long long v = I0 << (sh & 63u);
-                            const int ih = (int)(I0 >> 32), t = (int)(T[jj] >> 32);
-                            if ((v >> (sh & 63u)) == I0 && sh < 64u && (uint32_t)(ih + (1 << 21)) < (1u << 22) &&
-                                (uint32_t)(t + (1 << 30)) < (1u << 31))
+                            const long long v = shl64(I0, sh);
+                            // |I| < 2^53 and |T| < 2^62, tested in unsigned arithmetic
+                            // (T may have wrapped: a signed test could overflow)
+                            if ((v >> (sh & 63u)) == I0 && sh < 64u && below_pow2(I0, 53) &&
+                                below_pow2((long long)T[jj], 62))
                                 continue;
                             T[jj] -= (unsigned long long)v;
                         }
@@ -762,14 +837,13 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         const int bnd = min(min(lsx + (int)((w >> 21) & 0x3fu), lmx + (int)((w >> 15) & 0x3fu)),
                                             wx + ww + 8);                   // |I| < 2^bnd
                         const bool fits = wx <= 31 && ww <= 31 && bnd <= 62;
-                        if (bnd > 53 && (unsigned long long)(Ij + (1ll << 53)) >= (1ull << 54))
+                        if (bnd > 53 && !below_pow2(Ij, 53))
                             Ij = round_to_53_bits(Ij);                      // |result| <= 2^bnd
                         const int sh = shr + (int)(w & 0xffu);
-                        const long long Tn = (long long)T[jj] + (Ij << (sh & 63));
+                        const long long Tn = (long long)(T[jj] + (unsigned long long)shl64(Ij, (uint32_t)sh));
                         const int ib = 64 - __clzll(Ij ^ (Ij >> 63));          // |Ij| <= 2^ib
                         // no bit of I << sh lost, and the running sum stays below 2^62
-                        const bool ok_add = ib + sh <= 61 &&
-                                            (unsigned long long)(Tn + (1ll << 62)) < (1ull << 63);
+                        const bool ok_add = ib + sh <= 61 && below_pow2(Tn, 62);
                         // a zero line (wx or ww 0) adds +0, which changes nothing
                         const bool live = fits && !(defer & bit) && wx != 0 && ww != 0;
                         T[jj] = (live && ok_add) ? (unsigned long long)Tn : T[jj];
@@ -886,7 +960,7 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
         bool ok = sh >= 0 && sh < 62;
         __int128 v = 0;
         if (ok) {
-            v = J << sh;
+            v = (__int128)((unsigned __int128)J << sh);
             ok = (v >> sh) == J && v >= -((__int128)1 << 61) && v < ((__int128)1 << 61);
         }
         if (ok) {
@@ -957,15 +1031,17 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
                 int bm = 0, be = 0;
                 bool bad = false;
                 decode(hb[e], bm, be, bad);
-                const bool t53 = (unsigned long long)(T + (1ll << 53)) < (1ull << 54);   // |T| < 2^53
+                const bool t53 = below_pow2(T, 53);
                 long long Tv = T;
                 int gs = G;
                 bool fused = !bad;
                 if (bm != 0) {
-                    if (be >= G && be - G <= 54) {
-                        Tv = (t53 ? T : round_to_53_bits(T)) + ((long long)bm << (be - G));
+                    // the exact sum stays below 2^63: |T| < 2^61 and the bias
+                    // term below 2^62, or |T| < 2^53 shifted by at most 9
+                    if (be >= G && be - G <= 54 && below_pow2(T, 61)) {
+                        Tv = (t53 ? T : round_to_53_bits(T)) + shl64(bm, (uint32_t)(be - G));
                     } else if (be < G && G - be <= 9 && t53) {
-                        Tv = (T << (G - be)) + bm;
+                        Tv = shl64(T, (uint32_t)(G - be)) + bm;
                         gs = be;
                     } else {
                         fused = false;
@@ -1006,11 +1082,11 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             int gs = G;
             bool fused = !bad;
             if (fused && bm != 0) {
-                if ((unsigned long long)(Tv ^ (Tv >> 63)) >> 53) Tv = round_to_53_bits(Tv);
-                if (be >= G && be - G <= 54) {
-                    Tv += (long long)bm << (be - G);
-                } else if (be < G && G - be <= 9 && (unsigned long long)(Tv + (1ll << 53)) < (1ull << 54)) {
-                    Tv = (Tv << (G - be)) + bm;
+                if (be >= G && be - G <= 54 && below_pow2(Tv, 61)) {
+                    if (!below_pow2(Tv, 53)) Tv = round_to_53_bits(Tv);
+                    Tv += shl64(bm, (uint32_t)(be - G));
+                } else if (be < G && G - be <= 9 && below_pow2(Tv, 53)) {
+                    Tv = shl64(Tv, (uint32_t)(G - be)) + bm;
                     gs = be;
                 } else {
                     fused = false;
@@ -1083,19 +1159,15 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
     return cudaGetLastError();
 }
 
-// Pieces the chunk range of each output tile is cut into: only when the
-// output tiles are few (under two waves), the count (<= 8, <= chunks) that
-// minimises waves x chunks per piece, the smaller on ties.  The result does
-// not depend on it: the pieces' integer sums add exactly.
+// Pieces the chunk range of each output tile is cut into: the smallest count
+// in {1, 2, 4, 8} (at most half the chunks, unless 1) that gives the launch at
+// least four work units per SM, so that the units handed out last are short
+// and the SMs finish close together.  The result does not depend on it: the
+// pieces' integer sums add exactly.
 int choose_pieces(int64_t tiles, int64_t nchunks, int sms) {
-    if (tiles >= 2 * (int64_t)sms || nchunks <= 1) return 1;
-    int best = 1;
-    int64_t best_cost = ((tiles + sms - 1) / sms) * nchunks;
-    for (int s = 2; s <= 8 && s <= nchunks; ++s) {
-        const int64_t cost = ((tiles * s + sms - 1) / sms) * ((nchunks + s - 1) / s);
-        if (cost < best_cost) { best = s; best_cost = cost; }
-    }
-    return best;
+    int s = 1;
+    while (s < 8 && 2 * s <= nchunks && tiles * s < 4 * (int64_t)sms) s *= 2;
+    return s;
 }
 
 template <bool RCONTIG, bool FLAG_ONLY>
@@ -1209,7 +1281,7 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     int *cntA = invA + LpA;                              // planes per (row tile, chunk)
     int *cntB = cntA + tiles_m * nchunks;                // planes per (column tile, chunk)
     uint2 *clist = reinterpret_cast<uint2 *>(reinterpret_cast<char *>(cntA) + cntBytes);
-    unsigned int *ccount = reinterpret_cast<unsigned int *>(clist + ccap);
+    unsigned int *ccount = reinterpret_cast<unsigned int *>(clist + ccap);   // chunk repairs, work units
     unsigned int *work = ccount + 4;
 
     // the deferral counter and the plane counts start at 0, the line grains
@@ -1219,7 +1291,7 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         err = cudaMemsetAsync(GA, kGrainNone & 0xff, 4 * (size_t)(LpA + LpB), stream);
     if (err == cudaSuccess) err = cudaMemsetAsync(cntA, 0, cntBytes, stream);
     if (err == cudaSuccess) err = cudaMemsetAsync(flagA, 0, 4 * (size_t)LpA, stream);
-    if (err == cudaSuccess) err = cudaMemsetAsync(ccount, 0, sizeof(unsigned int), stream);
+    if (err == cudaSuccess) err = cudaMemsetAsync(ccount, 0, 4 * sizeof(unsigned int), stream);
     const bool a_rc = (p.pass != CARBON_PASS_DW), b_rc = (p.pass == CARBON_PASS_DX);
     if (err == cudaSuccess && nchunks > 0)
         err = a_rc ? launch_prep<true, true>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, nullptr, (int)nchunks, nullptr, flagA, stream)
@@ -1266,6 +1338,7 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         a.chunk_count = ccount;
         a.chunk_list = clist;
         a.chunk_cap = (unsigned int)ccap;
+        a.unit_counter = ccount + 1;
         const int64_t units = tiles_m * tiles_n * pieces;
         const int grid = (int)(units < sms ? units : sms);
         err = out_f64 ? launch_tc_main<true>(ma, mb, a, grid, ia, SA, SB, LpA, LpB, work, stream)

@@ -238,3 +238,31 @@ def test_plane_counts_per_tile_and_trailing_zeros(pass_):
         X = bf16(lines(Kd, Mt, 4).T)
         dY = bf16(lines(Nd, Mt, 5).T)
         check("dw", X, dY, None, Mt, Kd, Nd)
+
+
+def test_outer_sum_wraps_within_a_piece():
+    """Two chunks of one piece whose shifted chunk sums each fit 63 bits but
+    whose running sum passes 2^63 (the int64 sum wraps): rows of integers
+    8..504 in chunks 0 and 1 and one entry near 2^-25 in chunk 2 (so the row's
+    grain is 28 bits below those chunks), columns whose chunk sums give about
+    2^61 and 2^62 in grain units, scaled per column across the boundary.  The
+    kernel must notice the wrap and send the output to the fix-up, never keep
+    the wrapped sum (a signed range test that overflowed once let it through).
+    With 2 x 2 output tiles and 3 chunks the chunk range is cut in two pieces,
+    chunks 0 and 1 together."""
+    rng = np.random.default_rng(7)
+    M, K, N = 130, 768, 70
+    X = np.zeros((M, K))
+    W = np.zeros((K, N))
+    for i in range(M):
+        X[i, :512] = np.ldexp(rng.integers(1, 64, 512).astype(np.float64), 3)
+        X[i, 512 + int(rng.integers(0, 256))] = np.ldexp(1.0, int(rng.integers(-26, -24)))
+    for j in range(N):
+        c = 0.6 + 0.9 * j / N
+        for q, target in ((0, 700.0), (1, 1500.0), (2, 1.0)):
+            w = rng.random(256) + 0.5
+            w = w / w.sum() * target * c / 256.0
+            w[int(rng.integers(0, 256))] = np.ldexp(1.0 + rng.integers(0, 128) / 128.0, -20)
+            W[256 * q:256 * q + 256, j] = w
+    _, fixups = check("fwd", bf16(X), bf16(W), None, M, K, N)
+    assert fixups > 0
