@@ -1007,13 +1007,14 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
         const int64_t j0 = jg * 8;
         // every load first: the partial sums (a warp reads 32 consecutive
         // rows of one column), the column grains and the bias
-        long long t0[8];
+        long long t0[8], t1[8];
         int gw[8];
         uint32_t hb[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const bool in = j0 + e < cols;
             t0[e] = in ? __ldg(&Tout[(j0 + e) * rows + i]) : 0ll;
+            t1[e] = (in && pieces > 1) ? __ldg(&Tout[plane + (j0 + e) * rows + i]) : 0ll;
             gw[e] = in ? __ldg(&GB[j0 + e]) : 0;
             hb[e] = (in && bias != nullptr) ? ld_bits(bias, j0 + e) : 0u;
         }
@@ -1057,9 +1058,9 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             const int64_t j = j0 + e;
             if (j >= cols) { skip |= 1u << e; continue; }
             // the pieces' partial sums add exactly (128 bits)
-            bool deferred = t0[e] == kDeferredSum;
-            __int128 acc = t0[e];
-            for (int k = 1; k < pieces && !deferred; ++k) {
+            bool deferred = t0[e] == kDeferredSum || (pieces > 1 && t1[e] == kDeferredSum);
+            __int128 acc = (__int128)t0[e] + (__int128)t1[e];
+            for (int k = 2; k < pieces && !deferred; ++k) {
                 const long long t = __ldg(&Tout[k * plane + j * rows + i]);
                 deferred = t == kDeferredSum;
                 acc += t;
@@ -1161,12 +1162,14 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
 
 // Pieces the chunk range of each output tile is cut into: the smallest count
 // in {1, 2, 4, 8} (at most half the chunks, unless 1) that gives the launch at
-// least four work units per SM, so that the units handed out last are short
-// and the SMs finish close together.  The result does not depend on it: the
-// pieces' integer sums add exactly.
+// least four work units per SM and work units of at most 8 chunks, so that
+// the units handed out last are short and the SMs finish close together.  The
+// result does not depend on it: the pieces' integer sums add exactly.
 int choose_pieces(int64_t tiles, int64_t nchunks, int sms) {
     int s = 1;
-    while (s < 8 && 2 * s <= nchunks && tiles * s < 4 * (int64_t)sms) s *= 2;
+    while (s < 8 && 2 * s <= nchunks &&
+           (tiles * s < 4 * (int64_t)sms || (nchunks + s - 1) / s > 8))
+        s *= 2;
     return s;
 }
 
