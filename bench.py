@@ -240,6 +240,59 @@ def oracle_sample(host_layers, target_s, threads=None):
 
 # -------------------------------------------------------------------- main
 
+def max_over_ranks(ms, pg=None, device=None):
+    """The largest of every rank's time (the job ends with its slowest rank);
+    the local value when there is no process group."""
+    if pg is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gflops(flops_per_rank, world, ms):
+    """Whole-job throughput: every rank runs its own replica of the step (weak
+    scaling), so the job does world x the flops of one rank in the slowest
+    rank's time."""
+    return flops_per_rank * world / (ms * 1e-3) / 1e9
+
+
+# ------------------------------------------------------ recorded DRAM traffic
+
+def csrc_sha256():
+    """Hash of the library's CUDA sources: a traffic figure recorded with one
+    hash says nothing about kernels built from other sources."""
+    import hashlib
+    d = os.path.join(ROOT, "deterministic_invariant_gemm_fwd_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` (dram__bytes_read.sum +
+    dram__bytes_write.sum, averaged over the launches of one bench step) from
+    the ncu summaries in profiles/, when they were taken from the current
+    sources; None otherwise.  A summary records it on a line
+    `traffic <kernel> bytes_per_launch=<B> csrc_sha256=<hex>`."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    cur = csrc_sha256()
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name)) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 4 and parts[0] == "traffic" and parts[1] == kernel:
+                    kv = dict(p.split("=", 1) for p in parts[2:])
+                    if kv.get("csrc_sha256") == cur:
+                        return int(kv["bytes_per_launch"])
+    return None
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -399,14 +452,10 @@ def main():
                 per_gemm_ms[(t, p, K, N)] = a.elapsed_time(b) / reps
         assert cg.carbon_get_device_status(stream.cuda_stream) == 0
 
-    step_ms = sum(a.elapsed_time(b) for a, b in step_events) / args.steps
-    if pg is not None:
-        t = torch.tensor([step_ms], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_events) / args.steps, pg, device)
     tier_flops = {t: sum(2.0 * M * K * N for (_, _, M, K, N) in wl.gemm_list(t)) for t in tiers}
     flops = sum(tier_flops.values())
-    value = flops * world / (step_ms * 1e-3) / 1e9
+    value = whole_job_gflops(flops, world, step_ms)
 
     tier_info, rooflines = {}, {}
     pk, pk_kind = peaks()
@@ -442,7 +491,8 @@ def main():
             achieved = kg_flops / (main_ms * 1e-3) / 1e12 if main_ms > 0 else 0.0
             rooflines["exact"] = {
                 "bound": "tensor", "unit": "TFLOP/s", "achieved": _r(achieved), "peak": _r(peak),
-                "frac": _r(achieved / peak), "traffic": None, "kernel": "exact_tc_kernel",
+                "frac": _r(achieved / peak), "traffic": recorded_traffic("exact_tc_kernel"),
+                "traffic_unit": "bytes per launch (ncu, profiles/)", "kernel": "exact_tc_kernel",
                 "peak_kind": f"bf16 burst, of {pk_kind}",
                 "note": ("algorithmic work = the digit-pair MMAs the kernel issues (counted live: "
                          f"{main_kg} plane products of 2*128*64*256 flops in {main_n} launches), "
@@ -493,11 +543,8 @@ def main():
             e1.record(stream)
             stream.synchronize()
             e2e_ms = e0.elapsed_time(e1) / args.steps
-        if pg is not None:
-            t_ = torch.tensor([e2e_ms], device=device)
-            pg.all_reduce(t_, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t_.item())
-        e2e = {"value": _r(flops * world / (e2e_ms * 1e-3) / 1e9), "unit": "GFLOP/s",
+        e2e_ms = max_over_ranks(e2e_ms, pg, device)
+        e2e = {"value": _r(whole_job_gflops(flops, world, e2e_ms)), "unit": "GFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": _r(e2e_ms)}
 
     cpu = None
