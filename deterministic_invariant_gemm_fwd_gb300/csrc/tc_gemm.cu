@@ -7,8 +7,9 @@
 // fp32, rounded once to bf16 (RNE).
 //
 // Determinism and batch invariance by construction:
-//  * the output tile is always 128 rows x BN columns; BN depends on the
-//    output column count only; rows past M are zero-filled by TMA and their
+//  * the output tile is always 128 rows x BN columns; BN (128, 192 or 256)
+//    depends on the output column count and the pass only; rows past M are
+//    zero-filled by TMA and their
 //    results dropped, so row i's instruction sequence is the same for every M;
 //  * each tile's reduction runs its k-blocks of 64 in ascending order, four
 //    K=16 MMAs per block in ascending order, into one TMEM accumulator; the
@@ -281,7 +282,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     bar.tempty0 = bar.tfull0 + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + (2 * kStages + 4) * 8);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    constexpr uint32_t kTmemCols = 2 * BN;                 // 256 or 512: powers of two
+    constexpr uint32_t kTmemCols = BN == 128 ? 256u : 512u;   // two accumulators, rounded to a power of two
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t tmem_base = setup_cta<BN>(smem, bar, &map_a, &map_b, tmem_slot, abort_flag, kTmemCols);
@@ -584,7 +585,25 @@ cudaError_t launch_split(const CUtensorMap &ma, const CUtensorMap &mb, const TcA
 }
 
 // Output-tile width from the output column count only (never from M).
-int choose_bn(int64_t cols) { return cols <= 128 ? 128 : 256; }
+// Output tile width from the column count and the pass only (never the row
+// count, so a row's tiles, and its bits, do not depend on the batch): 128 for
+// at most 128 columns; otherwise 256, or 192 when that fills the SMs better
+// for a reference batch of 8192 rows on 152 SMs (768 columns: 256 tiles of
+// 192 run in two fuller waves than 192 tiles of 256).  dW keeps 256: its
+// token split is sized for that.
+double wave_fill(int64_t tiles) {
+    const int64_t waves = (tiles + 151) / 152;
+    return (double)tiles / (double)(waves * 152);
+}
+
+int choose_bn(int64_t cols, int pass) {
+    if (cols <= 128) return 128;
+    if (pass == CARBON_PASS_DW) return 256;
+    const int64_t ref_tiles_m = 8192 / kBM;
+    const double f256 = wave_fill(ref_tiles_m * ((cols + 255) / 256));
+    const double f192 = wave_fill(ref_tiles_m * ((cols + 191) / 192));
+    return f192 > f256 ? 192 : 256;
+}
 
 // dW split count from the output tile count only: the largest s in
 // {1, 2, 4, 8} with tiles * s <= 152 (GB300's SM count, fixed here so the
@@ -621,7 +640,7 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
 
     cudaError_t err = cudaSuccess;
 
-    const int bn = choose_bn(p.cols);
+    const int bn = choose_bn(p.cols, p.pass);
     CUtensorMap ma, mb, mo;
     bool ok;
     switch (p.pass) {
@@ -668,6 +687,9 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
         if (bn == 128)
             err = out_f32 ? launch_persistent_pass<128, true>(p.pass, ma, mb, mo, a, grid, stream)
                           : launch_persistent_pass<128, false>(p.pass, ma, mb, mo, a, grid, stream);
+        else if (bn == 192)
+            err = out_f32 ? launch_persistent_pass<192, true>(p.pass, ma, mb, mo, a, grid, stream)
+                          : launch_persistent_pass<192, false>(p.pass, ma, mb, mo, a, grid, stream);
         else
             err = out_f32 ? launch_persistent_pass<256, true>(p.pass, ma, mb, mo, a, grid, stream)
                           : launch_persistent_pass<256, false>(p.pass, ma, mb, mo, a, grid, stream);
