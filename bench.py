@@ -508,7 +508,9 @@ def main():
             achieved = fl_all / (ms * 1e-3) / 1e12
             peak = float(pk["bf16_tflops"])
             rooflines["tc"] = {"bound": "tensor", "unit": "TFLOP/s", "achieved": _r(achieved),
-                               "peak": _r(peak), "frac": _r(achieved / peak), "traffic": None,
+                               "peak": _r(peak), "frac": _r(achieved / peak),
+                               "traffic": recorded_traffic("tc_tier"),
+                               "traffic_unit": "bytes per launch (ncu, profiles/)",
                                "kernel": "tc_gemm_kernel + tc_dw_split_kernel",
                                "peak_kind": f"bf16 burst, of {pk_kind}",
                                "frac_of_sustained": _r(achieved / float(pk.get("bf16_tflops_sustained", peak)))}
