@@ -208,6 +208,69 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------- fp32 exact tier (FP64 pipe)
+
+def fp32_exact_section(device, stream, fp64_rate, stress=True):
+    """The fp32 workloads of the exact tier, which run the float64 KBN kernel
+    on the FP64 pipe: the toy MLP's nine GEMMs (M = 512 tokens, fwd + dX +
+    dW of (K, N) in {(256,512), (512,512), (512,256)}) and the cancellation
+    stress dW (65536 tokens, K = 768, N = 3072).  Each is run once untimed,
+    then timed once with CUDA events on `stream`.  FP64 utilisation is the
+    literal algorithm's floor, 5 FP64 instructions per multiply-add (product,
+    sum, two for the exact error, one for the compensation), over the time
+    and the measured DFMA rate; the kernel folds the product into the sum's
+    FMA and proves whole slices exact, so the figure can pass 1."""
+    import torch
+    import deterministic_invariant_gemm_fwd_gb300 as cg
+    from deterministic_invariant_gemm_fwd_gb300 import inputs
+
+    def run(calls, macs):
+        for c in calls:
+            c()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for c in calls:
+            c()
+        e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1)
+        mac_rate = macs / (ms * 1e-3)
+        return {"ms": _r(ms), "gflops": _r(2.0 * mac_rate / 1e9),
+                "fp64_util_vs_literal": _r(5.0 * mac_rate / fp64_rate)}
+
+    s = stream.cuda_stream
+    out = {"unit": "ms, GFLOP/s (2 MNK / t), 5 MNK / (t x measured DFMA rate)",
+           "fp64_dfma_rate_tops": _r(fp64_rate / 1e12)}
+    calls, macs = [], 0
+    torch.cuda.synchronize(device)
+    for L in inputs.toy_mlp(SEED):
+        M, K, N = L["M"], L["K"], L["N"]
+        X, W, b, dY = (torch.from_numpy(L[k]).to(device) for k in ("X", "W", "b", "dY"))
+        Y = torch.empty((M, N), dtype=torch.float32, device=device)
+        dX = torch.empty((M, K), dtype=torch.float32, device=device)
+        dW = torch.empty((K, N), dtype=torch.float32, device=device)
+        calls += [lambda Y=Y, X=X, W=W, b=b, M=M, K=K, N=N: cg.carbon_gemm_fwd(Y, X, W, b, M, K, N, "f32", "exact", s),
+                  lambda dX=dX, dY=dY, W=W, M=M, K=K, N=N: cg.carbon_gemm_dx(dX, dY, W, M, K, N, "f32", "exact", s),
+                  lambda dW=dW, X=X, dY=dY, M=M, K=K, N=N: cg.carbon_gemm_dw(dW, X, dY, M, K, N, "f32", "exact", s)]
+        macs += 3 * M * K * N
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        out["toy_mlp_9_gemms"] = run(calls, macs)
+        if stress:
+            S = inputs.stress_dw(SEED)
+            M, K, N = S["M"], S["K"], S["N"]
+            X = torch.from_numpy(S["X"]).to(device)
+            dY = torch.from_numpy(S["dY"]).to(device)
+            dW = torch.empty((K, N), dtype=torch.float32, device=device)
+            torch.cuda.synchronize(device)
+            out["stress_dw_65536x768x3072"] = run(
+                [lambda: cg.carbon_gemm_dw(dW, X, dY, M, K, N, "f32", "exact", s)], M * K * N)
+            del X, dY, dW
+    assert cg.carbon_get_device_status(s) == 0
+    return out
+
+
 # ------------------------------------------------------------ CPU baseline
 
 def oracle_sample(host_layers, target_s, threads=None):
@@ -339,6 +402,8 @@ def main():
     ap.add_argument("--tiers", default="auto")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fp32", action="store_true",
+                    help="skip the fp32 exact-tier section (toy MLP and cancellation stress)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the TC tier eagerly inside the timed region")
     ap.add_argument("--gemm", default=None,
@@ -549,6 +614,12 @@ def main():
         e2e = {"value": _r(whole_job_gflops(flops, world, e2e_ms)), "unit": "GFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": _r(e2e_ms)}
 
+    fp32 = None
+    if "exact" in tiers and not args.no_fp32 and only is None:
+        if fp64_rate is None:
+            fp64_rate, _ = cg.carbon_measure_fp64_rate(stream.cuda_stream)
+        fp32 = fp32_exact_section(device, stream, fp64_rate)
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         v, dt, macs, threads, per = oracle_sample(host, args.cpu_seconds)
@@ -576,6 +647,7 @@ def main():
             "tiers": tier_info,
             "roofline": rooflines[dom],
             "rooflines": rooflines,
+            "fp32_exact": fp32,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
