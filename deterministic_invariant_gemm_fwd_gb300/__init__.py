@@ -8,6 +8,9 @@ and call it.  Weights are stored [in, out] (sgemm-bi page, "Use").
     Y  = linear_fwd(X, W, b, tier="exact")   # Y  = X.W + b
     dX = linear_dx(dY, W, tier="exact")      # dX = dY.W^T
     dW = linear_dw(X, dY, tier="exact")      # dW = X^T.dY
+
+``deterministic_invariant_gemm_fwd_gb300.nn`` wraps them in an autograd
+``Linear`` / ``deterministic_linear`` (with a deterministic bias gradient).
 """
 from __future__ import annotations
 
