@@ -27,8 +27,9 @@ same shapes stand in for them):
 
 The second parameter of N(mu, sigma) is the standard deviation.  Normal
 draws are made in float64 and rounded to nearest-even into fp32; bf16 operands
-are rounded to nearest-even from that fp32 value.  bf16 tensors are carried as
-``numpy.uint16`` bit patterns.
+are rounded to nearest-even from that fp32 value (fp16 operands likewise, to
+IEEE binary16).  bf16 and fp16 tensors are carried as ``numpy.uint16`` bit
+patterns.
 
 Seeds 42, 123, 7, 999 and 2024 are the five seeds of the Carbon README's
 "Toy Model" table.
@@ -62,6 +63,18 @@ def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     return r
 
 
+def f32_to_f16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32 values to IEEE binary16 (nearest, ties to even; numpy's
+    conversion) and return the bits.  Values beyond 65504 become infinities.
+    This is the input encoding step of the data recipe, not part of the GEMM."""
+    return np.ascontiguousarray(a, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen binary16 bit patterns to fp32 values (exact)."""
+    return np.ascontiguousarray(b, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns to fp32 values (exact)."""
     b = np.ascontiguousarray(b, dtype=np.uint16)
@@ -81,6 +94,8 @@ def _encode(a: np.ndarray, dtype: str) -> np.ndarray:
         return np.ascontiguousarray(a, dtype=np.float32)
     if dtype == "bf16":
         return f32_to_bf16_bits(a)
+    if dtype == "f16":
+        return f32_to_f16_bits(a)
     raise ValueError(f"unknown dtype {dtype!r}")
 
 

@@ -26,7 +26,7 @@ CFLAGS = ["-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math",
           "-fPIC", "-shared", "-pthread"]
 
 PASSES = {"fwd": 0, "dx": 1, "dw": 2}
-DTYPES = {"f32": 0, "bf16": 1}
+DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
 CHUNK = 256
 
 _lib = None

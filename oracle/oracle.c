@@ -15,7 +15,7 @@
  * the single double fl(s + c), and the chunk values are combined left to
  * right with KBN again.  The forward pass then adds the bias in float64
  * (one rounded addition) and every pass rounds the float64 value once,
- * to nearest-even, to the output type (fp32 or bf16).  sgemm-bi's
+ * to nearest-even, to the output type (fp32, bf16 or fp16).  sgemm-bi's
  * "Determinism contracts" table describes the same final step as an RNE
  * downcast.
  *
@@ -27,7 +27,7 @@
  *
  * Build: -O2 -ffp-contract=off -fno-fast-math.  With contraction off every
  * `a * b` and `a + b` below is one IEEE-754 binary64 operation rounded to
- * nearest-even; products of two fp32 (or two bf16) values are exact in
+ * nearest-even; products of two fp32 (or two bf16, or two fp16) values are exact in
  * binary64, so the only roundings are the additions the algorithm names.
  */
 #include <float.h>
@@ -43,14 +43,35 @@
 
 #define ORACLE_CHUNK 256
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
 enum { ORACLE_FWD = 0, ORACLE_DX = 1, ORACLE_DW = 2 };
 
 /* ---- input decoding (exact widening to binary64) ------------------------ */
 
+/* IEEE binary16 from its fields: 5 exponent bits (bias 15), 10 fraction
+ * bits; exponent field 0 holds zeros and subnormals (quantum 2^-24), 31
+ * infinities and NaNs. */
+static double decode_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1, ex = (h >> 10) & 31, fr = h & 1023;
+    double v;
+    if (ex == 31)
+        v = fr ? NAN : INFINITY;
+    else if (ex == 0)
+        v = ldexp((double)fr, -24);
+    else
+        v = ldexp((double)(1024 + fr), ex - 25);
+    return sign ? -v : v;
+}
+
 static double decode(const void *base, int dtype, int64_t idx)
 {
     float f;
+    if (dtype == ORACLE_F16) {
+        uint16_t h;
+        memcpy(&h, (const char *)base + 2 * idx, 2);
+        return decode_f16(h);          /* exact: binary16 is a subset of binary64 */
+    }
     if (dtype == ORACLE_F32) {
         memcpy(&f, (const char *)base + 4 * idx, 4);
     } else {
@@ -106,6 +127,39 @@ static uint16_t round_to_bf16_bits(double y)
     f = (float)r;                       /* exact: r has <= 8 significant bits */
     memcpy(&u, &f, 4);
     return (uint16_t)(u >> 16) | sign;
+}
+
+/* binary64 -> binary16, nearest-even, in one rounding.  binary16 has 11
+ * significant bits, normal exponents -14..15, subnormal quantum 2^-24 and
+ * largest finite (2 - 2^-10) * 2^15 = 65504; the same quantum method as
+ * for bf16, then the fields of the (exact) rounded value. */
+static uint16_t round_to_f16_bits(double y)
+{
+    double a, quantum, n, r;
+    int e, E;
+    uint16_t sign = signbit(y) ? 0x8000u : 0u;
+
+    if (isnan(y))
+        return 0x7E00u | sign;
+    a = fabs(y);
+    if (a >= 0x1p16)                    /* beyond every finite binary16 */
+        return 0x7C00u | sign;
+    if (a == 0.0)
+        return sign;
+    (void)frexp(a, &e);
+    E = e - 1;                          /* floor(log2(a)) */
+    if (E < -14)
+        E = -14;                        /* subnormal range: fixed quantum 2^-24 */
+    quantum = ldexp(1.0, E - 10);
+    n = nearbyint(a / quantum);         /* default mode: ties to even */
+    r = n * quantum;
+    if (r >= 65520.0)                   /* rounded past 65504 */
+        return 0x7C00u | sign;
+    if (r < 0x1p-14)                    /* subnormal (or zero): r = k * 2^-24 */
+        return (uint16_t)(sign | (uint16_t)(r * 0x1p24));
+    (void)frexp(r, &e);
+    E = e - 1;
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(ldexp(r, 10 - E) - 1024.0));
 }
 
 /* ---- the summation ------------------------------------------------------- */
@@ -181,7 +235,7 @@ static void one_output(const job_t *jb, int64_t i, int64_t j, int64_t slot)
             uint32_t u = round_to_f32_bits(y);
             memcpy((char *)jb->out + 4 * slot, &u, 4);
         } else {
-            uint16_t h = round_to_bf16_bits(y);
+            uint16_t h = jb->dtype == ORACLE_F16 ? round_to_f16_bits(y) : round_to_bf16_bits(y);
             memcpy((char *)jb->out + 2 * slot, &h, 2);
         }
     }
@@ -243,7 +297,7 @@ static int check(int pass, int dtype, int64_t M, int64_t K, int64_t N)
 {
     if (pass < ORACLE_FWD || pass > ORACLE_DW)
         return -1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F16)
         return -1;
     if (M < 0 || K < 0 || N < 0)
         return -1;
@@ -297,7 +351,7 @@ void oracle_round(int dtype, const double *y, void *out, int64_t n)
             uint32_t u = round_to_f32_bits(y[k]);
             memcpy((char *)out + 4 * k, &u, 4);
         } else {
-            uint16_t h = round_to_bf16_bits(y[k]);
+            uint16_t h = dtype == ORACLE_F16 ? round_to_f16_bits(y[k]) : round_to_bf16_bits(y[k]);
             memcpy((char *)out + 2 * k, &h, 2);
         }
     }

@@ -2,9 +2,9 @@
 
 Nothing here follows the oracle's algorithm.  The exact result of a matrix
 product is taken with Python's unbounded rationals and numpy's object-array
-matmul (the mathematical definition, no rounding anywhere); rounding to fp32
-or bf16 is done from the definition of round-to-nearest-even on the exact
-rational value.
+matmul (the mathematical definition, no rounding anywhere); rounding to fp32,
+bf16 or fp16 is done from the definition of round-to-nearest-even on the
+exact rational value.
 """
 from __future__ import annotations
 
@@ -18,11 +18,18 @@ FORMATS = {
     # significand bits (incl. hidden), min normal exponent, max exponent
     "f32": (24, -126, 127),
     "bf16": (8, -126, 127),
+    "f16": (11, -14, 15),
 }
 
 
 def to_fractions(a: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact rational values of fp32 arrays or bf16 bit arrays."""
+    """Exact rational values of fp32 arrays or bf16 / fp16 bit arrays."""
+    if dtype == "f16":
+        a = np.asarray(a, dtype=np.uint16).view(np.float16).astype(np.float64)
+        flat = [Fraction(float(v)) for v in a.ravel()]
+        out = np.empty(len(flat), dtype=object)
+        out[:] = flat
+        return out.reshape(np.shape(a))
     if dtype == "bf16":
         a = (np.asarray(a, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
     flat = [Fraction(float(v)) for v in np.asarray(a, dtype=np.float32).ravel()]
@@ -133,6 +140,8 @@ def near_midpoint(q: Fraction, fmt: str, tol: Fraction) -> bool:
 
 def value_bits(v, fmt: str) -> int:
     """Bit pattern of a value (Fraction or +-inf) that is exact in ``fmt``."""
+    if fmt == "f16":
+        return int(np.array([float(v)], dtype=np.float16).view(np.uint16)[0])
     f = np.float32(float(v))
     u = int(np.array([f], dtype=np.float32).view(np.uint32)[0])
     return u if fmt == "f32" else (u >> 16)

@@ -24,12 +24,16 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form.json")
 
 def _enc(values, dtype):
     a = np.array(values, dtype=np.float64).astype(np.float32)
+    if dtype == "f16":
+        return inputs.f32_to_f16_bits(a)
     return a if dtype == "f32" else inputs.f32_to_bf16_bits(a)
 
 
 def _as_f64(out, dtype):
     if dtype == "f32":
         return out.astype(np.float64)
+    if dtype == "f16":
+        return inputs.f16_bits_to_f32(out).astype(np.float64)
     return inputs.bf16_bits_to_f32(out).astype(np.float64)
 
 
@@ -98,12 +102,15 @@ def _random_operands(rng, pass_, M, K, N, dtype, scale_a=1.0, scale_b=0.02):
     if dtype == "bf16":
         A, B = inputs.f32_to_bf16_bits(A), inputs.f32_to_bf16_bits(B)
         bias = None if bias is None else inputs.f32_to_bf16_bits(bias)
+    if dtype == "f16":
+        A, B = inputs.f32_to_f16_bits(A), inputs.f32_to_f16_bits(B)
+        bias = None if bias is None else inputs.f32_to_f16_bits(bias)
     return A, B, bias
 
 
 @pytest.mark.parametrize("seed", inputs.SEEDS)
 @pytest.mark.parametrize("pass_", ["fwd", "dx", "dw"])
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_exact_rational(seed, pass_, dtype):
     rng = np.random.default_rng(seed)
     shapes = SMALL_SHAPES[seed % 3::2] if pass_ != "fwd" else SMALL_SHAPES
@@ -172,24 +179,38 @@ def _rounding_corpus(rng, n=20000):
     # subnormal bf16/fp32 region and zeros
     vals += [2.0 ** -133, 1.5 * 2.0 ** -133, 2.0 ** -134, 3 * 2.0 ** -135, 2.0 ** -149,
              2.0 ** -150, 1.5 * 2.0 ** -149, 0.0, -0.0, 5e-324]
+    # binary16: midpoints across its exponent range, the overflow boundary
+    # (65504, the midpoint 65520 above it) and the subnormal region (quantum 2^-24)
+    vals += list(rng.standard_normal(n // 4) * np.ldexp(1.0, rng.integers(-30, 18, n // 4)))
+    for e in (-16, -15, -14, -13, -1, 0, 1, 10, 14, 15):
+        for k in (0, 1, 2, 3, 1023, 2047 - 1024):
+            mid = (1024 + k + 0.5) * 2.0 ** (e - 10)
+            for d in (0.0, 1.0, -1.0):
+                v = np.nextafter(mid, np.inf) if d > 0 else (
+                    np.nextafter(mid, -np.inf) if d < 0 else mid)
+                vals += [v, -v]
+    vals += [65504.0, 65519.99, 65520.0, np.nextafter(65520.0, 0), 65536.0, 1e6,
+             2.0 ** -24, 2.0 ** -25, np.nextafter(2.0 ** -25, 1), 3 * 2.0 ** -26, 2.0 ** -26,
+             1.5 * 2.0 ** -24, 2.5 * 2.0 ** -24, 1023.5 * 2.0 ** -24, 2.0 ** -14]
     return np.array(vals, dtype=np.float64)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_output_rounding_is_rne(dtype):
     y = _rounding_corpus(np.random.default_rng(2024))
     got = oracle.round_out(dtype, y)
     if dtype == "f32":
         got = got.view(np.uint32)
+    inf_bits = {"f32": 0x7F800000, "bf16": 0x7F80, "f16": 0x7C00}[dtype]
+    sign_bit = 0x80000000 if dtype == "f32" else 0x8000
     for v, g in zip(y, got):
         r = ex.rne(Fraction(float(v)), dtype)
         if isinstance(r, float):                      # overflow
-            want = (0x7F800000 if dtype == "f32" else 0x7F80) | (
-                (0x80000000 if dtype == "f32" else 0x8000) if v < 0 else 0)
+            want = inf_bits | (sign_bit if v < 0 else 0)
         else:
             want = ex.value_bits(r, dtype)
             if r == 0 and np.signbit(v):
-                want |= 0x80000000 if dtype == "f32" else 0x8000
+                want |= sign_bit
         assert int(g) == want, (v.hex(), hex(int(g)), hex(want))
 
 
@@ -198,6 +219,21 @@ def test_rounding_special_values():
     b = oracle.round_out("bf16", y)
     assert list(b[:2]) == [0x7F80, 0xFF80]
     assert (int(b[2]) & 0x7F80) == 0x7F80 and (int(b[2]) & 0x7F) != 0
+    h = oracle.round_out("f16", y)
+    assert list(h[:2]) == [0x7C00, 0xFC00]
+    assert (int(h[2]) & 0x7C00) == 0x7C00 and (int(h[2]) & 0x3FF) != 0
+
+
+def test_f16_decoding_is_exact():
+    """Every binary16 bit pattern decodes to its value: the oracle's sums of
+    one product x * 1 return x itself, for all finite patterns."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    finite = bits[(bits & 0x7C00) != 0x7C00]
+    K = finite.size
+    one = inputs.f32_to_f16_bits(np.ones((1, 1), dtype=np.float32))
+    _, y = oracle.gemm("fwd", "f16", finite.reshape(K, 1), one, None, K, 1, 1)
+    want = finite.view(np.float16).astype(np.float64)
+    assert np.array_equal(y.reshape(K), want)
 
 
 # --------------------------------------------------------------------------
@@ -226,7 +262,7 @@ def test_column_permutation():
     assert np.array_equal(Yp.view(np.uint32), Y[:, perm].view(np.uint32))
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_pass_transposition_identities(dtype):
     rng = np.random.default_rng(999)
     M, K, N = 37, 300, 29       # R spans two chunks for fwd/dX; dW R=37
