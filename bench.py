@@ -323,35 +323,48 @@ def whole_job_gflops(flops_per_rank, world, ms):
 
 # ------------------------------------------------------ recorded DRAM traffic
 
-def csrc_sha256():
-    """Hash of the library's CUDA sources: a traffic figure recorded with one
-    hash says nothing about kernels built from other sources."""
+# The CUDA sources each recorded figure belongs to: the kernel's .cu file and
+# the library-internal headers it includes.
+KERNEL_SOURCES = {
+    "exact_tc_kernel": ("exact_tc.cu", "exact_bf16.cuh", "exact_common.cuh", "tcgen05.cuh",
+                        "device_sync.cuh", "carbon_internal.h"),
+    "tc_tier": ("tc_gemm.cu", "tcgen05.cuh", "device_sync.cuh", "carbon_internal.h"),
+}
+
+
+def sources_sha256(names, read=None):
+    """Hash of the named files of the library's CUDA sources: a traffic figure
+    recorded with one hash says nothing about kernels built from other
+    sources.  `read(name)` returns a file's bytes (default: the working tree)."""
     import hashlib
     d = os.path.join(ROOT, "deterministic_invariant_gemm_fwd_gb300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(d, name), "rb") as f:
+                return f.read()
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        with open(os.path.join(d, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(names):
+        h.update(name.encode() + b"\0" + read(name))
     return h.hexdigest()
 
 
 def recorded_traffic(kernel):
     """DRAM bytes per launch of `kernel` (dram__bytes_read.sum +
     dram__bytes_write.sum, averaged over the launches of one bench step) from
-    the ncu summaries in profiles/, when they were taken from the current
-    sources; None otherwise.  A summary records it on a line
-    `traffic <kernel> bytes_per_launch=<B> csrc_sha256=<hex>`."""
+    the ncu summaries in profiles/, when they were taken from the kernel's
+    current sources (KERNEL_SOURCES); None otherwise.  A summary records it
+    on a line `traffic <kernel> bytes_per_launch=<B> sources_sha256=<hex>`."""
     d = os.path.join(ROOT, "profiles")
-    if not os.path.isdir(d):
+    if not os.path.isdir(d) or kernel not in KERNEL_SOURCES:
         return None
-    cur = csrc_sha256()
+    cur = sources_sha256(KERNEL_SOURCES[kernel])
     for name in sorted(os.listdir(d)):
         with open(os.path.join(d, name)) as f:
             for line in f:
                 parts = line.split()
                 if len(parts) == 4 and parts[0] == "traffic" and parts[1] == kernel:
                     kv = dict(p.split("=", 1) for p in parts[2:])
-                    if kv.get("csrc_sha256") == cur:
+                    if kv.get("sources_sha256") == cur:
                         return int(kv["bytes_per_launch"])
     return None
 

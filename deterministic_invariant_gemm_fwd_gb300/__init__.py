@@ -31,7 +31,9 @@ def _dtype_code(t):
         return "f32"
     if t.dtype == torch.bfloat16:
         return "bf16"
-    raise TypeError(f"unsupported dtype {t.dtype}; expected float32 or bfloat16")
+    if t.dtype == torch.float16:
+        return "f16"
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float32, bfloat16 or float16")
 
 
 def _check2d(name, t):

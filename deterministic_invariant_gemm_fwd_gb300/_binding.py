@@ -17,13 +17,13 @@ LIB_PATH = os.path.join(HERE, "libcarbon_gemm.so")
 HEADERS = [os.path.join(os.path.dirname(HERE), "include", h)
            for h in ("carbon_gemm.h", "carbon_gemm_debug.h")]
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 TIER_EXACT, TIER_TC = 0, 1
 PASS_FWD, PASS_DX, PASS_DW = 0, 1, 2
 STATUS = {0: "CARBON_OK", 1: "CARBON_ERR_INVALID_ARG", 2: "CARBON_ERR_UNSUPPORTED",
           3: "CARBON_ERR_MISALIGNED", 4: "CARBON_ERR_CUDA", 5: "CARBON_ERR_TIMEOUT",
           6: "CARBON_ERR_SCRATCH_LIMIT"}
-DTYPES = {"f32": F32, "bf16": BF16}
+DTYPES = {"f32": F32, "bf16": BF16, "f16": F16}
 TIERS = {"exact": TIER_EXACT, "tc": TIER_TC}
 PASSES = {"fwd": PASS_FWD, "dx": PASS_DX, "dw": PASS_DW}
 

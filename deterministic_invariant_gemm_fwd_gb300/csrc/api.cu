@@ -60,7 +60,8 @@ bool mul_ok(int64_t a, int64_t b, int64_t *out) {
 carbon_status_t check_args(const Problem &p, int tier, bool *nothing_to_do) {
     *nothing_to_do = false;
     if (p.M < 0 || p.K < 0 || p.N < 0) return CARBON_ERR_INVALID_ARG;
-    if (p.dtype != CARBON_F32 && p.dtype != CARBON_BF16) return CARBON_ERR_INVALID_ARG;
+    if (p.dtype != CARBON_F32 && p.dtype != CARBON_BF16 && p.dtype != CARBON_F16)
+        return CARBON_ERR_INVALID_ARG;
     if (tier != CARBON_TIER_EXACT && tier != CARBON_TIER_TC) return CARBON_ERR_INVALID_ARG;
     int64_t mk, kn, mn, t;
     if (!mul_ok(p.M, p.K, &mk) || !mul_ok(p.K, p.N, &kn) || !mul_ok(p.M, p.N, &mn))
@@ -79,7 +80,7 @@ carbon_status_t check_args(const Problem &p, int tier, bool *nothing_to_do) {
     if (out_elems > 0 && p.out == nullptr) return CARBON_ERR_INVALID_ARG;
     if (out_elems > 0 && a_elems > 0 && p.A == nullptr) return CARBON_ERR_INVALID_ARG;
     if (out_elems > 0 && b_elems > 0 && p.B == nullptr) return CARBON_ERR_INVALID_ARG;
-    if (tier == CARBON_TIER_TC && p.dtype != CARBON_BF16) return CARBON_ERR_UNSUPPORTED;
+    if (tier == CARBON_TIER_TC && p.dtype == CARBON_F32) return CARBON_ERR_UNSUPPORTED;
     if (out_elems == 0) *nothing_to_do = true;
     return CARBON_OK;
 }
@@ -143,7 +144,7 @@ carbon_status_t carbon_debug_tc_f32(carbon_pass_t pass, float *acc, const void *
 
 carbon_status_t carbon_debug_round(carbon_dtype_t dtype, void *out, const double *in,
                                    int64_t n, carbon_stream_t stream) {
-    if (dtype != CARBON_F32 && dtype != CARBON_BF16) return CARBON_ERR_INVALID_ARG;
+    if (dtype != CARBON_F32 && dtype != CARBON_BF16 && dtype != CARBON_F16) return CARBON_ERR_INVALID_ARG;
     if (n < 0 || (n > 0 && (out == nullptr || in == nullptr))) return CARBON_ERR_INVALID_ARG;
     if (n == 0) return CARBON_OK;
     carbon_status_t st = carbon::current_device(nullptr, nullptr);

@@ -52,6 +52,7 @@
 #include "carbon_internal.h"
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "exact_common.cuh"
 
@@ -113,9 +114,41 @@ __device__ __forceinline__ int grain_key_b(double v) {
     return lsb_exponent(v) << 20;
 }
 
+// float64 -> IEEE binary16, round to nearest even, one rounding: 11
+// significant bits, normal exponents -14..15 (largest finite 65504),
+// subnormal quantum 2^-24, on the integer fields of the float64.
+__device__ __forceinline__ unsigned short exact_round_f16(double y) {
+    const unsigned long long u = (unsigned long long)__double_as_longlong(y);
+    const unsigned int sign = (unsigned int)(u >> 48) & 0x8000u;
+    const unsigned long long mag = u & 0x7fffffffffffffffull;
+    if (mag > 0x7ff0000000000000ull) return (unsigned short)(sign | 0x7e00u);  // NaN
+    const int E = (int)(mag >> 52) - 1023;
+    if (E >= 16) return (unsigned short)(sign | 0x7c00u);                     // |y| >= 2^16
+    if (E >= -14) {                                                           // normal range
+        const unsigned long long lsb = (mag >> 42) & 1ull;
+        const unsigned long long r = (mag + 0x000001ffffffffffull + lsb) >> 42;
+        const int Ed = (int)(r >> 10);                                        // biased, after carry
+        if (Ed - 1023 >= 16) return (unsigned short)(sign | 0x7c00u);
+        return (unsigned short)(sign | ((unsigned int)(Ed - 1023 + 15) << 10) | (unsigned int)(r & 0x3ff));
+    }
+    if (E < -25) return (unsigned short)sign;                                 // below half the quantum
+    // subnormal range: n = RNE(|y| / 2^-24), 0 <= n <= 1024 (1024 = min normal)
+    const unsigned long long sig = (mag & 0x000fffffffffffffull) | 0x0010000000000000ull;
+    const int shift = 28 - E;                                                 // 43 .. 53
+    const unsigned long long n = sig >> shift;
+    const unsigned long long rem = sig & ((1ull << shift) - 1ull);
+    const unsigned long long half = 1ull << (shift - 1);
+    const unsigned long long nr = n + ((rem > half || (rem == half && (n & 1ull))) ? 1ull : 0ull);
+    return (unsigned short)(sign | (unsigned int)nr);
+}
+
+// The fp32 bit pattern of an operand element (bf16 is the top half of an
+// fp32; fp16 widens to fp32 exactly with the hardware conversion).
 template <int DT>
 __device__ __forceinline__ uint32_t load_bits(const void *base, int64_t idx) {
     if (DT == CARBON_F32) return __ldg(static_cast<const unsigned int *>(base) + idx);
+    if (DT == CARBON_F16)
+        return __float_as_uint(__half2float(__ushort_as_half(__ldg(static_cast<const unsigned short *>(base) + idx))));
     return (uint32_t)__ldg(static_cast<const unsigned short *>(base) + idx) << 16;
 }
 
@@ -270,6 +303,8 @@ exact_kbn_kernel(const KArgs p) {
                 static_cast<double *>(p.out)[o] = y;
             else if (DT == CARBON_F32)
                 static_cast<float *>(p.out)[o] = __double2float_rn(y);
+            else if (DT == CARBON_F16)
+                static_cast<unsigned short *>(p.out)[o] = exact_round_f16(y);
             else
                 static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
         }
@@ -281,6 +316,7 @@ __global__ void round_kernel(int dtype, void *out, const double *in, int64_t n) 
          k += (int64_t)gridDim.x * blockDim.x) {
         const double y = in[k];
         if (dtype == CARBON_F32) static_cast<float *>(out)[k] = __double2float_rn(y);
+        else if (dtype == CARBON_F16) static_cast<unsigned short *>(out)[k] = exact_round_f16(y);
         else static_cast<unsigned short *>(out)[k] = exact_round_bf16(y);
     }
 }
@@ -322,9 +358,9 @@ carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream
     a.tiles_n = (p.cols + kBN - 1) / kBN;
     const int64_t tiles = tiles_m * a.tiles_n;
     if (tiles > 0x7fffffff) return CARBON_ERR_INVALID_ARG;
-    const cudaError_t err = (p.dtype == CARBON_F32)
-        ? launch_dtype<CARBON_F32>(p.pass, a, tiles, out_f64, stream)
-        : launch_dtype<CARBON_BF16>(p.pass, a, tiles, out_f64, stream);
+    const cudaError_t err = (p.dtype == CARBON_F32)   ? launch_dtype<CARBON_F32>(p.pass, a, tiles, out_f64, stream)
+                          : (p.dtype == CARBON_F16) ? launch_dtype<CARBON_F16>(p.pass, a, tiles, out_f64, stream)
+                                                    : launch_dtype<CARBON_BF16>(p.pass, a, tiles, out_f64, stream);
     count_launch();
     return note_cuda(err);
 }

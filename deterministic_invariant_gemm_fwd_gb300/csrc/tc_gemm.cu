@@ -46,6 +46,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <mutex>
 
@@ -91,10 +92,16 @@ struct Smem {
     static_assert(kBM * kPartialPitch * 4 <= kPipeBytes, "partial tile must fit the ring");
 };
 
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B,
+// The kernels' operand and output types: bf16 operands and output, bf16
+// operands with the fp32 accumulator stored (inspection path), fp16
+// operands and output.
+enum OutType { OT_BF16 = 0, OT_F32 = 1, OT_F16 = 2 };
+
+// Instruction descriptor, kind::f16: fp32 accumulate, A and B both bf16 or
+// both fp16 (one format field value for both, so they can never differ),
 // majorness of A and B, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t instr_desc(int bn, int a_major, int b_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_major << 15) |
+__host__ __device__ constexpr uint32_t instr_desc(int bn, int a_major, int b_major, bool f16) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((uint32_t)a_major << 15) |
            ((uint32_t)b_major << 16) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
@@ -166,6 +173,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);                 // RNE, one rounding each
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Two fp32 values rounded to the output type and packed (bf16 or fp16).
+template <int OT>
+__device__ __forceinline__ uint32_t pack_out(float lo, float hi) {
+    return OT == OT_F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+// A 16-bit bias element of the operand type, widened to fp32 (exactly).
+template <int OT>
+__device__ __forceinline__ float bias_value(const void *bias, int64_t j) {
+    const unsigned short h = static_cast<const unsigned short *>(bias)[j];
+    return OT == OT_F16 ? __half2float(__ushort_as_half(h)) : __uint_as_float((uint32_t)h << 16);
+}
+
 // ---- the roles shared by both kernels -----------------------------------------
 
 struct Bars {
@@ -217,11 +242,11 @@ __device__ __forceinline__ void drain_producer(const Bars &bar, int s, uint32_t 
 }
 
 // MMA issuer: nkb k-blocks from the ring into the accumulator at TMEM column d.
-template <int BN, int A_MAJOR, int B_MAJOR>
+template <int BN, int A_MAJOR, int B_MAJOR, bool F16>
 __device__ __forceinline__ bool mma_tile(uint32_t d, uint32_t sbase, const Bars &bar, int nkb,
                                          int &s, uint32_t &ph, volatile uint32_t *abort_flag) {
     using L = Smem<BN>;
-    constexpr uint32_t idesc = instr_desc(BN, A_MAJOR, B_MAJOR);
+    constexpr uint32_t idesc = instr_desc(BN, A_MAJOR, B_MAJOR, F16);
     for (int kb = 0; kb < nkb; ++kb) {
         if (!wait_or_abort(bar.full(s), ph, abort_flag)) return false;
         tc_fence_after();
@@ -266,11 +291,12 @@ __device__ __forceinline__ uint32_t setup_cta(uint8_t *smem, const Bars &bar,
 
 // ---- persistent kernel (fwd, dX, dW without split) ----------------------------
 
-template <int BN, int A_MAJOR, int B_MAJOR, bool OUT_F32>
+template <int BN, int A_MAJOR, int B_MAJOR, int OT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const __grid_constant__ CUtensorMap map_out, const TcArgs p) {
     using L = Smem<BN>;
+    constexpr bool OUT_F32 = OT == OT_F32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -306,8 +332,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
                 if (!wait_or_abort(bar.tempty(acc), aph ^ 1u, abort_flag)) break;
                 tc_fence_after();
-                if (!mma_tile<BN, A_MAJOR, B_MAJOR>(tmem_base + (uint32_t)(acc * BN), sbase, bar,
-                                                    p.num_kb, s, ph, abort_flag))
+                if (!mma_tile<BN, A_MAJOR, B_MAJOR, OT == OT_F16>(tmem_base + (uint32_t)(acc * BN), sbase,
+                                                                  bar, p.num_kb, s, ph, abort_flag))
                     break;
                 mma_commit(bar.tfull(acc));            // accumulator ready
                 if (++acc == 2) { acc = 0; aph ^= 1u; }
@@ -319,7 +345,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         const int quarter = warp % 4;                    // TMEM lanes 32*quarter .. +31
         const uint32_t stg = sbase + L::kStagingOffset + ew * 4096;
         float *bias_s = reinterpret_cast<float *>(smem + L::kBiasOffset) + ew * BN;
-        const __nv_bfloat16 *bias = static_cast<const __nv_bfloat16 *>(p.bias);
+        const void *bias = p.bias;
         int acc = 0, nstores = 0;
         uint32_t aph = 0;
         for (int t = blockIdx.x; t < num_tiles && !aborted(abort_flag); t += gridDim.x) {
@@ -328,7 +354,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             if (bias) {                                   // this warp's copy of the tile's bias
                 __syncwarp();                             // the previous tile's reads are done
                 for (int i = lane; i < BN; i += 32)
-                    bias_s[i] = (n0 + i < p.cols) ? __bfloat162float(bias[n0 + i]) : 0.0f;
+                    bias_s[i] = (n0 + i < p.cols) ? bias_value<OT>(bias, n0 + i) : 0.0f;
                 __syncwarp();
             }
             if (!wait_or_abort(bar.tfull(acc), aph, abort_flag)) break;
@@ -370,10 +396,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         uint4 w;
-                        w.x = pack_bf16x2(f[8 * g + 0], f[8 * g + 1]);
-                        w.y = pack_bf16x2(f[8 * g + 2], f[8 * g + 3]);
-                        w.z = pack_bf16x2(f[8 * g + 4], f[8 * g + 5]);
-                        w.w = pack_bf16x2(f[8 * g + 6], f[8 * g + 7]);
+                        w.x = pack_out<OT>(f[8 * g + 0], f[8 * g + 1]);
+                        w.y = pack_out<OT>(f[8 * g + 2], f[8 * g + 3]);
+                        w.z = pack_out<OT>(f[8 * g + 4], f[8 * g + 5]);
+                        w.w = pack_out<OT>(f[8 * g + 6], f[8 * g + 7]);
                         st_shared_v4(buf + lane * 64 + 16 * (g ^ ((lane >> 1) & 3)), w);
                     }
                     fence_proxy_async_smem();
@@ -403,11 +429,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
 // ---- dW with few tiles: token range split over a cluster --------------------
 
-template <int BN, bool OUT_F32>
+template <int BN, int OT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const TcArgs p) {
     using L = Smem<BN>;
+    constexpr bool OUT_F32 = OT == OT_F32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -444,7 +471,7 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         if (lane == 0 && nkb > 0) {
             int s = 0;
             uint32_t ph = 0;
-            if (mma_tile<BN, MN_MAJOR, MN_MAJOR>(tmem_base, sbase, bar, nkb, s, ph, abort_flag))
+            if (mma_tile<BN, MN_MAJOR, MN_MAJOR, OT == OT_F16>(tmem_base, sbase, bar, nkb, s, ph, abort_flag))
                 mma_commit(bar.tfull(0));
         }
     } else {
@@ -496,9 +523,9 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + grow * p.cols + gcol) = a;
         } else {
             uint2 w;
-            w.x = pack_bf16x2(a.x, a.y);
-            w.y = pack_bf16x2(a.z, a.w);
-            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) + grow * p.cols + gcol) = w;
+            w.x = pack_out<OT>(a.x, a.y);
+            w.y = pack_out<OT>(a.z, a.w);
+            *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(p.out) + grow * p.cols + gcol) = w;
         }
     }
     cluster_sync_all();                                    // peers are done reading this CTA
@@ -509,22 +536,23 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 }
 
 // Fills an output whose reduction is empty: bias (fwd) or +0.
-template <bool OUT_F32>
+template <int OT>
 __global__ void tc_fill_kernel(void *out, const void *bias, int64_t rows, int64_t cols) {
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const float v = bias ? __bfloat162float(static_cast<const __nv_bfloat16 *>(bias)[i % cols]) : 0.0f;
-        if (OUT_F32) static_cast<float *>(out)[i] = v;
-        else static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
+        const float v = bias ? bias_value<OT>(bias, i % cols) : 0.0f;
+        if (OT == OT_F32) static_cast<float *>(out)[i] = v;
+        else static_cast<unsigned short *>(out)[i] = (unsigned short)(pack_out<OT>(v, 0.0f) & 0xffffu);
     }
 }
 
 // ---- host side ----------------------------------------------------------------
 
-// 2-D bf16 tensor map over a row-major [outer, inner] matrix with a
-// {box_inner, box_outer} box; out-of-range elements read as 0 and are not
-// written by stores.
+// 2-D tensor map of 16-bit elements (bf16, also used for fp16 data: the
+// copies move bytes, and the fill of 0x0000 is +0 in both formats) over a
+// row-major [outer, inner] matrix with a {box_inner, box_outer} box;
+// out-of-range elements read as 0 and are not written by stores.
 bool encode_map(CUtensorMap *map, const void *base, int64_t inner, int64_t outer, int box_inner,
                 int box_outer, CUtensorMapSwizzle swizzle) {
     return encode_tensor_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, (uint64_t)inner,
@@ -541,10 +569,10 @@ cudaError_t prepare(Kern kern, int smem) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-template <int BN, int AM, int BM_, bool F32>
+template <int BN, int AM, int BM_, int OT>
 cudaError_t launch_persistent(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mo,
                               const TcArgs &a, int grid, cudaStream_t stream) {
-    auto kern = tc_gemm_kernel<BN, AM, BM_, F32>;
+    auto kern = tc_gemm_kernel<BN, AM, BM_, OT>;
     const int smem = (int)Smem<BN>::kDynamic;
     cudaError_t err = prepare(kern, smem);
     if (err != cudaSuccess) return err;
@@ -552,20 +580,28 @@ cudaError_t launch_persistent(const CUtensorMap &ma, const CUtensorMap &mb, cons
     return cudaGetLastError();
 }
 
-template <int BN, bool F32>
+template <int BN, int OT>
 cudaError_t launch_persistent_pass(int pass, const CUtensorMap &ma, const CUtensorMap &mb,
                                    const CUtensorMap &mo, const TcArgs &a, int grid, cudaStream_t s) {
     switch (pass) {
-    case CARBON_PASS_FWD: return launch_persistent<BN, K_MAJOR, MN_MAJOR, F32>(ma, mb, mo, a, grid, s);
-    case CARBON_PASS_DX:  return launch_persistent<BN, K_MAJOR, K_MAJOR, F32>(ma, mb, mo, a, grid, s);
-    default:              return launch_persistent<BN, MN_MAJOR, MN_MAJOR, F32>(ma, mb, mo, a, grid, s);
+    case CARBON_PASS_FWD: return launch_persistent<BN, K_MAJOR, MN_MAJOR, OT>(ma, mb, mo, a, grid, s);
+    case CARBON_PASS_DX:  return launch_persistent<BN, K_MAJOR, K_MAJOR, OT>(ma, mb, mo, a, grid, s);
+    default:              return launch_persistent<BN, MN_MAJOR, MN_MAJOR, OT>(ma, mb, mo, a, grid, s);
     }
 }
 
-template <int BN, bool F32>
+template <int OT>
+cudaError_t launch_persistent_bn(int bn, int pass, const CUtensorMap &ma, const CUtensorMap &mb,
+                                 const CUtensorMap &mo, const TcArgs &a, int grid, cudaStream_t s) {
+    if (bn == 128) return launch_persistent_pass<128, OT>(pass, ma, mb, mo, a, grid, s);
+    if (bn == 192) return launch_persistent_pass<192, OT>(pass, ma, mb, mo, a, grid, s);
+    return launch_persistent_pass<256, OT>(pass, ma, mb, mo, a, grid, s);
+}
+
+template <int BN, int OT>
 cudaError_t launch_split(const CUtensorMap &ma, const CUtensorMap &mb, const TcArgs &a,
                          cudaStream_t stream) {
-    auto kern = tc_dw_split_kernel<BN, F32>;
+    auto kern = tc_dw_split_kernel<BN, OT>;
     const int smem = (int)Smem<BN>::kDynamic;
     cudaError_t err = prepare(kern, smem);
     if (err != cudaSuccess) return err;
@@ -584,7 +620,6 @@ cudaError_t launch_split(const CUtensorMap &ma, const CUtensorMap &mb, const TcA
     return cudaLaunchKernelEx(&cfg, kern, ma, mb, a);
 }
 
-// Output-tile width from the output column count only (never from M).
 // Output tile width from the column count and the pass only (never the row
 // count, so a row's tiles, and its bits, do not depend on the batch): 128 for
 // at most 128 columns; otherwise 256, or 192 when that fills the SMs better
@@ -630,8 +665,9 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
     if (p.R == 0) {
         const int64_t n = p.rows * p.cols;
         const int blocks = (int)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535);
-        if (out_f32) tc_fill_kernel<true><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
-        else tc_fill_kernel<false><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
+        if (out_f32) tc_fill_kernel<OT_F32><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
+        else if (p.dtype == CARBON_F16) tc_fill_kernel<OT_F16><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
+        else tc_fill_kernel<OT_BF16><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
         count_launch();
         return note_cuda(cudaGetLastError());
     }
@@ -677,22 +713,22 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
         if (a.splits > a.num_kb) a.splits = 1;
         a.kb_per_split = (a.num_kb + a.splits - 1) / a.splits;
     }
+    // operand / output type: the fp32 inspection path takes bf16 operands
+    const int ot = out_f32 ? OT_F32 : (p.dtype == CARBON_F16 ? OT_F16 : OT_BF16);
     if (a.splits > 1) {
         if (bn == 128)
-            err = out_f32 ? launch_split<128, true>(ma, mb, a, stream) : launch_split<128, false>(ma, mb, a, stream);
+            err = ot == OT_F32 ? launch_split<128, OT_F32>(ma, mb, a, stream)
+                : ot == OT_F16 ? launch_split<128, OT_F16>(ma, mb, a, stream)
+                               : launch_split<128, OT_BF16>(ma, mb, a, stream);
         else
-            err = out_f32 ? launch_split<256, true>(ma, mb, a, stream) : launch_split<256, false>(ma, mb, a, stream);
+            err = ot == OT_F32 ? launch_split<256, OT_F32>(ma, mb, a, stream)
+                : ot == OT_F16 ? launch_split<256, OT_F16>(ma, mb, a, stream)
+                               : launch_split<256, OT_BF16>(ma, mb, a, stream);
     } else {
         const int grid = (int)(tiles < sms ? tiles : sms);
-        if (bn == 128)
-            err = out_f32 ? launch_persistent_pass<128, true>(p.pass, ma, mb, mo, a, grid, stream)
-                          : launch_persistent_pass<128, false>(p.pass, ma, mb, mo, a, grid, stream);
-        else if (bn == 192)
-            err = out_f32 ? launch_persistent_pass<192, true>(p.pass, ma, mb, mo, a, grid, stream)
-                          : launch_persistent_pass<192, false>(p.pass, ma, mb, mo, a, grid, stream);
-        else
-            err = out_f32 ? launch_persistent_pass<256, true>(p.pass, ma, mb, mo, a, grid, stream)
-                          : launch_persistent_pass<256, false>(p.pass, ma, mb, mo, a, grid, stream);
+        err = ot == OT_F32 ? launch_persistent_bn<OT_F32>(bn, p.pass, ma, mb, mo, a, grid, stream)
+            : ot == OT_F16 ? launch_persistent_bn<OT_F16>(bn, p.pass, ma, mb, mo, a, grid, stream)
+                           : launch_persistent_bn<OT_BF16>(bn, p.pass, ma, mb, mo, a, grid, stream);
     }
     count_launch();
     return note_cuda(err);

@@ -20,8 +20,8 @@ values combined with KBN, one rounding), so it is bit-identical run to run,
 for every batch split into the same tokens, and to the CPU oracle.
 
 Leading dimensions of the input are flattened into the token dimension.
-There is no CPU path: inputs must be CUDA tensors (float32 or bfloat16; the
-tensor-core tier takes bfloat16).
+There is no CPU path: inputs must be CUDA tensors (float32, bfloat16 or
+float16; the tensor-core tier takes bfloat16 or float16).
 """
 from __future__ import annotations
 
@@ -29,7 +29,7 @@ import math
 
 import torch
 
-from . import carbon_gemm_dw, linear_dw, linear_dx, linear_fwd
+from . import _dtype_code, carbon_gemm_dw, linear_dw, linear_dx, linear_fwd
 
 
 def bias_grad(dY, stream=None):
@@ -41,8 +41,7 @@ def bias_grad(dY, stream=None):
     M, N = dY.shape
     ones = torch.ones((M, 1), dtype=dY.dtype, device=dY.device)
     db = torch.empty((1, N), dtype=dY.dtype, device=dY.device)
-    dtype = "f32" if dY.dtype == torch.float32 else "bf16"
-    carbon_gemm_dw(db, ones, dY, M, 1, N, dtype, "exact", stream)
+    carbon_gemm_dw(db, ones, dY, M, 1, N, _dtype_code(dY), "exact", stream)
     return db.view(N)
 
 

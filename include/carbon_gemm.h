@@ -16,7 +16,7 @@
  * Two tiers (tier argument):
  *
  * CARBON_TIER_EXACT - every product is formed in float64 (exactly: products
- *   of two fp32 or two bf16 values fit in binary64), and products are summed
+ *   of two fp32, two bf16 or two fp16 values fit in binary64), and products are summed
  *   with Kahan-Babushka-Neumaier compensation in a fixed order (Carbon
  *   README, "How It Works": tiles, upcast to float64, KBN compensation in a
  *   fixed order).  The order depends only on the reduction length R (K for
@@ -24,20 +24,23 @@
  *   chunk is summed left to right with KBN and contributes the single double
  *   fl(s + c); the chunk values are combined left to right with KBN again.
  *   The forward pass adds the bias once in float64.  The float64 value is
- *   rounded once, to nearest-even, to fp32 or bf16 (the RNE downcast of
+ *   rounded once, to nearest-even, to fp32, bf16 or fp16 (the RNE downcast of
  *   sgemm-bi's "Determinism contracts").  The result is a pure function of
  *   the inputs' bits: identical on every run, for every M, on every device,
  *   and identical to a plain CPU implementation of the same steps.
- *   Accepts CARBON_F32 and CARBON_BF16, any shape, any element alignment.
+ *   Accepts CARBON_F32, CARBON_BF16 and CARBON_F16, any shape, any element
+ *   alignment.
  *
- * CARBON_TIER_TC - bf16 x bf16 products accumulated in fp32 on the tensor
- *   cores (tcgen05, accumulators in tensor memory), with a K schedule that
+ * CARBON_TIER_TC - bf16 x bf16 (or fp16 x fp16) products accumulated in
+ *   fp32 on the tensor cores (tcgen05, accumulators in tensor memory), with a
+ *   K schedule that
  *   depends only on the shape of the reduction and the output columns, never
  *   on the batch size of fwd/dX (sgemm-bi, "Determinism contracts", tensor
  *   core tier: fixed tile families, shape-only dispatch).  fwd adds the bias
- *   in fp32; the fp32 value is rounded once, to nearest-even, to bf16.
- *   Bit-identical run to run; fwd and dX rows are bit-identical for every M.
- *   Accepts CARBON_BF16 only (CARBON_F32 -> CARBON_ERR_UNSUPPORTED).  Base
+ *   in fp32; the fp32 value is rounded once, to nearest-even, to the input
+ *   type.  Bit-identical run to run; fwd and dX rows are bit-identical for
+ *   every M.  Accepts CARBON_BF16 and CARBON_F16 (CARBON_F32 ->
+ *   CARBON_ERR_UNSUPPORTED).  Base
  *   pointers must be 16-byte aligned and K and N multiples of 8 (16-byte row
  *   pitch), else CARBON_ERR_MISALIGNED.
  *
@@ -51,8 +54,8 @@
  *     memory pool with
  *     cudaMallocAsync on `stream` and released with cudaFreeAsync on `stream`
  *     before the call returns.  If the pool cannot supply it the call returns
- *     CARBON_ERR_CUDA and enqueues nothing.  The fp32 exact tier and the TC
- *     tier use no workspace.
+ *     CARBON_ERR_CUDA and enqueues nothing.  The fp32 and fp16 exact tier and
+ *     the TC tier use no workspace.
  *   - Calls are asynchronous: they validate, enqueue the kernels on `stream`
  *     and return.  Argument errors are returned synchronously and nothing is
  *     enqueued.  Errors raised while kernels run are reported by
@@ -85,12 +88,13 @@ typedef enum { CARBON_PASS_FWD = 0, CARBON_PASS_DX = 1, CARBON_PASS_DW = 2 } car
 
 typedef enum {
     CARBON_F32 = 0,     /* IEEE binary32 */
-    CARBON_BF16 = 1     /* bfloat16 (top 16 bits of binary32) */
+    CARBON_BF16 = 1,    /* bfloat16 (top 16 bits of binary32) */
+    CARBON_F16 = 2      /* IEEE binary16 (sgemm-bi lists float16 among its dtypes, "Use") */
 } carbon_dtype_t;
 
 typedef enum {
     CARBON_TIER_EXACT = 0,  /* float64 products, fixed-order KBN, one RNE */
-    CARBON_TIER_TC = 1      /* bf16 tcgen05 MMA, fp32 accumulate */
+    CARBON_TIER_TC = 1      /* bf16 or fp16 tcgen05 MMA, fp32 accumulate */
 } carbon_tier_t;
 
 typedef enum {

@@ -35,7 +35,8 @@ carbon_status_t carbon_debug_tc_f32(carbon_pass_t pass, float *acc,
                                     carbon_stream_t stream);
 
 /* The exact tier's device-side output rounding applied to n float64 values
- * (out: fp32 or bf16 elements), to check it against round-to-nearest-even. */
+ * (out: fp32, bf16 or fp16 elements), to check it against
+ * round-to-nearest-even. */
 carbon_status_t carbon_debug_round(carbon_dtype_t dtype, void *out, const double *in,
                                    int64_t n, carbon_stream_t stream);
 

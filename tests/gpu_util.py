@@ -2,12 +2,13 @@
 import numpy as np
 
 
-def dev(a, device="cuda"):
-    """numpy fp32 array or uint16 bf16-bit array -> CUDA tensor."""
+def dev(a, device="cuda", f16=False):
+    """numpy fp32 array, or uint16 bit array of bf16 (or of fp16 when f16) ->
+    CUDA tensor."""
     import torch
     a = np.ascontiguousarray(a)
     if a.dtype == np.uint16:
-        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.float16 if f16 else torch.bfloat16)
     return torch.from_numpy(a).to(device)
 
 
@@ -15,7 +16,7 @@ def host_bits(t):
     """CUDA tensor -> numpy array of its raw bits (uint16/uint32/uint64)."""
     import torch
     t = t.detach().contiguous().cpu()
-    if t.dtype == torch.bfloat16:
+    if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).numpy().view(np.uint16)
     if t.dtype == torch.float32:
         return t.view(torch.int32).numpy().view(np.uint32)
@@ -32,4 +33,4 @@ def bits(a):
 
 def torch_dtype(dtype):
     import torch
-    return torch.float32 if dtype == "f32" else torch.bfloat16
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]

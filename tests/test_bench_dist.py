@@ -66,15 +66,20 @@ def test_reference_arm_prints_on_rank_zero_only(capsys):
 
 
 def test_recorded_traffic_needs_matching_sources(tmp_path, monkeypatch):
-    """A traffic figure is reported only with the source hash it was taken on."""
+    """A traffic figure is reported only with the hash of the kernel's
+    sources it was taken on."""
+    files = bench.KERNEL_SOURCES["exact_tc_kernel"]
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "k.md").write_text(f"traffic some_kernel bytes_per_launch=1234 csrc_sha256={bench.csrc_sha256()}\n"
-                               "traffic other_kernel bytes_per_launch=99 csrc_sha256=0000\n")
+    (prof / "k.md").write_text(
+        f"traffic exact_tc_kernel bytes_per_launch=1234 sources_sha256={bench.sources_sha256(files)}\n"
+        "traffic tc_tier bytes_per_launch=99 sources_sha256=0000\n")
     csrc = os.path.join(bench.ROOT, "deterministic_invariant_gemm_fwd_gb300", "csrc")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "deterministic_invariant_gemm_fwd_gb300").mkdir()
     os.symlink(csrc, tmp_path / "deterministic_invariant_gemm_fwd_gb300" / "csrc")
-    assert bench.recorded_traffic("some_kernel") == 1234
-    assert bench.recorded_traffic("other_kernel") is None
+    assert bench.recorded_traffic("exact_tc_kernel") == 1234
+    assert bench.recorded_traffic("tc_tier") is None
     assert bench.recorded_traffic("missing") is None
+    # one changed byte in one of the kernel's files changes the hash
+    assert bench.sources_sha256(files, lambda n: b"x") != bench.sources_sha256(files)
