@@ -8,6 +8,7 @@
 
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 namespace carbon {
@@ -85,10 +86,34 @@ carbon_status_t check_args(const Problem &p, int tier, bool *nothing_to_do) {
     return CARBON_OK;
 }
 
+// Host-side fault injection, for tests of a caller's error handling: the
+// environment variable CARBON_FAULT holds a comma-separated list of fault
+// names; "launch" makes every GEMM call fail after its argument checks with
+// CARBON_ERR_CUDA, as a failed launch would, enqueuing nothing and touching
+// no device.  Read at each call; off when unset.
+bool fault_injected(const char *name) {
+    const char *v = std::getenv("CARBON_FAULT");
+    if (v == nullptr) return false;
+    const size_t n = std::strlen(name);
+    for (const char *q = v; *q;) {
+        const char *end = std::strchr(q, ',');
+        const size_t len = end ? (size_t)(end - q) : std::strlen(q);
+        if (len == n && std::strncmp(q, name, n) == 0) return true;
+        if (!end) break;
+        q = end + 1;
+    }
+    return false;
+}
+
 carbon_status_t run(const Problem &p, int tier, int debug_out, carbon_stream_t stream) {
     bool nothing = false;
     carbon_status_t st = check_args(p, tier, &nothing);
     if (st != CARBON_OK || nothing) return st;
+    if (fault_injected("launch")) {
+        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
+                      "injected launch failure (CARBON_FAULT=launch)");
+        return CARBON_ERR_CUDA;
+    }
     st = current_device(nullptr, nullptr);
     if (st != CARBON_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -68,6 +68,12 @@
  *   - The output must not overlap any input (undefined result otherwise).
  *   - A current device other than compute capability 10.3 (GB300):
  *     CARBON_ERR_UNSUPPORTED.  There is no fallback path.
+ *   - Fault injection, for testing a caller's error handling: with the
+ *     environment variable CARBON_FAULT containing "launch" (a
+ *     comma-separated list), carbon_gemm_fwd/dx/dw fail after their argument
+ *     checks with CARBON_ERR_CUDA, as a failed launch would:
+ *     carbon_last_cuda_error() names the injection, nothing is enqueued and
+ *     no device is touched.
  *   - Thread-safe.
  */
 #ifndef CARBON_GEMM_H
