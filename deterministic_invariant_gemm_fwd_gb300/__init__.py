@@ -19,7 +19,7 @@ from ._binding import (CarbonError, carbon_abi_version, carbon_debug_exact_y64, 
                        carbon_debug_kernel_timing,
                        carbon_debug_launch_count, carbon_debug_round,
                        carbon_debug_tc_f32, carbon_debug_timeout_probe,
-                       carbon_gemm_dw, carbon_gemm_dx, carbon_gemm_fwd,
+                       carbon_gemm_dw, carbon_gemm_dw_f32, carbon_gemm_dx, carbon_gemm_fwd,
                        carbon_get_device_status, carbon_measure_fp64_rate,
                        carbon_measure_int_mac_rate,
                        carbon_status_string)
@@ -82,4 +82,20 @@ def linear_dw(X, dY, tier="exact", stream=None):
     N = dY.shape[1]
     dW = torch.empty((K, N), dtype=X.dtype, device=X.device)
     carbon_gemm_dw(dW, X, dY, M, K, N, _dtype_code(X), tier, stream)
+    return dW
+
+
+def linear_dw_f32(X, dY, tier="exact", stream=None):
+    """dW[K,N] in fp32 = X[M,K]^T . dY[M,N] for bf16 X and dY."""
+    import torch
+    _check2d("X", X)
+    _check2d("dY", dY)
+    if X.dtype != torch.bfloat16 or dY.dtype != torch.bfloat16:
+        raise TypeError("linear_dw_f32 takes bfloat16 operands")
+    M, K = X.shape
+    if dY.shape[0] != M:
+        raise ValueError("X and dY disagree on M")
+    N = dY.shape[1]
+    dW = torch.empty((K, N), dtype=torch.float32, device=X.device)
+    carbon_gemm_dw_f32(dW, X, dY, M, K, N, tier, stream)
     return dW

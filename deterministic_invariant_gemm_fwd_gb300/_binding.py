@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
         "carbon_gemm_fwd": [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp],
         "carbon_gemm_dx": [vp, vp, vp, i64, i64, i64, i32, i32, vp],
         "carbon_gemm_dw": [vp, vp, vp, i64, i64, i64, i32, i32, vp],
+        "carbon_gemm_dw_f32": [vp, vp, vp, i64, i64, i64, i32, vp],
         "carbon_get_device_status": [vp],
         "carbon_gemm_exact_bf16_noalloc": [i32, vp, vp, vp, vp, i64, i64, i64, vp],
         "carbon_debug_exact_y64": [i32, vp, vp, vp, vp, i64, i64, i64, i32, vp],
@@ -137,6 +138,13 @@ def carbon_gemm_dw(dW, X, dY, M, K, N, dtype, tier, stream=None) -> None:
     _check(lib.carbon_gemm_dw(_ptr(dW), _ptr(X), _ptr(dY), M, K, N,
                               _code(DTYPES, dtype), _code(TIERS, tier), _stream(stream)),
            "carbon_gemm_dw")
+
+
+def carbon_gemm_dw_f32(dW, X, dY, M, K, N, tier, stream=None) -> None:
+    """dW (fp32) = X^T.dY of bf16 operands: the exact tier's float64 value
+    rounded once to fp32, or the tensor-core tier's fp32 accumulator."""
+    _check(lib.carbon_gemm_dw_f32(_ptr(dW), _ptr(X), _ptr(dY), M, K, N, _code(TIERS, tier),
+                                  _stream(stream)), "carbon_gemm_dw_f32")
 
 
 def carbon_gemm_exact_bf16_noalloc(pass_, out, A, B, bias, M, K, N, stream=None) -> None:

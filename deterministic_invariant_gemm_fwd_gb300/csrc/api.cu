@@ -105,15 +105,20 @@ bool fault_injected(const char *name) {
     return false;
 }
 
+// CARBON_ERR_CUDA with the injection named, when "launch" is injected.
+carbon_status_t injected_launch_failure() {
+    if (!fault_injected("launch")) return CARBON_OK;
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
+                  "injected launch failure (CARBON_FAULT=launch)");
+    return CARBON_ERR_CUDA;
+}
+
 carbon_status_t run(const Problem &p, int tier, int debug_out, carbon_stream_t stream) {
     bool nothing = false;
     carbon_status_t st = check_args(p, tier, &nothing);
     if (st != CARBON_OK || nothing) return st;
-    if (fault_injected("launch")) {
-        std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
-                      "injected launch failure (CARBON_FAULT=launch)");
-        return CARBON_ERR_CUDA;
-    }
+    st = injected_launch_failure();
+    if (st != CARBON_OK) return st;
     st = current_device(nullptr, nullptr);
     if (st != CARBON_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -149,6 +154,33 @@ carbon_status_t carbon_gemm_dw(void *dW, const void *X, const void *dY, int64_t 
                                carbon_stream_t stream) {
     return carbon::run(make_problem(CARBON_PASS_DW, dtype, dW, X, dY, nullptr, M, K, N),
                        tier, 0, stream);
+}
+
+carbon_status_t carbon_gemm_dw_f32(float *dW, const void *X, const void *dY, int64_t M, int64_t K,
+                                   int64_t N, carbon_tier_t tier, carbon_stream_t stream) {
+    const carbon::Problem p = make_problem(CARBON_PASS_DW, CARBON_BF16, dW, X, dY, nullptr, M, K, N);
+    if (tier == CARBON_TIER_TC) return carbon::run(p, CARBON_TIER_TC, 1, stream);   // the fp32 accumulator
+    if (tier != CARBON_TIER_EXACT) return CARBON_ERR_INVALID_ARG;
+    // exact tier: the float64 value into a staging buffer, then one rounding to fp32
+    bool nothing = false;
+    carbon_status_t st = carbon::check_args(p, CARBON_TIER_EXACT, &nothing);
+    if (st != CARBON_OK || nothing) return st;
+    st = carbon::injected_launch_failure();
+    if (st != CARBON_OK) return st;
+    st = carbon::current_device(nullptr, nullptr);
+    if (st != CARBON_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t n = K * N;
+    double *y64 = nullptr;
+    cudaError_t err = cudaMallocAsync(reinterpret_cast<void **>(&y64), (size_t)n * sizeof(double), s);
+    if (err != cudaSuccess) return carbon::note_cuda(err);
+    carbon::Problem q = p;
+    q.out = y64;
+    st = carbon::run(q, CARBON_TIER_EXACT, 1, stream);
+    if (st == CARBON_OK) st = carbon::exact_round_launch(CARBON_F32, dW, y64, n, s);
+    const cudaError_t ferr = cudaFreeAsync(y64, s);
+    if (st == CARBON_OK && ferr != cudaSuccess) st = carbon::note_cuda(ferr);
+    return st;
 }
 
 carbon_status_t carbon_debug_exact_y64(carbon_pass_t pass, double *y64, const void *A,

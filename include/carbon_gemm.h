@@ -132,6 +132,20 @@ carbon_status_t carbon_gemm_dw(void *dW, const void *X, const void *dY,
                                carbon_dtype_t dtype, carbon_tier_t tier,
                                carbon_stream_t stream);
 
+/* Weight gradient of bf16 operands into an fp32 output (sgemm-bi's dW is
+ * f32-accumulated, "Determinism contracts"): dW[K,N] fp32 = X[M,K]^T . dY[M,N]
+ * with X and dY bf16.  CARBON_TIER_EXACT: the same float64 value as
+ * carbon_gemm_dw (fixed-order KBN), rounded once, to nearest-even, to fp32;
+ * it takes a float64 staging buffer of 8 bytes per output, on top of
+ * carbon_gemm_dw's workspace, from the stream-ordered pool (released before
+ * the call returns; CARBON_ERR_CUDA if the pool cannot supply it).
+ * CARBON_TIER_TC: the fp32 accumulator of the tensor-core kernels, the value
+ * carbon_gemm_dw would round to bf16.  Arguments, alignment and errors as for
+ * carbon_gemm_dw with CARBON_BF16. */
+carbon_status_t carbon_gemm_dw_f32(float *dW, const void *X, const void *dY,
+                                   int64_t M, int64_t K, int64_t N,
+                                   carbon_tier_t tier, carbon_stream_t stream);
+
 /* Exact tier, bf16, without any device allocation.  (No counterpart in the
  * source pages: this entry point exists for callers, not for the method.)
  *

@@ -48,3 +48,17 @@ def test_only_the_named_fault_is_injected(monkeypatch):
     st = b.lib.carbon_gemm_fwd(FAKE, FAKE, FAKE, None, 16, 16, 16, 1, 0, None)
     assert st != 0
     assert "injected" not in b.lib.carbon_last_cuda_error().decode()
+
+
+@pytest.mark.parametrize("tier", ["exact", "tc"])
+def test_dw_f32_injected_failure_is_reported(injected, tier):
+    with pytest.raises(cg.CarbonError) as err:
+        cg.carbon_gemm_dw_f32(FAKE, FAKE, FAKE, 16, 16, 16, tier, 0)
+    assert err.value.status == CUDA_ERR and "injected launch failure" in str(err.value)
+
+
+def test_dw_f32_argument_errors():
+    assert b.lib.carbon_gemm_dw_f32(FAKE, FAKE, FAKE, -1, 16, 16, 0, None) == INVALID
+    assert b.lib.carbon_gemm_dw_f32(FAKE, FAKE, FAKE, 16, 16, 16, 9, None) == INVALID
+    assert b.lib.carbon_gemm_dw_f32(None, FAKE, FAKE, 16, 16, 16, 0, None) == INVALID
+    assert b.lib.carbon_gemm_dw_f32(FAKE, FAKE, FAKE, 16, 0, 16, 0, None) == 0     # empty output
