@@ -320,3 +320,70 @@ def test_stress_rows_cancel_exactly_and_oracle_is_within_bound():
     terms = ex.term_matrices("dw", X, dY, "f32")
     for idx in np.ndindex(y64.shape):
         assert abs(Fraction(float(y64[idx]))) <= ex.kbn_bound(terms[idx])
+
+
+# --------------------------------------------------------------------------
+# The pins fail on plausible mistakes.  Each mutant is a copy of the oracle's
+# source with one planted mistake, compiled on the CPU into a temporary
+# folder; at least one closed form must reject it.
+
+MUTANTS = {
+    "inner_chunk_right_to_left": (
+        "for (r = q0; r < q1; ++r) {",
+        "for (r = q1 - 1; r >= q0; --r) {"),
+    "chunks_right_to_left": (
+        "for (q0 = 0; q0 < R; q0 += ORACLE_CHUNK) {",
+        "for (q0 = R > 0 ? ((R - 1) / ORACLE_CHUNK) * ORACLE_CHUNK : -1; q0 >= 0;"
+        " q0 -= ORACLE_CHUNK) {"),
+    "chunk_width_128": ("#define ORACLE_CHUNK 256", "#define ORACLE_CHUNK 128"),
+    "chunk_width_512": ("#define ORACLE_CHUNK 256", "#define ORACLE_CHUNK 512"),
+    "no_compensation_in_chunk": (
+        "kbn_step(&S, &C, s + c);", "kbn_step(&S, &C, s);"),
+    "pair_passed_to_outer_level": (
+        "kbn_step(&S, &C, s + c);", "kbn_step(&S, &C, s); kbn_step(&S, &C, c);"),
+    "kbn_branch_swapped": (
+        "if (fabs(*sum) >= fabs(x))", "if (fabs(*sum) < fabs(x))"),
+    "output_rounded_before_bias": (
+        "y = y + decode(jb->bias, jb->dtype, j);",
+        "y = (double)(float)y + decode(jb->bias, jb->dtype, j);"),
+    "bf16_rounded_through_fp32": (
+        "round_to_f16_bits(y) : round_to_bf16_bits(y);",
+        "round_to_f16_bits(y) : round_to_bf16_bits((double)(float)y);"),
+    "bf16_ties_away_from_zero": (
+        "n = nearbyint(a / quantum);         /* default mode: ties to even */\n    r = n * quantum;\n    if (r >= 0x1p128)",
+        "n = round(a / quantum);\n    r = n * quantum;\n    if (r >= 0x1p128)"),
+}
+
+
+def _mutant_rejected(lib_path):
+    import ctypes
+    lib = ctypes.CDLL(lib_path)
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    lib.oracle_gemm.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                                i64, i64, i64, vp, vp, ctypes.c_int]
+    lib.oracle_gemm.restype = ctypes.c_int
+    failed = []
+    for case, dtype, pass_ in (p.values for p in _golden_params()):
+        A, B, bias, (M, K, N) = _case_operands(case, pass_, dtype)
+        out = np.empty(oracle.out_shape(pass_, M, K, N),
+                       dtype=np.float32 if dtype == "f32" else np.uint16)
+        ptr = (lambda a: None if a is None else a.ctypes.data_as(vp))
+        rc = lib.oracle_gemm(oracle.PASSES[pass_], oracle.DTYPES[dtype], ptr(A), ptr(B),
+                             ptr(bias), M, K, N, ptr(out), None, 1)
+        assert rc == 0
+        if float(_as_f64(out, dtype).ravel()[0]) != float.fromhex(case["expect"]):
+            failed.append(case["name"])
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistakes(name, tmp_path):
+    import subprocess
+    src = open(oracle._SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found once"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    lib = str(tmp_path / f"lib{name}.so")
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", lib, str(path), "-lm"], check=True)
+    assert _mutant_rejected(lib), f"no closed form rejects the mutant {name}"
