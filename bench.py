@@ -65,7 +65,7 @@ def step_flops(M=TOKENS, layers=LAYERS):
 
 
 def make_host_layers(seed, M=TOKENS, layers=LAYERS):
-    from deterministic_invariant_gemm_fwd_gb300 import inputs
+    import seeded_inputs as inputs
     return inputs.gpt2(seed, M=M, layers=layers)
 
 
@@ -210,33 +210,38 @@ class ClockSampler:
 
 # ------------------------------------------------- fp32 exact tier (FP64 pipe)
 
-def fp32_exact_section(device, stream, fp64_rate, stress=True):
+def fp32_exact_section(device, stream, fp64_rate, stress=True, repeats=(7, 3)):
     """The fp32 workloads of the exact tier, which run the float64 KBN kernel
     on the FP64 pipe: the toy MLP's nine GEMMs (M = 512 tokens, fwd + dX +
     dW of (K, N) in {(256,512), (512,512), (512,256)}) and the cancellation
     stress dW (65536 tokens, K = 768, N = 3072).  Each is run once untimed,
-    then timed once with CUDA events on `stream`.  FP64 utilisation is the
+    then timed `repeats` times with CUDA events on `stream` (the median is
+    reported, with the spread).  FP64 utilisation is the
     literal algorithm's floor, 5 FP64 instructions per multiply-add (product,
     sum, two for the exact error, one for the compensation), over the time
     and the measured DFMA rate; the kernel folds the product into the sum's
     FMA and proves whole slices exact, so the figure can pass 1."""
     import torch
     import deterministic_invariant_gemm_fwd_gb300 as cg
-    from deterministic_invariant_gemm_fwd_gb300 import inputs
+    import seeded_inputs as inputs
 
-    def run(calls, macs):
+    def run(calls, macs, reps):
         for c in calls:
             c()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for c in calls:
-            c()
-        e1.record(stream)
-        stream.synchronize()
-        ms = e0.elapsed_time(e1)
+        times = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for c in calls:
+                c()
+            e1.record(stream)
+            stream.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
         mac_rate = macs / (ms * 1e-3)
-        return {"ms": _r(ms), "gflops": _r(2.0 * mac_rate / 1e9),
+        return {"ms": _r(ms), "ms_min_max": [_r(min(times)), _r(max(times))], "repeats": reps,
+                "gflops": _r(2.0 * mac_rate / 1e9),
                 "fp64_util_vs_literal": _r(5.0 * mac_rate / fp64_rate)}
 
     s = stream.cuda_stream
@@ -256,7 +261,7 @@ def fp32_exact_section(device, stream, fp64_rate, stress=True):
         macs += 3 * M * K * N
     torch.cuda.synchronize(device)
     with torch.cuda.stream(stream):
-        out["toy_mlp_9_gemms"] = run(calls, macs)
+        out["toy_mlp_9_gemms"] = run(calls, macs, repeats[0])
         if stress:
             S = inputs.stress_dw(SEED)
             M, K, N = S["M"], S["K"], S["N"]
@@ -265,7 +270,8 @@ def fp32_exact_section(device, stream, fp64_rate, stress=True):
             dW = torch.empty((K, N), dtype=torch.float32, device=device)
             torch.cuda.synchronize(device)
             out["stress_dw_65536x768x3072"] = run(
-                [lambda: cg.carbon_gemm_dw(dW, X, dY, M, K, N, "f32", "exact", s)], M * K * N)
+                [lambda: cg.carbon_gemm_dw(dW, X, dY, M, K, N, "f32", "exact", s)], M * K * N,
+                repeats[1])
             del X, dY, dW
     assert cg.carbon_get_device_status(s) == 0
     return out
@@ -277,7 +283,7 @@ def oracle_sample(host_layers, target_s, threads=None):
     """Time the oracle on a random sample of outputs of every exact-tier GEMM
     of the step.  Returns (useful GFLOP/s, seconds, sampled MACs, threads)."""
     import oracle
-    from deterministic_invariant_gemm_fwd_gb300 import inputs
+    import seeded_inputs as inputs
     threads = threads or oracle.default_threads()
 
     def run(per_gemm):
@@ -417,6 +423,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fp32", action="store_true",
                     help="skip the fp32 exact-tier section (toy MLP and cancellation stress)")
+    ap.add_argument("--fp32-only", action="store_true",
+                    help="profiling aid: run only the fp32 exact-tier section (toy MLP and, "
+                         "unless --no-stress, the cancellation stress dW) and print it")
+    ap.add_argument("--no-stress", action="store_true",
+                    help="with --fp32-only: leave out the cancellation stress dW")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the TC tier eagerly inside the timed region")
     ap.add_argument("--gemm", default=None,
@@ -441,6 +452,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
         pg = dist
+
+    if args.fp32_only:
+        stream = torch.cuda.Stream(device)
+        fp64_rate, _ = cg.carbon_measure_fp64_rate(stream.cuda_stream)
+        out = fp32_exact_section(device, stream, fp64_rate, stress=not args.no_stress)
+        if rank == 0:
+            print(json.dumps({"fp32_exact": out}), flush=True)
+        return
 
     tiers = ["exact", "tc"] if args.tiers == "auto" else args.tiers.split(",")
     if "tc" in tiers and not tc_available():

@@ -3,8 +3,10 @@
 Argument marshalling only: every step of the GEMMs runs in the library's
 CUDA kernels.  Functions take torch tensors (or raw integer device pointers)
 and the same arguments as the C entry points, and raise ``CarbonError`` on a
-status other than CARBON_OK.  There is no fallback: if the compiled library
-is missing, importing the binding raises.
+status other than CARBON_OK.  The library is loaded on the first call (or the
+first access to ``lib``), so importing the package maps no CUDA code; there
+is no fallback: if the compiled library is missing, that first call raises
+``ImportError``.
 """
 from __future__ import annotations
 
@@ -82,7 +84,21 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-lib = _load()
+_LIB = None
+
+
+def _lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name):
+    # ``_binding.lib`` loads the library on first access.
+    if name == "lib":
+        return _lib()
+    raise AttributeError(name)
 
 
 def declared_functions() -> list:
@@ -114,7 +130,7 @@ def _stream(stream) -> int | None:
 
 def _check(status: int, where: str) -> None:
     if status != 0:
-        detail = lib.carbon_last_cuda_error().decode() if status == 4 else ""
+        detail = _lib().carbon_last_cuda_error().decode() if status == 4 else ""
         raise CarbonError(status, where, detail)
 
 
@@ -123,19 +139,19 @@ def _code(table, v):
 
 
 def carbon_gemm_fwd(Y, X, W, bias, M, K, N, dtype, tier, stream=None) -> None:
-    _check(lib.carbon_gemm_fwd(_ptr(Y), _ptr(X), _ptr(W), _ptr(bias), M, K, N,
+    _check(_lib().carbon_gemm_fwd(_ptr(Y), _ptr(X), _ptr(W), _ptr(bias), M, K, N,
                                _code(DTYPES, dtype), _code(TIERS, tier), _stream(stream)),
            "carbon_gemm_fwd")
 
 
 def carbon_gemm_dx(dX, dY, W, M, K, N, dtype, tier, stream=None) -> None:
-    _check(lib.carbon_gemm_dx(_ptr(dX), _ptr(dY), _ptr(W), M, K, N,
+    _check(_lib().carbon_gemm_dx(_ptr(dX), _ptr(dY), _ptr(W), M, K, N,
                               _code(DTYPES, dtype), _code(TIERS, tier), _stream(stream)),
            "carbon_gemm_dx")
 
 
 def carbon_gemm_dw(dW, X, dY, M, K, N, dtype, tier, stream=None) -> None:
-    _check(lib.carbon_gemm_dw(_ptr(dW), _ptr(X), _ptr(dY), M, K, N,
+    _check(_lib().carbon_gemm_dw(_ptr(dW), _ptr(X), _ptr(dY), M, K, N,
                               _code(DTYPES, dtype), _code(TIERS, tier), _stream(stream)),
            "carbon_gemm_dw")
 
@@ -143,49 +159,49 @@ def carbon_gemm_dw(dW, X, dY, M, K, N, dtype, tier, stream=None) -> None:
 def carbon_gemm_dw_f32(dW, X, dY, M, K, N, tier, stream=None) -> None:
     """dW (fp32) = X^T.dY of bf16 operands: the exact tier's float64 value
     rounded once to fp32, or the tensor-core tier's fp32 accumulator."""
-    _check(lib.carbon_gemm_dw_f32(_ptr(dW), _ptr(X), _ptr(dY), M, K, N, _code(TIERS, tier),
+    _check(_lib().carbon_gemm_dw_f32(_ptr(dW), _ptr(X), _ptr(dY), M, K, N, _code(TIERS, tier),
                                   _stream(stream)), "carbon_gemm_dw_f32")
 
 
 def carbon_gemm_exact_bf16_noalloc(pass_, out, A, B, bias, M, K, N, stream=None) -> None:
     """Exact-tier bf16 GEMM that allocates no device memory (fixed 64 MiB
     library workspace); same bits as carbon_gemm_fwd/dx/dw with the exact tier."""
-    _check(lib.carbon_gemm_exact_bf16_noalloc(_code(PASSES, pass_), _ptr(out), _ptr(A), _ptr(B),
+    _check(_lib().carbon_gemm_exact_bf16_noalloc(_code(PASSES, pass_), _ptr(out), _ptr(A), _ptr(B),
                                               _ptr(bias), M, K, N, _stream(stream)),
            "carbon_gemm_exact_bf16_noalloc")
 
 
 def carbon_get_device_status(stream=None) -> int:
     """Synchronises the stream; returns the status code (does not raise)."""
-    return int(lib.carbon_get_device_status(_stream(stream)))
+    return int(_lib().carbon_get_device_status(_stream(stream)))
 
 
 def carbon_debug_exact_y64(pass_, y64, A, B, bias, M, K, N, dtype, stream=None) -> None:
-    _check(lib.carbon_debug_exact_y64(_code(PASSES, pass_), _ptr(y64), _ptr(A), _ptr(B),
+    _check(_lib().carbon_debug_exact_y64(_code(PASSES, pass_), _ptr(y64), _ptr(A), _ptr(B),
                                       _ptr(bias), M, K, N, _code(DTYPES, dtype),
                                       _stream(stream)), "carbon_debug_exact_y64")
 
 
 def carbon_debug_tc_f32(pass_, acc, A, B, bias, M, K, N, stream=None) -> None:
-    _check(lib.carbon_debug_tc_f32(_code(PASSES, pass_), _ptr(acc), _ptr(A), _ptr(B),
+    _check(_lib().carbon_debug_tc_f32(_code(PASSES, pass_), _ptr(acc), _ptr(A), _ptr(B),
                                    _ptr(bias), M, K, N, _stream(stream)),
            "carbon_debug_tc_f32")
 
 
 def carbon_debug_round(dtype, out, inp, n, stream=None) -> None:
-    _check(lib.carbon_debug_round(_code(DTYPES, dtype), _ptr(out), _ptr(inp), n,
+    _check(_lib().carbon_debug_round(_code(DTYPES, dtype), _ptr(out), _ptr(inp), n,
                                   _stream(stream)), "carbon_debug_round")
 
 
 def carbon_debug_timeout_probe(budget_ns: int, stream=None) -> None:
-    _check(lib.carbon_debug_timeout_probe(budget_ns, _stream(stream)),
+    _check(_lib().carbon_debug_timeout_probe(budget_ns, _stream(stream)),
            "carbon_debug_timeout_probe")
 
 
 def carbon_measure_fp64_rate(stream=None) -> tuple:
     """(DFMA lane-ops/s, DADD lane-ops/s) measured on the current device."""
     a, b = ctypes.c_double(), ctypes.c_double()
-    _check(lib.carbon_measure_fp64_rate(ctypes.byref(a), ctypes.byref(b), _stream(stream)),
+    _check(_lib().carbon_measure_fp64_rate(ctypes.byref(a), ctypes.byref(b), _stream(stream)),
            "carbon_measure_fp64_rate")
     return a.value, b.value
 
@@ -193,32 +209,32 @@ def carbon_measure_fp64_rate(stream=None) -> tuple:
 def carbon_measure_int_mac_rate(stream=None) -> float:
     """32x32->64-bit integer multiply-adds per second on the current device."""
     a = ctypes.c_double()
-    _check(lib.carbon_measure_int_mac_rate(ctypes.byref(a), _stream(stream)),
+    _check(_lib().carbon_measure_int_mac_rate(ctypes.byref(a), _stream(stream)),
            "carbon_measure_int_mac_rate")
     return a.value
 
 
 def carbon_status_string(status: int) -> str:
-    return lib.carbon_status_string(status).decode()
+    return _lib().carbon_status_string(status).decode()
 
 
 def carbon_abi_version() -> int:
-    return int(lib.carbon_abi_version())
+    return int(_lib().carbon_abi_version())
 
 
 def carbon_debug_launch_count() -> int:
-    return int(lib.carbon_debug_launch_count())
+    return int(_lib().carbon_debug_launch_count())
 
 
 def carbon_debug_kernel_timing(enable: bool) -> None:
     """Start (and clear) or stop event timing of the exact tier's tensor-core kernel."""
-    lib.carbon_debug_kernel_timing(1 if enable else 0)
+    _lib().carbon_debug_kernel_timing(1 if enable else 0)
 
 
 def carbon_debug_kernel_time():
     """(milliseconds, launches, plane products) recorded since timing was enabled."""
     ms, n, kg = ctypes.c_double(), ctypes.c_int64(), ctypes.c_int64()
-    _check(lib.carbon_debug_kernel_time(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(kg)),
+    _check(_lib().carbon_debug_kernel_time(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(kg)),
            "carbon_debug_kernel_time")
     return ms.value, int(n.value), int(kg.value)
 
@@ -226,6 +242,6 @@ def carbon_debug_kernel_time():
 def carbon_debug_exact_path_counts():
     """(chunk repairs, whole-output fix-ups) recorded since timing was enabled."""
     r, f = ctypes.c_int64(), ctypes.c_int64()
-    _check(lib.carbon_debug_exact_path_counts(ctypes.byref(r), ctypes.byref(f)),
+    _check(_lib().carbon_debug_exact_path_counts(ctypes.byref(r), ctypes.byref(f)),
            "carbon_debug_exact_path_counts")
     return int(r.value), int(f.value)

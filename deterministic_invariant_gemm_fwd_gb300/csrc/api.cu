@@ -105,6 +105,8 @@ bool fault_injected(const char *name) {
     return false;
 }
 
+}  // namespace
+
 // CARBON_ERR_CUDA with the injection named, when "launch" is injected.
 carbon_status_t injected_launch_failure() {
     if (!fault_injected("launch")) return CARBON_OK;
@@ -112,6 +114,8 @@ carbon_status_t injected_launch_failure() {
                   "injected launch failure (CARBON_FAULT=launch)");
     return CARBON_ERR_CUDA;
 }
+
+namespace {
 
 carbon_status_t run(const Problem &p, int tier, int debug_out, carbon_stream_t stream) {
     bool nothing = false;

@@ -48,6 +48,10 @@ void count_launch(int n = 1);
 // Checks that the current device is a GB300 (compute capability 10.3) and
 // returns its SM count.
 carbon_status_t current_device(int *device, int *sm_count);
+// Host-side fault injection: CARBON_ERR_CUDA (message names the injection)
+// when the environment variable CARBON_FAULT lists "launch", else CARBON_OK.
+// Every GEMM entry point calls it after its argument checks.
+carbon_status_t injected_launch_failure();
 
 // Exact tier (exact_kbn.cu).  out_f64 selects the float64 pre-rounding output.
 carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream);

@@ -45,6 +45,8 @@
 #include "exact_common.cuh"
 #include "exact_bf16.cuh"
 
+#include <cudaTypedefs.h>
+
 #include <cstring>
 #include <mutex>
 
@@ -564,38 +566,87 @@ carbon_status_t exact_take_device_status() {
 // loop, a watchdog), or a process where the stream-ordered pool is
 // unavailable.  For them carbon_gemm_exact_bf16_noalloc runs the same two
 // kernels as the bf16 exact tier above, with the workspace taken from a
-// fixed array in device memory that the library reserves when it is loaded.
+// fixed array in device memory.  The array belongs to this file's module,
+// which CUDA loads onto a device (reserving the array there) the first time
+// the module is used on that device -- under the default lazy module loading
+// that is the first no-allocation call on that device.  Callers whose
+// allocator later takes all free memory, or who capture streams, should make
+// one small call on each device beforehand.
 
 namespace carbon {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;   // 64 MiB per device
 
-// Fixed workspace of the no-allocation entry point.  Every GPU that loads
-// this library holds it until the process exits.  Host code must not use the
+// Fixed workspace of the no-allocation entry point.  Every GPU on which the
+// module has been loaded holds it until the process exits.  Host code must not use the
 // symbol as an address (it is a host-side stand-in); the device address comes
 // from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[128];
+// Driver calls that identify the current context, fetched through the
+// runtime (the library does not link libcuda).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (the first call on each device does this; it is not a stream
-// operation, but make that first call before any stream capture).
+void find_context_calls() {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+        g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+        g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+}
+
+struct ScratchSlot {
+    unsigned long long ctx_id;   // context the address belongs to (0 = none yet)
+    void *ptr;
+};
+std::mutex g_noalloc_mu;
+ScratchSlot g_noalloc_slot[128];
+
+// Unique id of the calling thread's current context, or 0 if none is current
+// or the driver cannot say.
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_once, find_context_calls);
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current && g_ctx_id && g_ctx_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+        g_ctx_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
+
+// Device address of g_noalloc_scratch in the current device's current
+// context.  It is looked up with cudaGetSymbolAddress once per device and
+// context: the first call on a device loads this file's module there (under
+// CUDA's default lazy loading), which is when the 64 MiB array is reserved,
+// and a new context (after cudaDeviceReset, say) gets a fresh lookup rather
+// than a stale address.  If the context cannot be identified the address is
+// looked up on every call (cheap once the module is loaded).
 cudaError_t noalloc_scratch(void **ptr) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    ScratchSlot &slot = g_noalloc_slot[dev];
+    if (id == 0 || slot.ctx_id != id || slot.ptr == nullptr) {
         void *p = nullptr;
         err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (err != cudaSuccess) return err;
-        g_noalloc_ptr[dev] = p;
+        // the lookup makes the device's primary context current if no
+        // context was, so ask again for the identity to cache it under
+        if (id == 0) id = current_context_id();
+        slot.ptr = p;
+        slot.ctx_id = id;
     }
-    *ptr = g_noalloc_ptr[dev];
+    *ptr = slot.ptr;
     return cudaSuccess;
 }
 
@@ -612,6 +663,10 @@ extern "C" carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, vo
     int64_t mk, kn, mn;
     if (__builtin_mul_overflow(M, K, &mk) || __builtin_mul_overflow(K, N, &kn) ||
         __builtin_mul_overflow(M, N, &mn))
+        return CARBON_ERR_INVALID_ARG;
+    int64_t bytes;   // byte counts must fit as well, as in the other entry points
+    if (__builtin_mul_overflow(mk, 8, &bytes) || __builtin_mul_overflow(kn, 8, &bytes) ||
+        __builtin_mul_overflow(mn, 8, &bytes))
         return CARBON_ERR_INVALID_ARG;
     const Problem p = make_problem(pass, CARBON_BF16, out, A, B, bias, M, K, N);
     const int64_t a_elems = (pass == CARBON_PASS_DX) ? mn : mk;
@@ -632,7 +687,9 @@ extern "C" carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, vo
                         16.0 * (double)nchunks * (double)(LpA + LpB) + 4.0 * ((double)out_elems + 1.0);
     if (need > (double)kNoAllocScratchBytes) return CARBON_ERR_SCRATCH_LIMIT;
 
-    carbon_status_t st = current_device(nullptr, nullptr);
+    carbon_status_t st = injected_launch_failure();
+    if (st != CARBON_OK) return st;
+    st = current_device(nullptr, nullptr);
     if (st != CARBON_OK) return st;
     void *scratch = nullptr;
     cudaError_t err = noalloc_scratch(&scratch);

@@ -47,15 +47,25 @@
  * Conventions
  *   - Pointers are DEVICE pointers on the current CUDA device; the caller
  *     owns every buffer.
- *   - Workspace: with CARBON_BF16 the exact tier converts its operands once
- *     into scaled int32 form in a workspace of about 4 bytes per operand
- *     element (plus 16 bytes per 256 reduction indices per output row and
- *     column, and 4 bytes per output), taken from the device's stream-ordered
- *     memory pool with
- *     cudaMallocAsync on `stream` and released with cudaFreeAsync on `stream`
- *     before the call returns.  If the pool cannot supply it the call returns
- *     CARBON_ERR_CUDA and enqueues nothing.  The fp32 and fp16 exact tier and
- *     the TC tier use no workspace.
+ *   - Workspace: with CARBON_BF16 the exact tier builds a workspace on each
+ *     call, taken from the device's stream-ordered memory pool with
+ *     cudaMallocAsync on `stream` and released with cudaFreeAsync on
+ *     `stream` before the call returns.  With R the reduction length (K, N
+ *     or M for fwd, dX, dW), Rp = R rounded up to a multiple of 256, rows and
+ *     cols the output's shape, La = rows rounded up to 128, Lb = cols rounded
+ *     up to 64, C = Rp / 256 chunks and P in {1, 2, 4, 8} pieces per output
+ *     (chosen from the tile and chunk counts), it takes about
+ *       8 * Rp * (La + Lb)          digit planes of both operands (four bf16
+ *                                   planes per element),
+ *     + 12 * rows * cols * P        int64 partial sums and the fix-up list,
+ *     + 12 * min(rows*cols*C, 2^22) chunk-repair list,
+ *     + 16 * C * (La + Lb)          statistics per operand line and chunk,
+ *     + 20 * (La + Lb)              line grains, row flags and row order
+ *     bytes; e.g. about 422 MB for fwd with M = 8192, K = 768, N = 3072, and
+ *     about 417 MB for dW of the same shapes.  If the pool cannot supply it
+ *     the call returns CARBON_ERR_CUDA and enqueues nothing.  The fp32 and
+ *     fp16 exact tier and the TC tier use no workspace (carbon_gemm_dw_f32's
+ *     exact tier adds an 8-byte float64 staging value per output).
  *   - Calls are asynchronous: they validate, enqueue the kernels on `stream`
  *     and return.  Argument errors are returned synchronously and nothing is
  *     enqueued.  Errors raised while kernels run are reported by
@@ -155,9 +165,14 @@ carbon_status_t carbon_gemm_dw_f32(float *dW, const void *X, const void *dY,
  * memory, latency-critical loops that must never block on or fail in an
  * allocator, or processes where the stream-ordered pool is unavailable.  The
  * workspace the bf16 exact tier needs comes instead from a fixed 64 MiB array
- * in device memory that the library reserves on every GPU that loads it,
- * until the process exits.  No cudaMalloc, cudaMallocAsync, cudaFree or other
- * allocating call is made.
+ * in device memory, part of the library's code module for this entry point.
+ * CUDA reserves it on a device when it loads that module there -- with the
+ * default lazy module loading, during the first call of this function on
+ * that device -- and keeps it until the process exits.  No cudaMalloc,
+ * cudaMallocAsync, cudaFree or other allocating call is made by the library;
+ * but if the caller's allocator will later hold all free device memory, make
+ * one small call (say M = K = N = 64) on each device before it does, so that
+ * the module and its array are already in place.
  *
  * pass: CARBON_PASS_FWD (A = X, B = W, bias allowed), CARBON_PASS_DX
  * (A = dY, B = W), CARBON_PASS_DW (A = X, B = dY); out, A, B, bias, M, K, N
@@ -168,8 +183,10 @@ carbon_status_t carbon_gemm_dw_f32(float *dW, const void *X, const void *dY,
  * column counts rounded up to multiples of 64, and rows*cols the output's size
  * (e.g. fwd with M = 8192, K = 768, N = 768 needs 52.8 MB);
  * larger problems return CARBON_ERR_SCRATCH_LIMIT and enqueue nothing.
- * The first call on each device looks the array's device address up (not a
- * stream operation); make that first call before any stream capture.  All
+ * The first call on each device (and the first after a new context, e.g.
+ * after cudaDeviceReset) looks the array's device address up (not a stream
+ * operation); make that first call before any stream capture.  Fault
+ * injection (CARBON_FAULT=launch) applies as to the other entry points.  All
  * calls share the array and it keeps the last call's contents; the one word
  * that must start at zero is cleared on `stream` by each call.  Calls whose kernels may overlap on the GPU (other
  * streams, other host threads) race on the array: order them on one stream. */
@@ -190,10 +207,11 @@ const char *carbon_status_string(carbon_status_t status);
  * ("" if none). */
 const char *carbon_last_cuda_error(void);
 
-/* ABI version of this header: (major << 16) | minor. */
+/* ABI version of this header: (major << 16) | minor.  Minor 1 added
+ * carbon_gemm_exact_bf16_noalloc and CARBON_ERR_SCRATCH_LIMIT. */
 int carbon_abi_version(void);
 
-#define CARBON_ABI_VERSION ((1 << 16) | 0)
+#define CARBON_ABI_VERSION ((1 << 16) | 1)
 
 #ifdef __cplusplus
 }

@@ -2,6 +2,7 @@
 function its headers declare, and rejects bad arguments before touching the
 device."""
 import ctypes
+import os
 
 import pytest
 
@@ -22,7 +23,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_status_names():
-    assert b.carbon_abi_version() >> 16 == 1
+    assert b.carbon_abi_version() == (1 << 16) | 1    # minor 1: the no-allocation entry point
     for code, name in b.STATUS.items():
         assert b.carbon_status_string(code) == name
 
@@ -78,3 +79,19 @@ def test_debug_round_validation():
     assert b.lib.carbon_debug_round(0, None, FAKE, 4, None) == INVALID
     assert b.lib.carbon_debug_round(0, None, None, 0, None) == 0
     assert b.lib.carbon_debug_timeout_probe(0, None) == INVALID
+
+
+def test_import_maps_no_cuda_library():
+    """Importing the package and the input generator loads no CUDA code: the
+    library is mapped on the first call only (so the oracle-only benchmark
+    arm never loads it)."""
+    import subprocess
+    import sys
+    code = ("import deterministic_invariant_gemm_fwd_gb300, seeded_inputs\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "assert 'libcarbon_gemm' not in maps, 'library mapped at import'\n"
+            "from deterministic_invariant_gemm_fwd_gb300 import _binding\n"
+            "_binding.carbon_abi_version()\n"
+            "assert 'libcarbon_gemm' in open('/proc/self/maps').read()\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    subprocess.run([sys.executable, "-c", code], check=True, cwd=root)

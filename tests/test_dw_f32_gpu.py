@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import oracle
-from deterministic_invariant_gemm_fwd_gb300 import inputs
+import seeded_inputs as inputs
 from tests.gpu_util import dev, host_bits
 
 pytestmark = pytest.mark.gpu

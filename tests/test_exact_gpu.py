@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
-from deterministic_invariant_gemm_fwd_gb300 import inputs
+import seeded_inputs as inputs
 from tests.gpu_util import bits, dev, host_bits, torch_dtype
 
 pytestmark = pytest.mark.gpu
@@ -112,6 +112,25 @@ def test_gpt2_full_size_sampled(seed):
             assert np.array_equal(out[rows, cols], ref), (li, pass_)
 
 
+@pytest.mark.slow
+def test_gpt2_full_size_dense():
+    """M = 8192, seed 42: every output of all 12 GEMMs (rounded and float64
+    before rounding) against the oracle.  The kernel's paths that depend on
+    the batch (row regrouping in 1024-row groups, the chunk range cut into
+    pieces, run-time work units) only run at sizes like these."""
+    for li, layer in enumerate(inputs.gpt2(42)):
+        M, K, N = layer["M"], layer["K"], layer["N"]
+        for pass_ in ("fwd", "dx", "dw"):
+            A, B, bias = layer_operands(layer, pass_)
+            ref, ref64 = oracle.gemm(pass_, "bf16", A, B, bias, M, K, N)
+            got = host_bits(gpu_pass(pass_, "bf16", A, B, bias, M, K, N))
+            assert np.array_equal(got, bits(ref)), \
+                (li, pass_, int(np.count_nonzero(got != bits(ref))))
+            got64 = host_bits(gpu_pass(pass_, "bf16", A, B, bias, M, K, N, f64=True))
+            assert np.array_equal(got64, bits(ref64)), \
+                (li, pass_, int(np.count_nonzero(got64 != bits(ref64))))
+
+
 # ---------------------------------------------------------- stress (dW only)
 
 def test_stress_dw_full_size_sampled():
@@ -123,6 +142,18 @@ def test_stress_dw_full_size_sampled():
     ref, ref64 = oracle.gemm_at("dw", "f32", d["X"], d["dY"], None, M, K, N, rows, cols)
     assert np.array_equal(host_bits(out)[rows, cols], bits(ref))
     assert np.array_equal(host_bits(out64)[rows, cols], bits(ref64))
+
+
+@pytest.mark.slow
+def test_stress_dw_full_size_dense():
+    """65536 tokens, K = 768, N = 3072: every output against the oracle."""
+    d = inputs.stress_dw(42)
+    M, K, N = d["M"], d["K"], d["N"]
+    ref, ref64 = oracle.gemm("dw", "f32", d["X"], d["dY"], None, M, K, N)
+    got = host_bits(gpu_pass("dw", "f32", d["X"], d["dY"], None, M, K, N))
+    assert np.array_equal(got, bits(ref)), int(np.count_nonzero(got != bits(ref)))
+    got64 = host_bits(gpu_pass("dw", "f32", d["X"], d["dY"], None, M, K, N, f64=True))
+    assert np.array_equal(got64, bits(ref64)), int(np.count_nonzero(got64 != bits(ref64)))
 
 
 def test_stress_dw_reduced_dense():

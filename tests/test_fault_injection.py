@@ -62,3 +62,23 @@ def test_dw_f32_argument_errors():
     assert b.lib.carbon_gemm_dw_f32(FAKE, FAKE, FAKE, 16, 16, 16, 9, None) == INVALID
     assert b.lib.carbon_gemm_dw_f32(None, FAKE, FAKE, 16, 16, 16, 0, None) == INVALID
     assert b.lib.carbon_gemm_dw_f32(FAKE, FAKE, FAKE, 16, 0, 16, 0, None) == 0     # empty output
+
+
+def test_noalloc_injected_failure_is_reported(injected):
+    st = b.lib.carbon_gemm_exact_bf16_noalloc(0, FAKE, FAKE, FAKE, None, 16, 16, 16, None)
+    assert st == CUDA_ERR
+    assert "CARBON_FAULT" in b.lib.carbon_last_cuda_error().decode()
+
+
+def test_noalloc_argument_errors_and_limit_come_first(injected):
+    SCRATCH_LIMIT = 6
+    assert b.lib.carbon_gemm_exact_bf16_noalloc(0, FAKE, FAKE, FAKE, None, -1, 16, 16, None) == INVALID
+    assert b.lib.carbon_gemm_exact_bf16_noalloc(3, FAKE, FAKE, FAKE, None, 16, 16, 16, None) == INVALID
+    assert b.lib.carbon_gemm_exact_bf16_noalloc(0, None, FAKE, FAKE, None, 16, 16, 16, None) == INVALID
+    # byte counts that overflow int64
+    big = 1 << 31
+    assert b.lib.carbon_gemm_exact_bf16_noalloc(0, FAKE, FAKE, FAKE, None, big, big, 4, None) == INVALID
+    # beyond the fixed workspace: rejected before the injected failure
+    assert b.lib.carbon_gemm_exact_bf16_noalloc(
+        0, FAKE, FAKE, FAKE, None, 8192, 3072, 768, None) == SCRATCH_LIMIT
+    assert b.lib.carbon_gemm_exact_bf16_noalloc(0, FAKE, FAKE, FAKE, None, 0, 16, 16, None) == 0

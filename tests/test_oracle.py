@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 
 import oracle
-from deterministic_invariant_gemm_fwd_gb300 import inputs
+import seeded_inputs as inputs
 from tests import exact_ref as ex
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form.json")

@@ -4,10 +4,13 @@ carbon_gemm_exact_bf16_noalloc exists for callers that cannot allocate device
 memory while they run (a framework allocator that owns the whole GPU, a
 latency-critical loop that must never wait on or fail in an allocator, a
 process without the stream-ordered pool).  It takes its workspace from a
-fixed 64 MiB array the library reserves when it is loaded, so it must give
+fixed 64 MiB device array that CUDA reserves when the library's module for
+this entry point loads on the device (its first call there), so it must give
 the same bits as the regular bf16 exact-tier entry points (the exact tier's
 tolerance is bit-identity), also when called twice in a row with different
-inputs (the array keeps the previous call's contents).
+inputs (the array keeps the previous call's contents).  Its kernels are the
+integer-pipe exact kernels, which no other entry point runs, so the outputs
+are also compared with the CPU oracle element by element.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process.
@@ -15,7 +18,8 @@ already run every other test; it also passes on its own in a fresh process.
 import numpy as np
 import pytest
 
-from deterministic_invariant_gemm_fwd_gb300 import inputs
+import oracle
+import seeded_inputs as inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -84,6 +88,8 @@ def test_noalloc_matches_regular_entry_point_twice_in_a_row(pass_):
         got = _noalloc(pass_, A, B, bias, M, K, N)
         assert cg.carbon_get_device_status() == 0
         assert np.array_equal(_bits(got), _bits(ref)), (pass_, M, K, N)
+        want, _ = oracle.gemm(pass_, "bf16", A, B, bias, M, K, N)
+        assert np.array_equal(_bits(got), want), (pass_, M, K, N, "oracle")
 
 
 def test_noalloc_rejects_problems_beyond_its_workspace():
