@@ -6,7 +6,9 @@ is plain C: products in float64, Kahan-Babushka-Neumaier accumulation in
 256-wide chunks left to right, chunk values combined left to right with KBN,
 bias added in float64, one round-to-nearest-even to the output type (Carbon
 README, "How It Works"; sgemm-bi "Determinism contracts" for the downcast).
-It shares nothing with the CUDA library.
+It shares nothing with the CUDA library.  ``gemm_superacc`` computes the
+correctly rounded tier (README "Roadmap": superaccumulators): the exact dot
+product plus the bias, rounded once.
 
 Every function of the oracle has pins in ``tests/test_oracle.py``: closed
 forms, exact rational sums within the KBN error bound, exact rounding, and
@@ -54,6 +56,9 @@ def _load():
                                        i64, i64, i64, vp, vp, i64, vp, vp,
                                        ctypes.c_int]
         lib.oracle_gemm_at.restype = ctypes.c_int
+        lib.oracle_gemm_superacc.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                                             i64, i64, i64, vp, vp, i64, vp, ctypes.c_int]
+        lib.oracle_gemm_superacc.restype = ctypes.c_int
         lib.oracle_round.argtypes = [ctypes.c_int, vp, vp, i64]
         lib.oracle_round.restype = None
         lib.oracle_chunk_width.restype = ctypes.c_int
@@ -127,6 +132,35 @@ def gemm_at(pass_: str, dtype: str, A, B, bias, M: int, K: int, N: int,
     if rc:
         raise RuntimeError(f"oracle_gemm_at failed ({rc})")
     return out, y64
+
+
+def gemm_superacc(pass_: str, dtype: str, A, B, bias, M: int, K: int, N: int,
+                  rows=None, cols=None, threads: int | None = None):
+    """Correctly rounded tier: RNE of the exact dot product (+ bias for fwd),
+    every output (dense) or the outputs (rows[k], cols[k]).  Returns the
+    rounded outputs (fp32 array, or uint16 bits of bf16 / fp16)."""
+    lib = _load()
+    A, B, bias = _prep(A, dtype), _prep(B, dtype), _prep(bias, dtype)
+    if rows is None:
+        out = np.empty(out_shape(pass_, M, K, N), dtype=_np_dtype(dtype))
+        rc = lib.oracle_gemm_superacc(PASSES[pass_], DTYPES[dtype], _ptr(A), _ptr(B),
+                                      _ptr(bias), M, K, N, None, None, 0, _ptr(out),
+                                      threads or default_threads())
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        R, C = out_shape(pass_, M, K, N)
+        if rows.shape != cols.shape or rows.ndim != 1:
+            raise ValueError("rows/cols must be 1-D and of equal length")
+        if rows.size and (rows.min() < 0 or rows.max() >= R or cols.min() < 0 or cols.max() >= C):
+            raise ValueError("sample coordinates out of range")
+        out = np.empty(rows.shape, dtype=_np_dtype(dtype))
+        rc = lib.oracle_gemm_superacc(PASSES[pass_], DTYPES[dtype], _ptr(A), _ptr(B),
+                                      _ptr(bias), M, K, N, _ptr(rows), _ptr(cols), rows.size,
+                                      _ptr(out), threads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_gemm_superacc failed ({rc})")
+    return out
 
 
 def round_out(dtype: str, y64) -> np.ndarray:

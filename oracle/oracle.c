@@ -19,6 +19,10 @@
  * "Determinism contracts" table describes the same final step as an RNE
  * downcast.
  *
+ * A second mode computes the correctly rounded result that the README's
+ * "Roadmap" superaccumulators stand for: the exact sum of the products and
+ * the bias, rounded once to the output type, independent of any order.
+ *
  * Layouts (weights stored [in, out], sgemm-bi "Use"): row-major X[M,K],
  * W[K,N], b[N], Y[M,N], dY[M,N], dX[M,K], dW[K,N].
  *   fwd : Y[i,j]  = sum_r X[i,r]  * W[r,j]   (R = K)
@@ -197,10 +201,142 @@ static double fixed_order_dot(const void *A, int64_t a0, int64_t as,
     return S + C;
 }
 
+/* ---- the correctly rounded tier: a superaccumulator ---------------------- */
+
+/* The Carbon README's "Roadmap" names superaccumulators, exact summation that
+ * needs no fixed order.  The value such a sum stands for has a plain
+ * definition: the exact sum of the products (each exact in float64) plus the
+ * bias, rounded once, to nearest-even, to the output type.  Written out here
+ * with a fixed-point accumulator wide enough for any product of two inputs:
+ * 32-bit digits, each held in an int64 so that carries can wait, bit 0 of
+ * the accumulator weighing 2^-SA_OFFSET.  Every product of two fp32 values
+ * lies in [2^-298, 2^256) in magnitude, so as m * 2^e with |m| < 2^53 its
+ * lowest bit is at e >= -350 and its highest below 2^256. */
+#define SA_DIGITS 24                    /* 768 bits */
+#define SA_OFFSET 360
+
+typedef struct {
+    int64_t d[SA_DIGITS];
+    int nan, pinf, ninf;                /* non-finite terms seen */
+    int64_t adds;                       /* additions since the last carry pass */
+} superacc_t;
+
+static void sa_carry(superacc_t *a)
+{
+    int k;
+    for (k = 0; k + 1 < SA_DIGITS; ++k) {
+        int64_t c = a->d[k] >> 32;      /* arithmetic shift: floor division by 2^32 */
+        a->d[k] -= c * ((int64_t)1 << 32);
+        a->d[k + 1] += c;
+    }
+    a->adds = 0;
+}
+
+/* Adds the float64 value x exactly. */
+static void sa_add(superacc_t *a, double x)
+{
+    int e, k, s, neg;
+    double f;
+    uint64_t u;
+    unsigned __int128 v;
+    if (isnan(x)) { a->nan = 1; return; }
+    if (isinf(x)) { if (x > 0) a->pinf = 1; else a->ninf = 1; return; }
+    if (x == 0.0)
+        return;
+    f = frexp(x, &e);                   /* x = f * 2^e, 0.5 <= |f| < 1 */
+    neg = f < 0;
+    u = (uint64_t)ldexp(fabs(f), 53);   /* exact: an integer below 2^53 */
+    e = e - 53 + SA_OFFSET;             /* x = +-u * 2^(e - SA_OFFSET), e >= 10 */
+    k = e / 32;
+    s = e % 32;
+    v = (unsigned __int128)u << s;      /* below 2^85: three digits */
+    if (neg) {
+        a->d[k] -= (int64_t)(uint32_t)v;
+        a->d[k + 1] -= (int64_t)(uint32_t)(v >> 32);
+        a->d[k + 2] -= (int64_t)(v >> 64);
+    } else {
+        a->d[k] += (int64_t)(uint32_t)v;
+        a->d[k + 1] += (int64_t)(uint32_t)(v >> 32);
+        a->d[k + 2] += (int64_t)(v >> 64);
+    }
+    if (++a->adds == ((int64_t)1 << 28))
+        sa_carry(a);
+}
+
+static int sa_bit(const superacc_t *a, int i)
+{
+    return i < 0 ? 0 : (int)((a->d[i / 32] >> (i % 32)) & 1);
+}
+
+/* Rounds the accumulated value once to the output type; returns its bits
+ * (fp32 bits, or the 16-bit pattern of bf16 / fp16).  A NaN term, or both
+ * infinities, gives NaN; otherwise an infinite term gives that infinity; an
+ * exact sum of zero gives +0. */
+static uint32_t sa_round(superacc_t *a, int dtype)
+{
+    int p, qmin, top, k, q, neg = 0;
+    uint64_t n = 0;
+    int half, sticky = 0;
+    double v;
+    if (a->nan || (a->pinf && a->ninf))
+        v = NAN;
+    else if (a->pinf || a->ninf)
+        v = a->pinf ? INFINITY : -INFINITY;
+    else {
+        sa_carry(a);                    /* digits 0..SA_DIGITS-2 now in [0, 2^32) */
+        if (a->d[SA_DIGITS - 1] < 0) {  /* negative: take the magnitude */
+            neg = 1;
+            for (k = 0; k < SA_DIGITS; ++k)
+                a->d[k] = -a->d[k];
+            sa_carry(a);
+        }
+        /* precision and the bit index of the smallest quantum (subnormals) */
+        p = dtype == ORACLE_F32 ? 24 : (dtype == ORACLE_F16 ? 11 : 8);
+        qmin = (dtype == ORACLE_F32 ? -149 : (dtype == ORACLE_F16 ? -24 : -133)) + SA_OFFSET;
+        for (top = 32 * SA_DIGITS - 1; top >= 0 && !sa_bit(a, top); --top)
+            ;
+        if (top < 0)
+            return 0u;                  /* exact zero: +0 */
+        q = top - (p - 1) > qmin ? top - (p - 1) : qmin;   /* quantum bit */
+        for (k = top; k >= q; --k)
+            n = 2 * n + (uint64_t)sa_bit(a, k);
+        half = sa_bit(a, q - 1);
+        for (k = q - 2; k >= 0 && !sticky; --k)
+            sticky = sa_bit(a, k);
+        if (half && (sticky || (n & 1)))
+            ++n;                        /* nearest, ties to even */
+        v = ldexp((double)n, q - SA_OFFSET);   /* exact; may reach the overflow bound */
+        if (neg)
+            v = -v;
+    }
+    /* v is NaN, infinite, or exact in the output type except when it is the
+     * power of two just past the largest finite value, which the routines
+     * below send to infinity: no second rounding happens */
+    if (dtype == ORACLE_F32)
+        return round_to_f32_bits(v);
+    return dtype == ORACLE_F16 ? round_to_f16_bits(v) : round_to_bf16_bits(v);
+}
+
+/* Correctly rounded a[a0 + r*as] . b[b0 + r*bs] (+ bias), r = 0..R-1. */
+static uint32_t exact_dot_rounded(const void *A, int64_t a0, int64_t as,
+                                  const void *B, int64_t b0, int64_t bs,
+                                  int64_t R, int dtype, const void *bias, int64_t j)
+{
+    superacc_t acc;
+    int64_t r;
+    memset(&acc, 0, sizeof acc);
+    for (r = 0; r < R; ++r)
+        sa_add(&acc, decode(A, dtype, a0 + r * as) * decode(B, dtype, b0 + r * bs));
+    if (bias)
+        sa_add(&acc, decode(bias, dtype, j));
+    return sa_round(&acc, dtype);
+}
+
 /* ---- one output element --------------------------------------------------- */
 
 typedef struct {
     int pass, dtype;
+    int superacc;       /* correctly rounded tier instead of fixed-order KBN */
     const void *A, *B, *bias;
     int64_t M, K, N;
     void *out;          /* output-typed array, or NULL */
@@ -212,9 +348,35 @@ typedef struct {
     int64_t ncols_out;  /* row length of the output matrix */
 } job_t;
 
+static void one_output_rounded(const job_t *jb, int64_t i, int64_t j, int64_t slot)
+{
+    uint32_t u;
+    switch (jb->pass) {
+    case ORACLE_FWD:
+        u = exact_dot_rounded(jb->A, i * jb->K, 1, jb->B, j, jb->N, jb->K, jb->dtype, jb->bias, j);
+        break;
+    case ORACLE_DX:
+        u = exact_dot_rounded(jb->A, i * jb->N, 1, jb->B, j * jb->N, 1, jb->N, jb->dtype, NULL, 0);
+        break;
+    default:
+        u = exact_dot_rounded(jb->A, i, jb->K, jb->B, j, jb->N, jb->M, jb->dtype, NULL, 0);
+        break;
+    }
+    if (jb->dtype == ORACLE_F32) {
+        memcpy((char *)jb->out + 4 * slot, &u, 4);
+    } else {
+        uint16_t h = (uint16_t)u;
+        memcpy((char *)jb->out + 2 * slot, &h, 2);
+    }
+}
+
 static void one_output(const job_t *jb, int64_t i, int64_t j, int64_t slot)
 {
     double y;
+    if (jb->superacc) {
+        one_output_rounded(jb, i, j, slot);
+        return;
+    }
     switch (jb->pass) {
     case ORACLE_FWD:    /* X[i, r] * W[r, j] */
         y = fixed_order_dot(jb->A, i * jb->K, 1, jb->B, j, jb->N, jb->K, jb->dtype);
@@ -301,6 +463,10 @@ static int check(int pass, int dtype, int64_t M, int64_t K, int64_t N)
         return -1;
     if (M < 0 || K < 0 || N < 0)
         return -1;
+    /* the superaccumulator's digits take 2^28 additions between carry passes;
+     * reduction lengths stay far below 2^31 */
+    if (M >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31))
+        return -1;
     return 0;
 }
 
@@ -358,3 +524,24 @@ void oracle_round(int dtype, const double *y, void *out, int64_t n)
 }
 
 int oracle_chunk_width(void) { return ORACLE_CHUNK; }
+
+/* Correctly rounded tier: out = RNE(exact dot product + bias), dense (out
+ * non-NULL) or at the listed outputs (rows != NULL, count of them). */
+int oracle_gemm_superacc(int pass, int dtype, const void *A, const void *B, const void *bias,
+                         int64_t M, int64_t K, int64_t N, const int64_t *rows,
+                         const int64_t *cols, int64_t count, void *out, int nthreads)
+{
+    job_t jb;
+    if (check(pass, dtype, M, K, N) || !out || count < 0 || (rows && !cols))
+        return -1;
+    memset(&jb, 0, sizeof jb);
+    jb.pass = pass; jb.dtype = dtype; jb.A = A; jb.B = B; jb.superacc = 1;
+    jb.bias = (pass == ORACLE_FWD) ? bias : NULL;
+    jb.M = M; jb.K = K; jb.N = N; jb.out = out;
+    if (rows) {
+        jb.rows = rows; jb.cols = cols;
+        return launch(jb, count, nthreads);
+    }
+    jb.ncols_out = (pass == ORACLE_DX) ? K : N;
+    return launch(jb, ((pass == ORACLE_DW) ? K : M) * jb.ncols_out, nthreads);
+}

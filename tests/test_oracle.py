@@ -387,3 +387,126 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
     lib = str(tmp_path / f"lib{name}.so")
     subprocess.run(["gcc", *oracle.CFLAGS, "-o", lib, str(path), "-lm"], check=True)
     assert _mutant_rejected(lib), f"no closed form rejects the mutant {name}"
+
+
+# --------------------------------------------------------------------------
+# The correctly rounded tier (superaccumulator; Carbon README, "Roadmap"):
+# RNE of the exact dot product plus the bias.  Pinned to the closed forms'
+# expect_superacc values and to exact rationals (no midpoint exception: the
+# value is defined exactly).
+
+@pytest.mark.parametrize("case,dtype,pass_", list(_golden_params()))
+def test_superacc_closed_form(case, dtype, pass_):
+    A, B, bias, (M, K, N) = _case_operands(case, pass_, dtype)
+    out = oracle.gemm_superacc(pass_, dtype, A, B, bias, M, K, N)
+    got = float(_as_f64(out, dtype).ravel()[0])
+    expect = float.fromhex(case["expect_superacc"])
+    assert got == expect, (got, expect)
+    if expect == 0:
+        assert not np.signbit(got)
+
+
+def _superacc_want(exact, dtype):
+    r = ex.rne(exact, dtype)
+    if isinstance(r, float):            # overflow
+        inf_bits = {"f32": 0x7F800000, "bf16": 0x7F80, "f16": 0x7C00}[dtype]
+        return inf_bits | ((0x80000000 if dtype == "f32" else 0x8000) if r < 0 else 0)
+    return ex.value_bits(r, dtype)
+
+
+@pytest.mark.parametrize("seed", inputs.SEEDS)
+@pytest.mark.parametrize("pass_", ["fwd", "dx", "dw"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_superacc_exact_rational(seed, pass_, dtype):
+    rng = np.random.default_rng(seed + 77)
+    shapes = SMALL_SHAPES[seed % 3::2] if pass_ != "fwd" else SMALL_SHAPES
+    for (M, K, N) in shapes:
+        A, B, bias = _random_operands(rng, pass_, M, K, N, dtype)
+        out = oracle.gemm_superacc(pass_, dtype, A, B, bias, M, K, N)
+        exact = ex.exact_product(pass_, A, B, dtype)
+        bvals = ex.to_fractions(bias, dtype) if bias is not None else None
+        got = out.view(np.uint32) if dtype == "f32" else out
+        for idx in np.ndindex(exact.shape):
+            e = exact[idx] + (bvals[idx[1]] if bvals is not None else 0)
+            assert int(got[idx]) == _superacc_want(e, dtype), (pass_, M, K, N, idx)
+
+
+def test_superacc_wide_range_and_cancellation():
+    """Values spread over 2^+-60 with exact cancellation between them: the
+    result is the exact sum rounded once, and the same for any order of the
+    reduction index."""
+    rng = np.random.default_rng(3)
+    K = 700
+    x = (rng.choice([-1.0, 1.0], K) * np.ldexp(1.0, rng.integers(-60, 61, K))).astype(np.float32)
+    x[350:] = -x[:350][rng.permutation(350)]          # cancels the first half exactly...
+    x[699] = np.float32(2.0 ** -70)                     # ...but for a tiny residue
+    w = np.ones(K, dtype=np.float32)
+    for perm in (np.arange(K), rng.permutation(K), np.arange(K)[::-1]):
+        xa, wa = np.ascontiguousarray(x[perm]), np.ascontiguousarray(w[perm])
+        out = oracle.gemm_superacc("fwd", "f32", xa.reshape(1, K), wa.reshape(K, 1), None, 1, K, 1)
+        exact = sum((Fraction(float(v)) for v in x), Fraction(0))
+        assert int(out.view(np.uint32)[0, 0]) == _superacc_want(exact, "f32")
+
+
+def test_superacc_non_finite_and_overflow():
+    big = np.float32(2.0 ** 127)
+    cases = [  # (x, w, expected fp32 bits)
+        ([big, big, -big], [big, big, big], 0x7F800000),          # exact 2^254: overflows to +inf
+        ([np.inf, 1.0], [1.0, 1.0], 0x7F800000),                   # +inf
+        ([np.inf, -np.inf], [1.0, 1.0], None),                     # NaN
+        ([np.nan, 1.0], [1.0, 1.0], None),
+        ([-big, -big], [big, big], 0xFF800000),                    # -inf
+    ]
+    for xv, wv, want in cases:
+        K = len(xv)
+        x = np.array(xv, dtype=np.float32).reshape(1, K)
+        w = np.array(wv, dtype=np.float32).reshape(K, 1)
+        got = int(oracle.gemm_superacc("fwd", "f32", x, w, None, 1, K, 1).view(np.uint32)[0, 0])
+        if want is None:
+            assert (got & 0x7F800000) == 0x7F800000 and (got & 0x7FFFFF) != 0
+        else:
+            assert got == want, hex(got)
+
+
+SUPERACC_MUTANTS = {
+    "no_sticky_bit": ("sticky = sa_bit(a, k);", "sticky = 0;"),
+    "ties_away_from_zero": ("if (half && (sticky || (n & 1)))", "if (half)"),
+    "bias_left_out": ("    if (bias)\n        sa_add(&acc, decode(bias, dtype, j));", "    (void)bias;"),
+    "sign_of_negative_sums_lost": ("            neg = 1;\n", ""),
+    "rounded_through_float64": (
+        "        v = ldexp((double)n, q - SA_OFFSET);   /* exact; may reach the overflow bound */",
+        "        { double hi = 0; for (k = 32 * SA_DIGITS - 1; k >= 0; --k) hi = 2 * hi + sa_bit(a, k);"
+        " v = ldexp(hi, -SA_OFFSET); (void)n; }"),
+}
+
+
+def _superacc_mutant_rejected(lib_path):
+    import ctypes
+    lib = ctypes.CDLL(lib_path)
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    lib.oracle_gemm_superacc.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                                         i64, i64, i64, vp, vp, i64, vp, ctypes.c_int]
+    failed = []
+    ptr = (lambda a: None if a is None else a.ctypes.data_as(vp))
+    for case, dtype, pass_ in (p.values for p in _golden_params()):
+        A, B, bias, (M, K, N) = _case_operands(case, pass_, dtype)
+        out = np.empty(oracle.out_shape(pass_, M, K, N),
+                       dtype=np.float32 if dtype == "f32" else np.uint16)
+        assert lib.oracle_gemm_superacc(oracle.PASSES[pass_], oracle.DTYPES[dtype], ptr(A),
+                                        ptr(B), ptr(bias), M, K, N, None, None, 0, ptr(out), 1) == 0
+        if float(_as_f64(out, dtype).ravel()[0]) != float.fromhex(case["expect_superacc"]):
+            failed.append(case["name"])
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(SUPERACC_MUTANTS))
+def test_superacc_pins_catch_planted_mistakes(name, tmp_path):
+    import subprocess
+    src = open(oracle._SRC).read()
+    old, new = SUPERACC_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found once"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    lib = str(tmp_path / f"lib{name}.so")
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", lib, str(path), "-lm"], check=True)
+    assert _superacc_mutant_rejected(lib), f"no closed form rejects the mutant {name}"
