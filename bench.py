@@ -277,6 +277,36 @@ def fp32_exact_section(device, stream, fp64_rate, stress=True, repeats=(7, 3)):
     return out
 
 
+# ------------------------------------------- correctly rounded tier (bf16)
+
+def superacc_section(wl, stream, flush, exact_ms, reps=5):
+    """The correctly rounded tier (exact sum and bias rounded once) on the
+    same 12 GPT-2 GEMMs: one untimed pass, then `reps` passes timed with CUDA
+    events on `stream`, L2 flushed before each; the median is reported."""
+    import torch
+    import deterministic_invariant_gemm_fwd_gb300 as cg
+    with torch.cuda.stream(stream):
+        wl.launch("superacc", stream)
+        stream.synchronize()
+        times = []
+        for _ in range(reps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            wl.launch("superacc", stream)
+            e1.record(stream)
+            stream.synchronize()
+            times.append(e0.elapsed_time(e1))
+    assert cg.carbon_get_device_status(stream.cuda_stream) == 0
+    ms = statistics.median(times)
+    fl = sum(2.0 * M * K * N for (_, _, M, K, N) in wl.gemm_list("superacc"))
+    return {"ms_per_12_gemms": _r(ms), "ms_min_max": [_r(min(times)), _r(max(times))],
+            "repeats": reps, "gflops": _r(fl / (ms * 1e-3) / 1e9),
+            "vs_exact_tier_time": _r(ms / exact_ms) if exact_ms else None,
+            "timing": "CUDA events around the 12 launches, L2 flushed before each pass"}
+
+
 # ------------------------------------------------------------ CPU baseline
 
 def oracle_sample(host_layers, target_s, threads=None):
@@ -428,6 +458,8 @@ def main():
                          "unless --no-stress, the cancellation stress dW) and print it")
     ap.add_argument("--no-stress", action="store_true",
                     help="with --fp32-only: leave out the cancellation stress dW")
+    ap.add_argument("--no-superacc", action="store_true",
+                    help="skip the correctly rounded tier's section (the same 12 GEMMs)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the TC tier eagerly inside the timed region")
     ap.add_argument("--gemm", default=None,
@@ -466,7 +498,8 @@ def main():
         tiers = [t for t in tiers if t != "tc"]
     host = make_host_layers(SEED + rank)
     only = set(args.gemm.split(",")) if args.gemm else None
-    wl = Workload(host, device, tiers, only)
+    do_superacc = not args.no_superacc and only is None and "exact" in tiers
+    wl = Workload(host, device, tiers + (["superacc"] if do_superacc else []), only)
     stream = torch.cuda.Stream(device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
@@ -527,8 +560,10 @@ def main():
         launches = cg.carbon_debug_launch_count() - launches0 + graph_nodes * len(graph_events)
         assert cg.carbon_get_device_status(stream.cuda_stream) == 0
         main_ms = main_n = main_kg = 0
+        phases = None
         if "exact" in tiers:
             main_ms, main_n, main_kg = cg.carbon_debug_kernel_time()
+            phases = cg.carbon_debug_exact_phase_time()
             cg.carbon_debug_kernel_timing(False)
 
         # per-GEMM kernel time: back-to-back eager launches between two events
@@ -595,6 +630,10 @@ def main():
                          f"{main_kg} plane products of 2*128*64*256 flops in {main_n} launches), "
                          "over the kernel's own CUDA-event time"),
                 "kernel_ms_per_step": _r(main_ms / args.steps),
+                "phases_ms_per_step": ({"pre_pass": _r(phases[0] / args.steps),
+                                        "exact_tc_kernel": _r(phases[1] / args.steps),
+                                        "post_pass": _r(phases[2] / args.steps)}
+                                       if phases else None),
                 "kernel_share_of_tier": _r(main_ms / ms) if ms > 0 else None,
                 "mma_flops_per_useful_flop": _r(kg_flops / fl_all) if fl_all > 0 else None,
                 "useful_tflops_kernel": _r(fl_all / (main_ms * 1e-3) / 1e12) if main_ms > 0 else None,
@@ -646,6 +685,10 @@ def main():
         e2e = {"value": _r(whole_job_gflops(flops, world, e2e_ms)), "unit": "GFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": _r(e2e_ms)}
 
+    superacc = None
+    if do_superacc:
+        superacc = superacc_section(wl, stream, flush, tier_info.get("exact", {}).get("ms_per_step"))
+
     fp32 = None
     if "exact" in tiers and not args.no_fp32 and only is None:
         if fp64_rate is None:
@@ -680,6 +723,7 @@ def main():
             "roofline": rooflines[dom],
             "rooflines": rooflines,
             "fp32_exact": fp32,
+            "superacc": superacc,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,

@@ -15,10 +15,12 @@ and call it.  Weights are stored [in, out] (sgemm-bi page, "Use").
 from __future__ import annotations
 
 from ._binding import (CarbonError, carbon_abi_version, carbon_debug_exact_y64,  # noqa: F401
-                       carbon_debug_exact_path_counts, carbon_debug_kernel_time,
+                       carbon_debug_exact_path_counts, carbon_debug_exact_phase_time,
+                       carbon_debug_kernel_time,
                        carbon_debug_kernel_timing,
                        carbon_debug_launch_count, carbon_debug_round,
                        carbon_debug_tc_f32, carbon_debug_timeout_probe,
+                       carbon_chunk_values_combine, carbon_gemm_chunk_values,
                        carbon_gemm_dw, carbon_gemm_dw_f32, carbon_gemm_dx, carbon_gemm_fwd,
                        carbon_get_device_status, carbon_measure_fp64_rate,
                        carbon_measure_int_mac_rate,

@@ -20,13 +20,13 @@ HEADERS = [os.path.join(os.path.dirname(HERE), "include", h)
            for h in ("carbon_gemm.h", "carbon_gemm_debug.h")]
 
 F32, BF16, F16 = 0, 1, 2
-TIER_EXACT, TIER_TC = 0, 1
+TIER_EXACT, TIER_TC, TIER_SUPERACC = 0, 1, 2
 PASS_FWD, PASS_DX, PASS_DW = 0, 1, 2
 STATUS = {0: "CARBON_OK", 1: "CARBON_ERR_INVALID_ARG", 2: "CARBON_ERR_UNSUPPORTED",
           3: "CARBON_ERR_MISALIGNED", 4: "CARBON_ERR_CUDA", 5: "CARBON_ERR_TIMEOUT",
           6: "CARBON_ERR_SCRATCH_LIMIT"}
 DTYPES = {"f32": F32, "bf16": BF16, "f16": F16}
-TIERS = {"exact": TIER_EXACT, "tc": TIER_TC}
+TIERS = {"exact": TIER_EXACT, "tc": TIER_TC, "superacc": TIER_SUPERACC}
 PASSES = {"fwd": PASS_FWD, "dx": PASS_DX, "dw": PASS_DW}
 
 
@@ -53,6 +53,8 @@ def _load() -> ctypes.CDLL:
         "carbon_gemm_dw_f32": [vp, vp, vp, i64, i64, i64, i32, vp],
         "carbon_get_device_status": [vp],
         "carbon_gemm_exact_bf16_noalloc": [i32, vp, vp, vp, vp, i64, i64, i64, vp],
+        "carbon_gemm_chunk_values": [i32, vp, vp, vp, i64, i64, i64, i32, vp],
+        "carbon_chunk_values_combine": [vp, vp, i64, i64, i64, vp, i32, vp],
         "carbon_debug_exact_y64": [i32, vp, vp, vp, vp, i64, i64, i64, i32, vp],
         "carbon_debug_tc_f32": [i32, vp, vp, vp, vp, i64, i64, i64, vp],
         "carbon_debug_round": [i32, vp, vp, i64, vp],
@@ -78,6 +80,8 @@ def _load() -> ctypes.CDLL:
                                              ctypes.POINTER(ctypes.c_int64),
                                              ctypes.POINTER(ctypes.c_int64)]
     lib.carbon_debug_kernel_time.restype = ctypes.c_int
+    lib.carbon_debug_exact_phase_time.argtypes = [ctypes.POINTER(ctypes.c_double)] * 3
+    lib.carbon_debug_exact_phase_time.restype = ctypes.c_int
     lib.carbon_debug_exact_path_counts.argtypes = [ctypes.POINTER(ctypes.c_int64),
                                                    ctypes.POINTER(ctypes.c_int64)]
     lib.carbon_debug_exact_path_counts.restype = ctypes.c_int
@@ -171,6 +175,21 @@ def carbon_gemm_exact_bf16_noalloc(pass_, out, A, B, bias, M, K, N, stream=None)
            "carbon_gemm_exact_bf16_noalloc")
 
 
+def carbon_gemm_chunk_values(pass_, P, A, B, M, K, N, dtype, stream=None) -> None:
+    """Exact-tier chunk values of one rank's share of a reduction:
+    P[q][i][j] = fl(s + c) of chunk q, float64 [ceil(R/256)][rows][cols]."""
+    _check(_lib().carbon_gemm_chunk_values(_code(PASSES, pass_), _ptr(P), _ptr(A), _ptr(B),
+                                           M, K, N, _code(DTYPES, dtype), _stream(stream)),
+           "carbon_gemm_chunk_values")
+
+
+def carbon_chunk_values_combine(out, P, nchunks, rows, cols, bias, dtype, stream=None) -> None:
+    """Outer KBN over chunk values in chunk order, the bias, one rounding."""
+    _check(_lib().carbon_chunk_values_combine(_ptr(out), _ptr(P), nchunks, rows, cols, _ptr(bias),
+                                              _code(DTYPES, dtype), _stream(stream)),
+           "carbon_chunk_values_combine")
+
+
 def carbon_get_device_status(stream=None) -> int:
     """Synchronises the stream; returns the status code (does not raise)."""
     return int(_lib().carbon_get_device_status(_stream(stream)))
@@ -237,6 +256,15 @@ def carbon_debug_kernel_time():
     _check(_lib().carbon_debug_kernel_time(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(kg)),
            "carbon_debug_kernel_time")
     return ms.value, int(n.value), int(kg.value)
+
+
+def carbon_debug_exact_phase_time():
+    """(pre-pass, tensor-core kernel, post-pass) milliseconds of the bf16 exact
+    tier's calls recorded since timing was enabled."""
+    a, b, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _check(_lib().carbon_debug_exact_phase_time(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+           "carbon_debug_exact_phase_time")
+    return a.value, b.value, c.value
 
 
 def carbon_debug_exact_path_counts():

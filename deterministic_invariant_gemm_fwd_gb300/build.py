@@ -21,7 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libcarbon_gemm.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "exact_kbn.cu", "exact_int.cu", "exact_tc.cu", "tc_gemm.cu", "measure.cu"]
+SOURCES = ["api.cu", "exact_kbn.cu", "exact_int.cu", "exact_tc.cu", "superacc.cu", "tc_gemm.cu",
+           "measure.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

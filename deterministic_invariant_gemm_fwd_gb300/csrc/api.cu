@@ -63,7 +63,8 @@ carbon_status_t check_args(const Problem &p, int tier, bool *nothing_to_do) {
     if (p.M < 0 || p.K < 0 || p.N < 0) return CARBON_ERR_INVALID_ARG;
     if (p.dtype != CARBON_F32 && p.dtype != CARBON_BF16 && p.dtype != CARBON_F16)
         return CARBON_ERR_INVALID_ARG;
-    if (tier != CARBON_TIER_EXACT && tier != CARBON_TIER_TC) return CARBON_ERR_INVALID_ARG;
+    if (tier != CARBON_TIER_EXACT && tier != CARBON_TIER_TC && tier != CARBON_TIER_SUPERACC)
+        return CARBON_ERR_INVALID_ARG;
     int64_t mk, kn, mn, t;
     if (!mul_ok(p.M, p.K, &mk) || !mul_ok(p.K, p.N, &kn) || !mul_ok(p.M, p.N, &mn))
         return CARBON_ERR_INVALID_ARG;
@@ -127,8 +128,12 @@ carbon_status_t run(const Problem &p, int tier, int debug_out, carbon_stream_t s
     if (st != CARBON_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tier == CARBON_TIER_EXACT)
-        return p.dtype == CARBON_BF16 ? exact_tc_launch(p, debug_out != 0, s)
+        return p.dtype == CARBON_BF16 ? exact_tc_launch(p, debug_out != 0, false, s)
                                       : exact_launch(p, debug_out != 0, s);
+    if (tier == CARBON_TIER_SUPERACC) {
+        if (debug_out) return CARBON_ERR_UNSUPPORTED;    // no float64 value: one rounding of the exact sum
+        return p.dtype == CARBON_BF16 ? exact_tc_launch(p, false, true, s) : superacc_launch(p, s);
+    }
     return tc_launch(p, debug_out != 0, s);
 }
 
@@ -164,6 +169,7 @@ carbon_status_t carbon_gemm_dw_f32(float *dW, const void *X, const void *dY, int
                                    int64_t N, carbon_tier_t tier, carbon_stream_t stream) {
     const carbon::Problem p = make_problem(CARBON_PASS_DW, CARBON_BF16, dW, X, dY, nullptr, M, K, N);
     if (tier == CARBON_TIER_TC) return carbon::run(p, CARBON_TIER_TC, 1, stream);   // the fp32 accumulator
+    if (tier == CARBON_TIER_SUPERACC) return CARBON_ERR_UNSUPPORTED;
     if (tier != CARBON_TIER_EXACT) return CARBON_ERR_INVALID_ARG;
     // exact tier: the float64 value into a staging buffer, then one rounding to fp32
     bool nothing = false;
@@ -185,6 +191,44 @@ carbon_status_t carbon_gemm_dw_f32(float *dW, const void *X, const void *dY, int
     const cudaError_t ferr = cudaFreeAsync(y64, s);
     if (st == CARBON_OK && ferr != cudaSuccess) st = carbon::note_cuda(ferr);
     return st;
+}
+
+carbon_status_t carbon_gemm_chunk_values(carbon_pass_t pass, double *P, const void *A,
+                                        const void *B, int64_t M, int64_t K, int64_t N,
+                                        carbon_dtype_t dtype, carbon_stream_t stream) {
+    if (pass < CARBON_PASS_FWD || pass > CARBON_PASS_DW) return CARBON_ERR_INVALID_ARG;
+    const carbon::Problem p = make_problem(pass, dtype, P, A, B, nullptr, M, K, N);
+    bool nothing = false;
+    carbon_status_t st = carbon::check_args(p, CARBON_TIER_EXACT, &nothing);
+    if (st != CARBON_OK || nothing) return st;
+    int64_t chunks = (p.R + 255) / 256, total;
+    if (__builtin_mul_overflow(chunks, p.rows * p.cols, &total) ||
+        __builtin_mul_overflow(total, (int64_t)8, &total))
+        return CARBON_ERR_INVALID_ARG;
+    st = carbon::injected_launch_failure();
+    if (st != CARBON_OK) return st;
+    st = carbon::current_device(nullptr, nullptr);
+    if (st != CARBON_OK) return st;
+    return carbon::exact_chunk_values_launch(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+carbon_status_t carbon_chunk_values_combine(void *out, const double *P, int64_t nchunks,
+                                            int64_t rows, int64_t cols, const void *bias,
+                                            carbon_dtype_t dtype, carbon_stream_t stream) {
+    if (dtype != CARBON_F32 && dtype != CARBON_BF16 && dtype != CARBON_F16) return CARBON_ERR_INVALID_ARG;
+    if (nchunks < 0 || rows < 0 || cols < 0) return CARBON_ERR_INVALID_ARG;
+    int64_t n, total;
+    if (__builtin_mul_overflow(rows, cols, &n) || __builtin_mul_overflow(n, nchunks, &total) ||
+        __builtin_mul_overflow(total, (int64_t)8, &total))
+        return CARBON_ERR_INVALID_ARG;
+    if (n == 0) return CARBON_OK;
+    if (out == nullptr || (nchunks > 0 && P == nullptr)) return CARBON_ERR_INVALID_ARG;
+    carbon_status_t st = carbon::injected_launch_failure();
+    if (st != CARBON_OK) return st;
+    st = carbon::current_device(nullptr, nullptr);
+    if (st != CARBON_OK) return st;
+    return carbon::exact_combine_launch(dtype, out, P, nchunks, rows, cols, bias,
+                                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 carbon_status_t carbon_debug_exact_y64(carbon_pass_t pass, double *y64, const void *A,
@@ -250,6 +294,10 @@ void carbon_debug_kernel_timing(int enable) { carbon::exact_tc_timing(enable); }
 
 carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t *plane_products) {
     return carbon::exact_tc_time(ms, launches, plane_products);
+}
+
+carbon_status_t carbon_debug_exact_phase_time(double *pre_ms, double *main_ms, double *post_ms) {
+    return carbon::exact_tc_phase_time(pre_ms, main_ms, post_ms);
 }
 
 carbon_status_t carbon_debug_exact_path_counts(int64_t *chunk_repairs, int64_t *fixups) {

@@ -57,10 +57,23 @@ carbon_status_t injected_launch_failure();
 carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream);
 // bf16 exact tier on the integer pipes (exact_int.cu); same bits.
 carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t stream);
-// bf16 exact tier on the tensor cores (exact_tc.cu); same bits.
-carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t stream);
+// bf16 exact tier on the tensor cores (exact_tc.cu); same bits.  super: the
+// correctly rounded tier instead (exact total and bias rounded once).
+carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, bool super, cudaStream_t stream);
+// Correctly rounded tier, one output per warp, any dtype (superacc.cu).
+carbon_status_t superacc_launch(const Problem &p, cudaStream_t stream);
+// The same kernel for the bf16 outputs listed in work_list[0 .. *work_count).
+cudaError_t superacc_fixup_bf16(const Problem &p, const unsigned int *work_count,
+                                const unsigned int *work_list, int blocks, cudaStream_t stream);
 carbon_status_t exact_round_launch(int dtype, void *out, const double *in, int64_t n,
                                    cudaStream_t stream);
+// Chunk values fl(s + c) of every output into p.out (float64
+// [ceil(R/256)][rows][cols]), and the outer KBN + bias + rounding over chunk
+// values computed elsewhere (exact_kbn.cu).
+carbon_status_t exact_chunk_values_launch(const Problem &p, cudaStream_t stream);
+carbon_status_t exact_combine_launch(int dtype, void *out, const double *P, int64_t nchunks,
+                                     int64_t rows, int64_t cols, const void *bias,
+                                     cudaStream_t stream);
 
 // 2-D tiled TMA tensor map over a row-major [outer, inner] matrix (row pitch
 // row_bytes); out-of-range elements read as zero.  cudaErrorInvalidValue if
@@ -76,6 +89,7 @@ carbon_status_t exact_tc_take_device_status();
 // Kernel timing of the bf16 exact tier's tensor-core kernel (exact_tc.cu).
 void exact_tc_timing(int enable);
 carbon_status_t exact_tc_time(double *ms, int64_t *launches, int64_t *kgroups);
+carbon_status_t exact_tc_phase_time(double *pre_ms, double *main_ms, double *post_ms);
 carbon_status_t exact_tc_path_counts(int64_t *repairs, int64_t *fixups);
 
 // Tensor-core tier (tc_gemm.cu).  out_f32 selects the fp32 pre-rounding output.

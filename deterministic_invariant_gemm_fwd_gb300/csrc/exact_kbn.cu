@@ -183,7 +183,12 @@ __device__ __forceinline__ void stage_slice(const KArgs &p, double (*As)[kBM + 1
     }
 }
 
-template <int DT, int PASS, bool OUT_F64>
+// Output modes: the rounded output, the float64 value before the rounding,
+// or the chunk values fl(s + c) themselves (P[chunk][rows][cols], no outer
+// sum and no bias), for reductions split across ranks on chunk boundaries.
+constexpr int kOutRounded = 0, kOutF64 = 1, kOutChunks = 2;
+
+template <int DT, int PASS, int OUT>
 __global__ void __launch_bounds__(kThreads)
 exact_kbn_kernel(const KArgs p) {
     __shared__ double As[kBK][kBM + 1];
@@ -281,13 +286,24 @@ exact_kbn_kernel(const KArgs p) {
                 }
             }
         }
+        if constexpr (OUT == kOutChunks) {
+            double *P = static_cast<double *>(p.out) + (q0 / kChunk) * p.rows * p.cols;
 #pragma unroll
-        for (int m = 0; m < kTM; ++m)
+            for (int m = 0; m < kTM; ++m)
 #pragma unroll
-            for (int n = 0; n < kTN; ++n)
-                kbn_value_step(S[m][n], C[m][n], __dadd_rn(s[m][n], c[m][n]));
+                for (int n = 0; n < kTN; ++n) {
+                    const int64_t i = i0 + ty + kTY * m, j = j0 + tx + kTX * n;
+                    if (i < p.rows && j < p.cols) P[i * p.cols + j] = __dadd_rn(s[m][n], c[m][n]);
+                }
+        } else {
+#pragma unroll
+            for (int m = 0; m < kTM; ++m)
+#pragma unroll
+                for (int n = 0; n < kTN; ++n)
+                    kbn_value_step(S[m][n], C[m][n], __dadd_rn(s[m][n], c[m][n]));
+        }
     }
-
+    if constexpr (OUT != kOutChunks) {
 #pragma unroll
     for (int m = 0; m < kTM; ++m) {
         const int64_t i = i0 + ty + kTY * m;
@@ -299,7 +315,7 @@ exact_kbn_kernel(const KArgs p) {
             double y = __dadd_rn(S[m][n], C[m][n]);
             if (p.bias) y = __dadd_rn(y, widen(load_bits<DT>(p.bias, j)));
             const int64_t o = i * p.cols + j;
-            if (OUT_F64)
+            if (OUT == kOutF64)
                 static_cast<double *>(p.out)[o] = y;
             else if (DT == CARBON_F32)
                 static_cast<float *>(p.out)[o] = __double2float_rn(y);
@@ -308,6 +324,7 @@ exact_kbn_kernel(const KArgs p) {
             else
                 static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
         }
+    }
     }
 }
 
@@ -321,31 +338,49 @@ __global__ void round_kernel(int dtype, void *out, const double *in, int64_t n) 
     }
 }
 
-template <int DT, int PASS, bool OUT_F64>
+template <int DT, int PASS, int OUT>
 cudaError_t launch_one(const KArgs &a, int64_t tiles, cudaStream_t stream) {
-    exact_kbn_kernel<DT, PASS, OUT_F64><<<(unsigned)tiles, kThreads, 0, stream>>>(a);
+    exact_kbn_kernel<DT, PASS, OUT><<<(unsigned)tiles, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
 template <int DT, int PASS>
-cudaError_t launch_pass(const KArgs &a, int64_t tiles, bool out_f64, cudaStream_t stream) {
-    return out_f64 ? launch_one<DT, PASS, true>(a, tiles, stream)
-                   : launch_one<DT, PASS, false>(a, tiles, stream);
+cudaError_t launch_pass(const KArgs &a, int64_t tiles, int out, cudaStream_t stream) {
+    return out == kOutChunks ? launch_one<DT, PASS, kOutChunks>(a, tiles, stream)
+         : out == kOutF64    ? launch_one<DT, PASS, kOutF64>(a, tiles, stream)
+                             : launch_one<DT, PASS, kOutRounded>(a, tiles, stream);
 }
 
 template <int DT>
-cudaError_t launch_dtype(int pass, const KArgs &a, int64_t tiles, bool out_f64, cudaStream_t s) {
+cudaError_t launch_dtype(int pass, const KArgs &a, int64_t tiles, int out, cudaStream_t s) {
     switch (pass) {
-    case CARBON_PASS_FWD: return launch_pass<DT, CARBON_PASS_FWD>(a, tiles, out_f64, s);
-    case CARBON_PASS_DX:  return launch_pass<DT, CARBON_PASS_DX>(a, tiles, out_f64, s);
-    default:              return launch_pass<DT, CARBON_PASS_DW>(a, tiles, out_f64, s);
+    case CARBON_PASS_FWD: return launch_pass<DT, CARBON_PASS_FWD>(a, tiles, out, s);
+    case CARBON_PASS_DX:  return launch_pass<DT, CARBON_PASS_DX>(a, tiles, out, s);
+    default:              return launch_pass<DT, CARBON_PASS_DW>(a, tiles, out, s);
     }
 }
 
-}  // namespace
+// The outer KBN over chunk values in chunk order, the bias, one rounding: the
+// steps the kernel above takes after its chunks, for chunk values that were
+// computed elsewhere (P[q][rows][cols], q = 0 .. nchunks - 1).
+template <int DT>
+__global__ void __launch_bounds__(256)
+combine_kernel(void *out, const double *__restrict__ P, int64_t nchunks, int64_t rows, int64_t cols,
+               const void *bias) {
+    const int64_t n = rows * cols;
+    for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < n;
+         o += (int64_t)gridDim.x * blockDim.x) {
+        double S = 0.0, C = 0.0;
+        for (int64_t q = 0; q < nchunks; ++q) kbn_value_step(S, C, __ldg(&P[q * n + o]));
+        double y = __dadd_rn(S, C);
+        if (bias) y = __dadd_rn(y, widen(load_bits<DT>(bias, o % cols)));
+        if (DT == CARBON_F32) static_cast<float *>(out)[o] = __double2float_rn(y);
+        else if (DT == CARBON_F16) static_cast<unsigned short *>(out)[o] = exact_round_f16(y);
+        else static_cast<unsigned short *>(out)[o] = exact_round_bf16(y);
+    }
+}
 
-carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream) {
-    if (p.rows == 0 || p.cols == 0) return CARBON_OK;
+KArgs make_kargs(const Problem &p) {
     KArgs a;
     a.A = p.A; a.B = p.B; a.bias = p.bias; a.out = p.out;
     a.rows = p.rows; a.cols = p.cols; a.R = p.R;
@@ -354,15 +389,45 @@ carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream
     case CARBON_PASS_DX:  a.a_si = p.N; a.a_sr = 1; a.b_sr = 1;   a.b_sj = p.N; break;
     default:              a.a_si = 1;   a.a_sr = p.K; a.b_sr = p.N; a.b_sj = 1; break;
     }
-    const int64_t tiles_m = (p.rows + kBM - 1) / kBM;
     a.tiles_n = (p.cols + kBN - 1) / kBN;
+    return a;
+}
+
+carbon_status_t launch_kbn(const Problem &p, int out, cudaStream_t stream) {
+    if (p.rows == 0 || p.cols == 0) return CARBON_OK;
+    KArgs a = make_kargs(p);
+    const int64_t tiles_m = (p.rows + kBM - 1) / kBM;
     const int64_t tiles = tiles_m * a.tiles_n;
     if (tiles > 0x7fffffff) return CARBON_ERR_INVALID_ARG;
-    const cudaError_t err = (p.dtype == CARBON_F32)   ? launch_dtype<CARBON_F32>(p.pass, a, tiles, out_f64, stream)
-                          : (p.dtype == CARBON_F16) ? launch_dtype<CARBON_F16>(p.pass, a, tiles, out_f64, stream)
-                                                    : launch_dtype<CARBON_BF16>(p.pass, a, tiles, out_f64, stream);
+    const cudaError_t err = (p.dtype == CARBON_F32)   ? launch_dtype<CARBON_F32>(p.pass, a, tiles, out, stream)
+                          : (p.dtype == CARBON_F16) ? launch_dtype<CARBON_F16>(p.pass, a, tiles, out, stream)
+                                                    : launch_dtype<CARBON_BF16>(p.pass, a, tiles, out, stream);
     count_launch();
     return note_cuda(err);
+}
+
+}  // namespace
+
+carbon_status_t exact_chunk_values_launch(const Problem &p, cudaStream_t stream) {
+    if (p.R == 0) return CARBON_OK;                       // no chunks: nothing to write
+    return launch_kbn(p, kOutChunks, stream);
+}
+
+carbon_status_t exact_combine_launch(int dtype, void *out, const double *P, int64_t nchunks,
+                                     int64_t rows, int64_t cols, const void *bias,
+                                     cudaStream_t stream) {
+    const int64_t n = rows * cols;
+    if (n == 0) return CARBON_OK;
+    const int64_t blocks = (n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192;
+    if (dtype == CARBON_F32) combine_kernel<CARBON_F32><<<(unsigned)blocks, 256, 0, stream>>>(out, P, nchunks, rows, cols, bias);
+    else if (dtype == CARBON_F16) combine_kernel<CARBON_F16><<<(unsigned)blocks, 256, 0, stream>>>(out, P, nchunks, rows, cols, bias);
+    else combine_kernel<CARBON_BF16><<<(unsigned)blocks, 256, 0, stream>>>(out, P, nchunks, rows, cols, bias);
+    count_launch();
+    return note_cuda(cudaGetLastError());
+}
+
+carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream) {
+    return launch_kbn(p, out_f64 ? kOutF64 : kOutRounded, stream);
 }
 
 carbon_status_t exact_round_launch(int dtype, void *out, const double *in, int64_t n,

@@ -86,6 +86,7 @@
 #include "carbon_internal.h"
 #include "device_sync.cuh"
 #include "exact_bf16.cuh"
+#include "superacc.cuh"
 #include "tcgen05.cuh"
 
 #include <algorithm>
@@ -105,7 +106,29 @@ __device__ unsigned long long g_exact_tc_fixups = 0;
 // Optional CUDA-event timing of the main kernel (carbon_debug_kernel_timing).
 std::mutex g_timing_mu;
 bool g_timing_on = false;
-std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_timing_events;
+// One call's events: before its first device operation, around the main
+// kernel, after its last kernel (pre-pass, main kernel, post-pass).
+struct CallEvents {
+    cudaEvent_t e[4];
+};
+std::vector<CallEvents> g_timing_events;
+
+// Events of a call while timing is on and the stream is not being captured;
+// all null otherwise.
+CallEvents timing_events(cudaStream_t s) {
+    CallEvents ev = {{nullptr, nullptr, nullptr, nullptr}};
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (!g_timing_on || cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+        return ev;
+    for (int k = 0; k < 4; ++k)
+        if (cudaEventCreate(&ev.e[k]) != cudaSuccess) {
+            for (int m = 0; m < k; ++m) cudaEventDestroy(ev.e[m]);
+            return CallEvents{{nullptr, nullptr, nullptr, nullptr}};
+        }
+    g_timing_events.push_back(ev);
+    return ev;
+}
 
 constexpr int kRowTile = 128;                         // output rows per tile = MMA M = TMEM lanes
 constexpr int kColTile = 64;                          // output columns per tile
@@ -162,6 +185,7 @@ struct TcxArgs {
     void *out;
     int64_t rows, cols, LpA, LpB;
     int tiles_m, tiles_n, nchunks;
+    int row_fast;                                     // tile order: row tile fastest (else column tile)
     int splits, cps;                                  // chunk range split into pieces of cps chunks
     const int4 *SA, *SB;                              // statistics [chunk][Lp]
     const int *GA, *GB;                               // line grains (smallest base) [Lp]
@@ -175,6 +199,16 @@ struct TcxArgs {
     unsigned int chunk_cap;
     unsigned int *unit_counter;                       // next work unit (starts at 0)
 };
+
+// Row and column tile of tile t.  Consecutive tiles share the operand whose
+// digit planes are the larger of the two (the column tile when the B planes
+// are larger, e.g. dW of a 768 x 3072 weight: the 6 row tiles of each column
+// tile run together, so the B planes are read from DRAM about once instead of
+// once per row tile); the order does not change any result.
+__device__ __forceinline__ void tile_of(const TcxArgs &p, int t, int &tm, int &tn) {
+    if (p.row_fast) { tm = t % p.tiles_m; tn = t / p.tiles_m; }
+    else            { tm = t / p.tiles_n; tn = t % p.tiles_n; }
+}
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile uint32_t *flag) {
@@ -457,7 +491,9 @@ __device__ __forceinline__ long long round_to_53_bits(long long I) {
     return neg ? -(long long)r : (long long)r;
 }
 
-template <bool OUT_F64>
+// SUPER: the correctly rounded tier (chunk sums are added exactly, never
+// rounded to 53 bits; the finalize rounds the exact total once).
+template <bool SUPER>
 __global__ void __launch_bounds__(kTcxThreads, 1)
 exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const TcxArgs p) {
@@ -525,7 +561,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 if (u < 0 || *abort_flag) break;
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
-                const int tm = t / p.tiles_n;
+                int tm, tn;
+                tile_of(p, t, tm, tn);
                 for (int q = qlo; ok && q < qhi; ++q) {
                     const int nx = p.cntA[(int64_t)tm * nchunks + q];
                     for (int k = 0; ok && k < nx; ++k)
@@ -559,7 +596,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 if (u < 0 || *abort_flag) break;
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
-                const int tm = t / p.tiles_n, tn = t % p.tiles_n;
+                int tm, tn;
+                tile_of(p, t, tm, tn);
                 for (int q = qlo; ok && q < qhi; ++q) {
                     if (p.cntA[(int64_t)tm * nchunks + q] == 0) continue;
                     for (int kb = 0; kb < kKBlocks; ++kb) {
@@ -599,7 +637,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 if (u < 0 || *abort_flag) break;
                 const int t = u / p.splits, qlo = (u % p.splits) * p.cps;
                 const int qhi = min(nchunks, qlo + p.cps);
-                const int tm = t / p.tiles_n, tn = t % p.tiles_n;
+                int tm, tn;
+                tile_of(p, t, tm, tn);
                 for (int q = qlo; ok && q < qhi; ++q) {
                     const int nx = p.cntA[(int64_t)tm * nchunks + q];
                     if (nx == 0) continue;
@@ -670,7 +709,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             if (!(got & 2)) break;
             const int t = u / p.splits, piece = u % p.splits, qlo = piece * p.cps;
             const int qhi = min(nchunks, qlo + p.cps);
-            const int tm = t / p.tiles_n, tn = t % p.tiles_n;
+            int tm, tn;
+            tile_of(p, t, tm, tn);
             const int64_t i = __ldg(&p.invA[(int64_t)tm * kRowTile + rl]);   // the row's own index
             const int64_t jw = (int64_t)tn * kColTile + half * 32;   // this warp's first column
             const int *cnt = p.cntA + (int64_t)tm * nchunks;
@@ -808,13 +848,14 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     }
                     // a row that fails redoes its outputs one by one (its additions
                     // are still in T; each output keeps or takes back its own)
-                    added = !(lost == 0u && shs < 64u && ah < (1u << 21) && th < (1u << 30));
+                    added = !(lost == 0u && shs < 64u && (SUPER || ah < (1u << 21)) && th < (1u << 30));
                     redo = added ? 0xffffffffu : 0u;
                 }
                 if (redo != 0u) {
                     // per output: the chunk value is the exact chunk sum rounded
                     // once to float64 (KBN recovers every rounding error of its
-                    // loop exactly while wx + ww < 90), i.e. I itself when |I| < 2^53
+                    // loop exactly while wx + ww < 90), i.e. I itself when |I| < 2^53;
+                    // the correctly rounded tier adds I itself
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
                         const uint32_t bit = 1u << jj;
@@ -826,7 +867,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                             const long long v = shl64(I0, sh);
                             // |I| < 2^53 and |T| < 2^62, tested in unsigned arithmetic
                             // (T may have wrapped: a signed test could overflow)
-                            if ((v >> (sh & 63u)) == I0 && sh < 64u && below_pow2(I0, 53) &&
+                            if ((v >> (sh & 63u)) == I0 && sh < 64u && (SUPER || below_pow2(I0, 53)) &&
                                 below_pow2((long long)T[jj], 62))
                                 continue;
                             T[jj] -= (unsigned long long)v;
@@ -837,7 +878,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         const int bnd = min(min(lsx + (int)((w >> 21) & 0x3fu), lmx + (int)((w >> 15) & 0x3fu)),
                                             wx + ww + 8);                   // |I| < 2^bnd
                         const bool fits = wx <= 31 && ww <= 31 && bnd <= 62;
-                        if (bnd > 53 && !below_pow2(Ij, 53))
+                        if (!SUPER && bnd > 53 && !below_pow2(Ij, 53))
                             Ij = round_to_53_bits(Ij);                      // |result| <= 2^bnd
                         const int sh = shr + (int)(w & 0xffu);
                         const long long Tn = (long long)(T[jj] + (unsigned long long)shl64(Ij, (uint32_t)sh));
@@ -869,14 +910,23 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             if (!ok) break;
 
             // ---- this piece's exact partial sums go to the finalize kernel
-            // (deferred outputs: a sentinel no sum reaches, |T| < 2^62), stored
-            // column-major so that a warp's 32 rows make one contiguous store
+            // (deferred outputs: a sentinel no sum reaches, |T| < 2^62), row-major:
+            // a lane's 32 outputs are 256 contiguous bytes of its row
             if (i < p.rows) {
-                long long *tcol = p.Tout + (int64_t)piece * p.rows * p.cols + jw * p.rows + i;
+                long long *trow = p.Tout + (int64_t)piece * p.rows * p.cols + i * p.cols + jw;
+                if (jw + 32 <= p.cols && (p.cols & 1) == 0) {        // 16-byte aligned pairs
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    if (jw + jj < p.cols)
-                        tcol[(int64_t)jj * p.rows] = ((defer >> jj) & 1u) ? kDeferredSum : (long long)T[jj];
+                    for (int jj = 0; jj < 32; jj += 2) {
+                        const long long v0 = ((defer >> jj) & 1u) ? kDeferredSum : (long long)T[jj];
+                        const long long v1 = ((defer >> (jj + 1)) & 1u) ? kDeferredSum : (long long)T[jj + 1];
+                        *reinterpret_cast<longlong2 *>(trow + jj) = make_longlong2(v0, v1);
+                    }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        if (jw + jj < p.cols)
+                            trow[jj] = ((defer >> jj) & 1u) ? kDeferredSum : (long long)T[jj];
+                }
             }
             // outputs for the fix-up pass
             for (uint32_t dm = defer; dm != 0u; dm &= dm - 1u) {
@@ -918,6 +968,7 @@ __device__ __forceinline__ __int128 round_i128_to_53_bits(__int128 I) {
     return neg ? -r : r;
 }
 
+template <bool SUPER>
 __global__ void __launch_bounds__(256)
 exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
                           int64_t LpA, int64_t LpB, const int *__restrict__ GA,
@@ -955,7 +1006,7 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
             I += ((__int128)hi << 64) | (__int128)(unsigned long long)lo;
         }
         if (lane != 0) continue;
-        const __int128 J = round_i128_to_53_bits(I);
+        const __int128 J = SUPER ? I : round_i128_to_53_bits(I);
         const int sh = (sa.x - __ldg(&GA[i])) + (sb.x - __ldg(&GB[j]));
         bool ok = sh >= 0 && sh < 62;
         __int128 v = 0;
@@ -964,7 +1015,7 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
             ok = (v >> sh) == J && v >= -((__int128)1 << 61) && v < ((__int128)1 << 61);
         }
         if (ok) {
-            long long *slot = Tout + (q / cps) * p.rows * p.cols + j * p.rows + i;
+            long long *slot = Tout + (q / cps) * p.rows * p.cols + i * p.cols + j;
             const long long add = (long long)v;
             const long long old = (long long)atomicAdd(reinterpret_cast<unsigned long long *>(slot),
                                                        (unsigned long long)add);
@@ -992,35 +1043,62 @@ __global__ void exact_count_kernel(const unsigned int *chunk_count, unsigned int
 // even), all on integers; values outside those fast ranges take the float64
 // route.  The chunk range of an output may have been split into pieces whose
 // partial sums T add exactly.  One thread per 8 consecutive outputs of a row,
-// consecutive threads on consecutive rows (T is stored column-major).
-template <bool OUT_F64>
+// consecutive threads on consecutive groups of the same row (T is stored
+// row-major), so a warp reads 2 KiB of sums and writes 512 bytes of outputs,
+// each contiguous.
+// Output modes of the finalize: the KBN tier's bf16 outputs, its float64
+// values (inspection), and the correctly rounded tier's bf16 outputs (the
+// exact total and the bias rounded once, never through float64).
+constexpr int kFinBf16 = 0, kFinF64 = 1, kFinSuper = 2;
+
+template <int MODE>
 __global__ void __launch_bounds__(256)
 exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int *__restrict__ GA,
                       const int *__restrict__ GB, const unsigned short *__restrict__ bias, void *out,
                       int64_t rows, int64_t cols, int vec_out) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // a row per thread
-    if (i >= rows) return;
-    const int64_t gpr = (cols + 7) / 8;
+    const int64_t gpr = (cols + 7) / 8;                  // 8-column groups per row
     const int64_t plane = rows * cols;
-    const int gx = __ldg(&GA[i]);
-    for (int64_t jg = blockIdx.y; jg < gpr; jg += gridDim.y) {   // 8 columns per step
-        const int64_t j0 = jg * 8;
-        // every load first: the partial sums (a warp reads 32 consecutive
-        // rows of one column), the column grains and the bias
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < rows * gpr;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = g / gpr, j0 = (g % gpr) * 8;
+        const int gx = __ldg(&GA[i]);
+        const long long *trow = Tout + i * cols + j0;
+        // every load first: the partial sums, the column grains and the bias
         long long t0[8], t1[8];
         int gw[8];
         uint32_t hb[8];
+        if (vec_out && j0 + 8 <= cols) {                  // 16-byte aligned groups
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const bool in = j0 + e < cols;
-            t0[e] = in ? __ldg(&Tout[(j0 + e) * rows + i]) : 0ll;
-            t1[e] = (in && pieces > 1) ? __ldg(&Tout[plane + (j0 + e) * rows + i]) : 0ll;
-            gw[e] = in ? __ldg(&GB[j0 + e]) : 0;
-            hb[e] = (in && bias != nullptr) ? ld_bits(bias, j0 + e) : 0u;
+            for (int e = 0; e < 8; e += 2) {
+                const longlong2 a = __ldg(reinterpret_cast<const longlong2 *>(trow + e));
+                t0[e] = a.x; t0[e + 1] = a.y;
+                if (pieces > 1) {
+                    const longlong2 b2 = __ldg(reinterpret_cast<const longlong2 *>(trow + plane + e));
+                    t1[e] = b2.x; t1[e + 1] = b2.y;
+                } else {
+                    t1[e] = 0ll; t1[e + 1] = 0ll;
+                }
+            }
+            const int4 g0 = __ldg(reinterpret_cast<const int4 *>(GB + j0));
+            const int4 g1 = __ldg(reinterpret_cast<const int4 *>(GB + j0 + 4));
+            gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
+            gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hb[e] = bias != nullptr ? ld_bits(bias, j0 + e) : 0u;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const bool in = j0 + e < cols;
+                t0[e] = in ? __ldg(trow + e) : 0ll;
+                t1[e] = (in && pieces > 1) ? __ldg(trow + plane + e) : 0ll;
+                gw[e] = in ? __ldg(&GB[j0 + e]) : 0;
+                hb[e] = (in && bias != nullptr) ? ld_bits(bias, j0 + e) : 0u;
+            }
         }
         uint32_t packed[4] = {0u, 0u, 0u, 0u};
         uint32_t skip = 0u;
-        if (!OUT_F64 && pieces == 1) {
+        constexpr bool OUT_F64 = MODE == kFinF64;
+        if (MODE == kFinBf16 && pieces == 1) {
             // one piece: 64-bit sums; the common case (the bias joins the sum
             // exactly, the two roundings on the integer) stays straight-line,
             // the rest takes the float64 route of out_bits_f64
@@ -1061,12 +1139,19 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             bool deferred = t0[e] == kDeferredSum || (pieces > 1 && t1[e] == kDeferredSum);
             __int128 acc = (__int128)t0[e] + (__int128)t1[e];
             for (int k = 2; k < pieces && !deferred; ++k) {
-                const long long t = __ldg(&Tout[k * plane + j * rows + i]);
+                const long long t = __ldg(&Tout[k * plane + i * cols + j]);
                 deferred = t == kDeferredSum;
                 acc += t;
             }
             if (deferred) { skip |= 1u << e; continue; }
             const int G = gx + gw[e];
+            if (MODE == kFinSuper) {
+                int bm = 0, be = 0;
+                bool bad = false;
+                if (bias != nullptr) decode(hb[e], bm, be, bad);
+                packed[e / 2] |= sacc::exact_sum_bf16(acc, G, bm, be, bad, hb[e]) << (16 * (e & 1));
+                continue;
+            }
             const bool small = acc >= -((__int128)1 << 62) && acc < ((__int128)1 << 62);
             if (OUT_F64 || !small) {
                 double y = small ? round_int_to_double((long long)acc, G) : round_i128_to_double(acc, G);
@@ -1110,54 +1195,52 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
     }
 }
 
-template <bool F64>
+template <int MODE>
 cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const TcxArgs &a, int grid,
-                           const IArgs &ia, const int4 *SA, const int4 *SB, int64_t LpA, int64_t LpB,
-                           unsigned int *work, cudaStream_t s) {
-    auto kern = exact_tc_kernel<F64>;
+                           const Problem &prob, const IArgs &ia, const int4 *SA, const int4 *SB,
+                           int64_t LpA, int64_t LpB, unsigned int *work, const CallEvents &ev,
+                           cudaStream_t s) {
+    constexpr bool SUPER = MODE == kFinSuper;
+    auto kern = exact_tc_kernel<SUPER>;
     const int smem = (int)sizeof(TcxSmem) + 1024;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    cudaEvent_t t0 = nullptr, t1 = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(g_timing_mu);
-        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-        if (g_timing_on && cudaStreamIsCapturing(s, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone &&
-            cudaEventCreate(&t0) == cudaSuccess && cudaEventCreate(&t1) == cudaSuccess) {
-            g_timing_events.emplace_back(t0, t1);
-        } else {
-            t0 = t1 = nullptr;
-        }
-    }
-    if (t0) cudaEventRecord(t0, s);
+    if (ev.e[1]) cudaEventRecord(ev.e[1], s);
     kern<<<grid, kTcxThreads, smem, s>>>(ma, mb, a);
     count_launch();
-    if (t1) cudaEventRecord(t1, s);
+    if (ev.e[2]) cudaEventRecord(ev.e[2], s);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    exact_chunk_repair_kernel<<<kFixBlocks, 256, 0, s>>>(ia, SA, SB, LpA, LpB, a.GA, a.GB, a.chunk_count,
-                                                          a.chunk_list, a.chunk_cap, a.Tout, a.cps,
-                                                          work, work + 1);
+    exact_chunk_repair_kernel<SUPER><<<kFixBlocks, 256, 0, s>>>(
+        ia, SA, SB, LpA, LpB, a.GA, a.GB, a.chunk_count, a.chunk_list, a.chunk_cap, a.Tout, a.cps,
+        work, work + 1);
     count_launch();
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    if (t0) {
+    if (ev.e[0]) {
         exact_count_kernel<<<1, 1, 0, s>>>(a.chunk_count, a.chunk_cap, work);
         count_launch();
     }
     {
-        const int64_t gpr = (a.cols + 7) / 8;
-        const dim3 grid((unsigned)((a.rows + 255) / 256), (unsigned)(gpr < 65535 ? gpr : 65535));
+        const int64_t groups = a.rows * ((a.cols + 7) / 8);
+        const int64_t want = (groups + 255) / 256, cap = 152 * 64;
+        const unsigned grid = (unsigned)(want < cap ? want : cap);
         const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0 && (a.cols % 8) == 0) ? 1 : 0;
-        exact_finalize_kernel<F64><<<grid, 256, 0, s>>>(a.Tout, a.splits, a.GA, a.GB, a.bias, a.out,
-                                                         a.rows, a.cols, vec_out);
+        exact_finalize_kernel<MODE><<<grid, 256, 0, s>>>(a.Tout, a.splits, a.GA, a.GB, a.bias, a.out,
+                                                          a.rows, a.cols, vec_out);
         count_launch();
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
-    exact_fixup_kernel<F64><<<kFixBlocks, kFixWarps * 32, 0, s>>>(ia, SA, SB, LpA, LpB, work, work + 1);
-    count_launch();
-    return cudaGetLastError();
+    if (SUPER) {
+        err = superacc_fixup_bf16(prob, work, work + 1, kFixBlocks, s);
+    } else {
+        exact_fixup_kernel<MODE == kFinF64><<<kFixBlocks, kFixWarps * 32, 0, s>>>(ia, SA, SB, LpA, LpB, work, work + 1);
+        count_launch();
+        err = cudaGetLastError();
+    }
+    if (ev.e[3]) cudaEventRecord(ev.e[3], s);
+    return err;
 }
 
 // Pieces the chunk range of each output tile is cut into: the smallest count
@@ -1224,11 +1307,13 @@ row_order_kernel(const int *__restrict__ flag, int64_t rows, int64_t Lp, int *__
 
 }  // namespace
 
-carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t stream) {
+carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, bool super, cudaStream_t stream) {
     if (p.rows == 0 || p.cols == 0) return CARBON_OK;
     // deferred outputs are listed by 32-bit index; larger outputs take the
-    // float64 kernel, which computes the same bits
-    if (p.rows * p.cols >= ((int64_t)1 << 32)) return exact_launch(p, out_f64, stream);
+    // float64 kernel (or the warp-per-output superaccumulator), which compute
+    // the same bits
+    if (p.rows * p.cols >= ((int64_t)1 << 32))
+        return super ? superacc_launch(p, stream) : exact_launch(p, out_f64, stream);
     int dev = 0, sms = 0;
     carbon_status_t st = current_device(&dev, &sms);
     if (st != CARBON_OK) return st;
@@ -1287,6 +1372,8 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
     unsigned int *ccount = reinterpret_cast<unsigned int *>(clist + ccap);   // chunk repairs, work units
     unsigned int *work = ccount + 4;
 
+    const CallEvents ev = timing_events(stream);
+    if (ev.e[0]) cudaEventRecord(ev.e[0], stream);
     // the deferral counter and the plane counts start at 0, the line grains
     // at kGrainNone
     err = cudaMemsetAsync(work, 0, sizeof(unsigned int), stream);
@@ -1332,6 +1419,7 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         a.out = p.out;
         a.rows = p.rows; a.cols = p.cols; a.LpA = LpA; a.LpB = LpB;
         a.tiles_m = (int)tiles_m; a.tiles_n = (int)tiles_n; a.nchunks = (int)nchunks;
+        a.row_fast = LpB > LpA ? 1 : 0;                  // keep the larger planes' tiles together
         a.splits = pieces;
         a.cps = (int)((nchunks + pieces - 1) / pieces);
         a.SA = SA; a.SB = SB; a.GA = GA; a.GB = GB; a.cntA = cntA; a.invA = invA;
@@ -1344,8 +1432,9 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
         a.unit_counter = ccount + 1;
         const int64_t units = tiles_m * tiles_n * pieces;
         const int grid = (int)(units < sms ? units : sms);
-        err = out_f64 ? launch_tc_main<true>(ma, mb, a, grid, ia, SA, SB, LpA, LpB, work, stream)
-                      : launch_tc_main<false>(ma, mb, a, grid, ia, SA, SB, LpA, LpB, work, stream);
+        err = super ? launch_tc_main<kFinSuper>(ma, mb, a, grid, p, ia, SA, SB, LpA, LpB, work, ev, stream)
+            : out_f64 ? launch_tc_main<kFinF64>(ma, mb, a, grid, p, ia, SA, SB, LpA, LpB, work, ev, stream)
+                      : launch_tc_main<kFinBf16>(ma, mb, a, grid, p, ia, SA, SB, LpA, LpB, work, ev, stream);
     }
     const cudaError_t ferr = cudaFreeAsync(ws, stream);
     if (err == cudaSuccess) err = ferr;
@@ -1355,7 +1444,8 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, cudaStream_t str
 void exact_tc_timing(int enable) {
     std::lock_guard<std::mutex> lk(g_timing_mu);
     if (enable) {
-        for (auto &e : g_timing_events) { cudaEventDestroy(e.first); cudaEventDestroy(e.second); }
+        for (auto &c : g_timing_events)
+            for (auto &e : c.e) cudaEventDestroy(e);
         g_timing_events.clear();
         const unsigned long long zero = 0;
         cudaMemcpyToSymbol(g_exact_tc_kgroups, &zero, sizeof zero);
@@ -1365,24 +1455,46 @@ void exact_tc_timing(int enable) {
     g_timing_on = enable != 0;
 }
 
+// Milliseconds between events a and b of every recorded call, summed.
+static cudaError_t sum_between(int a, int b, double *total) {
+    *total = 0.0;
+    for (auto &c : g_timing_events) {
+        if (c.e[a] == nullptr || c.e[b] == nullptr) continue;
+        cudaError_t err = cudaEventSynchronize(c.e[b]);
+        float t = 0.0f;
+        if (err == cudaSuccess) err = cudaEventElapsedTime(&t, c.e[a], c.e[b]);
+        if (err != cudaSuccess) return err;
+        *total += t;
+    }
+    return cudaSuccess;
+}
+
 carbon_status_t exact_tc_time(double *ms, int64_t *launches, int64_t *kgroups) {
     std::lock_guard<std::mutex> lk(g_timing_mu);
     double total = 0.0;
-    for (auto &e : g_timing_events) {
-        cudaError_t err = cudaEventSynchronize(e.second);
-        float t = 0.0f;
-        if (err == cudaSuccess) err = cudaEventElapsedTime(&t, e.first, e.second);
-        if (err != cudaSuccess) return note_cuda(err);
-        total += t;
-    }
+    const cudaError_t err = sum_between(1, 2, &total);
+    if (err != cudaSuccess) return note_cuda(err);
     if (ms) *ms = total;
     if (launches) *launches = (int64_t)g_timing_events.size();
     if (kgroups) {
         unsigned long long v = 0;
-        const cudaError_t err = cudaMemcpyFromSymbol(&v, g_exact_tc_kgroups, sizeof v);
-        if (err != cudaSuccess) return note_cuda(err);
+        const cudaError_t e2 = cudaMemcpyFromSymbol(&v, g_exact_tc_kgroups, sizeof v);
+        if (e2 != cudaSuccess) return note_cuda(e2);
         *kgroups = (int64_t)v;
     }
+    return CARBON_OK;
+}
+
+carbon_status_t exact_tc_phase_time(double *pre_ms, double *main_ms, double *post_ms) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    double v[3];
+    for (int k = 0; k < 3; ++k) {
+        const cudaError_t err = sum_between(k, k + 1, &v[k]);
+        if (err != cudaSuccess) return note_cuda(err);
+    }
+    if (pre_ms) *pre_ms = v[0];
+    if (main_ms) *main_ms = v[1];
+    if (post_ms) *post_ms = v[2];
     return CARBON_OK;
 }
 

@@ -11,13 +11,16 @@ It Works").
     backward  dX = dY.W^T        carbon_gemm_dx
               dW = X^T.dY        carbon_gemm_dw
               db = sum_t dY[t]   carbon_gemm_dw with a column of ones for X,
-                                 always on the exact tier
+                                 on the exact tier (on the correctly
+                                 rounded tier when the layer uses it)
 
 The bias gradient is the one piece the sgemm-bi page leaves to a plain
 PyTorch column sum ("Determinism contracts"); here it is the exact tier's
 fixed-order sum over tokens (256-token chunks summed with KBN, the chunk
 values combined with KBN, one rounding), so it is bit-identical run to run,
-for every batch split into the same tokens, and to the CPU oracle.
+for every batch split into the same tokens, and to the CPU oracle.  A layer
+on the correctly rounded tier ("superacc") takes db from that tier too: the
+exact column sum rounded once.
 
 Leading dimensions of the input are flattened into the token dimension.
 There is no CPU path: inputs must be CUDA tensors (float32, bfloat16 or
@@ -32,16 +35,18 @@ import torch
 from . import _dtype_code, carbon_gemm_dw, linear_dw, linear_dx, linear_fwd
 
 
-def bias_grad(dY, stream=None):
-    """db[N] = sum over tokens t of dY[t, :], on the exact tier: the GEMM
-    dW = X^T.dY with X a column of ones (every product is exact), in dY's
-    dtype."""
+def bias_grad(dY, stream=None, tier="exact"):
+    """db[N] = sum over tokens t of dY[t, :]: the GEMM dW = X^T.dY with X a
+    column of ones (every product is exact), in dY's dtype, on the exact tier
+    (fixed-order KBN) or, with tier="superacc", correctly rounded."""
+    if tier not in ("exact", "superacc"):
+        raise ValueError("the bias gradient runs on the exact or the superacc tier")
     if dY.dim() != 2 or not dY.is_contiguous() or not dY.is_cuda:
         raise ValueError("dY must be a contiguous 2-D CUDA tensor")
     M, N = dY.shape
     ones = torch.ones((M, 1), dtype=dY.dtype, device=dY.device)
     db = torch.empty((1, N), dtype=dY.dtype, device=dY.device)
-    carbon_gemm_dw(db, ones, dY, M, 1, N, _dtype_code(dY), "exact", stream)
+    carbon_gemm_dw(db, ones, dY, M, 1, N, _dtype_code(dY), tier, stream)
     return db.view(N)
 
 
@@ -69,7 +74,7 @@ class _LinearFunction(torch.autograd.Function):
         if ctx.needs_input_grad[1]:
             dw = linear_dw(x2, g2, ctx.tier)
         if ctx.has_bias and ctx.needs_input_grad[2]:
-            db = bias_grad(g2)
+            db = bias_grad(g2, tier="superacc" if ctx.tier == "superacc" else "exact")
         return dx, dw, db, None
 
 

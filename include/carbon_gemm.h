@@ -13,7 +13,7 @@
  * columns).  M is the number of tokens (rows of X, dY); K = in-features,
  * N = out-features.  Every operand and the output have the same dtype.
  *
- * Two tiers (tier argument):
+ * Three tiers (tier argument):
  *
  * CARBON_TIER_EXACT - every product is formed in float64 (exactly: products
  *   of two fp32, two bf16 or two fp16 values fit in binary64), and products are summed
@@ -43,6 +43,22 @@
  *   CARBON_ERR_UNSUPPORTED).  Base
  *   pointers must be 16-byte aligned and K and N multiples of 8 (16-byte row
  *   pitch), else CARBON_ERR_MISALIGNED.
+ *
+ * CARBON_TIER_SUPERACC - the correctly rounded tier (Carbon README,
+ *   "Roadmap": superaccumulators, exact summation that needs no fixed
+ *   order): the exact value of sum_r A(i,r) B(r,j) (+ bias), rounded once, to
+ *   nearest-even, to the output type.  No order of the reduction shows in
+ *   the result, so it is the same for any split or order of the reduction,
+ *   as well as for every run, every M and every device.  An exact sum of
+ *   zero gives +0; NaN operands (or inf times 0, or both infinities) give
+ *   NaN, otherwise an infinite product or bias gives that infinity.  It
+ *   differs from CARBON_TIER_EXACT where KBN's chunk values or its float64
+ *   value round (e.g. 2^100 + 1 in one 256-chunk and -2^100 + 1 in the next:
+ *   exact tier 0, this tier 2).  Accepts CARBON_F32, CARBON_BF16 and
+ *   CARBON_F16, any shape and alignment.  bf16 runs the tensor-core exact
+ *   sums of CARBON_TIER_EXACT (same workspace, below) without its rounding of
+ *   chunk values; fp32 and fp16 run one warp per output over the reduction
+ *   (no workspace; far slower than the bf16 path).
  *
  * Conventions
  *   - Pointers are DEVICE pointers on the current CUDA device; the caller
@@ -109,8 +125,9 @@ typedef enum {
 } carbon_dtype_t;
 
 typedef enum {
-    CARBON_TIER_EXACT = 0,  /* float64 products, fixed-order KBN, one RNE */
-    CARBON_TIER_TC = 1      /* bf16 or fp16 tcgen05 MMA, fp32 accumulate */
+    CARBON_TIER_EXACT = 0,    /* float64 products, fixed-order KBN, one RNE */
+    CARBON_TIER_TC = 1,       /* bf16 or fp16 tcgen05 MMA, fp32 accumulate */
+    CARBON_TIER_SUPERACC = 2  /* exact sum (+ bias) rounded once: correctly rounded */
 } carbon_tier_t;
 
 typedef enum {
@@ -151,7 +168,8 @@ carbon_status_t carbon_gemm_dw(void *dW, const void *X, const void *dY,
  * the call returns; CARBON_ERR_CUDA if the pool cannot supply it).
  * CARBON_TIER_TC: the fp32 accumulator of the tensor-core kernels, the value
  * carbon_gemm_dw would round to bf16.  Arguments, alignment and errors as for
- * carbon_gemm_dw with CARBON_BF16. */
+ * carbon_gemm_dw with CARBON_BF16.  CARBON_TIER_SUPERACC:
+ * CARBON_ERR_UNSUPPORTED. */
 carbon_status_t carbon_gemm_dw_f32(float *dW, const void *X, const void *dY,
                                    int64_t M, int64_t K, int64_t N,
                                    carbon_tier_t tier, carbon_stream_t stream);
@@ -195,6 +213,44 @@ carbon_status_t carbon_gemm_exact_bf16_noalloc(carbon_pass_t pass, void *out, co
                                                int64_t M, int64_t K, int64_t N,
                                                carbon_stream_t stream);
 
+/* ---- reductions split across ranks (exact tier) ----------------------------
+ *
+ * The Carbon README ("How It Works") replaces the data-parallel gradient
+ * all-reduce with an all-gather followed by a reduction in rank order; its
+ * "Roadmap" lists a deterministic multi-GPU all-reduce.  With the exact
+ * tier's fixed order, a reduction split across ranks on 256-index chunk
+ * boundaries can give the single-device bits exactly: each rank computes the
+ * chunk values of its own chunks (they are the same doubles the single-device
+ * call forms), the chunk values are gathered in rank order (= chunk order),
+ * and the outer KBN, the bias and the rounding run once over all of them.
+ * Typical use is dW = X^T . dY with the tokens (M) split across ranks: rank
+ * r holds tokens [m_r, m_{r+1}) with every m_r a multiple of 256. */
+
+/* Chunk values of one rank's share of the reduction.  pass, A, B, M, K, N and
+ * dtype as in carbon_gemm_fwd / _dx / _dw with CARBON_TIER_EXACT (bias is not
+ * taken: it joins in carbon_chunk_values_combine), the reduction being this
+ * rank's share only (e.g. dW: A = X rows m_r .. m_{r+1}-1, B = the same rows
+ * of dY, M = m_{r+1} - m_r).  P: device float64 [C][rows][cols], C =
+ * ceil(R / 256), rows x cols the output shape of the pass; P[q][i][j] is the
+ * chunk value fl(s + c) of KBN over the products of reduction indices
+ * 256q .. min(256q + 255, R - 1), left to right.  Runs the float64 KBN kernel
+ * of the exact tier for every dtype (for bf16 slower than carbon_gemm_dw's
+ * tensor-core path); no workspace.  Errors as for the per-pass entry points;
+ * R == 0 writes nothing. */
+carbon_status_t carbon_gemm_chunk_values(carbon_pass_t pass, double *P, const void *A,
+                                         const void *B, int64_t M, int64_t K, int64_t N,
+                                         carbon_dtype_t dtype, carbon_stream_t stream);
+
+/* out[i][j] = RNE_dtype( KBN over q = 0 .. nchunks-1 of P[q][i][j], left to
+ * right, (+ bias[j]) ): the exact tier's steps after its chunk values.  With P
+ * the chunk values of every rank in rank order this is bit-identical to the
+ * single-device exact-tier call over the whole reduction.  P: device float64
+ * [nchunks][rows][cols]; bias: device, dtype-typed [cols], or NULL; out:
+ * device [rows][cols] of dtype.  nchunks == 0 gives +0 (or the bias). */
+carbon_status_t carbon_chunk_values_combine(void *out, const double *P, int64_t nchunks,
+                                            int64_t rows, int64_t cols, const void *bias,
+                                            carbon_dtype_t dtype, carbon_stream_t stream);
+
 /* Synchronises `stream`, then reports (and clears) the device status word
  * that kernels set when a bounded wait gives up (CARBON_ERR_TIMEOUT), or
  * CARBON_ERR_CUDA if the stream reports an error. */
@@ -208,10 +264,12 @@ const char *carbon_status_string(carbon_status_t status);
 const char *carbon_last_cuda_error(void);
 
 /* ABI version of this header: (major << 16) | minor.  Minor 1 added
- * carbon_gemm_exact_bf16_noalloc and CARBON_ERR_SCRATCH_LIMIT. */
+ * carbon_gemm_exact_bf16_noalloc and CARBON_ERR_SCRATCH_LIMIT; minor 2 the
+ * CARBON_TIER_SUPERACC tier, carbon_gemm_chunk_values and
+ * carbon_chunk_values_combine. */
 int carbon_abi_version(void);
 
-#define CARBON_ABI_VERSION ((1 << 16) | 1)
+#define CARBON_ABI_VERSION ((1 << 16) | 2)
 
 #ifdef __cplusplus
 }

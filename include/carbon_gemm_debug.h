@@ -76,6 +76,13 @@ void carbon_debug_kernel_timing(int enable);
  * since the last carbon_debug_kernel_timing(1).  Any pointer may be NULL. */
 carbon_status_t carbon_debug_kernel_time(double *ms, int64_t *launches, int64_t *plane_products);
 
+/* While kernel timing is on, the same calls' time split into three phases,
+ * summed over the calls in milliseconds (blocking): pre-pass (from the
+ * call's first device operation to the start of the tensor-core kernel:
+ * workspace set-up, digit planes, row order), the tensor-core kernel, and
+ * post-pass (chunk repair, finalize, fix-up).  Any pointer may be NULL. */
+carbon_status_t carbon_debug_exact_phase_time(double *pre_ms, double *main_ms, double *post_ms);
+
 /* While kernel timing is on, the bf16 exact tier also counts, per call, the
  * (output, chunk) pairs it recomputes in the chunk repair (a line of that
  * chunk too wide for the digit planes) and the outputs it recomputes whole

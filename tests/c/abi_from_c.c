@@ -22,7 +22,7 @@ int main(void)
 {
     void *fake = (void *)0x1000; /* never dereferenced */
     CHECK(carbon_abi_version() == CARBON_ABI_VERSION);
-    CHECK((carbon_abi_version() >> 16) == 1 && (carbon_abi_version() & 0xffff) >= 1);
+    CHECK((carbon_abi_version() >> 16) == 1 && (carbon_abi_version() & 0xffff) >= 2);
     CHECK(strcmp(carbon_status_string(CARBON_OK), "CARBON_OK") == 0);
     CHECK(strcmp(carbon_status_string(CARBON_ERR_MISALIGNED), "CARBON_ERR_MISALIGNED") == 0);
     /* argument errors come back before any device work */

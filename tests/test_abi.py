@@ -23,7 +23,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_status_names():
-    assert b.carbon_abi_version() == (1 << 16) | 1    # minor 1: the no-allocation entry point
+    assert b.carbon_abi_version() == (1 << 16) | 2    # minor 2: superacc tier, chunk values
     for code, name in b.STATUS.items():
         assert b.carbon_status_string(code) == name
 
@@ -95,3 +95,14 @@ def test_import_maps_no_cuda_library():
             "assert 'libcarbon_gemm' in open('/proc/self/maps').read()\n")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     subprocess.run([sys.executable, "-c", code], check=True, cwd=root)
+
+
+def test_superacc_tier_argument_checks():
+    SUPERACC = 2
+    # accepted as a tier: argument errors still come first, empty outputs are no-ops
+    assert b.lib.carbon_gemm_fwd(FAKE, FAKE, FAKE, None, -1, 3, 4, 0, SUPERACC, None) == INVALID
+    assert b.lib.carbon_gemm_dw(None, None, None, 5, 0, 4, 2, SUPERACC, None) == 0
+    assert b.lib.carbon_gemm_dx(FAKE, None, FAKE, 2, 3, 4, 1, SUPERACC, None) == INVALID
+    # no fp32 staging variant of the weight gradient on this tier
+    assert b.lib.carbon_gemm_dw_f32(FAKE, FAKE, FAKE, 16, 16, 16, SUPERACC, None) == UNSUPPORTED
+    assert b.lib.carbon_gemm_fwd(FAKE, FAKE, FAKE, None, 2, 3, 4, 0, 3, None) == INVALID

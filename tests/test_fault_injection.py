@@ -82,3 +82,14 @@ def test_noalloc_argument_errors_and_limit_come_first(injected):
     assert b.lib.carbon_gemm_exact_bf16_noalloc(
         0, FAKE, FAKE, FAKE, None, 8192, 3072, 768, None) == SCRATCH_LIMIT
     assert b.lib.carbon_gemm_exact_bf16_noalloc(0, FAKE, FAKE, FAKE, None, 0, 16, 16, None) == 0
+
+
+def test_chunk_value_entry_points_injected_failure(injected):
+    assert b.lib.carbon_gemm_chunk_values(2, FAKE, FAKE, FAKE, 300, 16, 16, 1, None) == CUDA_ERR
+    assert b.lib.carbon_chunk_values_combine(FAKE, FAKE, 2, 16, 16, None, 1, None) == CUDA_ERR
+    # argument errors first, empty outputs are no-ops
+    assert b.lib.carbon_gemm_chunk_values(5, FAKE, FAKE, FAKE, 300, 16, 16, 1, None) == INVALID
+    assert b.lib.carbon_gemm_chunk_values(2, None, FAKE, FAKE, 300, 16, 16, 1, None) == INVALID
+    assert b.lib.carbon_chunk_values_combine(FAKE, None, 2, 16, 16, None, 1, None) == INVALID
+    assert b.lib.carbon_chunk_values_combine(FAKE, FAKE, -1, 16, 16, None, 1, None) == INVALID
+    assert b.lib.carbon_chunk_values_combine(None, None, 2, 0, 16, None, 1, None) == 0
