@@ -561,9 +561,11 @@ def main():
         assert cg.carbon_get_device_status(stream.cuda_stream) == 0
         main_ms = main_n = main_kg = 0
         phases = None
+        repairs = fixups = 0
         if "exact" in tiers:
             main_ms, main_n, main_kg = cg.carbon_debug_kernel_time()
             phases = cg.carbon_debug_exact_phase_time()
+            repairs, fixups = cg.carbon_debug_exact_path_counts()
             cg.carbon_debug_kernel_timing(False)
 
         # per-GEMM kernel time: back-to-back eager launches between two events
@@ -634,6 +636,8 @@ def main():
                                         "exact_tc_kernel": _r(phases[1] / args.steps),
                                         "post_pass": _r(phases[2] / args.steps)}
                                        if phases else None),
+                "chunk_repairs_per_step": repairs // args.steps if phases else None,
+                "fixups_per_step": fixups // args.steps if phases else None,
                 "kernel_share_of_tier": _r(main_ms / ms) if ms > 0 else None,
                 "mma_flops_per_useful_flop": _r(kg_flops / fl_all) if fl_all > 0 else None,
                 "useful_tflops_kernel": _r(fl_all / (main_ms * 1e-3) / 1e12) if main_ms > 0 else None,

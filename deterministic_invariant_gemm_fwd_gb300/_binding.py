@@ -15,7 +15,9 @@ import os
 import re
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libcarbon_gemm.so")
+# CARBON_GEMM_LIBRARY may name another build of the library (the
+# bounds-checked libcarbon_gemm_bounds.so); default: the regular one.
+LIB_PATH = os.environ.get("CARBON_GEMM_LIBRARY") or os.path.join(HERE, "libcarbon_gemm.so")
 HEADERS = [os.path.join(os.path.dirname(HERE), "include", h)
            for h in ("carbon_gemm.h", "carbon_gemm_debug.h")]
 
@@ -24,7 +26,7 @@ TIER_EXACT, TIER_TC, TIER_SUPERACC = 0, 1, 2
 PASS_FWD, PASS_DX, PASS_DW = 0, 1, 2
 STATUS = {0: "CARBON_OK", 1: "CARBON_ERR_INVALID_ARG", 2: "CARBON_ERR_UNSUPPORTED",
           3: "CARBON_ERR_MISALIGNED", 4: "CARBON_ERR_CUDA", 5: "CARBON_ERR_TIMEOUT",
-          6: "CARBON_ERR_SCRATCH_LIMIT"}
+          6: "CARBON_ERR_SCRATCH_LIMIT", 7: "CARBON_ERR_OUT_OF_BOUNDS"}
 DTYPES = {"f32": F32, "bf16": BF16, "f16": F16}
 TIERS = {"exact": TIER_EXACT, "tc": TIER_TC, "superacc": TIER_SUPERACC}
 PASSES = {"fwd": PASS_FWD, "dx": PASS_DX, "dw": PASS_DW}

@@ -264,10 +264,14 @@ carbon_status_t carbon_get_device_status(carbon_stream_t stream) {
     const carbon_status_t ms = carbon::measure_take_device_status();
     const carbon_status_t ex = carbon::exact_take_device_status();
     const carbon_status_t et = carbon::exact_tc_take_device_status();
+    const carbon_status_t kb = carbon::kbn_take_device_status();
+    const carbon_status_t sa = carbon::superacc_take_device_status();
     if (st != CARBON_OK) return st;
     if (tc != CARBON_OK) return tc;
     if (ex != CARBON_OK) return ex;
     if (et != CARBON_OK) return et;
+    if (kb != CARBON_OK) return kb;
+    if (sa != CARBON_OK) return sa;
     return ms;
 }
 
@@ -280,6 +284,7 @@ const char *carbon_status_string(carbon_status_t status) {
     case CARBON_ERR_CUDA: return "CARBON_ERR_CUDA";
     case CARBON_ERR_TIMEOUT: return "CARBON_ERR_TIMEOUT";
     case CARBON_ERR_SCRATCH_LIMIT: return "CARBON_ERR_SCRATCH_LIMIT";
+    case CARBON_ERR_OUT_OF_BOUNDS: return "CARBON_ERR_OUT_OF_BOUNDS";
     }
     return "CARBON_ERR_UNKNOWN";
 }

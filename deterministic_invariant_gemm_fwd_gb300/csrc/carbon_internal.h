@@ -38,6 +38,34 @@ inline Problem make_problem(int pass, int dtype, void *out, const void *A, const
     return p;
 }
 
+// Launches kernel `kern` on `stream` with programmatic stream serialization:
+// it may be scheduled before the previous kernel on the stream has finished,
+// and must call wait_prior_grid() (device_sync.cuh) before touching global
+// memory.  cluster_x > 1 also sets a cluster of that many CTAs along x.
+template <typename... Params, typename... Args>
+cudaError_t launch_k(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, unsigned cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    unsigned n = 1;
+    if (cluster_x > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster_x;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Records a CUDA error message for carbon_last_cuda_error(); returns
 // CARBON_ERR_CUDA when err != cudaSuccess, CARBON_OK otherwise.
 carbon_status_t note_cuda(cudaError_t err);
@@ -99,5 +127,9 @@ carbon_status_t tc_take_device_status();
 
 // Measurement helpers (measure.cu).
 carbon_status_t measure_take_device_status();
+// Status words of the float64 KBN kernels and the superaccumulator
+// (bounds-checked build).
+carbon_status_t kbn_take_device_status();
+carbon_status_t superacc_take_device_status();
 
 }  // namespace carbon

@@ -75,6 +75,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Programmatic dependent launch.  The library launches its kernels with the
+// programmatic-serialization attribute (launch_k in carbon_internal.h), so a
+// kernel may be scheduled while the previous kernel on the stream is still
+// finishing: every kernel calls wait_prior_grid() before its first access to
+// global memory (which waits for the previous kernel to complete and its
+// writes to be visible; a no-op after a non-kernel stream operation), and
+// allow_next_grid() once its own CTAs are running, so the next kernel's CTAs
+// can take SMs as this kernel's CTAs retire and do their set-up meanwhile.
+__device__ __forceinline__ void wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_next_grid() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

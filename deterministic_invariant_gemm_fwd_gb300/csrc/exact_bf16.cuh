@@ -13,7 +13,9 @@
 // for an all-zero line, kWidthBad for a line holding inf or NaN.
 #pragma once
 
+#include "bounds.cuh"
 #include "carbon_internal.h"
+#include "device_sync.cuh"
 #include "exact_common.cuh"
 
 namespace carbon {
@@ -123,6 +125,10 @@ __device__ __forceinline__ int bit_count(unsigned long long v) { return 64 - __c
 constexpr int kFixWarps = 8;
 constexpr int kFixBlocks = 1024;
 
+// Status word of the fix-up kernel in the bounds-checked build (one per
+// translation unit that includes this header; read by its status function).
+__device__ unsigned int g_fixup_status = 0;
+
 template <bool OUT_F64>
 __global__ void __launch_bounds__(kFixWarps * 32)
 exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
@@ -130,25 +136,35 @@ exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__res
                    const unsigned int *__restrict__ work_list) {
     __shared__ double xs[kFixWarps][kChunk], ws[kFixWarps][kChunk];
     __shared__ double Pq[kFixWarps];
+    wait_prior_grid();
+    allow_next_grid();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t count = *work_count;
     const int64_t nq = (p.R + kChunk - 1) / kChunk;
+    const int64_t n_a = (p.rows > 0 && p.R > 0) ? (p.rows - 1) * p.a_si + (p.R - 1) * p.a_sr + 1 : 0;
+    const int64_t n_b = (p.cols > 0 && p.R > 0) ? (p.R - 1) * p.b_sr + (p.cols - 1) * p.b_sj + 1 : 0;
     for (int64_t item = blockIdx.x; item < count; item += gridDim.x) {
         const int64_t o = work_list[item];
         const int64_t i = o / p.cols, j = o % p.cols;
+        if (!in_bounds(&g_fixup_status, o, 1, p.rows * p.cols)) continue;
         double S = 0.0, C = 0.0;                        // thread 0's outer KBN state
         for (int64_t qb = 0; qb < nq; qb += kFixWarps) {
             const int64_t q = qb + warp;
             if (q < nq) {
                 const int64_t q0 = q * kChunk;
                 const int64_t qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
-                const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
+                const bool sok = in_bounds(&g_fixup_status, q * LpA + i, 1, nq * LpA) &&
+                                 in_bounds(&g_fixup_status, q * LpB + j, 1, nq * LpB);
+                const int4 sa = sok ? SA[q * LpA + i] : make_int4(0, kWidthBad, 0, 0);
+                const int4 sb = sok ? SB[q * LpB + j] : make_int4(0, kWidthBad, 0, 0);
                 uint32_t hx[kChunk / 32], hw[kChunk / 32];
 #pragma unroll
                 for (int t = 0; t < kChunk / 32; ++t) {
                     const int64_t r = q0 + lane + 32 * t;
-                    hx[t] = r < qend ? ld_bits(p.A, i * p.a_si + r * p.a_sr) : 0u;
-                    hw[t] = r < qend ? ld_bits(p.B, r * p.b_sr + j * p.b_sj) : 0u;
+                    hx[t] = (r < qend && in_bounds(&g_fixup_status, i * p.a_si + r * p.a_sr, 1, n_a))
+                                ? ld_bits(p.A, i * p.a_si + r * p.a_sr) : 0u;
+                    hw[t] = (r < qend && in_bounds(&g_fixup_status, r * p.b_sr + j * p.b_sj, 1, n_b))
+                                ? ld_bits(p.B, r * p.b_sr + j * p.b_sj) : 0u;
                 }
                 // KBN over a chunk captures every rounding error exactly and,
                 // while wx + ww < 90, also sums them exactly (each error is a
@@ -206,7 +222,7 @@ exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__res
         }
         if (threadIdx.x == 0) {
             double y = __dadd_rn(S, C);
-            if (p.bias) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
+            if (p.bias && in_bounds(&g_fixup_status, j, 1, p.cols)) y = __dadd_rn(y, widen_bf16(ld_bits(p.bias, j)));
             if (OUT_F64) static_cast<double *>(p.out)[o] = y;
             else static_cast<unsigned short *>(p.out)[o] = exact_round_bf16(y);
         }

@@ -550,10 +550,12 @@ carbon_status_t exact_int_launch(const Problem &p, bool out_f64, cudaStream_t st
 }
 
 carbon_status_t exact_take_device_status() {
-    unsigned int v = 0, zero = 0;
+    unsigned int v = 0, f = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_exact_status, sizeof v) != cudaSuccess) return CARBON_OK;
     if (v != 0) cudaMemcpyToSymbol(g_exact_status, &zero, sizeof zero);
-    return (carbon_status_t)v;
+    if (cudaMemcpyFromSymbol(&f, g_fixup_status, sizeof f) == cudaSuccess && f != 0)
+        cudaMemcpyToSymbol(g_fixup_status, &zero, sizeof zero);
+    return (carbon_status_t)(v != 0 ? v : f);
 }
 
 }  // namespace carbon

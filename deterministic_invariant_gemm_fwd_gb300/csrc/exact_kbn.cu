@@ -50,6 +50,8 @@
 // unchanged (s is never -0: it starts at +0 and fl(a + b) is -0 only when
 // both are -0).
 #include "carbon_internal.h"
+#include "bounds.cuh"
+#include "device_sync.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -58,6 +60,10 @@
 
 namespace carbon {
 namespace {
+
+// Status word: CARBON_ERR_OUT_OF_BOUNDS in the bounds-checked build.
+__device__ unsigned int g_kbn_status = 0;
+#define CHK(idx, len, n) in_bounds(&g_kbn_status, (int64_t)(idx), (int64_t)(len), (int64_t)(n))
 
 constexpr int kChunk = 256;              // documented chunk width
 constexpr int kBK = 32;                  // reduction slice staged per step (divides kChunk)
@@ -74,6 +80,7 @@ struct KArgs {
     int64_t rows, cols, R;
     int64_t a_si, a_sr, b_sr, b_sj;
     int64_t tiles_n;
+    int64_t n_a, n_b;                    // operand extents (elements), for the bounds checks
 };
 
 // Grain keys for the exactness proof, kept shifted left by 20 so they compare
@@ -165,7 +172,8 @@ __device__ __forceinline__ void stage_slice(const KArgs &p, double (*As)[kBM + 1
         else                        { rr = e % kBK; ii = e / kBK; }   // r contiguous in memory
         const int64_t i = i0 + ii, r = r0 + rr;
         double v = 0.0;
-        if (i < p.rows && r < rend) v = widen(load_bits<DT>(p.A, i * p.a_si + r * p.a_sr));
+        if (i < p.rows && r < rend && CHK(i * p.a_si + r * p.a_sr, 1, p.n_a))
+            v = widen(load_bits<DT>(p.A, i * p.a_si + r * p.a_sr));
         As[rr][ii] = v;
         Ag[rr][ii] = grain_key_a(v);
     }
@@ -177,7 +185,8 @@ __device__ __forceinline__ void stage_slice(const KArgs &p, double (*As)[kBM + 1
         else                        { jj = e % kBN; rr = e / kBN; }   // j contiguous in memory
         const int64_t j = j0 + jj, r = r0 + rr;
         double v = 0.0;
-        if (j < p.cols && r < rend) v = widen(load_bits<DT>(p.B, r * p.b_sr + j * p.b_sj));
+        if (j < p.cols && r < rend && CHK(r * p.b_sr + j * p.b_sj, 1, p.n_b))
+            v = widen(load_bits<DT>(p.B, r * p.b_sr + j * p.b_sj));
         Bs[rr][jj] = v;
         Bg[rr][jj] = grain_key_b(v);
     }
@@ -195,6 +204,8 @@ exact_kbn_kernel(const KArgs p) {
     __shared__ double Bs[kBK][kBN + 1];
     __shared__ int Ag[kBK][kBM + 1];
     __shared__ int Bg[kBK][kBN + 1];
+    wait_prior_grid();
+    allow_next_grid();
     const int tid = threadIdx.x;
     const int tx = tid % kTX, ty = tid / kTX;
     const int64_t tile = blockIdx.x;
@@ -293,7 +304,10 @@ exact_kbn_kernel(const KArgs p) {
 #pragma unroll
                 for (int n = 0; n < kTN; ++n) {
                     const int64_t i = i0 + ty + kTY * m, j = j0 + tx + kTX * n;
-                    if (i < p.rows && j < p.cols) P[i * p.cols + j] = __dadd_rn(s[m][n], c[m][n]);
+                    if (i < p.rows && j < p.cols &&
+                        CHK((q0 / kChunk) * p.rows * p.cols + i * p.cols + j, 1,
+                            ((p.R + kChunk - 1) / kChunk) * p.rows * p.cols))
+                        P[i * p.cols + j] = __dadd_rn(s[m][n], c[m][n]);
                 }
         } else {
 #pragma unroll
@@ -315,6 +329,7 @@ exact_kbn_kernel(const KArgs p) {
             double y = __dadd_rn(S[m][n], C[m][n]);
             if (p.bias) y = __dadd_rn(y, widen(load_bits<DT>(p.bias, j)));
             const int64_t o = i * p.cols + j;
+            if (!CHK(o, 1, p.rows * p.cols)) continue;
             if (OUT == kOutF64)
                 static_cast<double *>(p.out)[o] = y;
             else if (DT == CARBON_F32)
@@ -329,6 +344,8 @@ exact_kbn_kernel(const KArgs p) {
 }
 
 __global__ void round_kernel(int dtype, void *out, const double *in, int64_t n) {
+    wait_prior_grid();
+    allow_next_grid();
     for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < n;
          k += (int64_t)gridDim.x * blockDim.x) {
         const double y = in[k];
@@ -340,8 +357,7 @@ __global__ void round_kernel(int dtype, void *out, const double *in, int64_t n) 
 
 template <int DT, int PASS, int OUT>
 cudaError_t launch_one(const KArgs &a, int64_t tiles, cudaStream_t stream) {
-    exact_kbn_kernel<DT, PASS, OUT><<<(unsigned)tiles, kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_k(exact_kbn_kernel<DT, PASS, OUT>, dim3((unsigned)tiles), dim3(kThreads), 0, stream, 1, a);
 }
 
 template <int DT, int PASS>
@@ -367,11 +383,14 @@ template <int DT>
 __global__ void __launch_bounds__(256)
 combine_kernel(void *out, const double *__restrict__ P, int64_t nchunks, int64_t rows, int64_t cols,
                const void *bias) {
+    wait_prior_grid();
+    allow_next_grid();
     const int64_t n = rows * cols;
     for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < n;
          o += (int64_t)gridDim.x * blockDim.x) {
         double S = 0.0, C = 0.0;
-        for (int64_t q = 0; q < nchunks; ++q) kbn_value_step(S, C, __ldg(&P[q * n + o]));
+        for (int64_t q = 0; q < nchunks; ++q)
+            if (CHK(q * n + o, 1, nchunks * n)) kbn_value_step(S, C, __ldg(&P[q * n + o]));
         double y = __dadd_rn(S, C);
         if (bias) y = __dadd_rn(y, widen(load_bits<DT>(bias, o % cols)));
         if (DT == CARBON_F32) static_cast<float *>(out)[o] = __double2float_rn(y);
@@ -390,6 +409,8 @@ KArgs make_kargs(const Problem &p) {
     default:              a.a_si = 1;   a.a_sr = p.K; a.b_sr = p.N; a.b_sj = 1; break;
     }
     a.tiles_n = (p.cols + kBN - 1) / kBN;
+    a.n_a = (p.rows > 0 && p.R > 0) ? (p.rows - 1) * a.a_si + (p.R - 1) * a.a_sr + 1 : 0;
+    a.n_b = (p.cols > 0 && p.R > 0) ? (p.R - 1) * a.b_sr + (p.cols - 1) * a.b_sj + 1 : 0;
     return a;
 }
 
@@ -419,11 +440,13 @@ carbon_status_t exact_combine_launch(int dtype, void *out, const double *P, int6
     const int64_t n = rows * cols;
     if (n == 0) return CARBON_OK;
     const int64_t blocks = (n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192;
-    if (dtype == CARBON_F32) combine_kernel<CARBON_F32><<<(unsigned)blocks, 256, 0, stream>>>(out, P, nchunks, rows, cols, bias);
-    else if (dtype == CARBON_F16) combine_kernel<CARBON_F16><<<(unsigned)blocks, 256, 0, stream>>>(out, P, nchunks, rows, cols, bias);
-    else combine_kernel<CARBON_BF16><<<(unsigned)blocks, 256, 0, stream>>>(out, P, nchunks, rows, cols, bias);
+    const dim3 g((unsigned)blocks), b(256);
+    cudaError_t err;
+    if (dtype == CARBON_F32) err = launch_k(combine_kernel<CARBON_F32>, g, b, 0, stream, 1, out, P, nchunks, rows, cols, bias);
+    else if (dtype == CARBON_F16) err = launch_k(combine_kernel<CARBON_F16>, g, b, 0, stream, 1, out, P, nchunks, rows, cols, bias);
+    else err = launch_k(combine_kernel<CARBON_BF16>, g, b, 0, stream, 1, out, P, nchunks, rows, cols, bias);
     count_launch();
-    return note_cuda(cudaGetLastError());
+    return note_cuda(err);
 }
 
 carbon_status_t exact_launch(const Problem &p, bool out_f64, cudaStream_t stream) {
@@ -434,9 +457,17 @@ carbon_status_t exact_round_launch(int dtype, void *out, const double *in, int64
                                    cudaStream_t stream) {
     if (n == 0) return CARBON_OK;
     const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
-    round_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dtype, out, in, n);
+    const cudaError_t err = launch_k(round_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                                     dtype, out, in, n);
     count_launch();
-    return note_cuda(cudaGetLastError());
+    return note_cuda(err);
+}
+
+carbon_status_t kbn_take_device_status() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_kbn_status, sizeof v) != cudaSuccess) return CARBON_OK;
+    if (v != 0) cudaMemcpyToSymbol(g_kbn_status, &zero, sizeof zero);
+    return (carbon_status_t)v;
 }
 
 }  // namespace carbon

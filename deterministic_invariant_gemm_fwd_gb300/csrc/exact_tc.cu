@@ -84,6 +84,7 @@
 // CARBON_ERR_TIMEOUT and raises a CTA-wide abort flag, and the CTA still waits
 // for its copies and MMAs in flight and frees its tensor memory.
 #include "carbon_internal.h"
+#include "bounds.cuh"
 #include "device_sync.cuh"
 #include "exact_bf16.cuh"
 #include "superacc.cuh"
@@ -99,6 +100,10 @@ namespace carbon {
 namespace {
 
 __device__ unsigned int g_exact_tc_status = 0;
+
+// Bounds check of elements [idx, idx + len) of a buffer of n elements (the
+// bounds-checked build; always true otherwise).
+#define CHK(idx, len, n) in_bounds(&g_exact_tc_status, (int64_t)(idx), (int64_t)(len), (int64_t)(n))
 __device__ unsigned long long g_exact_tc_kgroups = 0;   // plane products issued (measurement)
 __device__ unsigned long long g_exact_tc_repairs = 0;   // chunk repairs and fix-ups (measurement)
 __device__ unsigned long long g_exact_tc_fixups = 0;
@@ -193,6 +198,7 @@ struct TcxArgs {
     const int *invA;                                  // row of each place in the A planes
     const int *cntB;                                  // B planes per (column tile, chunk)
     unsigned int *work_count, *work_list;             // deferred outputs
+    int64_t work_cap;                                 // entries work_list can hold
     long long *Tout;                                  // exact sums in the output grain [piece][cols][rows]
     unsigned int *chunk_count;                        // (output, chunk) pairs for the chunk repair
     uint2 *chunk_list;
@@ -283,16 +289,25 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
                   int4 *__restrict__ stats, int *__restrict__ grain, int *__restrict__ cnt,
                   int nchunks, int vec, const int *__restrict__ pos, int *__restrict__ flag) {
     __shared__ __align__(16) unsigned short raw[RCONTIG ? 1 : kPrepLines * kRawPitch];
+    wait_prior_grid();
+    allow_next_grid();
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int64_t line0 = (int64_t)blockIdx.x * kPrepLines;
     const int q = blockIdx.y;
     const int64_t q0 = (int64_t)q * kChunk;
+    // extents for the bounds-checked build: the operand, the planes, the
+    // statistics, the per-line arrays and the per-(tile, chunk) counts
+    const int64_t n_src = (nlines > 0 && R > 0) ? (nlines - 1) * ls + (R - 1) * rs + 1 : 0;
+    const int64_t n_planes = (int64_t)kPlanes * Lp * Rp, n_stats = (int64_t)nchunks * Lp;
+    const int64_t n_cnt = (Lp / tg) * nchunks;
     if (!RCONTIG) {
         if (vec && line0 + kPrepLines <= nlines && q0 + kChunk <= R) {
             // 8 lines at one reduction index per 16-byte load
             for (int e = tid; e < kPrepLines / 8 * kChunk; e += kPrepThreads) {
                 const int lg = e % (kPrepLines / 8), r = e / (kPrepLines / 8);
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + (line0 + 8 * lg) + (q0 + r) * rs));
+                const int64_t at = (line0 + 8 * lg) + (q0 + r) * rs;
+                if (!CHK(at, 8, n_src)) continue;
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + at));
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int t = 0; t < 8; ++t)
@@ -302,18 +317,19 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
             for (int e = tid; e < kPrepLines * kChunk; e += kPrepThreads) {
                 const int l = e % kPrepLines, r = e / kPrepLines;
                 const int64_t line = line0 + l, rr = q0 + r;
-                raw[l * kRawPitch + r] = (line < nlines && rr < R) ? src[line * ls + rr * rs] : (unsigned short)0;
+                raw[l * kRawPitch + r] = (line < nlines && rr < R && CHK(line * ls + rr * rs, 1, n_src))
+                                             ? src[line * ls + rr * rs] : (unsigned short)0;
             }
         }
         __syncthreads();
     }
     for (int l = warp; l < kPrepLines; l += kPrepThreads / 32) {
         const int64_t L = line0 + l;
-        const int64_t LP = (pos != nullptr) ? (int64_t)__ldg(&pos[L]) : L;   // the line's place in the planes
+        const int64_t LP = (pos != nullptr && CHK(L, 1, Lp)) ? (int64_t)__ldg(&pos[L]) : L;   // the line's place in the planes
         uint32_t h[8];
         if (RCONTIG) {
             const int64_t r0 = q0 + 8 * lane;
-            if (vec && L < nlines && r0 + 8 <= R) {
+            if (vec && L < nlines && r0 + 8 <= R && CHK(L * ls + r0, 8, n_src)) {
                 const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + L * ls + r0));
                 h[0] = v.x & 0xffffu; h[1] = v.x >> 16; h[2] = v.y & 0xffffu; h[3] = v.y >> 16;
                 h[4] = v.z & 0xffffu; h[5] = v.z >> 16; h[6] = v.w & 0xffffu; h[7] = v.w >> 16;
@@ -321,7 +337,7 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int64_t rr = r0 + e;
-                    h[e] = (L < nlines && rr < R) ? (uint32_t)__ldg(src + L * ls + rr) : 0u;
+                    h[e] = (L < nlines && rr < R && CHK(L * ls + rr, 1, n_src)) ? (uint32_t)__ldg(src + L * ls + rr) : 0u;
                 }
             }
         } else {
@@ -355,7 +371,7 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
         const bool use = width > 0 && width <= 31;
         const int n = digits_for_width(width);
         if (FLAG_ONLY) {                                  // the line needs four digits somewhere
-            if (lane == 0 && n == kPlanes && L < nlines) atomicOr(&flag[L], 1);
+            if (lane == 0 && n == kPlanes && L < nlines && CHK(L, 1, Lp)) atomicOr(&flag[L], 1);
             continue;
         }
         int X[8];
@@ -372,11 +388,13 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
         mx = __reduce_max_sync(0xffffffffu, mx);
         if (lane == 0) {
-            stats[(int64_t)q * Lp + L] = make_int4(base, width, bit_count(sum), bit_count(mx));
+            if (CHK((int64_t)q * Lp + L, 1, n_stats))
+                stats[(int64_t)q * Lp + L] = make_int4(base, width, bit_count(sum), bit_count(mx));
             // the grain also covers finite lines too wide for the digits,
             // whose chunks the chunk repair adds in the same grain
-            if (width > 0 && width <= 62) atomicMin(&grain[L], base);
-            if (use && cnt != nullptr) atomicMax(&cnt[(LP / tg) * nchunks + q], n);
+            if (width > 0 && width <= 62 && CHK(L, 1, Lp)) atomicMin(&grain[L], base);
+            if (use && cnt != nullptr && CHK((LP / tg) * nchunks + q, 1, n_cnt))
+                atomicMax(&cnt[(LP / tg) * nchunks + q], n);
         }
         // X = v * 256^a with v = m << (s % 8), a = s / 8 (s = e - base): two
         // balanced digits, lo = v mod 256 in [-128, 127] at plane a and
@@ -400,9 +418,12 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
         }
         const int64_t row = (LP / tg) * kPlanes * tg + LP % tg;
 #pragma unroll
-        for (int a = 0; a < kPlanes; ++a)
-            *reinterpret_cast<uint4 *>(planes + (row + (int64_t)a * tg) * Rp + q0 + 8 * lane) =
-                make_uint4(packed[a][0], packed[a][1], packed[a][2], packed[a][3]);
+        for (int a = 0; a < kPlanes; ++a) {
+            const int64_t at = (row + (int64_t)a * tg) * Rp + q0 + 8 * lane;
+            if (CHK(at, 8, n_planes))
+                *reinterpret_cast<uint4 *>(planes + at) =
+                    make_uint4(packed[a][0], packed[a][1], packed[a][2], packed[a][3]);
+        }
     }
 }
 
@@ -538,6 +559,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    wait_prior_grid();                                   // the digit planes and counters are written
+    allow_next_grid();
     const uint32_t tmem = sm.tmem_slot;
     const int nunits = p.tiles_m * p.tiles_n * p.splits;   // (tile, chunk piece) work units
     const int nchunks = p.nchunks;
@@ -564,7 +587,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 int tm, tn;
                 tile_of(p, t, tm, tn);
                 for (int q = qlo; ok && q < qhi; ++q) {
-                    const int nx = p.cntA[(int64_t)tm * nchunks + q];
+                    const int nx = CHK((int64_t)tm * nchunks + q, 1, (int64_t)p.tiles_m * nchunks)
+                                       ? p.cntA[(int64_t)tm * nchunks + q] : 0;
                     for (int k = 0; ok && k < nx; ++k)
                         for (int kb = 0; kb < kKBlocks; ++kb, ++g) {
                             if ((g & 1u) != mine) continue;
@@ -599,7 +623,9 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 int tm, tn;
                 tile_of(p, t, tm, tn);
                 for (int q = qlo; ok && q < qhi; ++q) {
-                    if (p.cntA[(int64_t)tm * nchunks + q] == 0) continue;
+                    if (!CHK((int64_t)tm * nchunks + q, 1, (int64_t)p.tiles_m * nchunks) ||
+                        p.cntA[(int64_t)tm * nchunks + q] == 0)
+                        continue;
                     for (int kb = 0; kb < kKBlocks; ++kb) {
                         if (!(ok = wait_or_abort(smem_addr(&sm.bempty[kb]), (bu & 1u) ^ 1u, abort_flag))) break;
                         const uint32_t fb = smem_addr(&sm.bfull[kb]);
@@ -640,9 +666,11 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 int tm, tn;
                 tile_of(p, t, tm, tn);
                 for (int q = qlo; ok && q < qhi; ++q) {
-                    const int nx = p.cntA[(int64_t)tm * nchunks + q];
+                    const int nx = CHK((int64_t)tm * nchunks + q, 1, (int64_t)p.tiles_m * nchunks)
+                                       ? p.cntA[(int64_t)tm * nchunks + q] : 0;
                     if (nx == 0) continue;
-                    const int nb = max(1, p.cntB[(int64_t)tn * nchunks + q]);
+                    const int nb = CHK((int64_t)tn * nchunks + q, 1, (int64_t)p.tiles_n * nchunks)
+                                       ? max(1, p.cntB[(int64_t)tn * nchunks + q]) : 1;
                     const uint32_t idesc_q = idesc0 | ((uint32_t)(kColTile * nb >> 3) << 17);
                     for (int k = 0; ok && k < nx; ++k) {
                         if (!(ok = wait_or_abort(smem_addr(&sm.tempty[acc]), aph, abort_flag))) break;
@@ -711,15 +739,18 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             const int qhi = min(nchunks, qlo + p.cps);
             int tm, tn;
             tile_of(p, t, tm, tn);
-            const int64_t i = __ldg(&p.invA[(int64_t)tm * kRowTile + rl]);   // the row's own index
+            const int64_t ia_at = (int64_t)tm * kRowTile + rl;
+            const int64_t i = CHK(ia_at, 1, p.LpA) ? (int64_t)__ldg(&p.invA[ia_at]) : 0;   // the row's own index
             const int64_t jw = (int64_t)tn * kColTile + half * 32;   // this warp's first column
             const int *cnt = p.cntA + (int64_t)tm * nchunks;
-            const int Gx = __ldg(&p.GA[i]);                   // output grain: 2^(Gx + Gw)
-            const int Gwl = __ldg(&p.GB[jw + lane]);
+            const int Gx = CHK(i, 1, p.LpA) ? __ldg(&p.GA[i]) : 0;      // output grain: 2^(Gx + Gw)
+            const int Gwl = CHK(jw + lane, 1, p.LpB) ? __ldg(&p.GB[jw + lane]) : 0;
+            const int64_t n_cnt = (int64_t)(p.tiles_m - tm) * nchunks;    // cnt's extent from here
+            const int64_t n_sa = (int64_t)nchunks * p.LpA, n_sb = (int64_t)nchunks * p.LpB;
             __syncwarp();                                    // last tile's reads are done
             // I, the chunk sum, starts at 0 (each plane pair's starting values
             // are taken out as it is added); T, the exact sum, too
-            int nx = qlo < qhi ? cnt[qlo] : 0;
+            int nx = (qlo < qhi && CHK(qlo, 1, n_cnt)) ? cnt[qlo] : 0;
             unsigned long long I[32], T[32];
             {
 #pragma unroll
@@ -728,12 +759,12 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             uint32_t defer = 0u;
             int4 rs = make_int4(0, 0, 0, 0), cl = rs;        // this chunk's statistics, loaded ahead
             if (qlo < qhi) {
-                rs = __ldg(&p.SA[(int64_t)qlo * p.LpA + i]);
-                cl = __ldg(&p.SB[(int64_t)qlo * p.LpB + jw + lane]);
+                if (CHK((int64_t)qlo * p.LpA + i, 1, n_sa)) rs = __ldg(&p.SA[(int64_t)qlo * p.LpA + i]);
+                if (CHK((int64_t)qlo * p.LpB + jw + lane, 1, n_sb)) cl = __ldg(&p.SB[(int64_t)qlo * p.LpB + jw + lane]);
             }
 
             for (int q = qlo; ok && q < qhi; ++q) {
-                const int nx_next = (q + 1 < qhi) ? cnt[q + 1] : 0;   // loaded a chunk ahead
+                const int nx_next = (q + 1 < qhi && CHK(q + 1, 1, n_cnt)) ? cnt[q + 1] : 0;   // loaded a chunk ahead
                 for (int k = 0; k < nx; ++k) {
                     if (!(ok = wait_or_abort(smem_addr(&sm.tfull[acc]), aph, abort_flag))) break;
                     tc_fence_after();
@@ -818,8 +849,9 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                                   ((uint32_t)cl.z << 15) | ((uint32_t)cl.w << 21);
                 __syncwarp();
                 if (q + 1 < qhi) {                           // next chunk's statistics
-                    rs = __ldg(&p.SA[(int64_t)(q + 1) * p.LpA + i]);
-                    cl = __ldg(&p.SB[(int64_t)(q + 1) * p.LpB + jw + lane]);
+                    if (CHK((int64_t)(q + 1) * p.LpA + i, 1, n_sa)) rs = __ldg(&p.SA[(int64_t)(q + 1) * p.LpA + i]);
+                    if (CHK((int64_t)(q + 1) * p.LpB + jw + lane, 1, n_sb))
+                        cl = __ldg(&p.SB[(int64_t)(q + 1) * p.LpB + jw + lane]);
                 }
                 // I is exact (modulo 2^64, and below 2^62) when every line fits.
                 // Then all 32 outputs take T += I << sh at once while the checks
@@ -894,7 +926,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         if (!fits && !(defer & bit) && wx > 0 && ww > 0 && wx <= 62 && ww <= 62 &&
                             wx + ww < 90 && i < p.rows && jw + jj < p.cols) {
                             const unsigned int e = atomicAdd(p.chunk_count, 1u);
-                            if (e < p.chunk_cap) {
+                            if (e < p.chunk_cap && CHK(e, 1, p.chunk_cap)) {
                                 p.chunk_list[e] = make_uint2((unsigned int)(i * p.cols + jw + jj), (unsigned int)q);
                                 bad = false;
                             }
@@ -910,29 +942,23 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             if (!ok) break;
 
             // ---- this piece's exact partial sums go to the finalize kernel
-            // (deferred outputs: a sentinel no sum reaches, |T| < 2^62), row-major:
-            // a lane's 32 outputs are 256 contiguous bytes of its row
+            // (deferred outputs: a sentinel no sum reaches, |T| < 2^62), stored
+            // column-major so that a warp's 32 rows make one contiguous store
             if (i < p.rows) {
-                long long *trow = p.Tout + (int64_t)piece * p.rows * p.cols + i * p.cols + jw;
-                if (jw + 32 <= p.cols && (p.cols & 1) == 0) {        // 16-byte aligned pairs
+                const int64_t t0 = (int64_t)piece * p.rows * p.cols + jw * p.rows + i;
+                const int64_t n_t = (int64_t)p.splits * p.rows * p.cols;
 #pragma unroll
-                    for (int jj = 0; jj < 32; jj += 2) {
-                        const long long v0 = ((defer >> jj) & 1u) ? kDeferredSum : (long long)T[jj];
-                        const long long v1 = ((defer >> (jj + 1)) & 1u) ? kDeferredSum : (long long)T[jj + 1];
-                        *reinterpret_cast<longlong2 *>(trow + jj) = make_longlong2(v0, v1);
-                    }
-                } else {
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj)
-                        if (jw + jj < p.cols)
-                            trow[jj] = ((defer >> jj) & 1u) ? kDeferredSum : (long long)T[jj];
-                }
+                for (int jj = 0; jj < 32; ++jj)
+                    if (jw + jj < p.cols && CHK(t0 + (int64_t)jj * p.rows, 1, n_t))
+                        p.Tout[t0 + (int64_t)jj * p.rows] = ((defer >> jj) & 1u) ? kDeferredSum : (long long)T[jj];
             }
             // outputs for the fix-up pass
             for (uint32_t dm = defer; dm != 0u; dm &= dm - 1u) {
                 const int jj = __ffs((int)dm) - 1;
-                if (i < p.rows && jw + jj < p.cols)
-                    p.work_list[atomicAdd(p.work_count, 1u)] = (unsigned int)(i * p.cols + jw + jj);
+                if (i < p.rows && jw + jj < p.cols) {
+                    const unsigned int at = atomicAdd(p.work_count, 1u);
+                    if (CHK(at, 1, p.work_cap)) p.work_list[at] = (unsigned int)(i * p.cols + jw + jj);
+                }
             }
         }
     }
@@ -974,15 +1000,23 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
                           int64_t LpA, int64_t LpB, const int *__restrict__ GA,
                           const int *__restrict__ GB, const unsigned int *__restrict__ chunk_count,
                           const uint2 *__restrict__ chunk_list, unsigned int chunk_cap,
-                          long long *Tout, int cps, unsigned int *work_count, unsigned int *work_list) {
+                          long long *Tout, int cps, unsigned int *work_count, unsigned int *work_list,
+                          int64_t n_tout, int64_t work_cap) {
+    wait_prior_grid();
+    allow_next_grid();
     const int lane = threadIdx.x % 32;
     const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32;
     const int64_t nw = (int64_t)gridDim.x * blockDim.x / 32;
     const int64_t count = min(*chunk_count, chunk_cap);
+    const int64_t nq = (p.R + kChunk - 1) / kChunk;
+    const int64_t n_a = (p.rows > 0 && p.R > 0) ? (p.rows - 1) * p.a_si + (p.R - 1) * p.a_sr + 1 : 0;
+    const int64_t n_b = (p.cols > 0 && p.R > 0) ? (p.R - 1) * p.b_sr + (p.cols - 1) * p.b_sj + 1 : 0;
     for (int64_t e = gw; e < count; e += nw) {
+        if (!CHK(e, 1, chunk_cap)) break;
         const uint2 en = chunk_list[e];
         const int64_t o = en.x, q = en.y;
         const int64_t i = o / p.cols, j = o % p.cols;
+        if (!CHK(q * LpA + i, 1, nq * LpA) || !CHK(q * LpB + j, 1, nq * LpB)) continue;
         const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
         const int64_t q0 = q * kChunk, qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
         __int128 I = 0;
@@ -990,6 +1024,7 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
         for (int t = 0; t < kChunk / 32; ++t) {
             const int64_t r = q0 + lane + 32 * t;
             if (r >= qend) continue;
+            if (!CHK(i * p.a_si + r * p.a_sr, 1, n_a) || !CHK(r * p.b_sr + j * p.b_sj, 1, n_b)) continue;
             int mx, ex, mw, ew;
             bool bx_, bw_;
             decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bx_);
@@ -1007,22 +1042,26 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
         }
         if (lane != 0) continue;
         const __int128 J = SUPER ? I : round_i128_to_53_bits(I);
-        const int sh = (sa.x - __ldg(&GA[i])) + (sb.x - __ldg(&GB[j]));
+        const int sh = (CHK(i, 1, LpA) && CHK(j, 1, LpB)) ? (sa.x - __ldg(&GA[i])) + (sb.x - __ldg(&GB[j])) : -1;
         bool ok = sh >= 0 && sh < 62;
         __int128 v = 0;
         if (ok) {
             v = (__int128)((unsigned __int128)J << sh);
             ok = (v >> sh) == J && v >= -((__int128)1 << 61) && v < ((__int128)1 << 61);
         }
+        if (ok && !CHK((q / cps) * p.rows * p.cols + j * p.rows + i, 1, n_tout)) ok = false;
         if (ok) {
-            long long *slot = Tout + (q / cps) * p.rows * p.cols + i * p.cols + j;
+            long long *slot = Tout + (q / cps) * p.rows * p.cols + j * p.rows + i;
             const long long add = (long long)v;
             const long long old = (long long)atomicAdd(reinterpret_cast<unsigned long long *>(slot),
                                                        (unsigned long long)add);
             const long long sum = (long long)((unsigned long long)old + (unsigned long long)add);
             ok = !((old >= 0) == (add >= 0) && (sum >= 0) != (old >= 0));
         }
-        if (!ok) work_list[atomicAdd(work_count, 1u)] = (unsigned int)o;
+        if (!ok) {
+            const unsigned int at = atomicAdd(work_count, 1u);
+            if (CHK(at, 1, work_cap)) work_list[at] = (unsigned int)o;
+        }
     }
 }
 
@@ -1030,6 +1069,8 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
 // counters (launched only while kernel timing is on).
 __global__ void exact_count_kernel(const unsigned int *chunk_count, unsigned int chunk_cap,
                                    const unsigned int *work_count) {
+    wait_prior_grid();
+    allow_next_grid();
     atomicAdd(&g_exact_tc_repairs, (unsigned long long)min(*chunk_count, chunk_cap));
     atomicAdd(&g_exact_tc_fixups, (unsigned long long)*work_count);
 }
@@ -1043,9 +1084,8 @@ __global__ void exact_count_kernel(const unsigned int *chunk_count, unsigned int
 // even), all on integers; values outside those fast ranges take the float64
 // route.  The chunk range of an output may have been split into pieces whose
 // partial sums T add exactly.  One thread per 8 consecutive outputs of a row,
-// consecutive threads on consecutive groups of the same row (T is stored
-// row-major), so a warp reads 2 KiB of sums and writes 512 bytes of outputs,
-// each contiguous.
+// consecutive threads on consecutive rows (T is stored column-major, so each
+// of a warp's loads is 256 contiguous bytes).
 // Output modes of the finalize: the KBN tier's bf16 outputs, its float64
 // values (inspection), and the correctly rounded tier's bf16 outputs (the
 // exact total and the bias rounded once, never through float64).
@@ -1056,44 +1096,28 @@ __global__ void __launch_bounds__(256)
 exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int *__restrict__ GA,
                       const int *__restrict__ GB, const unsigned short *__restrict__ bias, void *out,
                       int64_t rows, int64_t cols, int vec_out) {
+    wait_prior_grid();
+    allow_next_grid();
     const int64_t gpr = (cols + 7) / 8;                  // 8-column groups per row
     const int64_t plane = rows * cols;
-    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < rows * gpr;
-         g += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = g / gpr, j0 = (g % gpr) * 8;
-        const int gx = __ldg(&GA[i]);
-        const long long *trow = Tout + i * cols + j0;
-        // every load first: the partial sums, the column grains and the bias
+    const int64_t rblocks = (rows + 255) / 256;
+    for (int64_t b = blockIdx.x; b < rblocks * gpr; b += gridDim.x) {
+        const int64_t i = (b % rblocks) * 256 + threadIdx.x, j0 = (b / rblocks) * 8;
+        if (i >= rows) continue;
+        const int64_t n_t = (int64_t)pieces * plane;
+        const int gx = CHK(i, 1, rows) ? __ldg(&GA[i]) : 0;
+        // every load first: the partial sums (a warp reads 32 consecutive
+        // rows of one column), the column grains and the bias
         long long t0[8], t1[8];
         int gw[8];
         uint32_t hb[8];
-        if (vec_out && j0 + 8 <= cols) {                  // 16-byte aligned groups
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const longlong2 a = __ldg(reinterpret_cast<const longlong2 *>(trow + e));
-                t0[e] = a.x; t0[e + 1] = a.y;
-                if (pieces > 1) {
-                    const longlong2 b2 = __ldg(reinterpret_cast<const longlong2 *>(trow + plane + e));
-                    t1[e] = b2.x; t1[e + 1] = b2.y;
-                } else {
-                    t1[e] = 0ll; t1[e + 1] = 0ll;
-                }
-            }
-            const int4 g0 = __ldg(reinterpret_cast<const int4 *>(GB + j0));
-            const int4 g1 = __ldg(reinterpret_cast<const int4 *>(GB + j0 + 4));
-            gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
-            gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) hb[e] = bias != nullptr ? ld_bits(bias, j0 + e) : 0u;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const bool in = j0 + e < cols;
-                t0[e] = in ? __ldg(trow + e) : 0ll;
-                t1[e] = (in && pieces > 1) ? __ldg(trow + plane + e) : 0ll;
-                gw[e] = in ? __ldg(&GB[j0 + e]) : 0;
-                hb[e] = (in && bias != nullptr) ? ld_bits(bias, j0 + e) : 0u;
-            }
+        for (int e = 0; e < 8; ++e) {
+            const bool in = j0 + e < cols && CHK((j0 + e) * rows + i + (pieces > 1 ? plane : 0), 1, n_t);
+            t0[e] = in ? __ldg(&Tout[(j0 + e) * rows + i]) : 0ll;
+            t1[e] = (in && pieces > 1) ? __ldg(&Tout[plane + (j0 + e) * rows + i]) : 0ll;
+            gw[e] = in ? __ldg(&GB[j0 + e]) : 0;
+            hb[e] = (in && bias != nullptr) ? ld_bits(bias, j0 + e) : 0u;
         }
         uint32_t packed[4] = {0u, 0u, 0u, 0u};
         uint32_t skip = 0u;
@@ -1139,7 +1163,8 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             bool deferred = t0[e] == kDeferredSum || (pieces > 1 && t1[e] == kDeferredSum);
             __int128 acc = (__int128)t0[e] + (__int128)t1[e];
             for (int k = 2; k < pieces && !deferred; ++k) {
-                const long long t = __ldg(&Tout[k * plane + i * cols + j]);
+                if (!CHK(k * plane + j * rows + i, 1, n_t)) break;
+                const long long t = __ldg(&Tout[k * plane + j * rows + i]);
                 deferred = t == kDeferredSum;
                 acc += t;
             }
@@ -1156,7 +1181,7 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             if (OUT_F64 || !small) {
                 double y = small ? round_int_to_double((long long)acc, G) : round_i128_to_double(acc, G);
                 if (bias != nullptr) y = __dadd_rn(y, widen_bf16(hb[e]));
-                if (OUT_F64) static_cast<double *>(out)[i * cols + j] = y;
+                if (OUT_F64 && CHK(i * cols + j, 1, plane)) static_cast<double *>(out)[i * cols + j] = y;
                 else packed[e / 2] |= (uint32_t)exact_round_bf16(y) << (16 * (e & 1));
                 continue;
             }
@@ -1185,6 +1210,7 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
         }
         if (OUT_F64) continue;
         unsigned short *orow = static_cast<unsigned short *>(out) + i * cols + j0;
+        if (!CHK(i * cols + j0, min((int64_t)8, cols - j0), plane)) continue;
         if (skip == 0u && vec_out) {
             *reinterpret_cast<uint4 *>(orow) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         } else {
@@ -1194,6 +1220,11 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
         }
     }
 }
+
+// Blocks of the post-pass kernels that stride over the repair and fix-up
+// lists (GPT-2 data lists thousands of chunk repairs on some weight
+// gradients: fewer blocks cost more than their launch saves).
+constexpr int kPostBlocks = kFixBlocks;
 
 template <int MODE>
 cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const TcxArgs &a, int grid,
@@ -1206,38 +1237,38 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     if (ev.e[1]) cudaEventRecord(ev.e[1], s);
-    kern<<<grid, kTcxThreads, smem, s>>>(ma, mb, a);
+    err = launch_k(kern, dim3(grid), dim3(kTcxThreads), (size_t)smem, s, 1, ma, mb, a);
     count_launch();
     if (ev.e[2]) cudaEventRecord(ev.e[2], s);
-    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    exact_chunk_repair_kernel<SUPER><<<kFixBlocks, 256, 0, s>>>(
-        ia, SA, SB, LpA, LpB, a.GA, a.GB, a.chunk_count, a.chunk_list, a.chunk_cap, a.Tout, a.cps,
-        work, work + 1);
+    err = launch_k(exact_chunk_repair_kernel<SUPER>, dim3(kPostBlocks), dim3(256), 0, s, 1,
+                   ia, SA, SB, LpA, LpB, a.GA, a.GB, (const unsigned int *)a.chunk_count,
+                   (const uint2 *)a.chunk_list, a.chunk_cap, a.Tout, a.cps, work, work + 1,
+                   (int64_t)a.splits * a.rows * a.cols, a.work_cap);
     count_launch();
-    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if (ev.e[0]) {
-        exact_count_kernel<<<1, 1, 0, s>>>(a.chunk_count, a.chunk_cap, work);
+        err = launch_k(exact_count_kernel, dim3(1), dim3(1), 0, s, 1,
+                       (const unsigned int *)a.chunk_count, a.chunk_cap, (const unsigned int *)work);
         count_launch();
+        if (err != cudaSuccess) return err;
     }
     {
-        const int64_t groups = a.rows * ((a.cols + 7) / 8);
-        const int64_t want = (groups + 255) / 256, cap = 152 * 64;
+        const int64_t want = ((a.rows + 255) / 256) * ((a.cols + 7) / 8), cap = 152 * 64;
         const unsigned grid = (unsigned)(want < cap ? want : cap);
         const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0 && (a.cols % 8) == 0) ? 1 : 0;
-        exact_finalize_kernel<MODE><<<grid, 256, 0, s>>>(a.Tout, a.splits, a.GA, a.GB, a.bias, a.out,
-                                                          a.rows, a.cols, vec_out);
+        err = launch_k(exact_finalize_kernel<MODE>, dim3(grid), dim3(256), 0, s, 1,
+                       (const long long *)a.Tout, a.splits, a.GA, a.GB, a.bias, a.out, a.rows, a.cols,
+                       vec_out);
         count_launch();
-        err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
     if (SUPER) {
-        err = superacc_fixup_bf16(prob, work, work + 1, kFixBlocks, s);
+        err = superacc_fixup_bf16(prob, work, work + 1, kPostBlocks, s);
     } else {
-        exact_fixup_kernel<MODE == kFinF64><<<kFixBlocks, kFixWarps * 32, 0, s>>>(ia, SA, SB, LpA, LpB, work, work + 1);
+        err = launch_k(exact_fixup_kernel<MODE == kFinF64>, dim3(kPostBlocks), dim3(kFixWarps * 32), 0, s, 1,
+                       ia, SA, SB, LpA, LpB, (const unsigned int *)work, (const unsigned int *)(work + 1));
         count_launch();
-        err = cudaGetLastError();
     }
     if (ev.e[3]) cudaEventRecord(ev.e[3], s);
     return err;
@@ -1263,10 +1294,26 @@ cudaError_t launch_prep(const unsigned short *src, int64_t ls, int64_t rs, int64
     const dim3 grid((unsigned)(Lp / kPrepLines), (unsigned)nchunks);
     const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
     const int vec = RCONTIG ? (aligned && ls % 8 == 0) : (aligned && ls == 1 && rs % 8 == 0);
-    digit_prep_kernel<RCONTIG, FLAG_ONLY><<<grid, kPrepThreads, 0, s>>>(
-        src, ls, rs, nlines, R, Lp, Rp, tg, planes, stats, grain, cnt, nchunks, vec, pos, flag);
+    const cudaError_t err = launch_k(digit_prep_kernel<RCONTIG, FLAG_ONLY>, grid, dim3(kPrepThreads), 0, s, 1,
+                                     src, ls, rs, nlines, R, Lp, Rp, tg, planes, stats, grain, cnt,
+                                     nchunks, vec, pos, flag);
     count_launch();
-    return cudaGetLastError();
+    return err;
+}
+
+// Workspace set-up of one call, in place of separate memsets: the line grains
+// start at kGrainNone (n_grain ints from grain), the row flags, plane counts
+// and counters at 0 (n_zero ints from zero, n_cnt from counters).
+__global__ void __launch_bounds__(256)
+exact_init_kernel(int *__restrict__ grain, int64_t n_grain, int *__restrict__ zero, int64_t n_zero,
+                  unsigned int *__restrict__ counters, int n_cnt) {
+    wait_prior_grid();
+    allow_next_grid();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    for (int64_t k = t0; k < n_grain; k += stride) grain[k] = kGrainNone;
+    for (int64_t k = t0; k < n_zero; k += stride) zero[k] = 0;
+    if (t0 < n_cnt) counters[t0] = 0u;
 }
 
 // Places of the A rows in the digit planes: within each group of 1024 rows
@@ -1281,10 +1328,12 @@ __global__ void __launch_bounds__(kOrderGroup)
 row_order_kernel(const int *__restrict__ flag, int64_t rows, int64_t Lp, int *__restrict__ pos,
                  int *__restrict__ inv) {
     __shared__ int wz[kOrderGroup / 32], wv[kOrderGroup / 32];
+    wait_prior_grid();
+    allow_next_grid();
     const int t = threadIdx.x, warp = t / 32, lane = t % 32;
     const int64_t base = (int64_t)blockIdx.x * kOrderGroup, i = base + t;
     const bool valid = i < rows;
-    const bool z = valid && flag[i] == 0;            // three digits suffice everywhere
+    const bool z = valid && CHK(i, 1, Lp) && flag[i] == 0;   // three digits suffice everywhere
     const uint32_t below = (1u << lane) - 1u;
     const uint32_t bz = __ballot_sync(0xffffffffu, z), bv = __ballot_sync(0xffffffffu, valid);
     if (lane == 0) { wz[warp] = __popc(bz); wv[warp] = __popc(bv); }
@@ -1301,8 +1350,8 @@ row_order_kernel(const int *__restrict__ flag, int64_t rows, int64_t Lp, int *__
     const int rz = pz + __popc(bz & below);          // z rows before this one
     const int rv = pv + __popc(bv & below);          // valid rows before this one
     const int64_t place = base + (z ? rz : tz + (rv - rz));
-    pos[i] = (int)place;
-    inv[place] = (int)i;
+    if (CHK(i, 1, Lp)) pos[i] = (int)place;
+    if (CHK(place, 1, Lp)) inv[place] = (int)i;
 }
 
 }  // namespace
@@ -1374,23 +1423,28 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, bool super, cuda
 
     const CallEvents ev = timing_events(stream);
     if (ev.e[0]) cudaEventRecord(ev.e[0], stream);
-    // the deferral counter and the plane counts start at 0, the line grains
-    // at kGrainNone
-    err = cudaMemsetAsync(work, 0, sizeof(unsigned int), stream);
-    if (err == cudaSuccess)
-        err = cudaMemsetAsync(GA, kGrainNone & 0xff, 4 * (size_t)(LpA + LpB), stream);
-    if (err == cudaSuccess) err = cudaMemsetAsync(cntA, 0, cntBytes, stream);
-    if (err == cudaSuccess) err = cudaMemsetAsync(flagA, 0, 4 * (size_t)LpA, stream);
-    if (err == cudaSuccess) err = cudaMemsetAsync(ccount, 0, 4 * sizeof(unsigned int), stream);
+    // the line grains start at kGrainNone; the row flags, the plane counts,
+    // the chunk-repair and unit counters and the deferral counter at 0 (the
+    // plane counts follow the row flags, place and row arrays: one zeroed
+    // range covers flags .. counts, the place and row arrays being written
+    // in full by the row order anyway)
+    {
+        const int64_t n_zero = (int64_t)(cntA - flagA) + (int64_t)(cntBytes / 4);
+        const int64_t n_max = (LpA + LpB) > n_zero ? (LpA + LpB) : n_zero;
+        const int64_t want = (n_max + 255) / 256;
+        const unsigned blocks = (unsigned)(want < 1024 ? (want > 0 ? want : 1) : 1024);
+        err = launch_k(exact_init_kernel, dim3(blocks), dim3(256), 0, stream, 1, GA,
+                       (int64_t)(LpA + LpB), flagA, n_zero, ccount, 5);
+        count_launch();
+    }
     const bool a_rc = (p.pass != CARBON_PASS_DW), b_rc = (p.pass == CARBON_PASS_DX);
     if (err == cudaSuccess && nchunks > 0)
         err = a_rc ? launch_prep<true, true>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, nullptr, (int)nchunks, nullptr, flagA, stream)
                    : launch_prep<false, true>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, nullptr, (int)nchunks, nullptr, flagA, stream);
     if (err == cudaSuccess) {
-        row_order_kernel<<<(unsigned)((LpA + kOrderGroup - 1) / kOrderGroup), kOrderGroup, 0, stream>>>(
-            flagA, p.rows, LpA, posA, invA);
+        err = launch_k(row_order_kernel, dim3((unsigned)((LpA + kOrderGroup - 1) / kOrderGroup)),
+                       dim3(kOrderGroup), 0, stream, 1, flagA, p.rows, LpA, posA, invA);
         count_launch();
-        err = cudaGetLastError();
     }
     if (err == cudaSuccess && nchunks > 0)
         err = a_rc ? launch_prep<true, false>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, posA, nullptr, stream)
@@ -1425,6 +1479,7 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, bool super, cuda
         a.SA = SA; a.SB = SB; a.GA = GA; a.GB = GB; a.cntA = cntA; a.invA = invA;
         a.cntB = cntB;
         a.work_count = work; a.work_list = work + 1;
+        a.work_cap = (int64_t)(outs * pieces + ccap);
         a.Tout = Tout;
         a.chunk_count = ccount;
         a.chunk_list = clist;
@@ -1511,10 +1566,12 @@ carbon_status_t exact_tc_path_counts(int64_t *repairs, int64_t *fixups) {
 }
 
 carbon_status_t exact_tc_take_device_status() {
-    unsigned int v = 0, zero = 0;
+    unsigned int v = 0, f = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_exact_tc_status, sizeof v) != cudaSuccess) return CARBON_OK;
     if (v != 0) cudaMemcpyToSymbol(g_exact_tc_status, &zero, sizeof zero);
-    return (carbon_status_t)v;
+    if (cudaMemcpyFromSymbol(&f, g_fixup_status, sizeof f) == cudaSuccess && f != 0)
+        cudaMemcpyToSymbol(g_fixup_status, &zero, sizeof zero);
+    return (carbon_status_t)(v != 0 ? v : f);
 }
 
 }  // namespace carbon

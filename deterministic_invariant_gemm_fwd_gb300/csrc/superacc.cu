@@ -16,12 +16,18 @@
 // then the 32 accumulators are summed digit by digit with shuffles (integer
 // additions: exact) and lane 0 rounds.
 #include "carbon_internal.h"
+#include "bounds.cuh"
+#include "device_sync.cuh"
 #include "superacc.cuh"
 
 namespace carbon {
 namespace {
 
 constexpr int kSaWarps = 8;
+
+// Status word: CARBON_ERR_OUT_OF_BOUNDS in the bounds-checked build.
+__device__ unsigned int g_superacc_status = 0;
+#define CHK(idx, len, n) in_bounds(&g_superacc_status, (int64_t)(idx), (int64_t)(len), (int64_t)(n))
 
 struct SaArgs {
     const void *A, *B, *bias;
@@ -47,13 +53,18 @@ template <int DT, bool LIST>
 __global__ void __launch_bounds__(kSaWarps * 32)
 superacc_kernel(const SaArgs p, const unsigned int *__restrict__ work_count,
                 const unsigned int *__restrict__ work_list) {
+    wait_prior_grid();
+    allow_next_grid();
     const int lane = threadIdx.x % 32;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const int64_t nw = (int64_t)gridDim.x * blockDim.x / 32;
     const int64_t count = LIST ? (int64_t)*work_count : p.rows * p.cols;
+    const int64_t n_a = (p.rows > 0 && p.R > 0) ? (p.rows - 1) * p.a_si + (p.R - 1) * p.a_sr + 1 : 0;
+    const int64_t n_b = (p.cols > 0 && p.R > 0) ? (p.R - 1) * p.b_sr + (p.cols - 1) * p.b_sj + 1 : 0;
     for (int64_t item = gw; item < count; item += nw) {
         const int64_t o = LIST ? (int64_t)work_list[item] : item;
         const int64_t i = o / p.cols, j = o % p.cols;
+        if (!CHK(o, 1, p.rows * p.cols)) continue;             // warp-uniform
         long long acc[sacc::kDigits];
 #pragma unroll
         for (int d = 0; d < sacc::kDigits; ++d) acc[d] = 0ll;
@@ -63,6 +74,7 @@ superacc_kernel(const SaArgs p, const unsigned int *__restrict__ work_count,
             if ((++steps & 0xfffffu) == 0u) sacc::carry(acc);   // digits stay below 2^53
             long long ma, mb;
             int ea, eb, ca, cb;
+            if (!CHK(i * p.a_si + r * p.a_sr, 1, n_a) || !CHK(r * p.b_sr + j * p.b_sj, 1, n_b)) continue;
             sacc::decode_value<DT>(load_bits<DT>(p.A, i * p.a_si + r * p.a_sr), ma, ea, ca);
             sacc::decode_value<DT>(load_bits<DT>(p.B, r * p.b_sr + j * p.b_sj), mb, eb, cb);
             const int pc = sacc::product_class(ca, ma, cb, mb);
@@ -102,16 +114,15 @@ SaArgs make_args(const Problem &p) {
 template <bool LIST>
 cudaError_t launch(int dtype, const SaArgs &a, int blocks, const unsigned int *count,
                    const unsigned int *list, cudaStream_t s) {
+    const dim3 g((unsigned)blocks), b(kSaWarps * 32);
+    cudaError_t err;
     switch (dtype) {
-    case CARBON_F32:
-        superacc_kernel<CARBON_F32, LIST><<<blocks, kSaWarps * 32, 0, s>>>(a, count, list); break;
-    case CARBON_F16:
-        superacc_kernel<CARBON_F16, LIST><<<blocks, kSaWarps * 32, 0, s>>>(a, count, list); break;
-    default:
-        superacc_kernel<CARBON_BF16, LIST><<<blocks, kSaWarps * 32, 0, s>>>(a, count, list); break;
+    case CARBON_F32: err = launch_k(superacc_kernel<CARBON_F32, LIST>, g, b, 0, s, 1, a, count, list); break;
+    case CARBON_F16: err = launch_k(superacc_kernel<CARBON_F16, LIST>, g, b, 0, s, 1, a, count, list); break;
+    default:         err = launch_k(superacc_kernel<CARBON_BF16, LIST>, g, b, 0, s, 1, a, count, list); break;
     }
     count_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace
@@ -131,6 +142,13 @@ carbon_status_t superacc_launch(const Problem &p, cudaStream_t stream) {
 cudaError_t superacc_fixup_bf16(const Problem &p, const unsigned int *work_count,
                                 const unsigned int *work_list, int blocks, cudaStream_t stream) {
     return launch<true>(CARBON_BF16, make_args(p), blocks, work_count, work_list, stream);
+}
+
+carbon_status_t superacc_take_device_status() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_superacc_status, sizeof v) != cudaSuccess) return CARBON_OK;
+    if (v != 0) cudaMemcpyToSymbol(g_superacc_status, &zero, sizeof zero);
+    return (carbon_status_t)v;
 }
 
 }  // namespace carbon

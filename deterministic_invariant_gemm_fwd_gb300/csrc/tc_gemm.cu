@@ -40,6 +40,7 @@
 // records CARBON_ERR_TIMEOUT, raises a CTA-wide abort flag so the other roles
 // leave their loops, and the TMEM allocation is still released.
 #include "carbon_internal.h"
+#include "bounds.cuh"
 #include "device_sync.cuh"
 #include "tcgen05.cuh"
 
@@ -54,6 +55,7 @@ namespace carbon {
 namespace {
 
 __device__ unsigned int g_tc_status = 0;
+#define CHK(idx, len, n) in_bounds(&g_tc_status, (int64_t)(idx), (int64_t)(len), (int64_t)(n))
 
 constexpr int kBM = 128;          // tile rows (= MMA M, = TMEM lanes)
 constexpr int kBK = 64;           // k-block: 64 bf16 = one 128-byte swizzle row
@@ -286,6 +288,10 @@ __device__ __forceinline__ uint32_t setup_cta(uint8_t *smem, const Bars &bar,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // set-up done: wait for the previous kernel on the stream (its outputs
+    // may be this GEMM's operands) and let the next one be scheduled
+    wait_prior_grid();
+    allow_next_grid();
     return *tmem_slot;
 }
 
@@ -354,7 +360,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             if (bias) {                                   // this warp's copy of the tile's bias
                 __syncwarp();                             // the previous tile's reads are done
                 for (int i = lane; i < BN; i += 32)
-                    bias_s[i] = (n0 + i < p.cols) ? bias_value<OT>(bias, n0 + i) : 0.0f;
+                    bias_s[i] = (n0 + i < p.cols && CHK(n0 + i, 1, p.cols)) ? bias_value<OT>(bias, n0 + i) : 0.0f;
                 __syncwarp();
             }
             if (!wait_or_abort(bar.tfull(acc), aph, abort_flag)) break;
@@ -383,7 +389,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                         float *o = static_cast<float *>(p.out) + row * p.cols + n0 + c;
 #pragma unroll
                         for (int g = 0; g < 8; ++g)
-                            if (n0 + c + 4 * g < p.cols)
+                            if (n0 + c + 4 * g < p.cols &&
+                                CHK(row * p.cols + n0 + c + 4 * g, 4, (int64_t)p.rows * p.cols))
                                 *reinterpret_cast<float4 *>(o + 4 * g) =
                                     make_float4(f[4 * g], f[4 * g + 1], f[4 * g + 2], f[4 * g + 3]);
                     }
@@ -510,6 +517,7 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         const int cc = (idx % (BN / 4)) * 4;
         const int64_t grow = (int64_t)m0 + rr, gcol = (int64_t)n0 + cc;
         if (grow >= p.rows || gcol >= p.cols) continue;
+        if (!CHK(grow * p.cols + gcol, 4, (int64_t)p.rows * p.cols)) continue;
         const uint32_t off = part_addr + (uint32_t)(rr * L::kPartialPitch + cc) * 4u;
         float4 a = ld_cluster_f4(off, 0);
         for (int q = 1; q < p.splits; ++q) {
@@ -538,10 +546,12 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 // Fills an output whose reduction is empty: bias (fwd) or +0.
 template <int OT>
 __global__ void tc_fill_kernel(void *out, const void *bias, int64_t rows, int64_t cols) {
+    wait_prior_grid();
+    allow_next_grid();
     const int64_t n = rows * cols;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const float v = bias ? bias_value<OT>(bias, i % cols) : 0.0f;
+        const float v = (bias && CHK(i % cols, 1, cols)) ? bias_value<OT>(bias, i % cols) : 0.0f;
         if (OT == OT_F32) static_cast<float *>(out)[i] = v;
         else static_cast<unsigned short *>(out)[i] = (unsigned short)(pack_out<OT>(v, 0.0f) & 0xffffu);
     }
@@ -576,8 +586,7 @@ cudaError_t launch_persistent(const CUtensorMap &ma, const CUtensorMap &mb, cons
     const int smem = (int)Smem<BN>::kDynamic;
     cudaError_t err = prepare(kern, smem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, smem, stream>>>(ma, mb, mo, a);
-    return cudaGetLastError();
+    return launch_k(kern, dim3(grid), dim3(kThreads), (size_t)smem, stream, 1, ma, mb, mo, a);
 }
 
 template <int BN, int OT>
@@ -605,19 +614,8 @@ cudaError_t launch_split(const CUtensorMap &ma, const CUtensorMap &mb, const TcA
     const int smem = (int)Smem<BN>::kDynamic;
     cudaError_t err = prepare(kern, smem);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.splits, (unsigned)(a.tiles_m * a.tiles_n), 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)a.splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ma, mb, a);
+    return launch_k(kern, dim3((unsigned)a.splits, (unsigned)(a.tiles_m * a.tiles_n), 1), dim3(kThreads),
+                    (size_t)smem, stream, (unsigned)a.splits, ma, mb, a);
 }
 
 // Output tile width from the column count and the pass only (never the row
@@ -665,11 +663,13 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
     if (p.R == 0) {
         const int64_t n = p.rows * p.cols;
         const int blocks = (int)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535);
-        if (out_f32) tc_fill_kernel<OT_F32><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
-        else if (p.dtype == CARBON_F16) tc_fill_kernel<OT_F16><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
-        else tc_fill_kernel<OT_BF16><<<blocks, 256, 0, stream>>>(p.out, p.bias, p.rows, p.cols);
+        const dim3 g((unsigned)blocks), b(256);
+        cudaError_t ferr;
+        if (out_f32) ferr = launch_k(tc_fill_kernel<OT_F32>, g, b, 0, stream, 1, p.out, p.bias, p.rows, p.cols);
+        else if (p.dtype == CARBON_F16) ferr = launch_k(tc_fill_kernel<OT_F16>, g, b, 0, stream, 1, p.out, p.bias, p.rows, p.cols);
+        else ferr = launch_k(tc_fill_kernel<OT_BF16>, g, b, 0, stream, 1, p.out, p.bias, p.rows, p.cols);
         count_launch();
-        return note_cuda(cudaGetLastError());
+        return note_cuda(ferr);
     }
     if (p.rows > (int64_t)0x7fffffff || p.cols > (int64_t)0x7fffffff || p.R > (int64_t)0x7fffffff)
         return CARBON_ERR_INVALID_ARG;

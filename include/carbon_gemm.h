@@ -137,7 +137,8 @@ typedef enum {
     CARBON_ERR_MISALIGNED = 3,    /* TC tier: pointer/pitch not 16-byte aligned */
     CARBON_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
     CARBON_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up */
-    CARBON_ERR_SCRATCH_LIMIT = 6  /* needs more than the fixed no-allocation workspace */
+    CARBON_ERR_SCRATCH_LIMIT = 6, /* needs more than the fixed no-allocation workspace */
+    CARBON_ERR_OUT_OF_BOUNDS = 7  /* bounds-checked build only: a kernel skipped an access out of range */
 } carbon_status_t;
 
 /* Forward pass Y[M,N] = X[M,K] . W[K,N] + bias[N].
@@ -252,8 +253,11 @@ carbon_status_t carbon_chunk_values_combine(void *out, const double *P, int64_t 
                                             carbon_dtype_t dtype, carbon_stream_t stream);
 
 /* Synchronises `stream`, then reports (and clears) the device status word
- * that kernels set when a bounded wait gives up (CARBON_ERR_TIMEOUT), or
- * CARBON_ERR_CUDA if the stream reports an error. */
+ * that kernels set when a bounded wait gives up (CARBON_ERR_TIMEOUT) or, in
+ * the bounds-checked build (libcarbon_gemm_bounds.so, compiled with
+ * CARBON_DEBUG_BOUNDS), when a kernel skipped an access outside its buffer
+ * (CARBON_ERR_OUT_OF_BOUNDS); or CARBON_ERR_CUDA if the stream reports an
+ * error. */
 carbon_status_t carbon_get_device_status(carbon_stream_t stream);
 
 /* Static, human-readable name of a status code. */
@@ -265,8 +269,8 @@ const char *carbon_last_cuda_error(void);
 
 /* ABI version of this header: (major << 16) | minor.  Minor 1 added
  * carbon_gemm_exact_bf16_noalloc and CARBON_ERR_SCRATCH_LIMIT; minor 2 the
- * CARBON_TIER_SUPERACC tier, carbon_gemm_chunk_values and
- * carbon_chunk_values_combine. */
+ * CARBON_TIER_SUPERACC tier, carbon_gemm_chunk_values,
+ * carbon_chunk_values_combine and CARBON_ERR_OUT_OF_BOUNDS. */
 int carbon_abi_version(void);
 
 #define CARBON_ABI_VERSION ((1 << 16) | 2)

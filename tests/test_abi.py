@@ -106,3 +106,18 @@ def test_superacc_tier_argument_checks():
     # no fp32 staging variant of the weight gradient on this tier
     assert b.lib.carbon_gemm_dw_f32(FAKE, FAKE, FAKE, 16, 16, 16, SUPERACC, None) == UNSUPPORTED
     assert b.lib.carbon_gemm_fwd(FAKE, FAKE, FAKE, None, 2, 3, 4, 0, 3, None) == INVALID
+
+
+def test_bounds_checked_library_exports_the_same_symbols():
+    """build() also builds the bounds-checked library (CARBON_DEBUG_BOUNDS)."""
+    path = os.path.join(os.path.dirname(b.LIB_PATH), "libcarbon_gemm_bounds.so")
+    if not os.path.exists(path):
+        pytest.skip("bounds-checked library not built")
+    raw = ctypes.CDLL(path)
+    for name in b.declared_functions():
+        assert hasattr(raw, name), name
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    raw.carbon_gemm_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, vp]
+    raw.carbon_gemm_fwd.restype = i32
+    assert raw.carbon_gemm_fwd(None, None, None, None, 0, 3, 4, 0, 0, None) == 0
+    assert raw.carbon_gemm_fwd(None, None, None, None, -1, 3, 4, 0, 0, None) == INVALID
