@@ -282,18 +282,34 @@ constexpr int kRawPitch = kChunk + 8;                 // bf16 per staged line (1
 // base over the chunks where it is nonzero and finite with width <= 62 (the
 // chunk repair adds the wider chunks in it).  FLAG_ONLY: only sets
 // flag[line] when some chunk of the line needs four digits.
+struct PrepArgs {
+    const unsigned short *src;
+    int64_t ls, rs, nlines, R, Lp, Rp;
+    int tg;
+    unsigned short *planes;
+    int4 *stats;
+    int *grain, *cnt;
+    int nchunks, vec;
+    const int *pos;
+    int *flag;
+};
+
+// One block's work: lines bx * 32 .. + 31 of chunk by (see above).
 template <bool RCONTIG, bool FLAG_ONLY>
-__global__ void __launch_bounds__(kPrepThreads)
-digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs, int64_t nlines,
-                  int64_t R, int64_t Lp, int64_t Rp, int tg, unsigned short *__restrict__ planes,
-                  int4 *__restrict__ stats, int *__restrict__ grain, int *__restrict__ cnt,
-                  int nchunks, int vec, const int *__restrict__ pos, int *__restrict__ flag) {
+__device__ __forceinline__ void prep_block(const PrepArgs &pa, int bx, int by) {
+    const unsigned short *__restrict__ src = pa.src;
+    const int64_t ls = pa.ls, rs = pa.rs, nlines = pa.nlines, R = pa.R, Lp = pa.Lp, Rp = pa.Rp;
+    const int tg = pa.tg, nchunks = pa.nchunks, vec = pa.vec;
+    unsigned short *__restrict__ planes = pa.planes;
+    int4 *__restrict__ stats = pa.stats;
+    int *__restrict__ grain = pa.grain;
+    int *__restrict__ cnt = pa.cnt;
+    const int *__restrict__ pos = pa.pos;
+    int *__restrict__ flag = pa.flag;
     __shared__ __align__(16) unsigned short raw[RCONTIG ? 1 : kPrepLines * kRawPitch];
-    wait_prior_grid();
-    allow_next_grid();
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int64_t line0 = (int64_t)blockIdx.x * kPrepLines;
-    const int q = blockIdx.y;
+    const int64_t line0 = (int64_t)bx * kPrepLines;
+    const int q = by;
     const int64_t q0 = (int64_t)q * kChunk;
     // extents for the bounds-checked build: the operand, the planes, the
     // statistics, the per-line arrays and the per-(tile, chunk) counts
@@ -323,25 +339,42 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
         }
         __syncthreads();
     }
-    for (int l = warp; l < kPrepLines; l += kPrepThreads / 32) {
-        const int64_t L = line0 + l;
-        const int64_t LP = (pos != nullptr && CHK(L, 1, Lp)) ? (int64_t)__ldg(&pos[L]) : L;   // the line's place in the planes
-        uint32_t h[8];
+    // a warp's lines are l = warp, warp + 8, ...: their loads are all issued
+    // before the first line is worked on (the loads' latency, not the
+    // arithmetic, bounds this kernel)
+    constexpr int kLinesPerWarp = kPrepLines / (kPrepThreads / 32);
+    uint4 pre[kLinesPerWarp];
+    int64_t places[kLinesPerWarp];
+#pragma unroll
+    for (int it = 0; it < kLinesPerWarp; ++it) {
+        const int64_t L = line0 + warp + (kPrepThreads / 32) * it;
+        places[it] = (pos != nullptr && CHK(L, 1, Lp)) ? (int64_t)__ldg(&pos[L]) : L;
         if (RCONTIG) {
             const int64_t r0 = q0 + 8 * lane;
             if (vec && L < nlines && r0 + 8 <= R && CHK(L * ls + r0, 8, n_src)) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + L * ls + r0));
-                h[0] = v.x & 0xffffu; h[1] = v.x >> 16; h[2] = v.y & 0xffffu; h[3] = v.y >> 16;
-                h[4] = v.z & 0xffffu; h[5] = v.z >> 16; h[6] = v.w & 0xffffu; h[7] = v.w >> 16;
+                pre[it] = __ldg(reinterpret_cast<const uint4 *>(src + L * ls + r0));
             } else {
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int64_t rr = r0 + e;
-                    h[e] = (L < nlines && rr < R && CHK(L * ls + rr, 1, n_src)) ? (uint32_t)__ldg(src + L * ls + rr) : 0u;
+                    const uint32_t v = (L < nlines && rr < R && CHK(L * ls + rr, 1, n_src))
+                                           ? (uint32_t)__ldg(src + L * ls + rr) : 0u;
+                    w[e / 2] |= v << (16 * (e & 1));
                 }
+                pre[it] = make_uint4(w[0], w[1], w[2], w[3]);
             }
         } else {
-            const uint4 v = *reinterpret_cast<const uint4 *>(&raw[l * kRawPitch + 8 * lane]);
+            pre[it] = *reinterpret_cast<const uint4 *>(&raw[(warp + (kPrepThreads / 32) * it) * kRawPitch + 8 * lane]);
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < kLinesPerWarp; ++it) {
+        const int64_t L = line0 + warp + (kPrepThreads / 32) * it;
+        const int64_t LP = places[it];                       // the line's place in the planes
+        uint32_t h[8];
+        {
+            const uint4 v = pre[it];
             h[0] = v.x & 0xffffu; h[1] = v.x >> 16; h[2] = v.y & 0xffffu; h[3] = v.y >> 16;
             h[4] = v.z & 0xffffu; h[5] = v.z >> 16; h[6] = v.w & 0xffffu; h[7] = v.w >> 16;
         }
@@ -425,6 +458,24 @@ digit_prep_kernel(const unsigned short *__restrict__ src, int64_t ls, int64_t rs
                     make_uint4(packed[a][0], packed[a][1], packed[a][2], packed[a][3]);
         }
     }
+}
+
+template <bool RCONTIG, bool FLAG_ONLY>
+__global__ void __launch_bounds__(kPrepThreads) digit_prep_kernel(const PrepArgs pa) {
+    wait_prior_grid();
+    allow_next_grid();
+    prep_block<RCONTIG, FLAG_ONLY>(pa, blockIdx.x, blockIdx.y);
+}
+
+// Two independent passes in one launch (the A side's flag pass and the B
+// side's digit planes): blocks [0, nx1) take the first, the rest the second.
+template <bool RC1, bool FO1, bool RC2, bool FO2>
+__global__ void __launch_bounds__(kPrepThreads)
+digit_prep_pair_kernel(const PrepArgs p1, int nx1, const PrepArgs p2) {
+    wait_prior_grid();
+    allow_next_grid();
+    if ((int)blockIdx.x < nx1) prep_block<RC1, FO1>(p1, blockIdx.x, blockIdx.y);
+    else prep_block<RC2, FO2>(p2, blockIdx.x - nx1, blockIdx.y);
 }
 
 // ---- main kernel ----------------------------------------------------------------
@@ -1083,140 +1134,175 @@ __global__ void exact_count_kernel(const unsigned int *chunk_count, unsigned int
 // and the sum is rounded once more, to float64 and then to bf16 (both nearest
 // even), all on integers; values outside those fast ranges take the float64
 // route.  The chunk range of an output may have been split into pieces whose
-// partial sums T add exactly.  One thread per 8 consecutive outputs of a row,
-// consecutive threads on consecutive rows (T is stored column-major, so each
-// of a warp's loads is 256 contiguous bytes).
+// partial sums T add exactly.
+//
+// Layout of the work: a block takes 256 consecutive rows (a thread each) and
+// 8 consecutive columns.  T is stored column-major, so each of a warp's loads
+// is 256 contiguous bytes (32 rows of one column); the 8 columns' grains and
+// biases are decoded once per block into shared memory; a thread's 8 outputs
+// are 16 contiguous bytes of its row.
 // Output modes of the finalize: the KBN tier's bf16 outputs, its float64
 // values (inspection), and the correctly rounded tier's bf16 outputs (the
 // exact total and the bias rounded once, never through float64).
 constexpr int kFinBf16 = 0, kFinF64 = 1, kFinSuper = 2;
+constexpr int kFinCols = 8;
+
+// bf16 bits of RN_bf16(RN_float64(V * 2^s)), short path for |V| < 2^53 (the
+// float64 rounding is then exact): the eight leading bits rounded to nearest
+// even by adding half an ulp less one plus the kept part's lowest bit, the
+// exponent field taking the carry of a rounding up to 2^8.  False when the
+// result leaves the bf16 normal range (the caller takes the float64 route).
+__device__ __forceinline__ bool round_int_to_bf16_fast(long long V, int s, uint32_t &bits) {
+    if (V == 0) { bits = 0u; return true; }
+    const uint32_t sign = V < 0 ? 0x8000u : 0u;
+    const unsigned long long mag = V < 0 ? 0ull - (unsigned long long)V : (unsigned long long)V;
+    const int nb = 64 - __clzll((long long)mag);
+    if (nb > 53) return round_int_to_bf16(V, s, bits);     // a float64 rounding first
+    const int E = nb - 1 + s;                               // value in [2^E, 2^(E+1))
+    if (E < -126 || E > 127) return false;
+    uint32_t m8;
+    if (nb > 8) {
+        const int sh = nb - 8;
+        const unsigned long long r = mag + ((1ull << (sh - 1)) - 1ull) + ((mag >> sh) & 1ull);
+        m8 = (uint32_t)(r >> sh);                           // 128 .. 256
+    } else {
+        m8 = (uint32_t)mag << (8 - nb);                     // exact
+    }
+    const uint32_t b = (uint32_t)(E + 126) * 128u + m8;    // 256 carries into the exponent
+    if (b >= 0x7f80u) return false;                         // rounded past the largest finite
+    bits = sign | b;
+    return true;
+}
+
+// Output bits (KBN tier, bf16) of one output: exact sum T in grain 2^G, bias
+// bm * 2^be (bm = 0: none; bad: inf/NaN) of column j.
+__device__ __forceinline__ uint32_t kbn_bits(long long T, int G, int bm, int be, bool bad,
+                                             const unsigned short *bias, int64_t j) {
+    long long Tv = T;
+    int gs = G;
+    bool fused = !bad;
+    if (fused && bm != 0) {
+        // the exact sum stays below 2^63: |T| < 2^61 and the bias term below
+        // 2^62, or |T| < 2^53 shifted by at most 9
+        if (be >= G && be - G <= 54 && below_pow2(T, 61)) {
+            Tv = (below_pow2(T, 53) ? T : round_to_53_bits(T)) + shl64(bm, (uint32_t)(be - G));
+        } else if (be < G && G - be <= 9 && below_pow2(T, 53)) {
+            Tv = shl64(T, (uint32_t)(G - be)) + bm;
+            gs = be;
+        } else {
+            fused = false;
+        }
+    }
+    uint32_t bits = 0u;
+    if (!(fused && round_int_to_bf16_fast(Tv, gs, bits))) bits = out_bits_f64(T, G, bias, j);
+    return bits;
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(256)
 exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int *__restrict__ GA,
                       const int *__restrict__ GB, const unsigned short *__restrict__ bias, void *out,
                       int64_t rows, int64_t cols, int vec_out) {
+    __shared__ int s_gw[kFinCols], s_bm[kFinCols], s_be[kFinCols], s_bad[kFinCols];
+    __shared__ uint32_t s_hb[kFinCols];
     wait_prior_grid();
     allow_next_grid();
-    const int64_t gpr = (cols + 7) / 8;                  // 8-column groups per row
-    const int64_t plane = rows * cols;
-    const int64_t rblocks = (rows + 255) / 256;
-    for (int64_t b = blockIdx.x; b < rblocks * gpr; b += gridDim.x) {
-        const int64_t i = (b % rblocks) * 256 + threadIdx.x, j0 = (b / rblocks) * 8;
-        if (i >= rows) continue;
-        const int64_t n_t = (int64_t)pieces * plane;
-        const int gx = CHK(i, 1, rows) ? __ldg(&GA[i]) : 0;
-        // every load first: the partial sums (a warp reads 32 consecutive
-        // rows of one column), the column grains and the bias
-        long long t0[8], t1[8];
-        int gw[8];
-        uint32_t hb[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const bool in = j0 + e < cols && CHK((j0 + e) * rows + i + (pieces > 1 ? plane : 0), 1, n_t);
-            t0[e] = in ? __ldg(&Tout[(j0 + e) * rows + i]) : 0ll;
-            t1[e] = (in && pieces > 1) ? __ldg(&Tout[plane + (j0 + e) * rows + i]) : 0ll;
-            gw[e] = in ? __ldg(&GB[j0 + e]) : 0;
-            hb[e] = (in && bias != nullptr) ? ld_bits(bias, j0 + e) : 0u;
-        }
-        uint32_t packed[4] = {0u, 0u, 0u, 0u};
-        uint32_t skip = 0u;
-        constexpr bool OUT_F64 = MODE == kFinF64;
-        if (MODE == kFinBf16 && pieces == 1) {
-            // one piece: 64-bit sums; the common case (the bias joins the sum
-            // exactly, the two roundings on the integer) stays straight-line,
-            // the rest takes the float64 route of out_bits_f64
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const long long T = t0[e];
-                if (j0 + e >= cols || T == kDeferredSum) { skip |= 1u << e; continue; }
-                const int G = gx + gw[e];
-                int bm = 0, be = 0;
-                bool bad = false;
-                decode(hb[e], bm, be, bad);
-                const bool t53 = below_pow2(T, 53);
-                long long Tv = T;
-                int gs = G;
-                bool fused = !bad;
-                if (bm != 0) {
-                    // the exact sum stays below 2^63: |T| < 2^61 and the bias
-                    // term below 2^62, or |T| < 2^53 shifted by at most 9
-                    if (be >= G && be - G <= 54 && below_pow2(T, 61)) {
-                        Tv = (t53 ? T : round_to_53_bits(T)) + shl64(bm, (uint32_t)(be - G));
-                    } else if (be < G && G - be <= 9 && t53) {
-                        Tv = shl64(T, (uint32_t)(G - be)) + bm;
-                        gs = be;
-                    } else {
-                        fused = false;
-                    }
-                }
-                uint32_t bits = 0u;
-                if (!(fused && round_int_to_bf16(Tv, gs, bits))) bits = out_bits_f64(T, G, bias, j0 + e);
-                packed[e / 2] |= bits << (16 * (e & 1));
-            }
-        } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int64_t j = j0 + e;
-            if (j >= cols) { skip |= 1u << e; continue; }
-            // the pieces' partial sums add exactly (128 bits)
-            bool deferred = t0[e] == kDeferredSum || (pieces > 1 && t1[e] == kDeferredSum);
-            __int128 acc = (__int128)t0[e] + (__int128)t1[e];
-            for (int k = 2; k < pieces && !deferred; ++k) {
-                if (!CHK(k * plane + j * rows + i, 1, n_t)) break;
-                const long long t = __ldg(&Tout[k * plane + j * rows + i]);
-                deferred = t == kDeferredSum;
-                acc += t;
-            }
-            if (deferred) { skip |= 1u << e; continue; }
-            const int G = gx + gw[e];
-            if (MODE == kFinSuper) {
-                int bm = 0, be = 0;
-                bool bad = false;
-                if (bias != nullptr) decode(hb[e], bm, be, bad);
-                packed[e / 2] |= sacc::exact_sum_bf16(acc, G, bm, be, bad, hb[e]) << (16 * (e & 1));
-                continue;
-            }
-            const bool small = acc >= -((__int128)1 << 62) && acc < ((__int128)1 << 62);
-            if (OUT_F64 || !small) {
-                double y = small ? round_int_to_double((long long)acc, G) : round_i128_to_double(acc, G);
-                if (bias != nullptr) y = __dadd_rn(y, widen_bf16(hb[e]));
-                if (OUT_F64 && CHK(i * cols + j, 1, plane)) static_cast<double *>(out)[i * cols + j] = y;
-                else packed[e / 2] |= (uint32_t)exact_round_bf16(y) << (16 * (e & 1));
-                continue;
-            }
-            const long long T = (long long)acc;
-            int bm = 0, be = 0;
+    const int64_t plane = rows * cols, n_t = (int64_t)pieces * plane;
+    const int64_t rblocks = (rows + 255) / 256, cgroups = (cols + kFinCols - 1) / kFinCols;
+    for (int64_t b = blockIdx.x; b < rblocks * cgroups; b += gridDim.x) {
+        const int64_t i = (b % rblocks) * 256 + threadIdx.x, j0 = (b / rblocks) * kFinCols;
+        __syncthreads();                                    // the previous columns' data is read
+        if (threadIdx.x < kFinCols) {
+            const int64_t j = j0 + threadIdx.x;
+            int gw = 0, bm = 0, be = 0;
             bool bad = false;
-            if (bias != nullptr) decode(hb[e], bm, be, bad);
-            long long Tv = T;
-            int gs = G;
-            bool fused = !bad;
-            if (fused && bm != 0) {
-                if (be >= G && be - G <= 54 && below_pow2(Tv, 61)) {
-                    if (!below_pow2(Tv, 53)) Tv = round_to_53_bits(Tv);
-                    Tv += shl64(bm, (uint32_t)(be - G));
-                } else if (be < G && G - be <= 9 && below_pow2(Tv, 53)) {
-                    Tv = shl64(Tv, (uint32_t)(G - be)) + bm;
-                    gs = be;
+            uint32_t hb = 0u;
+            if (j < cols && CHK(j, 1, cols)) {
+                gw = __ldg(&GB[j]);
+                if (bias != nullptr) { hb = ld_bits(bias, j); decode(hb, bm, be, bad); }
+            }
+            s_gw[threadIdx.x] = gw; s_bm[threadIdx.x] = bm; s_be[threadIdx.x] = be;
+            s_bad[threadIdx.x] = bad ? 1 : 0; s_hb[threadIdx.x] = hb;
+        }
+        __syncthreads();
+        if (i >= rows) continue;
+        const int gx = CHK(i, 1, rows) ? __ldg(&GA[i]) : 0;
+        const int ncol = (int)min((int64_t)kFinCols, cols - j0);
+        // the pieces' partial sums: in 64 bits with an overflow bit per output
+        // (bf16 outputs; an overflowing output adds its pieces again in 128
+        // bits), in 128 bits for the other modes
+        long long sum[kFinCols];
+        __int128 acc[MODE == kFinBf16 ? 1 : kFinCols];
+        uint32_t deferred = 0u, ovf = 0u;
+        for (int k = 0; k < pieces; ++k) {
+            long long t[kFinCols];
+#pragma unroll
+            for (int e = 0; e < kFinCols; ++e) {
+                const int64_t at = k * plane + (j0 + e) * rows + i;
+                t[e] = (e < ncol && CHK(at, 1, n_t)) ? __ldg(&Tout[at]) : 0ll;
+            }
+#pragma unroll
+            for (int e = 0; e < kFinCols; ++e) {
+                deferred |= (t[e] == kDeferredSum ? 1u : 0u) << e;
+                if constexpr (MODE == kFinBf16) {
+                    if (k == 0) {
+                        sum[e] = t[e];
+                    } else {
+                        // two's complement sum; it overflowed when both terms
+                        // have one sign and the sum the other
+                        const long long v = (long long)((unsigned long long)sum[e] + (unsigned long long)t[e]);
+                        ovf |= ((((sum[e] ^ v) & (t[e] ^ v)) < 0) ? 1u : 0u) << e;
+                        sum[e] = v;
+                    }
                 } else {
-                    fused = false;
+                    acc[e] = (k == 0 ? (__int128)0 : acc[e]) + (__int128)t[e];
                 }
             }
+        }
+        uint32_t packed[kFinCols / 2];
+#pragma unroll
+        for (int e = 0; e < kFinCols / 2; ++e) packed[e] = 0u;
+#pragma unroll
+        for (int e = 0; e < kFinCols; ++e) {
+            if (e >= ncol || ((deferred >> e) & 1u)) continue;
+            const int64_t j = j0 + e;
+            const int G = gx + s_gw[e];
+            const int bm = s_bm[e], be = s_be[e];
+            const bool bad = s_bad[e] != 0;
+            const uint32_t hb = s_hb[e];
             uint32_t bits = 0u;
-            if (!(fused && round_int_to_bf16(Tv, gs, bits))) bits = out_bits_f64(T, G, bias, j);
+            if constexpr (MODE == kFinBf16) {
+                if (!((ovf >> e) & 1u)) {
+                    bits = kbn_bits(sum[e], G, bm, be, bad, bias, j);
+                } else {                                    // the pieces' sum needs 128 bits
+                    __int128 a = 0;
+                    for (int k = 0; k < pieces; ++k) {
+                        const int64_t at = k * plane + j * rows + i;
+                        if (CHK(at, 1, n_t)) a += __ldg(&Tout[at]);
+                    }
+                    double y = round_i128_to_double(a, G);
+                    if (bias != nullptr) y = __dadd_rn(y, widen_bf16(hb));
+                    bits = exact_round_bf16(y);
+                }
+            } else if constexpr (MODE == kFinSuper) {
+                bits = sacc::exact_sum_bf16(acc[e], G, bm, be, bad, hb);
+            } else {                                        // float64 value (inspection)
+                const bool small = acc[e] >= -((__int128)1 << 62) && acc[e] < ((__int128)1 << 62);
+                double y = small ? round_int_to_double((long long)acc[e], G) : round_i128_to_double(acc[e], G);
+                if (bias != nullptr) y = __dadd_rn(y, widen_bf16(hb));
+                if (CHK(i * cols + j, 1, plane)) static_cast<double *>(out)[i * cols + j] = y;
+            }
             packed[e / 2] |= bits << (16 * (e & 1));
         }
-        }
-        if (OUT_F64) continue;
+        if constexpr (MODE == kFinF64) continue;
         unsigned short *orow = static_cast<unsigned short *>(out) + i * cols + j0;
-        if (!CHK(i * cols + j0, min((int64_t)8, cols - j0), plane)) continue;
-        if (skip == 0u && vec_out) {
+        if (!CHK(i * cols + j0, ncol, plane)) continue;
+        if (deferred == 0u && ncol == kFinCols && vec_out) {
             *reinterpret_cast<uint4 *>(orow) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if (!((skip >> e) & 1u)) orow[e] = (unsigned short)(packed[e / 2] >> (16 * (e & 1)));
+            for (int e = 0; e < kFinCols; ++e)
+                if (e < ncol && !((deferred >> e) & 1u)) orow[e] = (unsigned short)(packed[e / 2] >> (16 * (e & 1)));
         }
     }
 }
@@ -1254,7 +1340,7 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
         if (err != cudaSuccess) return err;
     }
     {
-        const int64_t want = ((a.rows + 255) / 256) * ((a.cols + 7) / 8), cap = 152 * 64;
+        const int64_t want = ((a.rows + 255) / 256) * ((a.cols + kFinCols - 1) / kFinCols), cap = 152 * 32;
         const unsigned grid = (unsigned)(want < cap ? want : cap);
         const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0 && (a.cols % 8) == 0) ? 1 : 0;
         err = launch_k(exact_finalize_kernel<MODE>, dim3(grid), dim3(256), 0, s, 1,
@@ -1287,16 +1373,33 @@ int choose_pieces(int64_t tiles, int64_t nchunks, int sms) {
     return s;
 }
 
-template <bool RCONTIG, bool FLAG_ONLY>
-cudaError_t launch_prep(const unsigned short *src, int64_t ls, int64_t rs, int64_t nlines, int64_t R,
-                        int64_t Lp, int64_t Rp, int tg, unsigned short *planes, int4 *stats,
-                        int *grain, int *cnt, int nchunks, const int *pos, int *flag, cudaStream_t s) {
-    const dim3 grid((unsigned)(Lp / kPrepLines), (unsigned)nchunks);
+PrepArgs prep_args(const unsigned short *src, int64_t ls, int64_t rs, int64_t nlines, int64_t R,
+                   int64_t Lp, int64_t Rp, int tg, unsigned short *planes, int4 *stats, int *grain,
+                   int *cnt, int nchunks, const int *pos, int *flag, bool rcontig) {
+    PrepArgs a;
+    a.src = src; a.ls = ls; a.rs = rs; a.nlines = nlines; a.R = R; a.Lp = Lp; a.Rp = Rp; a.tg = tg;
+    a.planes = planes; a.stats = stats; a.grain = grain; a.cnt = cnt; a.nchunks = nchunks;
     const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-    const int vec = RCONTIG ? (aligned && ls % 8 == 0) : (aligned && ls == 1 && rs % 8 == 0);
-    const cudaError_t err = launch_k(digit_prep_kernel<RCONTIG, FLAG_ONLY>, grid, dim3(kPrepThreads), 0, s, 1,
-                                     src, ls, rs, nlines, R, Lp, Rp, tg, planes, stats, grain, cnt,
-                                     nchunks, vec, pos, flag);
+    a.vec = rcontig ? (aligned && ls % 8 == 0) : (aligned && ls == 1 && rs % 8 == 0);
+    a.pos = pos; a.flag = flag;
+    return a;
+}
+
+template <bool RCONTIG, bool FLAG_ONLY>
+cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s) {
+    const dim3 grid((unsigned)(a.Lp / kPrepLines), (unsigned)a.nchunks);
+    const cudaError_t err = launch_k(digit_prep_kernel<RCONTIG, FLAG_ONLY>, grid, dim3(kPrepThreads), 0, s, 1, a);
+    count_launch();
+    return err;
+}
+
+// The A side's flag pass and the B side's planes, in one launch.
+template <bool RCA, bool RCB>
+cudaError_t launch_flag_and_prep_b(const PrepArgs &fa, const PrepArgs &pb, cudaStream_t s) {
+    const int nx1 = (int)(fa.Lp / kPrepLines);
+    const dim3 grid((unsigned)(nx1 + pb.Lp / kPrepLines), (unsigned)fa.nchunks);
+    const cudaError_t err = launch_k(digit_prep_pair_kernel<RCA, true, RCB, false>, grid, dim3(kPrepThreads),
+                                     0, s, 1, fa, nx1, pb);
     count_launch();
     return err;
 }
@@ -1438,20 +1541,26 @@ carbon_status_t exact_tc_launch(const Problem &p, bool out_f64, bool super, cuda
         count_launch();
     }
     const bool a_rc = (p.pass != CARBON_PASS_DW), b_rc = (p.pass == CARBON_PASS_DX);
+    const PrepArgs fa = prep_args(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA,
+                                  nullptr, (int)nchunks, nullptr, flagA, a_rc);
+    const PrepArgs pa = prep_args(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA,
+                                  cntA, (int)nchunks, posA, nullptr, a_rc);
+    const PrepArgs pb = prep_args(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB,
+                                  cntB, (int)nchunks, nullptr, nullptr, b_rc);
+    // the A rows' four-digit flags and the B planes (independent) in one
+    // launch, then the row order, then the A planes at the ordered places
     if (err == cudaSuccess && nchunks > 0)
-        err = a_rc ? launch_prep<true, true>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, nullptr, (int)nchunks, nullptr, flagA, stream)
-                   : launch_prep<false, true>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, nullptr, (int)nchunks, nullptr, flagA, stream);
+        err = a_rc ? (b_rc ? launch_flag_and_prep_b<true, true>(fa, pb, stream)
+                           : launch_flag_and_prep_b<true, false>(fa, pb, stream))
+                   : (b_rc ? launch_flag_and_prep_b<false, true>(fa, pb, stream)
+                           : launch_flag_and_prep_b<false, false>(fa, pb, stream));
     if (err == cudaSuccess) {
         err = launch_k(row_order_kernel, dim3((unsigned)((LpA + kOrderGroup - 1) / kOrderGroup)),
                        dim3(kOrderGroup), 0, stream, 1, flagA, p.rows, LpA, posA, invA);
         count_launch();
     }
     if (err == cudaSuccess && nchunks > 0)
-        err = a_rc ? launch_prep<true, false>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, posA, nullptr, stream)
-                   : launch_prep<false, false>(ia.A, ia.a_si, ia.a_sr, p.rows, p.R, LpA, Rp, kRowTile, PA, SA, GA, cntA, (int)nchunks, posA, nullptr, stream);
-    if (err == cudaSuccess && nchunks > 0)
-        err = b_rc ? launch_prep<true, false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, cntB, (int)nchunks, nullptr, nullptr, stream)
-                   : launch_prep<false, false>(ia.B, ia.b_sj, ia.b_sr, p.cols, p.R, LpB, Rp, kColTile, PB, SB, GB, cntB, (int)nchunks, nullptr, nullptr, stream);
+        err = a_rc ? launch_prep<true, false>(pa, stream) : launch_prep<false, false>(pa, stream);
     // planes as 2-D [4 Lp][Rp] bf16 maps, 64-deep boxes, 128-byte swizzle:
     // one A plane of a row tile (128 rows), all four B planes of a column tile
     // (256 rows) per box

@@ -70,16 +70,30 @@ superacc_kernel(const SaArgs p, const unsigned int *__restrict__ work_count,
         for (int d = 0; d < sacc::kDigits; ++d) acc[d] = 0ll;
         int cls = sacc::kFinite;
         uint32_t steps = 0;
-        for (int64_t r = lane; r < p.R; r += 32) {
-            if ((++steps & 0xfffffu) == 0u) sacc::carry(acc);   // digits stay below 2^53
-            long long ma, mb;
-            int ea, eb, ca, cb;
-            if (!CHK(i * p.a_si + r * p.a_sr, 1, n_a) || !CHK(r * p.b_sr + j * p.b_sj, 1, n_b)) continue;
-            sacc::decode_value<DT>(load_bits<DT>(p.A, i * p.a_si + r * p.a_sr), ma, ea, ca);
-            sacc::decode_value<DT>(load_bits<DT>(p.B, r * p.b_sr + j * p.b_sj), mb, eb, cb);
-            const int pc = sacc::product_class(ca, ma, cb, mb);
-            if (pc != sacc::kFinite) { cls |= pc; continue; }
-            if (ma != 0 && mb != 0) sacc::add_scaled(acc, ma * mb, ea + eb + sacc::kOff);
+        // kUnroll reduction indices per lane and step, their loads issued
+        // first (the operand reads are strided: their latency bounds the loop)
+        constexpr int kUnroll = 4;
+        for (int64_t r0 = lane; r0 < p.R; r0 += 32 * kUnroll) {
+            if ((++steps & 0x3ffffu) == 0u) sacc::carry(acc);   // digits stay below 2^53
+            uint32_t ha[kUnroll], hb[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t r = r0 + 32 * u;
+                const bool in = r < p.R && CHK(i * p.a_si + r * p.a_sr, 1, n_a) &&
+                                CHK(r * p.b_sr + j * p.b_sj, 1, n_b);
+                ha[u] = in ? load_bits<DT>(p.A, i * p.a_si + r * p.a_sr) : 0u;
+                hb[u] = in ? load_bits<DT>(p.B, r * p.b_sr + j * p.b_sj) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                long long ma, mb;
+                int ea, eb, ca, cb;
+                sacc::decode_value<DT>(ha[u], ma, ea, ca);           // 0 bits: +0, adds nothing
+                sacc::decode_value<DT>(hb[u], mb, eb, cb);
+                const int pc = sacc::product_class(ca, ma, cb, mb);
+                if (pc != sacc::kFinite) { cls |= pc; continue; }
+                if (ma != 0 && mb != 0) sacc::add_scaled(acc, ma * mb, ea + eb + sacc::kOff);
+            }
         }
         if (p.bias != nullptr && lane == 0) {
             long long mb;
