@@ -142,7 +142,8 @@ constexpr int kMmaN = kColTile * kPlanes;             // 256
 constexpr int kKBlock = 64;                           // reduction indices per 128-byte swizzle row
 constexpr int kKBlocks = kChunk / kKBlock;            // 4
 constexpr int kUmmaK = 16;
-constexpr int kAStages = 5;
+constexpr int kAStages = 4;                           // one k-group of A plane blocks...
+constexpr int kAPairs = kAStages / 2;                 // ...signalled in pairs (half a k-group each)
 constexpr int kEpiWarps = 8;
 constexpr int kTcxThreads = 384;                      // warpgroup 0: TMA + MMA; 1-2: epilogue
 constexpr int kUnitSlots = 4;                         // work units handed from the B producer to the others
@@ -173,10 +174,10 @@ constexpr uint32_t kStartBBits = 0x4AC0u;                 // bf16 1.5 * 2^22
 
 struct __align__(1024) TcxSmem {
     uint8_t B[kKBlocks][kBBytes];                     // 128 KiB: the chunk's B planes
-    uint8_t A[kAStages][kABytes];                     // 80 KiB: A plane blocks
+    uint8_t A[kAStages][kABytes];                     // 64 KiB: A plane blocks
     uint8_t SA0[kStartABytes], SB0[kStartBBytes];     // 12 KiB: the accumulators' start tiles
     uint32_t pk[kEpiWarps][32];                       // packed column words of the current chunk
-    uint64_t afull[kAStages], aempty[kAStages], bfull[kKBlocks], bempty[kKBlocks];
+    uint64_t afull[kAPairs], aempty[kAPairs], bfull[kKBlocks], bempty[kKBlocks];
     uint64_t tfull[2], tempty[2], mdone;
     uint64_t ufull[kUnitSlots], uempty[kUnitSlots];
     int unit_q[kUnitSlots];                           // work unit in each slot (-1: no more)
@@ -576,8 +577,8 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
     volatile uint32_t *abort_flag = &sm.abort;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kAStages; ++s) {
-            mbar_init(smem_addr(&sm.afull[s]), 1);
+        for (int s = 0; s < kAPairs; ++s) {
+            mbar_init(smem_addr(&sm.afull[s]), 2);           // both A producers arrive
             mbar_init(smem_addr(&sm.aempty[s]), 1);
         }
         for (int kb = 0; kb < kKBlocks; ++kb) {
@@ -620,10 +621,13 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
       if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ A producers
-        // The A loads of the CTA, numbered g = 0, 1, ... in the order the MMA
-        // consumes them, go to stage g % kAStages; warp 0 issues the even g,
-        // warp 2 the odd ones (one thread's copies complete one after another,
-        // so two threads double the rate).
+        // The A loads of the CTA: k-group kg (counted over the CTA's units)
+        // puts its 64-deep block kb in stage kb; stages 0-1 and 2-3 form the
+        // pairs the MMA issuer waits for and releases together (two waits and
+        // two commits per k-group instead of four each).  Warp 0 issues blocks
+        // 0 and 2, warp 2 blocks 1 and 3 (one thread's copies complete one
+        // after another, so two threads double the rate); both arrive on the
+        // pair's barrier.
         if (lane == 0) {
             const uint32_t mine = warp == 0 ? 0u : 1u;
             uint32_t g = 0, n = 0;
@@ -640,24 +644,25 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                 for (int q = qlo; ok && q < qhi; ++q) {
                     const int nx = CHK((int64_t)tm * nchunks + q, 1, (int64_t)p.tiles_m * nchunks)
                                        ? p.cntA[(int64_t)tm * nchunks + q] : 0;
-                    for (int k = 0; ok && k < nx; ++k)
-                        for (int kb = 0; kb < kKBlocks; ++kb, ++g) {
-                            if ((g & 1u) != mine) continue;
-                            const uint32_t st = g % kAStages, use = g / kAStages;
-                            if (!(ok = wait_or_abort(smem_addr(&sm.aempty[st]), (use & 1u) ^ 1u, abort_flag))) break;
-                            const uint32_t fa = smem_addr(&sm.afull[st]);
+                    for (int k = 0; ok && k < nx; ++k) {
+                        for (int kb = 0; kb < kKBlocks; ++kb) {
+                            if ((uint32_t)(kb & 1) != mine) continue;
+                            const uint32_t pr = (uint32_t)kb >> 1;
+                            if (!(ok = wait_or_abort(smem_addr(&sm.aempty[pr]), (g & 1u) ^ 1u, abort_flag))) break;
+                            const uint32_t fa = smem_addr(&sm.afull[pr]);
                             mbar_arrive_expect_tx(fa, kABytes);
-                            tma_load_2d(smem_addr(&sm.A[st][0]), &map_a, fa, q * kChunk + kb * kKBlock,
+                            tma_load_2d(smem_addr(&sm.A[kb][0]), &map_a, fa, q * kChunk + kb * kKBlock,
                                         tm * kPlanes * kRowTile + k * kRowTile);
                         }
+                        if (ok) ++g;                                // k-groups issued
+                    }
                 }
             }
-            // the last use of each stage lands before the CTA may exit (an
-            // earlier use was consumed, hence landed, before the stage was reused)
-            for (uint32_t st = 0; st < (uint32_t)kAStages && st < g; ++st) {
-                const uint32_t last = st + ((g - 1u - st) / kAStages) * kAStages;
-                if ((last & 1u) == mine && !mbar_wait(smem_addr(&sm.afull[st]), (last / kAStages) & 1u)) break;
-            }
+            // the last use of each pair lands before the CTA may exit (an
+            // earlier use was consumed, hence landed, before the pair was reused)
+            if (g > 0)
+                for (uint32_t pr = 0; pr < (uint32_t)kAPairs; ++pr)
+                    if (!mbar_wait(smem_addr(&sm.afull[pr]), (g - 1u) & 1u)) break;
         }
       } else if (warp == 3) {
         // ------------------------------------------------------------ B producer
@@ -702,7 +707,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             constexpr uint32_t idesc = idesc0 | ((uint32_t)(kMmaN >> 3) << 17);
             const uint64_t sdesc_a0 = smem_desc_noswizzle(smem_addr(&sm.SA0[0]), 128, 256);
             const uint64_t sdesc_b0 = smem_desc_noswizzle(smem_addr(&sm.SB0[0]), 128, 256);
-            int s = 0, acc = 0;
+            int acc = 0;
             uint32_t ph = 0, bu = 0, aph = 0;
             unsigned long long kgroups = 0;
             uint32_t n = 0;
@@ -730,17 +735,21 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         mma_bf16(d, sdesc_a0, sdesc_b0, idesc, 0u);    // every element 1.5 * 2^23
                         for (int kb = 0; kb < kKBlocks; ++kb) {
                             if (k == 0 && !(ok = wait_or_abort(smem_addr(&sm.bfull[kb]), bu & 1u, abort_flag))) break;
-                            if (!(ok = wait_or_abort(smem_addr(&sm.afull[s]), ph, abort_flag))) break;
-                            tc_fence_after();
-                            const uint32_t sa = smem_addr(&sm.A[s][0]), sb = smem_addr(&sm.B[kb][0]);
+                            if ((kb & 1) == 0) {
+                                if (!(ok = wait_or_abort(smem_addr(&sm.afull[kb >> 1]), ph, abort_flag))) break;
+                                tc_fence_after();
+                            } else if (k == 0) {
+                                tc_fence_after();                   // after the bfull wait above
+                            }
+                            const uint32_t sa = smem_addr(&sm.A[kb][0]), sb = smem_addr(&sm.B[kb][0]);
 #pragma unroll
                             for (int kk = 0; kk < kKBlock / kUmmaK; ++kk)
                                 mma_bf16(d, smem_desc(sa + kk * (kUmmaK * 2), 16, 1024),
                                          smem_desc(sb + kk * (kUmmaK * 2), 16, 1024), idesc_q, 1u);
-                            mma_commit(smem_addr(&sm.aempty[s]));
+                            if (kb & 1) mma_commit(smem_addr(&sm.aempty[kb >> 1]));
                             if (k == nx - 1) mma_commit(smem_addr(&sm.bempty[kb]));
-                            if (++s == kAStages) { s = 0; ph ^= 1u; }
                         }
+                        ph ^= 1u;                                   // the next k-group's pair phase
                         if (!ok) break;
                         mma_commit(smem_addr(&sm.tfull[acc]));          // k-group done
                         kgroups += (unsigned long long)nb;              // A plane x nb B planes
