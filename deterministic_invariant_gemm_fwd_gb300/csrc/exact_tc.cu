@@ -177,7 +177,7 @@ struct __align__(1024) TcxSmem {
     uint8_t A[kAStages][kABytes];                     // 64 KiB: A plane blocks
     uint8_t SA0[kStartABytes], SB0[kStartBBytes];     // 12 KiB: the accumulators' start tiles
     uint32_t pk[kEpiWarps][32];                       // packed column words of the current chunk
-    uint64_t afull[kAPairs], aempty[kAPairs], bfull[kKBlocks], bempty[kKBlocks];
+    uint64_t afull[kAPairs], aempty[kAPairs], bfull[kKBlocks / 2], bempty[kKBlocks / 2];
     uint64_t tfull[2], tempty[2], mdone;
     uint64_t ufull[kUnitSlots], uempty[kUnitSlots];
     int unit_q[kUnitSlots];                           // work unit in each slot (-1: no more)
@@ -581,9 +581,9 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
             mbar_init(smem_addr(&sm.afull[s]), 2);           // both A producers arrive
             mbar_init(smem_addr(&sm.aempty[s]), 1);
         }
-        for (int kb = 0; kb < kKBlocks; ++kb) {
-            mbar_init(smem_addr(&sm.bfull[kb]), 1);
-            mbar_init(smem_addr(&sm.bempty[kb]), 1);
+        for (int pr = 0; pr < kKBlocks / 2; ++pr) {
+            mbar_init(smem_addr(&sm.bfull[pr]), 1);
+            mbar_init(smem_addr(&sm.bempty[pr]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&sm.tfull[b]), 1);
@@ -682,19 +682,21 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     if (!CHK((int64_t)tm * nchunks + q, 1, (int64_t)p.tiles_m * nchunks) ||
                         p.cntA[(int64_t)tm * nchunks + q] == 0)
                         continue;
-                    for (int kb = 0; kb < kKBlocks; ++kb) {
-                        if (!(ok = wait_or_abort(smem_addr(&sm.bempty[kb]), (bu & 1u) ^ 1u, abort_flag))) break;
-                        const uint32_t fb = smem_addr(&sm.bfull[kb]);
-                        mbar_arrive_expect_tx(fb, kBBytes);
-                        tma_load_2d(smem_addr(&sm.B[kb][0]), &map_b, fb, q * kChunk + kb * kKBlock,
-                                    tn * kPlanes * kColTile);
+                    // blocks 0-1 and 2-3 in pairs, one barrier each
+                    for (int pr = 0; pr < kKBlocks / 2; ++pr) {
+                        if (!(ok = wait_or_abort(smem_addr(&sm.bempty[pr]), (bu & 1u) ^ 1u, abort_flag))) break;
+                        const uint32_t fb = smem_addr(&sm.bfull[pr]);
+                        mbar_arrive_expect_tx(fb, 2 * kBBytes);
+                        for (int kb = 2 * pr; kb < 2 * pr + 2; ++kb)
+                            tma_load_2d(smem_addr(&sm.B[kb][0]), &map_b, fb, q * kChunk + kb * kKBlock,
+                                        tn * kPlanes * kColTile);
                     }
                     if (ok) ++bu;
                 }
             }
             if (bu > 0)
-                for (int kb = 0; kb < kKBlocks; ++kb)
-                    if (!mbar_wait(smem_addr(&sm.bfull[kb]), (bu - 1u) & 1u)) break;
+                for (int pr = 0; pr < kKBlocks / 2; ++pr)
+                    if (!mbar_wait(smem_addr(&sm.bfull[pr]), (bu - 1u) & 1u)) break;
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -734,20 +736,21 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         const uint32_t d = tmem + (uint32_t)(acc * kMmaN);
                         mma_bf16(d, sdesc_a0, sdesc_b0, idesc, 0u);    // every element 1.5 * 2^23
                         for (int kb = 0; kb < kKBlocks; ++kb) {
-                            if (k == 0 && !(ok = wait_or_abort(smem_addr(&sm.bfull[kb]), bu & 1u, abort_flag))) break;
-                            if ((kb & 1) == 0) {
+                            if ((kb & 1) == 0) {                     // a pair of A (and B) blocks
+                                if (k == 0 && !(ok = wait_or_abort(smem_addr(&sm.bfull[kb >> 1]), bu & 1u, abort_flag)))
+                                    break;
                                 if (!(ok = wait_or_abort(smem_addr(&sm.afull[kb >> 1]), ph, abort_flag))) break;
                                 tc_fence_after();
-                            } else if (k == 0) {
-                                tc_fence_after();                   // after the bfull wait above
                             }
                             const uint32_t sa = smem_addr(&sm.A[kb][0]), sb = smem_addr(&sm.B[kb][0]);
 #pragma unroll
                             for (int kk = 0; kk < kKBlock / kUmmaK; ++kk)
                                 mma_bf16(d, smem_desc(sa + kk * (kUmmaK * 2), 16, 1024),
                                          smem_desc(sb + kk * (kUmmaK * 2), 16, 1024), idesc_q, 1u);
-                            if (kb & 1) mma_commit(smem_addr(&sm.aempty[kb >> 1]));
-                            if (k == nx - 1) mma_commit(smem_addr(&sm.bempty[kb]));
+                            if (kb & 1) {
+                                mma_commit(smem_addr(&sm.aempty[kb >> 1]));
+                                if (k == nx - 1) mma_commit(smem_addr(&sm.bempty[kb >> 1]));
+                            }
                         }
                         ph ^= 1u;                                   // the next k-group's pair phase
                         if (!ok) break;
