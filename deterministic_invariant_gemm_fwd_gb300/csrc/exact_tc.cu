@@ -648,7 +648,16 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                         for (int kb = 0; kb < kKBlocks; ++kb) {
                             if ((uint32_t)(kb & 1) != mine) continue;
                             const uint32_t pr = (uint32_t)kb >> 1;
-                            if (!(ok = wait_or_abort(smem_addr(&sm.aempty[pr]), (g & 1u) ^ 1u, abort_flag))) break;
+                            // pair 0 is freed by its own commit; pair 1 when the
+                            // previous k-group has finished, which its accumulator's
+                            // commit (tfull) already signals
+                            if (pr == 0) {
+                                if (!(ok = wait_or_abort(smem_addr(&sm.aempty[0]), (g & 1u) ^ 1u, abort_flag))) break;
+                            } else if (g > 0) {
+                                if (!(ok = wait_or_abort(smem_addr(&sm.tfull[(g - 1u) & 1u]), ((g - 1u) >> 1) & 1u,
+                                                         abort_flag)))
+                                    break;
+                            }
                             const uint32_t fa = smem_addr(&sm.afull[pr]);
                             mbar_arrive_expect_tx(fa, kABytes);
                             tma_load_2d(smem_addr(&sm.A[kb][0]), &map_a, fa, q * kChunk + kb * kKBlock,
@@ -668,7 +677,7 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
         // ------------------------------------------------------------ B producer
         // per chunk the four planes of each 64-deep block, 256 rows in one box
         if (lane == 0) {
-            uint32_t bu = 0, n = 0;
+            uint32_t bu = 0, n = 0, kg = 0;                  // chunks and k-groups loaded
             bool ok = true;
             while (ok) {
                 int u;
@@ -682,16 +691,27 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                     if (!CHK((int64_t)tm * nchunks + q, 1, (int64_t)p.tiles_m * nchunks) ||
                         p.cntA[(int64_t)tm * nchunks + q] == 0)
                         continue;
-                    // blocks 0-1 and 2-3 in pairs, one barrier each
+                    // blocks 0-1 and 2-3 in pairs, one barrier each; pair 1 is
+                    // free once the previous chunk's last k-group has finished
+                    // (its accumulator's commit, tfull, signals that)
                     for (int pr = 0; pr < kKBlocks / 2; ++pr) {
-                        if (!(ok = wait_or_abort(smem_addr(&sm.bempty[pr]), (bu & 1u) ^ 1u, abort_flag))) break;
+                        if (pr == 0) {
+                            if (!(ok = wait_or_abort(smem_addr(&sm.bempty[0]), (bu & 1u) ^ 1u, abort_flag))) break;
+                        } else if (kg > 0) {
+                            if (!(ok = wait_or_abort(smem_addr(&sm.tfull[(kg - 1u) & 1u]), ((kg - 1u) >> 1) & 1u,
+                                                     abort_flag)))
+                                break;
+                        }
                         const uint32_t fb = smem_addr(&sm.bfull[pr]);
                         mbar_arrive_expect_tx(fb, 2 * kBBytes);
                         for (int kb = 2 * pr; kb < 2 * pr + 2; ++kb)
                             tma_load_2d(smem_addr(&sm.B[kb][0]), &map_b, fb, q * kChunk + kb * kKBlock,
                                         tn * kPlanes * kColTile);
                     }
-                    if (ok) ++bu;
+                    if (ok) {
+                        ++bu;
+                        kg += (uint32_t)p.cntA[(int64_t)tm * nchunks + q];   // this chunk's k-groups
+                    }
                 }
             }
             if (bu > 0)
@@ -747,9 +767,9 @@ exact_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant
                             for (int kk = 0; kk < kKBlock / kUmmaK; ++kk)
                                 mma_bf16(d, smem_desc(sa + kk * (kUmmaK * 2), 16, 1024),
                                          smem_desc(sb + kk * (kUmmaK * 2), 16, 1024), idesc_q, 1u);
-                            if (kb & 1) {
-                                mma_commit(smem_addr(&sm.aempty[kb >> 1]));
-                                if (k == nx - 1) mma_commit(smem_addr(&sm.bempty[kb >> 1]));
+                            if (kb == 1) {                          // pair 1 is signalled by tfull
+                                mma_commit(smem_addr(&sm.aempty[0]));
+                                if (k == nx - 1) mma_commit(smem_addr(&sm.bempty[0]));
                             }
                         }
                         ph ^= 1u;                                   // the next k-group's pair phase
