@@ -254,9 +254,12 @@ __device__ __forceinline__ void free_unit_slot(TcxSmem &sm, uint32_t n) {
 
 // ---- pre-pass: statistics and digit planes ------------------------------------
 
-// bf16 bits of an integer of magnitude <= 256 (exact).
-__device__ __forceinline__ uint32_t small_int_bf16(int d) {
-    return __float_as_uint((float)d) >> 16;
+// bf16 bits of two integers of magnitude <= 256 (exact), hi in the upper
+// half of the word and lo in the lower.
+__device__ __forceinline__ uint32_t small_int_bf16_pair(int hi, int lo) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"((float)hi), "f"((float)lo));
+    return r;
 }
 
 // Digits a line of this width needs (0: all zero, or not representable).
@@ -408,18 +411,19 @@ __device__ __forceinline__ void prep_block(const PrepArgs &pa, int bx, int by) {
             if (lane == 0 && n == kPlanes && L < nlines && CHK(L, 1, Lp)) atomicOr(&flag[L], 1);
             continue;
         }
-        int X[8];
         unsigned long long sum = 0ull;
         unsigned int mx = 0u;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            X[e] = (use && m[e] != 0) ? m[e] * (1 << (ex[e] - base)) : 0;     // |X| < 2^31
-            const unsigned int a = (unsigned int)abs(X[e]);
+            const int X = (use && m[e] != 0) ? m[e] * (1 << (ex[e] - base)) : 0;   // |X| < 2^31
+            const unsigned int a = (unsigned int)abs(X);
             sum += a;
             mx = max(mx, a);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        // the line's sum (below 2^39) from two 32-bit warp sums of its 16-bit
+        // halves (each below 2^24)
+        sum = ((unsigned long long)__reduce_add_sync(0xffffffffu, (unsigned)(sum >> 16)) << 16) +
+              __reduce_add_sync(0xffffffffu, (unsigned)(sum & 0xffffu));
         mx = __reduce_max_sync(0xffffffffu, mx);
         if (lane == 0) {
             if (CHK((int64_t)q * Lp + L, 1, n_stats))
@@ -434,21 +438,30 @@ __device__ __forceinline__ void prep_block(const PrepArgs &pa, int bx, int by) {
         // balanced digits, lo = v mod 256 in [-128, 127] at plane a and
         // hi = (v - lo) / 256 (|hi| <= 128) at plane a + 1; hi is 0 when a is
         // the line's top plane (then |v| < 2^(width % 8) <= 128)
-        uint32_t packed[kPlanes][4];
-#pragma unroll
-        for (int a = 0; a < kPlanes; ++a)
-#pragma unroll
-            for (int w = 0; w < 4; ++w) packed[a][w] = 0u;
+        // The pair (hi, lo) of a value, as bf16 bits in one word, is moved to
+        // the 16-bit fields a and a + 1 of a 64-bit word of the four planes
+        // (a = 3 only when hi is 0, so nothing is shifted out); plane p of two
+        // neighbouring values is then field p of their words, one byte
+        // permute per plane and pair.
+        static_assert(kPlanes == 4, "four 16-bit plane fields per 64-bit word");
+        uint32_t wlo[8], whi[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int sh = ex[e] - base;
             const int v = (use && m[e] != 0) ? m[e] * (1 << (sh & 7)) : 0;    // |v| < 2^15
-            const int a = sh >> 3;
-            const int lo = ((v + 128) & 255) - 128;
-            const uint32_t blo = small_int_bf16(lo), bhi = small_int_bf16((v - lo) >> 8);
+            const int lo = (int)(int8_t)v;                         // v mod 256 in [-128, 127]
+            const unsigned long long w = (unsigned long long)small_int_bf16_pair((v - lo) >> 8, lo)
+                                         << (16 * ((sh >> 3) & 3));            // v = 0: all zero
+            wlo[e] = (uint32_t)w;
+            whi[e] = (uint32_t)(w >> 32);
+        }
+        uint32_t packed[kPlanes][4];
 #pragma unroll
-            for (int p = 0; p < kPlanes; ++p)
-                packed[p][e / 2] |= (p == a ? blo : (p == a + 1 ? bhi : 0u)) << (16 * (e & 1));
+        for (int w = 0; w < 4; ++w) {
+            packed[0][w] = __byte_perm(wlo[2 * w], wlo[2 * w + 1], 0x5410);
+            packed[1][w] = __byte_perm(wlo[2 * w], wlo[2 * w + 1], 0x7632);
+            packed[2][w] = __byte_perm(whi[2 * w], whi[2 * w + 1], 0x5410);
+            packed[3][w] = __byte_perm(whi[2 * w], whi[2 * w + 1], 0x7632);
         }
         const int64_t row = (LP / tg) * kPlanes * tg + LP % tg;
 #pragma unroll
@@ -500,38 +513,6 @@ __device__ __forceinline__ void acc_pair_lo(unsigned long long &I, uint32_t P, u
 // which fits a signed 32-bit value.
 constexpr uint32_t kPairFix = 0u - 257u * kMagicBits;
 
-// bf16 bits of RN_bf16(RN_float64(V * 2^s)) (both nearest-even), |V| < 2^63,
-// computed on the integer: false when the result leaves the bf16 normal
-// range (the caller then rounds through float64).
-__device__ __forceinline__ bool round_int_to_bf16(long long V, int s, uint32_t &bits) {
-    if (V == 0) { bits = 0u; return true; }
-    const uint32_t sign = V < 0 ? 0x8000u : 0u;
-    unsigned long long mag = V < 0 ? 0ull - (unsigned long long)V : (unsigned long long)V;
-    int nb = 64 - __clzll((long long)mag);
-    if (nb > 53) {                                          // the float64 rounding
-        const int sh = nb - 53;
-        const unsigned long long rem = mag & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
-        unsigned long long m = mag >> sh;
-        m += (rem > half || (rem == half && (m & 1ull))) ? 1ull : 0ull;
-        mag = m << sh;
-        nb = 64 - __clzll((long long)mag);
-    }
-    uint32_t m8;
-    if (nb > 8) {                                           // the bf16 rounding
-        const int sh = nb - 8;
-        const unsigned long long rem = mag & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
-        m8 = (uint32_t)(mag >> sh);
-        m8 += (rem > half || (rem == half && (m8 & 1u))) ? 1u : 0u;
-        if (m8 == 256u) { m8 = 128u; ++nb; }
-    } else {
-        m8 = (uint32_t)mag << (8 - nb);
-    }
-    const int E = nb - 1 + s;                               // value in [2^E, 2^(E+1))
-    if (E < -126 || E > 127) return false;
-    bits = sign | ((uint32_t)(E + 127) << 7) | (m8 & 0x7fu);
-    return true;
-}
-
 // Output bits the long way: float64 value, bias in float64, one rounding.
 __device__ __noinline__ uint32_t out_bits_f64(long long T, int G, const unsigned short *bias, int64_t j) {
     double y = round_int_to_double(T, G);
@@ -562,6 +543,40 @@ __device__ __forceinline__ long long round_to_53_bits(long long I) {
     m += (rem > half || (rem == half && (m & 1ull))) ? 1ull : 0ull;
     const unsigned long long r = m << sh;
     return neg ? -(long long)r : (long long)r;
+}
+
+// bf16 bits of RN_bf16(V * 2^s) (nearest even), |V| < 2^53, on the conversion
+// units: V truncated to float32 with the lowest bit set when any bit was
+// dropped (rounding to odd at 24 bits), scaled by 2^s in the exponent field,
+// and rounded to nearest even to bf16.  Rounding to odd at p + 2 or more bits
+// and then to nearest at p bits gives the one rounding to nearest at p bits
+// (Boldo and Melquiond, "Emulation of FMA and correctly rounded sums: proved
+// algorithms using rounding to odd", IEEE Trans. Computers 57(4), 2008); here
+// p = 8.  False when the value or the result is not a bf16 normal number (the
+// caller then takes the float64 route).
+__device__ __forceinline__ bool round_small_int_to_bf16(long long V, int s, uint32_t &bits) {
+    float f;
+    long long back;
+    asm("cvt.rz.f32.s64 %0, %1;" : "=f"(f) : "l"(V));
+    asm("cvt.rzi.s64.f32 %0, %1;" : "=l"(back) : "f"(f));
+    uint32_t fb = __float_as_uint(f);
+    if (fb == 0u) { bits = 0u; return true; }               // V == 0
+    const int ef = (int)((fb >> 23) & 0xffu) + s;           // biased exponent of the result
+    if (ef < 1 || ef > 254) return false;
+    fb = (fb + ((uint32_t)s << 23)) | (back != V ? 1u : 0u);
+    unsigned short h;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(__uint_as_float(fb)));
+    if ((h & 0x7fffu) >= 0x7f80u) return false;             // rounded past the largest finite
+    bits = h;
+    return true;
+}
+
+// bf16 bits of RN_bf16(RN_float64(V * 2^s)) (both nearest even), |V| < 2^63:
+// V is first rounded to 53 significant bits when wider (the float64
+// rounding; exact otherwise).  False as above.
+__device__ __forceinline__ bool round_int_to_bf16(long long V, int s, uint32_t &bits) {
+    if (!below_pow2(V, 53)) V = round_to_53_bits(V);
+    return round_small_int_to_bf16(V, s, bits);
 }
 
 // SUPER: the correctly rounded tier (chunk sums are added exactly, never
@@ -1169,47 +1184,21 @@ __global__ void exact_count_kernel(const unsigned int *chunk_count, unsigned int
 // partial sums T add exactly.
 //
 // Layout of the work: a block takes 256 consecutive rows (a thread each) and
-// 8 consecutive columns.  T is stored column-major, so each of a warp's loads
-// is 256 contiguous bytes (32 rows of one column); the 8 columns' grains and
-// biases are decoded once per block into shared memory; a thread's 8 outputs
-// are 16 contiguous bytes of its row.
+// a group of 8 consecutive columns (a two-dimensional grid, no division).  T
+// is stored column-major, so each of a warp's loads is 256 contiguous bytes
+// (32 rows of one column); the 8 columns' grains and biases are decoded once
+// per block into one shared 16-byte word per column (one broadcast load per
+// output); a thread's 8 outputs are 16 contiguous bytes of its row.
 // Output modes of the finalize: the KBN tier's bf16 outputs, its float64
 // values (inspection), and the correctly rounded tier's bf16 outputs (the
 // exact total and the bias rounded once, never through float64).
 constexpr int kFinBf16 = 0, kFinF64 = 1, kFinSuper = 2;
 constexpr int kFinCols = 8;
 
-// bf16 bits of RN_bf16(RN_float64(V * 2^s)), short path for |V| < 2^53 (the
-// float64 rounding is then exact): the eight leading bits rounded to nearest
-// even by adding half an ulp less one plus the kept part's lowest bit, the
-// exponent field taking the carry of a rounding up to 2^8.  False when the
-// result leaves the bf16 normal range (the caller takes the float64 route).
-__device__ __forceinline__ bool round_int_to_bf16_fast(long long V, int s, uint32_t &bits) {
-    if (V == 0) { bits = 0u; return true; }
-    const uint32_t sign = V < 0 ? 0x8000u : 0u;
-    const unsigned long long mag = V < 0 ? 0ull - (unsigned long long)V : (unsigned long long)V;
-    const int nb = 64 - __clzll((long long)mag);
-    if (nb > 53) return round_int_to_bf16(V, s, bits);     // a float64 rounding first
-    const int E = nb - 1 + s;                               // value in [2^E, 2^(E+1))
-    if (E < -126 || E > 127) return false;
-    uint32_t m8;
-    if (nb > 8) {
-        const int sh = nb - 8;
-        const unsigned long long r = mag + ((1ull << (sh - 1)) - 1ull) + ((mag >> sh) & 1ull);
-        m8 = (uint32_t)(r >> sh);                           // 128 .. 256
-    } else {
-        m8 = (uint32_t)mag << (8 - nb);                     // exact
-    }
-    const uint32_t b = (uint32_t)(E + 126) * 128u + m8;    // 256 carries into the exponent
-    if (b >= 0x7f80u) return false;                         // rounded past the largest finite
-    bits = sign | b;
-    return true;
-}
-
 // Output bits (KBN tier, bf16) of one output: exact sum T in grain 2^G, bias
-// bm * 2^be (bm = 0: none; bad: inf/NaN) of column j.
-__device__ __forceinline__ uint32_t kbn_bits(long long T, int G, int bm, int be, bool bad,
-                                             const unsigned short *bias, int64_t j) {
+// bm * 2^be (bm = 0: none; bad: inf/NaN) of column j.  Every case.
+__device__ __noinline__ uint32_t kbn_bits_general(long long T, int G, int bm, int be, bool bad,
+                                                  const unsigned short *bias, int64_t j) {
     long long Tv = T;
     int gs = G;
     bool fused = !bad;
@@ -1226,8 +1215,25 @@ __device__ __forceinline__ uint32_t kbn_bits(long long T, int G, int bm, int be,
         }
     }
     uint32_t bits = 0u;
-    if (!(fused && round_int_to_bf16_fast(Tv, gs, bits))) bits = out_bits_f64(T, G, bias, j);
+    if (!(fused && round_int_to_bf16(Tv, gs, bits))) bits = out_bits_f64(T, G, bias, j);
     return bits;
+}
+
+// The same bits, with the common case inline: |T| < 2^53 (its float64 value
+// is exact), no bias or one at or above the grain, and a sum below 2^53 that
+// rounds to a bf16 normal number; the rest (rarely taken) in the general
+// function, out of line.
+__device__ __forceinline__ uint32_t kbn_bits(long long T, int G, int bm, int be, bool bad,
+                                             const unsigned short *bias, int64_t j) {
+    bool fast = !bad && below_pow2(T, 53);
+    long long Tv = T;
+    if (bm != 0) {
+        fast = fast && be >= G && be - G <= 54;             // T + the bias term stays below 2^63
+        Tv = T + shl64(bm, (uint32_t)(be - G) & 63u);
+    }
+    uint32_t bits = 0u;
+    if (fast && below_pow2(Tv, 53) && round_small_int_to_bf16(Tv, G, bits)) return bits;
+    return kbn_bits_general(T, G, bm, be, bad, bias, j);
 }
 
 template <int MODE>
@@ -1235,15 +1241,18 @@ __global__ void __launch_bounds__(256)
 exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int *__restrict__ GA,
                       const int *__restrict__ GB, const unsigned short *__restrict__ bias, void *out,
                       int64_t rows, int64_t cols, int vec_out) {
-    __shared__ int s_gw[kFinCols], s_bm[kFinCols], s_be[kFinCols], s_bad[kFinCols];
-    __shared__ uint32_t s_hb[kFinCols];
+    // the block's columns: grain of the column line, bias significand and
+    // exponent, and the bias bits with an inf/NaN flag in bit 16
+    __shared__ int4 s_col[kFinCols];
     wait_prior_grid();
     allow_next_grid();
     const int64_t plane = rows * cols, n_t = (int64_t)pieces * plane;
-    const int64_t rblocks = (rows + 255) / 256, cgroups = (cols + kFinCols - 1) / kFinCols;
-    for (int64_t b = blockIdx.x; b < rblocks * cgroups; b += gridDim.x) {
-        const int64_t i = (b % rblocks) * 256 + threadIdx.x, j0 = (b / rblocks) * kFinCols;
-        __syncthreads();                                    // the previous columns' data is read
+    const int64_t cgroups = (cols + kFinCols - 1) / kFinCols;
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    const int gx = (i < rows && CHK(i, 1, rows)) ? __ldg(&GA[i]) : 0;
+    for (int64_t cgi = blockIdx.y; cgi < cgroups; cgi += gridDim.y) {
+        const int64_t j0 = cgi * kFinCols;
+        if (cgi != (int64_t)blockIdx.y) __syncthreads();   // the previous columns' data is read
         if (threadIdx.x < kFinCols) {
             const int64_t j = j0 + threadIdx.x;
             int gw = 0, bm = 0, be = 0;
@@ -1253,13 +1262,12 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
                 gw = __ldg(&GB[j]);
                 if (bias != nullptr) { hb = ld_bits(bias, j); decode(hb, bm, be, bad); }
             }
-            s_gw[threadIdx.x] = gw; s_bm[threadIdx.x] = bm; s_be[threadIdx.x] = be;
-            s_bad[threadIdx.x] = bad ? 1 : 0; s_hb[threadIdx.x] = hb;
+            s_col[threadIdx.x] = make_int4(gw, bm, be, (int)(hb | (bad ? 0x10000u : 0u)));
         }
         __syncthreads();
         if (i >= rows) continue;
-        const int gx = CHK(i, 1, rows) ? __ldg(&GA[i]) : 0;
         const int ncol = (int)min((int64_t)kFinCols, cols - j0);
+        const long long *tp = Tout + j0 * rows + i;
         // the pieces' partial sums: in 64 bits with an overflow bit per output
         // (bf16 outputs; an overflowing output adds its pieces again in 128
         // bits), in 128 bits for the other modes
@@ -1270,8 +1278,8 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             long long t[kFinCols];
 #pragma unroll
             for (int e = 0; e < kFinCols; ++e) {
-                const int64_t at = k * plane + (j0 + e) * rows + i;
-                t[e] = (e < ncol && CHK(at, 1, n_t)) ? __ldg(&Tout[at]) : 0ll;
+                const int64_t off = k * plane + e * rows;
+                t[e] = (e < ncol && CHK(j0 * rows + i + off, 1, n_t)) ? __ldg(tp + off) : 0ll;
             }
 #pragma unroll
             for (int e = 0; e < kFinCols; ++e) {
@@ -1298,10 +1306,11 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
         for (int e = 0; e < kFinCols; ++e) {
             if (e >= ncol || ((deferred >> e) & 1u)) continue;
             const int64_t j = j0 + e;
-            const int G = gx + s_gw[e];
-            const int bm = s_bm[e], be = s_be[e];
-            const bool bad = s_bad[e] != 0;
-            const uint32_t hb = s_hb[e];
+            const int4 c = s_col[e];
+            const int G = gx + c.x;
+            const int bm = c.y, be = c.z;
+            const bool bad = (c.w >> 16) != 0;
+            const uint32_t hb = (uint32_t)c.w & 0xffffu;
             uint32_t bits = 0u;
             if constexpr (MODE == kFinBf16) {
                 if (!((ovf >> e) & 1u)) {
@@ -1372,10 +1381,12 @@ cudaError_t launch_tc_main(const CUtensorMap &ma, const CUtensorMap &mb, const T
         if (err != cudaSuccess) return err;
     }
     {
-        const int64_t want = ((a.rows + 255) / 256) * ((a.cols + kFinCols - 1) / kFinCols), cap = 152 * 32;
-        const unsigned grid = (unsigned)(want < cap ? want : cap);
+        // a block per 256 rows and group of 8 columns (groups past 65535 taken
+        // in turn by the blocks of the same rows)
+        const int64_t cgroups = (a.cols + kFinCols - 1) / kFinCols;
+        const dim3 grid((unsigned)((a.rows + 255) / 256), (unsigned)(cgroups < 65535 ? cgroups : 65535));
         const int vec_out = ((reinterpret_cast<uintptr_t>(a.out) & 15u) == 0 && (a.cols % 8) == 0) ? 1 : 0;
-        err = launch_k(exact_finalize_kernel<MODE>, dim3(grid), dim3(256), 0, s, 1,
+        err = launch_k(exact_finalize_kernel<MODE>, grid, dim3(256), 0, s, 1,
                        (const long long *)a.Tout, a.splits, a.GA, a.GB, a.bias, a.out, a.rows, a.cols,
                        vec_out);
         count_launch();

@@ -266,3 +266,62 @@ def test_outer_sum_wraps_within_a_piece():
             W[256 * q:256 * q + 256, j] = w
     _, fixups = check("fwd", bf16(X), bf16(W), None, M, K, N)
     assert fixups > 0
+
+
+def _tie_operands(rng, exps, ks, cs, hs, K, main_at, tie_at, tiny_at, sigma):
+    """Rows of m * 2^E (m of 8 bits, random sign) at reduction index main_at
+    (against W = 1), 2^(E-8+sigma) at tie_at (against c * 2^-sigma: c times
+    half a bf16 ulp of the main value) and +-2^(E-8-k) at tiny_at (against h),
+    for every E in exps and k in ks (k None: no tiny entry), 6 rows each, the
+    first with the largest m; columns for every (c, h) pair, three times.
+    The tie entries make the exact sums land on bf16 midpoints or near them,
+    the tiny ones decide them or vanish in the float64 rounding."""
+    rows = [(E, k, r) for E in exps for k in ks for r in range(6)]
+    cols = [(c, h) for c in cs for h in hs] * 3
+    M, N = len(rows), len(cols)
+    X = np.zeros((M, K))
+    W = np.zeros((K, N))
+    for i, (E, k, r) in enumerate(rows):
+        a = 127 if r == 0 else rng.integers(0, 128)              # 127: a midpoint rounds up a binade
+        a &= -(1 << max(0, -126 - E))                            # bf16 subnormals hold fewer bits
+        X[i, main_at] = rng.choice([-1.0, 1.0]) * np.ldexp(1.0 + a / 128.0, E)
+        X[i, tie_at] = np.ldexp(1.0, E - 8 + sigma)
+        if k is not None:
+            X[i, tiny_at] = rng.choice([-1.0, 1.0]) * np.ldexp(1.0, E - 8 - k)
+    for j, (c, h) in enumerate(cols):
+        W[main_at, j] = 1.0
+        W[tie_at, j] = np.ldexp(c, -sigma)
+        W[tiny_at, j] = h
+    return X, W, M, N
+
+
+def test_output_rounding_midpoints_and_double_rounding():
+    """The finalize rounds the exact sum on the conversion units (float32
+    truncation with a sticky bit, then one rounding to bf16): exact sums on
+    bf16 midpoints, just off them, and wider than 53 bits (where the float64
+    rounding of the literal algorithm comes first and may leave a midpoint),
+    in four chunks taken as four pieces, with biases that join the integer
+    sum, tie with it, or stay too far from its grain."""
+    rng = np.random.default_rng(21)
+    c = [0.0, 1.0, -1.0, 3.0, -3.0, 1.5, -1.5, 0.5]
+    X, W, M, N = _tie_operands(rng, exps=[0, 5, -9, 30, -40], ks=[None, 12, 37, 45, 50], cs=c,
+                               hs=[0.0, 1.0, -1.0], K=1024, main_at=0, tie_at=300, tiny_at=900,
+                               sigma=0)
+    b = np.array([[0.0, 2.0 ** -8, -(2.0 ** -8), 3 * 2.0 ** -9, 2.0 ** -100, 1.0, -1.0][j % 7]
+                  for j in range(N)])
+    repairs, fixups = check("fwd", bf16(X), bf16(W), bf16(b), M, 1024, N)
+    assert repairs == 0 and fixups == 0
+    check("fwd", bf16(X), bf16(W), None, M, 1024, N)
+
+
+def test_output_rounding_at_the_ends_of_the_range():
+    """Midpoints at the top of the bf16 range (rounding to inf goes the float64
+    way), at the smallest normal exponent, and below it (subnormal results)."""
+    rng = np.random.default_rng(22)
+    c = [0.0, 1.0, -1.0, 3.0, 1.5]
+    X, W, M, N = _tie_operands(rng, exps=[127, 126, -125, -126, -127, -130], ks=[None], cs=c,
+                               hs=[0.0], K=40, main_at=0, tie_at=1, tiny_at=2, sigma=6)
+    check("fwd", bf16(X), bf16(W), None, M, 40, N)
+    b = np.array([[0.0, 1.5 * 2.0 ** 126, -(2.0 ** 127), 2.0 ** -126, -(2.0 ** -133)][j % 5]
+                  for j in range(N)])
+    check("fwd", bf16(X), bf16(W), bf16(b), M, 40, N)
