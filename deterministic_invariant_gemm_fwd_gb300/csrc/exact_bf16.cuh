@@ -114,15 +114,17 @@ __device__ __forceinline__ int bit_count(unsigned long long v) { return 64 - __c
 
 // ---- fix-up pass: outputs the fast kernels left undone ----------------------
 //
-// One block per listed output recomputes it from the bf16 operands.  Its eight
-// warps take eight chunks at a time: the 32 lanes of a warp load the chunk's
+// One block per listed output recomputes it from the bf16 operands.  Its 32
+// warps take 32 chunks at a time (a 256-deep chunk of the literal loop below
+// is a chain of 256 dependent steps, so chunks in separate warps rather than
+// in turn): the 32 lanes of a warp load the chunk's
 // 256 operand pairs at once and reduce the exact chunk sum in 128-bit
 // integers; the chunk value is that sum rounded once to float64 (see the
 // argument in the loop).  Chunks with inf or NaN operands, or of extreme
 // width, run the float64 KBN loop on the warp's lane 0 from shared memory.
 // Thread 0 then combines the chunk values in order with the full KBN step, and
 // finally adds the bias and rounds.  Literal-algorithm bits throughout.
-constexpr int kFixWarps = 8;
+constexpr int kFixWarps = 32;
 constexpr int kFixBlocks = 1024;
 
 // Status word of the fix-up kernel in the bounds-checked build (one per
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(kFixWarps * 32)
 exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
                    int64_t LpA, int64_t LpB, const unsigned int *__restrict__ work_count,
                    const unsigned int *__restrict__ work_list) {
-    __shared__ double xs[kFixWarps][kChunk], ws[kFixWarps][kChunk];
+    __shared__ unsigned short xs[kFixWarps][kChunk], ws[kFixWarps][kChunk];   // bf16 bits
     __shared__ double Pq[kFixWarps];
     wait_prior_grid();
     allow_next_grid();
@@ -196,15 +198,15 @@ exact_fixup_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__res
                 } else {                                   // inf/NaN or extreme widths: literal loop
 #pragma unroll
                     for (int t = 0; t < kChunk / 32; ++t) {
-                        xs[warp][lane + 32 * t] = widen_bf16(hx[t]);
-                        ws[warp][lane + 32 * t] = widen_bf16(hw[t]);
+                        xs[warp][lane + 32 * t] = (unsigned short)hx[t];
+                        ws[warp][lane + 32 * t] = (unsigned short)hw[t];
                     }
                     __syncwarp();
                     double s_ = 0.0, c_ = 0.0;
                     if (lane == 0) {
                         const int len = (int)(qend - q0);
                         for (int k = 0; k < len; ++k) {
-                            const double x = xs[warp][k], w = ws[warp][k];
+                            const double x = widen_bf16(xs[warp][k]), w = widen_bf16(ws[warp][k]);
                             kbn_product_step(s_, c_, x, w,
                                              ((uint32_t)__double2hiint(x) & 0x7ff00000u) +
                                              ((uint32_t)__double2hiint(w) & 0x7ff00000u));

@@ -62,6 +62,7 @@ constexpr int kBK = 64;           // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kUMMA_K = 16;       // K of one tcgen05.mma kind::f16
 constexpr int kStages = 4;
 constexpr int kThreads = 192;     // 6 warps
+constexpr int kMaxSplits = 8;     // dW token split: pieces per cluster, at most
 constexpr int kEpiWarps = 4;
 constexpr uint32_t kABytes = kBM * kBK * 2;           // 16 KiB
 constexpr uint32_t kMNBlockBytes = 64 * kBK * 2;      // one 64-wide MN block of an MN-major tile
@@ -519,13 +520,20 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         if (grow >= p.rows || gcol >= p.cols) continue;
         if (!CHK(grow * p.cols + gcol, 4, (int64_t)p.rows * p.cols)) continue;
         const uint32_t off = part_addr + (uint32_t)(rr * L::kPartialPitch + cc) * 4u;
-        float4 a = ld_cluster_f4(off, 0);
-        for (int q = 1; q < p.splits; ++q) {
-            const float4 b = ld_cluster_f4(off, (uint32_t)q);
-            a.x = __fadd_rn(a.x, b.x);
-            a.y = __fadd_rn(a.y, b.y);
-            a.z = __fadd_rn(a.z, b.z);
-            a.w = __fadd_rn(a.w, b.w);
+        // all the partials' loads are issued before the first addition (the
+        // remote loads' latency would otherwise be paid once per piece)
+        float4 b[kMaxSplits];
+#pragma unroll
+        for (int q = 0; q < kMaxSplits; ++q)
+            if (q < p.splits) b[q] = ld_cluster_f4(off, (uint32_t)q);
+        float4 a = b[0];
+#pragma unroll
+        for (int q = 1; q < kMaxSplits; ++q) {
+            if (q >= p.splits) break;
+            a.x = __fadd_rn(a.x, b[q].x);
+            a.y = __fadd_rn(a.y, b[q].y);
+            a.z = __fadd_rn(a.z, b[q].z);
+            a.w = __fadd_rn(a.w, b[q].w);
         }
         if (OUT_F32) {
             *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + grow * p.cols + gcol) = a;
@@ -643,7 +651,7 @@ int choose_bn(int64_t cols, int pass) {
 // bits do not depend on the device a run lands on).
 int choose_splits(int64_t tiles) {
     int s = 1;
-    while (s < 8 && tiles * (2 * s) <= 152) s *= 2;
+    while (s < kMaxSplits && tiles * (2 * s) <= 152) s *= 2;
     return s;
 }
 
