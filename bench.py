@@ -667,24 +667,49 @@ def main():
                                for t in tiers for n, shape in (("Y", (M, N)), ("dX", (M, K)), ("dW", (K, N)))})
         h2d = sum(v.numel() * 2 for d in pinned_in for v in d.values())
         d2h = sum(v.numel() * 2 for d in pinned_out for v in d.values())
-        with torch.cuda.stream(stream):
-            barrier()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(args.steps):
-                for d, pi in zip(wl.layers, pinned_in):
+        # Copies overlap the GEMMs, layer by layer: a layer's inputs go up on
+        # one copy stream while the previous layer computes, its outputs come
+        # down on another while the next one computes.  Every step still moves
+        # all of its inputs up and all of its outputs down inside the timed
+        # region; events keep a layer's buffers from being overwritten while
+        # they are in use (inputs until its GEMMs are done, outputs until
+        # they are read back).
+        up_s, down_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        nl = len(wl.layers)
+        up_done = [torch.cuda.Event() for _ in range(nl)]
+        comp_done = [torch.cuda.Event() for _ in range(nl)]
+        down_done = [torch.cuda.Event() for _ in range(nl)]
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        up_s.wait_event(e0)
+        down_s.wait_event(e0)
+        for _ in range(args.steps):
+            for li, (d, pi, po) in enumerate(zip(wl.layers, pinned_in, pinned_out)):
+                with torch.cuda.stream(up_s):
+                    up_s.wait_event(comp_done[li])             # last step's GEMMs have read them
                     for k in ("X", "W", "b", "dY"):
                         d[k].view(torch.int16).copy_(pi[k], non_blocking=True)
+                    up_done[li].record(up_s)
+                stream.wait_event(up_done[li])
+                stream.wait_event(down_done[li])               # last step's outputs are read back
                 for t in tiers:
-                    wl.launch(t, stream)
-                for d, po in zip(wl.layers, pinned_out):
+                    for p_ in PASSES:
+                        if wl.only is None or f"{t}:{p_}:{d['K']}x{d['N']}" in wl.only:
+                            wl.launch_one(t, p_, d["K"], d["N"], stream)
+                comp_done[li].record(stream)
+                with torch.cuda.stream(down_s):
+                    down_s.wait_event(comp_done[li])
                     for t in tiers:
                         for n in ("Y", "dX", "dW"):
                             po[f"{n}_{t}"].copy_(d[f"{n}_{t}"].view(torch.int16), non_blocking=True)
-            e1.record(stream)
-            stream.synchronize()
-            e2e_ms = e0.elapsed_time(e1) / args.steps
+                    down_done[li].record(down_s)
+        stream.wait_event(down_done[nl - 1])
+        stream.wait_event(up_done[nl - 1])
+        e1.record(stream)
+        stream.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
         e2e_ms = max_over_ranks(e2e_ms, pg, device)
         e2e = {"value": _r(whole_job_gflops(flops, world, e2e_ms)), "unit": "GFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": _r(e2e_ms)}

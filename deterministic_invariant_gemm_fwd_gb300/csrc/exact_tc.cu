@@ -1092,6 +1092,40 @@ __device__ __forceinline__ __int128 round_i128_to_53_bits(__int128 I) {
     return neg ? -r : r;
 }
 
+// One listed (output, chunk): its operand bits as loaded by the lanes.
+struct RepairItem {
+    int64_t o, q;
+    int4 sa, sb;
+    uint32_t hx[kChunk / 32], hw[kChunk / 32];
+    bool valid;
+};
+
+// Loads list entry e (every lane: 8 of the chunk's 256 operand pairs).
+__device__ __forceinline__ void repair_load(const IArgs &p, const int4 *__restrict__ SA,
+                                            const int4 *__restrict__ SB, int64_t LpA, int64_t LpB,
+                                            const uint2 *__restrict__ chunk_list, unsigned int chunk_cap,
+                                            int64_t e, int lane, int64_t nq, int64_t n_a, int64_t n_b,
+                                            RepairItem &it) {
+    it.valid = CHK(e, 1, chunk_cap);
+    if (!it.valid) return;
+    const uint2 en = chunk_list[e];
+    it.o = en.x;
+    it.q = en.y;
+    const int64_t i = it.o / p.cols, j = it.o % p.cols;
+    it.valid = CHK(it.q * LpA + i, 1, nq * LpA) && CHK(it.q * LpB + j, 1, nq * LpB);
+    if (!it.valid) return;
+    it.sa = SA[it.q * LpA + i];
+    it.sb = SB[it.q * LpB + j];
+    const int64_t q0 = it.q * kChunk, qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
+#pragma unroll
+    for (int t = 0; t < kChunk / 32; ++t) {
+        const int64_t r = q0 + lane + 32 * t;
+        const bool in = r < qend && CHK(i * p.a_si + r * p.a_sr, 1, n_a) && CHK(r * p.b_sr + j * p.b_sj, 1, n_b);
+        it.hx[t] = in ? ld_bits(p.A, i * p.a_si + r * p.a_sr) : 0u;
+        it.hw[t] = in ? ld_bits(p.B, r * p.b_sr + j * p.b_sj) : 0u;
+    }
+}
+
 template <bool SUPER>
 __global__ void __launch_bounds__(256)
 exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4 *__restrict__ SB,
@@ -1109,57 +1143,60 @@ exact_chunk_repair_kernel(const IArgs p, const int4 *__restrict__ SA, const int4
     const int64_t nq = (p.R + kChunk - 1) / kChunk;
     const int64_t n_a = (p.rows > 0 && p.R > 0) ? (p.rows - 1) * p.a_si + (p.R - 1) * p.a_sr + 1 : 0;
     const int64_t n_b = (p.cols > 0 && p.R > 0) ? (p.R - 1) * p.b_sr + (p.cols - 1) * p.b_sj + 1 : 0;
+    // the next entry's loads are issued before this one is reduced
+    RepairItem cur, nxt;
+    cur.valid = false;
+    nxt.valid = false;
+    if (gw < count) repair_load(p, SA, SB, LpA, LpB, chunk_list, chunk_cap, gw, lane, nq, n_a, n_b, cur);
     for (int64_t e = gw; e < count; e += nw) {
-        if (!CHK(e, 1, chunk_cap)) break;
-        const uint2 en = chunk_list[e];
-        const int64_t o = en.x, q = en.y;
-        const int64_t i = o / p.cols, j = o % p.cols;
-        if (!CHK(q * LpA + i, 1, nq * LpA) || !CHK(q * LpB + j, 1, nq * LpB)) continue;
-        const int4 sa = SA[q * LpA + i], sb = SB[q * LpB + j];
-        const int64_t q0 = q * kChunk, qend = (p.R - q0 > kChunk) ? q0 + kChunk : p.R;
-        __int128 I = 0;
+        if (e + nw < count) repair_load(p, SA, SB, LpA, LpB, chunk_list, chunk_cap, e + nw, lane, nq, n_a, n_b, nxt);
+        if (cur.valid) {
+            const int64_t o = cur.o, q = cur.q;
+            const int64_t i = o / p.cols, j = o % p.cols;
+            const int4 sa = cur.sa, sb = cur.sb;
+            __int128 I = 0;
 #pragma unroll
-        for (int t = 0; t < kChunk / 32; ++t) {
-            const int64_t r = q0 + lane + 32 * t;
-            if (r >= qend) continue;
-            if (!CHK(i * p.a_si + r * p.a_sr, 1, n_a) || !CHK(r * p.b_sr + j * p.b_sj, 1, n_b)) continue;
-            int mx, ex, mw, ew;
-            bool bx_, bw_;
-            decode(ld_bits(p.A, i * p.a_si + r * p.a_sr), mx, ex, bx_);
-            decode(ld_bits(p.B, r * p.b_sr + j * p.b_sj), mw, ew, bw_);
-            if (mx == 0 || mw == 0) continue;
-            const long long X = line_int(mx, ex, sa.x);                       // |X| < 2^62
-            const long long W = line_int(mw, ew, sb.x);
-            I += (__int128)X * W;                                             // |X W| < 2^90
-        }
+            for (int t = 0; t < kChunk / 32; ++t) {
+                int mx, ex, mw, ew;
+                bool bx_, bw_;
+                decode(cur.hx[t], mx, ex, bx_);
+                decode(cur.hw[t], mw, ew, bw_);
+                if (mx == 0 || mw == 0) continue;
+                const long long X = line_int(mx, ex, sa.x);                       // |X| < 2^62
+                const long long W = line_int(mw, ew, sb.x);
+                I += (__int128)X * W;                                             // |X W| < 2^90
+            }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const long long lo = __shfl_xor_sync(0xffffffffu, (long long)(unsigned long long)I, off);
-            const long long hi = __shfl_xor_sync(0xffffffffu, (long long)(I >> 64), off);
-            I += ((__int128)hi << 64) | (__int128)(unsigned long long)lo;
+            for (int off = 16; off > 0; off >>= 1) {
+                const long long lo = __shfl_xor_sync(0xffffffffu, (long long)(unsigned long long)I, off);
+                const long long hi = __shfl_xor_sync(0xffffffffu, (long long)(I >> 64), off);
+                I += ((__int128)hi << 64) | (__int128)(unsigned long long)lo;
+            }
+            if (lane == 0) {
+                const __int128 J = SUPER ? I : round_i128_to_53_bits(I);
+                const int sh = (CHK(i, 1, LpA) && CHK(j, 1, LpB)) ? (sa.x - __ldg(&GA[i])) + (sb.x - __ldg(&GB[j])) : -1;
+                bool ok = sh >= 0 && sh < 62;
+                __int128 v = 0;
+                if (ok) {
+                    v = (__int128)((unsigned __int128)J << sh);
+                    ok = (v >> sh) == J && v >= -((__int128)1 << 61) && v < ((__int128)1 << 61);
+                }
+                if (ok && !CHK((q / cps) * p.rows * p.cols + j * p.rows + i, 1, n_tout)) ok = false;
+                if (ok) {
+                    long long *slot = Tout + (q / cps) * p.rows * p.cols + j * p.rows + i;
+                    const long long add = (long long)v;
+                    const long long old = (long long)atomicAdd(reinterpret_cast<unsigned long long *>(slot),
+                                                               (unsigned long long)add);
+                    const long long sum = (long long)((unsigned long long)old + (unsigned long long)add);
+                    ok = !((old >= 0) == (add >= 0) && (sum >= 0) != (old >= 0));
+                }
+                if (!ok) {
+                    const unsigned int at = atomicAdd(work_count, 1u);
+                    if (CHK(at, 1, work_cap)) work_list[at] = (unsigned int)o;
+                }
+            }
         }
-        if (lane != 0) continue;
-        const __int128 J = SUPER ? I : round_i128_to_53_bits(I);
-        const int sh = (CHK(i, 1, LpA) && CHK(j, 1, LpB)) ? (sa.x - __ldg(&GA[i])) + (sb.x - __ldg(&GB[j])) : -1;
-        bool ok = sh >= 0 && sh < 62;
-        __int128 v = 0;
-        if (ok) {
-            v = (__int128)((unsigned __int128)J << sh);
-            ok = (v >> sh) == J && v >= -((__int128)1 << 61) && v < ((__int128)1 << 61);
-        }
-        if (ok && !CHK((q / cps) * p.rows * p.cols + j * p.rows + i, 1, n_tout)) ok = false;
-        if (ok) {
-            long long *slot = Tout + (q / cps) * p.rows * p.cols + j * p.rows + i;
-            const long long add = (long long)v;
-            const long long old = (long long)atomicAdd(reinterpret_cast<unsigned long long *>(slot),
-                                                       (unsigned long long)add);
-            const long long sum = (long long)((unsigned long long)old + (unsigned long long)add);
-            ok = !((old >= 0) == (add >= 0) && (sum >= 0) != (old >= 0));
-        }
-        if (!ok) {
-            const unsigned int at = atomicAdd(work_count, 1u);
-            if (CHK(at, 1, work_cap)) work_list[at] = (unsigned int)o;
-        }
+        cur = nxt;
     }
 }
 
