@@ -545,25 +545,31 @@ __device__ __forceinline__ long long round_to_53_bits(long long I) {
     return neg ? -(long long)r : (long long)r;
 }
 
-// bf16 bits of RN_bf16(V * 2^s) (nearest even), |V| < 2^53, on the conversion
-// units: V truncated to float32 with the lowest bit set when any bit was
-// dropped (rounding to odd at 24 bits), scaled by 2^s in the exponent field,
-// and rounded to nearest even to bf16.  Rounding to odd at p + 2 or more bits
-// and then to nearest at p bits gives the one rounding to nearest at p bits
-// (Boldo and Melquiond, "Emulation of FMA and correctly rounded sums: proved
-// algorithms using rounding to odd", IEEE Trans. Computers 57(4), 2008); here
-// p = 8.  False when the value or the result is not a bf16 normal number (the
-// caller then takes the float64 route).
+// bf16 bits of RN_bf16(V * 2^s) (nearest even), |V| < 2^53: V truncated to
+// float32 (one conversion), the lowest bit set when the truncation dropped a
+// set bit (the low nb - 24 bits of |V|, nb its bit length, tested on the
+// integer) - rounding to odd at 24 bits -, scaled by 2^s in the exponent
+// field, and rounded to nearest even to bf16.  Rounding to odd at p + 2 or
+// more bits and then to nearest at p bits gives the one rounding to nearest
+// at p bits (Boldo and Melquiond, "Emulation of FMA and correctly rounded
+// sums: proved algorithms using rounding to odd", IEEE Trans. Computers
+// 57(4), 2008); here p = 8.  (The 64-bit conversion runs on the float64 pipe,
+// hence one, not a conversion back.)  False when the value or the result is
+// not a bf16 normal number (the caller then takes the float64 route).
 __device__ __forceinline__ bool round_small_int_to_bf16(long long V, int s, uint32_t &bits) {
     float f;
-    long long back;
     asm("cvt.rz.f32.s64 %0, %1;" : "=f"(f) : "l"(V));
-    asm("cvt.rzi.s64.f32 %0, %1;" : "=l"(back) : "f"(f));
     uint32_t fb = __float_as_uint(f);
     if (fb == 0u) { bits = 0u; return true; }               // V == 0
-    const int ef = (int)((fb >> 23) & 0xffu) + s;           // biased exponent of the result
+    const int e = (int)((fb >> 23) & 0xffu);                // 127 + nb - 1 (truncation keeps it)
+    const int ef = e + s;                                   // biased exponent of the result
     if (ef < 1 || ef > 254) return false;
-    fb = (fb + ((uint32_t)s << 23)) | (back != V ? 1u : 0u);
+    const int drop = e - 150;                               // nb - 24 bits truncated
+    if (drop > 0) {
+        const unsigned long long mag = V < 0 ? 0ull - (unsigned long long)V : (unsigned long long)V;
+        if ((mag << (64 - drop)) != 0ull) fb |= 1u;
+    }
+    fb += (uint32_t)s << 23;
     unsigned short h;
     asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(__uint_as_float(fb)));
     if ((h & 0x7fffu) >= 0x7f80u) return false;             // rounded past the largest finite
@@ -1274,7 +1280,7 @@ __device__ __forceinline__ uint32_t kbn_bits(long long T, int G, int bm, int be,
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)                  // 4 blocks per SM: at most 64 registers
 exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int *__restrict__ GA,
                       const int *__restrict__ GB, const unsigned short *__restrict__ bias, void *out,
                       int64_t rows, int64_t cols, int vec_out) {
