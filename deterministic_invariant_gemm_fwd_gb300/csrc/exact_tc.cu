@@ -415,7 +415,8 @@ __device__ __forceinline__ void prep_block(const PrepArgs &pa, int bx, int by) {
         unsigned int mx = 0u;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const int X = (use && m[e] != 0) ? m[e] * (1 << (ex[e] - base)) : 0;   // |X| < 2^31
+            // (m = 0 gives 0 whatever its exponent: the shift is masked into range)
+            const int X = use ? m[e] * (1 << ((ex[e] - base) & 31)) : 0;   // |X| < 2^31
             const unsigned int a = (unsigned int)abs(X);
             sum += a;
             mx = max(mx, a);
@@ -448,7 +449,7 @@ __device__ __forceinline__ void prep_block(const PrepArgs &pa, int bx, int by) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int sh = ex[e] - base;
-            const int v = (use && m[e] != 0) ? m[e] * (1 << (sh & 7)) : 0;    // |v| < 2^15
+            const int v = use ? m[e] * (1 << (sh & 7)) : 0;             // |v| < 2^15; m = 0: 0
             const int lo = (int)(int8_t)v;                         // v mod 256 in [-128, 127]
             const unsigned long long w = (unsigned long long)small_int_bf16_pair((v - lo) >> 8, lo)
                                          << (16 * ((sh >> 3) & 3));            // v = 0: all zero
