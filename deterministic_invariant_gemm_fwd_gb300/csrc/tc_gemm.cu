@@ -454,7 +454,9 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     bar.tempty0 = bar.tfull0 + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + (2 * kStages + 4) * 8);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    constexpr uint32_t kTmemCols = BN;                     // one accumulator: 128 or 256 columns
+    // one accumulator of BN columns, the allocation rounded up to a power of two
+    constexpr uint32_t kTmemCols = BN <= 128 ? 128u : 256u;
+    static_assert(BN <= 256, "one accumulator per CTA");
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t tmem_base = setup_cta<BN>(smem, bar, &map_a, &map_b, tmem_slot, abort_flag, kTmemCols);
@@ -626,26 +628,6 @@ cudaError_t launch_split(const CUtensorMap &ma, const CUtensorMap &mb, const TcA
                     (size_t)smem, stream, (unsigned)a.splits, ma, mb, a);
 }
 
-// Output tile width from the column count and the pass only (never the row
-// count, so a row's tiles, and its bits, do not depend on the batch): 128 for
-// at most 128 columns; otherwise 256, or 192 when that fills the SMs better
-// for a reference batch of 8192 rows on 152 SMs (768 columns: 256 tiles of
-// 192 run in two fuller waves than 192 tiles of 256).  dW keeps 256: its
-// token split is sized for that.
-double wave_fill(int64_t tiles) {
-    const int64_t waves = (tiles + 151) / 152;
-    return (double)tiles / (double)(waves * 152);
-}
-
-int choose_bn(int64_t cols, int pass) {
-    if (cols <= 128) return 128;
-    if (pass == CARBON_PASS_DW) return 256;
-    const int64_t ref_tiles_m = 8192 / kBM;
-    const double f256 = wave_fill(ref_tiles_m * ((cols + 255) / 256));
-    const double f192 = wave_fill(ref_tiles_m * ((cols + 191) / 192));
-    return f192 > f256 ? 192 : 256;
-}
-
 // dW split count from the output tile count only: the largest s in
 // {1, 2, 4, 8} with tiles * s <= 152 (GB300's SM count, fixed here so the
 // bits do not depend on the device a run lands on).
@@ -653,6 +635,42 @@ int choose_splits(int64_t tiles) {
     int s = 1;
     while (s < kMaxSplits && tiles * (2 * s) <= 152) s *= 2;
     return s;
+}
+
+// Output tile width.  Forward and dX: from the column count and the pass only
+// (never the row count, so a row's tiles, and its bits, do not depend on the
+// batch): 128 for at most 128 columns; otherwise 256, or 192 when that fills
+// the SMs better for a reference batch of 8192 rows on 152 SMs (768 columns:
+// 256 tiles of 192 run in two fuller waves than 192 tiles of 256).  dW (rows
+// and columns both weight dimensions): 256, or 192 when that gives each CTA
+// less work for a reference reduction of 8192 tokens (work per CTA = width x
+// k-blocks per piece x waves), e.g. 768 x 2304: 72 tiles of 192 in two pieces
+// fill 144 SMs where 54 tiles of 256 fill 108.  The width does not change a
+// dW output's summation: its pieces and their k-block order depend on the
+// split count alone, and 192 is chosen only where that count is the same.
+double wave_fill(int64_t tiles) {
+    const int64_t waves = (tiles + 151) / 152;
+    return (double)tiles / (double)(waves * 152);
+}
+
+int choose_bn(int64_t rows, int64_t cols, int pass) {
+    if (cols <= 128) return 128;
+    if (pass == CARBON_PASS_DW) {
+        const int64_t tiles_m = (rows + kBM - 1) / kBM, ref_kb = 8192 / kBK;
+        auto work = [&](int64_t bn) {
+            const int64_t tiles = tiles_m * ((cols + bn - 1) / bn);
+            const int s = choose_splits(tiles);
+            const int64_t waves = s > 1 ? 1 : (tiles + 151) / 152;
+            return bn * ((ref_kb + s - 1) / s) * waves;
+        };
+        const int64_t tiles192 = tiles_m * ((cols + 191) / 192), tiles256 = tiles_m * ((cols + 255) / 256);
+        const bool same_split = choose_splits(tiles192) == choose_splits(tiles256);
+        return (same_split && work(192) < work(256)) ? 192 : 256;
+    }
+    const int64_t ref_tiles_m = 8192 / kBM;
+    const double f256 = wave_fill(ref_tiles_m * ((cols + 255) / 256));
+    const double f192 = wave_fill(ref_tiles_m * ((cols + 191) / 192));
+    return f192 > f256 ? 192 : 256;
 }
 
 }  // namespace
@@ -684,7 +702,7 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
 
     cudaError_t err = cudaSuccess;
 
-    const int bn = choose_bn(p.cols, p.pass);
+    const int bn = choose_bn(p.rows, p.cols, p.pass);
     CUtensorMap ma, mb, mo;
     bool ok;
     switch (p.pass) {
@@ -728,6 +746,10 @@ carbon_status_t tc_launch(const Problem &p, bool out_f32, cudaStream_t stream) {
             err = ot == OT_F32 ? launch_split<128, OT_F32>(ma, mb, a, stream)
                 : ot == OT_F16 ? launch_split<128, OT_F16>(ma, mb, a, stream)
                                : launch_split<128, OT_BF16>(ma, mb, a, stream);
+        else if (bn == 192)
+            err = ot == OT_F32 ? launch_split<192, OT_F32>(ma, mb, a, stream)
+                : ot == OT_F16 ? launch_split<192, OT_F16>(ma, mb, a, stream)
+                               : launch_split<192, OT_BF16>(ma, mb, a, stream);
         else
             err = ot == OT_F32 ? launch_split<256, OT_F32>(ma, mb, a, stream)
                 : ot == OT_F16 ? launch_split<256, OT_F16>(ma, mb, a, stream)
