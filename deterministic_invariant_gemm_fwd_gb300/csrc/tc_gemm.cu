@@ -437,12 +437,65 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
 // ---- dW with few tiles: token range split over a cluster --------------------
 
+// Rows [piece * 128/S, (piece + 1) * 128/S) of the tile: the S fp32 partials
+// parked in the cluster's shared memory, added in piece order 0, 1, ..., S-1,
+// rounded once and stored.  A thread takes U = 16/S four-column vectors per
+// round and issues all of the round's 16 remote loads before its first
+// addition (a remote load's latency is many times a round's arithmetic).
+template <int S, int BN, int OT>
+__device__ __forceinline__ void combine_pieces(const TcArgs &p, uint32_t part_addr, int piece, int m0,
+                                               int n0) {
+    using L = Smem<BN>;
+    static_assert(S >= 2 && S <= kMaxSplits && kBM % S == 0, "split count");
+    constexpr int U = 16 / S, rows_per = kBM / S, vec_per_row = BN / 4, nvec = rows_per * vec_per_row;
+    const int r0 = piece * rows_per;
+    for (int first = threadIdx.x; first < nvec; first += U * kThreads) {
+        float4 b[U][S];
+        uint32_t live = 0u;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = first + u * kThreads;
+            const int rr = r0 + idx / vec_per_row, cc = (idx % vec_per_row) * 4;
+            const int64_t grow = (int64_t)m0 + rr, gcol = (int64_t)n0 + cc;
+            if (idx < nvec && grow < p.rows && gcol < p.cols &&
+                CHK(grow * p.cols + gcol, 4, (int64_t)p.rows * p.cols)) {
+                live |= 1u << u;
+                const uint32_t off = part_addr + (uint32_t)(rr * L::kPartialPitch + cc) * 4u;
+#pragma unroll
+                for (int q = 0; q < S; ++q) b[u][q] = ld_cluster_f4(off, (uint32_t)q);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (!((live >> u) & 1u)) continue;
+            const int idx = first + u * kThreads;
+            const int64_t grow = (int64_t)m0 + r0 + idx / vec_per_row, gcol = (int64_t)n0 + (idx % vec_per_row) * 4;
+            float4 a = b[u][0];
+#pragma unroll
+            for (int q = 1; q < S; ++q) {
+                a.x = __fadd_rn(a.x, b[u][q].x);
+                a.y = __fadd_rn(a.y, b[u][q].y);
+                a.z = __fadd_rn(a.z, b[u][q].z);
+                a.w = __fadd_rn(a.w, b[u][q].w);
+            }
+            if (OT == OT_F32) {
+                *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + grow * p.cols + gcol) = a;
+            } else {
+                uint2 w;
+                w.x = pack_out<OT>(a.x, a.y);
+                w.y = pack_out<OT>(a.z, a.w);
+                *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(p.out) + grow * p.cols + gcol) = w;
+            }
+        }
+    }
+}
+
+
 template <int BN, int OT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const TcArgs p) {
     using L = Smem<BN>;
-    constexpr bool OUT_F32 = OT == OT_F32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -511,40 +564,12 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
 
     // piece r rounds and stores rows [r*128/s, (r+1)*128/s) of the tile,
     // adding the partials in piece order 0, 1, ..., s-1
-    const int rows_per = kBM / p.splits;
-    const int r0 = piece * rows_per;
-    const int nvec = rows_per * (BN / 4);
     const uint32_t part_addr = smem_addr(part);
-    for (int idx = threadIdx.x; idx < nvec; idx += kThreads) {
-        const int rr = r0 + idx / (BN / 4);
-        const int cc = (idx % (BN / 4)) * 4;
-        const int64_t grow = (int64_t)m0 + rr, gcol = (int64_t)n0 + cc;
-        if (grow >= p.rows || gcol >= p.cols) continue;
-        if (!CHK(grow * p.cols + gcol, 4, (int64_t)p.rows * p.cols)) continue;
-        const uint32_t off = part_addr + (uint32_t)(rr * L::kPartialPitch + cc) * 4u;
-        // all the partials' loads are issued before the first addition (the
-        // remote loads' latency would otherwise be paid once per piece)
-        float4 b[kMaxSplits];
-#pragma unroll
-        for (int q = 0; q < kMaxSplits; ++q)
-            if (q < p.splits) b[q] = ld_cluster_f4(off, (uint32_t)q);
-        float4 a = b[0];
-#pragma unroll
-        for (int q = 1; q < kMaxSplits; ++q) {
-            if (q >= p.splits) break;
-            a.x = __fadd_rn(a.x, b[q].x);
-            a.y = __fadd_rn(a.y, b[q].y);
-            a.z = __fadd_rn(a.z, b[q].z);
-            a.w = __fadd_rn(a.w, b[q].w);
-        }
-        if (OUT_F32) {
-            *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + grow * p.cols + gcol) = a;
-        } else {
-            uint2 w;
-            w.x = pack_out<OT>(a.x, a.y);
-            w.y = pack_out<OT>(a.z, a.w);
-            *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(p.out) + grow * p.cols + gcol) = w;
-        }
+    switch (p.splits) {
+    case 2: combine_pieces<2, BN, OT>(p, part_addr, piece, m0, n0); break;
+    case 4: combine_pieces<4, BN, OT>(p, part_addr, piece, m0, n0); break;
+    case 8: combine_pieces<8, BN, OT>(p, part_addr, piece, m0, n0); break;
+    default: break;                                        // the host splits in 2, 4 or 8 only
     }
     cluster_sync_all();                                    // peers are done reading this CTA
     if (warp == 1) {
