@@ -653,12 +653,19 @@ cudaError_t launch_split(const CUtensorMap &ma, const CUtensorMap &mb, const TcA
                     (size_t)smem, stream, (unsigned)a.splits, ma, mb, a);
 }
 
+// Clusters of s CTAs that run at once on GB300 (152 SMs in 8 GPCs of about
+// 19, and a cluster's CTAs share one GPC): 16 of 8, 32 of 4, 72 of 2.  (18
+// clusters of 8 ran as two waves: dW of 768 x 768 took 26 us for 12 us of
+// work per CTA.)
+int clusters_at_once(int s) { return s >= 8 ? 16 : s == 4 ? 32 : s == 2 ? 72 : 152; }
+
 // dW split count from the output tile count only: the largest s in
-// {1, 2, 4, 8} with tiles * s <= 152 (GB300's SM count, fixed here so the
-// bits do not depend on the device a run lands on).
+// {1, 2, 4, 8} whose tiles * s CTAs run in one wave on GB300 (SM count and
+// GPC layout fixed here, so the bits do not depend on the device a run
+// lands on).
 int choose_splits(int64_t tiles) {
     int s = 1;
-    while (s < kMaxSplits && tiles * (2 * s) <= 152) s *= 2;
+    while (s < kMaxSplits && tiles * (2 * s) <= 152 && tiles <= clusters_at_once(2 * s)) s *= 2;
     return s;
 }
 
