@@ -38,32 +38,43 @@ inline Problem make_problem(int pass, int dtype, void *out, const void *A, const
     return p;
 }
 
-// Launches kernel `kern` on `stream` with programmatic stream serialization:
-// it may be scheduled before the previous kernel on the stream has finished,
-// and must call wait_prior_grid() (device_sync.cuh) before touching global
-// memory.  cluster_x > 1 also sets a cluster of that many CTAs along x.
+// Launches kernel `kern` on `stream`; with `early`, under programmatic
+// stream serialization: it may be scheduled before the previous kernel on
+// the stream has finished, and must call wait_prior_grid() (device_sync.cuh)
+// before touching global memory.  cluster_x > 1 also sets a cluster of that
+// many CTAs along x.
 template <typename... Params, typename... Args>
-cudaError_t launch_k(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
-                     cudaStream_t stream, unsigned cluster_x, Args &&...args) {
+cudaError_t launch_kernel(bool early, void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, unsigned cluster_x, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    unsigned n = 1;
-    if (cluster_x > 1) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = cluster_x;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        n = 2;
+    unsigned n = 0;
+    if (early) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
     }
-    cfg.attrs = attr;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
+// The library's usual launch: scheduled early (see launch_kernel).
+template <typename... Params, typename... Args>
+cudaError_t launch_k(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, unsigned cluster_x, Args &&...args) {
+    return launch_kernel(true, kern, grid, block, smem, stream, cluster_x, static_cast<Args &&>(args)...);
 }
 
 // Records a CUDA error message for carbon_last_cuda_error(); returns

@@ -355,9 +355,14 @@ __global__ void round_kernel(int dtype, void *out, const double *in, int64_t n) 
     }
 }
 
+// Not scheduled early: blocks of a grid launched before its predecessor ends
+// take whichever slots free up first, two to an SM where one would do, and
+// this kernel is bound by each SM's float64 pipe (the fp32 toy MLP's nine
+// GEMMs, grids of 128-256 blocks, took 9.0 ms that way instead of 6.9).
 template <int DT, int PASS, int OUT>
 cudaError_t launch_one(const KArgs &a, int64_t tiles, cudaStream_t stream) {
-    return launch_k(exact_kbn_kernel<DT, PASS, OUT>, dim3((unsigned)tiles), dim3(kThreads), 0, stream, 1, a);
+    return launch_kernel(false, exact_kbn_kernel<DT, PASS, OUT>, dim3((unsigned)tiles), dim3(kThreads), 0,
+                         stream, 1, a);
 }
 
 template <int DT, int PASS>
