@@ -62,12 +62,14 @@
 //    (bf16, reduction index contiguous, the four planes of a tile's lines
 //    together), the plane count per (tile, chunk) of each side.
 //  exact_tc_kernel: persistent, one CTA per SM, 128 x 64 output tiles taken
-//    in turn (unit u: tile u / pieces, column tile fastest, so that each CTA
-//    meets every kind of row tile).
-//   warps 0, 2 TMA producers of A: a 5-stage ring of A plane blocks (16 KiB
-//              each), alternate loads (one thread's copies complete in turn)
+//    in turn (unit u: tile u / pieces, handed out at run time; consecutive
+//    tiles share the operand whose planes are the larger).
+//   warps 0, 2 TMA producers of A: four stages of A plane blocks (16 KiB
+//              each, one k-group), signalled in pairs, alternate loads (one
+//              thread's copies complete in turn)
 //   warp 3     TMA producer of B: per chunk the four B planes of each 64-deep
-//              block (4 x 32 KiB, resident for the chunk)
+//              block (4 x 32 KiB, resident for the chunk), signalled in pairs;
+//              it also takes the work units and posts them to the others
 //   warp 1     MMA issuer: two accumulators of 256 TMEM columns used in turn,
 //              one per k-group, each k-group opened by one K = 16, N = 256 MMA
 //              of two constant shared-memory tiles that sets the accumulator
@@ -546,7 +548,7 @@ __device__ __forceinline__ long long round_to_53_bits(long long I) {
     return neg ? -(long long)r : (long long)r;
 }
 
-// bf16 bits of RN_bf16(V * 2^s) (nearest even), |V| < 2^53: V truncated to
+// bf16 bits of RN_bf16(V * 2^s) (nearest even), |V| <= 2^53: V truncated to
 // float32 (one conversion), the lowest bit set when the truncation dropped a
 // set bit (the low nb - 24 bits of |V|, nb its bit length, tested on the
 // integer) - rounding to odd at 24 bits -, scaled by 2^s in the exponent
@@ -565,10 +567,12 @@ __device__ __forceinline__ bool round_small_int_to_bf16(long long V, int s, uint
     const int e = (int)((fb >> 23) & 0xffu);                // 127 + nb - 1 (truncation keeps it)
     const int ef = e + s;                                   // biased exponent of the result
     if (ef < 1 || ef > 254) return false;
-    const int drop = e - 150;                               // nb - 24 bits truncated
+    // nb - 24 bits truncated, at most 30 (nb <= 54): all in the low word of
+    // |V|, which is minus the low word of V when V < 0
+    const int drop = e - 150;
     if (drop > 0) {
-        const unsigned long long mag = V < 0 ? 0ull - (unsigned long long)V : (unsigned long long)V;
-        if ((mag << (64 - drop)) != 0ull) fb |= 1u;
+        const uint32_t lo = (uint32_t)(unsigned long long)V;
+        if (((V < 0 ? 0u - lo : lo) & ((1u << drop) - 1u)) != 0u) fb |= 1u;
     }
     fb += (uint32_t)s << 23;
     unsigned short h;
@@ -580,9 +584,16 @@ __device__ __forceinline__ bool round_small_int_to_bf16(long long V, int s, uint
 
 // bf16 bits of RN_bf16(RN_float64(V * 2^s)) (both nearest even), |V| < 2^63:
 // V is first rounded to 53 significant bits when wider (the float64
-// rounding; exact otherwise).  False as above.
+// rounding; exact otherwise), and its zero low bits moved into the scale, so
+// that what is rounded to bf16 is below 2^54 (2^53 after a rounding carry).
+// False as above.
 __device__ __forceinline__ bool round_int_to_bf16(long long V, int s, uint32_t &bits) {
-    if (!below_pow2(V, 53)) V = round_to_53_bits(V);
+    if (!below_pow2(V, 53)) {
+        const unsigned long long mag = V < 0 ? 0ull - (unsigned long long)V : (unsigned long long)V;
+        const int sh = 11 - __clzll((long long)mag);        // bits below the 53 kept ones
+        V = round_to_53_bits(V) >> sh;                      // exact: those bits are now zero
+        s += sh;
+    }
     return round_small_int_to_bf16(V, s, bits);
 }
 
@@ -1327,7 +1338,8 @@ exact_finalize_kernel(const long long *__restrict__ Tout, int pieces, const int 
             }
 #pragma unroll
             for (int e = 0; e < kFinCols; ++e) {
-                deferred |= (t[e] == kDeferredSum ? 1u : 0u) << e;
+                // the sentinel's high word alone: a sum's is within +-2^30
+                deferred |= ((uint32_t)((unsigned long long)t[e] >> 32) == 0x80000000u ? 1u : 0u) << e;
                 if constexpr (MODE == kFinBf16) {
                     if (k == 0) {
                         sum[e] = t[e];

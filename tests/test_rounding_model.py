@@ -2,9 +2,10 @@
 
 The exact tier's finalize rounds an integer sum V (in units of 2^s) to bf16
 without a 64-bit integer rounding routine: V is first rounded to 53
-significant bits when wider (the float64 rounding of the literal algorithm),
-then truncated to float32 with the lowest bit set when a set bit was dropped
-(rounding to odd at 24 bits), scaled by 2^s in the exponent field and rounded
+significant bits when wider (the float64 rounding of the literal algorithm)
+and its zero low bits moved into s, then truncated to float32 with the lowest bit set when a set bit was dropped
+(rounding to odd at 24 bits; the dropped bits, at most 29, are tested in the
+low 32-bit word of |V|), scaled by 2^s in the exponent field and rounded
 to nearest even at bf16's 8 bits.  Rounding to odd at p + 2 or more bits and
 then to nearest at p bits equals one rounding to nearest at p bits (Boldo and
 Melquiond, "Emulation of FMA and correctly rounded sums: proved algorithms
@@ -16,7 +17,7 @@ with the oracle by the GPU tests.
 """
 import random
 
-M64 = (1 << 64) - 1
+M32 = (1 << 32) - 1
 
 
 def rn_bits(mag, p):
@@ -64,17 +65,18 @@ def below_pow2(v, k):
 
 def via_round_to_odd(V, s):
     """The kernel's steps; None where it takes the float64 route."""
-    if not below_pow2(V, 53):
+    if not below_pow2(V, 53):                       # the float64 rounding, zero bits to s
         m, sh = rn_bits(abs(V), 53)
-        V = (m << sh) * (1 if V > 0 else -1)
+        V, s = m * (1 if V > 0 else -1), s + sh
     if V == 0:
         return 0
     fb = f32_truncated_bits(V)
     e = (fb >> 23) & 0xFF
     if not 1 <= e + s <= 254:
         return None
-    drop = e - 150                                    # bits the truncation dropped
-    if drop > 0 and ((abs(V) << (64 - drop)) & M64) != 0:
+    drop = e - 150                                    # bits the truncation dropped (<= 29)
+    lo = V & M32                                      # the low word of V; of |V|, minus it
+    if drop > 0 and ((((-lo) & M32) if V < 0 else lo) & ((1 << drop) - 1)) != 0:
         fb |= 1
     fb = (fb + ((s << 23) & 0xFFFFFFFF)) & 0xFFFFFFFF
     h = bf16_nearest_even(fb)
@@ -90,6 +92,16 @@ def cases(rng, n):
             V = (V >> (nb - 9)) << (nb - 9)                       # 9 bits: midpoint or exact
         elif r < 0.5 and nb > 54:
             V = ((V >> (nb - 54)) << (nb - 54)) | rng.choice([0, 1, 1 << rng.randint(0, nb - 55)])
+        V = min(V, (1 << 63) - 1)
+        yield (-V if rng.random() < 0.5 else V), rng.randint(-200, 140)
+    for _ in range(n // 4):
+        # wide sums whose float64 rounding leaves a bf16 midpoint, or one just
+        # off it by a bit far below the kept 24 (past the low 32-bit word)
+        nb = rng.randint(40, 63)
+        top = (rng.getrandbits(7) | 0x80) << 1 | 1            # 8 bits and the midpoint bit
+        V = top << (nb - 9)
+        if rng.random() < 0.7:
+            V |= 1 << rng.randint(max(0, nb - 53), nb - 10)    # a bit the float64 rounding may keep
         V = min(V, (1 << 63) - 1)
         yield (-V if rng.random() < 0.5 else V), rng.randint(-200, 140)
     for s in range(-200, 141, 7):
