@@ -60,7 +60,12 @@ __device__ unsigned int g_tc_status = 0;
 constexpr int kBM = 128;          // tile rows (= MMA M, = TMEM lanes)
 constexpr int kBK = 64;           // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kUMMA_K = 16;       // K of one tcgen05.mma kind::f16
-constexpr int kStages = 4;
+// Ring stages per tile width: as many as the shared memory holds beside the
+// staging and bias copies (the kernel waits on operand arrival more than on
+// anything else: releasing stages in pairs, which shortens the look-ahead by
+// a stage, made the tier 12% slower).
+template <int BN>
+constexpr int stages_for() { return BN >= 256 ? 4 : (BN >= 192 ? 5 : 6); }
 constexpr int kThreads = 192;     // 6 warps
 constexpr int kMaxSplits = 8;     // dW token split: pieces per cluster, at most
 constexpr int kEpiWarps = 4;
@@ -79,6 +84,7 @@ struct TcArgs {
 
 template <int BN>
 struct Smem {
+    static constexpr int kStages = stages_for<BN>();
     static constexpr uint32_t kBBytes = BN * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kPipeBytes = kStages * kStageBytes;
@@ -90,6 +96,7 @@ struct Smem {
     // full[S], empty[S], tfull[2], tempty[2], then tmem base slot and abort flag
     static constexpr uint32_t kBytes = kBarOffset + (2 * kStages + 4) * 8 + 16;
     static constexpr uint32_t kDynamic = kBytes + 1024;   // room to align the base to 1 KiB
+    static_assert(kDynamic <= 232448, "shared memory per block");
     // split kernel: fp32 partial tile [128][BN + 4] placed over the pipeline ring
     static constexpr uint32_t kPartialPitch = BN + 4;
     static_assert(kBM * kPartialPitch * 4 <= kPipeBytes, "partial tile must fit the ring");
@@ -229,7 +236,7 @@ __device__ __forceinline__ bool produce_tile(const CUtensorMap *ma, const CUtens
             for (int j = 0; j < BN / 64; ++j)
                 tma_load_2d(sb + j * kMNBlockBytes, mb, bar.full(s), n0 + 64 * j, k0);
         }
-        if (++s == kStages) { s = 0; ph ^= 1u; }
+        if (++s == L::kStages) { s = 0; ph ^= 1u; }
     }
     return true;
 }
@@ -237,7 +244,9 @@ __device__ __forceinline__ bool produce_tile(const CUtensorMap *ma, const CUtens
 // Lets every load the producer issued land before the CTA may exit: a stage
 // armed in the last pass completes with parity ph; stages not armed in it
 // completed earlier, so their wait returns at once.
+template <int BN>
 __device__ __forceinline__ void drain_producer(const Bars &bar, int s, uint32_t ph) {
+    constexpr int kStages = Smem<BN>::kStages;
     for (int i = 0; i < kStages; ++i) {
         if (--s < 0) { s = kStages - 1; ph ^= 1u; }
         if (!mbar_wait(bar.full(s), ph)) break;
@@ -259,7 +268,7 @@ __device__ __forceinline__ bool mma_tile(uint32_t d, uint32_t sbase, const Bars 
             mma_bf16(d, operand_desc<A_MAJOR>(sa, k), operand_desc<B_MAJOR>(sb, k), idesc,
                      (kb | k) != 0 ? 1u : 0u);
         mma_commit(bar.empty(s));                  // stage free once these MMAs finish
-        if (++s == kStages) { s = 0; ph ^= 1u; }
+        if (++s == L::kStages) { s = 0; ph ^= 1u; }
     }
     return true;
 }
@@ -272,7 +281,7 @@ __device__ __forceinline__ uint32_t setup_cta(uint8_t *smem, const Bars &bar,
                                               uint32_t tmem_cols) {
     const int warp = threadIdx.x / 32;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < Smem<BN>::kStages; ++s) {
             mbar_init(bar.full(s), 1);
             mbar_init(bar.empty(s), 1);
         }
@@ -310,10 +319,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const uint32_t sbase = smem_addr(smem);
     Bars bar;
     bar.full0 = sbase + L::kBarOffset;
-    bar.empty0 = bar.full0 + 8 * kStages;
-    bar.tfull0 = bar.empty0 + 8 * kStages;
+    bar.empty0 = bar.full0 + 8 * L::kStages;
+    bar.tfull0 = bar.empty0 + 8 * L::kStages;
     bar.tempty0 = bar.tfull0 + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + (2 * kStages + 4) * 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + (2 * L::kStages + 4) * 8);
     volatile uint32_t *abort_flag = tmem_slot + 1;
     constexpr uint32_t kTmemCols = BN == 128 ? 256u : 512u;   // two accumulators, rounded to a power of two
 
@@ -330,7 +339,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                                                         (t / p.tiles_n) * kBM, (t % p.tiles_n) * BN,
                                                         0, p.num_kb, s, ph, abort_flag))
                     break;
-            drain_producer(bar, s, ph);
+            drain_producer<BN>(bar, s, ph);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -502,10 +511,10 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     const uint32_t sbase = smem_addr(smem);
     Bars bar;
     bar.full0 = sbase + L::kBarOffset;
-    bar.empty0 = bar.full0 + 8 * kStages;
-    bar.tfull0 = bar.empty0 + 8 * kStages;
+    bar.empty0 = bar.full0 + 8 * L::kStages;
+    bar.tfull0 = bar.empty0 + 8 * L::kStages;
     bar.tempty0 = bar.tfull0 + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + (2 * kStages + 4) * 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kBarOffset + (2 * L::kStages + 4) * 8);
     volatile uint32_t *abort_flag = tmem_slot + 1;
     // one accumulator of BN columns, the allocation rounded up to a power of two
     constexpr uint32_t kTmemCols = BN <= 128 ? 128u : 256u;
@@ -528,7 +537,7 @@ tc_dw_split_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             uint32_t ph = 0;
             produce_tile<BN, MN_MAJOR, MN_MAJOR>(&map_a, &map_b, sbase, bar, m0, n0, kb0, kb1, s, ph,
                                                  abort_flag);
-            drain_producer(bar, s, ph);
+            drain_producer<BN>(bar, s, ph);
         }
     } else if (warp == 1) {
         if (lane == 0 && nkb > 0) {
