@@ -16,8 +16,8 @@
  * Three tiers (tier argument):
  *
  * CARBON_TIER_EXACT - every product is formed in float64 (exactly: products
- *   of two fp32, two bf16 or two fp16 values fit in binary64), and products are summed
- *   with Kahan-Babushka-Neumaier compensation in a fixed order (Carbon
+ *   of two fp32, two bf16 or two fp16 values fit in binary64), and products
+ *   are summed with Kahan-Babushka-Neumaier compensation in a fixed order (Carbon
  *   README, "How It Works": tiles, upcast to float64, KBN compensation in a
  *   fixed order).  The order depends only on the reduction length R (K for
  *   fwd, N for dX, M for dW): R is cut into 256-wide chunks from index 0; each
@@ -33,16 +33,15 @@
  *
  * CARBON_TIER_TC - bf16 x bf16 (or fp16 x fp16) products accumulated in
  *   fp32 on the tensor cores (tcgen05, accumulators in tensor memory), with a
- *   K schedule that
- *   depends only on the shape of the reduction and the output columns, never
- *   on the batch size of fwd/dX (sgemm-bi, "Determinism contracts", tensor
- *   core tier: fixed tile families, shape-only dispatch).  fwd adds the bias
- *   in fp32; the fp32 value is rounded once, to nearest-even, to the input
- *   type.  Bit-identical run to run; fwd and dX rows are bit-identical for
- *   every M.  Accepts CARBON_BF16 and CARBON_F16 (CARBON_F32 ->
- *   CARBON_ERR_UNSUPPORTED).  Base
- *   pointers must be 16-byte aligned and K and N multiples of 8 (16-byte row
- *   pitch), else CARBON_ERR_MISALIGNED.
+ *   K schedule that depends only on the shape of the reduction and the output
+ *   columns, never on the batch size of fwd/dX (sgemm-bi, "Determinism
+ *   contracts", tensor core tier: fixed tile families, shape-only dispatch).
+ *   fwd adds the bias in fp32; the fp32 value is rounded once, to
+ *   nearest-even, to the input type.  Bit-identical run to run; fwd and dX
+ *   rows are bit-identical for every M.  Accepts CARBON_BF16 and CARBON_F16
+ *   (CARBON_F32 -> CARBON_ERR_UNSUPPORTED).  Base pointers must be 16-byte
+ *   aligned and K and N multiples of 8 (16-byte row pitch), else
+ *   CARBON_ERR_MISALIGNED.
  *
  * CARBON_TIER_SUPERACC - the correctly rounded tier (Carbon README,
  *   "Roadmap": superaccumulators, exact summation that needs no fixed
