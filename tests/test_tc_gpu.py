@@ -100,12 +100,15 @@ def test_small_integer_inputs_accumulate_exactly():
 
 
 @pytest.mark.parametrize("M,K,N", [(2048, 256, 256), (4000, 384, 200), (1100, 128, 1024), (2048, 768, 2304),
-                                   (2048, 768, 768)])
+                                   (2048, 768, 768), (2048, 3072, 768), (2048, 768, 1024), (2048, 512, 1024),
+                                   (2048, 512, 128)])
 def test_dw_token_split_accumulates_exactly(M, K, N):
     """dW shapes with few output tiles take the cluster split of the token
     range; with small-integer operands every partial and their in-order sum
-    are exact, so the result must equal the exact product.  (768 x 2304 takes
-    192-column tiles in two pieces, 768 x 768 in four.)"""
+    are exact, so the result must equal the exact product.  Tile width and
+    piece count: 768 x 2304 192 columns in two pieces, 768 x 768 192 in four,
+    the first three 192 in eight; 3072 x 768 256 in two, 768 x 1024 256 in
+    four, 512 x 1024 256 in eight, 512 x 128 128 in eight."""
     rng = np.random.default_rng(M)
     X = inputs.f32_to_bf16_bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
     dY = inputs.f32_to_bf16_bits(rng.integers(-4, 5, size=(M, N)).astype(np.float32))
